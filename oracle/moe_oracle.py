@@ -1,0 +1,320 @@
+"""CPU oracle for the sparse Mixture-of-Experts FFN forward pass.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the library path imports this module:
+only the tests, the smoke check in ``__graft_entry__`` and the CPU-baseline leg
+of ``bench.py`` may call it.  It shares no code with the CUDA path.
+
+Everything here is the plain definition of what the layer computes, in
+float64 numpy, with no blocking, fusion or reordering beyond the definition:
+
+* router scores ``z = x . W_g^T + b_g`` -- botmartz.com "Mixture of Experts (MoE)
+  and Mixtral: Scaling Without Dense Computation", section "Expert Routing"
+  (the router is an ``nn.Linear(d_model, num_experts)``); roadtointelligence.com
+  "Mixture of Experts (MoE)", the router formula G(x) = Softmax(TopK(x . W_g)).
+* softmax over all N experts, then the top-k, then renormalisation of the kept
+  k probabilities -- botmartz.com "Expert Routing"; matteuscruz.github.io
+  "What is a Mixture of Experts?", section "Architecture: router + experts".
+* the same gates written as a softmax over only the kept top-k logits --
+  roadtointelligence.com, router formula and the "Tiny example".
+* gates without renormalisation (the raw softmax probability of each kept
+  expert) -- codingnowai.in "Mixture of Experts", section "Code".
+* expert FFN Linear -> GELU -> Linear (botmartz.com "Expert Routing") or
+  Linear -> ReLU -> Linear (codingnowai.in "Code"), each with bias.
+* output y = sum over kept experts of gate * expert(x) -- roadtointelligence.com
+  output equation; matteuscruz.github.io "Architecture: router + experts".
+* expert capacity = capacity factor x batch / num_experts, tokens over capacity
+  dropped (layer output 0, the token passes on through the residual) --
+  matteuscruz.github.io "Load balancing: the core training challenge";
+  roadtointelligence.com "Keeping the experts busy".
+* one shared expert applied to every token with weight 1 --
+  roadtointelligence.com "Total versus active parameters" (DeepSeek-V3).
+* balance statistic std(mean_t router_probs)^2 with torch's default
+  (unbiased) std -- botmartz.com "Load Balancing: The Hidden Challenge".
+
+Readings taken where the pages are silent (each also listed in the design
+notes): top-k ties go to the lower expert index; slot 0 holds the largest
+score; capacity priority is token-major (token, then slot); the capacity is
+ceil(capacity_factor * T / N); a dropped (token, slot) contributes exactly 0;
+the shared expert uses the routed experts' FFN form and activation.
+"""
+
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+
+try:                                    # library erf; math.erf elementwise otherwise
+    from scipy.special import erf as _erf
+except ImportError:                     # pragma: no cover
+    _erf = np.vectorize(math.erf, otypes=[np.float64])
+
+ACT_GELU_ERF = 0
+ACT_RELU = 1
+
+
+# ---------------------------------------------------------------------------
+# number formats
+# ---------------------------------------------------------------------------
+
+def round_to_bf16(v):
+    """Round float64 values to the nearest bfloat16 value (ties to even).
+
+    bfloat16 keeps 8 significant bits and float32's exponent range, so for the
+    normal numbers this layer produces, rounding to 8 significant bits with
+    round-half-to-even is the whole definition.  Zeros, infinities and NaNs
+    pass through unchanged.
+    """
+    v = np.asarray(v, dtype=np.float64)
+    mant, expo = np.frexp(v)                      # v = mant * 2**expo, |mant| in [0.5, 1)
+    q = np.round(mant * 256.0)                    # numpy rounds half to even
+    out = np.ldexp(q / 256.0, expo)
+    return np.where(np.isfinite(v), out, v)
+
+
+# ---------------------------------------------------------------------------
+# router: scores, softmax, top-k, gates
+# ---------------------------------------------------------------------------
+
+def router_logits(x, W_g, b_g):
+    """z[t, e] = sum_i x[t, i] * W_g[e, i] + b_g[e]   (nn.Linear(d_model, N))."""
+    x = np.asarray(x, dtype=np.float64)
+    W_g = np.asarray(W_g, dtype=np.float64)
+    b_g = np.asarray(b_g, dtype=np.float64)
+    return x @ W_g.T + b_g
+
+
+def softmax(z):
+    """Softmax over the last axis (over all N experts), max-subtracted."""
+    z = np.asarray(z, dtype=np.float64)
+    m = np.max(z, axis=-1, keepdims=True)
+    e = np.exp(z - m)
+    return e / np.sum(e, axis=-1, keepdims=True)
+
+
+def topk_indices(z, k):
+    """Indices of the k largest scores per row, largest first.
+
+    Equal scores are ordered by the lower expert index (a stable sort of -z).
+    Selecting on the logits is the same as selecting on the softmax
+    probabilities, since the softmax is strictly increasing in each logit.
+    """
+    z = np.asarray(z, dtype=np.float64)
+    order = np.argsort(-z, axis=-1, kind="stable")
+    return order[..., :k]
+
+
+def gates_softmax_of_topk(z, idx):
+    """Gates as Softmax(TopK(z)): the scores outside the top-k are set to
+    minus infinity and a softmax is taken, so only the kept k are non-zero
+    (roadtointelligence.com router formula and "Tiny example")."""
+    z = np.asarray(z, dtype=np.float64)
+    masked = np.full_like(z, -np.inf)
+    np.put_along_axis(masked, idx, np.take_along_axis(z, idx, axis=-1), axis=-1)
+    g = softmax(masked)
+    return np.take_along_axis(g, idx, axis=-1)
+
+
+def gates_renormalised_probs(p, idx):
+    """Gates as top-k probabilities divided by their sum
+    (botmartz.com "Expert Routing"; matteuscruz.github.io "Architecture")."""
+    kept = np.take_along_axis(np.asarray(p, dtype=np.float64), idx, axis=-1)
+    return kept / np.sum(kept, axis=-1, keepdims=True)
+
+
+def gates_raw_probs(p, idx):
+    """Gates as the raw softmax probability of each kept expert, no
+    renormalisation (codingnowai.in "Mixture of Experts", section "Code")."""
+    return np.take_along_axis(np.asarray(p, dtype=np.float64), idx, axis=-1)
+
+
+def route(x, W_g, b_g, k, renormalize=True):
+    """Router + softmax + top-k (+ renormalise).  Returns (z, p, idx, w)."""
+    z = router_logits(x, W_g, b_g)
+    p = softmax(z)
+    idx = topk_indices(z, k)
+    w = gates_softmax_of_topk(z, idx) if renormalize else gates_raw_probs(p, idx)
+    return z, p, idx, w
+
+
+def topk_gap(z, k):
+    """Score gap between the k-th and (k+1)-th largest score of each token
+    (infinite when k == N).  Tokens with a gap below a threshold are near-ties
+    whose top-k set may legitimately differ under another summation order."""
+    z = np.asarray(z, dtype=np.float64)
+    N = z.shape[-1]
+    if k >= N:
+        return np.full(z.shape[:-1], np.inf)
+    s = -np.sort(-z, axis=-1)
+    return s[..., k - 1] - s[..., k]
+
+
+# ---------------------------------------------------------------------------
+# capacity and the per-expert grouping of (token, slot) assignments
+# ---------------------------------------------------------------------------
+
+def expert_capacity(capacity_factor, T, N):
+    """capacity factor x batch size / number of experts, rounded up."""
+    return int(math.ceil(capacity_factor * T / N))
+
+
+@dataclass
+class Grouping:
+    """Assignments grouped by expert.
+
+    groups[e]  : list of (t, j) kept for expert e, in token-major order
+    counts[e]  : assignments routed to e before capacity
+    kept[e]    : assignments kept (min(counts[e], capacity))
+    rank[t, j] : position of (t, j) among the assignments to its expert
+    keep[t, j] : True when the assignment is within capacity
+    """
+    groups: list
+    counts: np.ndarray
+    kept: np.ndarray
+    rank: np.ndarray
+    keep: np.ndarray
+    dropped: int = field(default=0)
+
+
+def group_by_expert(idx, N, capacity=0):
+    """Walk the assignments (t, j) in ascending token, then ascending slot;
+    an assignment's rank is how many earlier assignments chose the same
+    expert; it is kept when capacity <= 0 (unlimited) or rank < capacity."""
+    idx = np.asarray(idx)
+    T, k = idx.shape
+    counts = np.zeros(N, dtype=np.int64)
+    rank = np.zeros((T, k), dtype=np.int64)
+    keep = np.zeros((T, k), dtype=bool)
+    groups = [[] for _ in range(N)]
+    for t in range(T):
+        for j in range(k):
+            e = int(idx[t, j])
+            r = int(counts[e])
+            counts[e] += 1
+            rank[t, j] = r
+            if capacity <= 0 or r < capacity:
+                keep[t, j] = True
+                groups[e].append((t, j))
+    kept = np.array([len(g) for g in groups], dtype=np.int64)
+    return Grouping(groups, counts, kept, rank, keep, int(counts.sum() - kept.sum()))
+
+
+# ---------------------------------------------------------------------------
+# experts and the layer
+# ---------------------------------------------------------------------------
+
+def activation(h, act):
+    h = np.asarray(h, dtype=np.float64)
+    if act == ACT_GELU_ERF:
+        # nn.GELU() default: 0.5 * h * (1 + erf(h / sqrt(2)))
+        return 0.5 * h * (1.0 + _erf(h / math.sqrt(2.0)))
+    if act == ACT_RELU:
+        return np.maximum(h, 0.0)
+    raise ValueError(f"unknown activation {act}")
+
+
+def expert_ffn(xr, W1, b1, W2, b2, act, round_hidden_bf16=False):
+    """Linear(d, d_ff) -> activation -> Linear(d_ff, d) on the rows xr.
+
+    With round_hidden_bf16 the hidden activation is rounded to bfloat16
+    before the second Linear, the storage format of the hidden layer in the
+    bf16 layer; everything else stays float64.
+    """
+    xr = np.asarray(xr, dtype=np.float64)
+    h = xr @ np.asarray(W1, dtype=np.float64).T + np.asarray(b1, dtype=np.float64)
+    h = activation(h, act)
+    if round_hidden_bf16:
+        h = round_to_bf16(h)
+    return h @ np.asarray(W2, dtype=np.float64).T + np.asarray(b2, dtype=np.float64)
+
+
+@dataclass
+class LayerOutput:
+    y: np.ndarray            # [len(tokens), d] float64 layer output
+    tokens: np.ndarray       # token ids the rows of y belong to
+    z: np.ndarray            # [T, N] router scores
+    p: np.ndarray            # [T, N] router probabilities
+    idx: np.ndarray          # [T, k] selected experts, largest first
+    w: np.ndarray            # [T, k] gates
+    grouping: Grouping
+    mean_prob: np.ndarray    # [N]
+    balance: float
+
+
+def balance_statistic(p):
+    """std(mean over tokens of the router probabilities)^2, torch.std's default
+    unbiased estimator (botmartz.com "Load Balancing: The Hidden Challenge").
+    Returns (mean_prob, balance); balance is 0 for a single expert."""
+    m = np.mean(np.asarray(p, dtype=np.float64), axis=0)
+    if m.shape[0] < 2:
+        return m, 0.0
+    return m, float(np.std(m, ddof=1) ** 2)
+
+
+def moe_forward(x, W_g, b_g, W1, b1, W2, b2, *, k, act, capacity=0,
+                renormalize=True, shared=None, round_hidden_bf16=False,
+                tokens=None, idx_override=None):
+    """The whole layer for the tokens listed in ``tokens`` (default: all).
+
+    Routing, grouping and the statistics always cover all T tokens, because a
+    token's capacity rank depends on every earlier token.  ``W1`` etc. may be
+    any indexable of per-expert arrays (W1[e] is [d_ff, d]); experts are read
+    one at a time.  ``shared`` is None or (W1s, b1s, W2s, b2s).
+    ``idx_override`` replaces the top-k choice (used only for tokens whose
+    k-th score gap is a near-tie); the gates are then taken for those experts.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    T = x.shape[0]
+    N = np.asarray(b_g).shape[0]
+    z = router_logits(x, W_g, b_g)
+    p = softmax(z)
+    idx = topk_indices(z, k) if idx_override is None else np.asarray(idx_override, dtype=np.int64)
+    w = gates_softmax_of_topk(z, idx) if renormalize else gates_raw_probs(p, idx)
+    grouping = group_by_expert(idx, N, capacity)
+    mean_prob, balance = balance_statistic(p)
+
+    tokens = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    pos = {int(t): i for i, t in enumerate(tokens)}
+    y = np.zeros((len(tokens), x.shape[1]), dtype=np.float64)
+    for e in range(N):
+        rows = [(t, j) for (t, j) in grouping.groups[e] if t in pos]
+        if not rows:
+            continue
+        ts = np.array([t for t, _ in rows])
+        js = np.array([j for _, j in rows])
+        o = expert_ffn(x[ts], W1[e], b1[e], W2[e], b2[e], act, round_hidden_bf16)
+        for r, (t, j) in enumerate(zip(ts, js)):
+            y[pos[int(t)]] += w[t, j] * o[r]
+    if shared is not None:
+        W1s, b1s, W2s, b2s = shared
+        y += expert_ffn(x[tokens], W1s, b1s, W2s, b2s, act, round_hidden_bf16)
+    return LayerOutput(y, tokens, z, p, idx, w, grouping, mean_prob, balance)
+
+
+def moe_bruteforce(x, W_g, b_g, W1, b1, W2, b2, *, k, act, capacity=0,
+                   renormalize=True, shared=None):
+    """Every expert on every token, then mask and weight: the per-slot,
+    per-expert loop of botmartz.com "Expert Routing" and codingnowai.in "Code"
+    (output[mask] += weight[mask] * expert(x)[mask]), with the capacity mask
+    applied on top.  For tiny inputs only."""
+    x = np.asarray(x, dtype=np.float64)
+    T, d = x.shape
+    N = np.asarray(b_g).shape[0]
+    z = router_logits(x, W_g, b_g)
+    p = softmax(z)
+    idx = topk_indices(z, k)
+    if renormalize:
+        w = gates_renormalised_probs(p, idx)
+    else:
+        w = gates_raw_probs(p, idx)
+    keep = group_by_expert(idx, N, capacity).keep
+    all_out = np.stack([expert_ffn(x, W1[e], b1[e], W2[e], b2[e], act) for e in range(N)])
+    y = np.zeros((T, d))
+    for j in range(k):
+        for e in range(N):
+            mask = (idx[:, j] == e) & keep[:, j]
+            y[mask] += w[mask, j][:, None] * all_out[e][mask]
+    if shared is not None:
+        y += expert_ffn(x, *shared, act)
+    return y
