@@ -1,0 +1,378 @@
+"""Benchmark of the sparse-MoE FFN layer forward pass on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+One step = one pass of the whole layer (router + softmax + top-k, permute,
+grouped expert FFN, combine, load statistics) over one batch of T synthetic
+tokens, through the library's C ABI.  Prints one JSON line (rank 0).
+
+Timing: W untimed warm-up steps, then K timed steps between a barrier and a
+device synchronise on both sides; each step is bracketed by CUDA events on the
+launching stream, with L2 flushed (a 512 MiB buffer written) before every
+step, outside the events.  Multi-GPU (torchrun): every rank runs its own
+replica of the layer on its own GPU (data parallel, no exchange); the time is
+the max over ranks and the value counts every rank's tokens.
+
+--impl reference times the CPU oracle (float64 numpy) on the host cores, on a
+bounded sample of the same workload per step.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "c1_page1_bf16"
+METRIC = "MoE-layer tokens/s on 1 B300; % of bf16 tensor peak / % of HBM BW"
+L2_FLUSH_BYTES = 512 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+            "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------------------
+# clocks during the timed region
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"moe_bench_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------------
+# the CPU oracle as a timed baseline
+
+def oracle_step(tensors, wl, tokens):
+    """The oracle on the first `tokens` tokens of the batch, as a layer of that
+    many tokens (float64 numpy)."""
+    import numpy as np
+    import torch
+
+    from oracle import moe_oracle as O
+
+    f64 = lambda v: v.detach().to("cpu", torch.float64).numpy()  # noqa: E731
+    x = f64(tensors["x"][:tokens])
+    W = {n: f64(tensors[n]) for n in ("W_g", "b_g", "W1", "b1", "W2", "b2")}
+    shared = None
+    if wl.d_ff_shared:
+        shared = tuple(f64(tensors[n]) for n in ("W1s", "b1s", "W2s", "b2s"))
+    cap = O.expert_capacity(wl.capacity_factor, tokens, wl.n_experts) \
+        if wl.capacity_factor > 0 else 0
+
+    def run():
+        return O.moe_forward(x, W["W_g"], W["b_g"], W["W1"], W["b1"], W["W2"], W["b2"],
+                             k=wl.top_k, act=wl.act, capacity=cap,
+                             renormalize=bool(wl.renormalize), shared=shared,
+                             round_hidden_bf16=(wl.dtype == 1))
+    del np
+    return run
+
+
+def oracle_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return max(n) if n else 1
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_sample_tokens(wl):
+    # a sample that keeps one oracle pass to a few seconds of host work
+    per_token_flop = 4.0 * wl.d_model * wl.d_ff * wl.top_k + 4.0 * wl.d_model * wl.d_ff_shared
+    return int(max(16, min(wl.T, 2.0e10 / per_token_flop)))
+
+
+def run_reference(args, wl, rank, world):
+    import torch
+
+    from sparse_mixture_experts_68_b300 import synth
+    if rank != 0:
+        return None
+    tensors = synth.make_layer(wl, device="cpu")
+    S = cpu_sample_tokens(wl)
+    step = oracle_step(tensors, wl, S)
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = S * args.steps / dt
+    cores = oracle_threads()
+    del torch
+    return {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": wl.name, "description": wl.description, "T": wl.T,
+                   "sample_tokens_per_step": S},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"first {S} of {wl.T} tokens per step, as a layer of {S} "
+                                   "tokens (float64 numpy oracle)"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+# ---------------------------------------------------------------------------------------
+# the CUDA path
+
+def run_ours(args, wl, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    from sparse_mixture_experts_68_b300 import binding as B
+    from sparse_mixture_experts_68_b300 import synth
+    from sparse_mixture_experts_68_b300.workloads import flops
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    tensors = synth.make_layer(wl, device=dev)
+    layer = B.StagedLayer(wl, tensors, device=dev)
+    out = B.alloc_outputs(layer.cfg, dev)
+    x = tensors["x"]
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.fill_(1)
+        layer.run(x, out)
+    torch.cuda.synchronize(dev)
+    assert B.get_device_status() == B.MOE_OK
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    for i in range(K):
+        flush.fill_(i)
+        layer.run(x, out, events=ev[i], stream=stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    stage_ms = [[ev[i][s].elapsed_time(ev[i][s + 1]) for s in range(5)] for i in range(K)]
+    step_ms = [ev[i][0].elapsed_time(ev[i][5]) for i in range(K)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    assert B.get_device_status() == B.MOE_OK
+
+    kept_rows = int(out.kept.sum().item())
+    n_kept_experts = int((out.kept > 0).sum().item())
+    T = layer.cfg.T
+    value = T * K * world / (total_ms * 1e-3)
+
+    # roofline of the dominant kernel (the grouped FFN: two launches of the
+    # tcgen05 grouped GEMM per step)
+    pk = peaks()
+    es = wl.elem_bytes
+    ffn_ms = statistics.mean(s[2] for s in stage_ms)
+    ffn_flop = 4.0 * wl.d_model * wl.d_ff * kept_rows + 4.0 * wl.d_model * wl.d_ff_shared * T
+    ffn_weight_bytes = (n_kept_experts * 2 * wl.d_model * wl.d_ff +
+                        (2 * wl.d_model * wl.d_ff_shared if wl.d_ff_shared else 0)) * es
+    ffn_act_bytes = (kept_rows + (T if wl.d_ff_shared else 0)) * (
+        2 * wl.d_model + 2 * wl.d_ff) * es
+    ffn_bytes = ffn_weight_bytes + ffn_act_bytes
+    intensity = ffn_flop / ffn_bytes
+    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    launches = 2
+    if intensity >= ridge:
+        achieved = ffn_flop / launches / (ffn_ms / launches * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s"}
+    else:
+        achieved = ffn_bytes / launches / (ffn_ms / launches * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["kernel"] = "tc_grouped_gemm_kernel (grouped FFN, 2 launches/step)"
+    roof["peak_source"] = pk["source"] + " (burst)"
+
+    # whole-layer roofline time against the same peaks
+    layer_flop = flops(wl, kept_rows)
+    layer_bytes = ffn_weight_bytes + wl.n_experts * wl.d_model * es + 2 * T * wl.d_model * es
+    floor_ms = max(layer_flop / (pk["bf16_tflops"] * 1e12),
+                   layer_bytes / (pk["hbm_gbs"] * 1e9)) * 1e3
+
+    res = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if wl.dtype == 1 else "f32", "data": "synthetic",
+        "config": {"workload": wl.name, "description": wl.description, "T": T,
+                   "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write)"},
+        "tflops": layer_flop / (total_ms / K * 1e-3) / 1e12,
+        "layer_roofline_floor_ms": floor_ms,
+        "layer_roofline_frac": floor_ms / (total_ms / K),
+        "stage_ms": {n: statistics.mean(s[i] for s in stage_ms)
+                     for i, n in enumerate(B.StagedLayer.STAGES)},
+        "roofline": roof,
+        "gpu_launches": B.StagedLayer.LAUNCHES_PER_STEP * K,
+        "clocks": clk,
+    }
+
+    if not args.no_e2e:
+        res["e2e"] = measure_e2e(args, layer, wl, dev)
+    return res
+
+
+def measure_e2e(args, layer, wl, dev):
+    """Same metric through moe_forward_host: tokens copied in from pinned host
+    memory and the results copied back inside the timed call."""
+    import torch
+
+    from sparse_mixture_experts_68_b300 import binding as B
+    cfg = layer.cfg
+    ws = torch.empty(B.host_workspace_size(cfg), dtype=torch.uint8, device=dev)
+    xh = layer.t["x"].cpu().pin_memory()
+    oh = B.alloc_outputs(cfg, "cpu", pin_memory=True)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        B.forward_host(cfg, xh, layer.weights, oh, ws, stream)
+    K = args.steps
+    t0 = time.perf_counter()
+    for _ in range(K):
+        B.forward_host(cfg, xh, layer.weights, oh, ws, stream)
+    dt = time.perf_counter() - t0
+    es = wl.elem_bytes
+    T, k, N = cfg.T, cfg.top_k, cfg.n_experts
+    h2d = T * wl.d_model * es
+    d2h = T * wl.d_model * es + T * k * 8 + N * 12 + 8
+    return {"value": T * K / dt, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "api": "moe_forward_host (host buffers, synchronous)"}
+
+
+def cpu_baseline(wl):
+    import torch
+
+    from sparse_mixture_experts_68_b300 import synth
+    tensors = synth.make_layer(wl, device="cpu")
+    S = cpu_sample_tokens(wl)
+    step = oracle_step(tensors, wl, S)
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        step()
+        n += 1
+        if time.perf_counter() - t0 > 10.0 or n >= 3:
+            break
+    dt = time.perf_counter() - t0
+    del torch
+    return {"value": S * n / dt, "unit": "tokens/s", "cores": oracle_threads(),
+            "kind": "oracle",
+            "sample": f"{n} pass(es) over the first {S} of {wl.T} tokens, as a layer of "
+                      f"{S} tokens (float64 numpy oracle)"}
+
+
+def main():
+    args = parse()
+    from sparse_mixture_experts_68_b300.workloads import WORKLOADS
+    wl = WORKLOADS[args.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        res = run_reference(args, wl, rank, world)
+        if rank == 0 and res is not None:
+            print(json.dumps(res), flush=True)
+        return
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    res = run_ours(args, wl, rank, world, local_rank)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(wl)
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

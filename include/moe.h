@@ -1,0 +1,232 @@
+/*
+ * moe.h -- C ABI of libmoe.so: the forward pass of a sparse Mixture-of-Experts
+ * FFN layer on one NVIDIA B300 (sm_103a).
+ *
+ * The layer (botmartz.com "Mixture of Experts (MoE) and Mixtral: Scaling
+ * Without Dense Computation", sections "MoE Architecture" and "Expert
+ * Routing"; roadtointelligence.com "Mixture of Experts (MoE)", router formula
+ * and output equation; matteuscruz.github.io "What is a Mixture of Experts?",
+ * section "Architecture: router + experts"):
+ *
+ *   z   = x . W_g^T + b_g                       router scores, fp32   [T, N]
+ *   p   = softmax(z) over the N experts                                [T, N]
+ *   idx = the k experts with the largest z (ties: lower index; slot 0 largest)
+ *   w   = softmax over the kept k scores (= kept p renormalised to sum 1),
+ *         or the kept p themselves when renormalize == 0
+ *   y[t] = sum_j [kept] w[t,j] * E_idx[t,j](x[t])  (+ E_shared(x[t]))
+ *   E_e(v) = W2[e] . act(W1[e] . v + b1[e]) + b2[e],  act = GELU(erf) | ReLU
+ *
+ * With a capacity C > 0 (roadtointelligence.com "Keeping the experts busy";
+ * matteuscruz.github.io "Load balancing: the core training challenge"), the
+ * (token, slot) assignments of each expert are ranked in token-major order
+ * and those with rank >= C are dropped: they contribute 0 to y (the token
+ * passes on through the caller's residual connection).
+ *
+ * Conventions for every call below
+ *   - Pointers named x, y, W*, b*, and all index / statistic arrays are DEVICE
+ *     pointers (except in moe_forward_host, which says otherwise).  The caller
+ *     owns every buffer; the library allocates no memory.  `cfg` and the
+ *     structs are read during the call only.
+ *   - Layouts are row-major.  x, y: [T, d_model].  Weights follow
+ *     nn.Linear's [out, in]: W_g [N, d_model], W1 [N, d_ff, d_model],
+ *     W2 [N, d_model, d_ff], W1s [d_ff, d_model], W2s [d_model, d_ff];
+ *     biases b_g [N], b1 [N, d_ff], b2 [N, d_model], b1s [d_ff], b2s [d_model].
+ *     x, y, weights and biases share one element type, cfg->dtype.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and never synchronise, except moe_forward_host and
+ *     moe_get_device_status.
+ *   - Arguments are validated on the host before anything is launched; a
+ *     failed check returns a status and leaves every buffer untouched.  A
+ *     failed launch returns MOE_ERR_CUDA.  There is no CPU fallback.
+ *   - Every device pointer must be 16-byte aligned.  Requirements on sizes:
+ *     1 <= top_k <= n_experts <= 1024, T >= 0, d_model % 8 == 0; for bf16
+ *     also d_model % 64 == 0 and d_ff % 64 == 0; d_ff_shared is 0 or d_ff.
+ *     Otherwise MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED.
+ *   - Kernels that wait on on-chip barriers give up after a time limit
+ *     (moe_set_wait_limit_ns), record MOE_ERR_TIMEOUT in a device status word
+ *     and return; moe_get_device_status reports it.
+ *   - All kernels are deterministic: the same inputs give bit-identical
+ *     outputs (no order-dependent atomics).
+ *   - The library's only global state is that status word and the wait limit.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t moe_status;
+enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* null / misaligned pointer, bad size */
+  MOE_ERR_UNSUPPORTED = 2,   /* valid layer this build does not run (shape rule) */
+  MOE_ERR_WORKSPACE = 3,     /* workspace or scratch smaller than required */
+  MOE_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+  MOE_ERR_TIMEOUT = 5        /* a device-side barrier wait ran out of time */
+};
+
+enum { MOE_F32 = 0, MOE_BF16 = 1 };           /* moe_config.dtype */
+enum { MOE_ACT_GELU_ERF = 0, MOE_ACT_RELU = 1 };  /* moe_config.act  */
+
+/* Rows of the expert-grouped buffers are padded per expert to this multiple. */
+#define MOE_GROUP_ALIGN 128
+
+typedef struct moe_config {
+  int64_t T;            /* tokens (batch x sequence), >= 0                     */
+  int64_t d_model;      /* model width d                                        */
+  int64_t d_ff;         /* hidden width of each routed expert                   */
+  int64_t n_experts;    /* N routed experts                                     */
+  int64_t top_k;        /* k experts per token                                  */
+  int64_t capacity;     /* assignments kept per expert; <= 0 means unlimited    */
+  int64_t d_ff_shared;  /* 0: no shared expert; else its hidden width (= d_ff)  */
+  int32_t renormalize;  /* 1: gates = softmax over the kept k scores; 0: raw p  */
+  int32_t act;          /* MOE_ACT_*                                            */
+  int32_t dtype;        /* MOE_F32 or MOE_BF16 for x, y, weights, biases        */
+  int32_t reserved;     /* set to 0                                             */
+} moe_config;
+
+typedef struct moe_weights {
+  const void *W_g, *b_g;              /* router                                 */
+  const void *W1, *b1, *W2, *b2;      /* routed experts, stacked over N         */
+  const void *W1s, *b1s, *W2s, *b2s;  /* shared expert (NULL if d_ff_shared=0)  */
+} moe_weights;
+
+typedef struct moe_outputs {
+  void    *y;          /* [T, d_model], cfg->dtype                      required */
+  int32_t *topk_idx;   /* [T, k] expert of each slot, slot 0 largest    required */
+  float   *topk_w;     /* [T, k] gate of each slot                      required */
+  int32_t *counts;     /* [N] assignments routed to each expert         required */
+  int32_t *kept;       /* [N] assignments kept (min(counts, capacity))  required */
+  int32_t *dropped;    /* [1] total dropped assignments                 required */
+  float   *mean_prob;  /* [N] mean over tokens of p                     required */
+  float   *balance;    /* [1] std_unbiased(mean_prob)^2                 required */
+  float   *logits;     /* [T, N] router scores z; NULL = keep in workspace      */
+} moe_outputs;
+
+/* ---- sizes --------------------------------------------------------------- */
+
+/* Upper bound on the rows of the expert-grouped buffers Xp / H / Yp:
+ * T*k + N*(MOE_GROUP_ALIGN-1), plus T rounded up to MOE_GROUP_ALIGN when there
+ * is a shared expert.  Returns -1 for an invalid config. */
+int64_t moe_rows_max(const moe_config* cfg);
+
+/* Rows of the router's per-block probability partial sums ([rows, N] fp32). */
+int64_t moe_router_blocks(const moe_config* cfg);
+
+/* Bytes of scratch moe_permute needs (per-block histograms and bases). */
+size_t moe_permute_scratch_size(const moe_config* cfg);
+
+/* Bytes of workspace moe_forward needs; 0 for an invalid config. */
+size_t moe_workspace_size(const moe_config* cfg);
+
+/* ---- the steps of the layer ------------------------------------------------ */
+
+/* Router scores, softmax over all N experts, top-k and gates
+ * (botmartz.com "Expert Routing": router Linear, softmax, topk, renormalise;
+ * roadtointelligence.com router formula Softmax(TopK(x . W_g))).
+ *   x [T, d] dtype; W_g [N, d] dtype; b_g [N] dtype
+ *   logits        out [T, N] fp32: z, accumulated in fp32
+ *   topk_idx      out [T, k] int32, slot 0 = largest score, ties -> lower index
+ *   topk_w        out [T, k] fp32 gates
+ *   prob_partials out [moe_router_blocks(cfg), N] fp32: per token-block sums
+ *                 of p, consumed by moe_load_stats. */
+moe_status moe_router_topk(const moe_config* cfg, const void* x, const void* W_g,
+                           const void* b_g, float* logits, int32_t* topk_idx,
+                           float* topk_w, float* prob_partials, void* stream);
+
+/* Group the (token, slot) assignments by expert, in token-major order, apply
+ * the capacity and copy the kept tokens' rows into per-expert contiguous
+ * groups (matteuscruz.github.io "Distributed training and inference":
+ * grouping tokens by expert; "Load balancing": capacity buffer).
+ *   topk_idx  in  [T, k]
+ *   counts    out [N] routed assignments per expert
+ *   kept      out [N] kept assignments per expert
+ *   offsets   out [N + 2] first row of each group in Xp; groups padded to
+ *             MOE_GROUP_ALIGN rows; offsets[N] = end of the routed groups,
+ *             offsets[N+1] = end of the shared expert's group (rows
+ *             offsets[N] + t hold token t) or offsets[N] without one
+ *   row_token out [moe_rows_max] token of each routed row; -1 for padding
+ *   token_row out [T, k] row of each assignment in Xp; -1 when dropped
+ *   Xp        out [moe_rows_max, d] dtype; padding rows are left unwritten
+ *   scratch   device scratch of moe_permute_scratch_size(cfg) bytes. */
+moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk_idx,
+                       int32_t* counts, int32_t* kept, int32_t* offsets,
+                       int32_t* row_token, int32_t* token_row, void* Xp,
+                       void* scratch, size_t scratch_bytes, void* stream);
+
+/* Run every expert on its group (botmartz.com "Expert Routing": Linear ->
+ * GELU -> Linear; codingnowai.in "Code": Linear -> ReLU -> Linear):
+ *   H  = act(Xp[group e] . W1[e]^T + b1[e])   stored in dtype  [rows_max, d_ff]
+ *   Yp = H[group e] . W2[e]^T + b2[e]          stored in dtype  [rows_max, d]
+ * Only the kept[e] leading rows of each group are computed and written; the
+ * shared expert's group (when present) has T rows.  offsets/kept as written
+ * by moe_permute.  bf16 runs on the tensor cores (fp32 accumulate), fp32 on
+ * CUDA cores. */
+moe_status moe_grouped_ffn(const moe_config* cfg, const void* Xp, const int32_t* offsets,
+                           const int32_t* kept, const moe_weights* w, void* H, void* Yp,
+                           void* stream);
+
+/* Gate-weighted combine back to token order (roadtointelligence.com output
+ * equation; botmartz.com "Expert Routing" outputs[mask] += prob * expert(x)):
+ *   y[t] = sum_j [token_row[t,j] >= 0] topk_w[t,j] * Yp[token_row[t,j]]
+ *          (+ Yp[offsets[N] + t] with weight 1 for the shared expert)
+ * accumulated in fp32 in slot order, stored in dtype.  A token with every
+ * slot dropped and no shared expert gets y[t] = 0. */
+moe_status moe_combine(const moe_config* cfg, const void* Yp, const int32_t* token_row,
+                       const float* topk_w, const int32_t* offsets, void* y, void* stream);
+
+/* Load statistics (botmartz.com "Load Balancing: The Hidden Challenge"):
+ *   mean_prob[e] = (1/T) sum_t p[t, e]            (from prob_partials)
+ *   balance      = sum_e (mean_prob[e] - 1/N)^2 / (N - 1)   (0 when N == 1)
+ *                = torch.std(mean_prob)**2 with the unbiased default
+ *   dropped      = sum_e (counts[e] - kept[e])
+ * Sums run in fp64 in a fixed order. */
+moe_status moe_load_stats(const moe_config* cfg, const float* prob_partials,
+                          const int32_t* counts, const int32_t* kept, float* mean_prob,
+                          float* balance, int32_t* dropped, void* stream);
+
+/* The whole layer: router_topk -> permute -> grouped_ffn -> combine ->
+ * load_stats on `stream`, with intermediates carved from `workspace`
+ * (device, >= moe_workspace_size(cfg) bytes, 256-byte aligned). */
+moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* w,
+                       const moe_outputs* out, void* workspace, size_t workspace_bytes,
+                       void* stream);
+
+/* moe_forward for callers holding tokens and results in HOST memory: x and
+ * every non-NULL pointer in `out` are host pointers (page-locked memory makes
+ * the copies asynchronous); weights and workspace stay on the device.  The
+ * call copies x in, runs the layer, copies the results out and synchronises
+ * `stream` before returning.  The workspace must hold
+ * moe_workspace_size(cfg) bytes plus room for x and every output
+ * (moe_host_workspace_size). */
+size_t moe_host_workspace_size(const moe_config* cfg);
+moe_status moe_forward_host(const moe_config* cfg, const void* x_host, const moe_weights* w,
+                            const moe_outputs* out_host, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/* ---- status ---------------------------------------------------------------- */
+
+/* Synchronises `stream`, returns (and clears) the device status word:
+ * MOE_OK or MOE_ERR_TIMEOUT; MOE_ERR_CUDA if the synchronisation failed. */
+moe_status moe_get_device_status(void* stream);
+
+/* Time after which a device-side barrier wait gives up (default 2 s). */
+void moe_set_wait_limit_ns(uint64_t ns);
+uint64_t moe_get_wait_limit_ns(void);
+
+/* Launches one block that waits on an on-chip barrier nothing will complete,
+ * for at most `limit_ns`, then records MOE_ERR_TIMEOUT and returns: exercises
+ * the bounded-wait path without hanging the GPU. */
+moe_status moe_selftest_bounded_wait(uint64_t limit_ns, void* stream);
+
+const char* moe_status_string(moe_status s);
+int32_t moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H */

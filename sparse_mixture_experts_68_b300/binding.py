@@ -1,0 +1,331 @@
+"""ctypes binding of libmoe.so (the C ABI in include/moe.h).
+
+Argument marshalling only: every step of the layer runs in the library's
+CUDA kernels.  torch supplies device memory and streams.  If the library has
+not been built, loading it raises -- there is no fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+import os
+from dataclasses import dataclass
+
+import torch
+
+from .workloads import DT_F32, Workload
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe.so")
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, \
+    MOE_ERR_TIMEOUT = range(6)
+MOE_F32, MOE_BF16 = 0, 1
+MOE_ACT_GELU_ERF, MOE_ACT_RELU = 0, 1
+
+# Every symbol include/moe.h declares.
+EXPORTS = [
+    "moe_rows_max", "moe_router_blocks", "moe_permute_scratch_size", "moe_workspace_size",
+    "moe_router_topk", "moe_permute", "moe_grouped_ffn", "moe_combine", "moe_load_stats",
+    "moe_forward", "moe_host_workspace_size", "moe_forward_host", "moe_get_device_status",
+    "moe_set_wait_limit_ns", "moe_get_wait_limit_ns", "moe_selftest_bounded_wait",
+    "moe_status_string", "moe_version",
+]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+class MoeConfig(C.Structure):
+    _fields_ = [("T", C.c_int64), ("d_model", C.c_int64), ("d_ff", C.c_int64),
+                ("n_experts", C.c_int64), ("top_k", C.c_int64), ("capacity", C.c_int64),
+                ("d_ff_shared", C.c_int64), ("renormalize", C.c_int32), ("act", C.c_int32),
+                ("dtype", C.c_int32), ("reserved", C.c_int32)]
+
+
+class MoeWeights(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in
+                ("W_g", "b_g", "W1", "b1", "W2", "b2", "W1s", "b1s", "W2s", "b2s")]
+
+
+class MoeOutputs(C.Structure):
+    _fields_ = [("y", C.c_void_p), ("topk_idx", C.c_void_p), ("topk_w", C.c_void_p),
+                ("counts", C.c_void_p), ("kept", C.c_void_p), ("dropped", C.c_void_p),
+                ("mean_prob", C.c_void_p), ("balance", C.c_void_p), ("logits", C.c_void_p)]
+
+
+_lib = None
+
+
+def lib() -> C.CDLL:
+    """Load libmoe.so (once).  Raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is not built: run "
+                           "`python -m sparse_mixture_experts_68_b300.build`")
+    L = C.CDLL(LIB_PATH)
+    P = C.c_void_p
+    CP = C.POINTER(MoeConfig)
+    sig = {
+        "moe_rows_max": (C.c_int64, [CP]),
+        "moe_router_blocks": (C.c_int64, [CP]),
+        "moe_permute_scratch_size": (C.c_size_t, [CP]),
+        "moe_workspace_size": (C.c_size_t, [CP]),
+        "moe_host_workspace_size": (C.c_size_t, [CP]),
+        "moe_router_topk": (C.c_int32, [CP, P, P, P, P, P, P, P, P]),
+        "moe_permute": (C.c_int32, [CP, P, P, P, P, P, P, P, P, P, C.c_size_t, P]),
+        "moe_grouped_ffn": (C.c_int32, [CP, P, P, P, C.POINTER(MoeWeights), P, P, P]),
+        "moe_combine": (C.c_int32, [CP, P, P, P, P, P, P]),
+        "moe_load_stats": (C.c_int32, [CP, P, P, P, P, P, P, P]),
+        "moe_forward": (C.c_int32, [CP, P, C.POINTER(MoeWeights), C.POINTER(MoeOutputs), P,
+                                    C.c_size_t, P]),
+        "moe_forward_host": (C.c_int32, [CP, P, C.POINTER(MoeWeights),
+                                         C.POINTER(MoeOutputs), P, C.c_size_t, P]),
+        "moe_get_device_status": (C.c_int32, [P]),
+        "moe_set_wait_limit_ns": (None, [C.c_uint64]),
+        "moe_get_wait_limit_ns": (C.c_uint64, []),
+        "moe_selftest_bounded_wait": (C.c_int32, [C.c_uint64, P]),
+        "moe_status_string": (C.c_char_p, [C.c_int32]),
+        "moe_version": (C.c_int32, []),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(L, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = L
+    return L
+
+
+def status_string(s: int) -> str:
+    return lib().moe_status_string(s).decode()
+
+
+def _check(status: int, what: str):
+    if status != MOE_OK:
+        raise MoeError(status, what)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream=None) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def make_config(wl: Workload, T: int | None = None, capacity: int | None = None) -> MoeConfig:
+    return MoeConfig(T=wl.T if T is None else T, d_model=wl.d_model, d_ff=wl.d_ff,
+                     n_experts=wl.n_experts, top_k=wl.top_k,
+                     capacity=wl.capacity if capacity is None else capacity,
+                     d_ff_shared=wl.d_ff_shared, renormalize=wl.renormalize, act=wl.act,
+                     dtype=MOE_F32 if wl.dtype == DT_F32 else MOE_BF16, reserved=0)
+
+
+def make_weights(t: dict) -> MoeWeights:
+    return MoeWeights(*[_ptr(t.get(n)) for n in
+                        ("W_g", "b_g", "W1", "b1", "W2", "b2", "W1s", "b1s", "W2s", "b2s")])
+
+
+def rows_max(cfg: MoeConfig) -> int:
+    return int(lib().moe_rows_max(C.byref(cfg)))
+
+
+def router_blocks(cfg: MoeConfig) -> int:
+    return int(lib().moe_router_blocks(C.byref(cfg)))
+
+
+def workspace_size(cfg: MoeConfig) -> int:
+    return int(lib().moe_workspace_size(C.byref(cfg)))
+
+
+def host_workspace_size(cfg: MoeConfig) -> int:
+    return int(lib().moe_host_workspace_size(C.byref(cfg)))
+
+
+def permute_scratch_size(cfg: MoeConfig) -> int:
+    return int(lib().moe_permute_scratch_size(C.byref(cfg)))
+
+
+# ---- one call per step -------------------------------------------------------------
+
+def router_topk(cfg, x, W_g, b_g, logits, topk_idx, topk_w, prob_partials, stream=None):
+    _check(lib().moe_router_topk(C.byref(cfg), _ptr(x), _ptr(W_g), _ptr(b_g), _ptr(logits),
+                                 _ptr(topk_idx), _ptr(topk_w), _ptr(prob_partials),
+                                 _stream(stream)), "moe_router_topk")
+
+
+def permute(cfg, x, topk_idx, counts, kept, offsets, row_token, token_row, Xp, scratch,
+            stream=None):
+    _check(lib().moe_permute(C.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(counts), _ptr(kept),
+                             _ptr(offsets), _ptr(row_token), _ptr(token_row), _ptr(Xp),
+                             _ptr(scratch), scratch.numel() * scratch.element_size(),
+                             _stream(stream)), "moe_permute")
+
+
+def grouped_ffn(cfg, Xp, offsets, kept, weights: MoeWeights, H, Yp, stream=None):
+    _check(lib().moe_grouped_ffn(C.byref(cfg), _ptr(Xp), _ptr(offsets), _ptr(kept),
+                                 C.byref(weights), _ptr(H), _ptr(Yp), _stream(stream)),
+           "moe_grouped_ffn")
+
+
+def combine(cfg, Yp, token_row, topk_w, offsets, y, stream=None):
+    _check(lib().moe_combine(C.byref(cfg), _ptr(Yp), _ptr(token_row), _ptr(topk_w),
+                             _ptr(offsets), _ptr(y), _stream(stream)), "moe_combine")
+
+
+def load_stats(cfg, prob_partials, counts, kept, mean_prob, balance, dropped, stream=None):
+    _check(lib().moe_load_stats(C.byref(cfg), _ptr(prob_partials), _ptr(counts), _ptr(kept),
+                                _ptr(mean_prob), _ptr(balance), _ptr(dropped),
+                                _stream(stream)), "moe_load_stats")
+
+
+def get_device_status(stream=None) -> int:
+    return int(lib().moe_get_device_status(_stream(stream)))
+
+
+def set_wait_limit_ns(ns: int):
+    lib().moe_set_wait_limit_ns(int(ns))
+
+
+def get_wait_limit_ns() -> int:
+    return int(lib().moe_get_wait_limit_ns())
+
+
+def selftest_bounded_wait(limit_ns: int, stream=None):
+    _check(lib().moe_selftest_bounded_wait(int(limit_ns), _stream(stream)),
+           "moe_selftest_bounded_wait")
+
+
+# ---- the whole layer --------------------------------------------------------------
+
+@dataclass
+class Outputs:
+    y: torch.Tensor
+    topk_idx: torch.Tensor
+    topk_w: torch.Tensor
+    counts: torch.Tensor
+    kept: torch.Tensor
+    dropped: torch.Tensor
+    mean_prob: torch.Tensor
+    balance: torch.Tensor
+    logits: torch.Tensor | None = None
+
+    def struct(self) -> MoeOutputs:
+        return MoeOutputs(_ptr(self.y), _ptr(self.topk_idx), _ptr(self.topk_w),
+                          _ptr(self.counts), _ptr(self.kept), _ptr(self.dropped),
+                          _ptr(self.mean_prob), _ptr(self.balance), _ptr(self.logits))
+
+
+def alloc_outputs(cfg: MoeConfig, device, with_logits=False, pin_memory=False) -> Outputs:
+    T, k, N, d = cfg.T, cfg.top_k, cfg.n_experts, cfg.d_model
+    dt = torch.float32 if cfg.dtype == MOE_F32 else torch.bfloat16
+    kw = dict(device=device, pin_memory=pin_memory) if pin_memory else dict(device=device)
+    return Outputs(
+        y=torch.empty((T, d), dtype=dt, **kw),
+        topk_idx=torch.empty((T, k), dtype=torch.int32, **kw),
+        topk_w=torch.empty((T, k), dtype=torch.float32, **kw),
+        counts=torch.empty((N,), dtype=torch.int32, **kw),
+        kept=torch.empty((N,), dtype=torch.int32, **kw),
+        dropped=torch.empty((1,), dtype=torch.int32, **kw),
+        mean_prob=torch.empty((N,), dtype=torch.float32, **kw),
+        balance=torch.empty((1,), dtype=torch.float32, **kw),
+        logits=torch.empty((T, N), dtype=torch.float32, **kw) if with_logits else None)
+
+
+def forward(cfg: MoeConfig, x, weights: MoeWeights, out: Outputs, workspace, stream=None):
+    _check(lib().moe_forward(C.byref(cfg), _ptr(x), C.byref(weights), C.byref(out.struct()),
+                             _ptr(workspace), workspace.numel() * workspace.element_size(),
+                             _stream(stream)), "moe_forward")
+
+
+def forward_host(cfg: MoeConfig, x_host, weights: MoeWeights, out_host: Outputs, workspace,
+                 stream=None):
+    _check(lib().moe_forward_host(C.byref(cfg), _ptr(x_host), C.byref(weights),
+                                  C.byref(out_host.struct()), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(),
+                                  _stream(stream)), "moe_forward_host")
+
+
+class MoeLayer:
+    """Device-resident weights + workspace of one layer; ``forward`` runs it."""
+
+    def __init__(self, wl: Workload, tensors: dict, device="cuda", T: int | None = None,
+                 capacity: int | None = None):
+        self.wl = wl
+        self.t = tensors
+        self.device = torch.device(device)
+        self.cfg = make_config(wl, T=T, capacity=capacity)
+        self.weights = make_weights(tensors)
+        self.workspace = torch.empty(max(workspace_size(self.cfg), 256), dtype=torch.uint8,
+                                     device=self.device)
+
+    def set_tokens(self, T: int):
+        self.cfg = make_config(self.wl, T=T, capacity=self.cfg.capacity)
+        need = workspace_size(self.cfg)
+        if need > self.workspace.numel():
+            self.workspace = torch.empty(need, dtype=torch.uint8, device=self.device)
+
+    def forward(self, x, out: Outputs | None = None, with_logits=False, stream=None) -> Outputs:
+        if out is None:
+            out = alloc_outputs(self.cfg, self.device, with_logits=with_logits)
+        forward(self.cfg, x, self.weights, out, self.workspace, stream)
+        return out
+
+
+class StagedLayer(MoeLayer):
+    """The layer as its five C-ABI steps with every intermediate in its own
+    tensor, so a caller can place CUDA events between the steps."""
+
+    STAGES = ("router_topk", "permute", "grouped_ffn", "combine", "load_stats")
+
+    def __init__(self, wl: Workload, tensors: dict, device="cuda", T: int | None = None,
+                 capacity: int | None = None):
+        super().__init__(wl, tensors, device, T, capacity)
+        cfg, dev = self.cfg, self.device
+        T, k, N = cfg.T, cfg.top_k, cfg.n_experts
+        rows = rows_max(cfg)
+        dt = torch.float32 if cfg.dtype == MOE_F32 else torch.bfloat16
+        self.logits = torch.empty((T, N), dtype=torch.float32, device=dev)
+        self.pp = torch.empty((max(router_blocks(cfg), 1), N), dtype=torch.float32, device=dev)
+        self.offsets = torch.empty(N + 2, dtype=torch.int32, device=dev)
+        self.row_token = torch.empty(max(rows, 1), dtype=torch.int32, device=dev)
+        self.token_row = torch.empty((T, k), dtype=torch.int32, device=dev)
+        self.scratch = torch.empty(max(permute_scratch_size(cfg), 256), dtype=torch.uint8,
+                                   device=dev)
+        self.Xp = torch.empty((rows, cfg.d_model), dtype=dt, device=dev)
+        self.H = torch.empty((rows, cfg.d_ff), dtype=dt, device=dev)
+        self.Yp = torch.empty((rows, cfg.d_model), dtype=dt, device=dev)
+
+    def run(self, x, out: Outputs, events=None, stream=None):
+        """events: None or a list of 6 torch.cuda.Event recorded around the steps."""
+        cfg, t = self.cfg, self.t
+        ev = events or [None] * 6
+
+        def mark(i):
+            if ev[i] is not None:
+                ev[i].record(stream)
+
+        mark(0)
+        router_topk(cfg, x, t["W_g"], t["b_g"], self.logits, out.topk_idx, out.topk_w,
+                    self.pp, stream)
+        mark(1)
+        permute(cfg, x, out.topk_idx, out.counts, out.kept, self.offsets, self.row_token,
+                self.token_row, self.Xp, self.scratch, stream)
+        mark(2)
+        grouped_ffn(cfg, self.Xp, self.offsets, out.kept, self.weights, self.H, self.Yp,
+                    stream)
+        mark(3)
+        combine(cfg, self.Yp, self.token_row, out.topk_w, self.offsets, out.y, stream)
+        mark(4)
+        load_stats(cfg, self.pp, out.counts, out.kept, out.mean_prob, out.balance,
+                   out.dropped, stream)
+        mark(5)
+
+    # kernels launched per step (router 2, permute 4, grouped FFN 2, combine 1, stats 1)
+    LAUNCHES_PER_STEP = 10

@@ -1,0 +1,399 @@
+// C ABI of libmoe (declared in include/moe.h): host-side validation,
+// workspace layout, and the sequence of launches of one layer.
+#include <atomic>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+__device__ int32_t g_device_status = MOE_OK;
+
+namespace {
+
+std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t elem_bytes(const moe_config& c) { return c.dtype == MOE_F32 ? 4 : 2; }
+
+moe_status check_config(const moe_config* cfg) {
+  if (!cfg) return MOE_ERR_INVALID_ARG;
+  const moe_config& c = *cfg;
+  if (c.T < 0 || c.d_model <= 0 || c.d_ff <= 0 || c.n_experts < 1 || c.top_k < 1 ||
+      c.top_k > c.n_experts || c.d_ff_shared < 0 || c.reserved != 0)
+    return MOE_ERR_INVALID_ARG;
+  if (c.dtype != MOE_F32 && c.dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (c.act != MOE_ACT_GELU_ERF && c.act != MOE_ACT_RELU) return MOE_ERR_INVALID_ARG;
+  if (c.renormalize != 0 && c.renormalize != 1) return MOE_ERR_INVALID_ARG;
+  if (c.n_experts > 1024) return MOE_ERR_UNSUPPORTED;
+  if (c.d_model % 8 != 0 || c.d_ff % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if (c.dtype == MOE_BF16 && (c.d_model % 64 != 0 || c.d_ff % 64 != 0))
+    return MOE_ERR_UNSUPPORTED;
+  if (c.d_ff_shared != 0 && c.d_ff_shared != c.d_ff) return MOE_ERR_UNSUPPORTED;
+  // 32-bit row indices inside the kernels
+  const int64_t rows = c.T * c.top_k + c.n_experts * (kGroupAlign - 1) + c.T + kGroupAlign;
+  if (rows >= (int64_t(1) << 31) || c.T * c.top_k >= (int64_t(1) << 31))
+    return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int64_t rows_max_of(const moe_config& c) {
+  int64_t r = c.T * c.top_k + c.n_experts * (kGroupAlign - 1);
+  if (c.d_ff_shared > 0) r += round_up(c.T, kGroupAlign);
+  return r;
+}
+
+int64_t router_blocks_of(const moe_config& c) { return ceil_div(c.T, kRouterTokensPerBlock); }
+
+// Workspace of moe_forward: every region 256-byte aligned.
+struct Workspace {
+  float* logits;
+  float* prob_partials;
+  int32_t* offsets;
+  int32_t* row_token;
+  int32_t* token_row;
+  void* scratch;
+  size_t scratch_bytes;
+  void* Xp;
+  void* H;
+  void* Yp;
+  size_t bytes;
+};
+
+Workspace layout(const moe_config& c, void* base) {
+  Workspace w{};
+  uintptr_t p = reinterpret_cast<uintptr_t>(base);
+  size_t off = 0;
+  auto take = [&](size_t n) {
+    const size_t at = off;
+    off += (n + 255) / 256 * 256;
+    return reinterpret_cast<void*>(p + at);
+  };
+  const int64_t rows = rows_max_of(c);
+  const int64_t es = elem_bytes(c);
+  w.logits = static_cast<float*>(take(size_t(c.T * c.n_experts) * 4));
+  w.prob_partials = static_cast<float*>(take(size_t(router_blocks_of(c) * c.n_experts) * 4));
+  w.offsets = static_cast<int32_t*>(take(size_t(c.n_experts + 2) * 4));
+  w.row_token = static_cast<int32_t*>(take(size_t(rows) * 4));
+  w.token_row = static_cast<int32_t*>(take(size_t(c.T * c.top_k) * 4));
+  w.scratch_bytes = permute_scratch_bytes(c);
+  w.scratch = take(w.scratch_bytes);
+  w.Xp = take(size_t(rows * c.d_model * es));
+  w.H = take(size_t(rows * c.d_ff * es));
+  w.Yp = take(size_t(rows * c.d_model * es));
+  w.bytes = off;
+  return w;
+}
+
+// Device status word address and SM count, per device.
+struct DeviceInfo {
+  int32_t* status = nullptr;
+  int num_sms = 0;
+};
+
+bool device_info(DeviceInfo* out) {
+  static std::mutex mu;
+  static DeviceInfo cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev].status) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_device_status) != cudaSuccess) return false;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return false;
+    cache[dev].status = static_cast<int32_t*>(ptr);
+    cache[dev].num_sms = sms;
+  }
+  *out = cache[dev];
+  return true;
+}
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+moe_status check_weights(const moe_config& c, const moe_weights* w, bool router, bool experts) {
+  if (!w) return MOE_ERR_INVALID_ARG;
+  if (router && (!w->W_g || !w->b_g || !aligned16(w->W_g) || !aligned16(w->b_g)))
+    return MOE_ERR_INVALID_ARG;
+  if (experts) {
+    const void* ps[] = {w->W1, w->b1, w->W2, w->b2};
+    for (const void* q : ps)
+      if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+    if (c.d_ff_shared > 0) {
+      const void* ss[] = {w->W1s, w->b1s, w->W2s, w->b2s};
+      for (const void* q : ss)
+        if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+    }
+  }
+  return MOE_OK;
+}
+
+__global__ void bounded_wait_selftest_kernel(uint64_t limit_ns, int32_t* status) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    // nothing arrives on `bar`: the wait runs out after limit_ns
+    mbar_wait_bounded(&bar, 0, limit_ns, status);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_bounded_wait_selftest(uint64_t limit_ns, int32_t* status, cudaStream_t s) {
+  bounded_wait_selftest_kernel<<<1, 32, 0, s>>>(limit_ns, status);
+  return cudaGetLastError();
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int32_t moe_version(void) { return 1; }
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported layer shape";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+void moe_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns); }
+uint64_t moe_get_wait_limit_ns(void) { return g_wait_limit_ns.load(); }
+
+int64_t moe_rows_max(const moe_config* cfg) {
+  if (check_config(cfg) != MOE_OK) return -1;
+  return rows_max_of(*cfg);
+}
+
+int64_t moe_router_blocks(const moe_config* cfg) {
+  if (check_config(cfg) != MOE_OK) return -1;
+  return router_blocks_of(*cfg);
+}
+
+size_t moe_permute_scratch_size(const moe_config* cfg) {
+  if (check_config(cfg) != MOE_OK) return 0;
+  return permute_scratch_bytes(*cfg);
+}
+
+size_t moe_workspace_size(const moe_config* cfg) {
+  if (check_config(cfg) != MOE_OK) return 0;
+  return layout(*cfg, nullptr).bytes;
+}
+
+moe_status moe_router_topk(const moe_config* cfg, const void* x, const void* W_g,
+                           const void* b_g, float* logits, int32_t* topk_idx, float* topk_w,
+                           float* prob_partials, void* stream) {
+  moe_status st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  const void* ps[] = {x, W_g, b_g, logits, topk_idx, topk_w, prob_partials};
+  for (const void* q : ps)
+    if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_router_logits(*cfg, x, W_g, b_g, logits, s);
+  if (e == cudaSuccess) e = launch_router_softmax_topk(*cfg, logits, topk_idx, topk_w,
+                                                       prob_partials, s);
+  return cuda_status(e);
+}
+
+moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk_idx,
+                       int32_t* counts, int32_t* kept, int32_t* offsets, int32_t* row_token,
+                       int32_t* token_row, void* Xp, void* scratch, size_t scratch_bytes,
+                       void* stream) {
+  moe_status st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  const void* ps[] = {x, topk_idx, counts, kept, offsets, row_token, token_row, Xp, scratch};
+  for (const void* q : ps)
+    if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  if (scratch_bytes < permute_scratch_bytes(*cfg)) return MOE_ERR_WORKSPACE;
+  return cuda_status(launch_permute(*cfg, x, topk_idx, counts, kept, offsets, row_token,
+                                    token_row, Xp, scratch, rows_max_of(*cfg),
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_grouped_ffn(const moe_config* cfg, const void* Xp, const int32_t* offsets,
+                           const int32_t* kept, const moe_weights* w, void* H, void* Yp,
+                           void* stream) {
+  moe_status st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  st = check_weights(*cfg, w, false, true);
+  if (st != MOE_OK) return st;
+  const void* ps[] = {Xp, offsets, kept, H, Yp};
+  for (const void* q : ps)
+    if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  DeviceInfo di;
+  if (!device_info(&di)) return MOE_ERR_CUDA;
+  GroupedFfnArgs a{};
+  a.Xp = Xp; a.offsets = offsets; a.kept = kept; a.w = w; a.H = H; a.Yp = Yp;
+  a.rows_max = rows_max_of(*cfg);
+  a.status = di.status;
+  a.wait_limit_ns = g_wait_limit_ns.load();
+  a.num_sms = di.num_sms;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return cuda_status(cfg->dtype == MOE_F32 ? launch_grouped_ffn_f32(*cfg, a, s)
+                                           : launch_grouped_ffn_bf16(*cfg, a, s));
+}
+
+moe_status moe_combine(const moe_config* cfg, const void* Yp, const int32_t* token_row,
+                       const float* topk_w, const int32_t* offsets, void* y, void* stream) {
+  moe_status st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  const void* ps[] = {Yp, token_row, topk_w, offsets, y};
+  for (const void* q : ps)
+    if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_combine(*cfg, Yp, token_row, topk_w, offsets, y,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_load_stats(const moe_config* cfg, const float* prob_partials,
+                          const int32_t* counts, const int32_t* kept, float* mean_prob,
+                          float* balance, int32_t* dropped, void* stream) {
+  moe_status st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  const void* ps[] = {prob_partials, counts, kept, mean_prob, balance, dropped};
+  for (const void* q : ps)
+    if (!q) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_load_stats(*cfg, prob_partials, counts, kept, mean_prob, balance,
+                                       dropped, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* w,
+                       const moe_outputs* out, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  moe_status st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  const moe_config& c = *cfg;
+  st = check_weights(c, w, true, true);
+  if (st != MOE_OK) return st;
+  // token-sized buffers may be NULL when there are no tokens
+  auto token_buf_ok = [&](const void* q) { return c.T == 0 || (q && aligned16(q)); };
+  if (!out || !token_buf_ok(x) || !workspace ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return MOE_ERR_INVALID_ARG;
+  if (!token_buf_ok(out->y) || !token_buf_ok(out->topk_idx) || !token_buf_ok(out->topk_w))
+    return MOE_ERR_INVALID_ARG;
+  const void* ps[] = {out->counts, out->kept};
+  for (const void* q : ps)
+    if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  if (!out->dropped || !out->mean_prob || !out->balance) return MOE_ERR_INVALID_ARG;
+  if (out->logits && !aligned16(out->logits)) return MOE_ERR_INVALID_ARG;
+  Workspace ws = layout(c, workspace);
+  if (workspace_bytes < ws.bytes) return MOE_ERR_WORKSPACE;
+  DeviceInfo di;
+  if (!device_info(&di)) return MOE_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* logits = out->logits ? out->logits : ws.logits;
+
+  cudaError_t e = launch_router_logits(c, x, w->W_g, w->b_g, logits, s);
+  if (e == cudaSuccess)
+    e = launch_router_softmax_topk(c, logits, out->topk_idx, out->topk_w, ws.prob_partials, s);
+  if (e == cudaSuccess)
+    e = launch_permute(c, x, out->topk_idx, out->counts, out->kept, ws.offsets, ws.row_token,
+                       ws.token_row, ws.Xp, ws.scratch, rows_max_of(c), s);
+  if (e == cudaSuccess) {
+    GroupedFfnArgs a{};
+    a.Xp = ws.Xp; a.offsets = ws.offsets; a.kept = out->kept; a.w = w; a.H = ws.H;
+    a.Yp = ws.Yp; a.rows_max = rows_max_of(c); a.status = di.status;
+    a.wait_limit_ns = g_wait_limit_ns.load(); a.num_sms = di.num_sms;
+    e = c.dtype == MOE_F32 ? launch_grouped_ffn_f32(c, a, s) : launch_grouped_ffn_bf16(c, a, s);
+  }
+  if (e == cudaSuccess)
+    e = launch_combine(c, ws.Yp, ws.token_row, out->topk_w, ws.offsets, out->y, s);
+  if (e == cudaSuccess)
+    e = launch_load_stats(c, ws.prob_partials, out->counts, out->kept, out->mean_prob,
+                          out->balance, out->dropped, s);
+  return cuda_status(e);
+}
+
+size_t moe_host_workspace_size(const moe_config* cfg) {
+  if (check_config(cfg) != MOE_OK) return 0;
+  const moe_config& c = *cfg;
+  auto r = [](size_t n) { return (n + 255) / 256 * 256; };
+  const size_t es = size_t(elem_bytes(c));
+  return layout(c, nullptr).bytes + 2 * r(size_t(c.T * c.d_model) * es) +
+         2 * r(size_t(c.T * c.top_k) * 4) + 3 * r(size_t(c.n_experts) * 4) + 2 * r(4) +
+         r(size_t(c.T * c.n_experts) * 4);
+}
+
+moe_status moe_forward_host(const moe_config* cfg, const void* x_host, const moe_weights* w,
+                            const moe_outputs* oh, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  moe_status st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  if (!x_host || !oh || !oh->y || !oh->topk_idx || !oh->topk_w || !oh->counts || !oh->kept ||
+      !oh->dropped || !oh->mean_prob || !oh->balance || !workspace ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return MOE_ERR_INVALID_ARG;
+  const moe_config& c = *cfg;
+  if (workspace_bytes < moe_host_workspace_size(cfg)) return MOE_ERR_WORKSPACE;
+  const size_t base = layout(c, nullptr).bytes;
+  uint8_t* p = static_cast<uint8_t*>(workspace) + base;
+  auto take = [&](size_t n) {
+    uint8_t* at = p;
+    p += (n + 255) / 256 * 256;
+    return static_cast<void*>(at);
+  };
+  const size_t es = size_t(elem_bytes(c));
+  const size_t xb = size_t(c.T * c.d_model) * es, kb = size_t(c.T * c.top_k) * 4,
+               nb = size_t(c.n_experts) * 4, lb = size_t(c.T * c.n_experts) * 4;
+  void* xd = take(xb);
+  moe_outputs od{};
+  od.y = take(xb);
+  od.topk_idx = static_cast<int32_t*>(take(kb));
+  od.topk_w = static_cast<float*>(take(kb));
+  od.counts = static_cast<int32_t*>(take(nb));
+  od.kept = static_cast<int32_t*>(take(nb));
+  od.mean_prob = static_cast<float*>(take(nb));
+  od.dropped = static_cast<int32_t*>(take(4));
+  od.balance = static_cast<float*>(take(4));
+  od.logits = oh->logits ? static_cast<float*>(take(lb)) : nullptr;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (xb && cudaMemcpyAsync(xd, x_host, xb, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  st = moe_forward(cfg, xd, w, &od, workspace, base, stream);
+  if (st != MOE_OK) return st;
+  struct Copy { void* dst; const void* src; size_t n; };
+  const Copy copies[] = {{oh->y, od.y, xb},
+                         {oh->topk_idx, od.topk_idx, kb},
+                         {oh->topk_w, od.topk_w, kb},
+                         {oh->counts, od.counts, nb},
+                         {oh->kept, od.kept, nb},
+                         {oh->mean_prob, od.mean_prob, nb},
+                         {oh->dropped, od.dropped, 4},
+                         {oh->balance, od.balance, 4},
+                         {oh->logits, od.logits, oh->logits ? lb : 0}};
+  for (const Copy& cp : copies)
+    if (cp.n && cudaMemcpyAsync(cp.dst, cp.src, cp.n, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  return cuda_status(cudaStreamSynchronize(s));
+}
+
+moe_status moe_get_device_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  int32_t v = MOE_OK;
+  const int32_t zero = MOE_OK;
+  if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof(v)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (v != MOE_OK && cudaMemcpyToSymbol(g_device_status, &zero, sizeof(zero)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return v;
+}
+
+moe_status moe_selftest_bounded_wait(uint64_t limit_ns, void* stream) {
+  DeviceInfo di;
+  if (!device_info(&di)) return MOE_ERR_CUDA;
+  return cuda_status(
+      launch_bounded_wait_selftest(limit_ns, di.status, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,37 @@
+// fp32 expert FFN on CUDA cores: H = act(Xp . W1[e]^T + b1[e]),
+// Yp = H . W2[e]^T + b2[e] per expert group (botmartz.com "Mixture of Experts
+// (MoE) and Mixtral", "Expert Routing": Linear -> GELU -> Linear;
+// codingnowai.in "Mixture of Experts", "Code": Linear -> ReLU -> Linear).
+// The fp32 layer keeps full fp32 products and sums (tf32 tensor-core inputs
+// would round the operands to 11 bits).
+#include "kernels.h"
+#include "simt_gemm.cuh"
+
+namespace moe {
+
+cudaError_t launch_grouped_ffn_f32(const moe_config& c, const GroupedFfnArgs& g,
+                                   cudaStream_t s) {
+  if (g.rows_max == 0) return cudaSuccess;
+  SimtGemmArgs a{};
+  a.offsets = g.offsets;
+  a.kept = g.kept;
+  a.n_routed = int32_t(c.n_experts);
+  a.shared_rows = c.d_ff_shared > 0 ? int32_t(c.T) : 0;
+  a.act = c.act;
+  // first Linear: [rows, d] x [d_ff, d]^T
+  a.A = g.Xp; a.B = g.w->W1; a.Bs = g.w->W1s; a.bias = g.w->b1; a.bias_s = g.w->b1s;
+  a.C = g.H; a.K = c.d_model; a.Nc = c.d_ff;
+  dim3 grid1(unsigned(ceil_div(c.d_ff, kSimtBN)), unsigned(ceil_div(g.rows_max, kSimtBM)));
+  simt_gemm_kernel<float, float><<<grid1, kSimtThreads, 0, s>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // second Linear: [rows, d_ff] x [d, d_ff]^T
+  a.act = -1;
+  a.A = g.H; a.B = g.w->W2; a.Bs = g.w->W2s; a.bias = g.w->b2; a.bias_s = g.w->b2s;
+  a.C = g.Yp; a.K = c.d_ff; a.Nc = c.d_model;
+  dim3 grid2(unsigned(ceil_div(c.d_model, kSimtBN)), unsigned(ceil_div(g.rows_max, kSimtBM)));
+  simt_gemm_kernel<float, float><<<grid2, kSimtThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,498 @@
+// bf16 expert FFN on the 5th-generation tensor cores (tcgen05 + TMEM, fed by
+// TMA), sm_103a.
+//
+//   H  = act(Xp[group e] . W1[e]^T + b1[e])     (first Linear + activation)
+//   Yp = H[group e] . W2[e]^T + b2[e]             (second Linear)
+//
+// per expert group e (botmartz.com "Mixture of Experts (MoE) and Mixtral",
+// "Expert Routing": each expert is Linear(d_model, d_ff) -> GELU ->
+// Linear(d_ff, d_model); codingnowai.in "Mixture of Experts", "Code": ReLU).
+//
+// One persistent kernel per Linear.  The output tiles of all groups form one
+// list -- group by group, within a group the n-tiles outermost and the m-tiles
+// innermost, so CTAs working at the same time share a weight tile in L2 --
+// and CTA b takes tiles b, b + gridDim.x, ...  Roles inside a CTA:
+//   warp 0      TMA producer: A tile [128 x 64] and B tile [BN x 64] per
+//               k-block into a kStages-deep shared-memory ring (128B swizzle)
+//   warp 1      allocates TMEM; one thread issues tcgen05.mma
+//               (M=128, N=BN, K=16, bf16 x bf16 -> fp32) into one of two TMEM
+//               accumulators and commits to the ring's "empty" barriers
+//   warps 2-9   epilogue: tcgen05.ld the accumulator (two warps per TMEM lane
+//               quarter, each half of the columns), + bias, activation, bf16,
+//               store the live rows; then free the accumulator
+// Double-buffered accumulators let the epilogue of one tile overlap the
+// main loop of the next.  Every wait is bounded (a time limit, then the
+// device status word records MOE_ERR_TIMEOUT and the CTA winds down).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "kernels.h"
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;                 // rows per tile = TMEM lanes
+constexpr int BK = 64;                  // 64 bf16 = 128 B = one swizzle row
+constexpr int kStages = 4;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = (2 + kEpiWarps) * 32;
+constexpr int kMaxGroups = 1025;        // 1024 routed + 1 shared
+
+enum { EPI_BIAS = 0, EPI_BIAS_GELU = 1, EPI_BIAS_RELU = 2 };
+
+template <int BN>
+struct Layout {
+  static constexpr int kABytes = BM * BK * 2;
+  static constexpr int kBBytes = BN * BK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kA = 0;
+  static constexpr int kB = kStages * kABytes;
+  static constexpr int kBar = kB + kStages * kBBytes;       // full[S], empty[S], tfull[2], tempty[2], done
+  static constexpr int kNumBars = 2 * kStages + 5;
+  static constexpr int kTmemSlot = kBar + kNumBars * 8;
+  static constexpr int kAbort = kTmemSlot + 4;
+  static constexpr int kTileStart = (kAbort + 4 + 15) / 16 * 16;   // int32 [kMaxGroups + 1]
+  static constexpr int kGroupOff = kTileStart + (kMaxGroups + 1) * 4;  // int32 [kMaxGroups]
+  static constexpr int kBytes = kGroupOff + kMaxGroups * 4;
+  static constexpr int kAlloc = kBytes + 1024;              // room to align the base to 1 KB
+  static_assert(kAlloc <= 227 * 1024, "shared memory budget");
+};
+
+struct TcParams {
+  const int32_t* offsets;          // [n_groups + 1] first row of each group
+  const int32_t* kept;             // [n_routed] live rows of each routed group
+  const __nv_bfloat16* bias;       // [n_routed, Nd]
+  const __nv_bfloat16* bias_s;     // [Nd] shared expert
+  __nv_bfloat16* out;              // [rows, Nd]
+  int64_t Nd;
+  int32_t n_routed;
+  int32_t shared_rows;             // live rows of the shared group; 0 = none
+  int32_t num_kb;                  // K / BK
+  int32_t* status;
+  uint64_t wait_limit_ns;
+};
+
+// ---- PTX wrappers ------------------------------------------------------------------
+
+__device__ __forceinline__ void tma_load_2d(const CUtensorMap* map, uint32_t dst, uint32_t bar,
+                                            int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(const CUtensorMap* map, uint32_t dst, uint32_t bar,
+                                            int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 B, 8-row groups 1024 B apart (stride byte offset); descriptor version 1.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+  return uint64_t((saddr & 0x3FFFFu) >> 4) | (uint64_t(1) << 16) |
+         (uint64_t(1024 >> 4) << 32) | (uint64_t(1) << 46) | (uint64_t(2) << 61);
+}
+
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major.
+template <int BN>
+__host__ __device__ constexpr uint32_t idesc_bf16_f32() {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(BN >> 3) << 17) |
+         (uint32_t(BM >> 4) << 24);
+}
+
+// Bounded wait that also gives up when another role has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
+                                              const TcParams& p, volatile int* abort_flag) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait(a, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(a, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > p.wait_limit_ns) {
+        atomicCAS(p.status, MOE_OK, MOE_ERR_TIMEOUT);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+struct TileCoord {
+  int g, m, n;
+};
+
+// Largest group g with tile_start[g] <= tile (non-empty by construction).
+__device__ __forceinline__ TileCoord decode_tile(int tile, const int32_t* tile_start,
+                                                 int n_groups, int ntiles) {
+  int lo = 0, hi = n_groups - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (tile_start[mid] <= tile) lo = mid; else hi = mid - 1;
+  }
+  const int local = tile - tile_start[lo];
+  const int mt = (tile_start[lo + 1] - tile_start[lo]) / ntiles;
+  return TileCoord{lo, local % mt, local / mt};
+}
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                           const __grid_constant__ CUtensorMap tmB,
+                           const __grid_constant__ CUtensorMap tmBs, const TcParams p) {
+  using L = Layout<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kStages;
+  uint64_t* tfull = bars + 2 * kStages;
+  uint64_t* tempty = bars + 2 * kStages + 2;
+  uint64_t* done = bars + 2 * kStages + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
+  int32_t* tile_start = reinterpret_cast<int32_t*>(smem + L::kTileStart);
+  int32_t* grp_off = reinterpret_cast<int32_t*>(smem + L::kGroupOff);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_groups = p.n_routed + (p.shared_rows > 0 ? 1 : 0);
+  const int ntiles = int(p.Nd / BN);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], kEpiWarps);
+    }
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(2 * BN));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  if (warp == 2) {
+    // tile_start[g] = sum over earlier groups of m-tiles x n-tiles (warp scan)
+    int32_t carry = 0;
+    for (int base = 0; base < n_groups; base += 32) {
+      const int g = base + lane;
+      int32_t live = 0, off = 0;
+      if (g < n_groups) {
+        off = p.offsets[g];
+        live = g < p.n_routed ? p.kept[g] : p.shared_rows;
+        grp_off[g] = off;
+      }
+      const int32_t tiles = int32_t((live + BM - 1) / BM) * ntiles;
+      int32_t incl = tiles;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (g < n_groups) tile_start[g] = carry + incl - tiles;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) tile_start[n_groups] = carry;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total_tiles = tile_start[n_groups];
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      int last_parity[kStages];
+#pragma unroll
+      for (int s = 0; s < kStages; ++s) last_parity[s] = -1;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        const TileCoord tc = decode_tile(tile, tile_start, n_groups, ntiles);
+        const int row0 = grp_off[tc.g] + tc.m * BM;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!wait_or_abort(&empty[stage], phase ^ 1u, p, abort_flag)) { ok = false; break; }
+          const uint32_t fb = smem_u32(&full[stage]);
+          mbar_arrive_expect_tx(&full[stage], L::kStageBytes);
+          tma_load_2d(&tmA, smem_u32(smem + L::kA + stage * L::kABytes), fb, kb * BK, row0);
+          if (tc.g < p.n_routed)
+            tma_load_3d(&tmB, smem_u32(smem + L::kB + stage * L::kBBytes), fb, kb * BK,
+                        tc.n * BN, tc.g);
+          else
+            tma_load_2d(&tmBs, smem_u32(smem + L::kB + stage * L::kBBytes), fb, kb * BK,
+                        tc.n * BN);
+          last_parity[stage] = int(phase);
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        // wind down: let copies already in flight land before the CTA exits
+        for (int s = 0; s < kStages; ++s)
+          if (last_parity[s] >= 0) {
+            const uint32_t a = smem_u32(&full[s]);
+            const uint64_t t0 = global_timer_ns();
+            while (!mbar_try_wait(a, uint32_t(last_parity[s])) &&
+                   global_timer_ns() - t0 < p.wait_limit_ns) {
+            }
+          }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32<BN>();
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        if (!wait_or_abort(&tempty[acc], acc_phase ^ 1u, p, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!wait_or_abort(&full[stage], phase, p, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t ad = sdesc_sw128(smem_u32(smem + L::kA + stage * L::kABytes));
+          const uint64_t bd = sdesc_sw128(smem_u32(smem + L::kB + stage * L::kBBytes));
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)   // +32 bytes along K per step
+            tc_mma(d_tmem, ad + uint64_t(2 * kk), bd + uint64_t(2 * kk), idesc,
+                   (kb | kk) != 0 ? 1u : 0u);
+          tc_commit(smem_u32(&empty[stage]));
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit(smem_u32(&tfull[acc]));
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      // every MMA issued by this thread has completed once `done` flips
+      tc_commit(smem_u32(done));
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_try_wait(smem_u32(done), 0) && global_timer_ns() - t0 < p.wait_limit_ns) {
+      }
+    }
+  } else {
+    // ---------------- epilogue ----------------
+    const int q = warp & 3;                      // TMEM lane quarter of this warp
+    const int half = (warp - 2) >> 2;            // which half of the tile's columns
+    constexpr int kCols = BN / 2;
+    uint32_t acc = 0, acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+      const TileCoord tc = decode_tile(tile, tile_start, n_groups, ntiles);
+      bool ok = true;
+      if (lane == 0) ok = wait_or_abort(&tfull[acc], acc_phase, p, abort_flag);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      tc_fence_after();
+      const bool routed = tc.g < p.n_routed;
+      const int live = routed ? p.kept[tc.g] : p.shared_rows;
+      const int row_in_group = tc.m * BM + q * 32 + lane;
+      const bool valid = row_in_group < live;
+      const int64_t out_row = int64_t(grp_off[tc.g]) + row_in_group;
+      const __nv_bfloat16* bias = routed ? p.bias + int64_t(tc.g) * p.Nd : p.bias_s;
+#pragma unroll 1
+      for (int c = half * kCols; c < (half + 1) * kCols; c += 32) {
+        uint32_t r[32];
+        tmem_ld_32cols(tmem_base + (uint32_t(q * 32) << 16) + acc * BN + c, r);
+        if (valid) {
+          const int64_t col = int64_t(tc.n) * BN + c;
+          const uint4* bsrc = reinterpret_cast<const uint4*>(bias + col);
+          uint4* dst = reinterpret_cast<uint4*>(p.out + out_row * p.Nd + col);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const uint4 bv = __ldg(bsrc + v);
+            const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&bv);
+            uint4 o;
+            __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float2 bf = __bfloat1622float2(b2[i]);
+              float x0 = __uint_as_float(r[8 * v + 2 * i]) + bf.x;
+              float x1 = __uint_as_float(r[8 * v + 2 * i + 1]) + bf.y;
+              if (EPI == EPI_BIAS_GELU) { x0 = gelu_erf(x0); x1 = gelu_erf(x1); }
+              if (EPI == EPI_BIAS_RELU) { x0 = fmaxf(x0, 0.f); x1 = fmaxf(x1, 0.f); }
+              o2[i] = __floats2bfloat162_rn(x0, x1);
+            }
+            dst[v] = o;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(2 * BN));
+  }
+}
+
+// ---- host side -----------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// bf16 tensor [outer, inner] (or [z, outer, inner]) read in boxes of
+// [box_outer, 64] with 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t z,
+              uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {inner, outer, z};
+  const cuuint64_t strides[2] = {inner * 2, inner * outer * 2};
+  const cuuint32_t box[3] = {uint32_t(BK), box_outer, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const cuuint32_t rank = z > 0 ? 3 : 2;
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, int EPI>
+cudaError_t launch_tc(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& Bs,
+                      const TcParams& p, int grid, cudaStream_t s) {
+  auto kern = tc_grouped_gemm_kernel<BN, EPI>;
+  const int smem = Layout<BN>::kAlloc;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, smem, s>>>(A, B, Bs, p);
+  return cudaGetLastError();
+}
+
+template <int BN>
+cudaError_t launch_epi(int epi, const CUtensorMap& A, const CUtensorMap& B,
+                       const CUtensorMap& Bs, const TcParams& p, int grid, cudaStream_t s) {
+  if (epi == EPI_BIAS_GELU) return launch_tc<BN, EPI_BIAS_GELU>(A, B, Bs, p, grid, s);
+  if (epi == EPI_BIAS_RELU) return launch_tc<BN, EPI_BIAS_RELU>(A, B, Bs, p, grid, s);
+  return launch_tc<BN, EPI_BIAS>(A, B, Bs, p, grid, s);
+}
+
+int pick_bn(int64_t Nd) {
+  if (Nd % 256 == 0) return 256;
+  if (Nd % 128 == 0) return 128;
+  return 64;
+}
+
+// One grouped Linear: out[group g] = epi(A[group g] . W[g]^T + bias[g]).
+cudaError_t grouped_linear(const moe_config& c, const GroupedFfnArgs& g, const void* A,
+                           const void* W, const void* Ws, const void* bias,
+                           const void* bias_s, void* out, int64_t K, int64_t Nd, int epi,
+                           cudaStream_t s) {
+  const int bn = pick_bn(Nd);
+  const int64_t N = c.n_experts;
+  CUtensorMap mA, mB, mBs;
+  if (!make_map(&mA, A, uint64_t(K), uint64_t(g.rows_max), 0, BM)) return cudaErrorInvalidValue;
+  if (!make_map(&mB, W, uint64_t(K), uint64_t(Nd), uint64_t(N), uint32_t(bn)))
+    return cudaErrorInvalidValue;
+  if (c.d_ff_shared > 0) {
+    if (!make_map(&mBs, Ws, uint64_t(K), uint64_t(Nd), 0, uint32_t(bn)))
+      return cudaErrorInvalidValue;
+  } else {
+    mBs = mB;
+  }
+  TcParams p{};
+  p.offsets = g.offsets;
+  p.kept = g.kept;
+  p.bias = static_cast<const __nv_bfloat16*>(bias);
+  p.bias_s = static_cast<const __nv_bfloat16*>(bias_s);
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.Nd = Nd;
+  p.n_routed = int32_t(N);
+  p.shared_rows = c.d_ff_shared > 0 ? int32_t(c.T) : 0;
+  p.num_kb = int32_t(K / BK);
+  p.status = g.status;
+  p.wait_limit_ns = g.wait_limit_ns;
+  const int64_t max_tiles = ceil_div(g.rows_max, BM) * (Nd / bn);
+  const int grid = int(max_tiles < g.num_sms ? max_tiles : g.num_sms);
+  if (grid <= 0) return cudaSuccess;
+  if (bn == 256) return launch_epi<256>(epi, mA, mB, mBs, p, grid, s);
+  if (bn == 128) return launch_epi<128>(epi, mA, mB, mBs, p, grid, s);
+  return launch_epi<64>(epi, mA, mB, mBs, p, grid, s);
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_ffn_bf16(const moe_config& c, const GroupedFfnArgs& g,
+                                    cudaStream_t s) {
+  if (g.rows_max == 0) return cudaSuccess;
+  const int epi1 = c.act == MOE_ACT_RELU ? EPI_BIAS_RELU : EPI_BIAS_GELU;
+  cudaError_t e = grouped_linear(c, g, g.Xp, g.w->W1, g.w->W1s, g.w->b1, g.w->b1s, g.H,
+                                 c.d_model, c.d_ff, epi1, s);
+  if (e != cudaSuccess) return e;
+  return grouped_linear(c, g, g.H, g.w->W2, g.w->W2s, g.w->b2, g.w->b2s, g.Yp, c.d_ff,
+                        c.d_model, EPI_BIAS, s);
+}
+
+}  // namespace moe

@@ -1,0 +1,65 @@
+// Internal launchers of libmoe's kernels (host functions, one per step).
+// The C ABI in api.cu validates arguments and calls these; each returns the
+// cudaError_t of its launches.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+// ---- router (router.cu) ------------------------------------------------------
+
+constexpr int kRouterTokensPerBlock = 32;   // tokens per softmax/top-k block
+
+cudaError_t launch_router_logits(const moe_config& c, const void* x, const void* W_g,
+                                 const void* b_g, float* logits, cudaStream_t s);
+cudaError_t launch_router_softmax_topk(const moe_config& c, const float* logits,
+                                       int32_t* topk_idx, float* topk_w,
+                                       float* prob_partials, cudaStream_t s);
+
+// ---- permutation (permute.cu) ------------------------------------------------
+
+constexpr int kPermuteTokensPerBlock = 128;  // tokens per histogram / rank block
+
+size_t permute_scratch_bytes(const moe_config& c);
+cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* topk_idx,
+                           int32_t* counts, int32_t* kept, int32_t* offsets,
+                           int32_t* row_token, int32_t* token_row, void* Xp, void* scratch,
+                           int64_t rows_max, cudaStream_t s);
+
+// ---- grouped expert FFN ----------------------------------------------------------
+
+struct GroupedFfnArgs {
+  const void* Xp;
+  const int32_t* offsets;   // [N + 2]
+  const int32_t* kept;      // [N]
+  const moe_weights* w;
+  void* H;
+  void* Yp;
+  int64_t rows_max;
+  int32_t* status;          // device status word
+  uint64_t wait_limit_ns;
+  int num_sms;
+};
+
+// fp32 path on CUDA cores (grouped_ffn_f32.cu)
+cudaError_t launch_grouped_ffn_f32(const moe_config& c, const GroupedFfnArgs& a, cudaStream_t s);
+// bf16 path on tcgen05 tensor cores (grouped_ffn_sm103.cu)
+cudaError_t launch_grouped_ffn_bf16(const moe_config& c, const GroupedFfnArgs& a, cudaStream_t s);
+
+// ---- combine and statistics (combine.cu) ----------------------------------------
+
+cudaError_t launch_combine(const moe_config& c, const void* Yp, const int32_t* token_row,
+                           const float* topk_w, const int32_t* offsets, void* y,
+                           cudaStream_t s);
+cudaError_t launch_load_stats(const moe_config& c, const float* prob_partials,
+                              const int32_t* counts, const int32_t* kept, float* mean_prob,
+                              float* balance, int32_t* dropped, cudaStream_t s);
+
+// ---- self test of the bounded wait (api.cu) ---------------------------------------
+cudaError_t launch_bounded_wait_selftest(uint64_t limit_ns, int32_t* status, cudaStream_t s);
+
+}  // namespace moe

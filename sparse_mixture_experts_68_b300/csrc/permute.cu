@@ -1,0 +1,217 @@
+// Permutation of the (token, slot) assignments into per-expert contiguous
+// groups with an optional capacity (matteuscruz.github.io "What is a Mixture
+// of Experts?", sections "Distributed training and inference" -- grouping
+// tokens by expert -- and "Load balancing" -- capacity factor x batch /
+// experts, overflow dropped; roadtointelligence.com "Mixture of Experts
+// (MoE)", "Keeping the experts busy").
+//
+// A stable counting sort in four launches, with no order-dependent atomics:
+//   hist  : per token-block, per expert assignment counts
+//   scan  : per expert, exclusive scan over blocks (the block's base rank),
+//           totals, capacity clamp, padded group offsets (one block)
+//   rank  : per token-block, one warp walks the block's assignments in
+//           token-major order; rank = base + earlier matches in the block
+//   copy  : one warp per grouped row copies the token's x row (16-byte
+//           vectors); the shared expert's group is x in token order
+#include "kernels.h"
+#include "common.cuh"
+
+namespace moe {
+
+namespace {
+
+struct PermuteScratch {
+  int32_t* block_counts;  // [nblk][N]
+  int32_t* block_base;    // [nblk][N]
+};
+
+inline int64_t permute_blocks(const moe_config& c) {
+  return ceil_div(c.T, kPermuteTokensPerBlock);
+}
+
+PermuteScratch carve(const moe_config& c, void* scratch) {
+  const int64_t n = permute_blocks(c) * c.n_experts;
+  PermuteScratch p;
+  p.block_counts = static_cast<int32_t*>(scratch);
+  p.block_base = p.block_counts + round_up(n, 64);
+  return p;
+}
+
+__global__ void __launch_bounds__(256)
+    permute_hist_kernel(const int32_t* __restrict__ topk_idx, int T, int k, int N,
+                        int32_t* __restrict__ block_counts) {
+  extern __shared__ int32_t cnt[];
+  for (int e = threadIdx.x; e < N; e += blockDim.x) cnt[e] = 0;
+  __syncthreads();
+  const int64_t a0 = int64_t(blockIdx.x) * kPermuteTokensPerBlock * k;
+  const int64_t a1 = min(int64_t(T) * k, a0 + int64_t(kPermuteTokensPerBlock) * k);
+  for (int64_t a = a0 + threadIdx.x; a < a1; a += blockDim.x) {
+    const int e = topk_idx[a];
+    if (e >= 0 && e < N) atomicAdd(&cnt[e], 1);  // out-of-range experts are not counted
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < N; e += blockDim.x)
+    block_counts[int64_t(blockIdx.x) * N + e] = cnt[e];
+}
+
+// One block of 1024 threads.  Thread e owns expert e (N <= 1024).
+__global__ void __launch_bounds__(1024)
+    permute_scan_kernel(const int32_t* __restrict__ block_counts, int nblk, int N, int T,
+                        int64_t capacity, int has_shared, int32_t* __restrict__ block_base,
+                        int32_t* __restrict__ counts, int32_t* __restrict__ kept,
+                        int32_t* __restrict__ offsets, int32_t* __restrict__ row_token) {
+  __shared__ int32_t warp_tot[32];
+  const int e = threadIdx.x;
+  int32_t total = 0, kp = 0, padded = 0;
+  if (e < N) {
+    for (int b = 0; b < nblk; ++b) {
+      block_base[int64_t(b) * N + e] = total;
+      total += block_counts[int64_t(b) * N + e];
+    }
+    kp = (capacity > 0 && int64_t(total) > capacity) ? int32_t(capacity) : total;
+    padded = int32_t(round_up(kp, kGroupAlign));
+    counts[e] = total;
+    kept[e] = kp;
+  }
+  // exclusive scan of padded over e (warp shuffles, then warp totals)
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int32_t incl = padded;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int32_t w = warp_tot[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t v = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += v;
+    }
+    warp_tot[lane] = w;                          // inclusive over warps
+  }
+  __syncthreads();
+  const int32_t excl = incl - padded + (warp > 0 ? warp_tot[warp - 1] : 0);
+  if (e < N) {
+    offsets[e] = excl;
+    for (int32_t r = excl + kp; r < excl + padded; ++r) row_token[r] = -1;   // padding rows
+  }
+  if (e == N - 1) {
+    const int32_t end = excl + padded;
+    offsets[N] = end;
+    offsets[N + 1] = end + (has_shared ? int32_t(round_up(T, kGroupAlign)) : 0);
+  }
+}
+
+// One warp per block walks the block's assignments in token-major order.
+__global__ void __launch_bounds__(32)
+    permute_rank_kernel(const int32_t* __restrict__ topk_idx, int T, int k, int N,
+                        int64_t capacity, const int32_t* __restrict__ block_base,
+                        const int32_t* __restrict__ offsets, int32_t* __restrict__ row_token,
+                        int32_t* __restrict__ token_row) {
+  extern __shared__ int32_t run[];              // next rank per expert
+  const int lane = threadIdx.x;
+  for (int e = lane; e < N; e += 32) run[e] = block_base[int64_t(blockIdx.x) * N + e];
+  __syncwarp();
+  const int64_t a0 = int64_t(blockIdx.x) * kPermuteTokensPerBlock * k;
+  const int64_t a1 = min(int64_t(T) * k, a0 + int64_t(kPermuteTokensPerBlock) * k);
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  for (int64_t base = a0; base < a1; base += 32) {
+    const int64_t a = base + lane;
+    const int e = a < a1 ? topk_idx[a] : -1;
+    const bool valid = e >= 0 && e < N;          // out-of-range experts: dropped
+    const int key = valid ? e : (0x40000000 | lane);     // invalid lanes match nobody
+    const uint32_t same = __match_any_sync(0xffffffffu, key);
+    int32_t rank = 0;
+    if (valid) rank = run[e] + __popc(same & lt_mask);
+    __syncwarp();
+    if (valid && (same & lt_mask) == 0) run[e] += __popc(same);   // group leader advances
+    __syncwarp();
+    if (a < a1) {
+      const bool keep = valid && (capacity <= 0 || rank < capacity);
+      int32_t row = -1;
+      if (keep) {
+        row = offsets[e] + rank;
+        row_token[row] = int32_t(a / k);
+      }
+      token_row[a] = row;
+    }
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+    permute_copy_kernel(const T* __restrict__ x, int64_t d, int Ttok, int N,
+                        const int32_t* __restrict__ offsets,
+                        const int32_t* __restrict__ row_token, T* __restrict__ Xp) {
+  const int lane = threadIdx.x & 31;
+  const int64_t routed_end = offsets[N], total = offsets[N + 1];
+  const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
+  constexpr int V = Vec16<T>::n;
+  for (int64_t r = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); r < total;
+       r += warps) {
+    int64_t t;
+    if (r < routed_end) {
+      t = row_token[r];
+    } else {
+      t = r - routed_end;
+      if (t >= Ttok) t = -1;
+    }
+    if (t < 0) continue;                          // padding row
+    const uint4* src = reinterpret_cast<const uint4*>(x + t * d);
+    uint4* dst = reinterpret_cast<uint4*>(Xp + r * d);
+    const int64_t nv = d / V;
+    for (int64_t i = lane; i < nv; i += 32) dst[i] = __ldg(src + i);
+  }
+}
+
+}  // namespace
+
+size_t permute_scratch_bytes(const moe_config& c) {
+  const int64_t n = permute_blocks(c) * c.n_experts;
+  return size_t(2 * round_up(n, 64)) * sizeof(int32_t);
+}
+
+cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* topk_idx,
+                           int32_t* counts, int32_t* kept, int32_t* offsets,
+                           int32_t* row_token, int32_t* token_row, void* Xp, void* scratch,
+                           int64_t rows_max, cudaStream_t s) {
+  const int N = int(c.n_experts), k = int(c.top_k), T = int(c.T);
+  const int nblk = int(permute_blocks(c));
+  PermuteScratch p = carve(c, scratch);
+  const size_t smemN = size_t(N) * sizeof(int32_t);
+  if (nblk > 0) {
+    permute_hist_kernel<<<nblk, 256, smemN, s>>>(topk_idx, T, k, N, p.block_counts);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  permute_scan_kernel<<<1, 1024, 0, s>>>(p.block_counts, nblk, N, T, c.capacity,
+                                         c.d_ff_shared > 0 ? 1 : 0, p.block_base, counts,
+                                         kept, offsets, row_token);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (nblk > 0) {
+    permute_rank_kernel<<<nblk, 32, smemN, s>>>(topk_idx, T, k, N, c.capacity, p.block_base,
+                                                offsets, row_token, token_row);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (rows_max > 0) {
+    const int64_t want = ceil_div(rows_max, 8);
+    const unsigned blocks = unsigned(want < 148 * 8 ? want : 148 * 8);
+    if (c.dtype == MOE_F32)
+      permute_copy_kernel<float><<<blocks, 256, 0, s>>>(
+          static_cast<const float*>(x), c.d_model, T, N, offsets, row_token,
+          static_cast<float*>(Xp));
+    else
+      permute_copy_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
+          static_cast<const __nv_bfloat16*>(x), c.d_model, T, N, offsets, row_token,
+          static_cast<__nv_bfloat16*>(Xp));
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+}  // namespace moe

@@ -1,0 +1,165 @@
+"""Comparison of the CUDA path with the CPU oracle on the same seeded inputs.
+
+Bars (per-token row error e_t = ||y_gpu[t] - y_ref[t]||_2 / max(||y_ref[t]||_2, 1e-6)):
+  fp32 layer: max_t e_t <= 1e-4;  bf16 layer: max_t e_t <= 2e-2.
+Top-k sets, counts, kept counts, group order and the dropped set are compared
+exactly.  A token whose oracle score gap between the k-th and (k+1)-th expert
+is below 1e-4 may pick another set; a token with a gap below 1e-4 inside its
+kept k may order them differently.  For the rest of the comparison the oracle
+is re-run with the GPU's choice for every token (the same choice as the
+oracle's own wherever it is not a near-tie).
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from oracle import moe_oracle as O
+
+TIE_EPS = 1e-4
+TOL = {0: 1e-4, 1: 2e-2}          # by dtype code: fp32, bf16
+GATE_RTOL = 1e-5
+MEAN_PROB_RTOL = 1e-5
+BALANCE_RTOL = 1e-4
+
+
+def to64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+class Experts:
+    """Per-expert float64 copies of a stacked device weight, fetched on use
+    (nothing is kept, so a layer with 15 GB of weights fits in host memory)."""
+
+    def __init__(self, t: torch.Tensor):
+        self.t = t
+
+    def __getitem__(self, e):
+        return to64(self.t[e])
+
+
+def near_tie_sets(z: np.ndarray, k: int):
+    """(set_tie, order_tie) boolean masks over tokens."""
+    N = z.shape[1]
+    s = -np.sort(-z, axis=1)
+    set_tie = np.zeros(z.shape[0], dtype=bool)
+    if k < N:
+        set_tie = (s[:, k - 1] - s[:, k]) < TIE_EPS
+    order_tie = np.zeros(z.shape[0], dtype=bool)
+    if k > 1:
+        order_tie = np.any(np.diff(-s[:, :k], axis=1) < TIE_EPS, axis=1)
+    return set_tie, order_tie
+
+
+def row_errors(y_gpu: np.ndarray, y_ref: np.ndarray) -> np.ndarray:
+    num = np.linalg.norm(y_gpu - y_ref, axis=1)
+    den = np.maximum(np.linalg.norm(y_ref, axis=1), 1e-6)
+    return num / den
+
+
+def check_routing(wl_dtype, cfg, tensors, out, z_ref, report):
+    """Top-k, gates: exact / near-tie rules above.  Returns the GPU top-k."""
+    k = cfg.top_k
+    idx_gpu = out.topk_idx.cpu().numpy().astype(np.int64)
+    w_gpu = out.topk_w.cpu().numpy().astype(np.float64)
+    idx_ref = O.topk_indices(z_ref, k)
+    set_tie, order_tie = near_tie_sets(z_ref, k)
+    same_set = np.all(np.sort(idx_gpu, 1) == np.sort(idx_ref, 1), axis=1)
+    bad_set = ~same_set & ~set_tie
+    assert not bad_set.any(), f"top-k set differs for tokens {np.nonzero(bad_set)[0][:10]}"
+    same_order = np.all(idx_gpu == idx_ref, axis=1)
+    bad_order = same_set & ~same_order & ~order_tie & ~set_tie
+    assert not bad_order.any(), f"top-k order differs for tokens {np.nonzero(bad_order)[0][:10]}"
+    # gates for the GPU's choice, by the oracle
+    p_ref = O.softmax(z_ref)
+    if cfg.renormalize:
+        w_ref = O.gates_softmax_of_topk(z_ref, idx_gpu)
+    else:
+        w_ref = O.gates_raw_probs(p_ref, idx_gpu)
+    np.testing.assert_allclose(w_gpu, w_ref, rtol=GATE_RTOL, atol=1e-7)
+    report["near_tie_tokens"] = int(set_tie.sum())
+    report["order_tie_tokens"] = int(order_tie.sum())
+    return idx_gpu
+
+
+def check_layer(wl, cfg, tensors, out, tokens=None, capacity=None, check_logits=True):
+    """Full comparison of one moe_forward against the oracle.  Returns a report."""
+    report = {}
+    x = to64(tensors["x"])
+    W_g, b_g = to64(tensors["W_g"]), to64(tensors["b_g"])
+    z_ref = O.router_logits(x, W_g, b_g)
+    if check_logits and out.logits is not None:
+        zg = out.logits.cpu().numpy().astype(np.float64)
+        err = np.abs(zg - z_ref).max() / max(np.abs(z_ref).max(), 1e-30)
+        report["logit_max_rel"] = float(err)
+        assert err < 1e-5, f"router scores differ: {err}"
+    idx_gpu = check_routing(cfg.dtype, cfg, tensors, out, z_ref, report)
+
+    cap = cfg.capacity if capacity is None else capacity
+    shared = None
+    if cfg.d_ff_shared:
+        shared = tuple(to64(tensors[n]) for n in ("W1s", "b1s", "W2s", "b2s"))
+    ref = O.moe_forward(x, W_g, b_g, Experts(tensors["W1"]), Experts(tensors["b1"]),
+                        Experts(tensors["W2"]), Experts(tensors["b2"]), k=cfg.top_k,
+                        act=cfg.act, capacity=cap, renormalize=bool(cfg.renormalize),
+                        shared=shared, round_hidden_bf16=(cfg.dtype == 1), tokens=tokens,
+                        idx_override=idx_gpu)
+    g = ref.grouping
+    # counts and drops: exact
+    np.testing.assert_array_equal(out.counts.cpu().numpy(), g.counts)
+    np.testing.assert_array_equal(out.kept.cpu().numpy(), g.kept)
+    assert int(out.dropped.cpu().item()) == g.dropped
+    # statistics
+    np.testing.assert_allclose(out.mean_prob.cpu().numpy(), ref.mean_prob,
+                               rtol=MEAN_PROB_RTOL, atol=1e-8)
+    bal = float(out.balance.cpu().item())
+    assert abs(bal - ref.balance) <= BALANCE_RTOL * abs(ref.balance) + 1e-9, \
+        f"balance {bal} vs {ref.balance}"
+    # output rows
+    y_gpu = out.y.float().cpu().numpy().astype(np.float64)
+    rows = ref.tokens
+    e = row_errors(y_gpu[rows], ref.y)
+    report["max_row_rel_l2"] = float(e.max()) if e.size else 0.0
+    report["tensor_rel_l2"] = float(np.linalg.norm(y_gpu[rows] - ref.y) /
+                                    max(np.linalg.norm(ref.y), 1e-30)) if e.size else 0.0
+    tol = TOL[cfg.dtype]
+    assert report["max_row_rel_l2"] <= tol, \
+        f"max row rel L2 {report['max_row_rel_l2']} > {tol} (token {rows[int(np.argmax(e))]})"
+    # fully dropped tokens without a shared expert: exactly zero
+    if not cfg.d_ff_shared:
+        dropped_all = ~g.keep.any(axis=1)
+        for t in rows[dropped_all[rows]]:
+            assert np.all(y_gpu[t] == 0.0), f"dropped token {t} is not zero"
+        report["fully_dropped_checked"] = int(dropped_all[rows].sum())
+    return report, ref
+
+
+def check_grouping(cfg, tensors_x, offsets, row_token, token_row, Xp, ref_grouping, T):
+    """Permutation layout: offsets padded per group, rows in token order, the
+    copied rows equal x, dropped slots -1."""
+    N, k = cfg.n_experts, cfg.top_k
+    off = offsets.cpu().numpy().astype(np.int64)
+    rt = row_token.cpu().numpy().astype(np.int64)
+    tr = token_row.cpu().numpy().astype(np.int64).reshape(T, k)
+    kept = ref_grouping.kept
+    for e in range(N):
+        assert off[e + 1] - off[e] == -(-kept[e] // 128) * 128
+        want = [t for t, _ in ref_grouping.groups[e]]
+        got = rt[off[e]: off[e] + kept[e]].tolist()
+        assert got == want, f"expert {e}: group order differs"
+        assert np.all(rt[off[e] + kept[e]: off[e + 1]] == -1)
+        for r, (t, j) in enumerate(ref_grouping.groups[e]):
+            assert tr[t, j] == off[e] + r
+    assert np.all(tr[~ref_grouping.keep] == -1)
+    shared_rows = -(-T // 128) * 128 if cfg.d_ff_shared else 0
+    assert off[N + 1] == off[N] + shared_rows
+    # copied rows: sample up to 64 kept rows and every shared row
+    x = tensors_x
+    xs = Xp[: off[N + 1]]
+    rows = [r for r in range(off[N]) if rt[r] >= 0]
+    rng = np.random.default_rng(0)
+    for r in rng.choice(rows, size=min(64, len(rows)), replace=False) if rows else []:
+        assert torch.equal(xs[int(r)], x[int(rt[r])])
+    if cfg.d_ff_shared:
+        assert torch.equal(xs[off[N]: off[N] + T], x)

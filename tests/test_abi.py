@@ -1,0 +1,114 @@
+"""The C-ABI library loads, exports every symbol include/moe.h declares, and
+rejects bad arguments on the host before touching a GPU (no compute calls)."""
+
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from sparse_mixture_experts_68_b300 import binding as B
+from sparse_mixture_experts_68_b300.workloads import WORKLOADS
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(moe_[a-z_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(B.LIB_PATH):
+        from sparse_mixture_experts_68_b300 import build
+        build.build()
+    return B.lib()
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = header_functions()
+    assert len(declared) >= 15
+    assert sorted(B.EXPORTS) == declared
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_version(lib):
+    assert lib.moe_version() == 1
+    assert B.status_string(B.MOE_OK) == "ok"
+    assert B.status_string(B.MOE_ERR_TIMEOUT) == "device wait timed out"
+    assert B.status_string(99) == "unknown status"
+
+
+def test_sizes(lib):
+    wl = WORKLOADS["c4_deepseek_v3"]
+    cfg = B.make_config(wl)
+    assert B.rows_max(cfg) == 4096 * 8 + 256 * 127 + 4096
+    assert B.router_blocks(cfg) == 4096 // 32
+    assert B.workspace_size(cfg) > B.rows_max(cfg) * (2 * 7168 + 2048) * 2
+    assert B.host_workspace_size(cfg) > B.workspace_size(cfg)
+    c1 = B.make_config(WORKLOADS["c1_page1_bf16"])
+    assert B.rows_max(c1) == 2048 * 2 + 8 * 127
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("top_k", 0, B.MOE_ERR_INVALID_ARG),
+    ("top_k", 9, B.MOE_ERR_INVALID_ARG),          # k > N
+    ("T", -1, B.MOE_ERR_INVALID_ARG),
+    ("dtype", 7, B.MOE_ERR_INVALID_ARG),
+    ("act", 5, B.MOE_ERR_INVALID_ARG),
+    ("reserved", 1, B.MOE_ERR_INVALID_ARG),
+    ("n_experts", 2048, B.MOE_ERR_UNSUPPORTED),
+    ("d_model", 100, B.MOE_ERR_UNSUPPORTED),       # bf16 needs d % 64 == 0
+    ("d_ff_shared", 64, B.MOE_ERR_UNSUPPORTED),    # shared width must equal d_ff
+])
+def test_invalid_configs_rejected_on_host(lib, field, value, status):
+    cfg = B.make_config(WORKLOADS["c1_page1_bf16"])
+    setattr(cfg, field, value)
+    if field == "n_experts":
+        cfg.top_k = 2
+    assert B.workspace_size(cfg) == 0
+    assert B.rows_max(cfg) == -1
+    w = B.MoeWeights()
+    o = B.MoeOutputs()
+    st = lib.moe_forward(C.byref(cfg), None, C.byref(w), C.byref(o), None, 0, None)
+    assert st == status
+
+
+def test_null_and_misaligned_pointers_rejected(lib):
+    cfg = B.make_config(WORKLOADS["c1_page1_bf16"])
+    w = B.MoeWeights()
+    o = B.MoeOutputs()
+    assert lib.moe_forward(C.byref(cfg), None, C.byref(w), C.byref(o), None, 0, None) == \
+        B.MOE_ERR_INVALID_ARG
+    # misaligned (never dereferenced: validation fails first)
+    fake = 0x1000
+    w = B.MoeWeights(*([fake] * 6 + [None] * 4))
+    w.W1 = fake + 2
+    assert lib.moe_grouped_ffn(C.byref(cfg), fake, fake, fake, C.byref(w), fake, fake, None) \
+        == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_permute(C.byref(cfg), fake, fake, fake, fake, fake, fake, fake, fake, fake,
+                           0, None) == B.MOE_ERR_WORKSPACE
+    assert lib.moe_router_topk(C.byref(cfg), fake, fake, fake + 4, fake, fake, fake, fake,
+                               None) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_combine(None, fake, fake, fake, fake, fake, None) == B.MOE_ERR_INVALID_ARG
+
+
+def test_workspace_too_small_rejected(lib):
+    cfg = B.make_config(WORKLOADS["c1_page1_bf16"])
+    fake = 0x10000
+    w = B.MoeWeights(*([fake] * 6 + [None] * 4))
+    o = B.MoeOutputs(*([fake] * 8 + [None]))
+    st = lib.moe_forward(C.byref(cfg), fake, C.byref(w), C.byref(o), fake, 1024, None)
+    assert st == B.MOE_ERR_WORKSPACE
+
+
+def test_wait_limit_setting(lib):
+    old = B.get_wait_limit_ns()
+    B.set_wait_limit_ns(12345)
+    assert B.get_wait_limit_ns() == 12345
+    B.set_wait_limit_ns(old)

@@ -1,0 +1,251 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Small shapes run in full and span several tiles with ragged tails; the five
+layer workloads run at their full sizes, with every token routed and grouped
+and the output rows compared on all tokens (small layers) or on a seeded
+sample of tokens (large layers)."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_oracle as O
+from sparse_mixture_experts_68_b300 import binding as B
+from sparse_mixture_experts_68_b300 import synth
+from sparse_mixture_experts_68_b300.workloads import (ACT_GELU_ERF, ACT_RELU, DT_BF16, DT_F32,
+                                                      WORKLOADS, Workload)
+
+from parity import check_grouping, check_layer, to64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    B.lib()
+    yield
+    torch.cuda.synchronize()
+    assert B.get_device_status() == B.MOE_OK
+
+
+def run_layer(wl, T=None, capacity=None, with_logits=True, seed=None):
+    t = synth.make_layer(wl if T is None else wl.with_tokens(T), device="cuda", seed=seed)
+    layer = B.MoeLayer(wl, t, T=T, capacity=capacity)
+    out = layer.forward(t["x"], with_logits=with_logits)
+    torch.cuda.synchronize()
+    return t, layer, out
+
+
+SMALL = [
+    # name, T, d, f, N, k, act, dtype, cap, shared
+    Workload("bf16_multi_mtile", T=1000, d_model=256, d_ff=512, n_experts=4, top_k=2,
+             act=ACT_GELU_ERF, dtype=DT_BF16, seed=11),
+    Workload("bf16_relu_cap_bn64", T=333, d_model=128, d_ff=192, n_experts=8, top_k=1,
+             act=ACT_RELU, dtype=DT_BF16, capacity_factor=0.7, seed=12),
+    Workload("bf16_shared_k4", T=200, d_model=64, d_ff=128, n_experts=16, top_k=4,
+             act=ACT_GELU_ERF, dtype=DT_BF16, d_ff_shared=128, seed=13),
+    Workload("bf16_bn128_N3", T=257, d_model=192, d_ff=384, n_experts=3, top_k=3,
+             act=ACT_GELU_ERF, dtype=DT_BF16, seed=14),
+    Workload("bf16_single_expert", T=130, d_model=64, d_ff=256, n_experts=1, top_k=1,
+             act=ACT_RELU, dtype=DT_BF16, seed=15),
+    Workload("bf16_many_experts", T=300, d_model=128, d_ff=128, n_experts=300, top_k=6,
+             act=ACT_GELU_ERF, dtype=DT_BF16, d_ff_shared=128, seed=16),
+    Workload("f32_small", T=190, d_model=72, d_ff=136, n_experts=5, top_k=2,
+             act=ACT_GELU_ERF, dtype=DT_F32, seed=17),
+    Workload("f32_cap_shared", T=150, d_model=64, d_ff=96, n_experts=6, top_k=2,
+             act=ACT_RELU, dtype=DT_F32, capacity_factor=1.0, d_ff_shared=96, seed=18),
+    Workload("bf16_noreorm", T=400, d_model=128, d_ff=256, n_experts=8, top_k=2,
+             act=ACT_GELU_ERF, dtype=DT_BF16, renormalize=0, seed=19),
+]
+
+
+@pytest.mark.parametrize("wl", SMALL, ids=[w.name for w in SMALL])
+def test_small_layers_full_parity(wl):
+    t, layer, out = run_layer(wl)
+    report, ref = check_layer(wl, layer.cfg, t, out)
+    assert report["max_row_rel_l2"] <= (1e-4 if wl.dtype == DT_F32 else 2e-2)
+
+
+def test_stages_through_the_abi():
+    """Each step called on its own: router, permute (layout checked), grouped
+    FFN (hidden rows checked), combine, stats."""
+    wl = Workload("stages", T=700, d_model=128, d_ff=256, n_experts=6, top_k=2,
+                  act=ACT_GELU_ERF, dtype=DT_BF16, capacity_factor=1.1, d_ff_shared=256,
+                  seed=21)
+    t = synth.make_layer(wl, device="cuda")
+    cfg = B.make_config(wl)
+    dev = "cuda"
+    T, k, N = wl.T, wl.top_k, wl.n_experts
+    rows = B.rows_max(cfg)
+    logits = torch.empty((T, N), dtype=torch.float32, device=dev)
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    pp = torch.empty((B.router_blocks(cfg), N), dtype=torch.float32, device=dev)
+    B.router_topk(cfg, t["x"], t["W_g"], t["b_g"], logits, idx, w, pp)
+    counts = torch.empty(N, dtype=torch.int32, device=dev)
+    kept = torch.empty(N, dtype=torch.int32, device=dev)
+    offsets = torch.empty(N + 2, dtype=torch.int32, device=dev)
+    row_token = torch.empty(rows, dtype=torch.int32, device=dev)
+    token_row = torch.empty((T, k), dtype=torch.int32, device=dev)
+    Xp = torch.empty((rows, wl.d_model), dtype=torch.bfloat16, device=dev)
+    scratch = torch.empty(B.permute_scratch_size(cfg), dtype=torch.uint8, device=dev)
+    B.permute(cfg, t["x"], idx, counts, kept, offsets, row_token, token_row, Xp, scratch)
+    H = torch.empty((rows, wl.d_ff), dtype=torch.bfloat16, device=dev)
+    Yp = torch.empty((rows, wl.d_model), dtype=torch.bfloat16, device=dev)
+    weights = B.make_weights(t)
+    B.grouped_ffn(cfg, Xp, offsets, kept, weights, H, Yp)
+    y = torch.empty((T, wl.d_model), dtype=torch.bfloat16, device=dev)
+    B.combine(cfg, Yp, token_row, w, offsets, y)
+    mean_prob = torch.empty(N, dtype=torch.float32, device=dev)
+    balance = torch.empty(1, dtype=torch.float32, device=dev)
+    dropped = torch.empty(1, dtype=torch.int32, device=dev)
+    B.load_stats(cfg, pp, counts, kept, mean_prob, balance, dropped)
+    torch.cuda.synchronize()
+
+    out = B.Outputs(y, idx, w, counts, kept, dropped, mean_prob, balance, logits)
+    report, ref = check_layer(wl, cfg, t, out)
+    assert ref.grouping.dropped > 0                   # the capacity bites
+    check_grouping(cfg, t["x"], offsets, row_token, token_row, Xp, ref.grouping, T)
+    # hidden rows of every group against the oracle's first Linear + GELU
+    off = offsets.cpu().numpy()
+    x64 = to64(t["x"])
+    for e in range(N + 1):
+        n_live = int(kept[e].item()) if e < N else T
+        if n_live == 0:
+            continue
+        r0 = int(off[e])
+        toks = row_token[r0: r0 + n_live].cpu().numpy() if e < N else np.arange(T)
+        W1 = to64(t["W1"][e] if e < N else t["W1s"])
+        b1 = to64(t["b1"][e] if e < N else t["b1s"])
+        h_ref = O.activation(x64[toks] @ W1.T + b1, wl.act)
+        h_gpu = H[r0: r0 + n_live].double().cpu().numpy()
+        err = np.linalg.norm(h_gpu - h_ref) / np.linalg.norm(h_ref)
+        assert err < 5e-3, (e, err)
+
+
+def test_edge_cases_tokens_0_and_1():
+    wl = Workload("edge", T=1, d_model=64, d_ff=64, n_experts=4, top_k=2, dtype=DT_BF16,
+                  seed=31)
+    t, layer, out = run_layer(wl)
+    check_layer(wl, layer.cfg, t, out)
+    t0, layer0, out0 = run_layer(wl, T=0)
+    assert out0.counts.cpu().sum().item() == 0
+    assert out0.dropped.cpu().item() == 0
+    assert out0.balance.cpu().item() == 0.0
+
+
+def test_capacity_one_and_all_tokens_to_one_expert():
+    wl = Workload("collapse", T=260, d_model=64, d_ff=128, n_experts=4, top_k=1,
+                  dtype=DT_BF16, seed=32)
+    t = synth.make_layer(wl, device="cuda")
+    t["W_g"].zero_()
+    t["b_g"].copy_(torch.tensor([3.0, 0.0, -1.0, -2.0], device="cuda").to(torch.bfloat16))
+    for cap in (1, 3, 0):
+        layer = B.MoeLayer(wl, t, capacity=cap)
+        out = layer.forward(t["x"], with_logits=True)
+        torch.cuda.synchronize()
+        report, ref = check_layer(wl, layer.cfg, t, out, capacity=cap)
+        kept0 = ref.grouping.kept[0]
+        assert kept0 == (cap if cap > 0 else 260)
+        # balance of a collapsed router: every token puts the same p on expert 0
+        assert ref.grouping.counts.tolist() == [260, 0, 0, 0]
+
+
+def test_deterministic_bitwise():
+    wl = Workload("det", T=513, d_model=256, d_ff=512, n_experts=8, top_k=2,
+                  dtype=DT_BF16, capacity_factor=1.2, seed=33)
+    t, layer, out1 = run_layer(wl)
+    out2 = layer.forward(t["x"], with_logits=True)
+    torch.cuda.synchronize()
+    for a, b in [(out1.y, out2.y), (out1.topk_idx, out2.topk_idx), (out1.topk_w, out2.topk_w),
+                 (out1.mean_prob, out2.mean_prob), (out1.balance, out2.balance)]:
+        assert torch.equal(a, b)
+
+
+def test_forward_host_matches_device_path():
+    wl = Workload("host", T=300, d_model=128, d_ff=256, n_experts=8, top_k=2,
+                  dtype=DT_BF16, seed=34)
+    t, layer, out = run_layer(wl)
+    cfg = layer.cfg
+    ws = torch.empty(B.host_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    xh = t["x"].cpu().pin_memory()
+    oh = B.alloc_outputs(cfg, "cpu", with_logits=True, pin_memory=True)
+    B.forward_host(cfg, xh, layer.weights, oh, ws)
+    assert torch.equal(oh.y, out.y.cpu())
+    assert torch.equal(oh.topk_idx, out.topk_idx.cpu())
+    assert torch.equal(oh.counts, out.counts.cpu())
+    assert torch.equal(oh.logits, out.logits.cpu())
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    B.selftest_bounded_wait(2_000_000)            # 2 ms; nothing ever arrives
+    assert B.get_device_status() == B.MOE_ERR_TIMEOUT
+    assert B.get_device_status() == B.MOE_OK      # read clears it
+    wl = Workload("after", T=64, d_model=64, d_ff=64, n_experts=4, top_k=2, seed=35)
+    t, layer, out = run_layer(wl)
+    check_layer(wl, layer.cfg, t, out)
+
+
+# ---- the five layer workloads at full size ----------------------------------------
+
+def sample_tokens(T, n, seed, must=()):
+    rng = np.random.default_rng(seed)
+    pick = set(must) | {0, T - 1}
+    pick |= set(rng.choice(T, size=min(n, T), replace=False).tolist())
+    return np.array(sorted(pick))
+
+
+def test_workload_c0_pr1_fp32_full():
+    wl = WORKLOADS["c0_pr1_fp32"]
+    t, layer, out = run_layer(wl)
+    report, _ = check_layer(wl, layer.cfg, t, out)
+    assert report["max_row_rel_l2"] <= 1e-4
+
+
+def test_workload_c1_page1_bf16_full():
+    wl = WORKLOADS["c1_page1_bf16"]
+    t, layer, out = run_layer(wl)
+    check_layer(wl, layer.cfg, t, out)
+
+
+def test_workload_c2_switch_top1_capacity():
+    wl = WORKLOADS["c2_switch_top1"]
+    assert O.expert_capacity(wl.capacity_factor, wl.T, wl.n_experts) == wl.capacity == 160
+    t, layer, out = run_layer(wl)
+    kept = out.kept.cpu().numpy()
+    grp = O.group_by_expert(out.topk_idx.cpu().numpy(), wl.n_experts, 160)
+    dropped_tokens = np.nonzero(~grp.keep[:, 0])[0]
+    toks = sample_tokens(wl.T, 384, 2, must=dropped_tokens[:64].tolist())
+    report, ref = check_layer(wl, layer.cfg, t, out, tokens=toks)
+    assert ref.grouping.dropped > 0 and kept.max() == 160
+    assert report["fully_dropped_checked"] > 0
+
+
+def test_workload_c2_raw_gates_variant():
+    wl = WORKLOADS["c2_switch_top1"]
+    from dataclasses import replace
+    wl = replace(wl, renormalize=0)
+    t, layer, out = run_layer(wl, T=2048)
+    check_layer(wl, layer.cfg, t, out, tokens=sample_tokens(2048, 128, 3))
+
+
+def test_workload_c3_mixtral_decode_full():
+    wl = WORKLOADS["c3_mixtral_decode"]
+    t, layer, out = run_layer(wl)
+    check_layer(wl, layer.cfg, t, out)
+
+
+def test_workload_c3_mixtral_prefill_sampled():
+    wl = WORKLOADS["c3_mixtral_prefill"]
+    t, layer, out = run_layer(wl)
+    check_layer(wl, layer.cfg, t, out, tokens=sample_tokens(wl.T, 24, 4))
+
+
+def test_workload_c4_deepseek_v3_sampled():
+    wl = WORKLOADS["c4_deepseek_v3"]
+    t, layer, out = run_layer(wl)
+    report, _ = check_layer(wl, layer.cfg, t, out, tokens=sample_tokens(wl.T, 10, 5))
+    del t, layer, out
+    torch.cuda.empty_cache()
