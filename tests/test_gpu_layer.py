@@ -201,13 +201,15 @@ def test_workload_c0_pr1_fp32_full():
     wl = WORKLOADS["c0_pr1_fp32"]
     t, layer, out = run_layer(wl)
     report, _ = check_layer(wl, layer.cfg, t, out)
+    print("parity", wl.name, report)
     assert report["max_row_rel_l2"] <= 1e-4
 
 
 def test_workload_c1_page1_bf16_full():
     wl = WORKLOADS["c1_page1_bf16"]
     t, layer, out = run_layer(wl)
-    check_layer(wl, layer.cfg, t, out)
+    report, _ = check_layer(wl, layer.cfg, t, out)
+    print("parity", wl.name, report)
 
 
 def test_workload_c2_switch_top1_capacity():
@@ -219,6 +221,7 @@ def test_workload_c2_switch_top1_capacity():
     dropped_tokens = np.nonzero(~grp.keep[:, 0])[0]
     toks = sample_tokens(wl.T, 384, 2, must=dropped_tokens[:64].tolist())
     report, ref = check_layer(wl, layer.cfg, t, out, tokens=toks)
+    print("parity", wl.name, report, "dropped", ref.grouping.dropped)
     assert ref.grouping.dropped > 0 and kept.max() == 160
     assert report["fully_dropped_checked"] > 0
 
@@ -234,18 +237,21 @@ def test_workload_c2_raw_gates_variant():
 def test_workload_c3_mixtral_decode_full():
     wl = WORKLOADS["c3_mixtral_decode"]
     t, layer, out = run_layer(wl)
-    check_layer(wl, layer.cfg, t, out)
+    report, _ = check_layer(wl, layer.cfg, t, out)
+    print("parity", wl.name, report)
 
 
 def test_workload_c3_mixtral_prefill_sampled():
     wl = WORKLOADS["c3_mixtral_prefill"]
     t, layer, out = run_layer(wl)
-    check_layer(wl, layer.cfg, t, out, tokens=sample_tokens(wl.T, 24, 4))
+    report, _ = check_layer(wl, layer.cfg, t, out, tokens=sample_tokens(wl.T, 24, 4))
+    print("parity", wl.name, report)
 
 
 def test_workload_c4_deepseek_v3_sampled():
     wl = WORKLOADS["c4_deepseek_v3"]
     t, layer, out = run_layer(wl)
     report, _ = check_layer(wl, layer.cfg, t, out, tokens=sample_tokens(wl.T, 10, 5))
+    print("parity", wl.name, report)
     del t, layer, out
     torch.cuda.empty_cache()
