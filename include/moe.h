@@ -47,7 +47,8 @@
  *     and return; moe_get_device_status reports it.
  *   - All kernels are deterministic: the same inputs give bit-identical
  *     outputs (no order-dependent atomics).
- *   - The library's only global state is that status word and the wait limit.
+ *   - The library's only global state is that status word, the wait limit
+ *     and the fixed scratch array of moe_permute_noalloc.
  */
 #ifndef MOE_H
 #define MOE_H
@@ -157,6 +158,32 @@ moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk
                        int32_t* counts, int32_t* kept, int32_t* offsets,
                        int32_t* row_token, int32_t* token_row, void* Xp,
                        void* scratch, size_t scratch_bytes, void* stream);
+
+/* moe_permute for callers that cannot allocate device memory -- for example a
+ * plugin whose host framework owns every byte of device memory and forbids
+ * allocation in its execution path, or a latency-bound loop where a
+ * cudaMalloc would synchronise the device.  The pages have no counterpart:
+ * this is an interface convenience, not a step of the layer.
+ *
+ * Same arguments and results as moe_permute, minus the scratch: the
+ * per-block histograms and bases live in a fixed array inside the library,
+ * MOE_PERMUTE_STATIC_SCRATCH_INTS int32 (1 MiB) large, which every GPU that
+ * loads the library holds until the process exits.  Layers whose scratch
+ * need (moe_permute_scratch_size) exceeds it return MOE_ERR_WORKSPACE and
+ * launch nothing; with 128 tokens per block that is ceil(T/128) * N > 131072
+ * (for example T = 16384 with N = 1024 still fits).
+ *
+ * The array is shared by every call on a device: two calls whose kernels
+ * overlap on the GPU (different streams, no ordering) race on it, so order
+ * them on one stream or with events.  Nothing in it needs clearing between
+ * calls: every entry is written before it is read.  The first call on each
+ * device looks up the array's device address (cudaGetSymbolAddress); make that
+ * first call before any stream capture.  No memory is allocated by this call. */
+#define MOE_PERMUTE_STATIC_SCRATCH_INTS (1 << 18)
+moe_status moe_permute_noalloc(const moe_config* cfg, const void* x,
+                               const int32_t* topk_idx, int32_t* counts, int32_t* kept,
+                               int32_t* offsets, int32_t* row_token, int32_t* token_row,
+                               void* Xp, void* stream);
 
 /* Run every expert on its group (botmartz.com "Expert Routing": Linear ->
  * GELU -> Linear; codingnowai.in "Code": Linear -> ReLU -> Linear):

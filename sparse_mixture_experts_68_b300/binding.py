@@ -29,8 +29,9 @@ EXPORTS = [
     "moe_router_topk", "moe_permute", "moe_grouped_ffn", "moe_combine", "moe_load_stats",
     "moe_forward", "moe_host_workspace_size", "moe_forward_host", "moe_get_device_status",
     "moe_set_wait_limit_ns", "moe_get_wait_limit_ns", "moe_selftest_bounded_wait",
-    "moe_status_string", "moe_version",
+    "moe_status_string", "moe_version", "moe_permute_noalloc",
 ]
+PERMUTE_STATIC_SCRATCH_INTS = 1 << 18
 
 
 class MoeError(RuntimeError):
@@ -79,6 +80,7 @@ def lib() -> C.CDLL:
         "moe_host_workspace_size": (C.c_size_t, [CP]),
         "moe_router_topk": (C.c_int32, [CP, P, P, P, P, P, P, P, P]),
         "moe_permute": (C.c_int32, [CP, P, P, P, P, P, P, P, P, P, C.c_size_t, P]),
+        "moe_permute_noalloc": (C.c_int32, [CP, P, P, P, P, P, P, P, P, P]),
         "moe_grouped_ffn": (C.c_int32, [CP, P, P, P, C.POINTER(MoeWeights), P, P, P]),
         "moe_combine": (C.c_int32, [CP, P, P, P, P, P, P]),
         "moe_load_stats": (C.c_int32, [CP, P, P, P, P, P, P, P]),
@@ -166,6 +168,15 @@ def permute(cfg, x, topk_idx, counts, kept, offsets, row_token, token_row, Xp, s
                              _ptr(offsets), _ptr(row_token), _ptr(token_row), _ptr(Xp),
                              _ptr(scratch), scratch.numel() * scratch.element_size(),
                              _stream(stream)), "moe_permute")
+
+
+def permute_noalloc(cfg, x, topk_idx, counts, kept, offsets, row_token, token_row, Xp,
+                    stream=None):
+    """moe_permute with the library's fixed scratch array (no scratch argument)."""
+    _check(lib().moe_permute_noalloc(C.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(counts),
+                                     _ptr(kept), _ptr(offsets), _ptr(row_token),
+                                     _ptr(token_row), _ptr(Xp), _stream(stream)),
+           "moe_permute_noalloc")
 
 
 def grouped_ffn(cfg, Xp, offsets, kept, weights: MoeWeights, H, Yp, stream=None):

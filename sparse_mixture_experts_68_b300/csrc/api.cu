@@ -143,6 +143,9 @@ __global__ void bounded_wait_selftest_kernel(uint64_t limit_ns, int32_t* status)
 
 }  // namespace
 
+moe_status validate_config(const moe_config* cfg) { return check_config(cfg); }
+int64_t rows_max_for(const moe_config& c) { return rows_max_of(c); }
+
 cudaError_t launch_bounded_wait_selftest(uint64_t limit_ns, int32_t* status, cudaStream_t s) {
   bounded_wait_selftest_kernel<<<1, 32, 0, s>>>(limit_ns, status);
   return cudaGetLastError();

@@ -59,6 +59,10 @@ cudaError_t launch_load_stats(const moe_config& c, const float* prob_partials,
                               const int32_t* counts, const int32_t* kept, float* mean_prob,
                               float* balance, int32_t* dropped, cudaStream_t s);
 
+// ---- host-side checks shared with entry points outside api.cu -------------------------
+moe_status validate_config(const moe_config* cfg);   // as every moe_* entry checks cfg
+int64_t rows_max_for(const moe_config& c);             // moe_rows_max without the check
+
 // ---- self test of the bounded wait (api.cu) ---------------------------------------
 cudaError_t launch_bounded_wait_selftest(uint64_t limit_ns, int32_t* status, cudaStream_t s);
 

@@ -13,6 +13,8 @@
 //           token-major order; rank = base + earlier matches in the block
 //   copy  : one warp per grouped row copies the token's x row (16-byte
 //           vectors); the shared expert's group is x in token order
+#include <mutex>
+
 #include "kernels.h"
 #include "common.cuh"
 
@@ -215,3 +217,60 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* to
 }
 
 }  // namespace moe
+
+// ---- moe_permute_noalloc: the same step with its scratch in a fixed array ---------------
+//
+// For callers that cannot allocate device memory.  The per-block histograms
+// and bases live in this file-scope array (1 MiB on every GPU that loads the
+// library).  Host code must not pass the array's name to a kernel -- on the
+// host it is only a stand-in symbol -- so each device's address is looked up
+// once with cudaGetSymbolAddress, with that device current, and passed in.
+
+static __device__ __align__(256) int32_t g_permute_static_scratch[MOE_PERMUTE_STATIC_SCRATCH_INTS];
+
+namespace moe {
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_scratch_mu;
+void* g_static_scratch_addr[kMaxDevices] = {};
+
+// Device address of the array for the current device (looked up on first use).
+cudaError_t static_scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_static_scratch_mu);
+  if (g_static_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_permute_static_scratch);
+    if (e != cudaSuccess) return e;
+    g_static_scratch_addr[dev] = p;
+  }
+  *out = g_static_scratch_addr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status moe_permute_noalloc(const moe_config* cfg, const void* x,
+                                          const int32_t* topk_idx, int32_t* counts,
+                                          int32_t* kept, int32_t* offsets, int32_t* row_token,
+                                          int32_t* token_row, void* Xp, void* stream) {
+  using namespace moe;
+  moe_status st = validate_config(cfg);
+  if (st != MOE_OK) return st;
+  const void* ps[] = {x, topk_idx, counts, kept, offsets, row_token, token_row, Xp};
+  for (const void* q : ps)
+    if (!q || (reinterpret_cast<uintptr_t>(q) & 15u) != 0) return MOE_ERR_INVALID_ARG;
+  if (permute_scratch_bytes(*cfg) > size_t(MOE_PERMUTE_STATIC_SCRATCH_INTS) * sizeof(int32_t))
+    return MOE_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  if (static_scratch_address(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
+  const cudaError_t e = launch_permute(*cfg, x, topk_idx, counts, kept, offsets, row_token,
+                                       token_row, Xp, scratch, rows_max_for(*cfg),
+                                       static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
