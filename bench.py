@@ -24,7 +24,6 @@ import argparse
 import json
 import os
 import statistics
-import subprocess
 import sys
 import time
 
@@ -64,52 +63,76 @@ def peaks():
 # clocks during the timed region
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """Polls the GPU's SM clock and clock-event reasons (read-only NVML queries,
+    the same counters nvidia-smi prints) every ~2 ms on a thread; keeps only the
+    samples taken between mark_start() and mark_end()."""
 
     def __init__(self, gpu_index: int):
+        import threading
         self.gpu = gpu_index
-        self.proc = None
-        self.path = os.path.join("/tmp", f"moe_bench_clocks_{os.getpid()}.csv")
+        self.samples = []
+        self.window = [None, None]
+        self.stop_evt = threading.Event()
+        self.thread = None
+        self.err = None
+
+    # clock-event reason bits of NVML's nvmlClocksEventReason* constants
+    MASKS = {"hw_slowdown": 0x8, "hw_thermal_slowdown": 0x40, "sw_thermal_slowdown": 0x20,
+             "sw_power_cap": 0x4}
+
+    def _run(self):
+        # the driver's NVML library through ctypes: read-only queries
+        import ctypes as C
+        try:
+            nv = C.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise RuntimeError("nvmlInit_v2 failed")
+            h = C.c_void_p()
+            if nv.nvmlDeviceGetHandleByIndex_v2(C.c_uint(self.gpu), C.byref(h)) != 0:
+                raise RuntimeError("nvmlDeviceGetHandleByIndex_v2 failed")
+            v = C.c_uint()
+            nv.nvmlDeviceGetMaxClockInfo(h, C.c_int(1), C.byref(v))   # 1: SM clock
+            self.max_mhz = int(v.value)
+            reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            r = C.c_ulonglong()
+            while not self.stop_evt.is_set():
+                t = time.time()
+                nv.nvmlDeviceGetClockInfo(h, C.c_int(1), C.byref(v))
+                reasons_fn(h, C.byref(r))
+                self.samples.append((t, int(v.value),
+                                     [k for k, m in self.MASKS.items() if r.value & m]))
+                time.sleep(0.002)
+            nv.nvmlShutdown()
+        except Exception as e:  # no NVML: report it, do not fail the run
+            self.err = repr(e)
 
     def start(self):
-        try:
-            self.out = open(self.path, "w")
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=self.out, stderr=subprocess.DEVNULL)
-        except (OSError, FileNotFoundError):
-            self.proc = None
+        import threading
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        self.thread.start()
+
+    def mark_start(self):
+        self.window[0] = time.time()
+
+    def mark_end(self):
+        self.window[1] = time.time()
 
     def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        self.out.close()
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                smax.append(float(f[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        os.unlink(self.path)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        self.stop_evt.set()
+        if self.thread:
+            self.thread.join(timeout=5)
+        if self.err:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [f"nvml: {self.err}"]}
+        t0, t1 = self.window
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        if not inside and self.samples:   # window shorter than one poll: nearest sample
+            mid = 0.5 * (t0 + t1)
+            inside = [min(self.samples, key=lambda s: abs(s[0] - mid))]
+        reasons = sorted({r for s in inside for r in s[2]})
+        return {"sm_mhz": statistics.median(s[1] for s in inside) if inside else None,
+                "sm_max_mhz": getattr(self, "max_mhz", None), "reasons": reasons,
+                "samples": len(inside), "source": "NVML, polled every ~2 ms"}
 
 
 # ---------------------------------------------------------------------------------------
@@ -192,6 +215,9 @@ def run_reference(args, wl, rank, world):
 # ---------------------------------------------------------------------------------------
 # the CUDA path
 
+STAGES = ("router_topk", "permute", "ffn_linear1", "ffn_linear2", "combine", "load_stats")
+
+
 def run_ours(args, wl, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -203,34 +229,58 @@ def run_ours(args, wl, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     tensors = synth.make_layer(wl, device=dev)
-    layer = B.StagedLayer(wl, tensors, device=dev)
+    layer = B.MoeLayer(wl, tensors, device=dev)
     out = B.alloc_outputs(layer.cfg, dev)
     x = tensors["x"]
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
-    stream = torch.cuda.current_stream(dev)
 
-    for _ in range(max(args.warmup, 3)):
-        flush.fill_(1)
-        layer.run(x, out)
+    # the layer as one CUDA graph: moe_forward_profiled with seven timing
+    # events recorded as graph nodes at the kernel boundaries
+    stream = torch.cuda.Stream(dev)
+    events = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
+    with torch.cuda.stream(stream):
+        for ev in events:
+            ev.record(stream)               # creates the underlying CUDA events
+        for _ in range(3):                  # warm: module loading, tensor-map setup
+            B.forward_profiled(layer.cfg, x, layer.weights, out, layer.workspace, events,
+                               stream)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        B.forward_profiled(layer.cfg, x, layer.weights, out, layer.workspace, events, stream)
+    torch.cuda.synchronize(dev)
+
+    def step(i):
+        with torch.cuda.stream(stream):
+            flush.fill_(i)                  # L2 flush, outside the timed events
+            graph.replay()
+
+    for i in range(max(args.warmup, 3)):
+        step(i)
     torch.cuda.synchronize(dev)
     assert B.get_device_status() == B.MOE_OK
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
     clocks = ClockSampler(local_rank)
     clocks.start()
+    time.sleep(0.05)
+    for i in range(3):
+        step(i)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
+    clocks.mark_start()
+    stage_ms, step_ms = [], []
     for i in range(K):
-        flush.fill_(i)
-        layer.run(x, out, events=ev[i], stream=stream)
+        step(i)
+        stream.synchronize()                # read this replay's events before the next
+        stage_ms.append([events[s].elapsed_time(events[s + 1]) for s in range(6)])
+        step_ms.append(events[0].elapsed_time(events[6]))
     torch.cuda.synchronize(dev)
+    clocks.mark_end()
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
-    stage_ms = [[ev[i][s].elapsed_time(ev[i][s + 1]) for s in range(5)] for i in range(K)]
-    step_ms = [ev[i][0].elapsed_time(ev[i][5]) for i in range(K)]
     total_ms = sum(step_ms)
     if world > 1:
         t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
@@ -242,36 +292,42 @@ def run_ours(args, wl, rank, world, local_rank):
     n_kept_experts = int((out.kept > 0).sum().item())
     T = layer.cfg.T
     value = T * K * world / (total_ms * 1e-3)
+    mean_stage = {n: statistics.mean(s[i] for s in stage_ms) for i, n in enumerate(STAGES)}
 
-    # roofline of the dominant kernel (the grouped FFN: two launches of the
-    # tcgen05 grouped GEMM per step)
+    # roofline of the dominant kernel: the tcgen05 grouped GEMM, launched once
+    # per Linear (two launches per step)
     pk = peaks()
     es = wl.elem_bytes
-    ffn_ms = statistics.mean(s[2] for s in stage_ms)
-    ffn_flop = 4.0 * wl.d_model * wl.d_ff * kept_rows + 4.0 * wl.d_model * wl.d_ff_shared * T
-    ffn_weight_bytes = (n_kept_experts * 2 * wl.d_model * wl.d_ff +
-                        (2 * wl.d_model * wl.d_ff_shared if wl.d_ff_shared else 0)) * es
-    ffn_act_bytes = (kept_rows + (T if wl.d_ff_shared else 0)) * (
-        2 * wl.d_model + 2 * wl.d_ff) * es
-    ffn_bytes = ffn_weight_bytes + ffn_act_bytes
-    intensity = ffn_flop / ffn_bytes
-    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    rows_sh = T if wl.d_ff_shared else 0
+    f1 = 2.0 * wl.d_model * wl.d_ff * (kept_rows + rows_sh)        # per Linear
+    wbytes = (n_kept_experts + (1 if wl.d_ff_shared else 0)) * wl.d_model * wl.d_ff * es
+    b1 = wbytes + (kept_rows + rows_sh) * (wl.d_model + wl.d_ff) * es   # Linear 1 bytes
+    b2 = wbytes + (kept_rows + rows_sh) * (wl.d_ff + wl.d_model) * es   # Linear 2 bytes
+    ffn_ms = mean_stage["ffn_linear1"] + mean_stage["ffn_linear2"]
     launches = 2
-    if intensity >= ridge:
-        achieved = ffn_flop / launches / (ffn_ms / launches * 1e-3) / 1e12
+    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    if (2 * f1) / (b1 + b2) >= ridge:
+        achieved = 2 * f1 / launches / (ffn_ms / launches * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
                 "unit": "TFLOP/s"}
     else:
-        achieved = ffn_bytes / launches / (ffn_ms / launches * 1e-3) / 1e9
+        achieved = (b1 + b2) / launches / (ffn_ms / launches * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = None
-    roof["kernel"] = "tc_grouped_gemm_kernel (grouped FFN, 2 launches/step)"
+    roof["kernel"] = "tc_grouped_gemm_kernel (two launches per step: Linear 1, Linear 2)"
     roof["peak_source"] = pk["source"] + " (burst)"
+    roof["per_launch"] = {
+        "linear1": {"ms": mean_stage["ffn_linear1"], "flop": f1, "bytes": b1,
+                    "tflops": f1 / (mean_stage["ffn_linear1"] * 1e-3) / 1e12,
+                    "gbs": b1 / (mean_stage["ffn_linear1"] * 1e-3) / 1e9},
+        "linear2": {"ms": mean_stage["ffn_linear2"], "flop": f1, "bytes": b2,
+                    "tflops": f1 / (mean_stage["ffn_linear2"] * 1e-3) / 1e12,
+                    "gbs": b2 / (mean_stage["ffn_linear2"] * 1e-3) / 1e9}}
 
     # whole-layer roofline time against the same peaks
     layer_flop = flops(wl, kept_rows)
-    layer_bytes = ffn_weight_bytes + wl.n_experts * wl.d_model * es + 2 * T * wl.d_model * es
+    layer_bytes = wbytes + wl.n_experts * wl.d_model * es + 2 * T * wl.d_model * es
     floor_ms = max(layer_flop / (pk["bf16_tflops"] * 1e12),
                    layer_bytes / (pk["hbm_gbs"] * 1e9)) * 1e3
 
@@ -282,14 +338,14 @@ def run_ours(args, wl, rank, world, local_rank):
         "dtype": "bf16" if wl.dtype == 1 else "f32", "data": "synthetic",
         "config": {"workload": wl.name, "description": wl.description, "T": T,
                    "parallelism": f"replicas{world}" if world > 1 else "single",
-                   "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write)"},
+                   "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write)",
+                   "launch": "moe_forward_profiled captured once as a CUDA graph, replayed"},
         "tflops": layer_flop / (total_ms / K * 1e-3) / 1e12,
         "layer_roofline_floor_ms": floor_ms,
         "layer_roofline_frac": floor_ms / (total_ms / K),
-        "stage_ms": {n: statistics.mean(s[i] for s in stage_ms)
-                     for i, n in enumerate(B.StagedLayer.STAGES)},
+        "stage_ms": mean_stage,
         "roofline": roof,
-        "gpu_launches": B.StagedLayer.LAUNCHES_PER_STEP * K,
+        "gpu_launches": B.forward_launch_count(layer.cfg) * K,
         "clocks": clk,
     }
 

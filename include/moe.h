@@ -124,6 +124,10 @@ size_t moe_permute_scratch_size(const moe_config* cfg);
 /* Bytes of workspace moe_forward needs; 0 for an invalid config. */
 size_t moe_workspace_size(const moe_config* cfg);
 
+/* Number of kernels one moe_forward call launches for this layer (the
+ * kernels are chosen by shape); -1 for an invalid config. */
+int32_t moe_forward_launch_count(const moe_config* cfg);
+
 /* ---- the steps of the layer ------------------------------------------------ */
 
 /* Router scores, softmax over all N experts, top-k and gates
@@ -222,6 +226,19 @@ moe_status moe_load_stats(const moe_config* cfg, const float* prob_partials,
 moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* w,
                        const moe_outputs* out, void* workspace, size_t workspace_bytes,
                        void* stream);
+
+/* moe_forward that also records seven caller-owned CUDA events (cudaEvent_t,
+ * timing enabled) on `stream` at the step boundaries, for per-kernel timing:
+ *   events[0] before the router      events[4] after the second Linear
+ *   events[1] after the router        events[5] after the combine
+ *   events[2] after the permutation   events[6] after the statistics
+ *   events[3] after the first Linear (H)
+ * A NULL entry is skipped.  While `stream` is being captured into a CUDA
+ * graph, the events become external event-record nodes, so every replay of
+ * the graph records them.  Otherwise identical to moe_forward. */
+moe_status moe_forward_profiled(const moe_config* cfg, const void* x, const moe_weights* w,
+                                const moe_outputs* out, void* workspace,
+                                size_t workspace_bytes, void* const* events, void* stream);
 
 /* moe_forward for callers holding tokens and results in HOST memory: x and
  * every non-NULL pointer in `out` are host pointers (page-locked memory makes

@@ -29,7 +29,8 @@ EXPORTS = [
     "moe_router_topk", "moe_permute", "moe_grouped_ffn", "moe_combine", "moe_load_stats",
     "moe_forward", "moe_host_workspace_size", "moe_forward_host", "moe_get_device_status",
     "moe_set_wait_limit_ns", "moe_get_wait_limit_ns", "moe_selftest_bounded_wait",
-    "moe_status_string", "moe_version", "moe_permute_noalloc",
+    "moe_status_string", "moe_version", "moe_permute_noalloc", "moe_forward_profiled",
+    "moe_forward_launch_count",
 ]
 PERMUTE_STATIC_SCRATCH_INTS = 1 << 18
 
@@ -77,6 +78,7 @@ def lib() -> C.CDLL:
         "moe_router_blocks": (C.c_int64, [CP]),
         "moe_permute_scratch_size": (C.c_size_t, [CP]),
         "moe_workspace_size": (C.c_size_t, [CP]),
+        "moe_forward_launch_count": (C.c_int32, [CP]),
         "moe_host_workspace_size": (C.c_size_t, [CP]),
         "moe_router_topk": (C.c_int32, [CP, P, P, P, P, P, P, P, P]),
         "moe_permute": (C.c_int32, [CP, P, P, P, P, P, P, P, P, P, C.c_size_t, P]),
@@ -86,6 +88,9 @@ def lib() -> C.CDLL:
         "moe_load_stats": (C.c_int32, [CP, P, P, P, P, P, P, P]),
         "moe_forward": (C.c_int32, [CP, P, C.POINTER(MoeWeights), C.POINTER(MoeOutputs), P,
                                     C.c_size_t, P]),
+        "moe_forward_profiled": (C.c_int32, [CP, P, C.POINTER(MoeWeights),
+                                             C.POINTER(MoeOutputs), P, C.c_size_t,
+                                             C.POINTER(C.c_void_p), P]),
         "moe_forward_host": (C.c_int32, [CP, P, C.POINTER(MoeWeights),
                                          C.POINTER(MoeOutputs), P, C.c_size_t, P]),
         "moe_get_device_status": (C.c_int32, [P]),
@@ -144,6 +149,10 @@ def router_blocks(cfg: MoeConfig) -> int:
 
 def workspace_size(cfg: MoeConfig) -> int:
     return int(lib().moe_workspace_size(C.byref(cfg)))
+
+
+def forward_launch_count(cfg: MoeConfig) -> int:
+    return int(lib().moe_forward_launch_count(C.byref(cfg)))
 
 
 def host_workspace_size(cfg: MoeConfig) -> int:
@@ -255,6 +264,19 @@ def forward(cfg: MoeConfig, x, weights: MoeWeights, out: Outputs, workspace, str
                              _stream(stream)), "moe_forward")
 
 
+def forward_profiled(cfg: MoeConfig, x, weights: MoeWeights, out: Outputs, workspace,
+                     events, stream=None):
+    """moe_forward recording seven torch.cuda.Event (timing enabled) at the step
+    boundaries: before the router, after router / permute / first Linear /
+    second Linear / combine / statistics."""
+    assert len(events) == 7
+    handles = (C.c_void_p * 7)(*[ev.cuda_event if ev is not None else None for ev in events])
+    _check(lib().moe_forward_profiled(C.byref(cfg), _ptr(x), C.byref(weights),
+                                      C.byref(out.struct()), _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(), handles,
+                                      _stream(stream)), "moe_forward_profiled")
+
+
 def forward_host(cfg: MoeConfig, x_host, weights: MoeWeights, out_host: Outputs, workspace,
                  stream=None):
     _check(lib().moe_forward_host(C.byref(cfg), _ptr(x_host), C.byref(weights),
@@ -288,55 +310,3 @@ class MoeLayer:
         forward(self.cfg, x, self.weights, out, self.workspace, stream)
         return out
 
-
-class StagedLayer(MoeLayer):
-    """The layer as its five C-ABI steps with every intermediate in its own
-    tensor, so a caller can place CUDA events between the steps."""
-
-    STAGES = ("router_topk", "permute", "grouped_ffn", "combine", "load_stats")
-
-    def __init__(self, wl: Workload, tensors: dict, device="cuda", T: int | None = None,
-                 capacity: int | None = None):
-        super().__init__(wl, tensors, device, T, capacity)
-        cfg, dev = self.cfg, self.device
-        T, k, N = cfg.T, cfg.top_k, cfg.n_experts
-        rows = rows_max(cfg)
-        dt = torch.float32 if cfg.dtype == MOE_F32 else torch.bfloat16
-        self.logits = torch.empty((T, N), dtype=torch.float32, device=dev)
-        self.pp = torch.empty((max(router_blocks(cfg), 1), N), dtype=torch.float32, device=dev)
-        self.offsets = torch.empty(N + 2, dtype=torch.int32, device=dev)
-        self.row_token = torch.empty(max(rows, 1), dtype=torch.int32, device=dev)
-        self.token_row = torch.empty((T, k), dtype=torch.int32, device=dev)
-        self.scratch = torch.empty(max(permute_scratch_size(cfg), 256), dtype=torch.uint8,
-                                   device=dev)
-        self.Xp = torch.empty((rows, cfg.d_model), dtype=dt, device=dev)
-        self.H = torch.empty((rows, cfg.d_ff), dtype=dt, device=dev)
-        self.Yp = torch.empty((rows, cfg.d_model), dtype=dt, device=dev)
-
-    def run(self, x, out: Outputs, events=None, stream=None):
-        """events: None or a list of 6 torch.cuda.Event recorded around the steps."""
-        cfg, t = self.cfg, self.t
-        ev = events or [None] * 6
-
-        def mark(i):
-            if ev[i] is not None:
-                ev[i].record(stream)
-
-        mark(0)
-        router_topk(cfg, x, t["W_g"], t["b_g"], self.logits, out.topk_idx, out.topk_w,
-                    self.pp, stream)
-        mark(1)
-        permute(cfg, x, out.topk_idx, out.counts, out.kept, self.offsets, self.row_token,
-                self.token_row, self.Xp, self.scratch, stream)
-        mark(2)
-        grouped_ffn(cfg, self.Xp, self.offsets, out.kept, self.weights, self.H, self.Yp,
-                    stream)
-        mark(3)
-        combine(cfg, self.Yp, self.token_row, out.topk_w, self.offsets, out.y, stream)
-        mark(4)
-        load_stats(cfg, self.pp, out.counts, out.kept, out.mean_prob, out.balance,
-                   out.dropped, stream)
-        mark(5)
-
-    # kernels launched per step (router 2, permute 4, grouped FFN 2, combine 1, stats 1)
-    LAUNCHES_PER_STEP = 10

@@ -45,7 +45,7 @@ int64_t rows_max_of(const moe_config& c) {
   return r;
 }
 
-int64_t router_blocks_of(const moe_config& c) { return ceil_div(c.T, kRouterTokensPerBlock); }
+int64_t router_blocks_of(const moe_config& c) { return router_partial_rows(c); }
 
 // Workspace of moe_forward: every region 256-byte aligned.
 struct Workspace {
@@ -153,6 +153,20 @@ cudaError_t launch_bounded_wait_selftest(uint64_t limit_ns, int32_t* status, cud
 
 }  // namespace moe
 
+namespace moe {
+
+cudaError_t record_event(void* event, cudaStream_t s) {
+  if (!event) return cudaSuccess;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(s, &cs);
+  if (e != cudaSuccess) return e;
+  return cudaEventRecordWithFlags(static_cast<cudaEvent_t>(event), s,
+                                  cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal
+                                                                      : cudaEventRecordDefault);
+}
+
+}  // namespace moe
+
 using namespace moe;
 
 extern "C" {
@@ -202,11 +216,11 @@ moe_status moe_router_topk(const moe_config* cfg, const void* x, const void* W_g
   const void* ps[] = {x, W_g, b_g, logits, topk_idx, topk_w, prob_partials};
   for (const void* q : ps)
     if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_router_logits(*cfg, x, W_g, b_g, logits, s);
-  if (e == cudaSuccess) e = launch_router_softmax_topk(*cfg, logits, topk_idx, topk_w,
-                                                       prob_partials, s);
-  return cuda_status(e);
+  DeviceInfo di;
+  if (!device_info(&di)) return MOE_ERR_CUDA;
+  return cuda_status(launch_router(*cfg, x, W_g, b_g, logits, topk_idx, topk_w, prob_partials,
+                                   di.num_sms, di.status, g_wait_limit_ns.load(),
+                                   static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk_idx,
@@ -270,9 +284,9 @@ moe_status moe_load_stats(const moe_config* cfg, const float* prob_partials,
                                        dropped, static_cast<cudaStream_t>(stream)));
 }
 
-moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* w,
-                       const moe_outputs* out, void* workspace, size_t workspace_bytes,
-                       void* stream) {
+static moe_status forward_impl(const moe_config* cfg, const void* x, const moe_weights* w,
+                               const moe_outputs* out, void* workspace, size_t workspace_bytes,
+                               void* const* events, void* stream) {
   moe_status st = check_config(cfg);
   if (st != MOE_OK) return st;
   const moe_config& c = *cfg;
@@ -296,26 +310,55 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* 
   if (!device_info(&di)) return MOE_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* logits = out->logits ? out->logits : ws.logits;
+  void* const none[7] = {};
+  void* const* ev = events ? events : none;
 
-  cudaError_t e = launch_router_logits(c, x, w->W_g, w->b_g, logits, s);
+  cudaError_t e = record_event(ev[0], s);
   if (e == cudaSuccess)
-    e = launch_router_softmax_topk(c, logits, out->topk_idx, out->topk_w, ws.prob_partials, s);
+    e = launch_router(c, x, w->W_g, w->b_g, logits, out->topk_idx, out->topk_w,
+                      ws.prob_partials, di.num_sms, di.status, g_wait_limit_ns.load(), s);
+  if (e == cudaSuccess) e = record_event(ev[1], s);
   if (e == cudaSuccess)
     e = launch_permute(c, x, out->topk_idx, out->counts, out->kept, ws.offsets, ws.row_token,
                        ws.token_row, ws.Xp, ws.scratch, rows_max_of(c), s);
+  if (e == cudaSuccess) e = record_event(ev[2], s);
   if (e == cudaSuccess) {
     GroupedFfnArgs a{};
     a.Xp = ws.Xp; a.offsets = ws.offsets; a.kept = out->kept; a.w = w; a.H = ws.H;
     a.Yp = ws.Yp; a.rows_max = rows_max_of(c); a.status = di.status;
     a.wait_limit_ns = g_wait_limit_ns.load(); a.num_sms = di.num_sms;
+    a.mid_event = ev[3];
     e = c.dtype == MOE_F32 ? launch_grouped_ffn_f32(c, a, s) : launch_grouped_ffn_bf16(c, a, s);
   }
+  if (e == cudaSuccess) e = record_event(ev[4], s);
   if (e == cudaSuccess)
     e = launch_combine(c, ws.Yp, ws.token_row, out->topk_w, ws.offsets, out->y, s);
+  if (e == cudaSuccess) e = record_event(ev[5], s);
   if (e == cudaSuccess)
     e = launch_load_stats(c, ws.prob_partials, out->counts, out->kept, out->mean_prob,
                           out->balance, out->dropped, s);
+  if (e == cudaSuccess) e = record_event(ev[6], s);
   return cuda_status(e);
+}
+
+moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* w,
+                       const moe_outputs* out, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  return forward_impl(cfg, x, w, out, workspace, workspace_bytes, nullptr, stream);
+}
+
+moe_status moe_forward_profiled(const moe_config* cfg, const void* x, const moe_weights* w,
+                                const moe_outputs* out, void* workspace,
+                                size_t workspace_bytes, void* const* events, void* stream) {
+  if (!events) return MOE_ERR_INVALID_ARG;
+  return forward_impl(cfg, x, w, out, workspace, workspace_bytes, events, stream);
+}
+
+int32_t moe_forward_launch_count(const moe_config* cfg) {
+  if (check_config(cfg) != MOE_OK) return -1;
+  const moe_config& c = *cfg;
+  const int ffn = rows_max_of(c) > 0 ? 2 : 0;
+  return router_launch_count(c) + permute_launch_count(c) + ffn + (c.T > 0 ? 1 : 0) + 1;
 }
 
 size_t moe_host_workspace_size(const moe_config* cfg) {

@@ -24,6 +24,7 @@ cudaError_t launch_grouped_ffn_f32(const moe_config& c, const GroupedFfnArgs& g,
   dim3 grid1(unsigned(ceil_div(c.d_ff, kSimtBN)), unsigned(ceil_div(g.rows_max, kSimtBM)));
   simt_gemm_kernel<float, float><<<grid1, kSimtThreads, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = record_event(g.mid_event, s);
   if (e != cudaSuccess) return e;
   // second Linear: [rows, d_ff] x [d, d_ff]^T
   a.act = -1;

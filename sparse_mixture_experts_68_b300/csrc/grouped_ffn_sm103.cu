@@ -17,9 +17,10 @@
 //   warp 1      allocates TMEM; one thread issues tcgen05.mma
 //               (M=128, N=BN, K=16, bf16 x bf16 -> fp32) into one of two TMEM
 //               accumulators and commits to the ring's "empty" barriers
-//   warps 2-9   epilogue: tcgen05.ld the accumulator (two warps per TMEM lane
-//               quarter, each half of the columns), + bias, activation, bf16,
-//               store the live rows; then free the accumulator
+//   warps 2-17  epilogue: tcgen05.ld the accumulator (four warps per TMEM
+//               lane quarter, each a quarter of the columns), + bias,
+//               activation, bf16, store the live rows; then free the
+//               accumulator
 // Double-buffered accumulators let the epilogue of one tile overlap the
 // main loop of the next.  Every wait is bounded (a time limit, then the
 // device status word records MOE_ERR_TIMEOUT and the CTA winds down).
@@ -36,22 +37,31 @@ namespace {
 
 constexpr int BM = 128;                 // rows per tile = TMEM lanes
 constexpr int BK = 64;                  // 64 bf16 = 128 B = one swizzle row
-constexpr int kStages = 4;
-constexpr int kEpiWarps = 8;
-constexpr int kThreads = (2 + kEpiWarps) * 32;
 constexpr int kMaxGroups = 1025;        // 1024 routed + 1 shared
 
-enum { EPI_BIAS = 0, EPI_BIAS_GELU = 1, EPI_BIAS_RELU = 2 };
+// Epilogues: + bias then bf16 (second Linear), + bias, GELU / ReLU then bf16
+// (first Linear), + bias then fp32 (router scores).
+enum { EPI_BIAS = 0, EPI_BIAS_GELU = 1, EPI_BIAS_RELU = 2, EPI_BIAS_F32 = 3 };
 
-template <int BN>
+// A kernel variant: output tile width BN, depth of the shared-memory ring,
+// number of epilogue warps (a multiple of 4: one set per TMEM lane quarter).
+template <int BN_, int STAGES_, int EPI_WARPS_>
+struct TileCfg {
+  static constexpr int BN = BN_;
+  static constexpr int STAGES = STAGES_;
+  static constexpr int EPI_WARPS = EPI_WARPS_;
+  static constexpr int THREADS = (2 + EPI_WARPS) * 32;
+};
+
+template <int BN, int STAGES>
 struct Layout {
   static constexpr int kABytes = BM * BK * 2;
   static constexpr int kBBytes = BN * BK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kA = 0;
-  static constexpr int kB = kStages * kABytes;
-  static constexpr int kBar = kB + kStages * kBBytes;       // full[S], empty[S], tfull[2], tempty[2], done
-  static constexpr int kNumBars = 2 * kStages + 5;
+  static constexpr int kB = STAGES * kABytes;
+  static constexpr int kBar = kB + STAGES * kBBytes;        // full[S], empty[S], tfull[2], tempty[2], done
+  static constexpr int kNumBars = 2 * STAGES + 5;
   static constexpr int kTmemSlot = kBar + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
   static constexpr int kTileStart = (kAbort + 4 + 15) / 16 * 16;   // int32 [kMaxGroups + 1]
@@ -62,14 +72,16 @@ struct Layout {
 };
 
 struct TcParams {
-  const int32_t* offsets;          // [n_groups + 1] first row of each group
+  const int32_t* offsets;          // [n_groups + 1] first row of each group; nullptr:
+                                   // one group of dense_rows rows starting at row 0
   const int32_t* kept;             // [n_routed] live rows of each routed group
   const __nv_bfloat16* bias;       // [n_routed, Nd]
   const __nv_bfloat16* bias_s;     // [Nd] shared expert
-  __nv_bfloat16* out;              // [rows, Nd]
+  void* out;                       // [rows, Nd], bf16 (fp32 for EPI_BIAS_F32)
   int64_t Nd;
   int32_t n_routed;
   int32_t shared_rows;             // live rows of the shared group; 0 = none
+  int32_t dense_rows;              // rows of the single group when offsets == nullptr
   int32_t num_kb;                  // K / BK
   int32_t* status;
   uint64_t wait_limit_ns;
@@ -132,6 +144,67 @@ __device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32]
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+__device__ __forceinline__ void tmem_ld_16cols(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+template <int CW>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[CW]) {
+  if constexpr (CW == 32) tmem_ld_32cols(taddr, r);
+  else tmem_ld_16cols(taddr, r);
+}
+
+// Epilogue of CW accumulator columns of one row: + bias, activation, store.
+template <int EPI, int CW>
+__device__ __forceinline__ void epilogue_store(const uint32_t (&r)[CW],
+                                               const __nv_bfloat16* __restrict__ bias,
+                                               void* out_row_col) {
+  const uint4* bsrc = reinterpret_cast<const uint4*>(bias);
+  if constexpr (EPI == EPI_BIAS_F32) {
+    float4* dst = reinterpret_cast<float4*>(out_row_col);
+#pragma unroll
+    for (int v = 0; v < CW / 8; ++v) {
+      const uint4 bv = __ldg(bsrc + v);
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&bv);
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const float2 b0 = __bfloat1622float2(b2[2 * i]);
+        const float2 b1 = __bfloat1622float2(b2[2 * i + 1]);
+        dst[2 * v + i] = make_float4(__uint_as_float(r[8 * v + 4 * i]) + b0.x,
+                                     __uint_as_float(r[8 * v + 4 * i + 1]) + b0.y,
+                                     __uint_as_float(r[8 * v + 4 * i + 2]) + b1.x,
+                                     __uint_as_float(r[8 * v + 4 * i + 3]) + b1.y);
+      }
+    }
+  } else {
+    uint4* dst = reinterpret_cast<uint4*>(out_row_col);
+#pragma unroll
+    for (int v = 0; v < CW / 8; ++v) {
+      const uint4 bv = __ldg(bsrc + v);
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&bv);
+      uint4 o;
+      __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 bf = __bfloat1622float2(b2[i]);
+        float x0 = __uint_as_float(r[8 * v + 2 * i]) + bf.x;
+        float x1 = __uint_as_float(r[8 * v + 2 * i + 1]) + bf.y;
+        if (EPI == EPI_BIAS_GELU) { x0 = gelu_erf(x0); x1 = gelu_erf(x1); }
+        if (EPI == EPI_BIAS_RELU) { x0 = fmaxf(x0, 0.f); x1 = fmaxf(x1, 0.f); }
+        o2[i] = __floats2bfloat162_rn(x0, x1);
+      }
+      dst[v] = o;
+    }
+  }
+}
+
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
 // 128 B, 8-row groups 1024 B apart (stride byte offset); descriptor version 1.
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
@@ -182,12 +255,15 @@ __device__ __forceinline__ TileCoord decode_tile(int tile, const int32_t* tile_s
   return TileCoord{lo, local % mt, local / mt};
 }
 
-template <int BN, int EPI>
-__global__ void __launch_bounds__(kThreads, 1)
+template <class CFG, int EPI, int MINB>
+__global__ void __launch_bounds__(CFG::THREADS, MINB)
     tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmBs, const TcParams p) {
-  using L = Layout<BN>;
+  constexpr int BN = CFG::BN;
+  constexpr int kStages = CFG::STAGES;
+  constexpr int kEpiWarps = CFG::EPI_WARPS;
+  using L = Layout<BN, kStages>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -203,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int32_t* grp_off = reinterpret_cast<int32_t*>(smem + L::kGroupOff);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_groups = p.n_routed + (p.shared_rows > 0 ? 1 : 0);
+  const int n_groups = p.offsets ? p.n_routed + (p.shared_rows > 0 ? 1 : 0) : 1;
   const int ntiles = int(p.Nd / BN);
 
   if (threadIdx.x == 0) {
@@ -232,8 +308,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int g = base + lane;
       int32_t live = 0, off = 0;
       if (g < n_groups) {
-        off = p.offsets[g];
-        live = g < p.n_routed ? p.kept[g] : p.shared_rows;
+        if (p.offsets) {
+          off = p.offsets[g];
+          live = g < p.n_routed ? p.kept[g] : p.shared_rows;
+        } else {
+          live = p.dense_rows;
+        }
         grp_off[g] = off;
       }
       const int32_t tiles = int32_t((live + BM - 1) / BM) * ntiles;
@@ -328,8 +408,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------- epilogue ----------------
     const int q = warp & 3;                      // TMEM lane quarter of this warp
-    const int half = (warp - 2) >> 2;            // which half of the tile's columns
-    constexpr int kCols = BN / 2;
+    const int part = (warp - 2) >> 2;            // which share of the tile's columns
+    constexpr int kCols = BN / (kEpiWarps / 4);
+    constexpr int CW = kCols < 32 ? kCols : 32;  // columns per tcgen05.ld
     uint32_t acc = 0, acc_phase = 0;
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
       const TileCoord tc = decode_tile(tile, tile_start, n_groups, ntiles);
@@ -339,36 +420,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const bool routed = tc.g < p.n_routed;
-      const int live = routed ? p.kept[tc.g] : p.shared_rows;
+      const int live = p.offsets ? (routed ? p.kept[tc.g] : p.shared_rows) : p.dense_rows;
       const int row_in_group = tc.m * BM + q * 32 + lane;
       const bool valid = row_in_group < live;
       const int64_t out_row = int64_t(grp_off[tc.g]) + row_in_group;
       const __nv_bfloat16* bias = routed ? p.bias + int64_t(tc.g) * p.Nd : p.bias_s;
+      constexpr int kOutBytes = EPI == EPI_BIAS_F32 ? 4 : 2;
 #pragma unroll 1
-      for (int c = half * kCols; c < (half + 1) * kCols; c += 32) {
-        uint32_t r[32];
-        tmem_ld_32cols(tmem_base + (uint32_t(q * 32) << 16) + acc * BN + c, r);
+      for (int c = part * kCols; c < (part + 1) * kCols; c += CW) {
+        uint32_t r[CW];
+        tmem_ld_cols<CW>(tmem_base + (uint32_t(q * 32) << 16) + acc * BN + c, r);
         if (valid) {
           const int64_t col = int64_t(tc.n) * BN + c;
-          const uint4* bsrc = reinterpret_cast<const uint4*>(bias + col);
-          uint4* dst = reinterpret_cast<uint4*>(p.out + out_row * p.Nd + col);
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const uint4 bv = __ldg(bsrc + v);
-            const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&bv);
-            uint4 o;
-            __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(&o);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float2 bf = __bfloat1622float2(b2[i]);
-              float x0 = __uint_as_float(r[8 * v + 2 * i]) + bf.x;
-              float x1 = __uint_as_float(r[8 * v + 2 * i + 1]) + bf.y;
-              if (EPI == EPI_BIAS_GELU) { x0 = gelu_erf(x0); x1 = gelu_erf(x1); }
-              if (EPI == EPI_BIAS_RELU) { x0 = fmaxf(x0, 0.f); x1 = fmaxf(x1, 0.f); }
-              o2[i] = __floats2bfloat162_rn(x0, x1);
-            }
-            dst[v] = o;
-          }
+          epilogue_store<EPI, CW>(r, bias + col,
+                                  static_cast<uint8_t*>(p.out) +
+                                      (out_row * p.Nd + col) * kOutBytes);
         }
       }
       tc_fence_before();
@@ -420,29 +486,60 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, int EPI>
+template <class CFG, int EPI>
 cudaError_t launch_tc(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& Bs,
                       const TcParams& p, int grid, cudaStream_t s) {
-  auto kern = tc_grouped_gemm_kernel<BN, EPI>;
-  const int smem = Layout<BN>::kAlloc;
+  constexpr int smem = Layout<CFG::BN, CFG::STAGES>::kAlloc;
+  constexpr int minb = smem <= 110 * 1024 ? 2 : 1;    // two CTAs per SM when they fit
+  auto kern = tc_grouped_gemm_kernel<CFG, EPI, minb>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, smem, s>>>(A, B, Bs, p);
+  kern<<<grid, CFG::THREADS, smem, s>>>(A, B, Bs, p);
   return cudaGetLastError();
 }
 
-template <int BN>
+template <class CFG>
 cudaError_t launch_epi(int epi, const CUtensorMap& A, const CUtensorMap& B,
                        const CUtensorMap& Bs, const TcParams& p, int grid, cudaStream_t s) {
-  if (epi == EPI_BIAS_GELU) return launch_tc<BN, EPI_BIAS_GELU>(A, B, Bs, p, grid, s);
-  if (epi == EPI_BIAS_RELU) return launch_tc<BN, EPI_BIAS_RELU>(A, B, Bs, p, grid, s);
-  return launch_tc<BN, EPI_BIAS>(A, B, Bs, p, grid, s);
+  if (epi == EPI_BIAS_F32) return launch_tc<CFG, EPI_BIAS_F32>(A, B, Bs, p, grid, s);
+  if (epi == EPI_BIAS_GELU) return launch_tc<CFG, EPI_BIAS_GELU>(A, B, Bs, p, grid, s);
+  if (epi == EPI_BIAS_RELU) return launch_tc<CFG, EPI_BIAS_RELU>(A, B, Bs, p, grid, s);
+  return launch_tc<CFG, EPI_BIAS>(A, B, Bs, p, grid, s);
 }
 
-int pick_bn(int64_t Nd) {
-  if (Nd % 256 == 0) return 256;
-  if (Nd % 128 == 0) return 128;
-  return 64;
+// The kernel variants this library instantiates.
+enum TileChoice { TILE_256 = 0, TILE_128 = 1, TILE_64 = 2, TILE_128_2CTA = 3, NUM_TILES };
+using Cfg256 = TileCfg<256, 4, 16>;        // one CTA per SM, 192 KB ring
+using Cfg128 = TileCfg<128, 4, 16>;
+using Cfg64 = TileCfg<64, 6, 16>;
+using Cfg128x2 = TileCfg<128, 3, 8>;       // two CTAs per SM, 96 KB ring each
+
+int tile_bn(int choice) {
+  switch (choice) {
+    case TILE_256: return 256;
+    case TILE_64: return 64;
+    default: return 128;
+  }
+}
+
+int tile_ctas_per_sm(int choice) { return choice == TILE_128_2CTA ? 2 : 1; }
+
+cudaError_t launch_choice(int choice, int epi, const CUtensorMap& A, const CUtensorMap& B,
+                          const CUtensorMap& Bs, const TcParams& p, int grid, cudaStream_t s) {
+  switch (choice) {
+    case TILE_256: return launch_epi<Cfg256>(epi, A, B, Bs, p, grid, s);
+    case TILE_128: return launch_epi<Cfg128>(epi, A, B, Bs, p, grid, s);
+    case TILE_64: return launch_epi<Cfg64>(epi, A, B, Bs, p, grid, s);
+    default: return launch_epi<Cfg128x2>(epi, A, B, Bs, p, grid, s);
+  }
+}
+
+// Tile variant for one grouped Linear with output width Nd: the widest tile
+// that divides Nd (256-wide tiles load the least shared memory per MMA).
+int pick_tile(int64_t Nd) {
+  if (Nd % 256 == 0) return TILE_256;
+  if (Nd % 128 == 0) return TILE_128;
+  return TILE_64;
 }
 
 // One grouped Linear: out[group g] = epi(A[group g] . W[g]^T + bias[g]).
@@ -450,7 +547,8 @@ cudaError_t grouped_linear(const moe_config& c, const GroupedFfnArgs& g, const v
                            const void* W, const void* Ws, const void* bias,
                            const void* bias_s, void* out, int64_t K, int64_t Nd, int epi,
                            cudaStream_t s) {
-  const int bn = pick_bn(Nd);
+  const int choice = pick_tile(Nd);
+  const int bn = tile_bn(choice);
   const int64_t N = c.n_experts;
   CUtensorMap mA, mB, mBs;
   if (!make_map(&mA, A, uint64_t(K), uint64_t(g.rows_max), 0, BM)) return cudaErrorInvalidValue;
@@ -467,7 +565,7 @@ cudaError_t grouped_linear(const moe_config& c, const GroupedFfnArgs& g, const v
   p.kept = g.kept;
   p.bias = static_cast<const __nv_bfloat16*>(bias);
   p.bias_s = static_cast<const __nv_bfloat16*>(bias_s);
-  p.out = static_cast<__nv_bfloat16*>(out);
+  p.out = out;
   p.Nd = Nd;
   p.n_routed = int32_t(N);
   p.shared_rows = c.d_ff_shared > 0 ? int32_t(c.T) : 0;
@@ -475,11 +573,10 @@ cudaError_t grouped_linear(const moe_config& c, const GroupedFfnArgs& g, const v
   p.status = g.status;
   p.wait_limit_ns = g.wait_limit_ns;
   const int64_t max_tiles = ceil_div(g.rows_max, BM) * (Nd / bn);
-  const int grid = int(max_tiles < g.num_sms ? max_tiles : g.num_sms);
+  const int64_t slots = int64_t(g.num_sms) * tile_ctas_per_sm(choice);
+  const int grid = int(max_tiles < slots ? max_tiles : slots);
   if (grid <= 0) return cudaSuccess;
-  if (bn == 256) return launch_epi<256>(epi, mA, mB, mBs, p, grid, s);
-  if (bn == 128) return launch_epi<128>(epi, mA, mB, mBs, p, grid, s);
-  return launch_epi<64>(epi, mA, mB, mBs, p, grid, s);
+  return launch_choice(choice, epi, mA, mB, mBs, p, grid, s);
 }
 
 }  // namespace
@@ -490,9 +587,41 @@ cudaError_t launch_grouped_ffn_bf16(const moe_config& c, const GroupedFfnArgs& g
   const int epi1 = c.act == MOE_ACT_RELU ? EPI_BIAS_RELU : EPI_BIAS_GELU;
   cudaError_t e = grouped_linear(c, g, g.Xp, g.w->W1, g.w->W1s, g.w->b1, g.w->b1s, g.H,
                                  c.d_model, c.d_ff, epi1, s);
+  if (e == cudaSuccess) e = record_event(g.mid_event, s);
   if (e != cudaSuccess) return e;
   return grouped_linear(c, g, g.H, g.w->W2, g.w->W2s, g.w->b2, g.w->b2s, g.Yp, c.d_ff,
                         c.d_model, EPI_BIAS, s);
+}
+
+// Router scores z = x . W_g^T + b_g (fp32) as one dense group on the tensor
+// cores: bf16 products are exact in fp32, so only the summation order differs
+// from a CUDA-core dot product.  N % 64 == 0; 64-wide tiles give ceil(T/128)
+// * N/64 tiles to spread over the SMs.
+cudaError_t launch_router_logits_tc(const moe_config& c, const void* x, const void* W_g,
+                                    const void* b_g, float* logits, int num_sms,
+                                    int32_t* status, uint64_t wait_limit_ns, cudaStream_t s) {
+  if (c.T == 0) return cudaSuccess;
+  constexpr int bn = 64;
+  CUtensorMap mA, mB;
+  if (!make_map(&mA, x, uint64_t(c.d_model), uint64_t(c.T), 0, BM)) return cudaErrorInvalidValue;
+  if (!make_map(&mB, W_g, uint64_t(c.d_model), uint64_t(c.n_experts), 1, bn))
+    return cudaErrorInvalidValue;
+  TcParams p{};
+  p.offsets = nullptr;
+  p.kept = nullptr;
+  p.bias = static_cast<const __nv_bfloat16*>(b_g);
+  p.bias_s = nullptr;
+  p.out = logits;
+  p.Nd = c.n_experts;
+  p.n_routed = 1;
+  p.shared_rows = 0;
+  p.dense_rows = int32_t(c.T);
+  p.num_kb = int32_t(c.d_model / BK);
+  p.status = status;
+  p.wait_limit_ns = wait_limit_ns;
+  const int64_t tiles = ceil_div(c.T, BM) * (c.n_experts / bn);
+  const int grid = int(tiles < num_sms ? tiles : num_sms);
+  return launch_tc<Cfg64, EPI_BIAS_F32>(mA, mB, mB, p, grid, s);
 }
 
 }  // namespace moe

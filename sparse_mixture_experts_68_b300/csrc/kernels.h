@@ -12,13 +12,29 @@ namespace moe {
 
 // ---- router (router.cu) ------------------------------------------------------
 
-constexpr int kRouterTokensPerBlock = 32;   // tokens per softmax/top-k block
+constexpr int kRouterTokensPerBlock = 8;    // tokens per router pass (one per warp)
+constexpr int kRouterMaxBlocks = 296;       // router blocks (grid-stride over 8-token groups)
+
+// Rows of the router's probability partial sums: one per router block.
+inline int64_t router_partial_rows(const moe_config& c) {
+  const int64_t groups = (c.T + kRouterTokensPerBlock - 1) / kRouterTokensPerBlock;
+  return groups < kRouterMaxBlocks ? groups : kRouterMaxBlocks;
+}
 
 cudaError_t launch_router_logits(const moe_config& c, const void* x, const void* W_g,
                                  const void* b_g, float* logits, cudaStream_t s);
 cudaError_t launch_router_softmax_topk(const moe_config& c, const float* logits,
                                        int32_t* topk_idx, float* topk_w,
                                        float* prob_partials, cudaStream_t s);
+// router scores on the tensor cores, fp32 out (grouped_ffn_sm103.cu)
+cudaError_t launch_router_logits_tc(const moe_config& c, const void* x, const void* W_g,
+                                    const void* b_g, float* logits, int num_sms,
+                                    int32_t* status, uint64_t wait_limit_ns, cudaStream_t s);
+// the whole router step, kernels chosen by shape
+cudaError_t launch_router(const moe_config& c, const void* x, const void* W_g,
+                          const void* b_g, float* logits, int32_t* topk_idx, float* topk_w,
+                          float* prob_partials, int num_sms, int32_t* status,
+                          uint64_t wait_limit_ns, cudaStream_t s);
 
 // ---- permutation (permute.cu) ------------------------------------------------
 
@@ -43,7 +59,11 @@ struct GroupedFfnArgs {
   int32_t* status;          // device status word
   uint64_t wait_limit_ns;
   int num_sms;
+  void* mid_event;          // cudaEvent_t recorded between the two Linears, or nullptr
 };
+
+// Records a caller's event on s (as an external node while s is capturing).
+cudaError_t record_event(void* event, cudaStream_t s);
 
 // fp32 path on CUDA cores (grouped_ffn_f32.cu)
 cudaError_t launch_grouped_ffn_f32(const moe_config& c, const GroupedFfnArgs& a, cudaStream_t s);
@@ -58,6 +78,10 @@ cudaError_t launch_combine(const moe_config& c, const void* Yp, const int32_t* t
 cudaError_t launch_load_stats(const moe_config& c, const float* prob_partials,
                               const int32_t* counts, const int32_t* kept, float* mean_prob,
                               float* balance, int32_t* dropped, cudaStream_t s);
+
+// ---- kernels launched per step, for the chosen dispatch ------------------------------
+int router_launch_count(const moe_config& c);
+int permute_launch_count(const moe_config& c);
 
 // ---- host-side checks shared with entry points outside api.cu -------------------------
 moe_status validate_config(const moe_config* cfg);   // as every moe_* entry checks cfg

@@ -143,6 +143,129 @@ __global__ void __launch_bounds__(32)
   }
 }
 
+// The whole counting sort in one block of 32 warps, for layers whose
+// assignments (T*k) and per-warp expert counts fit in shared memory: the
+// expert ids are staged as 16-bit values; warp w owns the contiguous range
+// [w*L, (w+1)*L) of assignments.  Pass 1 counts per (warp, expert) with
+// __match_any_sync; a per-expert scan over warps gives each warp's base rank;
+// a scan over experts gives the padded group offsets; pass 2 re-walks the
+// ranges and writes ranks.  Same results as hist + scan + rank.
+constexpr int kSortWarps = 32;
+
+__global__ void __launch_bounds__(kSortWarps * 32)
+    permute_sort_kernel(const int32_t* __restrict__ topk_idx, int T, int k, int N,
+                        int64_t capacity, int has_shared, int32_t* __restrict__ counts,
+                        int32_t* __restrict__ kept, int32_t* __restrict__ offsets,
+                        int32_t* __restrict__ row_token, int32_t* __restrict__ token_row) {
+  extern __shared__ int32_t sm[];
+  const int A = T * k;
+  int32_t* cnt = sm;                              // [kSortWarps][N], then base ranks
+  int32_t* off = cnt + kSortWarps * N;            // [N] group offsets
+  int32_t* warp_tot = off + N;                    // [32]
+  int16_t* ids = reinterpret_cast<int16_t*>(warp_tot + 32);   // [A]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < kSortWarps * N; i += blockDim.x) cnt[i] = 0;
+  for (int a = threadIdx.x; a < A; a += blockDim.x) {
+    const int e = topk_idx[a];
+    ids[a] = int16_t((e >= 0 && e < N) ? e : -1);   // out-of-range experts: dropped
+  }
+  __syncthreads();
+  const int L = (A + kSortWarps - 1) / kSortWarps;
+  const int a_begin = warp * L, a_end = min(A, a_begin + L);
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  int32_t* my = cnt + warp * N;
+  // pass 1: per-warp counts
+  for (int base = a_begin; base < a_end; base += 32) {
+    const int a = base + lane;
+    const int e = a < a_end ? ids[a] : -1;
+    const int key = e >= 0 ? e : (0x40000000 | lane);
+    const uint32_t same = __match_any_sync(0xffffffffu, key);
+    if (e >= 0 && (same & lt_mask) == 0) my[e] += __popc(same);
+    __syncwarp();
+  }
+  __syncthreads();
+  // per expert: base rank of each warp, totals, capacity, padded size
+  int32_t padded = 0;
+  for (int e = threadIdx.x; e < N; e += blockDim.x) {
+    int32_t run = 0;
+    for (int w = 0; w < kSortWarps; ++w) {
+      const int32_t c = cnt[w * N + e];
+      cnt[w * N + e] = run;
+      run += c;
+    }
+    const int32_t kp = (capacity > 0 && int64_t(run) > capacity) ? int32_t(capacity) : run;
+    counts[e] = run;
+    kept[e] = kp;
+    off[e] = kp;                                   // kept for now; offsets below
+    padded = int32_t(round_up(kp, kGroupAlign));   // N <= blockDim: one expert per thread
+  }
+  // exclusive scan of padded sizes over experts (thread e holds expert e)
+  int32_t incl = padded;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int32_t w = warp_tot[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t v = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += v;
+    }
+    warp_tot[lane] = w;
+  }
+  __syncthreads();
+  const int32_t excl = incl - padded + (warp > 0 ? warp_tot[warp - 1] : 0);
+  const int e_me = threadIdx.x;
+  if (e_me < N) {
+    const int32_t kp = off[e_me];
+    offsets[e_me] = excl;
+    for (int32_t r = excl + kp; r < excl + padded; ++r) row_token[r] = -1;
+  }
+  __syncthreads();
+  if (e_me < N) off[e_me] = excl;
+  if (e_me == N - 1) {
+    offsets[N] = excl + padded;
+    offsets[N + 1] = excl + padded + (has_shared ? int32_t(round_up(T, kGroupAlign)) : 0);
+  }
+  __syncthreads();
+  // pass 2: ranks in token-major order
+  for (int base = a_begin; base < a_end; base += 32) {
+    const int a = base + lane;
+    const int e = a < a_end ? ids[a] : -1;
+    const int key = e >= 0 ? e : (0x40000000 | lane);
+    const uint32_t same = __match_any_sync(0xffffffffu, key);
+    int32_t rank = 0;
+    if (e >= 0) rank = my[e] + __popc(same & lt_mask);
+    __syncwarp();
+    if (e >= 0 && (same & lt_mask) == 0) my[e] += __popc(same);
+    __syncwarp();
+    if (a < a_end) {
+      const bool keep = e >= 0 && (capacity <= 0 || rank < capacity);
+      int32_t row = -1;
+      if (keep) {
+        row = off[e] + rank;
+        row_token[row] = a / k;
+      }
+      token_row[a] = row;
+    }
+  }
+}
+
+size_t sort_smem_bytes(const moe_config& c) {
+  const int64_t A = c.T * c.top_k;
+  return size_t(kSortWarps * c.n_experts + c.n_experts + 32) * 4 + size_t(A) * 2 + 16;
+}
+
+// Above ~16K assignments the multi-block histogram path is faster.
+bool single_block_sort_fits(const moe_config& c) {
+  return c.n_experts <= kSortWarps * 32 && c.T * c.top_k <= 16384 &&
+         sort_smem_bytes(c) <= 200 * 1024;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256)
     permute_copy_kernel(const T* __restrict__ x, int64_t d, int Ttok, int N,
@@ -165,7 +288,13 @@ __global__ void __launch_bounds__(256)
     const uint4* src = reinterpret_cast<const uint4*>(x + t * d);
     uint4* dst = reinterpret_cast<uint4*>(Xp + r * d);
     const int64_t nv = d / V;
-    for (int64_t i = lane; i < nv; i += 32) dst[i] = __ldg(src + i);
+    int64_t i = lane;
+    for (; i + 96 < nv; i += 128) {                 // four 16-byte loads in flight
+      const uint4 a0 = __ldg(src + i), a1 = __ldg(src + i + 32), a2 = __ldg(src + i + 64),
+                  a3 = __ldg(src + i + 96);
+      dst[i] = a0; dst[i + 32] = a1; dst[i + 64] = a2; dst[i + 96] = a3;
+    }
+    for (; i < nv; i += 32) dst[i] = __ldg(src + i);
   }
 }
 
@@ -176,6 +305,33 @@ size_t permute_scratch_bytes(const moe_config& c) {
   return size_t(2 * round_up(n, 64)) * sizeof(int32_t);
 }
 
+namespace {
+
+cudaError_t launch_copy(const moe_config& c, const void* x, const int32_t* offsets,
+                        const int32_t* row_token, void* Xp, int64_t rows_max, cudaStream_t s) {
+  if (rows_max <= 0) return cudaSuccess;
+  const int N = int(c.n_experts), T = int(c.T);
+  const int64_t want = ceil_div(rows_max, 8);
+  const unsigned blocks = unsigned(want < 148 * 8 ? want : 148 * 8);
+  if (c.dtype == MOE_F32)
+    permute_copy_kernel<float><<<blocks, 256, 0, s>>>(static_cast<const float*>(x), c.d_model,
+                                                      T, N, offsets, row_token,
+                                                      static_cast<float*>(Xp));
+  else
+    permute_copy_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(x), c.d_model, T, N, offsets, row_token,
+        static_cast<__nv_bfloat16*>(Xp));
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int permute_launch_count(const moe_config& c) {
+  const int copy = moe::rows_max_for(c) > 0 ? 1 : 0;
+  if (single_block_sort_fits(c)) return 1 + copy;
+  return (c.T > 0 ? 3 : 1) + copy;
+}
+
 cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* topk_idx,
                            int32_t* counts, int32_t* kept, int32_t* offsets,
                            int32_t* row_token, int32_t* token_row, void* Xp, void* scratch,
@@ -184,6 +340,19 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* to
   const int nblk = int(permute_blocks(c));
   PermuteScratch p = carve(c, scratch);
   const size_t smemN = size_t(N) * sizeof(int32_t);
+  cudaError_t e;
+  if (single_block_sort_fits(c)) {
+    const size_t smem = sort_smem_bytes(c);
+    e = cudaFuncSetAttribute(permute_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(smem));
+    if (e != cudaSuccess) return e;
+    permute_sort_kernel<<<1, kSortWarps * 32, smem, s>>>(topk_idx, T, k, N, c.capacity,
+                                                         c.d_ff_shared > 0 ? 1 : 0, counts,
+                                                         kept, offsets, row_token, token_row);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_copy(c, x, offsets, row_token, Xp, rows_max, s);
+  }
   if (nblk > 0) {
     permute_hist_kernel<<<nblk, 256, smemN, s>>>(topk_idx, T, k, N, p.block_counts);
     cudaError_t e = cudaGetLastError();
@@ -192,7 +361,7 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* to
   permute_scan_kernel<<<1, 1024, 0, s>>>(p.block_counts, nblk, N, T, c.capacity,
                                          c.d_ff_shared > 0 ? 1 : 0, p.block_base, counts,
                                          kept, offsets, row_token);
-  cudaError_t e = cudaGetLastError();
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (nblk > 0) {
     permute_rank_kernel<<<nblk, 32, smemN, s>>>(topk_idx, T, k, N, c.capacity, p.block_base,
@@ -200,20 +369,7 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* to
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  if (rows_max > 0) {
-    const int64_t want = ceil_div(rows_max, 8);
-    const unsigned blocks = unsigned(want < 148 * 8 ? want : 148 * 8);
-    if (c.dtype == MOE_F32)
-      permute_copy_kernel<float><<<blocks, 256, 0, s>>>(
-          static_cast<const float*>(x), c.d_model, T, N, offsets, row_token,
-          static_cast<float*>(Xp));
-    else
-      permute_copy_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
-          static_cast<const __nv_bfloat16*>(x), c.d_model, T, N, offsets, row_token,
-          static_cast<__nv_bfloat16*>(Xp));
-    e = cudaGetLastError();
-  }
-  return e;
+  return launch_copy(c, x, offsets, row_token, Xp, rows_max, s);
 }
 
 }  // namespace moe

@@ -44,8 +44,10 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
 #pragma unroll
   for (int i = 0; i < NPL; ++i) psum[i] = 0.f;
 
+  const int groups = (T + kRouterTokensPerBlock - 1) / kRouterTokensPerBlock;
+  for (int grp = blockIdx.x; grp < groups; grp += gridDim.x)
   for (int q = 0; q < kTokPerWarp; ++q) {
-    const int t = blockIdx.x * kRouterTokensPerBlock + warp * kTokPerWarp + q;
+    const int t = grp * kRouterTokensPerBlock + warp * kTokPerWarp + q;
     if (t >= T) break;
     const float* zr = logits + int64_t(t) * N;
     float z[NPL];
@@ -73,6 +75,8 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
     // top-k by repeated warp arg-max over the not yet selected experts
     uint32_t taken = 0;                          // bit i: expert lane + 32 i selected
     float kept_sum = 0.f;
+    int my_e = 0;
+    float my_g = 0.f;
     int32_t* out_i = topk_idx + int64_t(t) * k;
     float* out_w = topk_w + int64_t(t) * k;
     for (int j = 0; j < k; ++j) {
@@ -95,14 +99,24 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
       if ((be & 31) == lane) taken |= 1u << (be >> 5);
       const float g = expf(bv - m);              // m is the largest score: slot 0's
       kept_sum += g;
-      if (lane == 0) {
-        out_i[j] = be;
-        out_w[j] = renorm ? g : g * inv;
+      if (lane == (j & 31)) { my_e = be; my_g = g; }   // slot j is held by lane j % 32
+      if (k > 32 && ((j & 31) == 31 || j == k - 1)) {  // k > 32: flush 32 slots at a time
+        const int j0 = j & ~31;
+        if (lane <= j - j0) {
+          out_i[j0 + lane] = my_e;
+          out_w[j0 + lane] = my_g;                      // unnormalised for now
+        }
       }
     }
-    if (renorm && lane == 0) {
-      const float r = 1.0f / kept_sum;
-      for (int j = 0; j < k; ++j) out_w[j] *= r;
+    // gate = exp(z - max) / (sum over the kept k), or / (sum over all N)
+    const float scale = renorm ? 1.0f / kept_sum : inv;
+    if (k <= 32) {
+      if (lane < k) {
+        out_i[lane] = my_e;
+        out_w[lane] = my_g * scale;
+      }
+    } else {
+      for (int j = lane; j < k; j += 32) out_w[j] *= scale;  // each lane rescales its own writes
     }
   }
 
@@ -120,12 +134,219 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
   }
 }
 
+// Fused router for small expert counts (N <= 64) whose W_g fits in shared
+// memory: one warp per token computes all N scores (lanes split d in 16-byte
+// vectors against W_g staged in shared memory), reduce-scatters them across
+// the warp so lane l holds experts [l*NPL, (l+1)*NPL), then takes the softmax,
+// the top-k and the gates as above.  One pass over x, no score round trip.
+template <typename TIn, int NPAD>
+__global__ void __launch_bounds__(kRouterWarps * 32)
+    router_fused_kernel(const TIn* __restrict__ x, const TIn* __restrict__ W_g,
+                        const TIn* __restrict__ b_g, int T, int d, int N, int k, int renorm,
+                        float* __restrict__ logits, int32_t* __restrict__ topk_idx,
+                        float* __restrict__ topk_w, float* __restrict__ prob_partials) {
+  constexpr int V = Vec16<TIn>::n;
+  constexpr int NPL = NPAD / 32;
+  extern __shared__ uint4 wsm[];                 // W_g [N][d], then partial sums
+  const int dv = d / V;                          // 16-byte vectors per row
+  const int nvec = N * dv;
+  const uint4* wsrc = reinterpret_cast<const uint4*>(W_g);
+  {
+    // four independent loads in flight per thread
+    int i = threadIdx.x;
+    for (; i + 3 * int(blockDim.x) < nvec; i += 4 * blockDim.x) {
+      const uint4 a0 = __ldg(wsrc + i), a1 = __ldg(wsrc + i + blockDim.x),
+                  a2 = __ldg(wsrc + i + 2 * blockDim.x), a3 = __ldg(wsrc + i + 3 * blockDim.x);
+      wsm[i] = a0; wsm[i + blockDim.x] = a1; wsm[i + 2 * blockDim.x] = a2;
+      wsm[i + 3 * blockDim.x] = a3;
+    }
+    for (; i < nvec; i += blockDim.x) wsm[i] = __ldg(wsrc + i);
+  }
+  float* red = reinterpret_cast<float*>(wsm + nvec);   // [kRouterWarps][NPAD]
+  __syncthreads();
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kTokPerWarp = kRouterTokensPerBlock / kRouterWarps;
+  float psum[NPL];
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) psum[i] = 0.f;
+
+  const int groups = (T + kRouterTokensPerBlock - 1) / kRouterTokensPerBlock;
+  for (int grp = blockIdx.x; grp < groups; grp += gridDim.x)
+  for (int q = 0; q < kTokPerWarp; ++q) {
+    const int t = grp * kRouterTokensPerBlock + warp * kTokPerWarp + q;
+    if (t >= T) break;
+    float acc[NPAD];
+#pragma unroll
+    for (int e = 0; e < NPAD; ++e) acc[e] = 0.f;
+    const uint4* xr = reinterpret_cast<const uint4*>(x + int64_t(t) * d);
+    // x is read once: up to four 16-byte loads per lane in flight
+    for (int c0 = lane; c0 < dv; c0 += 4 * 32) {
+      uint4 xq[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int c = c0 + 32 * u;
+        xq[u] = c < dv ? __ldg(xr + c) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int c = c0 + 32 * u;
+        if (c >= dv) break;
+        float xv[V];
+        Vec16<TIn>::load(reinterpret_cast<const TIn*>(&xq[u]), xv);
+#pragma unroll
+        for (int e = 0; e < NPAD; ++e) {
+          if (e < N) {
+            float wv[V];
+            Vec16<TIn>::load(reinterpret_cast<const TIn*>(wsm + e * dv + c), wv);
+#pragma unroll
+            for (int i = 0; i < V; ++i) acc[e] = fmaf(xv[i], wv[i], acc[e]);
+          }
+        }
+      }
+    }
+    // reduce-scatter: after the step with offset o, a lane keeps the half of
+    // its current range selected by bit o of its lane id
+#pragma unroll
+    for (int o = 16, S = NPAD; o >= 1; o >>= 1, S >>= 1) {
+      const bool upper = (lane & o) != 0;
+#pragma unroll
+      for (int i = 0; i < S / 2; ++i) {
+        const float send = upper ? acc[i] : acc[i + S / 2];
+        const float keep = upper ? acc[i + S / 2] : acc[i];
+        acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+      }
+    }
+    float z[NPL];
+    float m = -FLT_MAX;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      const int e = lane * NPL + i;
+      z[i] = e < N ? acc[i] + to_f32(b_g[e]) : -INFINITY;
+      if (e < N) logits[int64_t(t) * N + e] = z[i];
+      m = fmaxf(m, z[i]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float ex[NPL], ssum = 0.f;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      ex[i] = (lane * NPL + i < N) ? expf(z[i] - m) : 0.f;
+      ssum += ex[i];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
+    const float inv = 1.0f / ssum;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) psum[i] += ex[i] * inv;
+
+    uint32_t taken = 0;
+    float kept_sum = 0.f;
+    int my_e = 0;
+    float my_g = 0.f;
+    int32_t* out_i = topk_idx + int64_t(t) * k;
+    float* out_w = topk_w + int64_t(t) * k;
+    for (int j = 0; j < k; ++j) {
+      float bv = -INFINITY;
+      int be = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < NPL; ++i) {
+        const int e = lane * NPL + i;
+        if (e < N && !((taken >> i) & 1u) && (z[i] > bv || (z[i] == bv && e < be))) {
+          bv = z[i];
+          be = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
+      }
+      if (be / NPL == lane) taken |= 1u << (be % NPL);
+      const float g = expf(bv - m);
+      kept_sum += g;
+      if (lane == (j & 31)) { my_e = be; my_g = g; }   // slot j is held by lane j % 32
+      if (k > 32 && ((j & 31) == 31 || j == k - 1)) {  // k > 32: flush 32 slots at a time
+        const int j0 = j & ~31;
+        if (lane <= j - j0) {
+          out_i[j0 + lane] = my_e;
+          out_w[j0 + lane] = my_g;                      // unnormalised for now
+        }
+      }
+    }
+    // gate = exp(z - max) / (sum over the kept k), or / (sum over all N)
+    const float scale = renorm ? 1.0f / kept_sum : inv;
+    if (k <= 32) {
+      if (lane < k) {
+        out_i[lane] = my_e;
+        out_w[lane] = my_g * scale;
+      }
+    } else {
+      for (int j = lane; j < k; j += 32) out_w[j] *= scale;  // each lane rescales its own writes
+    }
+  }
+
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const int e = lane * NPL + i;
+    if (e < N) red[warp * NPAD + e] = psum[i];
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < N; e += blockDim.x) {
+    float v = 0.f;
+    for (int w = 0; w < kRouterWarps; ++w) v += red[w * NPAD + e];
+    prob_partials[int64_t(blockIdx.x) * N + e] = v;
+  }
+}
+
+constexpr size_t kFusedRouterSmemLimit = 200 * 1024;
+
+size_t fused_router_smem(const moe_config& c) {
+  const size_t es = c.dtype == MOE_F32 ? 4 : 2;
+  const int npad = c.n_experts <= 32 ? 32 : 64;
+  return size_t(c.n_experts * c.d_model) * es + size_t(kRouterWarps) * npad * sizeof(float);
+}
+
+bool fused_router_fits(const moe_config& c) {
+  return c.n_experts <= 64 && fused_router_smem(c) <= kFusedRouterSmemLimit;
+}
+
+cudaError_t launch_router_fused(const moe_config& c, const void* x, const void* W_g,
+                                const void* b_g, float* logits, int32_t* topk_idx,
+                                float* topk_w, float* prob_partials, cudaStream_t s) {
+  if (c.T == 0) return cudaSuccess;
+  const unsigned blocks = unsigned(router_partial_rows(c));
+  const size_t smem = fused_router_smem(c);
+  const int T = int(c.T), d = int(c.d_model), N = int(c.n_experts), k = int(c.top_k);
+  const int rn = c.renormalize ? 1 : 0;
+#define MOE_FUSED_CASE(TIN, NPAD)                                                          \
+  {                                                                                        \
+    auto kern = router_fused_kernel<TIN, NPAD>;                                            \
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,  \
+                                         int(smem));                                       \
+    if (e != cudaSuccess) return e;                                                        \
+    kern<<<blocks, kRouterWarps * 32, smem, s>>>(                                          \
+        static_cast<const TIN*>(x), static_cast<const TIN*>(W_g),                          \
+        static_cast<const TIN*>(b_g), T, d, N, k, rn, logits, topk_idx, topk_w,            \
+        prob_partials);                                                                    \
+    return cudaGetLastError();                                                             \
+  }
+  if (c.dtype == MOE_F32) {
+    if (N <= 32) MOE_FUSED_CASE(float, 32)
+    MOE_FUSED_CASE(float, 64)
+  }
+  if (N <= 32) MOE_FUSED_CASE(__nv_bfloat16, 32)
+  MOE_FUSED_CASE(__nv_bfloat16, 64)
+#undef MOE_FUSED_CASE
+}
+
 cudaError_t launch_router_softmax_topk(const moe_config& c, const float* logits,
                                        int32_t* topk_idx, float* topk_w,
                                        float* prob_partials, cudaStream_t s) {
   if (c.T == 0) return cudaSuccess;
   const int N = int(c.n_experts);
-  const unsigned blocks = unsigned(ceil_div(c.T, kRouterTokensPerBlock));
+  const unsigned blocks = unsigned(router_partial_rows(c));
   const size_t smem = size_t(kRouterWarps) * N * sizeof(float);
   const int T = int(c.T), k = int(c.top_k), rn = c.renormalize ? 1 : 0;
 #define MOE_ROUTER_CASE(NPL)                                                              \
@@ -147,6 +368,37 @@ cudaError_t launch_router_softmax_topk(const moe_config& c, const float* logits,
   if (N <= 512) MOE_ROUTER_CASE(16)
   MOE_ROUTER_CASE(32)
 #undef MOE_ROUTER_CASE
+}
+
+}  // namespace moe
+
+namespace moe {
+
+int router_launch_count(const moe_config& c) {
+  if (c.T == 0) return 0;
+  if (c.dtype == MOE_BF16 && c.n_experts % 64 == 0) return 2;
+  return fused_router_fits(c) ? 1 : 2;
+}
+
+// Scores + softmax + top-k for one layer, choosing the kernels by shape:
+// bf16 with N a multiple of 64: the tensor-core GEMM (fp32 scores) then the
+// softmax/top-k kernel; otherwise, when N <= 64 and W_g fits in shared
+// memory, the fused warp-per-token kernel; otherwise the CUDA-core GEMM then
+// the softmax/top-k kernel.
+cudaError_t launch_router(const moe_config& c, const void* x, const void* W_g,
+                          const void* b_g, float* logits, int32_t* topk_idx, float* topk_w,
+                          float* prob_partials, int num_sms, int32_t* status,
+                          uint64_t wait_limit_ns, cudaStream_t s) {
+  if (c.T == 0) return cudaSuccess;
+  cudaError_t e;
+  if (c.dtype == MOE_BF16 && c.n_experts % 64 == 0)
+    e = launch_router_logits_tc(c, x, W_g, b_g, logits, num_sms, status, wait_limit_ns, s);
+  else if (fused_router_fits(c))
+    return launch_router_fused(c, x, W_g, b_g, logits, topk_idx, topk_w, prob_partials, s);
+  else
+    e = launch_router_logits(c, x, W_g, b_g, logits, s);
+  if (e != cudaSuccess) return e;
+  return launch_router_softmax_topk(c, logits, topk_idx, topk_w, prob_partials, s);
 }
 
 }  // namespace moe

@@ -58,6 +58,22 @@ SMALL = [
              act=ACT_RELU, dtype=DT_F32, capacity_factor=1.0, d_ff_shared=96, seed=18),
     Workload("bf16_noreorm", T=400, d_model=128, d_ff=256, n_experts=8, top_k=2,
              act=ACT_GELU_ERF, dtype=DT_BF16, renormalize=0, seed=19),
+    # router paths: tensor-core scores (N % 64 == 0, ragged T), fused kernel
+    # with two experts per lane (32 < N <= 64), CUDA-core GEMM (large fp32 W_g)
+    Workload("bf16_tc_router", T=333, d_model=128, d_ff=128, n_experts=128, top_k=3,
+             act=ACT_GELU_ERF, dtype=DT_BF16, seed=20),
+    Workload("f32_fused_router_npl2", T=97, d_model=96, d_ff=64, n_experts=48, top_k=5,
+             act=ACT_RELU, dtype=DT_F32, seed=22),
+    Workload("f32_simt_router", T=70, d_model=1024, d_ff=64, n_experts=64, top_k=2,
+             act=ACT_GELU_ERF, dtype=DT_F32, seed=23),
+    # more than 32 slots per token: gates written in blocks of 32 lanes
+    Workload("f32_k40_fused", T=50, d_model=64, d_ff=64, n_experts=64, top_k=40,
+             act=ACT_RELU, dtype=DT_F32, seed=25),
+    Workload("bf16_k33_tc_router", T=70, d_model=64, d_ff=64, n_experts=128, top_k=33,
+             act=ACT_GELU_ERF, dtype=DT_BF16, seed=26),
+    # T*k too large for the one-block counting sort: histogram/scan/rank blocks
+    Workload("bf16_multiblock_permute", T=40000, d_model=64, d_ff=64, n_experts=12,
+             top_k=3, act=ACT_RELU, dtype=DT_BF16, capacity_factor=1.05, seed=24),
 ]
 
 
@@ -255,3 +271,38 @@ def test_workload_c4_deepseek_v3_sampled():
     print("parity", wl.name, report)
     del t, layer, out
     torch.cuda.empty_cache()
+
+
+def test_forward_profiled_and_graph_replay_match_forward():
+    """moe_forward_profiled (events at the kernel boundaries), eagerly and
+    captured into a CUDA graph and replayed, gives moe_forward's results bit
+    for bit, and its events time every step."""
+    wl = Workload("graph", T=600, d_model=128, d_ff=256, n_experts=16, top_k=2,
+                  dtype=DT_BF16, capacity_factor=1.3, d_ff_shared=256, seed=36)
+    t, layer, ref = run_layer(wl)
+    cfg = layer.cfg
+    assert B.forward_launch_count(cfg) >= 7
+    stream = torch.cuda.Stream()
+    events = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
+    out = B.alloc_outputs(cfg, "cuda", with_logits=True)
+    with torch.cuda.stream(stream):
+        for ev in events:
+            ev.record(stream)
+        B.forward_profiled(cfg, t["x"], layer.weights, out, layer.workspace, events, stream)
+    stream.synchronize()
+    for name in ("y", "topk_idx", "topk_w", "counts", "kept", "mean_prob", "balance", "logits"):
+        assert torch.equal(getattr(out, name), getattr(ref, name)), name
+    times = [events[i].elapsed_time(events[i + 1]) for i in range(6)]
+    assert all(v > 0 for v in times)
+    graph = torch.cuda.CUDAGraph()
+    out2 = B.alloc_outputs(cfg, "cuda", with_logits=True)
+    with torch.cuda.graph(graph, stream=stream):
+        B.forward_profiled(cfg, t["x"], layer.weights, out2, layer.workspace, events, stream)
+    for _ in range(2):
+        out2.y.zero_()
+        with torch.cuda.stream(stream):
+            graph.replay()
+        stream.synchronize()
+        assert torch.equal(out2.y, ref.y)
+        assert torch.equal(out2.counts, ref.counts)
+        assert events[0].elapsed_time(events[6]) > 0

@@ -55,8 +55,11 @@ def _same(ref, got, cfg):
     assert torch.equal(ref["Xp"][:end][live], got["Xp"][:end][live])
 
 
+# The first layer is large enough that the permute step runs as several
+# blocks and uses the scratch array; the second is small enough for the
+# one-block sort.  Both calls go through moe_permute_noalloc.
 LAYERS = [
-    Workload("noalloc_a", T=1500, d_model=128, d_ff=256, n_experts=16, top_k=2,
+    Workload("noalloc_a", T=40000, d_model=64, d_ff=64, n_experts=40, top_k=3,
              dtype=DT_BF16, capacity_factor=1.1, seed=41),
     Workload("noalloc_b", T=700, d_model=64, d_ff=128, n_experts=40, top_k=4,
              dtype=DT_BF16, d_ff_shared=128, seed=42),
