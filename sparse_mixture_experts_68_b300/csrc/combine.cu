@@ -23,46 +23,50 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
     combine_kernel(const T* __restrict__ Yp, const int32_t* __restrict__ token_row,
                    const float* __restrict__ topk_w, const int32_t* __restrict__ offsets,
                    int Ttok, int k, int N, int has_shared, int64_t d, T* __restrict__ y) {
+  constexpr int V = Vec16<T>::n;
+  constexpr int CB = 4;                            // 16-byte columns per lane per pass
   const int lane = threadIdx.x & 31;
   const int64_t t = int64_t(blockIdx.x) * kCombineWarps + (threadIdx.x >> 5);
   if (t >= Ttok) return;
-  constexpr int V = Vec16<T>::n;
   const int64_t shared_row = has_shared ? int64_t(offsets[N]) + t : -1;
-  // two 16-byte columns per lane per pass: c and c + 32V
-  for (int64_t c = int64_t(lane) * V; c < d; c += 64 * V) {
-    const bool two = c + 32 * V < d;
-    float a0[V], a1[V];
+  const int64_t nv = d / V;
+  for (int64_t c0 = lane; c0 < nv; c0 += 32 * CB) {
+    float acc[CB][V];
 #pragma unroll
-    for (int i = 0; i < V; ++i) a0[i] = a1[i] = 0.f;
-    for (int j = 0; j < k; ++j) {
-      const int32_t r = token_row[t * k + j];
+    for (int b = 0; b < CB; ++b)
+#pragma unroll
+      for (int i = 0; i < V; ++i) acc[b][i] = 0.f;
+    for (int j = 0; j <= k; ++j) {
+      int64_t r;
+      float g;
+      if (j < k) {
+        r = token_row[t * k + j];
+        g = topk_w[t * k + j];
+      } else {
+        r = shared_row;                            // the shared expert, weight 1
+        g = 1.f;
+      }
       if (r < 0) continue;
-      const float g = topk_w[t * k + j];
-      float v0[V], v1[V];
-      const T* row = Yp + int64_t(r) * d + c;
-      Vec16<T>::load(row, v0);
-      if (two) Vec16<T>::load(row + 32 * V, v1);
+      const uint4* row = reinterpret_cast<const uint4*>(Yp + r * d);
+      uint4 q[CB];
 #pragma unroll
-      for (int i = 0; i < V; ++i) a0[i] = fmaf(g, v0[i], a0[i]);
-      if (two) {
+      for (int b = 0; b < CB; ++b) {
+        const int64_t c = c0 + 32 * b;
+        q[b] = c < nv ? __ldg(row + c) : make_uint4(0, 0, 0, 0);
+      }
 #pragma unroll
-        for (int i = 0; i < V; ++i) a1[i] = fmaf(g, v1[i], a1[i]);
+      for (int b = 0; b < CB; ++b) {
+        float v[V];
+        Vec16<T>::load(reinterpret_cast<const T*>(&q[b]), v);
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc[b][i] = fmaf(g, v[i], acc[b][i]);
       }
     }
-    if (shared_row >= 0) {
-      float v0[V], v1[V];
-      const T* row = Yp + shared_row * d + c;
-      Vec16<T>::load(row, v0);
-      if (two) Vec16<T>::load(row + 32 * V, v1);
 #pragma unroll
-      for (int i = 0; i < V; ++i) a0[i] += v0[i];
-      if (two) {
-#pragma unroll
-        for (int i = 0; i < V; ++i) a1[i] += v1[i];
-      }
+    for (int b = 0; b < CB; ++b) {
+      const int64_t c = c0 + 32 * b;
+      if (c < nv) Vec16<T>::store(y + t * d + c * V, acc[b]);
     }
-    Vec16<T>::store(y + t * d + c, a0);
-    if (two) Vec16<T>::store(y + t * d + c + 32 * V, a1);
   }
 }
 

@@ -454,6 +454,315 @@ __global__ void __launch_bounds__(CFG::THREADS, MINB)
   }
 }
 
+// ---- CTA-pair variant (tcgen05 cta_group::2) ---------------------------------------------
+//
+// A 256 x BN output tile is computed by a cluster of two CTAs on two SMs.
+// Each CTA TMA-loads its own 128 rows of A and its half of the BN rows of B,
+// so each SM's shared memory holds (and its tensor core reads) half of B: per
+// k-block a CTA moves 32 KB through shared memory instead of 48 KB for the
+// same tensor work, which is what lets the MMA run near its peak rate.  The
+// even CTA of the pair issues the M=256 MMAs (cta_group::2); accumulator
+// rows 0-127 land in its TMEM, rows 128-255 in the odd CTA's.  Barriers: the
+// even CTA's "full" barrier counts both CTAs' arrivals and bytes; MMA commits
+// are multicast to both CTAs' "empty" and "accumulator full" barriers; both
+// CTAs' epilogue warps arrive on the even CTA's "accumulator empty" barrier.
+
+template <int BN, int STAGES>
+struct Layout2 {
+  static constexpr int kABytes = 128 * BK * 2;          // this CTA's 128 rows of A
+  static constexpr int kBBytes = (BN / 2) * BK * 2;     // this CTA's half of B
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kA = 0;
+  static constexpr int kB = STAGES * kABytes;
+  static constexpr int kBar = kB + STAGES * kBBytes;
+  static constexpr int kNumBars = 2 * STAGES + 5;
+  static constexpr int kTmemSlot = kBar + kNumBars * 8;
+  static constexpr int kAbort = kTmemSlot + 4;
+  static constexpr int kTileStart = (kAbort + 4 + 15) / 16 * 16;
+  static constexpr int kGroupOff = kTileStart + (kMaxGroups + 1) * 4;
+  static constexpr int kBytes = kGroupOff + kMaxGroups * 4;
+  static constexpr int kAlloc = kBytes + 1024;
+  static_assert(kAlloc <= 227 * 1024, "shared memory budget");
+};
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t nclusters_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+
+// Address of the same shared variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t peer_addr(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t bar_cluster, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cluster.b64 _, [%0], %1;" ::"r"(
+                   bar_cluster),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+               : "memory");
+}
+
+__device__ __forceinline__ void tma2_load_2d(const CUtensorMap* map, uint32_t dst, uint32_t bar,
+                                             int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma2_load_3d(const CUtensorMap* map, uint32_t dst, uint32_t bar,
+                                             int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc2_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+
+// Arrives on the barrier at the same offset in both CTAs of the pair once all
+// MMAs issued so far by this thread have completed.
+__device__ __forceinline__ void tc2_commit_both(uint32_t bar) {
+  const uint16_t mask = 0x3;
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+
+template <int BN>
+__host__ __device__ constexpr uint32_t idesc2_bf16_f32() {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(BN >> 3) << 17) |
+         (uint32_t(256 >> 4) << 24);
+}
+
+template <class CFG, int EPI>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CFG::THREADS, 1)
+    tc2_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                            const __grid_constant__ CUtensorMap tmB,
+                            const __grid_constant__ CUtensorMap tmBs, const TcParams p) {
+  constexpr int BN = CFG::BN;
+  constexpr int kStages = CFG::STAGES;
+  constexpr int kEpiWarps = CFG::EPI_WARPS;
+  constexpr int BM2 = 256;
+  using L = Layout2<BN, kStages>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint64_t* full = bars;                       // used in CTA 0: both CTAs' loads
+  uint64_t* empty = bars + kStages;            // per CTA: its ring slot is free
+  uint64_t* tfull = bars + 2 * kStages;        // per CTA: accumulator ready
+  uint64_t* tempty = bars + 2 * kStages + 2;   // used in CTA 0: both epilogues done
+  uint64_t* done = bars + 2 * kStages + 4;     // CTA 0: all MMAs complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
+  int32_t* tile_start = reinterpret_cast<int32_t*>(smem + L::kTileStart);
+  int32_t* grp_off = reinterpret_cast<int32_t*>(smem + L::kGroupOff);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const int pair = int(cluster_id_x()), npairs = int(nclusters_x());
+  const int n_groups = p.offsets ? p.n_routed + (p.shared_rows > 0 ? 1 : 0) : 1;
+  const int ntiles = int(p.Nd / BN);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 2);                  // one arrival per CTA, with its bytes
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 2 * kEpiWarps);    // every epilogue warp of both CTAs
+    }
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    __syncwarp();
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(2 * BN));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
+  }
+  if (warp == 2) {
+    int32_t carry = 0;
+    for (int base = 0; base < n_groups; base += 32) {
+      const int g = base + lane;
+      int32_t live = 0, off = 0;
+      if (g < n_groups) {
+        if (p.offsets) {
+          off = p.offsets[g];
+          live = g < p.n_routed ? p.kept[g] : p.shared_rows;
+        } else {
+          live = p.dense_rows;
+        }
+        grp_off[g] = off;
+      }
+      const int32_t tiles = int32_t((live + BM2 - 1) / BM2) * ntiles;
+      int32_t incl = tiles;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (g < n_groups) tile_start[g] = carry + incl - tiles;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) tile_start[n_groups] = carry;
+  }
+  tc_fence_before();
+  cluster_sync_all();                          // barriers of both CTAs are initialised
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total_tiles = tile_start[n_groups];
+
+  if (warp == 0) {
+    // ---------------- TMA producer (both CTAs) ----------------
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < total_tiles; tile += npairs) {
+        const TileCoord tc = decode_tile(tile, tile_start, n_groups, ntiles);
+        const int row0 = grp_off[tc.g] + tc.m * BM2 + int(rank) * 128;
+        const int col0 = tc.n * BN + int(rank) * (BN / 2);
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!wait_or_abort(&empty[stage], phase ^ 1u, p, abort_flag)) { ok = false; break; }
+          const uint32_t fb = peer_addr(smem_u32(&full[stage]), 0);
+          mbar_arrive_expect_tx_cluster(fb, L::kStageBytes);
+          tma2_load_2d(&tmA, smem_u32(smem + L::kA + stage * L::kABytes), fb, kb * BK, row0);
+          if (tc.g < p.n_routed)
+            tma2_load_3d(&tmB, smem_u32(smem + L::kB + stage * L::kBBytes), fb, kb * BK, col0,
+                         tc.g);
+          else
+            tma2_load_2d(&tmBs, smem_u32(smem + L::kB + stage * L::kBBytes), fb, kb * BK, col0);
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (CTA 0 of the pair) ----------------
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = idesc2_bf16_f32<BN>();
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < total_tiles; tile += npairs) {
+        if (!wait_or_abort(&tempty[acc], acc_phase ^ 1u, p, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!wait_or_abort(&full[stage], phase, p, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t ad = sdesc_sw128(smem_u32(smem + L::kA + stage * L::kABytes));
+          const uint64_t bd = sdesc_sw128(smem_u32(smem + L::kB + stage * L::kBBytes));
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            tc2_mma(d_tmem, ad + uint64_t(2 * kk), bd + uint64_t(2 * kk), idesc,
+                    (kb | kk) != 0 ? 1u : 0u);
+          tc2_commit_both(smem_u32(&empty[stage]));
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc2_commit_both(smem_u32(&tfull[acc]));
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      asm volatile(
+          "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+              smem_u32(done))
+          : "memory");
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_try_wait(smem_u32(done), 0) && global_timer_ns() - t0 < p.wait_limit_ns) {
+      }
+    }
+  } else {
+    // ---------------- epilogue (both CTAs) ----------------
+    const int q = warp & 3;
+    const int part = (warp - 2) >> 2;
+    constexpr int kCols = BN / (kEpiWarps / 4);
+    constexpr int CW = kCols < 32 ? kCols : 32;
+    const uint32_t tempty0 = peer_addr(smem_u32(&tempty[0]), 0);
+    const uint32_t tempty1 = peer_addr(smem_u32(&tempty[1]), 0);
+    uint32_t acc = 0, acc_phase = 0;
+    for (int tile = pair; tile < total_tiles; tile += npairs) {
+      const TileCoord tc = decode_tile(tile, tile_start, n_groups, ntiles);
+      bool ok = true;
+      if (lane == 0) ok = wait_or_abort(&tfull[acc], acc_phase, p, abort_flag);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      tc_fence_after();
+      const bool routed = tc.g < p.n_routed;
+      const int live = p.offsets ? (routed ? p.kept[tc.g] : p.shared_rows) : p.dense_rows;
+      const int row_in_group = tc.m * BM2 + int(rank) * 128 + q * 32 + lane;
+      const bool valid = row_in_group < live;
+      const int64_t out_row = int64_t(grp_off[tc.g]) + row_in_group;
+      const __nv_bfloat16* bias = routed ? p.bias + int64_t(tc.g) * p.Nd : p.bias_s;
+      constexpr int kOutBytes = EPI == EPI_BIAS_F32 ? 4 : 2;
+#pragma unroll 1
+      for (int c = part * kCols; c < (part + 1) * kCols; c += CW) {
+        uint32_t r[CW];
+        tmem_ld_cols<CW>(tmem_base + (uint32_t(q * 32) << 16) + acc * BN + c, r);
+        if (valid) {
+          const int64_t col = int64_t(tc.n) * BN + c;
+          epilogue_store<EPI, CW>(r, bias + col,
+                                  static_cast<uint8_t*>(p.out) +
+                                      (out_row * p.Nd + col) * kOutBytes);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acc ? tempty1 : tempty0);
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncwarp();
+  cluster_sync_all();       // every remote arrive and every MMA of the pair has landed
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(2 * BN));
+  }
+}
+
 // ---- host side -----------------------------------------------------------------------
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -508,24 +817,75 @@ cudaError_t launch_epi(int epi, const CUtensorMap& A, const CUtensorMap& B,
 }
 
 // The kernel variants this library instantiates.
-enum TileChoice { TILE_256 = 0, TILE_128 = 1, TILE_64 = 2, TILE_128_2CTA = 3, NUM_TILES };
+enum TileChoice {
+  TILE_256 = 0, TILE_128 = 1, TILE_64 = 2, TILE_128_2CTA = 3, TILE_256_PAIR = 4, NUM_TILES
+};
 using Cfg256 = TileCfg<256, 4, 16>;        // one CTA per SM, 192 KB ring
 using Cfg128 = TileCfg<128, 4, 16>;
 using Cfg64 = TileCfg<64, 6, 16>;
 using Cfg128x2 = TileCfg<128, 3, 8>;       // two CTAs per SM, 96 KB ring each
+using Cfg256Pair = TileCfg<256, 6, 16>;    // CTA pair, 256 x 256 tiles, 6 x 32 KB ring per CTA
 
 int tile_bn(int choice) {
   switch (choice) {
-    case TILE_256: return 256;
+    case TILE_256: case TILE_256_PAIR: return 256;
     case TILE_64: return 64;
     default: return 128;
   }
 }
 
+int tile_rows(int choice) { return choice == TILE_256_PAIR ? 256 : BM; }
 int tile_ctas_per_sm(int choice) { return choice == TILE_128_2CTA ? 2 : 1; }
 
+template <class CFG, int EPI>
+cudaError_t launch_pair(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& Bs,
+                        const TcParams& p, int64_t tiles, int num_sms, cudaStream_t s) {
+  constexpr int smem = Layout2<CFG::BN, CFG::STAGES>::kAlloc;
+  auto kern = tc2_grouped_gemm_kernel<CFG, EPI>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  // CTA pairs that can be resident at once (pairs sit on two SMs of one GPC)
+  static int max_pairs[64] = {};
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (max_pairs[dev] == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(num_sms & ~1));
+    cfg.blockDim = dim3(CFG::THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    max_pairs[dev] = n > 0 ? n : 1;
+  }
+  const int64_t pairs = tiles < max_pairs[dev] ? tiles : max_pairs[dev];
+  if (pairs <= 0) return cudaSuccess;
+  kern<<<unsigned(2 * pairs), CFG::THREADS, smem, s>>>(A, B, Bs, p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_choice(int choice, int epi, const CUtensorMap& A, const CUtensorMap& B,
-                          const CUtensorMap& Bs, const TcParams& p, int grid, cudaStream_t s) {
+                          const CUtensorMap& Bs, const TcParams& p, int64_t max_tiles,
+                          int num_sms, cudaStream_t s) {
+  if (choice == TILE_256_PAIR) {
+    if (epi == EPI_BIAS_GELU)
+      return launch_pair<Cfg256Pair, EPI_BIAS_GELU>(A, B, Bs, p, max_tiles, num_sms, s);
+    if (epi == EPI_BIAS_RELU)
+      return launch_pair<Cfg256Pair, EPI_BIAS_RELU>(A, B, Bs, p, max_tiles, num_sms, s);
+    return launch_pair<Cfg256Pair, EPI_BIAS>(A, B, Bs, p, max_tiles, num_sms, s);
+  }
+  const int64_t slots = int64_t(num_sms) * tile_ctas_per_sm(choice);
+  const int grid = int(max_tiles < slots ? max_tiles : slots);
+  if (grid <= 0) return cudaSuccess;
   switch (choice) {
     case TILE_256: return launch_epi<Cfg256>(epi, A, B, Bs, p, grid, s);
     case TILE_128: return launch_epi<Cfg128>(epi, A, B, Bs, p, grid, s);
@@ -534,9 +894,12 @@ cudaError_t launch_choice(int choice, int epi, const CUtensorMap& A, const CUten
   }
 }
 
-// Tile variant for one grouped Linear with output width Nd: the widest tile
-// that divides Nd (256-wide tiles load the least shared memory per MMA).
-int pick_tile(int64_t Nd) {
+// Tile variant for one grouped Linear with output width Nd and rows_per_group
+// rows in an average expert group: CTA-pair 256 x 256 tiles when the groups
+// fill them (half the shared-memory traffic per MMA); otherwise the widest
+// single-CTA tile that divides Nd.
+int pick_tile(int64_t Nd, int64_t rows_per_group) {
+  if (Nd % 256 == 0 && rows_per_group >= 256) return TILE_256_PAIR;
   if (Nd % 256 == 0) return TILE_256;
   if (Nd % 128 == 0) return TILE_128;
   return TILE_64;
@@ -547,15 +910,19 @@ cudaError_t grouped_linear(const moe_config& c, const GroupedFfnArgs& g, const v
                            const void* W, const void* Ws, const void* bias,
                            const void* bias_s, void* out, int64_t K, int64_t Nd, int epi,
                            cudaStream_t s) {
-  const int choice = pick_tile(Nd);
+  const int64_t groups = c.n_experts + (c.d_ff_shared > 0 ? 1 : 0);
+  const int64_t rows = c.T * c.top_k + (c.d_ff_shared > 0 ? c.T : 0);
+  const int choice = pick_tile(Nd, rows / groups);
   const int bn = tile_bn(choice);
+  // the CTA pair loads half of each B tile per CTA
+  const uint32_t b_box = uint32_t(choice == TILE_256_PAIR ? bn / 2 : bn);
   const int64_t N = c.n_experts;
   CUtensorMap mA, mB, mBs;
   if (!make_map(&mA, A, uint64_t(K), uint64_t(g.rows_max), 0, BM)) return cudaErrorInvalidValue;
-  if (!make_map(&mB, W, uint64_t(K), uint64_t(Nd), uint64_t(N), uint32_t(bn)))
+  if (!make_map(&mB, W, uint64_t(K), uint64_t(Nd), uint64_t(N), b_box))
     return cudaErrorInvalidValue;
   if (c.d_ff_shared > 0) {
-    if (!make_map(&mBs, Ws, uint64_t(K), uint64_t(Nd), 0, uint32_t(bn)))
+    if (!make_map(&mBs, Ws, uint64_t(K), uint64_t(Nd), 0, b_box))
       return cudaErrorInvalidValue;
   } else {
     mBs = mB;
@@ -572,11 +939,10 @@ cudaError_t grouped_linear(const moe_config& c, const GroupedFfnArgs& g, const v
   p.num_kb = int32_t(K / BK);
   p.status = g.status;
   p.wait_limit_ns = g.wait_limit_ns;
-  const int64_t max_tiles = ceil_div(g.rows_max, BM) * (Nd / bn);
-  const int64_t slots = int64_t(g.num_sms) * tile_ctas_per_sm(choice);
-  const int grid = int(max_tiles < slots ? max_tiles : slots);
-  if (grid <= 0) return cudaSuccess;
-  return launch_choice(choice, epi, mA, mB, mBs, p, grid, s);
+  // upper bound on the tiles (every group may add one partial m-tile)
+  const int64_t max_tiles =
+      (ceil_div(g.rows_max, tile_rows(choice)) + groups) * (Nd / bn);
+  return launch_choice(choice, epi, mA, mB, mBs, p, max_tiles, g.num_sms, s);
 }
 
 }  // namespace

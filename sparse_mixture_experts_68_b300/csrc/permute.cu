@@ -165,9 +165,29 @@ __global__ void __launch_bounds__(kSortWarps * 32)
   int16_t* ids = reinterpret_cast<int16_t*>(warp_tot + 32);   // [A]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < kSortWarps * N; i += blockDim.x) cnt[i] = 0;
-  for (int a = threadIdx.x; a < A; a += blockDim.x) {
-    const int e = topk_idx[a];
-    ids[a] = int16_t((e >= 0 && e < N) ? e : -1);   // out-of-range experts: dropped
+  {
+    // stage the expert ids: 16-byte loads, four in flight per thread
+    auto clamp = [N](int e) { return int16_t((e >= 0 && e < N) ? e : -1); };  // out of range: dropped
+    const int A4 = A / 4;
+    const int4* src = reinterpret_cast<const int4*>(topk_idx);
+    int i = threadIdx.x;
+    for (; i + 3 * int(blockDim.x) < A4; i += 4 * blockDim.x) {
+      int4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = __ldg(src + i + u * blockDim.x);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int a = 4 * (i + u * int(blockDim.x));
+        ids[a] = clamp(v[u].x); ids[a + 1] = clamp(v[u].y);
+        ids[a + 2] = clamp(v[u].z); ids[a + 3] = clamp(v[u].w);
+      }
+    }
+    for (; i < A4; i += blockDim.x) {
+      const int4 v = __ldg(src + i);
+      const int a = 4 * i;
+      ids[a] = clamp(v.x); ids[a + 1] = clamp(v.y); ids[a + 2] = clamp(v.z); ids[a + 3] = clamp(v.w);
+    }
+    for (int a = 4 * A4 + int(threadIdx.x); a < A; a += blockDim.x) ids[a] = clamp(topk_idx[a]);
   }
   __syncthreads();
   const int L = (A + kSortWarps - 1) / kSortWarps;
@@ -289,10 +309,12 @@ __global__ void __launch_bounds__(256)
     uint4* dst = reinterpret_cast<uint4*>(Xp + r * d);
     const int64_t nv = d / V;
     int64_t i = lane;
-    for (; i + 96 < nv; i += 128) {                 // four 16-byte loads in flight
-      const uint4 a0 = __ldg(src + i), a1 = __ldg(src + i + 32), a2 = __ldg(src + i + 64),
-                  a3 = __ldg(src + i + 96);
-      dst[i] = a0; dst[i + 32] = a1; dst[i + 64] = a2; dst[i + 96] = a3;
+    for (; i + 7 * 32 < nv; i += 8 * 32) {          // eight 16-byte loads in flight
+      uint4 a[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) a[u] = __ldg(src + i + 32 * u);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) dst[i + 32 * u] = a[u];
     }
     for (; i < nv; i += 32) dst[i] = __ldg(src + i);
   }

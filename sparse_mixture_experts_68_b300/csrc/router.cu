@@ -135,24 +135,27 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
 }
 
 // Fused router for small expert counts (N <= 64) whose W_g fits in shared
-// memory: one warp per token computes all N scores (lanes split d in 16-byte
-// vectors against W_g staged in shared memory), reduce-scatters them across
-// the warp so lane l holds experts [l*NPL, (l+1)*NPL), then takes the softmax,
-// the top-k and the gates as above.  One pass over x, no score round trip.
-template <typename TIn, int NPAD>
+// memory.  One warp per token: lanes split d in 16-byte vectors (up to 16 of
+// them loaded at once) against W_g staged in shared memory, padded with zero
+// rows to NE experts (8, 16, 32 or 64).  A butterfly reduce-scatter then
+// leaves each expert's score in DUP = 32/NE adjacent lanes (NE <= 32) or two
+// experts per lane (NE = 64); the softmax, the top-k and the gates follow as
+// above.  One pass over x, no score round trip.
+template <typename TIn, int NE>
 __global__ void __launch_bounds__(kRouterWarps * 32)
     router_fused_kernel(const TIn* __restrict__ x, const TIn* __restrict__ W_g,
                         const TIn* __restrict__ b_g, int T, int d, int N, int k, int renorm,
                         float* __restrict__ logits, int32_t* __restrict__ topk_idx,
                         float* __restrict__ topk_w, float* __restrict__ prob_partials) {
   constexpr int V = Vec16<TIn>::n;
-  constexpr int NPL = NPAD / 32;
-  extern __shared__ uint4 wsm[];                 // W_g [N][d], then partial sums
-  const int dv = d / V;                          // 16-byte vectors per row
-  const int nvec = N * dv;
+  constexpr int NPL = NE > 32 ? NE / 32 : 1;          // experts per lane after the reduce
+  constexpr int DUP = NE < 32 ? 32 / NE : 1;          // lanes holding the same expert
+  constexpr int kBatch = NE <= 16 ? 16 : (NE == 32 ? 8 : 2);   // 16-byte x loads in flight
+  extern __shared__ uint4 wsm[];                      // W_g [NE][d] (zero rows), then sums
+  const int dv = d / V;
+  const int nvec = N * dv, nvec_pad = NE * dv;
   const uint4* wsrc = reinterpret_cast<const uint4*>(W_g);
   {
-    // four independent loads in flight per thread
     int i = threadIdx.x;
     for (; i + 3 * int(blockDim.x) < nvec; i += 4 * blockDim.x) {
       const uint4 a0 = __ldg(wsrc + i), a1 = __ldg(wsrc + i + blockDim.x),
@@ -161,69 +164,76 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
       wsm[i + 3 * blockDim.x] = a3;
     }
     for (; i < nvec; i += blockDim.x) wsm[i] = __ldg(wsrc + i);
+    for (int j = nvec + int(threadIdx.x); j < nvec_pad; j += blockDim.x)
+      wsm[j] = make_uint4(0, 0, 0, 0);
   }
-  float* red = reinterpret_cast<float*>(wsm + nvec);   // [kRouterWarps][NPAD]
+  float* red = reinterpret_cast<float*>(wsm + nvec_pad);   // [kRouterWarps][NE]
   __syncthreads();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int kTokPerWarp = kRouterTokensPerBlock / kRouterWarps;
+  // experts held by this lane after the reduce: e0 .. e0 + NPL - 1
+  const int e0 = NE > 32 ? lane * NPL : lane / DUP;
+  const bool owner = (lane % DUP) == 0;               // one lane per expert writes
   float psum[NPL];
 #pragma unroll
   for (int i = 0; i < NPL; ++i) psum[i] = 0.f;
 
   const int groups = (T + kRouterTokensPerBlock - 1) / kRouterTokensPerBlock;
-  for (int grp = blockIdx.x; grp < groups; grp += gridDim.x)
-  for (int q = 0; q < kTokPerWarp; ++q) {
-    const int t = grp * kRouterTokensPerBlock + warp * kTokPerWarp + q;
+  for (int grp = blockIdx.x; grp < groups; grp += gridDim.x) {
+    const int t = grp * kRouterTokensPerBlock + warp;
     if (t >= T) break;
-    float acc[NPAD];
+    float acc[NE];
 #pragma unroll
-    for (int e = 0; e < NPAD; ++e) acc[e] = 0.f;
+    for (int e = 0; e < NE; ++e) acc[e] = 0.f;
     const uint4* xr = reinterpret_cast<const uint4*>(x + int64_t(t) * d);
-    // x is read once: up to four 16-byte loads per lane in flight
-    for (int c0 = lane; c0 < dv; c0 += 4 * 32) {
-      uint4 xq[4];
+    for (int c0 = lane; c0 < dv; c0 += kBatch * 32) {
+      uint4 xq[kBatch];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < kBatch; ++u) {
         const int c = c0 + 32 * u;
         xq[u] = c < dv ? __ldg(xr + c) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < kBatch; ++u) {
         const int c = c0 + 32 * u;
         if (c >= dv) break;
         float xv[V];
         Vec16<TIn>::load(reinterpret_cast<const TIn*>(&xq[u]), xv);
 #pragma unroll
-        for (int e = 0; e < NPAD; ++e) {
-          if (e < N) {
-            float wv[V];
-            Vec16<TIn>::load(reinterpret_cast<const TIn*>(wsm + e * dv + c), wv);
+        for (int e = 0; e < NE; ++e) {
+          float wv[V];
+          Vec16<TIn>::load(reinterpret_cast<const TIn*>(wsm + e * dv + c), wv);
 #pragma unroll
-            for (int i = 0; i < V; ++i) acc[e] = fmaf(xv[i], wv[i], acc[e]);
-          }
+          for (int i = 0; i < V; ++i) acc[e] = fmaf(xv[i], wv[i], acc[e]);
         }
       }
     }
-    // reduce-scatter: after the step with offset o, a lane keeps the half of
-    // its current range selected by bit o of its lane id
+    // reduce-scatter while more than NPL values remain, then all-reduce
+    // across the DUP lanes that share an expert
+    constexpr int kRsSteps = NE > 32 ? 5 : (NE == 32 ? 5 : (NE == 16 ? 4 : 3));
 #pragma unroll
-    for (int o = 16, S = NPAD; o >= 1; o >>= 1, S >>= 1) {
-      const bool upper = (lane & o) != 0;
+    for (int step = 0; step < 5; ++step) {
+      const int o = 16 >> step;
+      if (step < kRsSteps) {
+        const int S = NE >> step;                     // values still held per lane
+        const bool upper = (lane & o) != 0;
 #pragma unroll
-      for (int i = 0; i < S / 2; ++i) {
-        const float send = upper ? acc[i] : acc[i + S / 2];
-        const float keep = upper ? acc[i + S / 2] : acc[i];
-        acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        for (int i = 0; i < S / 2; ++i) {
+          const float send = upper ? acc[i] : acc[i + S / 2];
+          const float keep = upper ? acc[i + S / 2] : acc[i];
+          acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+      } else {
+        acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], o);
       }
     }
     float z[NPL];
     float m = -FLT_MAX;
 #pragma unroll
     for (int i = 0; i < NPL; ++i) {
-      const int e = lane * NPL + i;
+      const int e = e0 + i;
       z[i] = e < N ? acc[i] + to_f32(b_g[e]) : -INFINITY;
-      if (e < N) logits[int64_t(t) * N + e] = z[i];
+      if (e < N && owner) logits[int64_t(t) * N + e] = z[i];
       m = fmaxf(m, z[i]);
     }
 #pragma unroll
@@ -231,8 +241,8 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
     float ex[NPL], ssum = 0.f;
 #pragma unroll
     for (int i = 0; i < NPL; ++i) {
-      ex[i] = (lane * NPL + i < N) ? expf(z[i] - m) : 0.f;
-      ssum += ex[i];
+      ex[i] = (e0 + i < N) ? expf(z[i] - m) : 0.f;
+      if (owner) ssum += ex[i];
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
@@ -240,7 +250,7 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
 #pragma unroll
     for (int i = 0; i < NPL; ++i) psum[i] += ex[i] * inv;
 
-    uint32_t taken = 0;
+    uint32_t taken = 0;                                // bit i: expert e0 + i selected
     float kept_sum = 0.f;
     int my_e = 0;
     float my_g = 0.f;
@@ -251,7 +261,7 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
       int be = 0x7fffffff;
 #pragma unroll
       for (int i = 0; i < NPL; ++i) {
-        const int e = lane * NPL + i;
+        const int e = e0 + i;
         if (e < N && !((taken >> i) & 1u) && (z[i] > bv || (z[i] == bv && e < be))) {
           bv = z[i];
           be = e;
@@ -263,7 +273,7 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
         const int oe = __shfl_xor_sync(0xffffffffu, be, o);
         if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
       }
-      if (be / NPL == lane) taken |= 1u << (be % NPL);
+      if (be >= e0 && be < e0 + NPL) taken |= 1u << (be - e0);
       const float g = expf(bv - m);
       kept_sum += g;
       if (lane == (j & 31)) { my_e = be; my_g = g; }   // slot j is held by lane j % 32
@@ -275,7 +285,6 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
         }
       }
     }
-    // gate = exp(z - max) / (sum over the kept k), or / (sum over all N)
     const float scale = renorm ? 1.0f / kept_sum : inv;
     if (k <= 32) {
       if (lane < k) {
@@ -283,29 +292,31 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
         out_w[lane] = my_g * scale;
       }
     } else {
-      for (int j = lane; j < k; j += 32) out_w[j] *= scale;  // each lane rescales its own writes
+      for (int j = lane; j < k; j += 32) out_w[j] *= scale;
     }
   }
 
 #pragma unroll
   for (int i = 0; i < NPL; ++i) {
-    const int e = lane * NPL + i;
-    if (e < N) red[warp * NPAD + e] = psum[i];
+    const int e = e0 + i;
+    if (e < N && owner) red[warp * NE + e] = psum[i];
   }
   __syncthreads();
   for (int e = threadIdx.x; e < N; e += blockDim.x) {
     float v = 0.f;
-    for (int w = 0; w < kRouterWarps; ++w) v += red[w * NPAD + e];
+    for (int w = 0; w < kRouterWarps; ++w) v += red[w * NE + e];
     prob_partials[int64_t(blockIdx.x) * N + e] = v;
   }
 }
+
+int fused_ne(int64_t n) { return n <= 8 ? 8 : n <= 16 ? 16 : n <= 32 ? 32 : 64; }
 
 constexpr size_t kFusedRouterSmemLimit = 200 * 1024;
 
 size_t fused_router_smem(const moe_config& c) {
   const size_t es = c.dtype == MOE_F32 ? 4 : 2;
-  const int npad = c.n_experts <= 32 ? 32 : 64;
-  return size_t(c.n_experts * c.d_model) * es + size_t(kRouterWarps) * npad * sizeof(float);
+  const int ne = fused_ne(c.n_experts);
+  return size_t(ne * c.d_model) * es + size_t(kRouterWarps) * ne * sizeof(float);
 }
 
 bool fused_router_fits(const moe_config& c) {
@@ -333,9 +344,13 @@ cudaError_t launch_router_fused(const moe_config& c, const void* x, const void* 
     return cudaGetLastError();                                                             \
   }
   if (c.dtype == MOE_F32) {
+    if (N <= 8) MOE_FUSED_CASE(float, 8)
+    if (N <= 16) MOE_FUSED_CASE(float, 16)
     if (N <= 32) MOE_FUSED_CASE(float, 32)
     MOE_FUSED_CASE(float, 64)
   }
+  if (N <= 8) MOE_FUSED_CASE(__nv_bfloat16, 8)
+  if (N <= 16) MOE_FUSED_CASE(__nv_bfloat16, 16)
   if (N <= 32) MOE_FUSED_CASE(__nv_bfloat16, 32)
   MOE_FUSED_CASE(__nv_bfloat16, 64)
 #undef MOE_FUSED_CASE

@@ -66,6 +66,9 @@ SMALL = [
              act=ACT_RELU, dtype=DT_F32, seed=22),
     Workload("f32_simt_router", T=70, d_model=1024, d_ff=64, n_experts=64, top_k=2,
              act=ACT_GELU_ERF, dtype=DT_F32, seed=23),
+    # groups of >= 256 rows: the CTA-pair 256 x 256 tiles, with a shared expert
+    Workload("bf16_pair_shared", T=700, d_model=128, d_ff=256, n_experts=2, top_k=2,
+             act=ACT_GELU_ERF, dtype=DT_BF16, d_ff_shared=256, seed=27),
     # more than 32 slots per token: gates written in blocks of 32 lanes
     Workload("f32_k40_fused", T=50, d_model=64, d_ff=64, n_experts=64, top_k=40,
              act=ACT_RELU, dtype=DT_F32, seed=25),
