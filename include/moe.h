@@ -233,6 +233,8 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* 
  *   events[1] after the router        events[5] after the combine
  *   events[2] after the permutation   events[6] after the statistics
  *   events[3] after the first Linear (H)
+ * (when the permutation runs as a single block it also computes the
+ * statistics, and events[5] and events[6] then bracket no work) 
  * A NULL entry is skipped.  While `stream` is being captured into a CUDA
  * graph, the events become external event-record nodes, so every replay of
  * the graph records them.  Otherwise identical to moe_forward. */
@@ -251,6 +253,14 @@ size_t moe_host_workspace_size(const moe_config* cfg);
 moe_status moe_forward_host(const moe_config* cfg, const void* x_host, const moe_weights* w,
                             const moe_outputs* out_host, void* workspace,
                             size_t workspace_bytes, void* stream);
+
+/* The expert activation exactly as the FFN kernels evaluate it, applied
+ * elementwise to n fp32 values (device pointers): y[i] = act(x[i]).  GELU is
+ * the exact erf form, 0.5 x (1 + erf(x / sqrt 2)) (botmartz.com "Expert
+ * Routing": nn.GELU()), with erf evaluated by Abramowitz & Stegun's formula
+ * 7.1.26 (absolute error <= 1.5e-7); ReLU is max(x, 0) (codingnowai.in
+ * "Code").  Lets callers check the activation against other implementations. */
+moe_status moe_activation(int32_t act, const float* x, float* y, int64_t n, void* stream);
 
 /* ---- status ---------------------------------------------------------------- */
 

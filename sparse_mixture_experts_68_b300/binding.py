@@ -30,7 +30,7 @@ EXPORTS = [
     "moe_forward", "moe_host_workspace_size", "moe_forward_host", "moe_get_device_status",
     "moe_set_wait_limit_ns", "moe_get_wait_limit_ns", "moe_selftest_bounded_wait",
     "moe_status_string", "moe_version", "moe_permute_noalloc", "moe_forward_profiled",
-    "moe_forward_launch_count",
+    "moe_forward_launch_count", "moe_activation",
 ]
 PERMUTE_STATIC_SCRATCH_INTS = 1 << 18
 
@@ -97,6 +97,7 @@ def lib() -> C.CDLL:
         "moe_set_wait_limit_ns": (None, [C.c_uint64]),
         "moe_get_wait_limit_ns": (C.c_uint64, []),
         "moe_selftest_bounded_wait": (C.c_int32, [C.c_uint64, P]),
+        "moe_activation": (C.c_int32, [C.c_int32, P, P, C.c_int64, P]),
         "moe_status_string": (C.c_char_p, [C.c_int32]),
         "moe_version": (C.c_int32, []),
     }
@@ -215,6 +216,12 @@ def set_wait_limit_ns(ns: int):
 
 def get_wait_limit_ns() -> int:
     return int(lib().moe_get_wait_limit_ns())
+
+
+def activation(act: int, x, y, stream=None):
+    """The FFN kernels' activation applied elementwise (fp32 device tensors)."""
+    _check(lib().moe_activation(int(act), _ptr(x), _ptr(y), x.numel(), _stream(stream)),
+           "moe_activation")
 
 
 def selftest_bounded_wait(limit_ns: int, stream=None):

@@ -141,6 +141,13 @@ __global__ void bounded_wait_selftest_kernel(uint64_t limit_ns, int32_t* status)
   }
 }
 
+__global__ void activation_kernel(int act, const float* __restrict__ x, float* __restrict__ y,
+                                  int64_t n) {
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += int64_t(gridDim.x) * blockDim.x)
+    y[i] = apply_act(x[i], act);
+}
+
 }  // namespace
 
 moe_status validate_config(const moe_config* cfg) { return check_config(cfg); }
@@ -235,7 +242,7 @@ moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk
   if (scratch_bytes < permute_scratch_bytes(*cfg)) return MOE_ERR_WORKSPACE;
   return cuda_status(launch_permute(*cfg, x, topk_idx, counts, kept, offsets, row_token,
                                     token_row, Xp, scratch, rows_max_of(*cfg),
-                                    static_cast<cudaStream_t>(stream)));
+                                    static_cast<cudaStream_t>(stream), nullptr));
 }
 
 moe_status moe_grouped_ffn(const moe_config* cfg, const void* Xp, const int32_t* offsets,
@@ -318,9 +325,14 @@ static moe_status forward_impl(const moe_config* cfg, const void* x, const moe_w
     e = launch_router(c, x, w->W_g, w->b_g, logits, out->topk_idx, out->topk_w,
                       ws.prob_partials, di.num_sms, di.status, g_wait_limit_ns.load(), s);
   if (e == cudaSuccess) e = record_event(ev[1], s);
+  // small layers: the one-block permutation also computes the load statistics
+  const bool fused_stats = permute_fuses_stats(c);
+  const StatsArgs stats{ws.prob_partials, int(router_blocks_of(c)), out->mean_prob,
+                        out->balance, out->dropped};
   if (e == cudaSuccess)
     e = launch_permute(c, x, out->topk_idx, out->counts, out->kept, ws.offsets, ws.row_token,
-                       ws.token_row, ws.Xp, ws.scratch, rows_max_of(c), s);
+                       ws.token_row, ws.Xp, ws.scratch, rows_max_of(c), s,
+                       fused_stats ? &stats : nullptr);
   if (e == cudaSuccess) e = record_event(ev[2], s);
   if (e == cudaSuccess) {
     GroupedFfnArgs a{};
@@ -334,7 +346,7 @@ static moe_status forward_impl(const moe_config* cfg, const void* x, const moe_w
   if (e == cudaSuccess)
     e = launch_combine(c, ws.Yp, ws.token_row, out->topk_w, ws.offsets, out->y, s);
   if (e == cudaSuccess) e = record_event(ev[5], s);
-  if (e == cudaSuccess)
+  if (e == cudaSuccess && !fused_stats)
     e = launch_load_stats(c, ws.prob_partials, out->counts, out->kept, out->mean_prob,
                           out->balance, out->dropped, s);
   if (e == cudaSuccess) e = record_event(ev[6], s);
@@ -358,7 +370,8 @@ int32_t moe_forward_launch_count(const moe_config* cfg) {
   if (check_config(cfg) != MOE_OK) return -1;
   const moe_config& c = *cfg;
   const int ffn = rows_max_of(c) > 0 ? 2 : 0;
-  return router_launch_count(c) + permute_launch_count(c) + ffn + (c.T > 0 ? 1 : 0) + 1;
+  return router_launch_count(c) + permute_launch_count(c) + ffn + (c.T > 0 ? 1 : 0) +
+         (permute_fuses_stats(c) ? 0 : 1);
 }
 
 size_t moe_host_workspace_size(const moe_config* cfg) {
@@ -433,6 +446,16 @@ moe_status moe_get_device_status(void* stream) {
   if (v != MOE_OK && cudaMemcpyToSymbol(g_device_status, &zero, sizeof(zero)) != cudaSuccess)
     return MOE_ERR_CUDA;
   return v;
+}
+
+moe_status moe_activation(int32_t act, const float* x, float* y, int64_t n, void* stream) {
+  if (act != MOE_ACT_GELU_ERF && act != MOE_ACT_RELU) return MOE_ERR_INVALID_ARG;
+  if (n < 0 || (n > 0 && (!x || !y))) return MOE_ERR_INVALID_ARG;
+  if (n == 0) return MOE_OK;
+  const int64_t blocks64 = ceil_div(n, 256);
+  const unsigned blocks = unsigned(blocks64 < 4096 ? blocks64 : 4096);
+  activation_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(act, x, y, n);
+  return cuda_status(cudaGetLastError());
 }
 
 moe_status moe_selftest_bounded_wait(uint64_t limit_ns, void* stream) {

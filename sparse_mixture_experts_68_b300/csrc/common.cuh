@@ -60,8 +60,24 @@ template <> struct Vec16<__nv_bfloat16> {
 
 // ---- activations -------------------------------------------------------------
 
+// erf by Abramowitz & Stegun, "Handbook of Mathematical Functions", formula
+// 7.1.26: erf(z) = 1 - t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-z^2),
+// t = 1 / (1 + p z) for z >= 0, odd in z; absolute error <= 1.5e-7, below
+// fp32 resolution near 1 and far below the bf16 the hidden layer is stored in.
+__device__ __forceinline__ float erf_as7126(float z) {
+  const float a = fabsf(z);
+  const float t = __frcp_rn(fmaf(0.3275911f, a, 1.0f));
+  float poly = fmaf(t, 1.061405429f, -1.453152027f);
+  poly = fmaf(t, poly, 1.421413741f);
+  poly = fmaf(t, poly, -0.284496736f);
+  poly = fmaf(t, poly, 0.254829592f);
+  const float r = 1.0f - t * poly * __expf(-a * a);
+  return copysignf(r, z);
+}
+
+// GELU with the exact (erf) form: 0.5 v (1 + erf(v / sqrt(2))).
 __device__ __forceinline__ float gelu_erf(float v) {
-  return 0.5f * v * (1.0f + erff(v * 0.70710678118654752440f));
+  return 0.5f * v * (1.0f + erf_as7126(v * 0.70710678118654752440f));
 }
 __device__ __forceinline__ float apply_act(float v, int act) {
   return act == MOE_ACT_RELU ? fmaxf(v, 0.0f) : gelu_erf(v);

@@ -894,12 +894,13 @@ cudaError_t launch_choice(int choice, int epi, const CUtensorMap& A, const CUten
   }
 }
 
-// Tile variant for one grouped Linear with output width Nd and rows_per_group
-// rows in an average expert group: CTA-pair 256 x 256 tiles when the groups
-// fill them (half the shared-memory traffic per MMA); otherwise the widest
-// single-CTA tile that divides Nd.
-int pick_tile(int64_t Nd, int64_t rows_per_group) {
-  if (Nd % 256 == 0 && rows_per_group >= 256) return TILE_256_PAIR;
+// Tile variant for one grouped Linear with output width Nd, reduction length
+// K and rows_per_group rows in an average expert group: CTA-pair 256 x 256
+// tiles when the groups fill them and K is long enough to amortise the pair's
+// synchronisation (half the shared-memory traffic per MMA); otherwise the
+// widest single-CTA tile that divides Nd.
+int pick_tile(int64_t Nd, int64_t rows_per_group, int64_t K) {
+  if (Nd % 256 == 0 && rows_per_group >= 256 && K >= 2048) return TILE_256_PAIR;
   if (Nd % 256 == 0) return TILE_256;
   if (Nd % 128 == 0) return TILE_128;
   return TILE_64;
@@ -912,7 +913,7 @@ cudaError_t grouped_linear(const moe_config& c, const GroupedFfnArgs& g, const v
                            cudaStream_t s) {
   const int64_t groups = c.n_experts + (c.d_ff_shared > 0 ? 1 : 0);
   const int64_t rows = c.T * c.top_k + (c.d_ff_shared > 0 ? c.T : 0);
-  const int choice = pick_tile(Nd, rows / groups);
+  const int choice = pick_tile(Nd, rows / groups, K);
   const int bn = tile_bn(choice);
   // the CTA pair loads half of each B tile per CTA
   const uint32_t b_box = uint32_t(choice == TILE_256_PAIR ? bn / 2 : bn);

@@ -40,11 +40,22 @@ cudaError_t launch_router(const moe_config& c, const void* x, const void* W_g,
 
 constexpr int kPermuteTokensPerBlock = 128;  // tokens per histogram / rank block
 
+// Load statistics computed at the end of the permutation (moe_forward only).
+struct StatsArgs {
+  const float* prob_partials;   // nullptr: no statistics
+  int nblk;
+  float* mean_prob;
+  float* balance;
+  int32_t* dropped;
+};
+
 size_t permute_scratch_bytes(const moe_config& c);
+// true when launch_permute can also produce the load statistics
+bool permute_fuses_stats(const moe_config& c);
 cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* topk_idx,
                            int32_t* counts, int32_t* kept, int32_t* offsets,
                            int32_t* row_token, int32_t* token_row, void* Xp, void* scratch,
-                           int64_t rows_max, cudaStream_t s);
+                           int64_t rows_max, cudaStream_t s, const StatsArgs* stats);
 
 // ---- grouped expert FFN ----------------------------------------------------------
 

@@ -16,7 +16,7 @@
 #include <mutex>
 
 #include "kernels.h"
-#include "common.cuh"
+#include "stats.cuh"
 
 namespace moe {
 
@@ -156,7 +156,8 @@ __global__ void __launch_bounds__(kSortWarps * 32)
     permute_sort_kernel(const int32_t* __restrict__ topk_idx, int T, int k, int N,
                         int64_t capacity, int has_shared, int32_t* __restrict__ counts,
                         int32_t* __restrict__ kept, int32_t* __restrict__ offsets,
-                        int32_t* __restrict__ row_token, int32_t* __restrict__ token_row) {
+                        int32_t* __restrict__ row_token, int32_t* __restrict__ token_row,
+                        StatsArgs stats) {
   extern __shared__ int32_t sm[];
   const int A = T * k;
   int32_t* cnt = sm;                              // [kSortWarps][N], then base ranks
@@ -273,6 +274,12 @@ __global__ void __launch_bounds__(kSortWarps * 32)
       token_row[a] = row;
     }
   }
+  if (stats.prob_partials) {
+    // the load statistics as well, once counts and kept are in memory
+    __syncthreads();
+    block_load_stats(stats.prob_partials, stats.nblk, N, T, counts, kept, stats.mean_prob,
+                     stats.balance, stats.dropped);
+  }
 }
 
 size_t sort_smem_bytes(const moe_config& c) {
@@ -283,7 +290,7 @@ size_t sort_smem_bytes(const moe_config& c) {
 // Above ~16K assignments the multi-block histogram path is faster.
 bool single_block_sort_fits(const moe_config& c) {
   return c.n_experts <= kSortWarps * 32 && c.T * c.top_k <= 16384 &&
-         sort_smem_bytes(c) <= 200 * 1024;
+         sort_smem_bytes(c) <= 190 * 1024;
 }
 
 template <typename T>
@@ -354,10 +361,12 @@ int permute_launch_count(const moe_config& c) {
   return (c.T > 0 ? 3 : 1) + copy;
 }
 
+bool permute_fuses_stats(const moe_config& c) { return single_block_sort_fits(c); }
+
 cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* topk_idx,
                            int32_t* counts, int32_t* kept, int32_t* offsets,
                            int32_t* row_token, int32_t* token_row, void* Xp, void* scratch,
-                           int64_t rows_max, cudaStream_t s) {
+                           int64_t rows_max, cudaStream_t s, const StatsArgs* stats) {
   const int N = int(c.n_experts), k = int(c.top_k), T = int(c.T);
   const int nblk = int(permute_blocks(c));
   PermuteScratch p = carve(c, scratch);
@@ -368,9 +377,10 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* to
     e = cudaFuncSetAttribute(permute_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(smem));
     if (e != cudaSuccess) return e;
-    permute_sort_kernel<<<1, kSortWarps * 32, smem, s>>>(topk_idx, T, k, N, c.capacity,
-                                                         c.d_ff_shared > 0 ? 1 : 0, counts,
-                                                         kept, offsets, row_token, token_row);
+    const StatsArgs none{};
+    permute_sort_kernel<<<1, kSortWarps * 32, smem, s>>>(
+        topk_idx, T, k, N, c.capacity, c.d_ff_shared > 0 ? 1 : 0, counts, kept, offsets,
+        row_token, token_row, stats ? *stats : none);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return launch_copy(c, x, offsets, row_token, Xp, rows_max, s);
@@ -449,6 +459,6 @@ extern "C" moe_status moe_permute_noalloc(const moe_config* cfg, const void* x,
   if (static_scratch_address(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
   const cudaError_t e = launch_permute(*cfg, x, topk_idx, counts, kept, offsets, row_token,
                                        token_row, Xp, scratch, rows_max_for(*cfg),
-                                       static_cast<cudaStream_t>(stream));
+                                       static_cast<cudaStream_t>(stream), nullptr);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
