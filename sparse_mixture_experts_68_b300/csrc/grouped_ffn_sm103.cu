@@ -763,6 +763,230 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CFG::THREADS, 1)
   }
 }
 
+// ---- decode variant: the weights as the 128-row MMA operand ----------------------------
+//
+// When an expert sees only a few tokens (decoding), a 128-row activation tile
+// would be almost all padding.  Here the roles swap: each MMA takes 128 rows
+// of the expert's weight matrix as its M=128 operand and the group's token
+// rows, padded to NB (16 or 32), as its N operand.  The accumulator holds
+// out^T for 128 output features x NB tokens; each epilogue thread owns one
+// feature and writes it for every live token.  Per k-block a CTA moves 16 KB
+// of weights and NB x 128 B of activations, so nearly every byte loaded is a
+// weight byte, and the ring is deep (STAGES x ~18 KB).
+
+template <int NB, int STAGES>
+struct LayoutS {
+  static constexpr int kWBytes = 128 * BK * 2;
+  static constexpr int kXBytes = NB * BK * 2;
+  static constexpr int kStageBytes = kWBytes + kXBytes;
+  static constexpr int kW = 0;
+  static constexpr int kX = STAGES * kWBytes;
+  static constexpr int kBar = kX + STAGES * kXBytes;
+  static constexpr int kNumBars = 2 * STAGES + 5;
+  static constexpr int kTmemSlot = kBar + kNumBars * 8;
+  static constexpr int kAbort = kTmemSlot + 4;
+  static constexpr int kTileStart = (kAbort + 4 + 15) / 16 * 16;
+  static constexpr int kGroupOff = kTileStart + (kMaxGroups + 1) * 4;
+  static constexpr int kBytes = kGroupOff + kMaxGroups * 4;
+  static constexpr int kAlloc = kBytes + 1024;
+  static_assert(kXBytes % 1024 == 0, "token tiles must keep the 1 KB swizzle alignment");
+  static_assert(kAlloc <= 227 * 1024, "shared memory budget");
+};
+
+template <int NB>
+__host__ __device__ constexpr uint32_t idesc_swap_bf16_f32() {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(NB >> 3) << 17) |
+         (uint32_t(128 >> 4) << 24);
+}
+
+template <int NB, int STAGES, int EPI>
+__global__ void __launch_bounds__(6 * 32, 1)
+    tc_swap_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
+                        const __grid_constant__ CUtensorMap tmWs,
+                        const __grid_constant__ CUtensorMap tmX, const TcParams p) {
+  constexpr int kStages = STAGES;
+  constexpr int kEpiWarps = 4;
+  constexpr int kFeat = 128;                   // output features per tile
+  using L = LayoutS<NB, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kStages;
+  uint64_t* tfull = bars + 2 * kStages;
+  uint64_t* tempty = bars + 2 * kStages + 2;
+  uint64_t* done = bars + 2 * kStages + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
+  int32_t* tile_start = reinterpret_cast<int32_t*>(smem + L::kTileStart);
+  int32_t* grp_off = reinterpret_cast<int32_t*>(smem + L::kGroupOff);
+  constexpr uint32_t kTmemCols = 2 * NB < 32 ? 32 : 2 * NB;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_groups = p.n_routed + (p.shared_rows > 0 ? 1 : 0);
+  const int ntiles = int(p.Nd / kFeat);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], kEpiWarps);
+    }
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  if (warp == 2) {
+    int32_t carry = 0;
+    for (int base = 0; base < n_groups; base += 32) {
+      const int g = base + lane;
+      int32_t live = 0, off = 0;
+      if (g < n_groups) {
+        off = p.offsets[g];
+        live = g < p.n_routed ? p.kept[g] : p.shared_rows;
+        grp_off[g] = off;
+      }
+      const int32_t tiles = int32_t((live + NB - 1) / NB) * ntiles;
+      int32_t incl = tiles;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (g < n_groups) tile_start[g] = carry + incl - tiles;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) tile_start[n_groups] = carry;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total_tiles = tile_start[n_groups];
+
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      int last_parity[kStages];
+#pragma unroll
+      for (int s = 0; s < kStages; ++s) last_parity[s] = -1;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        const TileCoord tc = decode_tile(tile, tile_start, n_groups, ntiles);
+        const int r0 = grp_off[tc.g] + tc.m * NB;
+        const int f0 = tc.n * kFeat;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!wait_or_abort(&empty[stage], phase ^ 1u, p, abort_flag)) { ok = false; break; }
+          const uint32_t fb = smem_u32(&full[stage]);
+          mbar_arrive_expect_tx(&full[stage], L::kStageBytes);
+          if (tc.g < p.n_routed)
+            tma_load_3d(&tmW, smem_u32(smem + L::kW + stage * L::kWBytes), fb, kb * BK, f0,
+                        tc.g);
+          else
+            tma_load_2d(&tmWs, smem_u32(smem + L::kW + stage * L::kWBytes), fb, kb * BK, f0);
+          tma_load_2d(&tmX, smem_u32(smem + L::kX + stage * L::kXBytes), fb, kb * BK, r0);
+          last_parity[stage] = int(phase);
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        for (int s = 0; s < kStages; ++s)
+          if (last_parity[s] >= 0) {
+            const uint32_t a = smem_u32(&full[s]);
+            const uint64_t t0 = global_timer_ns();
+            while (!mbar_try_wait(a, uint32_t(last_parity[s])) &&
+                   global_timer_ns() - t0 < p.wait_limit_ns) {
+            }
+          }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_swap_bf16_f32<NB>();
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        if (!wait_or_abort(&tempty[acc], acc_phase ^ 1u, p, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * NB;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!wait_or_abort(&full[stage], phase, p, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t wd = sdesc_sw128(smem_u32(smem + L::kW + stage * L::kWBytes));
+          const uint64_t xd = sdesc_sw128(smem_u32(smem + L::kX + stage * L::kXBytes));
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            tc_mma(d_tmem, wd + uint64_t(2 * kk), xd + uint64_t(2 * kk), idesc,
+                   (kb | kk) != 0 ? 1u : 0u);
+          tc_commit(smem_u32(&empty[stage]));
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit(smem_u32(&tfull[acc]));
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      tc_commit(smem_u32(done));
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_try_wait(smem_u32(done), 0) && global_timer_ns() - t0 < p.wait_limit_ns) {
+      }
+    }
+  } else {
+    // epilogue: warps 2-5, one TMEM lane quarter each; thread = one feature
+    const int q = warp & 3;
+    uint32_t acc = 0, acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+      const TileCoord tc = decode_tile(tile, tile_start, n_groups, ntiles);
+      bool ok = true;
+      if (lane == 0) ok = wait_or_abort(&tfull[acc], acc_phase, p, abort_flag);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      tc_fence_after();
+      const bool routed = tc.g < p.n_routed;
+      const int live = routed ? p.kept[tc.g] : p.shared_rows;
+      const int feat = tc.n * kFeat + q * 32 + lane;
+      const __nv_bfloat16* bias = routed ? p.bias + int64_t(tc.g) * p.Nd : p.bias_s;
+      const float b = __bfloat162float(bias[feat]);
+      uint32_t r[NB];
+      tmem_ld_cols<NB>(tmem_base + (uint32_t(q * 32) << 16) + acc * NB, r);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);     // accumulator is in registers now
+      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+#pragma unroll
+      for (int i = 0; i < NB; ++i) {
+        const int row_in_group = tc.m * NB + i;
+        if (row_in_group < live) {
+          float v = __uint_as_float(r[i]) + b;
+          if (EPI == EPI_BIAS_GELU) v = gelu_erf(v);
+          if (EPI == EPI_BIAS_RELU) v = fmaxf(v, 0.f);
+          out[(int64_t(grp_off[tc.g]) + row_in_group) * p.Nd + feat] = __float2bfloat16_rn(v);
+        }
+      }
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(kTmemCols));
+  }
+}
+
 // ---- host side -----------------------------------------------------------------------
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -906,6 +1130,35 @@ int pick_tile(int64_t Nd, int64_t rows_per_group, int64_t K) {
   return TILE_64;
 }
 
+template <int NB, int EPI>
+cudaError_t launch_swap_epi(const CUtensorMap& W, const CUtensorMap& Ws, const CUtensorMap& X,
+                            const TcParams& p, int grid, cudaStream_t s) {
+  constexpr int kStagesSwap = 10;
+  constexpr int smem = LayoutS<NB, kStagesSwap>::kAlloc;
+  auto kern = tc_swap_gemm_kernel<NB, kStagesSwap, EPI>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, 6 * 32, smem, s>>>(W, Ws, X, p);
+  return cudaGetLastError();
+}
+
+template <int NB>
+cudaError_t launch_swap(int epi, const CUtensorMap& W, const CUtensorMap& Ws,
+                        const CUtensorMap& X, const TcParams& p, int grid, cudaStream_t s) {
+  if (epi == EPI_BIAS_GELU) return launch_swap_epi<NB, EPI_BIAS_GELU>(W, Ws, X, p, grid, s);
+  if (epi == EPI_BIAS_RELU) return launch_swap_epi<NB, EPI_BIAS_RELU>(W, Ws, X, p, grid, s);
+  return launch_swap_epi<NB, EPI_BIAS>(W, Ws, X, p, grid, s);
+}
+
+// Token rows per tile of the decode variant for an average group of
+// rows_per_group rows (0: use the regular tiles).
+int swap_rows(int64_t Nd, int64_t rows_per_group, int epi) {
+  if (epi == EPI_BIAS_F32 || Nd % 128 != 0) return 0;
+  if (rows_per_group <= 8) return 16;
+  if (rows_per_group <= 24) return 32;
+  return 0;
+}
+
 // One grouped Linear: out[group g] = epi(A[group g] . W[g]^T + bias[g]).
 cudaError_t grouped_linear(const moe_config& c, const GroupedFfnArgs& g, const void* A,
                            const void* W, const void* Ws, const void* bias,
@@ -913,6 +1166,36 @@ cudaError_t grouped_linear(const moe_config& c, const GroupedFfnArgs& g, const v
                            cudaStream_t s) {
   const int64_t groups = c.n_experts + (c.d_ff_shared > 0 ? 1 : 0);
   const int64_t rows = c.T * c.top_k + (c.d_ff_shared > 0 ? c.T : 0);
+  const int nb = swap_rows(Nd, rows / groups, epi);
+  if (nb > 0) {
+    // decode: weights as the MMA's 128-row operand, tokens as its NB columns
+    CUtensorMap mW, mWs, mX;
+    if (!make_map(&mW, W, uint64_t(K), uint64_t(Nd), uint64_t(c.n_experts), 128))
+      return cudaErrorInvalidValue;
+    if (c.d_ff_shared > 0) {
+      if (!make_map(&mWs, Ws, uint64_t(K), uint64_t(Nd), 0, 128)) return cudaErrorInvalidValue;
+    } else {
+      mWs = mW;
+    }
+    if (!make_map(&mX, A, uint64_t(K), uint64_t(g.rows_max), 0, uint32_t(nb)))
+      return cudaErrorInvalidValue;
+    TcParams p{};
+    p.offsets = g.offsets;
+    p.kept = g.kept;
+    p.bias = static_cast<const __nv_bfloat16*>(bias);
+    p.bias_s = static_cast<const __nv_bfloat16*>(bias_s);
+    p.out = out;
+    p.Nd = Nd;
+    p.n_routed = int32_t(c.n_experts);
+    p.shared_rows = c.d_ff_shared > 0 ? int32_t(c.T) : 0;
+    p.num_kb = int32_t(K / BK);
+    p.status = g.status;
+    p.wait_limit_ns = g.wait_limit_ns;
+    const int64_t max_tiles = (ceil_div(rows, nb) + groups) * (Nd / 128);
+    const int grid = int(max_tiles < g.num_sms ? max_tiles : g.num_sms);
+    return nb == 16 ? launch_swap<16>(epi, mW, mWs, mX, p, grid, s)
+                    : launch_swap<32>(epi, mW, mWs, mX, p, grid, s);
+  }
   const int choice = pick_tile(Nd, rows / groups, K);
   const int bn = tile_bn(choice);
   // the CTA pair loads half of each B tile per CTA

@@ -69,6 +69,11 @@ SMALL = [
     # groups of >= 256 rows: the CTA-pair 256 x 256 tiles, with a shared expert
     Workload("bf16_pair_shared", T=700, d_model=128, d_ff=256, n_experts=2, top_k=2,
              act=ACT_GELU_ERF, dtype=DT_BF16, d_ff_shared=256, seed=27),
+    # few tokens per expert: weights as the MMA's 128-row operand (decode)
+    Workload("bf16_decode_nb16", T=9, d_model=256, d_ff=384, n_experts=8, top_k=2,
+             act=ACT_RELU, dtype=DT_BF16, seed=28),
+    Workload("bf16_decode_nb32_cap", T=60, d_model=128, d_ff=256, n_experts=12, top_k=3,
+             act=ACT_GELU_ERF, dtype=DT_BF16, capacity_factor=1.5, seed=29),
     # more than 32 slots per token: gates written in blocks of 32 lanes
     Workload("f32_k40_fused", T=50, d_model=64, d_ff=64, n_experts=64, top_k=40,
              act=ACT_RELU, dtype=DT_F32, seed=25),
