@@ -60,6 +60,34 @@ def peaks():
 
 
 # ---------------------------------------------------------------------------------------
+# DRAM traffic of the dominant kernel, from the committed ncu summary
+
+KERNEL_SOURCES = ("sparse_mixture_experts_68_b300/csrc/grouped_ffn_sm103.cu",
+                  "sparse_mixture_experts_68_b300/csrc/common.cuh")
+
+
+def profiled_traffic(workload):
+    """(bytes per launch, summary path) from profiles/*_<workload>.md when the
+    kernel sources still hash to the summary's source_sha256, else (None, why)."""
+    import hashlib
+    for kind in ("grouped_gemm", "swap_gemm"):
+        path = os.path.join(ROOT, "profiles", f"{kind}_{workload}.md")
+        if not os.path.exists(path):
+            continue
+        fields = {}
+        for line in open(path):
+            if ":" in line and line.split(":")[0] in ("traffic_bytes_per_launch", "source_sha256"):
+                k, v = line.split(":", 1)
+                fields[k.strip()] = v.strip()
+        sha = hashlib.sha256(b"".join(open(os.path.join(ROOT, f), "rb").read()
+                                      for f in KERNEL_SOURCES)).hexdigest()
+        if fields.get("source_sha256") != sha:
+            return None, f"profiles/{kind}_{workload}.md predates the current kernel sources"
+        return float(fields["traffic_bytes_per_launch"]), f"profiles/{kind}_{workload}.md"
+    return None, "no ncu summary for this workload"
+
+
+# ---------------------------------------------------------------------------------------
 # clocks during the timed region
 
 class ClockSampler:
@@ -314,7 +342,8 @@ def run_ours(args, wl, rank, world, local_rank):
         achieved = (b1 + b2) / launches / (ffn_ms / launches * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    roof["traffic"], roof["traffic_source"] = profiled_traffic(wl.name)
+    roof["algorithmic_bytes_per_launch"] = (b1 + b2) / launches
     roof["kernel"] = "tc_grouped_gemm_kernel (two launches per step: Linear 1, Linear 2)"
     roof["peak_source"] = pk["source"] + " (burst)"
     roof["per_launch"] = {
