@@ -237,7 +237,9 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* 
  * statistics, and events[5] and events[6] then bracket no work) 
  * A NULL entry is skipped.  While `stream` is being captured into a CUDA
  * graph, the events become external event-record nodes, so every replay of
- * the graph records them.  Otherwise identical to moe_forward. */
+ * the graph records them.  Otherwise identical to moe_forward, except that
+ * its kernels do not overlap their neighbours (moe_forward lets each kernel
+ * start while the previous one finishes), so each interval times one step. */
 moe_status moe_forward_profiled(const moe_config* cfg, const void* x, const moe_weights* w,
                                 const moe_outputs* out, void* workspace,
                                 size_t workspace_bytes, void* const* events, void* stream);

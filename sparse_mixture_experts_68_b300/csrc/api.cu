@@ -363,7 +363,11 @@ moe_status moe_forward_profiled(const moe_config* cfg, const void* x, const moe_
                                 const moe_outputs* out, void* workspace,
                                 size_t workspace_bytes, void* const* events, void* stream) {
   if (!events) return MOE_ERR_INVALID_ARG;
-  return forward_impl(cfg, x, w, out, workspace, workspace_bytes, events, stream);
+  // kernels run back to back without overlapping, so each event pair times one step
+  pdl_enabled() = false;
+  const moe_status st = forward_impl(cfg, x, w, out, workspace, workspace_bytes, events, stream);
+  pdl_enabled() = true;
+  return st;
 }
 
 int32_t moe_forward_launch_count(const moe_config* cfg) {

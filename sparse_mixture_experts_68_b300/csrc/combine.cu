@@ -24,6 +24,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
                    int Ttok, int k, int N, int has_shared, int64_t d, T* __restrict__ y) {
   constexpr int V = Vec16<T>::n;
   constexpr int CB = 4;                            // 16-byte columns per lane per pass
+  pdl_launch_dependents();
+  pdl_wait_previous();
   const int lane = threadIdx.x & 31;
   const int64_t t = int64_t(blockIdx.x) * kCombineWarps + (threadIdx.x >> 5);
   if (t >= Ttok) return;
@@ -74,6 +76,8 @@ __global__ void __launch_bounds__(kStatsThreads)
                       const int32_t* __restrict__ counts, const int32_t* __restrict__ kept,
                       float* __restrict__ mean_prob, float* __restrict__ balance,
                       int32_t* __restrict__ dropped) {
+  pdl_launch_dependents();
+  pdl_wait_previous();
   block_load_stats(prob_partials, nblk, N, Ttok, counts, kept, mean_prob, balance, dropped);
 }
 
@@ -86,23 +90,21 @@ cudaError_t launch_combine(const moe_config& c, const void* Yp, const int32_t* t
   const unsigned blocks = unsigned(ceil_div(c.T, kCombineWarps));
   const int hs = c.d_ff_shared > 0 ? 1 : 0;
   if (c.dtype == MOE_F32)
-    combine_kernel<float><<<blocks, kCombineWarps * 32, 0, s>>>(
-        static_cast<const float*>(Yp), token_row, topk_w, offsets, int(c.T), int(c.top_k),
-        int(c.n_experts), hs, c.d_model, static_cast<float*>(y));
-  else
-    combine_kernel<__nv_bfloat16><<<blocks, kCombineWarps * 32, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(Yp), token_row, topk_w, offsets, int(c.T),
-        int(c.top_k), int(c.n_experts), hs, c.d_model, static_cast<__nv_bfloat16*>(y));
-  return cudaGetLastError();
+    return launch_pdl(combine_kernel<float>, dim3(blocks), dim3(kCombineWarps * 32), 0, s,
+                      static_cast<const float*>(Yp), token_row, topk_w, offsets, int(c.T),
+                      int(c.top_k), int(c.n_experts), hs, c.d_model, static_cast<float*>(y));
+  return launch_pdl(combine_kernel<__nv_bfloat16>, dim3(blocks), dim3(kCombineWarps * 32), 0,
+                    s, static_cast<const __nv_bfloat16*>(Yp), token_row, topk_w, offsets,
+                    int(c.T), int(c.top_k), int(c.n_experts), hs, c.d_model,
+                    static_cast<__nv_bfloat16*>(y));
 }
 
 cudaError_t launch_load_stats(const moe_config& c, const float* prob_partials,
                               const int32_t* counts, const int32_t* kept, float* mean_prob,
                               float* balance, int32_t* dropped, cudaStream_t s) {
   const int nblk = int(router_partial_rows(c));
-  load_stats_kernel<<<1, kStatsThreads, 0, s>>>(prob_partials, nblk, int(c.n_experts), int(c.T),
-                                      counts, kept, mean_prob, balance, dropped);
-  return cudaGetLastError();
+  return launch_pdl(load_stats_kernel, dim3(1), dim3(kStatsThreads), 0, s, prob_partials, nblk,
+                    int(c.n_experts), int(c.T), counts, kept, mean_prob, balance, dropped);
 }
 
 }  // namespace moe

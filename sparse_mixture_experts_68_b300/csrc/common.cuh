@@ -83,6 +83,21 @@ __device__ __forceinline__ float apply_act(float v, int act) {
   return act == MOE_ACT_RELU ? fmaxf(v, 0.0f) : gelu_erf(v);
 }
 
+// ---- programmatic dependent launch ----------------------------------------------
+// Every kernel of the layer lets the next launch start at once (its blocks can
+// then run their local set-up on SMs this kernel frees) and waits for the
+// previous kernel to complete -- with its memory visible -- before its first
+// global-memory access.  Both are no-ops when the launch had no programmatic
+// dependency.
+
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait_previous() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---- shared-memory barriers with a time limit ---------------------------------
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

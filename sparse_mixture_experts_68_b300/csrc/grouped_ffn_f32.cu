@@ -22,8 +22,7 @@ cudaError_t launch_grouped_ffn_f32(const moe_config& c, const GroupedFfnArgs& g,
   a.A = g.Xp; a.B = g.w->W1; a.Bs = g.w->W1s; a.bias = g.w->b1; a.bias_s = g.w->b1s;
   a.C = g.H; a.K = c.d_model; a.Nc = c.d_ff;
   dim3 grid1(unsigned(ceil_div(c.d_ff, kSimtBN)), unsigned(ceil_div(g.rows_max, kSimtBM)));
-  simt_gemm_kernel<float, float><<<grid1, kSimtThreads, 0, s>>>(a);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(simt_gemm_kernel<float, float>, grid1, dim3(kSimtThreads), 0, s, a);
   if (e == cudaSuccess) e = record_event(g.mid_event, s);
   if (e != cudaSuccess) return e;
   // second Linear: [rows, d_ff] x [d, d_ff]^T
@@ -31,8 +30,7 @@ cudaError_t launch_grouped_ffn_f32(const moe_config& c, const GroupedFfnArgs& g,
   a.A = g.H; a.B = g.w->W2; a.Bs = g.w->W2s; a.bias = g.w->b2; a.bias_s = g.w->b2s;
   a.C = g.Yp; a.K = c.d_ff; a.Nc = c.d_model;
   dim3 grid2(unsigned(ceil_div(c.d_model, kSimtBN)), unsigned(ceil_div(g.rows_max, kSimtBM)));
-  simt_gemm_kernel<float, float><<<grid2, kSimtThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(simt_gemm_kernel<float, float>, grid2, dim3(kSimtThreads), 0, s, a);
 }
 
 }  // namespace moe

@@ -301,6 +301,11 @@ __global__ void __launch_bounds__(CFG::THREADS, MINB)
                  "r"(2 * BN));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
+  // the next launch may start once this CTA holds its TMEM; global memory is
+  // touched only after the previous kernel has completed
+  __syncthreads();
+  pdl_launch_dependents();
+  pdl_wait_previous();
   if (warp == 2) {
     // tile_start[g] = sum over earlier groups of m-tiles x n-tiles (warp scan)
     int32_t carry = 0;
@@ -621,6 +626,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CFG::THREADS, 1)
                  "r"(2 * BN));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
   }
+  __syncthreads();
+  pdl_launch_dependents();
+  pdl_wait_previous();
   if (warp == 2) {
     int32_t carry = 0;
     for (int base = 0; base < n_groups; base += 32) {
@@ -846,6 +854,11 @@ __global__ void __launch_bounds__(6 * 32, 1)
                  "r"(kTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
+  // the next launch may start once this CTA holds its TMEM; global memory is
+  // touched only after the previous kernel has completed
+  __syncthreads();
+  pdl_launch_dependents();
+  pdl_wait_previous();
   if (warp == 2) {
     int32_t carry = 0;
     for (int base = 0; base < n_groups; base += 32) {
@@ -1027,8 +1040,7 @@ cudaError_t launch_tc(const CUtensorMap& A, const CUtensorMap& B, const CUtensor
   auto kern = tc_grouped_gemm_kernel<CFG, EPI, minb>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, CFG::THREADS, smem, s>>>(A, B, Bs, p);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(CFG::THREADS), smem, s, A, B, Bs, p);
 }
 
 template <class CFG>
@@ -1093,8 +1105,7 @@ cudaError_t launch_pair(const CUtensorMap& A, const CUtensorMap& B, const CUtens
   }
   const int64_t pairs = tiles < max_pairs[dev] ? tiles : max_pairs[dev];
   if (pairs <= 0) return cudaSuccess;
-  kern<<<unsigned(2 * pairs), CFG::THREADS, smem, s>>>(A, B, Bs, p);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(unsigned(2 * pairs)), dim3(CFG::THREADS), smem, s, A, B, Bs, p);
 }
 
 cudaError_t launch_choice(int choice, int epi, const CUtensorMap& A, const CUtensorMap& B,
@@ -1138,8 +1149,7 @@ cudaError_t launch_swap_epi(const CUtensorMap& W, const CUtensorMap& Ws, const C
   auto kern = tc_swap_gemm_kernel<NB, kStagesSwap, EPI>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, 6 * 32, smem, s>>>(W, Ws, X, p);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(6 * 32), smem, s, W, Ws, X, p);
 }
 
 template <int NB>

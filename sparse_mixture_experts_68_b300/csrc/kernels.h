@@ -10,6 +10,33 @@
 
 namespace moe {
 
+// Whether launch_pdl may overlap a kernel with its predecessor on the stream
+// (per host thread).  moe_forward_profiled turns it off so that the events
+// it records between kernels time each kernel alone.
+inline bool& pdl_enabled() {
+  static thread_local bool on = true;
+  return on;
+}
+
+// Launches `kern`, with programmatic stream serialisation when enabled: the
+// kernel may start while the previous kernel on the stream is finishing (see
+// pdl_* in common.cuh).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // ---- router (router.cu) ------------------------------------------------------
 
 constexpr int kRouterTokensPerBlock = 8;    // tokens per router pass (one per warp)

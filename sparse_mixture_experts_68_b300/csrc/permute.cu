@@ -43,6 +43,8 @@ __global__ void __launch_bounds__(256)
     permute_hist_kernel(const int32_t* __restrict__ topk_idx, int T, int k, int N,
                         int32_t* __restrict__ block_counts) {
   extern __shared__ int32_t cnt[];
+  pdl_launch_dependents();
+  pdl_wait_previous();
   for (int e = threadIdx.x; e < N; e += blockDim.x) cnt[e] = 0;
   __syncthreads();
   const int64_t a0 = int64_t(blockIdx.x) * kPermuteTokensPerBlock * k;
@@ -63,6 +65,8 @@ __global__ void __launch_bounds__(1024)
                         int32_t* __restrict__ counts, int32_t* __restrict__ kept,
                         int32_t* __restrict__ offsets, int32_t* __restrict__ row_token) {
   __shared__ int32_t warp_tot[32];
+  pdl_launch_dependents();
+  pdl_wait_previous();
   const int e = threadIdx.x;
   int32_t total = 0, kp = 0, padded = 0;
   if (e < N) {
@@ -114,6 +118,8 @@ __global__ void __launch_bounds__(32)
                         const int32_t* __restrict__ offsets, int32_t* __restrict__ row_token,
                         int32_t* __restrict__ token_row) {
   extern __shared__ int32_t run[];              // next rank per expert
+  pdl_launch_dependents();
+  pdl_wait_previous();
   const int lane = threadIdx.x;
   for (int e = lane; e < N; e += 32) run[e] = block_base[int64_t(blockIdx.x) * N + e];
   __syncwarp();
@@ -159,6 +165,8 @@ __global__ void __launch_bounds__(kSortWarps * 32)
                         int32_t* __restrict__ row_token, int32_t* __restrict__ token_row,
                         StatsArgs stats) {
   extern __shared__ int32_t sm[];
+  pdl_launch_dependents();
+  pdl_wait_previous();
   const int A = T * k;
   int32_t* cnt = sm;                              // [kSortWarps][N], then base ranks
   int32_t* off = cnt + kSortWarps * N;            // [N] group offsets
@@ -298,6 +306,8 @@ __global__ void __launch_bounds__(256)
     permute_copy_kernel(const T* __restrict__ x, int64_t d, int Ttok, int N,
                         const int32_t* __restrict__ offsets,
                         const int32_t* __restrict__ row_token, T* __restrict__ Xp) {
+  pdl_launch_dependents();
+  pdl_wait_previous();
   const int lane = threadIdx.x & 31;
   const int64_t routed_end = offsets[N], total = offsets[N + 1];
   const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
@@ -343,14 +353,12 @@ cudaError_t launch_copy(const moe_config& c, const void* x, const int32_t* offse
   const int64_t want = ceil_div(rows_max, 8);
   const unsigned blocks = unsigned(want < 148 * 8 ? want : 148 * 8);
   if (c.dtype == MOE_F32)
-    permute_copy_kernel<float><<<blocks, 256, 0, s>>>(static_cast<const float*>(x), c.d_model,
-                                                      T, N, offsets, row_token,
-                                                      static_cast<float*>(Xp));
-  else
-    permute_copy_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(x), c.d_model, T, N, offsets, row_token,
-        static_cast<__nv_bfloat16*>(Xp));
-  return cudaGetLastError();
+    return launch_pdl(permute_copy_kernel<float>, dim3(blocks), dim3(256), 0, s,
+                      static_cast<const float*>(x), c.d_model, T, N, offsets, row_token,
+                      static_cast<float*>(Xp));
+  return launch_pdl(permute_copy_kernel<__nv_bfloat16>, dim3(blocks), dim3(256), 0, s,
+                    static_cast<const __nv_bfloat16*>(x), c.d_model, T, N, offsets,
+                    row_token, static_cast<__nv_bfloat16*>(Xp));
 }
 
 }  // namespace
@@ -378,27 +386,24 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* to
                              int(smem));
     if (e != cudaSuccess) return e;
     const StatsArgs none{};
-    permute_sort_kernel<<<1, kSortWarps * 32, smem, s>>>(
-        topk_idx, T, k, N, c.capacity, c.d_ff_shared > 0 ? 1 : 0, counts, kept, offsets,
-        row_token, token_row, stats ? *stats : none);
-    e = cudaGetLastError();
+    e = launch_pdl(permute_sort_kernel, dim3(1), dim3(kSortWarps * 32), smem, s, topk_idx, T, k,
+                   N, c.capacity, c.d_ff_shared > 0 ? 1 : 0, counts, kept, offsets, row_token,
+                   token_row, stats ? *stats : none);
     if (e != cudaSuccess) return e;
     return launch_copy(c, x, offsets, row_token, Xp, rows_max, s);
   }
   if (nblk > 0) {
-    permute_hist_kernel<<<nblk, 256, smemN, s>>>(topk_idx, T, k, N, p.block_counts);
-    cudaError_t e = cudaGetLastError();
+    e = launch_pdl(permute_hist_kernel, dim3(nblk), dim3(256), smemN, s, topk_idx, T, k, N,
+                   p.block_counts);
     if (e != cudaSuccess) return e;
   }
-  permute_scan_kernel<<<1, 1024, 0, s>>>(p.block_counts, nblk, N, T, c.capacity,
-                                         c.d_ff_shared > 0 ? 1 : 0, p.block_base, counts,
-                                         kept, offsets, row_token);
-  e = cudaGetLastError();
+  e = launch_pdl(permute_scan_kernel, dim3(1), dim3(1024), 0, s, p.block_counts, nblk, N, T,
+                 c.capacity, c.d_ff_shared > 0 ? 1 : 0, p.block_base, counts, kept, offsets,
+                 row_token);
   if (e != cudaSuccess) return e;
   if (nblk > 0) {
-    permute_rank_kernel<<<nblk, 32, smemN, s>>>(topk_idx, T, k, N, c.capacity, p.block_base,
-                                                offsets, row_token, token_row);
-    e = cudaGetLastError();
+    e = launch_pdl(permute_rank_kernel, dim3(nblk), dim3(32), smemN, s, topk_idx, T, k, N,
+                   c.capacity, p.block_base, offsets, row_token, token_row);
     if (e != cudaSuccess) return e;
   }
   return launch_copy(c, x, offsets, row_token, Xp, rows_max, s);

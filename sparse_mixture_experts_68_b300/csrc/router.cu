@@ -19,10 +19,8 @@ cudaError_t launch_router_logits(const moe_config& c, const void* x, const void*
   a.act = -1;
   dim3 grid(unsigned(ceil_div(c.n_experts, kSimtBN)), unsigned(ceil_div(c.T, kSimtBM)));
   if (c.dtype == MOE_F32)
-    simt_gemm_kernel<float, float><<<grid, kSimtThreads, 0, s>>>(a);
-  else
-    simt_gemm_kernel<__nv_bfloat16, float><<<grid, kSimtThreads, 0, s>>>(a);
-  return cudaGetLastError();
+    return launch_pdl(simt_gemm_kernel<float, float>, grid, dim3(kSimtThreads), 0, s, a);
+  return launch_pdl(simt_gemm_kernel<__nv_bfloat16, float>, grid, dim3(kSimtThreads), 0, s, a);
 }
 
 // One warp per token.  Lane l holds the scores of experts l, l+32, ...,
@@ -38,6 +36,8 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
                                int renorm, int32_t* __restrict__ topk_idx,
                                float* __restrict__ topk_w, float* __restrict__ prob_partials) {
   extern __shared__ float red[];                 // [kRouterWarps][N]
+  pdl_launch_dependents();
+  pdl_wait_previous();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int kTokPerWarp = kRouterTokensPerBlock / kRouterWarps;
   float psum[NPL];
@@ -152,6 +152,8 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
   constexpr int DUP = NE < 32 ? 32 / NE : 1;          // lanes holding the same expert
   constexpr int kBatch = NE <= 16 ? 16 : (NE == 32 ? 8 : 2);   // 16-byte x loads in flight
   extern __shared__ uint4 wsm[];                      // W_g [NE][d] (zero rows), then sums
+  pdl_launch_dependents();
+  pdl_wait_previous();
   const int dv = d / V;
   const int nvec = N * dv, nvec_pad = NE * dv;
   const uint4* wsrc = reinterpret_cast<const uint4*>(W_g);
@@ -337,11 +339,10 @@ cudaError_t launch_router_fused(const moe_config& c, const void* x, const void* 
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,  \
                                          int(smem));                                       \
     if (e != cudaSuccess) return e;                                                        \
-    kern<<<blocks, kRouterWarps * 32, smem, s>>>(                                          \
-        static_cast<const TIN*>(x), static_cast<const TIN*>(W_g),                          \
-        static_cast<const TIN*>(b_g), T, d, N, k, rn, logits, topk_idx, topk_w,            \
-        prob_partials);                                                                    \
-    return cudaGetLastError();                                                             \
+    return launch_pdl(kern, dim3(blocks), dim3(kRouterWarps * 32), smem, s,                \
+                      static_cast<const TIN*>(x), static_cast<const TIN*>(W_g),            \
+                      static_cast<const TIN*>(b_g), T, d, N, k, rn, logits, topk_idx,      \
+                      topk_w, prob_partials);                                              \
   }
   if (c.dtype == MOE_F32) {
     if (N <= 8) MOE_FUSED_CASE(float, 8)
@@ -372,9 +373,8 @@ cudaError_t launch_router_softmax_topk(const moe_config& c, const float* logits,
                                            int(smem));                                     \
       if (e != cudaSuccess) return e;                                                      \
     }                                                                                      \
-    kern<<<blocks, kRouterWarps * 32, smem, s>>>(logits, T, N, k, rn, topk_idx, topk_w,   \
-                                                 prob_partials);                           \
-    return cudaGetLastError();                                                             \
+    return launch_pdl(kern, dim3(blocks), dim3(kRouterWarps * 32), smem, s, logits, T, N,  \
+                      k, rn, topk_idx, topk_w, prob_partials);                             \
   }
   if (N <= 32) MOE_ROUTER_CASE(1)
   if (N <= 64) MOE_ROUTER_CASE(2)

@@ -33,6 +33,8 @@ template <typename TIn, typename TOut>
 __global__ void __launch_bounds__(kSimtThreads) simt_gemm_kernel(SimtGemmArgs a) {
   __shared__ float As[kSimtBK][kSimtBM + 4];
   __shared__ float Bs[kSimtBK][kSimtBN + 4];
+  pdl_launch_dependents();
+  pdl_wait_previous();
 
   const int64_t row0 = int64_t(blockIdx.y) * kSimtBM;
   const int64_t col0 = int64_t(blockIdx.x) * kSimtBN;
