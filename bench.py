@@ -246,6 +246,23 @@ def run_reference(args, wl, rank, world):
 STAGES = ("router_topk", "permute", "ffn_linear1", "ffn_linear2", "combine", "load_stats")
 
 
+def job_time_ms(local_ms: float, world: int, device=None) -> float:
+    """The job's time for the timed steps: the max over ranks (each rank runs
+    its own replica of the layer on its own GPU)."""
+    if world <= 1:
+        return local_ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([local_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_step: int, steps: int, world: int, job_ms: float) -> float:
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    return tokens_per_step * steps * world / (job_ms * 1e-3)
+
+
 def run_ours(args, wl, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -318,11 +335,7 @@ def run_ours(args, wl, rank, world, local_rank):
         dist.barrier()
     clk = clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in marks]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = job_time_ms(sum(step_ms), world, dev)
     # per-kernel times: K steps of moe_forward_profiled, launched directly (its
     # events recorded between the kernels on the stream)
     stage_ms, prof_step_ms = [], []
@@ -339,7 +352,7 @@ def run_ours(args, wl, rank, world, local_rank):
     kept_rows = int(out.kept.sum().item())
     n_kept_experts = int((out.kept > 0).sum().item())
     T = layer.cfg.T
-    value = T * K * world / (total_ms * 1e-3)
+    value = job_tokens_per_s(T, K, world, total_ms)
     mean_stage = {n: statistics.mean(s[i] for s in stage_ms) for i, n in enumerate(STAGES)}
 
     # roofline of the dominant kernel: the tcgen05 grouped GEMM, launched once
