@@ -106,6 +106,7 @@ typedef struct moe_outputs {
   float   *mean_prob;  /* [N] mean over tokens of p                     required */
   float   *balance;    /* [1] std_unbiased(mean_prob)^2                 required */
   float   *logits;     /* [T, N] router scores z; NULL = keep in workspace      */
+  float   *cv_squared; /* [1] var_unbiased(counts) / mean(counts)^2; NULL = skip */
 } moe_outputs;
 
 /* ---- sizes --------------------------------------------------------------- */
@@ -215,10 +216,19 @@ moe_status moe_combine(const moe_config* cfg, const void* Yp, const int32_t* tok
  *   balance      = sum_e (mean_prob[e] - 1/N)^2 / (N - 1)   (0 when N == 1)
  *                = torch.std(mean_prob)**2 with the unbiased default
  *   dropped      = sum_e (counts[e] - kept[e])
- * Sums run in fp64 in a fixed order. */
+ *   cv_squared   = var(counts) / mean(counts)^2, unbiased variance over the N
+ *                  routed counts; 0 when N == 1 or nothing is routed.  The
+ *                  coefficient of variation the auxiliary loss penalises
+ *                  (matteuscruz.github.io "Load balancing: the core training
+ *                  challenge"; invest-in.ai "MoE - Mixture of Experts",
+ *                  "Common Usage Examples": cv_squared(expert_counts)); the
+ *                  pages give no formula, this is the plain reading.
+ *                  Optional: NULL skips it.
+ * One block; sums in a fixed order (compensated fp32 for the probabilities,
+ * exact integers for the counts), so results are deterministic. */
 moe_status moe_load_stats(const moe_config* cfg, const float* prob_partials,
                           const int32_t* counts, const int32_t* kept, float* mean_prob,
-                          float* balance, int32_t* dropped, void* stream);
+                          float* balance, int32_t* dropped, float* cv_squared, void* stream);
 
 /* The whole layer: router_topk -> permute -> grouped_ffn -> combine ->
  * load_stats on `stream`, with intermediates carved from `workspace`

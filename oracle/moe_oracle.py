@@ -30,6 +30,11 @@ float64 numpy, with no blocking, fusion or reordering beyond the definition:
   roadtointelligence.com "Total versus active parameters" (DeepSeek-V3).
 * balance statistic std(mean_t router_probs)^2 with torch's default
   (unbiased) std -- botmartz.com "Load Balancing: The Hidden Challenge".
+* squared coefficient of variation of the expert counts, the quantity the
+  auxiliary loss penalises -- matteuscruz.github.io "Load balancing: the core
+  training challenge"; named cv_squared(expert_counts) in invest-in.ai
+  "MoE - Mixture of Experts", "Common Usage Examples".  The pages give no
+  formula; read as var/mean^2 with the unbiased variance over the N counts.
 
 Readings taken where the pages are silent (each also listed in the design
 notes): top-k ties go to the lower expert index; slot 0 holds the largest
@@ -240,6 +245,7 @@ class LayerOutput:
     grouping: Grouping
     mean_prob: np.ndarray    # [N]
     balance: float
+    cv_squared: float = 0.0  # of the routed counts
 
 
 def balance_statistic(p):
@@ -250,6 +256,23 @@ def balance_statistic(p):
     if m.shape[0] < 2:
         return m, 0.0
     return m, float(np.std(m, ddof=1) ** 2)
+
+
+def cv_squared(counts):
+    """Squared coefficient of variation of the per-expert counts: the unbiased
+    variance over the N experts divided by the squared mean (matteuscruz.github.io
+    "Load balancing: the core training challenge" names the coefficient of
+    variation of the expert load; invest-in.ai "MoE - Mixture of Experts",
+    "Common Usage Examples", names cv_squared(expert_counts); the variance
+    estimator is torch's default, as in the balance statistic).  0 for a single
+    expert or when nothing was routed."""
+    c = np.asarray(counts, dtype=np.float64)
+    if c.shape[0] < 2:
+        return 0.0
+    m = float(np.mean(c))
+    if m == 0.0:
+        return 0.0
+    return float(np.var(c, ddof=1) / (m * m))
 
 
 def moe_forward(x, W_g, b_g, W1, b1, W2, b2, *, k, act, capacity=0,
@@ -289,7 +312,8 @@ def moe_forward(x, W_g, b_g, W1, b1, W2, b2, *, k, act, capacity=0,
     if shared is not None:
         W1s, b1s, W2s, b2s = shared
         y += expert_ffn(x[tokens], W1s, b1s, W2s, b2s, act, round_hidden_bf16)
-    return LayerOutput(y, tokens, z, p, idx, w, grouping, mean_prob, balance)
+    return LayerOutput(y, tokens, z, p, idx, w, grouping, mean_prob, balance,
+                       cv_squared(grouping.counts))
 
 
 def moe_bruteforce(x, W_g, b_g, W1, b1, W2, b2, *, k, act, capacity=0,

@@ -56,7 +56,8 @@ class MoeWeights(C.Structure):
 class MoeOutputs(C.Structure):
     _fields_ = [("y", C.c_void_p), ("topk_idx", C.c_void_p), ("topk_w", C.c_void_p),
                 ("counts", C.c_void_p), ("kept", C.c_void_p), ("dropped", C.c_void_p),
-                ("mean_prob", C.c_void_p), ("balance", C.c_void_p), ("logits", C.c_void_p)]
+                ("mean_prob", C.c_void_p), ("balance", C.c_void_p), ("logits", C.c_void_p),
+                ("cv_squared", C.c_void_p)]
 
 
 _lib = None
@@ -85,7 +86,7 @@ def lib() -> C.CDLL:
         "moe_permute_noalloc": (C.c_int32, [CP, P, P, P, P, P, P, P, P, P]),
         "moe_grouped_ffn": (C.c_int32, [CP, P, P, P, C.POINTER(MoeWeights), P, P, P]),
         "moe_combine": (C.c_int32, [CP, P, P, P, P, P, P]),
-        "moe_load_stats": (C.c_int32, [CP, P, P, P, P, P, P, P]),
+        "moe_load_stats": (C.c_int32, [CP, P, P, P, P, P, P, P, P]),
         "moe_forward": (C.c_int32, [CP, P, C.POINTER(MoeWeights), C.POINTER(MoeOutputs), P,
                                     C.c_size_t, P]),
         "moe_forward_profiled": (C.c_int32, [CP, P, C.POINTER(MoeWeights),
@@ -200,9 +201,10 @@ def combine(cfg, Yp, token_row, topk_w, offsets, y, stream=None):
                              _ptr(offsets), _ptr(y), _stream(stream)), "moe_combine")
 
 
-def load_stats(cfg, prob_partials, counts, kept, mean_prob, balance, dropped, stream=None):
+def load_stats(cfg, prob_partials, counts, kept, mean_prob, balance, dropped, cv_squared=None,
+               stream=None):
     _check(lib().moe_load_stats(C.byref(cfg), _ptr(prob_partials), _ptr(counts), _ptr(kept),
-                                _ptr(mean_prob), _ptr(balance), _ptr(dropped),
+                                _ptr(mean_prob), _ptr(balance), _ptr(dropped), _ptr(cv_squared),
                                 _stream(stream)), "moe_load_stats")
 
 
@@ -242,11 +244,13 @@ class Outputs:
     mean_prob: torch.Tensor
     balance: torch.Tensor
     logits: torch.Tensor | None = None
+    cv_squared: torch.Tensor | None = None
 
     def struct(self) -> MoeOutputs:
         return MoeOutputs(_ptr(self.y), _ptr(self.topk_idx), _ptr(self.topk_w),
                           _ptr(self.counts), _ptr(self.kept), _ptr(self.dropped),
-                          _ptr(self.mean_prob), _ptr(self.balance), _ptr(self.logits))
+                          _ptr(self.mean_prob), _ptr(self.balance), _ptr(self.logits),
+                          _ptr(self.cv_squared))
 
 
 def alloc_outputs(cfg: MoeConfig, device, with_logits=False, pin_memory=False) -> Outputs:
@@ -262,7 +266,8 @@ def alloc_outputs(cfg: MoeConfig, device, with_logits=False, pin_memory=False) -
         dropped=torch.empty((1,), dtype=torch.int32, **kw),
         mean_prob=torch.empty((N,), dtype=torch.float32, **kw),
         balance=torch.empty((1,), dtype=torch.float32, **kw),
-        logits=torch.empty((T, N), dtype=torch.float32, **kw) if with_logits else None)
+        logits=torch.empty((T, N), dtype=torch.float32, **kw) if with_logits else None,
+        cv_squared=torch.empty((1,), dtype=torch.float32, **kw))
 
 
 def forward(cfg: MoeConfig, x, weights: MoeWeights, out: Outputs, workspace, stream=None):

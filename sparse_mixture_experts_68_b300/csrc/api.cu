@@ -281,14 +281,15 @@ moe_status moe_combine(const moe_config* cfg, const void* Yp, const int32_t* tok
 
 moe_status moe_load_stats(const moe_config* cfg, const float* prob_partials,
                           const int32_t* counts, const int32_t* kept, float* mean_prob,
-                          float* balance, int32_t* dropped, void* stream) {
+                          float* balance, int32_t* dropped, float* cv_squared,
+                          void* stream) {
   moe_status st = check_config(cfg);
   if (st != MOE_OK) return st;
   const void* ps[] = {prob_partials, counts, kept, mean_prob, balance, dropped};
   for (const void* q : ps)
     if (!q) return MOE_ERR_INVALID_ARG;
   return cuda_status(launch_load_stats(*cfg, prob_partials, counts, kept, mean_prob, balance,
-                                       dropped, static_cast<cudaStream_t>(stream)));
+                                       dropped, cv_squared, static_cast<cudaStream_t>(stream)));
 }
 
 static moe_status forward_impl(const moe_config* cfg, const void* x, const moe_weights* w,
@@ -328,7 +329,7 @@ static moe_status forward_impl(const moe_config* cfg, const void* x, const moe_w
   // small layers: the one-block permutation also computes the load statistics
   const bool fused_stats = permute_fuses_stats(c);
   const StatsArgs stats{ws.prob_partials, int(router_blocks_of(c)), out->mean_prob,
-                        out->balance, out->dropped};
+                        out->balance, out->dropped, out->cv_squared};
   if (e == cudaSuccess)
     e = launch_permute(c, x, out->topk_idx, out->counts, out->kept, ws.offsets, ws.row_token,
                        ws.token_row, ws.Xp, ws.scratch, rows_max_of(c), s,
@@ -348,7 +349,7 @@ static moe_status forward_impl(const moe_config* cfg, const void* x, const moe_w
   if (e == cudaSuccess) e = record_event(ev[5], s);
   if (e == cudaSuccess && !fused_stats)
     e = launch_load_stats(c, ws.prob_partials, out->counts, out->kept, out->mean_prob,
-                          out->balance, out->dropped, s);
+                          out->balance, out->dropped, out->cv_squared, s);
   if (e == cudaSuccess) e = record_event(ev[6], s);
   return cuda_status(e);
 }
@@ -420,6 +421,7 @@ moe_status moe_forward_host(const moe_config* cfg, const void* x_host, const moe
   od.dropped = static_cast<int32_t*>(take(4));
   od.balance = static_cast<float*>(take(4));
   od.logits = oh->logits ? static_cast<float*>(take(lb)) : nullptr;
+  od.cv_squared = oh->cv_squared ? static_cast<float*>(take(4)) : nullptr;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (xb && cudaMemcpyAsync(xd, x_host, xb, cudaMemcpyHostToDevice, s) != cudaSuccess)
     return MOE_ERR_CUDA;
@@ -434,7 +436,8 @@ moe_status moe_forward_host(const moe_config* cfg, const void* x_host, const moe
                          {oh->mean_prob, od.mean_prob, nb},
                          {oh->dropped, od.dropped, 4},
                          {oh->balance, od.balance, 4},
-                         {oh->logits, od.logits, oh->logits ? lb : 0}};
+                         {oh->logits, od.logits, oh->logits ? lb : 0},
+                         {oh->cv_squared, od.cv_squared, oh->cv_squared ? size_t(4) : 0}};
   for (const Copy& cp : copies)
     if (cp.n && cudaMemcpyAsync(cp.dst, cp.src, cp.n, cudaMemcpyDeviceToHost, s) != cudaSuccess)
       return MOE_ERR_CUDA;

@@ -75,10 +75,11 @@ __global__ void __launch_bounds__(kStatsThreads)
     load_stats_kernel(const float* __restrict__ prob_partials, int nblk, int N, int Ttok,
                       const int32_t* __restrict__ counts, const int32_t* __restrict__ kept,
                       float* __restrict__ mean_prob, float* __restrict__ balance,
-                      int32_t* __restrict__ dropped) {
+                      int32_t* __restrict__ dropped, float* __restrict__ cv_squared) {
   pdl_launch_dependents();
   pdl_wait_previous();
-  block_load_stats(prob_partials, nblk, N, Ttok, counts, kept, mean_prob, balance, dropped);
+  block_load_stats(prob_partials, nblk, N, Ttok, counts, kept, mean_prob, balance, dropped,
+                   cv_squared);
 }
 
 }  // namespace
@@ -101,10 +102,12 @@ cudaError_t launch_combine(const moe_config& c, const void* Yp, const int32_t* t
 
 cudaError_t launch_load_stats(const moe_config& c, const float* prob_partials,
                               const int32_t* counts, const int32_t* kept, float* mean_prob,
-                              float* balance, int32_t* dropped, cudaStream_t s) {
+                              float* balance, int32_t* dropped, float* cv_squared,
+                              cudaStream_t s) {
   const int nblk = int(router_partial_rows(c));
   return launch_pdl(load_stats_kernel, dim3(1), dim3(kStatsThreads), 0, s, prob_partials, nblk,
-                    int(c.n_experts), int(c.T), counts, kept, mean_prob, balance, dropped);
+                    int(c.n_experts), int(c.T), counts, kept, mean_prob, balance, dropped,
+                    cv_squared);
 }
 
 }  // namespace moe

@@ -74,6 +74,7 @@ struct StatsArgs {
   float* mean_prob;
   float* balance;
   int32_t* dropped;
+  float* cv_squared;            // nullptr: not computed
 };
 
 size_t permute_scratch_bytes(const moe_config& c);
@@ -115,7 +116,8 @@ cudaError_t launch_combine(const moe_config& c, const void* Yp, const int32_t* t
                            cudaStream_t s);
 cudaError_t launch_load_stats(const moe_config& c, const float* prob_partials,
                               const int32_t* counts, const int32_t* kept, float* mean_prob,
-                              float* balance, int32_t* dropped, cudaStream_t s);
+                              float* balance, int32_t* dropped, float* cv_squared,
+                              cudaStream_t s);
 
 // ---- kernels launched per step, for the chosen dispatch ------------------------------
 int router_launch_count(const moe_config& c);

@@ -286,7 +286,7 @@ __global__ void __launch_bounds__(kSortWarps * 32)
     // the load statistics as well, once counts and kept are in memory
     __syncthreads();
     block_load_stats(stats.prob_partials, stats.nblk, N, T, counts, kept, stats.mean_prob,
-                     stats.balance, stats.dropped);
+                     stats.balance, stats.dropped, stats.cv_squared);
   }
 }
 

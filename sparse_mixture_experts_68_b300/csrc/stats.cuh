@@ -1,6 +1,9 @@
 // Load statistics (botmartz.com "Mixture of Experts (MoE) and Mixtral",
 // "Load Balancing: The Hidden Challenge"): mean over tokens of the router
-// probabilities, the unbiased variance of those means, and the dropped count.
+// probabilities, the unbiased variance of those means, and the dropped count;
+// also the squared coefficient of variation of the routed counts
+// (matteuscruz.github.io "Load balancing: the core training challenge";
+// invest-in.ai "MoE - Mixture of Experts", cv_squared(expert_counts)).
 // A block-wide device function so that the statistics can run either as
 // their own kernel or at the end of the one-block permutation.
 #pragma once
@@ -18,7 +21,9 @@ namespace moe {
 // Kahan sum per expert; the row groups are combined in order with
 // error-free additions (two-sum).  The deviation from the uniform load is
 // taken as (S - T/N) / T with S the compensated sum, so it keeps its
-// accuracy when the load is nearly uniform.
+// accuracy when the load is nearly uniform.  The counts' statistic is exact
+// integer arithmetic up to its last step: with S = sum c and Q = sum c^2,
+// var/mean^2 = N (N Q - S^2) / ((N - 1) S^2), N Q - S^2 in 128-bit integers.
 constexpr int kStatsThreads = 1024;
 constexpr int kStatsWarps = kStatsThreads / 32;
 
@@ -42,16 +47,19 @@ __device__ __forceinline__ void block_load_stats(const float* __restrict__ prob_
                                                  const int32_t* __restrict__ kept,
                                                  float* __restrict__ mean_prob,
                                                  float* __restrict__ balance,
-                                                 int32_t* __restrict__ dropped) {
+                                                 int32_t* __restrict__ dropped,
+                                                 float* __restrict__ cv_squared) {
   __shared__ float2 part[kStatsWarps][32];        // (sum, -compensation) per warp, lane
   __shared__ float2 sq[kStatsWarps];              // Kahan sum of squared deviations
   __shared__ int dr[kStatsWarps];
+  __shared__ long long cs[kStatsWarps], cq[kStatsWarps];   // sum c, sum c^2
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nchunks = (N + 31) / 32;
   const float invT = Ttok > 0 ? 1.0f / float(Ttok) : 0.f;
   const float tN = float(Ttok) / float(N);        // the per-expert sum of a uniform router
   float sq_s = 0.f, sq_c = 0.f;
   int my_dr = 0;
+  long long my_cs = 0, my_cq = 0;
   const int RG = nchunks >= kStatsWarps ? 1 : kStatsWarps / nchunks;
   const int chunks_per_pass = kStatsWarps / RG;
   for (int c0 = 0; c0 < nchunks; c0 += chunks_per_pass) {
@@ -89,7 +97,10 @@ __device__ __forceinline__ void block_load_stats(const float* __restrict__ prob_
       stats_two_sum(hi, -tN, dhi, dlo);
       const float dev = (dhi + (dlo + lo)) * invT;
       stats_kahan_add(dev * dev, sq_s, sq_c);
-      my_dr += counts[e] - kept[e];
+      const long long ce = counts[e];
+      my_dr += int(ce) - kept[e];
+      my_cs += ce;
+      my_cq += ce * ce;
     }
     __syncthreads();
   }
@@ -103,22 +114,44 @@ __device__ __forceinline__ void block_load_stats(const float* __restrict__ prob_
     sq_s = ns;
     sq_c = sq_c + oc - ne;
     my_dr += __shfl_xor_sync(0xffffffffu, my_dr, o);
+    my_cs += __shfl_xor_sync(0xffffffffu, my_cs, o);
+    my_cq += __shfl_xor_sync(0xffffffffu, my_cq, o);
   }
   if (lane == 0) {
     sq[warp] = make_float2(sq_s, sq_c);
     dr[warp] = my_dr;
+    cs[warp] = my_cs;
+    cq[warp] = my_cq;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     float v = 0.f, vc = 0.f;
     int w = 0;
+    long long S = 0, Q = 0;
     for (int i = 0; i < kStatsWarps; ++i) {
       stats_kahan_add(sq[i].x, v, vc);
       vc += sq[i].y;
       w += dr[i];
+      S += cs[i];
+      Q += cq[i];
     }
     *balance = (N > 1 && Ttok > 0) ? (v - vc) / float(N - 1) : 0.f;
     *dropped = w;
+    if (cv_squared) {
+      float r = 0.f;
+      if (N > 1 && S > 0) {
+        const unsigned __int128 nq = (unsigned __int128)(unsigned long long)N *
+                                     (unsigned long long)Q;
+        const unsigned __int128 s2 = (unsigned __int128)(unsigned long long)S *
+                                     (unsigned long long)S;
+        const unsigned __int128 num = nq - s2;            // >= 0 (Cauchy-Schwarz)
+        const double numd = double((unsigned long long)(num >> 64)) * 18446744073709551616.0 +
+                            double((unsigned long long)num);
+        const double sd = double(S);
+        r = float(double(N) * numd / (double(N - 1) * sd * sd));
+      }
+      *cv_squared = r;
+    }
   }
 }
 

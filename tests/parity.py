@@ -22,6 +22,7 @@ TOL = {0: 1e-4, 1: 2e-2}          # by dtype code: fp32, bf16
 GATE_RTOL = 1e-5
 MEAN_PROB_RTOL = 1e-5
 BALANCE_RTOL = 1e-4
+CV_RTOL = 1e-7             # one fp32 rounding of an almost exact fp64 value
 
 
 def to64(t: torch.Tensor) -> np.ndarray:
@@ -130,6 +131,11 @@ def check_layer(wl, cfg, tensors, out, tokens=None, capacity=None, check_logits=
     bal = float(out.balance.cpu().item())
     assert abs(bal - ref.balance) <= BALANCE_RTOL * abs(ref.balance) + 1e-9, \
         f"balance {bal} vs {ref.balance}"
+    if out.cv_squared is not None:
+        # exact integer sums, then one fp64 quotient rounded to fp32
+        cv = float(out.cv_squared.cpu().item())
+        assert abs(cv - ref.cv_squared) <= CV_RTOL * abs(ref.cv_squared), \
+            f"cv_squared {cv} vs {ref.cv_squared}"
     # output rows
     y_gpu = out.y.float().cpu().numpy().astype(np.float64)
     rows = ref.tokens

@@ -125,10 +125,11 @@ def test_stages_through_the_abi():
     mean_prob = torch.empty(N, dtype=torch.float32, device=dev)
     balance = torch.empty(1, dtype=torch.float32, device=dev)
     dropped = torch.empty(1, dtype=torch.int32, device=dev)
-    B.load_stats(cfg, pp, counts, kept, mean_prob, balance, dropped)
+    cv2 = torch.empty(1, dtype=torch.float32, device=dev)
+    B.load_stats(cfg, pp, counts, kept, mean_prob, balance, dropped, cv2)
     torch.cuda.synchronize()
 
-    out = B.Outputs(y, idx, w, counts, kept, dropped, mean_prob, balance, logits)
+    out = B.Outputs(y, idx, w, counts, kept, dropped, mean_prob, balance, logits, cv2)
     report, ref = check_layer(wl, cfg, t, out)
     assert ref.grouping.dropped > 0                   # the capacity bites
     check_grouping(cfg, t["x"], offsets, row_token, token_row, Xp, ref.grouping, T)
@@ -158,6 +159,7 @@ def test_edge_cases_tokens_0_and_1():
     assert out0.counts.cpu().sum().item() == 0
     assert out0.dropped.cpu().item() == 0
     assert out0.balance.cpu().item() == 0.0
+    assert out0.cv_squared.cpu().item() == 0.0
 
 
 def test_capacity_one_and_all_tokens_to_one_expert():
@@ -175,6 +177,8 @@ def test_capacity_one_and_all_tokens_to_one_expert():
         assert kept0 == (cap if cap > 0 else 260)
         # balance of a collapsed router: every token puts the same p on expert 0
         assert ref.grouping.counts.tolist() == [260, 0, 0, 0]
+        # all assignments on one of N experts: cv^2 = N exactly
+        assert out.cv_squared.cpu().item() == 4.0
 
 
 def test_deterministic_bitwise():
@@ -184,7 +188,8 @@ def test_deterministic_bitwise():
     out2 = layer.forward(t["x"], with_logits=True)
     torch.cuda.synchronize()
     for a, b in [(out1.y, out2.y), (out1.topk_idx, out2.topk_idx), (out1.topk_w, out2.topk_w),
-                 (out1.mean_prob, out2.mean_prob), (out1.balance, out2.balance)]:
+                 (out1.mean_prob, out2.mean_prob), (out1.balance, out2.balance),
+                 (out1.cv_squared, out2.cv_squared)]:
         assert torch.equal(a, b)
 
 

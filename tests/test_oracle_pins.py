@@ -252,6 +252,29 @@ def test_balance_closed_forms():
 
 # --- number format -----------------------------------------------------------
 
+def test_cv_squared_closed_forms():
+    """Uniform counts give 0; all of S assignments on one of N experts give
+    exactly N (var = S^2/N, mean^2 = S^2/N^2); two experts with counts (a, b)
+    give 2(a-b)^2/(a+b)^2; one expert or nothing routed gives 0."""
+    assert O.cv_squared([5, 5, 5, 5]) == 0.0
+    for N in (2, 3, 8, 64):
+        c = np.zeros(N, dtype=np.int64)
+        c[N // 2] = 1000
+        assert O.cv_squared(c) == pytest.approx(float(N), rel=1e-14)
+    for a, b in [(3, 1), (10, 0), (7, 9)]:
+        assert O.cv_squared([a, b]) == pytest.approx(2 * (a - b) ** 2 / (a + b) ** 2, rel=1e-14)
+    assert O.cv_squared([17]) == 0.0
+    assert O.cv_squared([0, 0, 0]) == 0.0
+    # the forward reports it for the routed counts (before capacity)
+    x, W_g, b_g, W1, b1, W2, b2, _ = _layer(_rng(11), 40, 8, 16, 4)
+    out = O.moe_forward(x, W_g, b_g, W1, b1, W2, b2, k=2, act=O.ACT_RELU, capacity=5)
+    c = out.grouping.counts
+    assert c.sum() == 80 and out.grouping.kept.max() <= 5
+    mean = 80 / 4
+    assert out.cv_squared == pytest.approx(sum((ci - mean) ** 2 for ci in c) / 3 / mean ** 2,
+                                           rel=1e-12)
+
+
 def test_round_to_bf16_matches_torch():
     rng = _rng(11)
     v = np.concatenate([rng.normal(0, 1, 5000), rng.normal(0, 1e-3, 500),
