@@ -30,6 +30,13 @@ float64 numpy, with no blocking, fusion or reordering beyond the definition:
   roadtointelligence.com "Total versus active parameters" (DeepSeek-V3).
 * balance statistic std(mean_t router_probs)^2 with torch's default
   (unbiased) std -- botmartz.com "Load Balancing: The Hidden Challenge".
+* expert-choice routing: each expert takes the tokens it scores highest
+  instead of each token taking its top-k experts, so every expert gets the same
+  load -- matteuscruz.github.io "Load balancing: the core training challenge"
+  (Zhou et al., 2022, as the page describes it).  Readings: the score is the
+  router probability p[t, e]; an expert takes C tokens (C = the capacity,
+  clamped to T; C <= 0 means all T); ties go to the lower token index; a picked
+  token's gate is p[t, e]; a token no expert picked outputs 0.
 * squared coefficient of variation of the expert counts, the quantity the
   auxiliary loss penalises -- matteuscruz.github.io "Load balancing: the core
   training challenge"; named cv_squared(expert_counts) in invest-in.ai
@@ -342,3 +349,89 @@ def moe_bruteforce(x, W_g, b_g, W1, b1, W2, b2, *, k, act, capacity=0,
     if shared is not None:
         y += expert_ffn(x, *shared, act)
     return y
+
+
+# ---------------------------------------------------------------------------
+# expert-choice routing
+# ---------------------------------------------------------------------------
+
+def expert_choice_tokens(T, capacity):
+    """Tokens each expert takes: the capacity, clamped to T; <= 0 means T."""
+    return T if capacity <= 0 else min(int(capacity), T)
+
+
+def expert_choice_select(p, C):
+    """For every expert e, the C tokens with the largest p[t, e], the lower
+    token index first among equal scores (matteuscruz.github.io "Load balancing:
+    the core training challenge": each expert selects its top tokens).  Returns
+    a list of N int arrays, each in ascending token order."""
+    p = np.asarray(p, dtype=np.float64)
+    T, N = p.shape
+    sel = []
+    for e in range(N):
+        order = np.lexsort((np.arange(T), -p[:, e]))   # by score descending, then token
+        sel.append(np.sort(order[:C]).astype(np.int64))
+    return sel
+
+
+def expert_choice_gap(p, C):
+    """Per expert, the score gap between its C-th and (C+1)-th largest token
+    (inf when C = T or C = 0)."""
+    p = np.asarray(p, dtype=np.float64)
+    T, N = p.shape
+    gaps = np.full(N, np.inf)
+    if 0 < C < T:
+        srt = -np.sort(-p, axis=0)
+        gaps = srt[C - 1] - srt[C]
+    return gaps
+
+
+@dataclass
+class ExpertChoiceOutput:
+    y: np.ndarray            # [len(tokens), d]
+    tokens: np.ndarray
+    z: np.ndarray            # [T, N]
+    p: np.ndarray            # [T, N]
+    sel: list                # N arrays of picked tokens, ascending
+    gate: list               # N arrays: p[sel[e], e]
+    token_picks: np.ndarray  # [T] experts that picked each token
+    unpicked: int            # tokens no expert picked
+    mean_prob: np.ndarray
+    balance: float
+
+
+def expert_choice_forward(x, W_g, b_g, W1, b1, W2, b2, *, capacity, act, shared=None,
+                          round_hidden_bf16=False, tokens=None, sel_override=None):
+    """The layer with expert-choice routing: router scores and softmax as in
+    top-k routing, then every expert e runs its FFN on its C picked tokens and
+    y[t] = sum over the experts that picked t of p[t, e] * expert_e(x[t])
+    (+ the shared expert with weight 1).  ``sel_override`` replaces the
+    selection (used only for experts whose C-th score gap is a near-tie)."""
+    x = np.asarray(x, dtype=np.float64)
+    T = x.shape[0]
+    N = np.asarray(b_g).shape[0]
+    z = router_logits(x, W_g, b_g)
+    p = softmax(z)
+    C = expert_choice_tokens(T, capacity)
+    sel = expert_choice_select(p, C) if sel_override is None else \
+        [np.asarray(s_, dtype=np.int64) for s_ in sel_override]
+    gate = [p[s_, e] for e, s_ in enumerate(sel)]
+    picks = np.zeros(T, dtype=np.int64)
+    for s_ in sel:
+        picks[s_] += 1
+    mean_prob, balance = balance_statistic(p)
+    tokens = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    pos = {int(t): i for i, t in enumerate(tokens)}
+    y = np.zeros((len(tokens), x.shape[1]), dtype=np.float64)
+    for e in range(N):
+        ts = np.array([t for t in sel[e] if int(t) in pos], dtype=np.int64)
+        if ts.size == 0:
+            continue
+        o = expert_ffn(x[ts], W1[e], b1[e], W2[e], b2[e], act, round_hidden_bf16)
+        for r, t in enumerate(ts):
+            y[pos[int(t)]] += p[t, e] * o[r]
+    if shared is not None:
+        W1s, b1s, W2s, b2s = shared
+        y += expert_ffn(x[tokens], W1s, b1s, W2s, b2s, act, round_hidden_bf16)
+    return ExpertChoiceOutput(y, tokens, z, p, sel, gate, picks, int((picks == 0).sum()),
+                              mean_prob, balance)

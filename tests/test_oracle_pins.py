@@ -283,3 +283,105 @@ def test_round_to_bf16_matches_torch():
     v = np.concatenate([v, ties])
     ref = torch.from_numpy(v).to(torch.bfloat16).to(torch.float64).numpy()
     np.testing.assert_array_equal(O.round_to_bf16(v.astype(np.float64)), ref)
+
+
+# --- expert-choice routing ------------------------------------------------
+
+def _bruteforce_pick(col, C):
+    """The C-subset of tokens with the largest total score; among equal totals
+    the lexicographically smallest ascending index tuple.  With distinct scores
+    that is the top C; with ties at the cut it keeps the lower token indices."""
+    import itertools
+    best, best_key = None, None
+    for sub in itertools.combinations(range(len(col)), C):
+        key = (-sum(col[list(sub)]), sub)
+        if best_key is None or key < best_key:
+            best, best_key = sub, key
+    return np.array(best, dtype=np.int64)
+
+
+def test_expert_choice_select_against_subset_bruteforce():
+    rng = _rng(41)
+    for trial in range(30):
+        T = int(rng.integers(1, 8))
+        N = int(rng.integers(1, 5))
+        # a few distinct levels (dyadic, so the subset sums are exact), many ties
+        p = rng.integers(0, 4, (T, N)) / 8.0
+        for C in range(0, T + 1):
+            sel = O.expert_choice_select(p, C)
+            for e in range(N):
+                np.testing.assert_array_equal(sel[e], _bruteforce_pick(p[:, e], C))
+
+
+def test_expert_choice_hand_case_and_balance():
+    p = np.array([[0.9, 0.1], [0.2, 0.8], [0.6, 0.4], [0.6, 0.4]])
+    sel = O.expert_choice_select(p, 2)
+    assert sel[0].tolist() == [0, 2]          # 0.9, then the tie 0.6 / 0.6 -> token 2
+    assert sel[1].tolist() == [1, 2]          # 0.8, then the tie 0.4 / 0.4 -> token 2
+    gaps = O.expert_choice_gap(p, 2)
+    assert gaps.tolist() == [0.0, 0.0]
+    assert O.expert_choice_gap(p, 1).tolist() == pytest.approx([0.3, 0.4])
+    assert np.isinf(O.expert_choice_gap(p, 4)).all()
+    assert O.expert_choice_tokens(100, 0) == 100
+    assert O.expert_choice_tokens(100, 250) == 100
+    assert O.expert_choice_tokens(100, 25) == 25
+    # perfect balance by construction: every expert takes exactly C tokens
+    x, W_g, b_g, W1, b1, W2, b2, _ = _layer(_rng(42), 37, 8, 16, 5)
+    out = O.expert_choice_forward(x, W_g, b_g, W1, b1, W2, b2, capacity=9, act=O.ACT_RELU)
+    assert [len(s) for s in out.sel] == [9] * 5
+    assert out.token_picks.sum() == 45
+    assert out.unpicked == int((out.token_picks == 0).sum())
+    assert O.cv_squared([len(s) for s in out.sel]) == 0.0
+    for e in range(5):
+        assert np.all(np.diff(out.sel[e]) > 0)
+        # every picked score is at least every unpicked one
+        rest = np.setdiff1d(np.arange(37), out.sel[e])
+        assert out.p[out.sel[e], e].min() >= out.p[rest, e].max()
+
+
+def test_expert_choice_all_tokens_equals_soft_mixture():
+    """C = T: every expert takes every token, so y = sum_e p[t, e] expert_e(x):
+    top-k routing with k = N (gates renormalised over all N are p)."""
+    x, W_g, b_g, W1, b1, W2, b2, shared = _layer(_rng(43), 12, 8, 16, 4, fs=16)
+    for cap in (0, 12, 50):
+        ec = O.expert_choice_forward(x, W_g, b_g, W1, b1, W2, b2, capacity=cap,
+                                     act=O.ACT_GELU_ERF, shared=shared)
+        ref = O.moe_bruteforce(x, W_g, b_g, W1, b1, W2, b2, k=4, act=O.ACT_GELU_ERF,
+                               shared=shared)
+        np.testing.assert_allclose(ec.y, ref, rtol=1e-12, atol=1e-12)
+        assert ec.unpicked == 0
+
+
+def test_expert_choice_single_expert_is_dense_ffn():
+    d, f = 8, 16
+    x, W_g, b_g, W1, b1, W2, b2, _ = _layer(_rng(44), 10, d, f, 1)
+    out = O.expert_choice_forward(x, W_g, b_g, W1, b1, W2, b2, capacity=0, act=O.ACT_GELU_ERF)
+    lin1 = torch.nn.Linear(d, f, dtype=torch.float64)
+    lin2 = torch.nn.Linear(f, d, dtype=torch.float64)
+    with torch.no_grad():
+        lin1.weight.copy_(torch.from_numpy(W1[0])); lin1.bias.copy_(torch.from_numpy(b1[0]))
+        lin2.weight.copy_(torch.from_numpy(W2[0])); lin2.bias.copy_(torch.from_numpy(b2[0]))
+        dense = lin2(torch.nn.GELU()(lin1(torch.from_numpy(x)))).numpy()
+    np.testing.assert_allclose(out.y, dense, rtol=1e-12, atol=1e-12)
+
+
+def test_expert_choice_forward_equals_masked_bruteforce():
+    """Every expert on every token, then the pick mask (chosen by the subset
+    brute force) and the p gates; unpicked tokens get only the shared expert."""
+    for seed, (T, N, C, fs) in enumerate([(7, 3, 2, 0), (6, 4, 1, 16), (8, 2, 5, 0)]):
+        x, W_g, b_g, W1, b1, W2, b2, shared = _layer(_rng(50 + seed), T, 8, 16, N, fs=fs)
+        out = O.expert_choice_forward(x, W_g, b_g, W1, b1, W2, b2, capacity=C,
+                                      act=O.ACT_RELU, shared=shared)
+        p = torch.softmax(torch.from_numpy(x @ W_g.T + b_g), dim=1).numpy()
+        y = np.zeros_like(x)
+        for e in range(N):
+            mask = np.zeros(T, dtype=bool)
+            mask[_bruteforce_pick(p[:, e], C)] = True
+            h = np.maximum(x @ W1[e].T + b1[e], 0.0)
+            y[mask] += p[mask, e][:, None] * (h @ W2[e].T + b2[e])[mask]
+        if shared is not None:
+            y += np.maximum(x @ shared[0].T + shared[1], 0.0) @ shared[2].T + shared[3]
+        np.testing.assert_allclose(out.y, y, rtol=1e-12, atol=1e-12)
+        if shared is None:
+            for t in np.nonzero(out.token_picks == 0)[0]:
+                assert np.all(out.y[t] == 0.0)
