@@ -184,6 +184,10 @@ def oracle_step(tensors, wl, tokens):
         if wl.capacity_factor > 0 else 0
 
     def run():
+        if wl.expert_choice:
+            return O.expert_choice_forward(x, W["W_g"], W["b_g"], W["W1"], W["b1"], W["W2"],
+                                           W["b2"], capacity=cap, act=wl.act, shared=shared,
+                                           round_hidden_bf16=(wl.dtype == 1))
         return O.moe_forward(x, W["W_g"], W["b_g"], W["W1"], W["b1"], W["W2"], W["b2"],
                              k=wl.top_k, act=wl.act, capacity=cap,
                              renormalize=bool(wl.renormalize), shared=shared,
@@ -203,7 +207,9 @@ def oracle_threads():
 
 def cpu_sample_tokens(wl):
     # a sample that keeps one oracle pass to a few seconds of host work
-    per_token_flop = 4.0 * wl.d_model * wl.d_ff * wl.top_k + 4.0 * wl.d_model * wl.d_ff_shared
+    from sparse_mixture_experts_68_b300.workloads import routed_rows
+    per_token_flop = (4.0 * wl.d_model * wl.d_ff * routed_rows(wl) / max(wl.T, 1)
+                      + 4.0 * wl.d_model * wl.d_ff_shared)
     return int(max(16, min(wl.T, 2.0e10 / per_token_flop)))
 
 
@@ -244,6 +250,55 @@ def run_reference(args, wl, rank, world):
 # the CUDA path
 
 STAGES = ("router_topk", "permute", "ffn_linear1", "ffn_linear2", "combine", "load_stats")
+EC_STAGES = ("router_probs", "select_and_copy", "ffn_linear1", "ffn_linear2", "combine",
+             "load_stats")
+
+
+class LayerCalls:
+    """The library calls one bench step makes: top-k routing (moe_forward) or
+    expert-choice routing (moe_ec_forward)."""
+
+    def __init__(self, wl, tensors, dev):
+        from sparse_mixture_experts_68_b300 import binding as B
+        self.B = B
+        self.ec = wl.expert_choice
+        if self.ec:
+            self.layer = B.MoeEcLayer(wl, tensors, device=dev)
+            self.out = B.alloc_ec_outputs(self.layer.cfg, dev)
+            self.stages = EC_STAGES
+            self.entry = "moe_ec_forward"
+        else:
+            self.layer = B.MoeLayer(wl, tensors, device=dev)
+            self.out = B.alloc_outputs(self.layer.cfg, dev)
+            self.stages = STAGES
+            self.entry = "moe_forward"
+        self.cfg = self.layer.cfg
+
+    def forward(self, x, stream):
+        B, L = self.B, self.layer
+        if self.ec:
+            B.ec_forward(L.cfg, x, L.weights, self.out, L.workspace, stream)
+        else:
+            B.forward(L.cfg, x, L.weights, self.out, L.workspace, stream)
+
+    def forward_profiled(self, x, events, stream):
+        B, L = self.B, self.layer
+        if self.ec:
+            B.ec_forward_profiled(L.cfg, x, L.weights, self.out, L.workspace, events, stream)
+        else:
+            B.forward_profiled(L.cfg, x, L.weights, self.out, L.workspace, events, stream)
+
+    def launch_count(self):
+        if self.ec:
+            return self.B.ec_forward_launch_count(self.cfg)
+        return self.B.forward_launch_count(self.cfg)
+
+    def kept(self):
+        """(routed rows the experts processed, experts with at least one row)"""
+        if self.ec:
+            C = self.B.ec_tokens_per_expert(self.cfg)
+            return self.cfg.n_experts * C, (self.cfg.n_experts if C > 0 else 0)
+        return int(self.out.kept.sum().item()), int((self.out.kept > 0).sum().item())
 
 
 def job_time_ms(local_ms: float, world: int, device=None) -> float:
@@ -274,8 +329,8 @@ def run_ours(args, wl, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     tensors = synth.make_layer(wl, device=dev)
-    layer = B.MoeLayer(wl, tensors, device=dev)
-    out = B.alloc_outputs(layer.cfg, dev)
+    calls = LayerCalls(wl, tensors, dev)
+    layer = calls.layer
     x = tensors["x"]
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
 
@@ -288,13 +343,12 @@ def run_ours(args, wl, rank, world, local_rank):
         for ev in events:
             ev.record(stream)               # creates the underlying CUDA events
         for _ in range(3):                  # warm: module loading, tensor-map setup
-            B.forward_profiled(layer.cfg, x, layer.weights, out, layer.workspace, events,
-                               stream)
-            B.forward(layer.cfg, x, layer.weights, out, layer.workspace, stream)
+            calls.forward_profiled(x, events, stream)
+            calls.forward(x, stream)
     stream.synchronize()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
-        B.forward(layer.cfg, x, layer.weights, out, layer.workspace, stream)
+        calls.forward(x, stream)
     torch.cuda.synchronize(dev)
 
     def flush_l2(i):
@@ -342,18 +396,17 @@ def run_ours(args, wl, rank, world, local_rank):
     for i in range(K):
         flush_l2(i)
         with torch.cuda.stream(stream):
-            B.forward_profiled(layer.cfg, x, layer.weights, out, layer.workspace, events,
-                               stream)
+            calls.forward_profiled(x, events, stream)
         stream.synchronize()                # read this step's events before the next
         stage_ms.append([events[s].elapsed_time(events[s + 1]) for s in range(6)])
         prof_step_ms.append(events[0].elapsed_time(events[6]))
     assert B.get_device_status() == B.MOE_OK
 
-    kept_rows = int(out.kept.sum().item())
-    n_kept_experts = int((out.kept > 0).sum().item())
+    kept_rows, n_kept_experts = calls.kept()
     T = layer.cfg.T
     value = job_tokens_per_s(T, K, world, total_ms)
-    mean_stage = {n: statistics.mean(s[i] for s in stage_ms) for i, n in enumerate(STAGES)}
+    mean_stage = {n: statistics.mean(s[i] for s in stage_ms)
+                  for i, n in enumerate(calls.stages)}
 
     # roofline of the dominant kernel: the tcgen05 grouped GEMM, launched once
     # per Linear (two launches per step)
@@ -401,20 +454,21 @@ def run_ours(args, wl, rank, world, local_rank):
         "config": {"workload": wl.name, "description": wl.description, "T": T,
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write)",
-                   "launch": "moe_forward captured once as a CUDA graph, replayed; per-kernel "
-                             "times from direct moe_forward_profiled calls"},
+                   "launch": f"{calls.entry} captured once as a CUDA graph, replayed; "
+                             f"per-kernel times from direct {calls.entry}_profiled calls"},
         "tflops": layer_flop / (total_ms / K * 1e-3) / 1e12,
         "layer_roofline_floor_ms": floor_ms,
         "layer_roofline_frac": floor_ms / (total_ms / K),
         "stage_ms": mean_stage,
         "profiled_ms_per_step": statistics.mean(prof_step_ms),
         "roofline": roof,
-        "gpu_launches": B.forward_launch_count(layer.cfg) * K,
+        "gpu_launches": calls.launch_count() * K,
         "clocks": clk,
     }
 
     if not args.no_e2e:
-        res["e2e"] = measure_e2e(args, layer, wl, dev)
+        res["e2e"] = measure_e2e_ec(args, calls, wl, dev) if calls.ec else \
+            measure_e2e(args, layer, wl, dev)
     return res
 
 
@@ -442,6 +496,42 @@ def measure_e2e(args, layer, wl, dev):
     d2h = T * wl.d_model * es + T * k * 8 + N * 12 + 8
     return {"value": T * K / dt, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "api": "moe_forward_host (host buffers, synchronous)"}
+
+
+def measure_e2e_ec(args, calls, wl, dev):
+    """Expert-choice layer end to end: x copied in from pinned host memory,
+    moe_ec_forward, y and the per-expert picks copied back, all on one stream
+    and inside the timed loop."""
+    import torch
+    cfg = calls.cfg
+    stream = torch.cuda.current_stream(dev)
+    xh = calls.layer.t["x"].cpu().pin_memory()
+    xd = torch.empty_like(calls.layer.t["x"])
+    o = calls.out
+    yh = torch.empty(o.y.shape, dtype=o.y.dtype).pin_memory()
+    th = torch.empty(o.ec_token.shape, dtype=o.ec_token.dtype).pin_memory()
+    gh = torch.empty(o.ec_gate.shape, dtype=o.ec_gate.dtype).pin_memory()
+
+    def step():
+        xd.copy_(xh, non_blocking=True)
+        calls.forward(xd, stream)
+        yh.copy_(o.y, non_blocking=True)
+        th.copy_(o.ec_token, non_blocking=True)
+        gh.copy_(o.ec_gate, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        step()
+    K = args.steps
+    t0 = time.perf_counter()
+    for _ in range(K):
+        step()
+    dt = time.perf_counter() - t0
+    es = wl.elem_bytes
+    T = cfg.T
+    return {"value": T * K / dt, "unit": "tokens/s", "h2d_bytes_per_step": T * wl.d_model * es,
+            "d2h_bytes_per_step": T * wl.d_model * es + th.numel() * 4 + gh.numel() * 4,
+            "api": "moe_ec_forward between pinned host copies on its stream (synchronous)"}
 
 
 def cpu_baseline(wl):

@@ -274,6 +274,92 @@ moe_status moe_forward_host(const moe_config* cfg, const void* x_host, const moe
  * "Code").  Lets callers check the activation against other implementations. */
 moe_status moe_activation(int32_t act, const float* x, float* y, int64_t n, void* stream);
 
+/* ---- expert-choice routing -------------------------------------------------
+ *
+ * matteuscruz.github.io "What is a Mixture of Experts?", "Load balancing: the
+ * core training challenge": expert choice routing (Zhou et al., 2022) turns
+ * the routing around -- every expert selects the tokens it scores highest
+ * rather than every token selecting its top-k experts -- so each expert gets
+ * the same load by construction, and a token may be processed by any number
+ * of experts (none included).  The page gives only the idea; this library
+ * reads it as follows (the same readings as its CPU oracle):
+ *   - the score of token t for expert e is the router probability
+ *     p[t, e] = softmax over the N experts of z[t, :], z = x . W_g^T + b_g;
+ *   - every expert takes C = moe_ec_tokens_per_expert(cfg) tokens:
+ *     cfg->capacity clamped to T, or all T when capacity <= 0;
+ *   - among equal scores the lower token index is taken first;
+ *   - a picked token's gate is p[t, e], and
+ *       y[t] = sum over the experts e that picked t of p[t, e] * expert_e(x[t])
+ *     (+ the shared expert's output with weight 1), so a token no expert
+ *     picked gets y[t] = 0 (+ shared).
+ * cfg->top_k and cfg->renormalize are not read; every other field means what
+ * it does for top-k routing.  The routed rows live in N groups of
+ * round_up(C, MOE_GROUP_ALIGN) rows (expert e from row e * that), each in
+ * ascending token order, then the shared group as for top-k routing. */
+
+typedef struct moe_ec_outputs {
+  void    *y;           /* [T, d_model], cfg->dtype                         required */
+  int32_t *ec_token;    /* [N, C] tokens each expert picked, ascending       required */
+  float   *ec_gate;     /* [N, C] p[ec_token, e]: the gate of each pick      required */
+  int32_t *token_picks; /* [T] number of experts that picked each token      required */
+  int32_t *unpicked;    /* [1] tokens no expert picked                       required */
+  float   *mean_prob;   /* [N] mean over tokens of p                         required */
+  float   *balance;     /* [1] std_unbiased(mean_prob)^2                     required */
+  float   *logits;      /* [T, N] router scores z; NULL = keep in workspace         */
+} moe_ec_outputs;
+
+/* C, the tokens every expert takes; -1 for an invalid config. */
+int64_t moe_ec_tokens_per_expert(const moe_config* cfg);
+/* Rows of the grouped buffers: N * round_up(C, MOE_GROUP_ALIGN), plus T rounded
+ * up to MOE_GROUP_ALIGN with a shared expert; -1 for an invalid config. */
+int64_t moe_ec_rows_max(const moe_config* cfg);
+/* Bytes of device workspace moe_ec_forward needs; 0 for an invalid config. */
+size_t moe_ec_workspace_size(const moe_config* cfg);
+/* Kernels one moe_ec_forward launches; -1 for an invalid config. */
+int32_t moe_ec_forward_launch_count(const moe_config* cfg);
+
+/* Router step without the top-k: scores, probabilities and their block sums.
+ *   logits        out [T, N] fp32 scores z
+ *   probT         out [N, T] fp32 probabilities, expert-major (probT[e*T + t] = p[t, e])
+ *   token_picks   out [T] int32, set to 0 (moe_ec_select counts into it)
+ *   prob_partials out [moe_router_blocks(cfg), N] fp32, as for moe_router_topk */
+moe_status moe_ec_router(const moe_config* cfg, const void* x, const void* W_g, const void* b_g,
+                         float* logits, float* probT, int32_t* token_picks,
+                         float* prob_partials, void* stream);
+
+/* Selection and grouping: every expert's C highest-probability tokens.
+ *   probT       in  [N, T] fp32, p >= 0 (as moe_ec_router writes it)
+ *   ec_token    out [N, C] int32, ascending per expert
+ *   ec_gate     out [N, C] fp32, probT[e, ec_token[e, i]]
+ *   offsets     out [N + 2] int32: offsets[e] = e * round_up(C, 128); offsets[N]
+ *               = end of the routed groups; offsets[N + 1] = end of the shared group
+ *   counts      out [N] int32, all C
+ *   row_token   out [moe_ec_rows_max(cfg)] int32, token of each grouped row (-1 = padding)
+ *   token_row   out [T, N] int32, grouped row of (t, e), -1 where e did not pick t
+ *   token_w     out [T, N] fp32, p[t, e] where e picked t, else 0
+ *   token_picks in/out [T] int32, incremented once per pick: zero it first
+ * Exact: the selection compares the fp32 bit patterns, so it is reproducible
+ * and equal to a stable sort of each expert's column by (-p, t). */
+moe_status moe_ec_select(const moe_config* cfg, const float* probT, int32_t* ec_token,
+                         float* ec_gate, int32_t* offsets, int32_t* counts, int32_t* row_token,
+                         int32_t* token_row, float* token_w, int32_t* token_picks,
+                         void* stream);
+
+/* The whole expert-choice layer: ec_router -> ec_select -> row copy ->
+ * grouped FFN (the same kernels as top-k routing, every group C rows) ->
+ * combine (one slot per expert) -> statistics, on `stream`; workspace as for
+ * moe_forward but moe_ec_workspace_size(cfg) bytes. */
+moe_status moe_ec_forward(const moe_config* cfg, const void* x, const moe_weights* w,
+                          const moe_ec_outputs* out, void* workspace, size_t workspace_bytes,
+                          void* stream);
+
+/* moe_ec_forward with seven events at the step boundaries, as in
+ * moe_forward_profiled (events[2] follows the selection and the row copy,
+ * events[5] the combine, events[6] the statistics). */
+moe_status moe_ec_forward_profiled(const moe_config* cfg, const void* x, const moe_weights* w,
+                                   const moe_ec_outputs* out, void* workspace,
+                                   size_t workspace_bytes, void* const* events, void* stream);
+
 /* ---- status ---------------------------------------------------------------- */
 
 /* Synchronises `stream`, returns (and clears) the device status word:

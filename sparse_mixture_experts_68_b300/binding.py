@@ -31,6 +31,9 @@ EXPORTS = [
     "moe_set_wait_limit_ns", "moe_get_wait_limit_ns", "moe_selftest_bounded_wait",
     "moe_status_string", "moe_version", "moe_permute_noalloc", "moe_forward_profiled",
     "moe_forward_launch_count", "moe_activation",
+    "moe_ec_tokens_per_expert", "moe_ec_rows_max", "moe_ec_workspace_size",
+    "moe_ec_forward_launch_count", "moe_ec_router", "moe_ec_select", "moe_ec_forward",
+    "moe_ec_forward_profiled",
 ]
 PERMUTE_STATIC_SCRATCH_INTS = 1 << 18
 
@@ -58,6 +61,12 @@ class MoeOutputs(C.Structure):
                 ("counts", C.c_void_p), ("kept", C.c_void_p), ("dropped", C.c_void_p),
                 ("mean_prob", C.c_void_p), ("balance", C.c_void_p), ("logits", C.c_void_p),
                 ("cv_squared", C.c_void_p)]
+
+
+class MoeEcOutputs(C.Structure):
+    _fields_ = [("y", C.c_void_p), ("ec_token", C.c_void_p), ("ec_gate", C.c_void_p),
+                ("token_picks", C.c_void_p), ("unpicked", C.c_void_p),
+                ("mean_prob", C.c_void_p), ("balance", C.c_void_p), ("logits", C.c_void_p)]
 
 
 _lib = None
@@ -99,6 +108,17 @@ def lib() -> C.CDLL:
         "moe_get_wait_limit_ns": (C.c_uint64, []),
         "moe_selftest_bounded_wait": (C.c_int32, [C.c_uint64, P]),
         "moe_activation": (C.c_int32, [C.c_int32, P, P, C.c_int64, P]),
+        "moe_ec_tokens_per_expert": (C.c_int64, [CP]),
+        "moe_ec_rows_max": (C.c_int64, [CP]),
+        "moe_ec_workspace_size": (C.c_size_t, [CP]),
+        "moe_ec_forward_launch_count": (C.c_int32, [CP]),
+        "moe_ec_router": (C.c_int32, [CP, P, P, P, P, P, P, P, P]),
+        "moe_ec_select": (C.c_int32, [CP, P, P, P, P, P, P, P, P, P, P]),
+        "moe_ec_forward": (C.c_int32, [CP, P, C.POINTER(MoeWeights), C.POINTER(MoeEcOutputs),
+                                       P, C.c_size_t, P]),
+        "moe_ec_forward_profiled": (C.c_int32, [CP, P, C.POINTER(MoeWeights),
+                                                C.POINTER(MoeEcOutputs), P, C.c_size_t,
+                                                C.POINTER(C.c_void_p), P]),
         "moe_status_string": (C.c_char_p, [C.c_int32]),
         "moe_version": (C.c_int32, []),
     }
@@ -322,3 +342,104 @@ class MoeLayer:
         forward(self.cfg, x, self.weights, out, self.workspace, stream)
         return out
 
+
+# ---- expert-choice routing ---------------------------------------------------------
+
+def ec_tokens_per_expert(cfg: MoeConfig) -> int:
+    return int(lib().moe_ec_tokens_per_expert(C.byref(cfg)))
+
+
+def ec_rows_max(cfg: MoeConfig) -> int:
+    return int(lib().moe_ec_rows_max(C.byref(cfg)))
+
+
+def ec_workspace_size(cfg: MoeConfig) -> int:
+    return int(lib().moe_ec_workspace_size(C.byref(cfg)))
+
+
+def ec_forward_launch_count(cfg: MoeConfig) -> int:
+    return int(lib().moe_ec_forward_launch_count(C.byref(cfg)))
+
+
+def ec_router(cfg, x, W_g, b_g, logits, probT, token_picks, prob_partials, stream=None):
+    _check(lib().moe_ec_router(C.byref(cfg), _ptr(x), _ptr(W_g), _ptr(b_g), _ptr(logits),
+                               _ptr(probT), _ptr(token_picks), _ptr(prob_partials),
+                               _stream(stream)), "moe_ec_router")
+
+
+def ec_select(cfg, probT, ec_token, ec_gate, offsets, counts, row_token, token_row, token_w,
+              token_picks, stream=None):
+    _check(lib().moe_ec_select(C.byref(cfg), _ptr(probT), _ptr(ec_token), _ptr(ec_gate),
+                               _ptr(offsets), _ptr(counts), _ptr(row_token), _ptr(token_row),
+                               _ptr(token_w), _ptr(token_picks), _stream(stream)),
+           "moe_ec_select")
+
+
+@dataclass
+class EcOutputs:
+    y: torch.Tensor
+    ec_token: torch.Tensor
+    ec_gate: torch.Tensor
+    token_picks: torch.Tensor
+    unpicked: torch.Tensor
+    mean_prob: torch.Tensor
+    balance: torch.Tensor
+    logits: torch.Tensor | None = None
+
+    def struct(self) -> MoeEcOutputs:
+        return MoeEcOutputs(_ptr(self.y), _ptr(self.ec_token), _ptr(self.ec_gate),
+                            _ptr(self.token_picks), _ptr(self.unpicked), _ptr(self.mean_prob),
+                            _ptr(self.balance), _ptr(self.logits))
+
+
+def alloc_ec_outputs(cfg: MoeConfig, device, with_logits=False) -> EcOutputs:
+    T, N, d = cfg.T, cfg.n_experts, cfg.d_model
+    Cn = ec_tokens_per_expert(cfg)
+    dt = torch.float32 if cfg.dtype == MOE_F32 else torch.bfloat16
+    kw = dict(device=device)
+    return EcOutputs(
+        y=torch.empty((T, d), dtype=dt, **kw),
+        ec_token=torch.empty((N, Cn), dtype=torch.int32, **kw),
+        ec_gate=torch.empty((N, Cn), dtype=torch.float32, **kw),
+        token_picks=torch.empty((T,), dtype=torch.int32, **kw),
+        unpicked=torch.empty((1,), dtype=torch.int32, **kw),
+        mean_prob=torch.empty((N,), dtype=torch.float32, **kw),
+        balance=torch.empty((1,), dtype=torch.float32, **kw),
+        logits=torch.empty((T, N), dtype=torch.float32, **kw) if with_logits else None)
+
+
+def ec_forward(cfg: MoeConfig, x, weights: MoeWeights, out: EcOutputs, workspace, stream=None):
+    _check(lib().moe_ec_forward(C.byref(cfg), _ptr(x), C.byref(weights), C.byref(out.struct()),
+                                _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                _stream(stream)), "moe_ec_forward")
+
+
+def ec_forward_profiled(cfg: MoeConfig, x, weights: MoeWeights, out: EcOutputs, workspace,
+                        events, stream=None):
+    assert len(events) == 7
+    handles = (C.c_void_p * 7)(*[ev.cuda_event if ev is not None else None for ev in events])
+    _check(lib().moe_ec_forward_profiled(C.byref(cfg), _ptr(x), C.byref(weights),
+                                         C.byref(out.struct()), _ptr(workspace),
+                                         workspace.numel() * workspace.element_size(), handles,
+                                         _stream(stream)), "moe_ec_forward_profiled")
+
+
+class MoeEcLayer:
+    """A layer with expert-choice routing: weights, workspace, ``forward``."""
+
+    def __init__(self, wl: Workload, tensors: dict, device="cuda", T: int | None = None,
+                 capacity: int | None = None):
+        self.wl = wl
+        self.t = tensors
+        self.device = torch.device(device)
+        self.cfg = make_config(wl, T=T, capacity=capacity)
+        self.weights = make_weights(tensors)
+        self.workspace = torch.empty(max(ec_workspace_size(self.cfg), 256), dtype=torch.uint8,
+                                     device=self.device)
+
+    def forward(self, x, out: EcOutputs | None = None, with_logits=False,
+                stream=None) -> EcOutputs:
+        if out is None:
+            out = alloc_ec_outputs(self.cfg, self.device, with_logits=with_logits)
+        ec_forward(self.cfg, x, self.weights, out, self.workspace, stream)
+        return out

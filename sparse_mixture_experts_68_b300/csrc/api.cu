@@ -87,6 +87,84 @@ Workspace layout(const moe_config& c, void* base) {
   return w;
 }
 
+// ---- expert-choice routing ----
+
+int64_t ec_tokens_of(const moe_config& c) {
+  return c.capacity <= 0 ? c.T : (c.capacity < c.T ? c.capacity : c.T);
+}
+
+int64_t ec_rows_max_of(const moe_config& c) {
+  int64_t r = c.n_experts * ec_group_rows(ec_tokens_of(c));
+  if (c.d_ff_shared > 0) r += round_up(c.T, kGroupAlign);
+  return r;
+}
+
+// the top-k fields are not read; everything else as for top-k routing
+moe_status check_ec_config(const moe_config* cfg) {
+  if (!cfg) return MOE_ERR_INVALID_ARG;
+  moe_config c = *cfg;
+  c.top_k = 1;
+  c.renormalize = 1;
+  const moe_status st = check_config(&c);
+  if (st != MOE_OK) return st;
+  if (ec_rows_max_of(c) >= (int64_t(1) << 31) || c.T * c.n_experts >= (int64_t(1) << 31))
+    return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+// the layer configuration the shared kernels see: one combine slot per expert
+moe_config ec_kernel_config(const moe_config& c) {
+  moe_config k = c;
+  k.top_k = c.n_experts;
+  k.capacity = 0;
+  k.renormalize = 1;
+  return k;
+}
+
+struct EcWorkspace {
+  float* logits;
+  float* probT;
+  float* prob_partials;
+  int32_t* offsets;
+  int32_t* counts;
+  int32_t* row_token;
+  int32_t* token_row;
+  float* token_w;
+  int32_t* scratch;
+  void* Xp;
+  void* H;
+  void* Yp;
+  size_t bytes;
+};
+
+EcWorkspace ec_layout(const moe_config& c, void* base) {
+  EcWorkspace w{};
+  uintptr_t p = reinterpret_cast<uintptr_t>(base);
+  size_t off = 0;
+  auto take = [&](size_t n) {
+    const size_t at = off;
+    off += (n + 255) / 256 * 256;
+    return reinterpret_cast<void*>(p + at);
+  };
+  const int64_t rows = ec_rows_max_of(c);
+  const int64_t es = elem_bytes(c);
+  const size_t tn = size_t(c.T * c.n_experts) * 4;
+  w.logits = static_cast<float*>(take(tn));
+  w.probT = static_cast<float*>(take(tn));
+  w.prob_partials = static_cast<float*>(take(size_t(router_blocks_of(c) * c.n_experts) * 4));
+  w.offsets = static_cast<int32_t*>(take(size_t(c.n_experts + 2) * 4));
+  w.counts = static_cast<int32_t*>(take(size_t(c.n_experts) * 4));
+  w.row_token = static_cast<int32_t*>(take(size_t(rows) * 4));
+  w.token_row = static_cast<int32_t*>(take(tn));
+  w.token_w = static_cast<float*>(take(tn));
+  w.scratch = static_cast<int32_t*>(take(4));
+  w.Xp = take(size_t(rows * c.d_model * es));
+  w.H = take(size_t(rows * c.d_ff * es));
+  w.Yp = take(size_t(rows * c.d_model * es));
+  w.bytes = off;
+  return w;
+}
+
 // Device status word address and SM count, per device.
 struct DeviceInfo {
   int32_t* status = nullptr;
@@ -385,8 +463,8 @@ size_t moe_host_workspace_size(const moe_config* cfg) {
   auto r = [](size_t n) { return (n + 255) / 256 * 256; };
   const size_t es = size_t(elem_bytes(c));
   return layout(c, nullptr).bytes + 2 * r(size_t(c.T * c.d_model) * es) +
-         2 * r(size_t(c.T * c.top_k) * 4) + 3 * r(size_t(c.n_experts) * 4) + 2 * r(4) +
-         r(size_t(c.T * c.n_experts) * 4);
+         2 * r(size_t(c.T * c.top_k) * 4) + 3 * r(size_t(c.n_experts) * 4) + 3 * r(4) +
+         r(size_t(c.T * c.n_experts) * 4);   // dropped, balance, cv_squared; logits
 }
 
 moe_status moe_forward_host(const moe_config* cfg, const void* x_host, const moe_weights* w,
@@ -442,6 +520,146 @@ moe_status moe_forward_host(const moe_config* cfg, const void* x_host, const moe
     if (cp.n && cudaMemcpyAsync(cp.dst, cp.src, cp.n, cudaMemcpyDeviceToHost, s) != cudaSuccess)
       return MOE_ERR_CUDA;
   return cuda_status(cudaStreamSynchronize(s));
+}
+
+// ---- expert-choice routing --------------------------------------------------------
+
+int64_t moe_ec_tokens_per_expert(const moe_config* cfg) {
+  if (check_ec_config(cfg) != MOE_OK) return -1;
+  return ec_tokens_of(*cfg);
+}
+
+int64_t moe_ec_rows_max(const moe_config* cfg) {
+  if (check_ec_config(cfg) != MOE_OK) return -1;
+  return ec_rows_max_of(*cfg);
+}
+
+size_t moe_ec_workspace_size(const moe_config* cfg) {
+  if (check_ec_config(cfg) != MOE_OK) return 0;
+  return ec_layout(*cfg, nullptr).bytes;
+}
+
+int32_t moe_ec_forward_launch_count(const moe_config* cfg) {
+  if (check_ec_config(cfg) != MOE_OK) return -1;
+  const moe_config& c = *cfg;
+  if (c.T == 0) return 2;                          // selection (group offsets), statistics
+  const int router = (c.dtype == MOE_BF16 && c.n_experts % 64 == 0) ? 2
+                                                                      : router_launch_count(c);
+  return router + 1 + 1 + 2 + 1 + 1;   // router, select, row copy, two Linears, combine, stats
+}
+
+moe_status moe_ec_router(const moe_config* cfg, const void* x, const void* W_g, const void* b_g,
+                         float* logits, float* probT, int32_t* token_picks,
+                         float* prob_partials, void* stream) {
+  moe_status st = check_ec_config(cfg);
+  if (st != MOE_OK) return st;
+  if (cfg->T == 0) return MOE_OK;
+  const void* ps[] = {x, W_g, b_g, logits, probT, token_picks, prob_partials};
+  for (const void* q : ps)
+    if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  DeviceInfo di;
+  if (!device_info(&di)) return MOE_ERR_CUDA;
+  return cuda_status(launch_router_probs(*cfg, x, W_g, b_g, logits, probT, token_picks,
+                                         prob_partials, di.num_sms, di.status,
+                                         g_wait_limit_ns.load(),
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_ec_select(const moe_config* cfg, const float* probT, int32_t* ec_token,
+                         float* ec_gate, int32_t* offsets, int32_t* counts, int32_t* row_token,
+                         int32_t* token_row, float* token_w, int32_t* token_picks,
+                         void* stream) {
+  moe_status st = check_ec_config(cfg);
+  if (st != MOE_OK) return st;
+  const moe_config& c = *cfg;
+  if (!offsets || !counts || !aligned16(offsets) || !aligned16(counts) ||
+      (ec_rows_max_of(c) > 0 && (!row_token || !aligned16(row_token))))
+    return MOE_ERR_INVALID_ARG;
+  if (c.T > 0) {
+    const void* ps[] = {probT, ec_token, ec_gate, token_row, token_w, token_picks};
+    for (const void* q : ps)
+      if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  }
+  return cuda_status(launch_ec_select(c, ec_tokens_of(c), probT, ec_token, ec_gate, offsets,
+                                      counts, row_token, token_row, token_w, token_picks,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+static moe_status ec_forward_impl(const moe_config* cfg, const void* x, const moe_weights* w,
+                                  const moe_ec_outputs* out, void* workspace,
+                                  size_t workspace_bytes, void* const* events, void* stream) {
+  moe_status st = check_ec_config(cfg);
+  if (st != MOE_OK) return st;
+  const moe_config& c = *cfg;
+  st = check_weights(c, w, true, true);
+  if (st != MOE_OK) return st;
+  auto token_buf_ok = [&](const void* q) { return c.T == 0 || (q && aligned16(q)); };
+  if (!out || !token_buf_ok(x) || !workspace ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return MOE_ERR_INVALID_ARG;
+  if (!token_buf_ok(out->y) || !token_buf_ok(out->ec_token) || !token_buf_ok(out->ec_gate) ||
+      !token_buf_ok(out->token_picks))
+    return MOE_ERR_INVALID_ARG;
+  if (!out->unpicked || !out->mean_prob || !out->balance || !aligned16(out->mean_prob))
+    return MOE_ERR_INVALID_ARG;
+  if (out->logits && !aligned16(out->logits)) return MOE_ERR_INVALID_ARG;
+  const EcWorkspace ws = ec_layout(c, workspace);
+  if (workspace_bytes < ws.bytes) return MOE_ERR_WORKSPACE;
+  DeviceInfo di;
+  if (!device_info(&di)) return MOE_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* logits = out->logits ? out->logits : ws.logits;
+  void* const none[7] = {};
+  void* const* ev = events ? events : none;
+  const int64_t C = ec_tokens_of(c), rows = ec_rows_max_of(c);
+  const moe_config kc = ec_kernel_config(c);
+
+  cudaError_t e = record_event(ev[0], s);
+  if (e == cudaSuccess)
+    e = launch_router_probs(c, x, w->W_g, w->b_g, logits, ws.probT, out->token_picks,
+                            ws.prob_partials, di.num_sms, di.status, g_wait_limit_ns.load(), s);
+  if (e == cudaSuccess) e = record_event(ev[1], s);
+  if (e == cudaSuccess)
+    e = launch_ec_select(c, C, ws.probT, out->ec_token, out->ec_gate, ws.offsets, ws.counts,
+                         ws.row_token, ws.token_row, ws.token_w, out->token_picks, s);
+  if (e == cudaSuccess && c.T > 0)
+    e = launch_row_copy(c, x, ws.offsets, ws.row_token, ws.Xp, rows, s);
+  if (e == cudaSuccess) e = record_event(ev[2], s);
+  if (e == cudaSuccess && c.T > 0) {
+    GroupedFfnArgs a{};
+    a.Xp = ws.Xp; a.offsets = ws.offsets; a.kept = ws.counts; a.w = w; a.H = ws.H;
+    a.Yp = ws.Yp; a.rows_max = rows; a.status = di.status;
+    a.wait_limit_ns = g_wait_limit_ns.load(); a.num_sms = di.num_sms;
+    a.mid_event = ev[3];
+    a.routed_rows = c.n_experts * C;
+    e = c.dtype == MOE_F32 ? launch_grouped_ffn_f32(kc, a, s) : launch_grouped_ffn_bf16(kc, a, s);
+  }
+  if (e == cudaSuccess) e = record_event(ev[4], s);
+  if (e == cudaSuccess)
+    e = launch_combine(kc, ws.Yp, ws.token_row, ws.token_w, ws.offsets, out->y, s);
+  if (e == cudaSuccess) e = record_event(ev[5], s);
+  if (e == cudaSuccess)
+    e = launch_ec_stats(c, ws.prob_partials, ws.counts, out->token_picks, out->mean_prob,
+                        out->balance, ws.scratch, out->unpicked, s);
+  if (e == cudaSuccess) e = record_event(ev[6], s);
+  return cuda_status(e);
+}
+
+moe_status moe_ec_forward(const moe_config* cfg, const void* x, const moe_weights* w,
+                          const moe_ec_outputs* out, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+  return ec_forward_impl(cfg, x, w, out, workspace, workspace_bytes, nullptr, stream);
+}
+
+moe_status moe_ec_forward_profiled(const moe_config* cfg, const void* x, const moe_weights* w,
+                                   const moe_ec_outputs* out, void* workspace,
+                                   size_t workspace_bytes, void* const* events, void* stream) {
+  if (!events) return MOE_ERR_INVALID_ARG;
+  pdl_enabled() = false;
+  const moe_status st =
+      ec_forward_impl(cfg, x, w, out, workspace, workspace_bytes, events, stream);
+  pdl_enabled() = true;
+  return st;
 }
 
 moe_status moe_get_device_status(void* stream) {

@@ -6,6 +6,10 @@
 // one warp per token, fp32 accumulation in slot order, 16-byte vectors.
 // Dropped slots (token_row < 0) add nothing; the shared expert's row adds
 // with weight 1 (roadtointelligence.com "Total versus active parameters").
+// With many slots per token (k > 8: wide top-k, or one slot per expert under
+// expert-choice routing) the warp first reads its token's slots 32 at a time
+// and keeps the live ones, in slot order, in shared memory, so the column
+// passes walk only those.
 //
 // Load statistics: see stats.cuh.
 #include "kernels.h"
@@ -16,20 +20,36 @@ namespace moe {
 namespace {
 
 constexpr int kCombineWarps = 8;
+constexpr int kCompactAbove = 8;                   // slots per token above which to compact
 
-template <typename T>
+template <typename T, bool COMPACT>
 __global__ void __launch_bounds__(kCombineWarps * 32)
     combine_kernel(const T* __restrict__ Yp, const int32_t* __restrict__ token_row,
                    const float* __restrict__ topk_w, const int32_t* __restrict__ offsets,
                    int Ttok, int k, int N, int has_shared, int64_t d, T* __restrict__ y) {
   constexpr int V = Vec16<T>::n;
   constexpr int CB = 4;                            // 16-byte columns per lane per pass
+  extern __shared__ int2 live[];                   // COMPACT: [kCombineWarps][k] (row, gate)
   pdl_launch_dependents();
   pdl_wait_previous();
   const int lane = threadIdx.x & 31;
   const int64_t t = int64_t(blockIdx.x) * kCombineWarps + (threadIdx.x >> 5);
   if (t >= Ttok) return;
   const int64_t shared_row = has_shared ? int64_t(offsets[N]) + t : -1;
+  int n_live = k;
+  int2* mine = live + (threadIdx.x >> 5) * k;
+  if (COMPACT) {
+    n_live = 0;
+    for (int j0 = 0; j0 < k; j0 += 32) {
+      const int j = j0 + lane;
+      const int r = j < k ? token_row[t * k + j] : -1;
+      const float g = j < k ? topk_w[t * k + j] : 0.f;
+      const uint32_t m = __ballot_sync(0xffffffffu, r >= 0);
+      if (r >= 0) mine[n_live + __popc(m & ((1u << lane) - 1u))] = make_int2(r, __float_as_int(g));
+      n_live += __popc(m);
+    }
+    __syncwarp();
+  }
   const int64_t nv = d / V;
   for (int64_t c0 = lane; c0 < nv; c0 += 32 * CB) {
     float acc[CB][V];
@@ -37,12 +57,18 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
     for (int b = 0; b < CB; ++b)
 #pragma unroll
       for (int i = 0; i < V; ++i) acc[b][i] = 0.f;
-    for (int j = 0; j <= k; ++j) {
+    for (int j = 0; j <= n_live; ++j) {
       int64_t r;
       float g;
-      if (j < k) {
-        r = token_row[t * k + j];
-        g = topk_w[t * k + j];
+      if (j < n_live) {
+        if (COMPACT) {
+          const int2 rg = mine[j];
+          r = rg.x;
+          g = __int_as_float(rg.y);
+        } else {
+          r = token_row[t * k + j];
+          g = topk_w[t * k + j];
+        }
       } else {
         r = shared_row;                            // the shared expert, weight 1
         g = 1.f;
@@ -90,14 +116,28 @@ cudaError_t launch_combine(const moe_config& c, const void* Yp, const int32_t* t
   if (c.T == 0) return cudaSuccess;
   const unsigned blocks = unsigned(ceil_div(c.T, kCombineWarps));
   const int hs = c.d_ff_shared > 0 ? 1 : 0;
-  if (c.dtype == MOE_F32)
-    return launch_pdl(combine_kernel<float>, dim3(blocks), dim3(kCombineWarps * 32), 0, s,
-                      static_cast<const float*>(Yp), token_row, topk_w, offsets, int(c.T),
-                      int(c.top_k), int(c.n_experts), hs, c.d_model, static_cast<float*>(y));
-  return launch_pdl(combine_kernel<__nv_bfloat16>, dim3(blocks), dim3(kCombineWarps * 32), 0,
-                    s, static_cast<const __nv_bfloat16*>(Yp), token_row, topk_w, offsets,
-                    int(c.T), int(c.top_k), int(c.n_experts), hs, c.d_model,
-                    static_cast<__nv_bfloat16*>(y));
+  const bool compact = c.top_k > kCompactAbove;
+  const size_t smem = compact ? size_t(kCombineWarps) * size_t(c.top_k) * sizeof(int2) : 0;
+  auto go = [&](auto kern, auto* Yt, auto* yt) -> cudaError_t {
+    if (smem > 48 * 1024) {
+      const cudaError_t e =
+          cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+      if (e != cudaSuccess) return e;
+    }
+    return launch_pdl(kern, dim3(blocks), dim3(kCombineWarps * 32), smem, s, Yt, token_row,
+                      topk_w, offsets, int(c.T), int(c.top_k), int(c.n_experts), hs,
+                      c.d_model, yt);
+  };
+  if (c.dtype == MOE_F32) {
+    const float* Yt = static_cast<const float*>(Yp);
+    float* yt = static_cast<float*>(y);
+    return compact ? go(combine_kernel<float, true>, Yt, yt)
+                   : go(combine_kernel<float, false>, Yt, yt);
+  }
+  const __nv_bfloat16* Yt = static_cast<const __nv_bfloat16*>(Yp);
+  __nv_bfloat16* yt = static_cast<__nv_bfloat16*>(y);
+  return compact ? go(combine_kernel<__nv_bfloat16, true>, Yt, yt)
+                 : go(combine_kernel<__nv_bfloat16, false>, Yt, yt);
 }
 
 cudaError_t launch_load_stats(const moe_config& c, const float* prob_partials,

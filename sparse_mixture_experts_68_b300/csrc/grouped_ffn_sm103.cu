@@ -1175,7 +1175,8 @@ cudaError_t grouped_linear(const moe_config& c, const GroupedFfnArgs& g, const v
                            const void* bias_s, void* out, int64_t K, int64_t Nd, int epi,
                            cudaStream_t s) {
   const int64_t groups = c.n_experts + (c.d_ff_shared > 0 ? 1 : 0);
-  const int64_t rows = c.T * c.top_k + (c.d_ff_shared > 0 ? c.T : 0);
+  const int64_t routed = g.routed_rows > 0 ? g.routed_rows : c.T * c.top_k;
+  const int64_t rows = routed + (c.d_ff_shared > 0 ? c.T : 0);
   const int nb = swap_rows(Nd, rows / groups, epi);
   if (nb > 0) {
     // decode: weights as the MMA's 128-row operand, tokens as its NB columns

@@ -50,9 +50,11 @@ inline int64_t router_partial_rows(const moe_config& c) {
 
 cudaError_t launch_router_logits(const moe_config& c, const void* x, const void* W_g,
                                  const void* b_g, float* logits, cudaStream_t s);
-cudaError_t launch_router_softmax_topk(const moe_config& c, const float* logits,
+// k == 0 with probT set: no top-k; writes probT [N, T] and zeroes picks [T]
+cudaError_t launch_router_softmax_topk(const moe_config& c, int k, const float* logits,
                                        int32_t* topk_idx, float* topk_w,
-                                       float* prob_partials, cudaStream_t s);
+                                       float* prob_partials, float* probT, int32_t* picks,
+                                       cudaStream_t s);
 // router scores on the tensor cores, fp32 out (grouped_ffn_sm103.cu)
 cudaError_t launch_router_logits_tc(const moe_config& c, const void* x, const void* W_g,
                                     const void* b_g, float* logits, int num_sms,
@@ -85,6 +87,36 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* to
                            int32_t* row_token, int32_t* token_row, void* Xp, void* scratch,
                            int64_t rows_max, cudaStream_t s, const StatsArgs* stats);
 
+// ---- expert-choice routing (router.cu, expert_choice.cu) -------------------------
+
+// Xp[r] = x[row_token[r]] for the routed rows [0, offsets[N]) (-1: padding,
+// left as is), Xp[offsets[N] + t] = x[t] for the shared group (permute.cu)
+cudaError_t launch_row_copy(const moe_config& c, const void* x, const int32_t* offsets,
+                            const int32_t* row_token, void* Xp, int64_t rows_max,
+                            cudaStream_t s);
+
+// scores, expert-major probabilities probT [N, T] (and picks [T] zeroed), block
+// sums of p: the router without its top-k
+cudaError_t launch_router_probs(const moe_config& c, const void* x, const void* W_g,
+                                const void* b_g, float* logits, float* probT, int32_t* picks,
+                                float* prob_partials, int num_sms, int32_t* status,
+                                uint64_t wait_limit_ns, cudaStream_t s);
+// every expert's C picked tokens, grouped in Cpad-row groups (plus the shared
+// expert's T rows), with the per-token slot view token_row / token_w [T, N]
+cudaError_t launch_ec_select(const moe_config& c, int64_t C, const float* probT,
+                             int32_t* ec_token, float* ec_gate, int32_t* offsets,
+                             int32_t* counts, int32_t* row_token, int32_t* token_row,
+                             float* token_w, int32_t* picks, cudaStream_t s);
+// mean_prob, balance and the tokens no expert picked
+cudaError_t launch_ec_stats(const moe_config& c, const float* prob_partials,
+                            const int32_t* counts, const int32_t* picks, float* mean_prob,
+                            float* balance, int32_t* scratch, int32_t* unpicked,
+                            cudaStream_t s);
+// rows of one expert's group: C rounded up to the group alignment
+inline int64_t ec_group_rows(int64_t C) {
+  return (C + MOE_GROUP_ALIGN - 1) / MOE_GROUP_ALIGN * MOE_GROUP_ALIGN;
+}
+
 // ---- grouped expert FFN ----------------------------------------------------------
 
 struct GroupedFfnArgs {
@@ -99,6 +131,7 @@ struct GroupedFfnArgs {
   uint64_t wait_limit_ns;
   int num_sms;
   void* mid_event;          // cudaEvent_t recorded between the two Linears, or nullptr
+  int64_t routed_rows;      // live routed rows for the tile heuristics; 0: T * top_k
 };
 
 // Records a caller's event on s (as an external node while s is capturing).

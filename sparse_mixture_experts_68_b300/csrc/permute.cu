@@ -363,6 +363,12 @@ cudaError_t launch_copy(const moe_config& c, const void* x, const int32_t* offse
 
 }  // namespace
 
+cudaError_t launch_row_copy(const moe_config& c, const void* x, const int32_t* offsets,
+                            const int32_t* row_token, void* Xp, int64_t rows_max,
+                            cudaStream_t s) {
+  return launch_copy(c, x, offsets, row_token, Xp, rows_max, s);
+}
+
 int permute_launch_count(const moe_config& c) {
   const int copy = moe::rows_max_for(c) > 0 ? 1 : 0;
   if (single_block_sort_fits(c)) return 1 + copy;

@@ -34,7 +34,8 @@ template <int NPL>
 __global__ void __launch_bounds__(kRouterWarps * 32)
     router_softmax_topk_kernel(const float* __restrict__ logits, int T, int N, int k,
                                int renorm, int32_t* __restrict__ topk_idx,
-                               float* __restrict__ topk_w, float* __restrict__ prob_partials) {
+                               float* __restrict__ topk_w, float* __restrict__ prob_partials,
+                               float* __restrict__ probT, int32_t* __restrict__ picks) {
   extern __shared__ float red[];                 // [kRouterWarps][N]
   pdl_launch_dependents();
   pdl_wait_previous();
@@ -71,6 +72,14 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
     const float inv = 1.0f / ssum;
 #pragma unroll
     for (int i = 0; i < NPL; ++i) psum[i] += ex[i] * inv;
+    if (probT) {                                 // expert-major probabilities
+#pragma unroll
+      for (int i = 0; i < NPL; ++i) {
+        const int e = lane + 32 * i;
+        if (e < N) probT[int64_t(e) * T + t] = ex[i] * inv;
+      }
+      if (lane == 0) picks[t] = 0;
+    }
 
     // top-k by repeated warp arg-max over the not yet selected experts
     uint32_t taken = 0;                          // bit i: expert lane + 32 i selected
@@ -146,7 +155,8 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
     router_fused_kernel(const TIn* __restrict__ x, const TIn* __restrict__ W_g,
                         const TIn* __restrict__ b_g, int T, int d, int N, int k, int renorm,
                         float* __restrict__ logits, int32_t* __restrict__ topk_idx,
-                        float* __restrict__ topk_w, float* __restrict__ prob_partials) {
+                        float* __restrict__ topk_w, float* __restrict__ prob_partials,
+                        float* __restrict__ probT, int32_t* __restrict__ picks) {
   constexpr int V = Vec16<TIn>::n;
   constexpr int NPL = NE > 32 ? NE / 32 : 1;          // experts per lane after the reduce
   constexpr int DUP = NE < 32 ? 32 / NE : 1;          // lanes holding the same expert
@@ -251,6 +261,14 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
     const float inv = 1.0f / ssum;
 #pragma unroll
     for (int i = 0; i < NPL; ++i) psum[i] += ex[i] * inv;
+    if (probT) {                                       // expert-major probabilities
+#pragma unroll
+      for (int i = 0; i < NPL; ++i) {
+        const int e = e0 + i;
+        if (e < N && owner) probT[int64_t(e) * T + t] = ex[i] * inv;
+      }
+      if (lane == 0) picks[t] = 0;
+    }
 
     uint32_t taken = 0;                                // bit i: expert e0 + i selected
     float kept_sum = 0.f;
@@ -325,13 +343,15 @@ bool fused_router_fits(const moe_config& c) {
   return c.n_experts <= 64 && fused_router_smem(c) <= kFusedRouterSmemLimit;
 }
 
-cudaError_t launch_router_fused(const moe_config& c, const void* x, const void* W_g,
+// k == 0 with probT set: probabilities only (expert-choice routing)
+cudaError_t launch_router_fused(const moe_config& c, int k, const void* x, const void* W_g,
                                 const void* b_g, float* logits, int32_t* topk_idx,
-                                float* topk_w, float* prob_partials, cudaStream_t s) {
+                                float* topk_w, float* prob_partials, float* probT,
+                                int32_t* picks, cudaStream_t s) {
   if (c.T == 0) return cudaSuccess;
   const unsigned blocks = unsigned(router_partial_rows(c));
   const size_t smem = fused_router_smem(c);
-  const int T = int(c.T), d = int(c.d_model), N = int(c.n_experts), k = int(c.top_k);
+  const int T = int(c.T), d = int(c.d_model), N = int(c.n_experts);
   const int rn = c.renormalize ? 1 : 0;
 #define MOE_FUSED_CASE(TIN, NPAD)                                                          \
   {                                                                                        \
@@ -342,7 +362,7 @@ cudaError_t launch_router_fused(const moe_config& c, const void* x, const void* 
     return launch_pdl(kern, dim3(blocks), dim3(kRouterWarps * 32), smem, s,                \
                       static_cast<const TIN*>(x), static_cast<const TIN*>(W_g),            \
                       static_cast<const TIN*>(b_g), T, d, N, k, rn, logits, topk_idx,      \
-                      topk_w, prob_partials);                                              \
+                      topk_w, prob_partials, probT, picks);                                \
   }
   if (c.dtype == MOE_F32) {
     if (N <= 8) MOE_FUSED_CASE(float, 8)
@@ -357,14 +377,15 @@ cudaError_t launch_router_fused(const moe_config& c, const void* x, const void* 
 #undef MOE_FUSED_CASE
 }
 
-cudaError_t launch_router_softmax_topk(const moe_config& c, const float* logits,
+cudaError_t launch_router_softmax_topk(const moe_config& c, int k, const float* logits,
                                        int32_t* topk_idx, float* topk_w,
-                                       float* prob_partials, cudaStream_t s) {
+                                       float* prob_partials, float* probT, int32_t* picks,
+                                       cudaStream_t s) {
   if (c.T == 0) return cudaSuccess;
   const int N = int(c.n_experts);
   const unsigned blocks = unsigned(router_partial_rows(c));
   const size_t smem = size_t(kRouterWarps) * N * sizeof(float);
-  const int T = int(c.T), k = int(c.top_k), rn = c.renormalize ? 1 : 0;
+  const int T = int(c.T), rn = c.renormalize ? 1 : 0;
 #define MOE_ROUTER_CASE(NPL)                                                              \
   {                                                                                        \
     auto kern = router_softmax_topk_kernel<NPL>;                                           \
@@ -374,7 +395,7 @@ cudaError_t launch_router_softmax_topk(const moe_config& c, const float* logits,
       if (e != cudaSuccess) return e;                                                      \
     }                                                                                      \
     return launch_pdl(kern, dim3(blocks), dim3(kRouterWarps * 32), smem, s, logits, T, N,  \
-                      k, rn, topk_idx, topk_w, prob_partials);                             \
+                      k, rn, topk_idx, topk_w, prob_partials, probT, picks);               \
   }
   if (N <= 32) MOE_ROUTER_CASE(1)
   if (N <= 64) MOE_ROUTER_CASE(2)
@@ -406,14 +427,37 @@ cudaError_t launch_router(const moe_config& c, const void* x, const void* W_g,
                           uint64_t wait_limit_ns, cudaStream_t s) {
   if (c.T == 0) return cudaSuccess;
   cudaError_t e;
+  const int k = int(c.top_k);
   if (c.dtype == MOE_BF16 && c.n_experts % 64 == 0)
     e = launch_router_logits_tc(c, x, W_g, b_g, logits, num_sms, status, wait_limit_ns, s);
   else if (fused_router_fits(c))
-    return launch_router_fused(c, x, W_g, b_g, logits, topk_idx, topk_w, prob_partials, s);
+    return launch_router_fused(c, k, x, W_g, b_g, logits, topk_idx, topk_w, prob_partials,
+                               nullptr, nullptr, s);
   else
     e = launch_router_logits(c, x, W_g, b_g, logits, s);
   if (e != cudaSuccess) return e;
-  return launch_router_softmax_topk(c, logits, topk_idx, topk_w, prob_partials, s);
+  return launch_router_softmax_topk(c, k, logits, topk_idx, topk_w, prob_partials, nullptr,
+                                    nullptr, s);
+}
+
+// The same kernels without the top-k: scores, the expert-major probabilities
+// probT [N, T] and the block sums of p (expert-choice routing).
+cudaError_t launch_router_probs(const moe_config& c, const void* x, const void* W_g,
+                                const void* b_g, float* logits, float* probT, int32_t* picks,
+                                float* prob_partials, int num_sms, int32_t* status,
+                                uint64_t wait_limit_ns, cudaStream_t s) {
+  if (c.T == 0) return cudaSuccess;
+  cudaError_t e;
+  if (c.dtype == MOE_BF16 && c.n_experts % 64 == 0)
+    e = launch_router_logits_tc(c, x, W_g, b_g, logits, num_sms, status, wait_limit_ns, s);
+  else if (fused_router_fits(c))
+    return launch_router_fused(c, 0, x, W_g, b_g, logits, nullptr, nullptr, prob_partials,
+                               probT, picks, s);
+  else
+    e = launch_router_logits(c, x, W_g, b_g, logits, s);
+  if (e != cudaSuccess) return e;
+  return launch_router_softmax_topk(c, 0, logits, nullptr, nullptr, prob_partials, probT,
+                                    picks, s);
 }
 
 }  // namespace moe

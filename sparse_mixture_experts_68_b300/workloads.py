@@ -41,6 +41,7 @@ class Workload:
     renormalize: int = 1
     zipf_router_bias: bool = False   # b_g[e] = 2 ln(1 / (e + 1))
     router_scale: float = 1.0        # multiplies W_g
+    expert_choice: bool = False      # each expert takes its capacity in tokens; top_k unused
     seed: int = 0
     description: str = ""
 
@@ -88,13 +89,39 @@ WORKLOADS = {
         router_scale=3.0, seed=4,
         description="T=4096, d=7168, 256 routed experts d_ff=2048 + 1 shared, "
                     "top-8, GELU, router weights x3, bf16"),
+    # expert-choice routing (matteuscruz.github.io "Load balancing": every
+    # expert picks its top tokens) at the same expert work as top-k routing:
+    # C = ceil(k * T / N) tokens per expert
+    "c3_mixtral_prefill_ec": Workload(
+        "c3_mixtral_prefill_ec", T=4096, d_model=4096, d_ff=14336, n_experts=8,
+        top_k=2, act=ACT_GELU_ERF, dtype=DT_BF16, capacity_factor=2.0, expert_choice=True,
+        seed=3,
+        description="expert choice: T=4096, d=4096, d_ff=14336, N=8, C=ceil(2T/N)=1024 "
+                    "tokens per expert, GELU, bf16"),
+    "c4_deepseek_v3_ec": Workload(
+        "c4_deepseek_v3_ec", T=4096, d_model=7168, d_ff=2048, n_experts=256,
+        top_k=8, act=ACT_GELU_ERF, dtype=DT_BF16, d_ff_shared=2048, capacity_factor=8.0,
+        expert_choice=True, router_scale=3.0, seed=4,
+        description="expert choice: T=4096, d=7168, 256 routed experts d_ff=2048 + 1 "
+                    "shared, C=ceil(8T/N)=128 tokens per expert, GELU, router weights x3, "
+                    "bf16"),
 }
+
+
+def routed_rows(wl: Workload) -> int:
+    """Expert rows of one call without capacity drops: T*k, or N*C for expert
+    choice."""
+    if wl.expert_choice:
+        C = wl.T if wl.capacity <= 0 else min(wl.capacity, wl.T)
+        return wl.n_experts * C
+    return wl.T * wl.top_k
 
 
 def flops(wl: Workload, kept_rows: int | None = None) -> float:
     """Algorithmic FLOPs of one layer call: router 2*T*d*N, routed experts
-    4*d*d_ff per kept (token, slot), shared expert 4*d*d_ff_s per token."""
-    rows = wl.T * wl.top_k if kept_rows is None else kept_rows
+    4*d*d_ff per kept (token, slot) -- or per (expert, picked token) --, shared
+    expert 4*d*d_ff_s per token."""
+    rows = routed_rows(wl) if kept_rows is None else kept_rows
     return (2.0 * wl.T * wl.d_model * wl.n_experts
             + 4.0 * wl.d_model * wl.d_ff * rows
             + 4.0 * wl.d_model * wl.d_ff_shared * wl.T)

@@ -183,3 +183,85 @@ def check_grouping(cfg, tensors_x, offsets, row_token, token_row, Xp, ref_groupi
         assert torch.equal(xs[int(r)], x[int(rt[r])])
     if cfg.d_ff_shared:
         assert torch.equal(xs[off[N]: off[N] + T], x)
+
+
+# ---- expert-choice routing -----------------------------------------------------------
+
+EC_GATE_RTOL = 1e-5
+
+
+def check_ec_layer(wl, cfg, tensors, out, tokens=None):
+    """Full comparison of one moe_ec_forward against the oracle.
+
+    The selection is exact for every expert whose oracle gap between its C-th
+    and (C+1)-th score exceeds what the GPU's fp32 scores can move p by
+    (4 max|dz| max_t p + 1e-7: a softmax moves p by at most 2 p max|dz|, on
+    both sides of the cut); for the others the GPU's set must still take every
+    token clearly above the cut and none clearly below.  The oracle then runs
+    on the GPU's selection."""
+    report = {}
+    x = to64(tensors["x"])
+    W_g, b_g = to64(tensors["W_g"]), to64(tensors["b_g"])
+    z_ref = O.router_logits(x, W_g, b_g)
+    p_ref = O.softmax(z_ref)
+    T, N = z_ref.shape
+    C = O.expert_choice_tokens(T, cfg.capacity)
+    dz = 0.0
+    if out.logits is not None:
+        zg = out.logits.cpu().numpy().astype(np.float64)
+        dz = float(np.abs(zg - z_ref).max()) if T else 0.0
+        err = dz / max(np.abs(z_ref).max(), 1e-30) if T else 0.0
+        report["logit_max_rel"] = float(err)
+        assert err < 1e-5, f"router scores differ: {err}"
+    sel_gpu = out.ec_token.cpu().numpy().astype(np.int64).reshape(N, C)
+    gate_gpu = out.ec_gate.cpu().numpy().astype(np.float64).reshape(N, C)
+    sel_ref = O.expert_choice_select(p_ref, C)
+    gaps = O.expert_choice_gap(p_ref, C)
+    eps = 4.0 * dz * (p_ref.max(axis=0) if T else np.zeros(N)) + 1e-7
+    near = gaps < eps
+    sel_use = []
+    for e in range(N):
+        g = sel_gpu[e]
+        assert np.all((g >= 0) & (g < T)) and np.all(np.diff(g) > 0), f"expert {e}: bad picks"
+        if not near[e]:
+            np.testing.assert_array_equal(g, sel_ref[e], err_msg=f"expert {e} picks differ")
+        else:
+            col = p_ref[:, e]
+            thr = -np.sort(-col)[C - 1]
+            inset = np.zeros(T, dtype=bool)
+            inset[g] = True
+            assert np.all(inset[col > thr + eps[e]]), f"expert {e}: misses a clear pick"
+            assert not np.any(inset[col < thr - eps[e]]), f"expert {e}: takes a clear reject"
+        sel_use.append(g)
+        if C:
+            np.testing.assert_allclose(gate_gpu[e], p_ref[g, e], rtol=2.0 * dz + EC_GATE_RTOL,
+                                       atol=1e-7, err_msg=f"expert {e} gates")
+    report["near_tie_experts"] = int(near.sum())
+    shared = None
+    if cfg.d_ff_shared:
+        shared = tuple(to64(tensors[n]) for n in ("W1s", "b1s", "W2s", "b2s"))
+    ref = O.expert_choice_forward(x, W_g, b_g, Experts(tensors["W1"]), Experts(tensors["b1"]),
+                                  Experts(tensors["W2"]), Experts(tensors["b2"]),
+                                  capacity=cfg.capacity, act=cfg.act, shared=shared,
+                                  round_hidden_bf16=(cfg.dtype == 1), tokens=tokens,
+                                  sel_override=sel_use)
+    np.testing.assert_array_equal(out.token_picks.cpu().numpy(), ref.token_picks)
+    assert int(out.unpicked.cpu().item()) == ref.unpicked
+    np.testing.assert_allclose(out.mean_prob.cpu().numpy(), ref.mean_prob,
+                               rtol=MEAN_PROB_RTOL, atol=1e-8)
+    bal = float(out.balance.cpu().item())
+    assert abs(bal - ref.balance) <= BALANCE_RTOL * abs(ref.balance) + 1e-9, \
+        f"balance {bal} vs {ref.balance}"
+    y_gpu = out.y.float().cpu().numpy().astype(np.float64)
+    rows = ref.tokens
+    e = row_errors(y_gpu[rows], ref.y)
+    report["max_row_rel_l2"] = float(e.max()) if e.size else 0.0
+    tol = TOL[cfg.dtype]
+    assert report["max_row_rel_l2"] <= tol, \
+        f"max row rel L2 {report['max_row_rel_l2']} > {tol} (token {rows[int(np.argmax(e))]})"
+    if not cfg.d_ff_shared:
+        lonely = ref.token_picks[rows] == 0
+        for t in rows[lonely]:
+            assert np.all(y_gpu[t] == 0.0), f"unpicked token {t} is not zero"
+        report["unpicked_checked"] = int(lonely.sum())
+    return report, ref

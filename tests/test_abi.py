@@ -53,6 +53,12 @@ def test_sizes(lib):
     assert B.host_workspace_size(cfg) > B.workspace_size(cfg)
     c1 = B.make_config(WORKLOADS["c1_page1_bf16"])
     assert B.rows_max(c1) == 2048 * 2 + 8 * 127
+    # the host path's extra room: x and y, topk_idx and topk_w, counts, kept and
+    # mean_prob, dropped, balance and cv_squared, logits; each 256-byte rounded
+    r = lambda n: (n + 255) // 256 * 256
+    T, d, k, N = 2048, 768, 2, 8
+    extra = 2 * r(T * d * 2) + 2 * r(T * k * 4) + 3 * r(N * 4) + 3 * r(4) + r(T * N * 4)
+    assert B.host_workspace_size(c1) - B.workspace_size(c1) == extra
 
 
 @pytest.mark.parametrize("field,value,status", [
@@ -112,3 +118,40 @@ def test_wait_limit_setting(lib):
     B.set_wait_limit_ns(12345)
     assert B.get_wait_limit_ns() == 12345
     B.set_wait_limit_ns(old)
+
+
+def test_expert_choice_sizes_and_validation(lib):
+    wl = WORKLOADS["c3_mixtral_prefill_ec"]
+    cfg = B.make_config(wl)
+    assert B.ec_tokens_per_expert(cfg) == 1024                  # ceil(2 * 4096 / 8)
+    assert B.ec_rows_max(cfg) == 8 * 1024
+    assert B.ec_workspace_size(cfg) > B.ec_rows_max(cfg) * (2 * 4096 + 14336) * 2
+    c4 = B.make_config(WORKLOADS["c4_deepseek_v3_ec"])
+    assert B.ec_tokens_per_expert(c4) == 128
+    assert B.ec_rows_max(c4) == 256 * 128 + 4096               # + the shared group
+    # capacity clamps to T; <= 0 means every token
+    for cap, want in [(0, 4096), (-3, 4096), (5000, 4096), (100, 100)]:
+        cfg.capacity = cap
+        assert B.ec_tokens_per_expert(cfg) == want
+        assert B.ec_rows_max(cfg) == 8 * (-(-want // 128) * 128)
+    # top_k and renormalize are not read
+    cfg.capacity = 100
+    cfg.top_k, cfg.renormalize = 0, 7
+    assert B.ec_workspace_size(cfg) > 0
+    cfg.top_k, cfg.renormalize = 2, 1
+    for field, value in [("n_experts", 2048), ("d_model", 100), ("dtype", 5), ("T", -1),
+                         ("reserved", 1)]:
+        bad = B.make_config(wl)
+        setattr(bad, field, value)
+        assert B.ec_workspace_size(bad) == 0
+        assert B.ec_tokens_per_expert(bad) == -1
+        assert B.ec_forward_launch_count(bad) == -1
+    o = B.MoeEcOutputs()
+    w = B.MoeWeights()
+    assert lib.moe_ec_forward(C.byref(cfg), None, C.byref(w), C.byref(o), None, 0, None) == \
+        B.MOE_ERR_INVALID_ARG
+    fake = 0x10000
+    w = B.MoeWeights(*([fake] * 6 + [None] * 4))
+    o = B.MoeEcOutputs(*([fake] * 7 + [None]))
+    assert lib.moe_ec_forward(C.byref(cfg), fake, C.byref(w), C.byref(o), fake, 1024, None) \
+        == B.MOE_ERR_WORKSPACE
