@@ -37,6 +37,14 @@ float64 numpy, with no blocking, fusion or reordering beyond the definition:
   router probability p[t, e]; an expert takes C tokens (C = the capacity,
   clamped to T; C <= 0 means all T); ties go to the lower token index; a picked
   token's gate is p[t, e]; a token no expert picked outputs 0.
+* the backward pass of the layer for the training loss
+  total = task + alpha * balance (botmartz.com "Load Balancing: The Hidden
+  Challenge": total_loss = task_loss + 0.01 * balance_loss; roadtointelligence.com
+  "Keeping the experts busy": coefficient 0.01).  The task loss enters as its
+  gradient dy = d task / d y; every other derivative is the chain rule through
+  the forward above, written out step by step (no automatic differentiation).
+  The top-k choice and the capacity drops are piecewise constant: they pass
+  no gradient.
 * squared coefficient of variation of the expert counts, the quantity the
   auxiliary loss penalises -- matteuscruz.github.io "Load balancing: the core
   training challenge"; named cv_squared(expert_counts) in invest-in.ai
@@ -435,3 +443,135 @@ def expert_choice_forward(x, W_g, b_g, W1, b1, W2, b2, *, capacity, act, shared=
         y += expert_ffn(x[tokens], W1s, b1s, W2s, b2s, act, round_hidden_bf16)
     return ExpertChoiceOutput(y, tokens, z, p, sel, gate, picks, int((picks == 0).sum()),
                               mean_prob, balance)
+
+
+# ---------------------------------------------------------------------------
+# backward pass
+# ---------------------------------------------------------------------------
+
+def activation_grad(a, act):
+    """d act / d a.  GELU(a) = a Phi(a), so GELU'(a) = Phi(a) + a phi(a) with
+    Phi the normal CDF 0.5 (1 + erf(a / sqrt 2)) and phi its density."""
+    a = np.asarray(a, dtype=np.float64)
+    if act == ACT_GELU_ERF:
+        cdf = 0.5 * (1.0 + _erf(a / math.sqrt(2.0)))
+        pdf = np.exp(-0.5 * a * a) / math.sqrt(2.0 * math.pi)
+        return cdf + a * pdf
+    if act == ACT_RELU:
+        return (a > 0.0).astype(np.float64)
+    raise ValueError(f"unknown activation {act}")
+
+
+def softmax_backward(p, dp):
+    """Gradient through p = softmax(z) along the last axis: p (dp - <p, dp>)."""
+    p = np.asarray(p, dtype=np.float64)
+    dp = np.asarray(dp, dtype=np.float64)
+    return p * (dp - np.sum(p * dp, axis=-1, keepdims=True))
+
+
+@dataclass
+class LayerGrads:
+    dx: np.ndarray           # [T, d]
+    dW_g: np.ndarray         # [N, d]
+    db_g: np.ndarray         # [N]
+    dW1: np.ndarray          # [N, d_ff, d]
+    db1: np.ndarray          # [N, d_ff]
+    dW2: np.ndarray          # [N, d, d_ff]
+    db2: np.ndarray          # [N, d]
+    dz: np.ndarray           # [T, N] gradient of the router scores
+    dw: np.ndarray           # [T, k] gradient of the gates
+    shared: tuple | None     # (dW1s, db1s, dW2s, db2s) or None
+
+
+def expert_ffn_backward(xr, W1, b1, W2, b2, act, dO, round_hidden_bf16=False):
+    """One expert's FFN backward on its rows xr given dO = d loss / d output:
+    returns (dxr, dW1, db1, dW2, db2).  The hidden activation h that multiplies
+    dO in dW2 is the one the forward fed to the second Linear (bf16-rounded
+    with round_hidden_bf16)."""
+    xr = np.asarray(xr, dtype=np.float64)
+    W1 = np.asarray(W1, dtype=np.float64)
+    W2 = np.asarray(W2, dtype=np.float64)
+    a = xr @ W1.T + np.asarray(b1, dtype=np.float64)      # pre-activation
+    h = activation(a, act)
+    if round_hidden_bf16:
+        h = round_to_bf16(h)
+    dW2 = dO.T @ h                                        # [d, d_ff]
+    db2 = dO.sum(axis=0)
+    dh = dO @ W2                                          # [rows, d_ff]
+    da = dh * activation_grad(a, act)
+    dW1 = da.T @ xr                                       # [d_ff, d]
+    db1 = da.sum(axis=0)
+    dxr = da @ W1                                         # [rows, d]
+    return dxr, dW1, db1, dW2, db2
+
+
+def moe_backward(x, W_g, b_g, W1, b1, W2, b2, dy, *, k, act, capacity=0, renormalize=True,
+                 shared=None, aux_weight=0.0, round_hidden_bf16=False, idx_override=None):
+    """Gradients of total = <dy, y> + aux_weight * balance with respect to x
+    and every parameter (botmartz.com "Load Balancing": total_loss = task_loss
+    + 0.01 * balance_loss, with dy standing for d task_loss / d y).
+
+    Steps, each the chain rule through the matching forward step:
+      1. combine y[t] = sum_kept w[t,j] o[t,j] (+ shared): d o[t,j] = w[t,j] dy[t],
+         d w[t,j] = <dy[t], o[t,j]> for kept (t, j), 0 for dropped ones;
+      2. each expert's FFN on its kept rows (expert_ffn_backward);
+      3. gates: renormalised, w = softmax over the k selected scores, so
+         dz[selected] = w (dw - <w, dw>); raw, w = p[selected], so
+         dp[selected] = dw and dz = p (dp - <p, dp>);
+      4. balance = sum_e (m_e - 1/N)^2 / (N - 1), m_e = mean_t p[t,e]:
+         d m_e = 2 (m_e - 1/N) / (N - 1), d p[t,e] = d m_e / T, through the softmax;
+      5. router scores z = x W_g^T + b_g: dW_g = dz^T x, db_g = sum_t dz, dx += dz W_g.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    dy = np.asarray(dy, dtype=np.float64)
+    W_g = np.asarray(W_g, dtype=np.float64)
+    T, d = x.shape
+    N = W_g.shape[0]
+    z = router_logits(x, W_g, b_g)
+    p = softmax(z)
+    idx = topk_indices(z, k) if idx_override is None else np.asarray(idx_override, dtype=np.int64)
+    w = gates_softmax_of_topk(z, idx) if renormalize else gates_raw_probs(p, idx)
+    grouping = group_by_expert(idx, N, capacity)
+
+    dx = np.zeros_like(x)
+    dw = np.zeros((T, k))
+    dW1, db1, dW2, db2 = [], [], [], []
+    for e in range(N):
+        rows = grouping.groups[e]
+        W1e, W2e = np.asarray(W1[e], dtype=np.float64), np.asarray(W2[e], dtype=np.float64)
+        if not rows:
+            dW1.append(np.zeros_like(W1e)); db1.append(np.zeros(W1e.shape[0]))
+            dW2.append(np.zeros_like(W2e)); db2.append(np.zeros(W2e.shape[0]))
+            continue
+        ts = np.array([t for t, _ in rows])
+        js = np.array([j for _, j in rows])
+        o = expert_ffn(x[ts], W1e, b1[e], W2e, b2[e], act, round_hidden_bf16)
+        dw[ts, js] = np.sum(dy[ts] * o, axis=1)                       # step 1
+        dO = w[ts, js][:, None] * dy[ts]
+        dxr, gW1, gb1, gW2, gb2 = expert_ffn_backward(x[ts], W1e, b1[e], W2e, b2[e], act, dO,
+                                                      round_hidden_bf16)   # step 2
+        np.add.at(dx, ts, dxr)
+        dW1.append(gW1); db1.append(gb1); dW2.append(gW2); db2.append(gb2)
+    shared_grads = None
+    if shared is not None:
+        dxs, gW1, gb1, gW2, gb2 = expert_ffn_backward(x, *shared, act, dy, round_hidden_bf16)
+        dx += dxs
+        shared_grads = (gW1, gb1, gW2, gb2)
+
+    dz = np.zeros((T, N))                                             # step 3
+    if renormalize:
+        dz_sel = w * (dw - np.sum(w * dw, axis=1, keepdims=True))
+        np.put_along_axis(dz, idx, dz_sel, axis=1)
+    else:
+        dp = np.zeros((T, N))
+        np.put_along_axis(dp, idx, dw, axis=1)
+        dz += softmax_backward(p, dp)
+    if aux_weight != 0.0 and N > 1 and T > 0:                         # step 4
+        m = p.mean(axis=0)
+        dm = aux_weight * 2.0 * (m - 1.0 / N) / (N - 1)
+        dz += softmax_backward(p, np.broadcast_to(dm / T, p.shape))
+    dW_g = dz.T @ x                                                   # step 5
+    db_g = dz.sum(axis=0)
+    dx += dz @ W_g
+    return LayerGrads(dx, dW_g, db_g, np.stack(dW1), np.stack(db1), np.stack(dW2),
+                      np.stack(db2), dz, dw, shared_grads)
