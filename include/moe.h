@@ -274,6 +274,47 @@ moe_status moe_forward_host(const moe_config* cfg, const void* x_host, const moe
  * "Code").  Lets callers check the activation against other implementations. */
 moe_status moe_activation(int32_t act, const float* x, float* y, int64_t n, void* stream);
 
+/* ---- backward pass ----------------------------------------------------------
+ *
+ * Gradients of the training loss total = task + aux_weight * balance
+ * (botmartz.com "Load Balancing: The Hidden Challenge": total_loss = task_loss
+ * + 0.01 * balance_loss; roadtointelligence.com "Keeping the experts busy":
+ * coefficient 0.01) with respect to x and every parameter, given
+ * dy = d task / d y.  The chain rule runs back through the forward of the
+ * same call sequence: combine, expert FFNs (the first Linear's
+ * pre-activation is recomputed), gates (softmax over the k selected scores,
+ * or the raw probabilities), the balance statistic and the router.  The top-k
+ * choice and the capacity drops pass no gradient.  bf16 layers only (an fp32
+ * config returns MOE_ERR_UNSUPPORTED); top-k routing only.
+ * Gradients are written in the layer dtype (bf16), accumulated in fp32. */
+
+typedef struct moe_grads {
+  void  *dx;                          /* [T, d_model]                      required */
+  void  *dW_g, *db_g;                 /* [N, d_model], [N]                 required */
+  void  *dW1, *db1, *dW2, *db2;       /* shapes of W1, b1, W2, b2          required */
+  void  *dW1s, *db1s, *dW2s, *db2s;   /* shared expert (NULL without one)           */
+  float *dz;                          /* [T, N] d total / d z (scores); NULL = skip */
+  float *dw;                          /* [T, k] d total / d gate; NULL = skip       */
+} moe_grads;
+
+/* Bytes of device workspace moe_backward needs; 0 for an invalid or
+ * unsupported config. */
+size_t moe_backward_workspace_size(const moe_config* cfg);
+/* Kernels one moe_backward launches; -1 for an invalid or unsupported config. */
+int32_t moe_backward_launch_count(const moe_config* cfg);
+
+/* The backward pass.  `fwd` and `fwd_workspace` are the outputs and the
+ * workspace of the moe_forward call on the same cfg, x and weights (the
+ * backward reads the saved grouping, the expert rows Xp, H and Yp, the
+ * scores, gates and mean_prob from them, and zeroes the padding rows of Xp
+ * and H in fwd_workspace).  dy [T, d_model] in the layer dtype.  `workspace`
+ * (device, >= moe_backward_workspace_size(cfg) bytes, 256-byte aligned) holds
+ * the backward's intermediates. */
+moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights* w,
+                        const moe_outputs* fwd, void* fwd_workspace, size_t fwd_workspace_bytes,
+                        const void* dy, float aux_weight, const moe_grads* grads,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
 /* ---- expert-choice routing -------------------------------------------------
  *
  * matteuscruz.github.io "What is a Mixture of Experts?", "Load balancing: the

@@ -33,7 +33,8 @@ EXPORTS = [
     "moe_forward_launch_count", "moe_activation",
     "moe_ec_tokens_per_expert", "moe_ec_rows_max", "moe_ec_workspace_size",
     "moe_ec_forward_launch_count", "moe_ec_router", "moe_ec_select", "moe_ec_forward",
-    "moe_ec_forward_profiled",
+    "moe_ec_forward_profiled", "moe_backward", "moe_backward_workspace_size",
+    "moe_backward_launch_count",
 ]
 PERMUTE_STATIC_SCRATCH_INTS = 1 << 18
 
@@ -61,6 +62,12 @@ class MoeOutputs(C.Structure):
                 ("counts", C.c_void_p), ("kept", C.c_void_p), ("dropped", C.c_void_p),
                 ("mean_prob", C.c_void_p), ("balance", C.c_void_p), ("logits", C.c_void_p),
                 ("cv_squared", C.c_void_p)]
+
+
+class MoeGrads(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in
+                ("dx", "dW_g", "db_g", "dW1", "db1", "dW2", "db2", "dW1s", "db1s", "dW2s",
+                 "db2s", "dz", "dw")]
 
 
 class MoeEcOutputs(C.Structure):
@@ -119,6 +126,11 @@ def lib() -> C.CDLL:
         "moe_ec_forward_profiled": (C.c_int32, [CP, P, C.POINTER(MoeWeights),
                                                 C.POINTER(MoeEcOutputs), P, C.c_size_t,
                                                 C.POINTER(C.c_void_p), P]),
+        "moe_backward_workspace_size": (C.c_size_t, [CP]),
+        "moe_backward_launch_count": (C.c_int32, [CP]),
+        "moe_backward": (C.c_int32, [CP, P, C.POINTER(MoeWeights), C.POINTER(MoeOutputs), P,
+                                     C.c_size_t, P, C.c_float, C.POINTER(MoeGrads), P,
+                                     C.c_size_t, P]),
         "moe_status_string": (C.c_char_p, [C.c_int32]),
         "moe_version": (C.c_int32, []),
     }
@@ -317,6 +329,61 @@ def forward_host(cfg: MoeConfig, x_host, weights: MoeWeights, out_host: Outputs,
                                   _stream(stream)), "moe_forward_host")
 
 
+# ---- backward pass -----------------------------------------------------------------
+
+def backward_workspace_size(cfg: MoeConfig) -> int:
+    return int(lib().moe_backward_workspace_size(C.byref(cfg)))
+
+
+def backward_launch_count(cfg: MoeConfig) -> int:
+    return int(lib().moe_backward_launch_count(C.byref(cfg)))
+
+
+@dataclass
+class Grads:
+    dx: torch.Tensor
+    dW_g: torch.Tensor
+    db_g: torch.Tensor
+    dW1: torch.Tensor
+    db1: torch.Tensor
+    dW2: torch.Tensor
+    db2: torch.Tensor
+    dW1s: torch.Tensor | None = None
+    db1s: torch.Tensor | None = None
+    dW2s: torch.Tensor | None = None
+    db2s: torch.Tensor | None = None
+    dz: torch.Tensor | None = None
+    dw: torch.Tensor | None = None
+
+    def struct(self) -> MoeGrads:
+        return MoeGrads(*[_ptr(getattr(self, n)) for n in
+                          ("dx", "dW_g", "db_g", "dW1", "db1", "dW2", "db2", "dW1s", "db1s",
+                           "dW2s", "db2s", "dz", "dw")])
+
+
+def alloc_grads(cfg: MoeConfig, device, with_scores=False) -> Grads:
+    T, d, f, N, k = cfg.T, cfg.d_model, cfg.d_ff, cfg.n_experts, cfg.top_k
+    dt = torch.float32 if cfg.dtype == MOE_F32 else torch.bfloat16
+    e = lambda *shape: torch.empty(shape, dtype=dt, device=device)  # noqa: E731
+    sh = cfg.d_ff_shared > 0
+    return Grads(
+        dx=e(T, d), dW_g=e(N, d), db_g=e(N), dW1=e(N, f, d), db1=e(N, f), dW2=e(N, d, f),
+        db2=e(N, d), dW1s=e(f, d) if sh else None, db1s=e(f) if sh else None,
+        dW2s=e(d, f) if sh else None, db2s=e(d) if sh else None,
+        dz=torch.empty((T, N), dtype=torch.float32, device=device) if with_scores else None,
+        dw=torch.empty((T, k), dtype=torch.float32, device=device) if with_scores else None)
+
+
+def backward(cfg: MoeConfig, x, weights: MoeWeights, fwd: Outputs, fwd_workspace, dy,
+             aux_weight: float, grads: Grads, workspace, stream=None):
+    _check(lib().moe_backward(C.byref(cfg), _ptr(x), C.byref(weights), C.byref(fwd.struct()),
+                              _ptr(fwd_workspace),
+                              fwd_workspace.numel() * fwd_workspace.element_size(), _ptr(dy),
+                              float(aux_weight), C.byref(grads.struct()), _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _stream(stream)),
+           "moe_backward")
+
+
 class MoeLayer:
     """Device-resident weights + workspace of one layer; ``forward`` runs it."""
 
@@ -341,6 +408,20 @@ class MoeLayer:
             out = alloc_outputs(self.cfg, self.device, with_logits=with_logits)
         forward(self.cfg, x, self.weights, out, self.workspace, stream)
         return out
+
+    def backward(self, x, out: Outputs, dy, aux_weight=0.01, grads: Grads | None = None,
+                 with_scores=False, stream=None) -> Grads:
+        """Gradients of total = task + aux_weight * balance given dy = d task / d y,
+        for the last ``forward`` (its outputs ``out`` and this layer's workspace)."""
+        if grads is None:
+            grads = alloc_grads(self.cfg, self.device, with_scores=with_scores)
+        need = backward_workspace_size(self.cfg)
+        if getattr(self, "bwd_workspace", None) is None or self.bwd_workspace.numel() < need:
+            self.bwd_workspace = torch.empty(max(need, 256), dtype=torch.uint8,
+                                             device=self.device)
+        backward(self.cfg, x, self.weights, out, self.workspace, dy, aux_weight, grads,
+                 self.bwd_workspace, stream)
+        return grads
 
 
 # ---- expert-choice routing ---------------------------------------------------------

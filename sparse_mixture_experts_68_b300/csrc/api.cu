@@ -1,6 +1,7 @@
 // C ABI of libmoe (declared in include/moe.h): host-side validation,
 // workspace layout, and the sequence of launches of one layer.
 #include <atomic>
+#include <cmath>
 #include <mutex>
 
 #include "common.cuh"
@@ -85,6 +86,47 @@ Workspace layout(const moe_config& c, void* base) {
   w.Yp = take(size_t(rows * c.d_model * es));
   w.bytes = off;
   return w;
+}
+
+// ---- backward ----
+
+struct BwdWorkspace {
+  void* dO;
+  void* A1;
+  void* dA;
+  void* dXp;
+  float* dz;
+  float* dw;
+  float* dxr;
+  size_t bytes;
+};
+
+BwdWorkspace bwd_layout(const moe_config& c, void* base) {
+  BwdWorkspace w{};
+  uintptr_t p = reinterpret_cast<uintptr_t>(base);
+  size_t off = 0;
+  auto take = [&](size_t n) {
+    const size_t at = off;
+    off += (n + 255) / 256 * 256;
+    return reinterpret_cast<void*>(p + at);
+  };
+  const int64_t rows = rows_max_of(c);
+  w.dO = take(size_t(rows * c.d_model) * 2);
+  w.A1 = take(size_t(rows * c.d_ff) * 2);
+  w.dA = take(size_t(rows * c.d_ff) * 2);
+  w.dXp = take(size_t(rows * c.d_model) * 2);
+  w.dz = static_cast<float*>(take(size_t(c.T * c.n_experts) * 4));
+  w.dw = static_cast<float*>(take(size_t(c.T * c.top_k) * 4));
+  w.dxr = static_cast<float*>(take(size_t(c.T * c.d_model) * 4));
+  w.bytes = off;
+  return w;
+}
+
+moe_status check_bwd_config(const moe_config* cfg) {
+  const moe_status st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  if (cfg->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
 }
 
 // ---- expert-choice routing ----
@@ -520,6 +562,66 @@ moe_status moe_forward_host(const moe_config* cfg, const void* x_host, const moe
     if (cp.n && cudaMemcpyAsync(cp.dst, cp.src, cp.n, cudaMemcpyDeviceToHost, s) != cudaSuccess)
       return MOE_ERR_CUDA;
   return cuda_status(cudaStreamSynchronize(s));
+}
+
+// ---- backward ----------------------------------------------------------------------
+
+size_t moe_backward_workspace_size(const moe_config* cfg) {
+  if (check_bwd_config(cfg) != MOE_OK) return 0;
+  return bwd_layout(*cfg, nullptr).bytes;
+}
+
+int32_t moe_backward_launch_count(const moe_config* cfg) {
+  if (check_bwd_config(cfg) != MOE_OK) return -1;
+  return backward_launch_count(*cfg);
+}
+
+moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights* w,
+                        const moe_outputs* fwd, void* fwd_workspace, size_t fwd_workspace_bytes,
+                        const void* dy, float aux_weight, const moe_grads* grads,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  moe_status st = check_bwd_config(cfg);
+  if (st != MOE_OK) return st;
+  const moe_config& c = *cfg;
+  st = check_weights(c, w, true, true);
+  if (st != MOE_OK) return st;
+  if (!fwd || !grads || !fwd_workspace || !workspace ||
+      (reinterpret_cast<uintptr_t>(fwd_workspace) & 255u) != 0 ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return MOE_ERR_INVALID_ARG;
+  auto ok16 = [](const void* q) { return q && aligned16(q); };
+  auto tok = [&](const void* q) { return c.T == 0 || ok16(q); };
+  if (!tok(x) || !tok(dy) || !tok(grads->dx) || !tok(fwd->topk_idx) || !tok(fwd->topk_w))
+    return MOE_ERR_INVALID_ARG;
+  const void* need[] = {grads->dW_g, grads->db_g, grads->dW1, grads->db1, grads->dW2,
+                        grads->db2, fwd->kept, fwd->mean_prob};
+  for (const void* q : need)
+    if (!ok16(q)) return MOE_ERR_INVALID_ARG;
+  if (c.d_ff_shared > 0) {
+    const void* ss[] = {grads->dW1s, grads->db1s, grads->dW2s, grads->db2s};
+    for (const void* q : ss)
+      if (!ok16(q)) return MOE_ERR_INVALID_ARG;
+  }
+  if (!std::isfinite(aux_weight)) return MOE_ERR_INVALID_ARG;
+  const Workspace fws = layout(c, fwd_workspace);
+  if (fwd_workspace_bytes < fws.bytes) return MOE_ERR_WORKSPACE;
+  const BwdWorkspace ws = bwd_layout(c, workspace);
+  if (workspace_bytes < ws.bytes) return MOE_ERR_WORKSPACE;
+  DeviceInfo di;
+  if (!device_info(&di)) return MOE_ERR_CUDA;
+  BackwardArgs a{};
+  a.w = w; a.g = grads; a.x = x; a.dy = dy;
+  a.Yp = fws.Yp; a.H = fws.H; a.Xp = fws.Xp; a.offsets = fws.offsets; a.kept = fwd->kept;
+  a.token_row = fws.token_row; a.topk_idx = fwd->topk_idx; a.topk_w = fwd->topk_w;
+  a.logits = fwd->logits ? fwd->logits : fws.logits; a.mean_prob = fwd->mean_prob;
+  a.aux_weight = aux_weight;
+  a.dO = ws.dO; a.A1 = ws.A1; a.dA = ws.dA; a.dXp = ws.dXp;
+  a.dz = grads->dz ? grads->dz : ws.dz;
+  a.dw = grads->dw ? grads->dw : ws.dw;
+  a.dxr = ws.dxr;
+  a.rows_max = rows_max_of(c);
+  a.status = di.status; a.wait_limit_ns = g_wait_limit_ns.load(); a.num_sms = di.num_sms;
+  return cuda_status(launch_backward(c, a, static_cast<cudaStream_t>(stream)));
 }
 
 // ---- expert-choice routing --------------------------------------------------------

@@ -1,0 +1,463 @@
+// Backward pass of the layer for the training loss total = task + alpha *
+// balance (botmartz.com "Mixture of Experts (MoE) and Mixtral", "Load
+// Balancing: The Hidden Challenge": total_loss = task_loss + 0.01 *
+// balance_loss; roadtointelligence.com "Keeping the experts busy": coefficient
+// 0.01).  The task loss enters as dy = d task / d y; the rest is the chain rule
+// through the forward, step by step:
+//
+//   gate step      per token: dw_j = <dy, Yp[row_j]>, dO[row_j] = w_j dy
+//                  (shared row: dy); the gates' softmax (over the k selected
+//                  scores, or the raw probabilities), plus the balance term
+//                  d p[t, e] = alpha 2 (m_e - 1/N) / ((N - 1) T), through the
+//                  softmax over all N -> dz [T, N]
+//   expert FFNs    A1 recomputed (first Linear without its activation), then
+//                  dA = (dO W2) act'(A1), dXp = dA W1, dW2 = dO^T H,
+//                  dW1 = dA^T Xp on the tensor cores (grouped_bwd_sm103.cu);
+//                  db2, db1 = column sums of dO, dA over each group's rows
+//   router         dW_g = dz^T x, db_g = sum_t dz, dx_router = dz W_g
+//                  (CUDA-core GEMMs: K or M is the expert count)
+//   dx             dx[t] = sum of dXp over t's kept rows (+ the shared row)
+//                  + dx_router[t]
+//
+// The top-k choice and the capacity drops are piecewise constant and pass no
+// gradient.  Every sum runs in a fixed order, so the gradients are
+// reproducible bit for bit.
+#include <float.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+// ---- zero the padding rows of grouped buffers ------------------------------------------
+
+struct PadBufs {
+  void* buf[3];
+  int64_t width[3];          // bf16 columns
+  int n;
+};
+
+// One block per group: rows [offsets[g] + live_g, offsets[g + 1]).
+__global__ void __launch_bounds__(256)
+    zero_pad_rows_kernel(const int32_t* __restrict__ offsets, const int32_t* __restrict__ kept,
+                         int n_routed, int shared_rows, PadBufs b) {
+  pdl_launch_dependents();
+  pdl_wait_previous();
+  const int g = blockIdx.x;
+  const int64_t live = g < n_routed ? kept[g] : shared_rows;
+  const int64_t r0 = offsets[g] + live, r1 = offsets[g + 1];
+  for (int i = 0; i < b.n; ++i) {
+    const int64_t nv = b.width[i] / 8;
+    uint4* base = static_cast<uint4*>(b.buf[i]);
+    for (int64_t j = threadIdx.x; j < (r1 - r0) * nv; j += blockDim.x)
+      base[(r0 + j / nv) * nv + j % nv] = make_uint4(0, 0, 0, 0);
+  }
+}
+
+// ---- gate step ------------------------------------------------------------------------
+
+constexpr int kGateWarps = 8;
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// One warp per token.  Shared memory per warp: p [N], dp [N], dz [N], dw [k].
+__global__ void __launch_bounds__(kGateWarps * 32)
+    bwd_gate_kernel(const __nv_bfloat16* __restrict__ dy, const __nv_bfloat16* __restrict__ Yp,
+                    const int32_t* __restrict__ token_row, const int32_t* __restrict__ topk_idx,
+                    const float* __restrict__ topk_w, const float* __restrict__ logits,
+                    const float* __restrict__ mean_prob, const int32_t* __restrict__ offsets,
+                    int T, int64_t d, int N, int k, int renorm, int has_shared, float aux,
+                    __nv_bfloat16* __restrict__ dO, float* __restrict__ dz_out,
+                    float* __restrict__ dw_out) {
+  extern __shared__ float gsm[];
+  pdl_launch_dependents();
+  pdl_wait_previous();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kGateWarps + warp;
+  if (t >= T) return;
+  float* P = gsm + size_t(warp) * (3 * N + k);
+  float* DP = P + N;
+  float* DZ = DP + N;
+  float* DW = DZ + N;
+  const int64_t nv = d / 8;
+  const uint4* dyr = reinterpret_cast<const uint4*>(dy + int64_t(t) * d);
+
+  // dw_j = <dy, o_j> and dO rows
+  for (int j = 0; j < k; ++j) {
+    const int64_t r = token_row[int64_t(t) * k + j];
+    float dot = 0.f;
+    if (r >= 0) {
+      const float wj = topk_w[int64_t(t) * k + j];
+      const uint4* orow = reinterpret_cast<const uint4*>(Yp + r * d);
+      uint4* drow = reinterpret_cast<uint4*>(dO + r * d);
+      for (int64_t c = lane; c < nv; c += 32) {
+        const uint4 a = __ldg(dyr + c), o = __ldg(orow + c);
+        const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+        const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&o);
+        uint4 q;
+        __nv_bfloat162* q2 = reinterpret_cast<__nv_bfloat162*>(&q);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 av = __bfloat1622float2(a2[i]), ov = __bfloat1622float2(o2[i]);
+          dot = fmaf(av.x, ov.x, fmaf(av.y, ov.y, dot));
+          q2[i] = __floats2bfloat162_rn(wj * av.x, wj * av.y);
+        }
+        drow[c] = q;
+      }
+      dot = warp_sum(dot);
+    }
+    if (lane == 0) DW[j] = dot;
+    if (dw_out && lane == 0) dw_out[int64_t(t) * k + j] = dot;
+  }
+  if (has_shared) {                           // the shared expert's gate is 1
+    uint4* drow = reinterpret_cast<uint4*>(dO + (int64_t(offsets[N]) + t) * d);
+    for (int64_t c = lane; c < nv; c += 32) drow[c] = __ldg(dyr + c);
+  }
+
+  // p = softmax(z) over all N
+  const float* zr = logits + int64_t(t) * N;
+  float m = -FLT_MAX;
+  for (int e = lane; e < N; e += 32) m = fmaxf(m, zr[e]);
+  m = warp_max(m);
+  float ssum = 0.f;
+  for (int e = lane; e < N; e += 32) {
+    const float ex = __expf(zr[e] - m);
+    P[e] = ex;
+    ssum += ex;
+  }
+  ssum = warp_sum(ssum);
+  const float inv = 1.0f / ssum;
+  // balance term: d p[t, e] = alpha 2 (m_e - 1/N) / ((N - 1) T)
+  const float cb = (aux != 0.f && N > 1) ? aux * 2.0f / (float(N - 1) * float(T)) : 0.f;
+  for (int e = lane; e < N; e += 32) {
+    P[e] *= inv;
+    DP[e] = cb * (mean_prob[e] - 1.0f / float(N));
+    DZ[e] = 0.f;
+  }
+  __syncwarp();
+  // gates
+  if (renorm) {
+    float sd = 0.f;
+    for (int j = lane; j < k; j += 32) sd += topk_w[int64_t(t) * k + j] * DW[j];
+    sd = warp_sum(sd);
+    for (int j = lane; j < k; j += 32) {
+      const float wj = topk_w[int64_t(t) * k + j];
+      DZ[topk_idx[int64_t(t) * k + j]] = wj * (DW[j] - sd);
+    }
+  } else {
+    for (int j = lane; j < k; j += 32) DP[topk_idx[int64_t(t) * k + j]] += DW[j];
+  }
+  __syncwarp();
+  // through the softmax over all N: p (dp - <p, dp>)
+  float pd = 0.f;
+  for (int e = lane; e < N; e += 32) pd += P[e] * DP[e];
+  pd = warp_sum(pd);
+  float* dzr = dz_out + int64_t(t) * N;
+  for (int e = lane; e < N; e += 32) dzr[e] = DZ[e] + P[e] * (DP[e] - pd);
+}
+
+// ---- column sums of groups (bias gradients) -----------------------------------------------
+
+// Block (g, chunk): columns chunk*256 .. +255 of group g's live rows; eight
+// warps take every eighth row, lanes 8 columns each; warps combine in order.
+__global__ void __launch_bounds__(256)
+    group_colsum_kernel(const __nv_bfloat16* __restrict__ src, int64_t width,
+                        const int32_t* __restrict__ offsets, const int32_t* __restrict__ kept,
+                        int n_routed, int shared_rows, __nv_bfloat16* __restrict__ out,
+                        __nv_bfloat16* __restrict__ out_s) {
+  __shared__ float part[8][256];
+  pdl_launch_dependents();
+  pdl_wait_previous();
+  const int g = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t c0 = int64_t(blockIdx.y) * 256 + lane * 8;
+  const int64_t live = g < n_routed ? kept[g] : shared_rows;
+  const int64_t r0 = offsets[g];
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  if (c0 < width) {
+    for (int64_t r = warp; r < live; r += 8) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(src + (r0 + r) * width + c0));
+      const __nv_bfloat162* v2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(v2[i]);
+        acc[2 * i] += f.x;
+        acc[2 * i + 1] += f.y;
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) part[warp][lane * 8 + i] = acc[i];
+  __syncthreads();
+  const int col = threadIdx.x;
+  const int64_t cc = int64_t(blockIdx.y) * 256 + col;
+  if (cc < width) {
+    float s = 0.f;
+    for (int w = 0; w < 8; ++w) s += part[w][col];
+    __nv_bfloat16* dst = g < n_routed ? out + int64_t(g) * width : out_s;
+    dst[cc] = __float2bfloat16_rn(s);
+  }
+}
+
+// db_g[e] = sum_t dz[t, e] (fp32 in, bf16 out), one thread per expert.
+__global__ void __launch_bounds__(256)
+    router_bias_grad_kernel(const float* __restrict__ dz, int T, int N,
+                            __nv_bfloat16* __restrict__ db_g) {
+  pdl_launch_dependents();
+  pdl_wait_previous();
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= N) return;
+  float s = 0.f;
+  for (int t = 0; t < T; ++t) s += dz[int64_t(t) * N + e];
+  db_g[e] = __float2bfloat16_rn(s);
+}
+
+// ---- router GEMMs on CUDA cores ---------------------------------------------------------------
+//
+// C[m, n] = sum_k A(m, k) B[k, n] with A fp32 addressed by strides (am, ak)
+// and B bf16 row-major [K, ldb]; C fp32 or bf16 row-major [M, ldc].
+constexpr int kRg = 64, kRk = 16;
+
+template <typename TOut>
+__global__ void __launch_bounds__(256)
+    router_grad_gemm_kernel(const float* __restrict__ A, int64_t am, int64_t ak,
+                            const __nv_bfloat16* __restrict__ B, int64_t ldb, int64_t M,
+                            int64_t Nn, int64_t K, TOut* __restrict__ C, int64_t ldc) {
+  __shared__ float As[kRk][kRg + 4];
+  __shared__ float Bs[kRk][kRg + 4];
+  pdl_launch_dependents();
+  pdl_wait_previous();
+  const int64_t m0 = int64_t(blockIdx.y) * kRg, n0 = int64_t(blockIdx.x) * kRg;
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  float acc[4][4] = {};
+  for (int64_t k0 = 0; k0 < K; k0 += kRk) {
+    // A tile 64 x 16: along m when A is m-contiguous, else along k
+    for (int i = tid; i < kRg * kRk; i += 256) {
+      int mm, kk;
+      if (am == 1) { mm = i % kRg; kk = i / kRg; } else { kk = i % kRk; mm = i / kRk; }
+      const int64_t gm = m0 + mm, gk = k0 + kk;
+      As[kk][mm] = (gm < M && gk < K) ? A[gm * am + gk * ak] : 0.f;
+    }
+    for (int i = tid; i < kRg * kRk; i += 256) {
+      const int nn = i % kRg, kk = i / kRg;
+      const int64_t gn = n0 + nn, gk = k0 + kk;
+      Bs[kk][nn] = (gn < Nn && gk < K) ? __bfloat162float(B[gk * ldb + gn]) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < kRk; ++kk) {
+      float av[4], bv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) av[i] = As[kk][ty + 16 * i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) bv[j] = Bs[kk][tx + 16 * j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int64_t gm = m0 + ty + 16 * i;
+    if (gm >= M) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int64_t gn = n0 + tx + 16 * j;
+      if (gn < Nn) C[gm * ldc + gn] = from_f32<TOut>(acc[i][j]);
+    }
+  }
+}
+
+// ---- dx -----------------------------------------------------------------------------------------
+
+constexpr int kDxWarps = 8;
+
+// dx[t] = sum over t's kept rows of dXp (slot order) + the shared row + dxr[t]
+__global__ void __launch_bounds__(kDxWarps * 32)
+    bwd_dx_kernel(const __nv_bfloat16* __restrict__ dXp, const int32_t* __restrict__ token_row,
+                  const int32_t* __restrict__ offsets, const float* __restrict__ dxr, int T,
+                  int k, int N, int has_shared, int64_t d, __nv_bfloat16* __restrict__ dx) {
+  pdl_launch_dependents();
+  pdl_wait_previous();
+  const int lane = threadIdx.x & 31;
+  const int64_t t = int64_t(blockIdx.x) * kDxWarps + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const int64_t nv = d / 8;
+  for (int64_t c = lane; c < nv; c += 32) {
+    float acc[8];
+    const float4* xr = reinterpret_cast<const float4*>(dxr + t * d) + 2 * c;
+    const float4 r0 = xr[0], r1 = xr[1];
+    acc[0] = r0.x; acc[1] = r0.y; acc[2] = r0.z; acc[3] = r0.w;
+    acc[4] = r1.x; acc[5] = r1.y; acc[6] = r1.z; acc[7] = r1.w;
+    for (int j = 0; j <= k; ++j) {
+      int64_t r;
+      if (j < k) r = token_row[t * k + j];
+      else r = has_shared ? int64_t(offsets[N]) + t : -1;
+      if (r < 0) continue;
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(dXp + r * d) + c);
+      const __nv_bfloat162* v2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(v2[i]);
+        acc[2 * i] += f.x;
+        acc[2 * i + 1] += f.y;
+      }
+    }
+    uint4 o;
+    __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o2[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+    reinterpret_cast<uint4*>(dx + t * d)[c] = o;
+  }
+}
+
+template <typename TOut>
+cudaError_t launch_router_grad_gemm(const float* A, int64_t am, int64_t ak,
+                                    const __nv_bfloat16* B, int64_t ldb, int64_t M, int64_t Nn,
+                                    int64_t K, TOut* C, int64_t ldc, cudaStream_t s) {
+  if (M == 0 || Nn == 0) return cudaSuccess;
+  dim3 grid(unsigned((Nn + kRg - 1) / kRg), unsigned((M + kRg - 1) / kRg));
+  return launch_pdl(router_grad_gemm_kernel<TOut>, grid, dim3(256), 0, s, A, am, ak, B, ldb, M,
+                    Nn, K, C, ldc);
+}
+
+// n bf16 zeros: 16-byte words, then the tail element by element.
+__global__ void __launch_bounds__(256) fill_zero_kernel(__nv_bfloat16* __restrict__ p,
+                                                        int64_t n) {
+  pdl_launch_dependents();
+  pdl_wait_previous();
+  const int64_t n16 = n / 8;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  const int64_t i0 = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (int64_t i = i0; i < n16; i += stride)
+    reinterpret_cast<uint4*>(p)[i] = make_uint4(0, 0, 0, 0);
+  for (int64_t i = n16 * 8 + i0; i < n; i += stride) p[i] = __float2bfloat16_rn(0.f);
+}
+
+// No tokens: every parameter gradient is zero.
+cudaError_t zero_param_grads(const moe_config& c, const moe_grads* g, cudaStream_t s) {
+  const int64_t N = c.n_experts, d = c.d_model, f = c.d_ff;
+  struct Buf { void* p; int64_t n; };
+  const Buf bufs[] = {{g->dW_g, N * d}, {g->db_g, N},     {g->dW1, N * f * d}, {g->db1, N * f},
+                      {g->dW2, N * d * f}, {g->db2, N * d}, {g->dW1s, f * d},  {g->db1s, f},
+                      {g->dW2s, d * f},  {g->db2s, d}};
+  const int nb = c.d_ff_shared > 0 ? 10 : 6;
+  for (int i = 0; i < nb; ++i) {
+    const int64_t want = (bufs[i].n / 8 + 255) / 256 + 1;
+    const cudaError_t e =
+        launch_pdl(fill_zero_kernel, dim3(unsigned(want < 1184 ? want : 1184)), dim3(256), 0, s,
+                   static_cast<__nv_bfloat16*>(bufs[i].p), bufs[i].n);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace
+
+int backward_launch_count(const moe_config& c) {
+  if (c.T == 0) return c.d_ff_shared > 0 ? 10 : 6;    // zero parameter gradients
+  // gate, padding, A1, dA, dXp, dW2, dW1, db2, db1, dx_router, dW_g, db_g, dx
+  return 13;
+}
+
+cudaError_t launch_backward(const moe_config& c, const BackwardArgs& a, cudaStream_t s) {
+  if (c.T == 0) return zero_param_grads(c, a.g, s);
+  const int N = int(c.n_experts), k = int(c.top_k), T = int(c.T);
+  const int64_t d = c.d_model, f = c.d_ff;
+  const int hs = c.d_ff_shared > 0 ? 1 : 0;
+  const moe_weights* w = a.w;
+  const int groups = N + hs;
+
+  // gate step: dO rows, dz
+  {
+    const size_t smem = size_t(kGateWarps) * (3 * N + k) * sizeof(float);
+    if (smem > 48 * 1024) {
+      const cudaError_t e = cudaFuncSetAttribute(
+          bwd_gate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+      if (e != cudaSuccess) return e;
+    }
+    const cudaError_t e = launch_pdl(
+        bwd_gate_kernel, dim3(unsigned((T + kGateWarps - 1) / kGateWarps)),
+        dim3(kGateWarps * 32), smem, s, static_cast<const __nv_bfloat16*>(a.dy),
+        static_cast<const __nv_bfloat16*>(a.Yp), a.token_row, a.topk_idx, a.topk_w, a.logits,
+        a.mean_prob, a.offsets, T, d, N, k, c.renormalize ? 1 : 0, hs, a.aux_weight,
+        static_cast<__nv_bfloat16*>(a.dO), a.dz, a.dw);
+    if (e != cudaSuccess) return e;
+  }
+  // padding rows of dO, H and Xp -> 0 (the wgrads run K over whole 64-row blocks)
+  {
+    PadBufs pb{};
+    pb.buf[0] = a.dO; pb.width[0] = d;
+    pb.buf[1] = a.H; pb.width[1] = f;
+    pb.buf[2] = a.Xp; pb.width[2] = d;
+    pb.n = 3;
+    const cudaError_t e = launch_pdl(zero_pad_rows_kernel, dim3(unsigned(groups)), dim3(256), 0,
+                                     s, a.offsets, a.kept, N, hs ? T : 0, pb);
+    if (e != cudaSuccess) return e;
+  }
+  GroupedFfnArgs ga{};
+  ga.offsets = a.offsets; ga.kept = a.kept; ga.w = w; ga.rows_max = a.rows_max;
+  ga.status = a.status; ga.wait_limit_ns = a.wait_limit_ns; ga.num_sms = a.num_sms;
+  BwdGemmArgs bg{};
+  bg.offsets = a.offsets; bg.kept = a.kept; bg.rows_max = a.rows_max; bg.status = a.status;
+  bg.wait_limit_ns = a.wait_limit_ns; bg.num_sms = a.num_sms;
+  cudaError_t e;
+  // A1 = Xp W1^T + b1 (the pre-activation, recomputed)
+  e = launch_grouped_linear_bf16(c, ga, a.Xp, w->W1, w->W1s, w->b1, w->b1s, a.A1, d, f, s);
+  if (e != cudaSuccess) return e;
+  // dA = (dO . W2) act'(A1);  dXp = dA . W1
+  e = launch_bwd_dgrad(c, bg, a.dO, w->W2, w->W2s, d, f, c.act, a.A1, a.dA, s);
+  if (e != cudaSuccess) return e;
+  e = launch_bwd_dgrad(c, bg, a.dA, w->W1, w->W1s, f, d, -1, nullptr, a.dXp, s);
+  if (e != cudaSuccess) return e;
+  // dW2 = dO^T H [d, f];  dW1 = dA^T Xp [f, d]
+  e = launch_bwd_wgrad(c, bg, a.dO, d, a.H, f, a.g->dW2, a.g->dW2s, s);
+  if (e != cudaSuccess) return e;
+  e = launch_bwd_wgrad(c, bg, a.dA, f, a.Xp, d, a.g->dW1, a.g->dW1s, s);
+  if (e != cudaSuccess) return e;
+  // db2, db1
+  e = launch_pdl(group_colsum_kernel, dim3(unsigned(groups), unsigned((d + 255) / 256)),
+                 dim3(256), 0, s, static_cast<const __nv_bfloat16*>(a.dO), d, a.offsets,
+                 a.kept, N, hs ? T : 0, static_cast<__nv_bfloat16*>(a.g->db2),
+                 static_cast<__nv_bfloat16*>(a.g->db2s));
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(group_colsum_kernel, dim3(unsigned(groups), unsigned((f + 255) / 256)),
+                 dim3(256), 0, s, static_cast<const __nv_bfloat16*>(a.dA), f, a.offsets,
+                 a.kept, N, hs ? T : 0, static_cast<__nv_bfloat16*>(a.g->db1),
+                 static_cast<__nv_bfloat16*>(a.g->db1s));
+  if (e != cudaSuccess) return e;
+  // router: dxr = dz W_g [T, d] fp32; dW_g = dz^T x [N, d]; db_g = sum_t dz
+  e = launch_router_grad_gemm<float>(a.dz, N, 1, static_cast<const __nv_bfloat16*>(w->W_g), d,
+                                     T, d, N, a.dxr, d, s);
+  if (e != cudaSuccess) return e;
+  e = launch_router_grad_gemm<__nv_bfloat16>(a.dz, 1, N, static_cast<const __nv_bfloat16*>(a.x),
+                                             d, N, d, T,
+                                             static_cast<__nv_bfloat16*>(a.g->dW_g), d, s);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(router_bias_grad_kernel, dim3(unsigned((N + 255) / 256)), dim3(256), 0, s,
+                 static_cast<const float*>(a.dz), T, N,
+                 static_cast<__nv_bfloat16*>(a.g->db_g));
+  if (e != cudaSuccess) return e;
+  // dx
+  return launch_pdl(bwd_dx_kernel, dim3(unsigned((T + kDxWarps - 1) / kDxWarps)),
+                    dim3(kDxWarps * 32), 0, s, static_cast<const __nv_bfloat16*>(a.dXp),
+                    a.token_row, a.offsets, static_cast<const float*>(a.dxr), T, k, N, hs, d,
+                    static_cast<__nv_bfloat16*>(a.g->dx));
+}
+
+}  // namespace moe

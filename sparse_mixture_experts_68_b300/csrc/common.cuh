@@ -79,6 +79,12 @@ __device__ __forceinline__ float erf_as7126(float z) {
 __device__ __forceinline__ float gelu_erf(float v) {
   return 0.5f * v * (1.0f + erf_as7126(v * 0.70710678118654752440f));
 }
+// d GELU / d v = Phi(v) + v phi(v): the normal CDF (from the erf above) plus
+// v times the normal density exp(-v^2 / 2) / sqrt(2 pi).
+__device__ __forceinline__ float gelu_erf_grad(float v) {
+  return 0.5f * (1.0f + erf_as7126(v * 0.70710678118654752440f)) +
+         v * 0.39894228040143267794f * __expf(-0.5f * v * v);
+}
 __device__ __forceinline__ float apply_act(float v, int act) {
   return act == MOE_ACT_RELU ? fmaxf(v, 0.0f) : gelu_erf(v);
 }

@@ -163,4 +163,62 @@ int64_t rows_max_for(const moe_config& c);             // moe_rows_max without t
 // ---- self test of the bounded wait (api.cu) ---------------------------------------
 cudaError_t launch_bounded_wait_selftest(uint64_t limit_ns, int32_t* status, cudaStream_t s);
 
+// ---- backward (grouped_bwd_sm103.cu, backward.cu) --------------------------------
+
+struct BwdGemmArgs {
+  const int32_t* offsets;   // [N + 2]
+  const int32_t* kept;      // [N]
+  int64_t rows_max;
+  int32_t* status;
+  uint64_t wait_limit_ns;
+  int num_sms;
+};
+// out = dOut . W[e] per group ([K, Nd] weights as stored), times act'(pre)
+// when act >= 0; group padding rows written as zeros
+cudaError_t launch_bwd_dgrad(const moe_config& c, const BwdGemmArgs& g, const void* dOut,
+                             const void* W, const void* Ws, int64_t K, int64_t Nd, int act,
+                             const void* pre, void* out, cudaStream_t s);
+// out[e] = L[group e]^T . R[group e] ([Md, Nd] per group; shared into out_s)
+cudaError_t launch_bwd_wgrad(const moe_config& c, const BwdGemmArgs& g, const void* Lm,
+                             int64_t Md, const void* Rm, int64_t Nd, void* out, void* out_s,
+                             cudaStream_t s);
+struct BackwardArgs {
+  const moe_weights* w;
+  const moe_grads* g;
+  const void* x;            // [T, d]
+  const void* dy;           // [T, d]
+  // saved by the forward
+  const void* Yp;           // [rows_max, d]
+  void* H;                  // [rows_max, d_ff] (padding rows zeroed here)
+  void* Xp;                 // [rows_max, d] (padding rows zeroed here)
+  const int32_t* offsets;
+  const int32_t* kept;
+  const int32_t* token_row;
+  const int32_t* topk_idx;
+  const float* topk_w;
+  const float* logits;
+  const float* mean_prob;
+  float aux_weight;
+  // backward scratch
+  void* dO;                 // [rows_max, d]
+  void* A1;                 // [rows_max, d_ff]
+  void* dA;                 // [rows_max, d_ff]
+  void* dXp;                // [rows_max, d]
+  float* dz;                // [T, N]
+  float* dw;                // [T, k]
+  float* dxr;               // [T, d]
+  int64_t rows_max;
+  int32_t* status;
+  uint64_t wait_limit_ns;
+  int num_sms;
+};
+cudaError_t launch_backward(const moe_config& c, const BackwardArgs& a, cudaStream_t s);
+int backward_launch_count(const moe_config& c);
+
+// the first Linear without its activation: out = A W^T + b per group (bf16)
+cudaError_t launch_grouped_linear_bf16(const moe_config& c, const GroupedFfnArgs& g,
+                                       const void* A, const void* W, const void* Ws,
+                                       const void* bias, const void* bias_s, void* out,
+                                       int64_t K, int64_t Nd, cudaStream_t s);
+
 }  // namespace moe

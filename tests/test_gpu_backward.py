@@ -1,0 +1,176 @@
+"""The backward pass on the GPU (through the C ABI) against the oracle's
+backward (float64 chain rule, pinned to torch autograd and finite
+differences): every gradient of total = <dy, y> + aux * balance.
+
+Bar: each gradient tensor within 2e-2 relative L2 of the oracle.  The GPU
+stores five bf16 intermediates on the way (dO = w dy, the recomputed
+pre-activation, dA, dXp and the expert outputs behind dw), each rounded to 8
+significant bits (relative 2^-9 ~ 2e-3 per element, independent across
+elements), so a tensor's relative L2 error is a few 1e-3; the bar leaves a
+5-10x margin.  The oracle takes the GPU's top-k choice (the forward parity
+checks that choice against the oracle's own)."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_oracle as O
+from sparse_mixture_experts_68_b300 import binding as B
+from sparse_mixture_experts_68_b300 import synth
+from sparse_mixture_experts_68_b300.workloads import (ACT_GELU_ERF, ACT_RELU, DT_BF16,
+                                                      WORKLOADS, Workload)
+
+from parity import Experts, check_layer, to64
+
+pytestmark = pytest.mark.gpu
+
+GRAD_TOL = 2e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    B.lib()
+    yield
+    torch.cuda.synchronize()
+    assert B.get_device_status() == B.MOE_OK
+
+
+def make_dy(wl, seed):
+    g = torch.Generator(device="cpu").manual_seed(1000 + seed)
+    return torch.randn((wl.T, wl.d_model), generator=g).to(torch.bfloat16).cuda()
+
+
+def rel_l2(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
+
+
+def run_backward(wl, aux):
+    t = synth.make_layer(wl, device="cuda")
+    layer = B.MoeLayer(wl, t)
+    out = layer.forward(t["x"], with_logits=True)
+    torch.cuda.synchronize()
+    check_layer(wl, layer.cfg, t, out)
+    dy = make_dy(wl, wl.seed)
+    grads = layer.backward(t["x"], out, dy, aux_weight=aux, with_scores=True)
+    torch.cuda.synchronize()
+    return t, layer, out, dy, grads
+
+
+def check_backward(wl, layer, t, out, dy, aux, grads):
+    cfg = layer.cfg
+    shared = None
+    if cfg.d_ff_shared:
+        shared = tuple(to64(t[n]) for n in ("W1s", "b1s", "W2s", "b2s"))
+    ref = O.moe_backward(to64(t["x"]), to64(t["W_g"]), to64(t["b_g"]), Experts(t["W1"]),
+                         Experts(t["b1"]), Experts(t["W2"]), Experts(t["b2"]), to64(dy),
+                         k=cfg.top_k, act=cfg.act, capacity=cfg.capacity,
+                         renormalize=bool(cfg.renormalize), shared=shared, aux_weight=aux,
+                         round_hidden_bf16=True,
+                         idx_override=out.topk_idx.cpu().numpy().astype(np.int64))
+    pairs = [("dx", grads.dx, ref.dx), ("dW_g", grads.dW_g, ref.dW_g),
+             ("db_g", grads.db_g, ref.db_g), ("dW1", grads.dW1, ref.dW1),
+             ("db1", grads.db1, ref.db1), ("dW2", grads.dW2, ref.dW2),
+             ("db2", grads.db2, ref.db2), ("dz", grads.dz, ref.dz), ("dw", grads.dw, ref.dw)]
+    if shared is not None:
+        pairs += [(n, getattr(grads, n), r) for n, r in zip(("dW1s", "db1s", "dW2s", "db2s"),
+                                                            ref.shared)]
+    report = {}
+    for name, g, r in pairs:
+        report[name] = rel_l2(to64(g), r)
+    bad = {n: v for n, v in report.items() if not v <= GRAD_TOL}
+    assert not bad, f"gradients off: {bad} (all: {report})"
+    # dropped slots pass no gradient to their gate
+    dw = grads.dw.cpu().numpy()
+    keep = O.group_by_expert(out.topk_idx.cpu().numpy(), cfg.n_experts, cfg.capacity).keep
+    assert np.all(dw[~keep] == 0.0)
+    return report
+
+
+SMALL = [
+    Workload("bwd_gelu", T=300, d_model=128, d_ff=256, n_experts=4, top_k=2,
+             act=ACT_GELU_ERF, dtype=DT_BF16, seed=81),
+    # d = 192: dW2's rows (d) end inside a 128-row tile; d_ff = 320: 64-wide tiles;
+    # capacity drops; shared expert; ReLU
+    Workload("bwd_relu_cap_shared", T=500, d_model=192, d_ff=320, n_experts=8, top_k=2,
+             act=ACT_RELU, dtype=DT_BF16, capacity_factor=0.8, d_ff_shared=320, seed=82),
+    Workload("bwd_raw_gates", T=700, d_model=256, d_ff=256, n_experts=16, top_k=3,
+             act=ACT_GELU_ERF, dtype=DT_BF16, renormalize=0, seed=83),
+    # N % 64 == 0 (tensor-core router), shared expert
+    Workload("bwd_many_experts", T=400, d_model=128, d_ff=128, n_experts=64, top_k=6,
+             act=ACT_GELU_ERF, dtype=DT_BF16, d_ff_shared=128, seed=84),
+    # ~1000-row groups: several m-tiles per group in the dgrads, many K blocks in the wgrads
+    Workload("bwd_big_groups", T=2000, d_model=256, d_ff=512, n_experts=2, top_k=1,
+             act=ACT_GELU_ERF, dtype=DT_BF16, seed=85),
+]
+
+
+@pytest.mark.parametrize("wl", SMALL, ids=[w.name for w in SMALL])
+@pytest.mark.parametrize("aux", [0.01, 0.5])
+def test_small_layers_backward(wl, aux):
+    t, layer, out, dy, grads = run_backward(wl, aux)
+    report = check_backward(wl, layer, t, out, dy, aux, grads)
+    print("grad parity", wl.name, aux, report)
+
+
+def test_workload_c1_page1_bf16_backward():
+    wl = WORKLOADS["c1_page1_bf16"]
+    t, layer, out, dy, grads = run_backward(wl, 0.01)
+    report = check_backward(wl, layer, t, out, dy, 0.01, grads)
+    print("grad parity", wl.name, report)
+
+
+def test_backward_deterministic_and_launch_count():
+    wl = SMALL[1]
+    t, layer, out, dy, g1 = run_backward(wl, 0.01)
+    g2 = layer.backward(t["x"], out, dy, aux_weight=0.01, with_scores=True)
+    torch.cuda.synchronize()
+    for n in ("dx", "dW_g", "db_g", "dW1", "db1", "dW2", "db2", "dW1s", "db1s", "dW2s", "db2s",
+              "dz", "dw"):
+        assert torch.equal(getattr(g1, n), getattr(g2, n)), n
+    assert B.backward_launch_count(layer.cfg) == 13
+
+
+def test_backward_no_tokens():
+    wl = SMALL[0]
+    t = synth.make_layer(wl.with_tokens(0), device="cuda")
+    layer = B.MoeLayer(wl, t, T=0)
+    out = layer.forward(t["x"], with_logits=True)
+    dy = torch.empty((0, wl.d_model), dtype=torch.bfloat16, device="cuda")
+    grads = B.alloc_grads(layer.cfg, "cuda")
+    for n in ("dW_g", "db_g", "dW1", "db1", "dW2", "db2"):
+        getattr(grads, n).fill_(1.0)
+    layer.backward(t["x"], out, dy, grads=grads)
+    torch.cuda.synchronize()
+    # no tokens: every parameter gradient is zero
+    for n in ("dW_g", "db_g", "dW1", "db1", "dW2", "db2"):
+        assert torch.all(getattr(grads, n) == 0), n
+    assert B.backward_launch_count(layer.cfg) == 6
+
+
+def test_balance_term_alone():
+    """dy = 0: only aux * balance has a gradient.  The expert weights get none;
+    the router and, through it, x get the balance statistic's gradient."""
+    wl = SMALL[3]
+    t = synth.make_layer(wl, device="cuda")
+    layer = B.MoeLayer(wl, t)
+    out = layer.forward(t["x"], with_logits=True)
+    dy = torch.zeros((wl.T, wl.d_model), dtype=torch.bfloat16, device="cuda")
+    grads = layer.backward(t["x"], out, dy, aux_weight=1.0, with_scores=True)
+    torch.cuda.synchronize()
+    for n in ("dW1", "db1", "dW2", "db2", "dW1s", "db1s", "dW2s", "db2s", "dw"):
+        assert torch.all(getattr(grads, n) == 0), n
+    ref = O.moe_backward(to64(t["x"]), to64(t["W_g"]), to64(t["b_g"]), Experts(t["W1"]),
+                         Experts(t["b1"]), Experts(t["W2"]), Experts(t["b2"]), to64(dy),
+                         k=wl.top_k, act=wl.act, shared=tuple(to64(t[n]) for n in
+                                                              ("W1s", "b1s", "W2s", "b2s")),
+                         aux_weight=1.0, round_hidden_bf16=True,
+                         idx_override=out.topk_idx.cpu().numpy().astype(np.int64))
+    for name, g, r in [("dz", grads.dz, ref.dz), ("dW_g", grads.dW_g, ref.dW_g),
+                       ("db_g", grads.db_g, ref.db_g), ("dx", grads.dx, ref.dx)]:
+        err = rel_l2(to64(g), r)
+        assert err <= GRAD_TOL, (name, err)
+    assert float(np.abs(ref.dz).max()) > 0.0
