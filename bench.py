@@ -33,6 +33,9 @@ if ROOT not in sys.path:
 
 DEFAULT_WORKLOAD = "c1_page1_bf16"
 METRIC = "MoE-layer tokens/s on 1 B300; % of bf16 tensor peak / % of HBM BW"
+TRAIN_METRIC = ("MoE-layer training tokens/s (forward + backward of task + 0.01 balance) "
+                "on 1 B300")
+AUX_WEIGHT = 0.01
 L2_FLUSH_BYTES = 512 << 20
 
 
@@ -45,6 +48,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--mode", default="forward", choices=["forward", "train"],
+                    help="train: one step = moe_forward + moe_backward (bf16 top-k layers)")
     return ap.parse_args()
 
 
@@ -196,6 +201,34 @@ def oracle_step(tensors, wl, tokens):
     return run
 
 
+def oracle_train_step(tensors, wl, tokens):
+    """Forward and backward of the oracle on the first `tokens` tokens."""
+    import numpy as np
+    import torch
+
+    from oracle import moe_oracle as O
+
+    f64 = lambda v: v.detach().to("cpu", torch.float64).numpy()  # noqa: E731
+    x = f64(tensors["x"][:tokens])
+    W = {n: f64(tensors[n]) for n in ("W_g", "b_g", "W1", "b1", "W2", "b2")}
+    shared = None
+    if wl.d_ff_shared:
+        shared = tuple(f64(tensors[n]) for n in ("W1s", "b1s", "W2s", "b2s"))
+    cap = O.expert_capacity(wl.capacity_factor, tokens, wl.n_experts) \
+        if wl.capacity_factor > 0 else 0
+    dy = np.random.default_rng(0).normal(0, 1, x.shape)
+
+    def run():
+        O.moe_forward(x, W["W_g"], W["b_g"], W["W1"], W["b1"], W["W2"], W["b2"], k=wl.top_k,
+                      act=wl.act, capacity=cap, renormalize=bool(wl.renormalize),
+                      shared=shared, round_hidden_bf16=True)
+        return O.moe_backward(x, W["W_g"], W["b_g"], W["W1"], W["b1"], W["W2"], W["b2"], dy,
+                              k=wl.top_k, act=wl.act, capacity=cap,
+                              renormalize=bool(wl.renormalize), shared=shared,
+                              aux_weight=AUX_WEIGHT, round_hidden_bf16=True)
+    return run
+
+
 def oracle_threads():
     try:
         from threadpoolctl import threadpool_info
@@ -220,8 +253,9 @@ def run_reference(args, wl, rank, world):
     if rank != 0:
         return None
     tensors = synth.make_layer(wl, device="cpu")
-    S = cpu_sample_tokens(wl)
-    step = oracle_step(tensors, wl, S)
+    train = args.mode == "train"
+    S = max(16, cpu_sample_tokens(wl) // 4) if train else cpu_sample_tokens(wl)
+    step = oracle_train_step(tensors, wl, S) if train else oracle_step(tensors, wl, S)
     for _ in range(args.warmup):
         step()
     t0 = time.perf_counter()
@@ -232,7 +266,8 @@ def run_reference(args, wl, rank, world):
     cores = oracle_threads()
     del torch
     return {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "metric": TRAIN_METRIC if train else METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "impl": "reference",
@@ -472,6 +507,181 @@ def run_ours(args, wl, rank, world, local_rank):
     return res
 
 
+def run_train(args, wl, rank, world, local_rank):
+    """One step = moe_forward + moe_backward of total = task + 0.01 balance with
+    a fixed synthetic dy, captured once as a CUDA graph and replayed."""
+    import torch
+    import torch.distributed as dist
+
+    from sparse_mixture_experts_68_b300 import binding as B
+    from sparse_mixture_experts_68_b300 import synth
+    from sparse_mixture_experts_68_b300.workloads import flops
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    tensors = synth.make_layer(wl, device=dev)
+    layer = B.MoeLayer(wl, tensors, device=dev)
+    cfg = layer.cfg
+    out = B.alloc_outputs(cfg, dev)
+    grads = B.alloc_grads(cfg, dev)
+    bws = torch.empty(B.backward_workspace_size(cfg), dtype=torch.uint8, device=dev)
+    g = torch.Generator(device="cpu").manual_seed(7)
+    dy = torch.randn((wl.T, wl.d_model), generator=g).to(torch.bfloat16).to(dev)
+    x = tensors["x"]
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(dev)
+    fev = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
+    bev = [torch.cuda.Event(enable_timing=True) for _ in range(8)]
+
+    def step():
+        B.forward(cfg, x, layer.weights, out, layer.workspace, stream)
+        B.backward(cfg, x, layer.weights, out, layer.workspace, dy, AUX_WEIGHT, grads, bws,
+                   stream)
+
+    def step_profiled():
+        B.forward_profiled(cfg, x, layer.weights, out, layer.workspace, fev, stream)
+        B.backward_profiled(cfg, x, layer.weights, out, layer.workspace, dy, AUX_WEIGHT, grads,
+                            bws, bev, stream)
+
+    with torch.cuda.stream(stream):
+        for ev in fev + bev:
+            ev.record(stream)
+        for _ in range(3):
+            step_profiled()
+            step()
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    torch.cuda.synchronize(dev)
+
+    def flush_l2(i):
+        with torch.cuda.stream(stream):
+            flush.fill_(i)
+
+    for i in range(max(args.warmup, 3)):
+        flush_l2(i)
+        with torch.cuda.stream(stream):
+            graph.replay()
+    torch.cuda.synchronize(dev)
+    assert B.get_device_status() == B.MOE_OK
+    K = args.steps
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.05)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.mark_start()
+    marks = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(K)]
+    for i in range(K):
+        flush_l2(i)
+        with torch.cuda.stream(stream):
+            marks[i][0].record(stream)
+            graph.replay()
+            marks[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    clocks.mark_end()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = job_time_ms(sum(a.elapsed_time(b) for a, b in marks), world, dev)
+    fwd_stage, bwd_stage = [], []
+    for i in range(K):
+        flush_l2(i)
+        with torch.cuda.stream(stream):
+            step_profiled()
+        stream.synchronize()
+        fwd_stage.append([fev[j].elapsed_time(fev[j + 1]) for j in range(6)])
+        bwd_stage.append([bev[j].elapsed_time(bev[j + 1]) for j in range(7)])
+    assert B.get_device_status() == B.MOE_OK
+    fnames = STAGES
+    bnames = ("gate_and_padding", "recompute_A1", "dgrad_dA", "dgrad_dXp", "wgrad_dW2",
+              "wgrad_dW1", "bias_router_dx")
+    fmean = {n: statistics.mean(s[i] for s in fwd_stage) for i, n in enumerate(fnames)}
+    bmean = {n: statistics.mean(s[i] for s in bwd_stage) for i, n in enumerate(bnames)}
+
+    kept_rows = int(out.kept.sum().item())
+    n_kept = int((out.kept > 0).sum().item())
+    T = cfg.T
+    rows = kept_rows + (T if wl.d_ff_shared else 0)
+    es = wl.elem_bytes
+    pk = peaks()
+    gemm_flop = 2.0 * wl.d_model * wl.d_ff * rows           # one grouped GEMM launch
+    wbytes = (n_kept + (1 if wl.d_ff_shared else 0)) * wl.d_model * wl.d_ff * es
+    act = rows * (wl.d_model + wl.d_ff) * es
+    gemm_names = [("forward_linear1", fmean["ffn_linear1"]), ("forward_linear2",
+                                                               fmean["ffn_linear2"])] + \
+        [(n, bmean[n]) for n in ("recompute_A1", "dgrad_dA", "dgrad_dXp", "wgrad_dW2",
+                                 "wgrad_dW1")]
+    gemm_ms = sum(ms for _, ms in gemm_names)
+    launches = len(gemm_names)
+    gemm_bytes = launches * (wbytes + act)
+    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    if gemm_flop * launches / gemm_bytes >= ridge:
+        ach = gemm_flop * launches / (gemm_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"], "unit": "TFLOP/s"}
+    else:
+        ach = gemm_bytes / (gemm_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["traffic_source"] = "no ncu summary for the training step"
+    roof["kernel"] = ("tcgen05 grouped GEMMs: tc_grouped_gemm_kernel (forward Linear 1, 2 and "
+                      "the recomputed A1) and tc_bwd_gemm_kernel (two dgrads, two wgrads)")
+    roof["peak_source"] = pk["source"] + " (burst)"
+    roof["per_launch"] = {n: {"ms": ms, "tflops": gemm_flop / (ms * 1e-3) / 1e12}
+                          for n, ms in gemm_names}
+    train_flop = 7.0 * gemm_flop + 3 * 2.0 * T * wl.d_model * wl.n_experts
+    res = {
+        "metric": TRAIN_METRIC, "value": job_tokens_per_s(T, K, world, total_ms),
+        "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "description": wl.description, "T": T,
+                   "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "aux_weight": AUX_WEIGHT,
+                   "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write)",
+                   "launch": "moe_forward + moe_backward captured once as a CUDA graph, "
+                             "replayed; per-kernel times from direct *_profiled calls"},
+        "tflops": train_flop / (total_ms / K * 1e-3) / 1e12,
+        "forward_stage_ms": fmean, "backward_stage_ms": bmean,
+        "roofline": roof,
+        "gpu_launches": (B.forward_launch_count(cfg) + B.backward_launch_count(cfg)) * K,
+        "clocks": clk,
+    }
+    del flops
+    if not args.no_e2e:
+        xh = x.cpu().pin_memory()
+        dyh = dy.cpu().pin_memory()
+        xd, dyd = torch.empty_like(x), torch.empty_like(dy)
+        dxh = torch.empty(grads.dx.shape, dtype=grads.dx.dtype).pin_memory()
+        cur = torch.cuda.current_stream(dev)
+
+        def e2e_step():
+            xd.copy_(xh, non_blocking=True)
+            dyd.copy_(dyh, non_blocking=True)
+            B.forward(cfg, xd, layer.weights, out, layer.workspace, cur)
+            B.backward(cfg, xd, layer.weights, out, layer.workspace, dyd, AUX_WEIGHT, grads,
+                       bws, cur)
+            dxh.copy_(grads.dx, non_blocking=True)
+            cur.synchronize()
+
+        for _ in range(3):
+            e2e_step()
+        t0 = time.perf_counter()
+        for _ in range(K):
+            e2e_step()
+        dt = time.perf_counter() - t0
+        res["e2e"] = {"value": T * K / dt, "unit": "tokens/s",
+                      "h2d_bytes_per_step": 2 * T * wl.d_model * es,
+                      "d2h_bytes_per_step": T * wl.d_model * es,
+                      "api": "moe_forward + moe_backward between pinned host copies of x, dy "
+                             "and dx on one stream (synchronous)"}
+    return res
+
+
 def measure_e2e(args, layer, wl, dev):
     """Same metric through moe_forward_host: tokens copied in from pinned host
     memory and the results copied back inside the timed call."""
@@ -534,13 +744,13 @@ def measure_e2e_ec(args, calls, wl, dev):
             "api": "moe_ec_forward between pinned host copies on its stream (synchronous)"}
 
 
-def cpu_baseline(wl):
+def cpu_baseline(wl, train=False):
     import torch
 
     from sparse_mixture_experts_68_b300 import synth
     tensors = synth.make_layer(wl, device="cpu")
-    S = cpu_sample_tokens(wl)
-    step = oracle_step(tensors, wl, S)
+    S = max(16, cpu_sample_tokens(wl) // 4) if train else cpu_sample_tokens(wl)
+    step = oracle_train_step(tensors, wl, S) if train else oracle_step(tensors, wl, S)
     t0 = time.perf_counter()
     n = 0
     while True:
@@ -553,7 +763,8 @@ def cpu_baseline(wl):
     return {"value": S * n / dt, "unit": "tokens/s", "cores": oracle_threads(),
             "kind": "oracle",
             "sample": f"{n} pass(es) over the first {S} of {wl.T} tokens, as a layer of "
-                      f"{S} tokens (float64 numpy oracle)"}
+                      f"{S} tokens (float64 numpy oracle"
+                      + (", forward and backward)" if train else ")")}
 
 
 def main():
@@ -573,10 +784,13 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
-    res = run_ours(args, wl, rank, world, local_rank)
+    if args.mode == "train":
+        res = run_train(args, wl, rank, world, local_rank)
+    else:
+        res = run_ours(args, wl, rank, world, local_rank)
     if rank == 0:
         if not args.no_cpu_baseline:
-            res["cpu_baseline"] = cpu_baseline(wl)
+            res["cpu_baseline"] = cpu_baseline(wl, train=args.mode == "train")
         print(json.dumps(res), flush=True)
     if world > 1:
         import torch.distributed as dist

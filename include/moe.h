@@ -315,6 +315,20 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
                         const void* dy, float aux_weight, const moe_grads* grads,
                         void* workspace, size_t workspace_bytes, void* stream);
 
+/* moe_backward with eight caller-owned CUDA events recorded on `stream` at
+ * the step boundaries (kernels not overlapping their neighbours):
+ *   events[0] start                     events[4] after dXp = dA W1
+ *   events[1] after the gate step       events[5] after dW2 = dO^T H
+ *             and the padding zeroing   events[6] after dW1 = dA^T Xp
+ *   events[2] after the recomputed A1   events[7] after the bias sums, the
+ *   events[3] after dA = (dO W2) act'(A1)         router gradients and dx
+ * A NULL entry is skipped. */
+moe_status moe_backward_profiled(const moe_config* cfg, const void* x, const moe_weights* w,
+                                 const moe_outputs* fwd, void* fwd_workspace,
+                                 size_t fwd_workspace_bytes, const void* dy, float aux_weight,
+                                 const moe_grads* grads, void* workspace,
+                                 size_t workspace_bytes, void* const* events, void* stream);
+
 /* ---- expert-choice routing -------------------------------------------------
  *
  * matteuscruz.github.io "What is a Mixture of Experts?", "Load balancing: the

@@ -34,7 +34,7 @@ EXPORTS = [
     "moe_ec_tokens_per_expert", "moe_ec_rows_max", "moe_ec_workspace_size",
     "moe_ec_forward_launch_count", "moe_ec_router", "moe_ec_select", "moe_ec_forward",
     "moe_ec_forward_profiled", "moe_backward", "moe_backward_workspace_size",
-    "moe_backward_launch_count",
+    "moe_backward_launch_count", "moe_backward_profiled",
 ]
 PERMUTE_STATIC_SCRATCH_INTS = 1 << 18
 
@@ -131,6 +131,10 @@ def lib() -> C.CDLL:
         "moe_backward": (C.c_int32, [CP, P, C.POINTER(MoeWeights), C.POINTER(MoeOutputs), P,
                                      C.c_size_t, P, C.c_float, C.POINTER(MoeGrads), P,
                                      C.c_size_t, P]),
+        "moe_backward_profiled": (C.c_int32, [CP, P, C.POINTER(MoeWeights),
+                                              C.POINTER(MoeOutputs), P, C.c_size_t, P,
+                                              C.c_float, C.POINTER(MoeGrads), P, C.c_size_t,
+                                              C.POINTER(C.c_void_p), P]),
         "moe_status_string": (C.c_char_p, [C.c_int32]),
         "moe_version": (C.c_int32, []),
     }
@@ -382,6 +386,20 @@ def backward(cfg: MoeConfig, x, weights: MoeWeights, fwd: Outputs, fwd_workspace
                               float(aux_weight), C.byref(grads.struct()), _ptr(workspace),
                               workspace.numel() * workspace.element_size(), _stream(stream)),
            "moe_backward")
+
+
+def backward_profiled(cfg: MoeConfig, x, weights: MoeWeights, fwd: Outputs, fwd_workspace, dy,
+                      aux_weight: float, grads: Grads, workspace, events, stream=None):
+    """moe_backward recording eight torch.cuda.Event at its step boundaries."""
+    assert len(events) == 8
+    handles = (C.c_void_p * 8)(*[ev.cuda_event if ev is not None else None for ev in events])
+    _check(lib().moe_backward_profiled(C.byref(cfg), _ptr(x), C.byref(weights),
+                                       C.byref(fwd.struct()), _ptr(fwd_workspace),
+                                       fwd_workspace.numel() * fwd_workspace.element_size(),
+                                       _ptr(dy), float(aux_weight), C.byref(grads.struct()),
+                                       _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), handles,
+                                       _stream(stream)), "moe_backward_profiled")
 
 
 class MoeLayer:

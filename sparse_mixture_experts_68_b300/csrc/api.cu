@@ -98,6 +98,10 @@ struct BwdWorkspace {
   float* dz;
   float* dw;
   float* dxr;
+  void* dz_bf;
+  void* dxr_bf;
+  int32_t* rgrp;
+  float* part;
   size_t bytes;
 };
 
@@ -118,6 +122,10 @@ BwdWorkspace bwd_layout(const moe_config& c, void* base) {
   w.dz = static_cast<float*>(take(size_t(c.T * c.n_experts) * 4));
   w.dw = static_cast<float*>(take(size_t(c.T * c.top_k) * 4));
   w.dxr = static_cast<float*>(take(size_t(c.T * c.d_model) * 4));
+  w.dz_bf = take(size_t(c.T * c.n_experts) * 2);
+  w.dxr_bf = take(size_t(round_up(c.T, kGroupAlign) * c.d_model) * 2);
+  w.rgrp = static_cast<int32_t*>(take(16));
+  w.part = static_cast<float*>(take(router_bwd_partial_bytes(c)));
   w.bytes = off;
   return w;
 }
@@ -576,10 +584,11 @@ int32_t moe_backward_launch_count(const moe_config* cfg) {
   return backward_launch_count(*cfg);
 }
 
-moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights* w,
-                        const moe_outputs* fwd, void* fwd_workspace, size_t fwd_workspace_bytes,
-                        const void* dy, float aux_weight, const moe_grads* grads,
-                        void* workspace, size_t workspace_bytes, void* stream) {
+static moe_status backward_impl(const moe_config* cfg, const void* x, const moe_weights* w,
+                                const moe_outputs* fwd, void* fwd_workspace,
+                                size_t fwd_workspace_bytes, const void* dy, float aux_weight,
+                                const moe_grads* grads, void* workspace, size_t workspace_bytes,
+                                void* const* events, void* stream) {
   moe_status st = check_bwd_config(cfg);
   if (st != MOE_OK) return st;
   const moe_config& c = *cfg;
@@ -619,9 +628,35 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
   a.dz = grads->dz ? grads->dz : ws.dz;
   a.dw = grads->dw ? grads->dw : ws.dw;
   a.dxr = ws.dxr;
+  a.dz_bf = ws.dz_bf;
+  a.dxr_bf = ws.dxr_bf;
+  a.rgrp = ws.rgrp;
+  a.part = ws.part;
   a.rows_max = rows_max_of(c);
   a.status = di.status; a.wait_limit_ns = g_wait_limit_ns.load(); a.num_sms = di.num_sms;
-  return cuda_status(launch_backward(c, a, static_cast<cudaStream_t>(stream)));
+  return cuda_status(launch_backward(c, a, events, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights* w,
+                        const moe_outputs* fwd, void* fwd_workspace, size_t fwd_workspace_bytes,
+                        const void* dy, float aux_weight, const moe_grads* grads,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  return backward_impl(cfg, x, w, fwd, fwd_workspace, fwd_workspace_bytes, dy, aux_weight,
+                       grads, workspace, workspace_bytes, nullptr, stream);
+}
+
+moe_status moe_backward_profiled(const moe_config* cfg, const void* x, const moe_weights* w,
+                                 const moe_outputs* fwd, void* fwd_workspace,
+                                 size_t fwd_workspace_bytes, const void* dy, float aux_weight,
+                                 const moe_grads* grads, void* workspace,
+                                 size_t workspace_bytes, void* const* events, void* stream) {
+  if (!events) return MOE_ERR_INVALID_ARG;
+  pdl_enabled() = false;
+  const moe_status st = backward_impl(cfg, x, w, fwd, fwd_workspace, fwd_workspace_bytes, dy,
+                                      aux_weight, grads, workspace, workspace_bytes, events,
+                                      stream);
+  pdl_enabled() = true;
+  return st;
 }
 
 // ---- expert-choice routing --------------------------------------------------------

@@ -38,7 +38,7 @@ struct PadBufs {
   int n;
 };
 
-// One block per group: rows [offsets[g] + live_g, offsets[g + 1]).
+// Blocks (g, y): rows offsets[g] + live_g + y, + gridDim.y, ... below offsets[g + 1].
 __global__ void __launch_bounds__(256)
     zero_pad_rows_kernel(const int32_t* __restrict__ offsets, const int32_t* __restrict__ kept,
                          int n_routed, int shared_rows, PadBufs b) {
@@ -46,13 +46,13 @@ __global__ void __launch_bounds__(256)
   pdl_wait_previous();
   const int g = blockIdx.x;
   const int64_t live = g < n_routed ? kept[g] : shared_rows;
-  const int64_t r0 = offsets[g] + live, r1 = offsets[g + 1];
-  for (int i = 0; i < b.n; ++i) {
-    const int64_t nv = b.width[i] / 8;
-    uint4* base = static_cast<uint4*>(b.buf[i]);
-    for (int64_t j = threadIdx.x; j < (r1 - r0) * nv; j += blockDim.x)
-      base[(r0 + j / nv) * nv + j % nv] = make_uint4(0, 0, 0, 0);
-  }
+  const int64_t r1 = offsets[g + 1];
+  for (int64_t r = offsets[g] + live + blockIdx.y; r < r1; r += gridDim.y)
+    for (int i = 0; i < b.n; ++i) {
+      const int64_t nv = b.width[i] / 8;
+      uint4* row = static_cast<uint4*>(b.buf[i]) + r * nv;
+      for (int64_t j = threadIdx.x; j < nv; j += blockDim.x) row[j] = make_uint4(0, 0, 0, 0);
+    }
 }
 
 // ---- gate step ------------------------------------------------------------------------
@@ -79,11 +79,17 @@ __global__ void __launch_bounds__(kGateWarps * 32)
                     const float* __restrict__ mean_prob, const int32_t* __restrict__ offsets,
                     int T, int64_t d, int N, int k, int renorm, int has_shared, float aux,
                     __nv_bfloat16* __restrict__ dO, float* __restrict__ dz_out,
-                    float* __restrict__ dw_out) {
+                    float* __restrict__ dw_out, __nv_bfloat16* __restrict__ dz_bf,
+                    int32_t* __restrict__ rgrp) {
   extern __shared__ float gsm[];
   pdl_launch_dependents();
   pdl_wait_previous();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (rgrp && blockIdx.x == 0 && threadIdx.x == 0) {
+    // the router's tensor-core GEMMs see one group of T rows
+    const int32_t tp = (T + 127) / 128 * 128;
+    rgrp[0] = 0; rgrp[1] = tp; rgrp[2] = tp; rgrp[3] = T;
+  }
   const int t = blockIdx.x * kGateWarps + warp;
   if (t >= T) return;
   float* P = gsm + size_t(warp) * (3 * N + k);
@@ -164,7 +170,11 @@ __global__ void __launch_bounds__(kGateWarps * 32)
   for (int e = lane; e < N; e += 32) pd += P[e] * DP[e];
   pd = warp_sum(pd);
   float* dzr = dz_out + int64_t(t) * N;
-  for (int e = lane; e < N; e += 32) dzr[e] = DZ[e] + P[e] * (DP[e] - pd);
+  for (int e = lane; e < N; e += 32) {
+    const float v = DZ[e] + P[e] * (DP[e] - pd);
+    dzr[e] = v;
+    if (dz_bf) dz_bf[int64_t(t) * N + e] = __float2bfloat16_rn(v);
+  }
 }
 
 // ---- column sums of groups (bias gradients) -----------------------------------------------
@@ -212,17 +222,27 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// db_g[e] = sum_t dz[t, e] (fp32 in, bf16 out), one thread per expert.
+// db_g[e] = sum_t dz[t, e] (fp32 in, bf16 out): block b takes experts
+// 32 b .. 32 b + 31 (one per lane), its eight warps every eighth token, and
+// the warps combine in order.
 __global__ void __launch_bounds__(256)
     router_bias_grad_kernel(const float* __restrict__ dz, int T, int N,
                             __nv_bfloat16* __restrict__ db_g) {
+  __shared__ float part[8][32];
   pdl_launch_dependents();
   pdl_wait_previous();
-  const int e = blockIdx.x * blockDim.x + threadIdx.x;
-  if (e >= N) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * 32 + lane;
   float s = 0.f;
-  for (int t = 0; t < T; ++t) s += dz[int64_t(t) * N + e];
-  db_g[e] = __float2bfloat16_rn(s);
+  if (e < N)
+    for (int t = warp; t < T; t += 8) s += dz[int64_t(t) * N + e];
+  part[warp][lane] = s;
+  __syncthreads();
+  if (warp == 0 && e < N) {
+    float v = 0.f;
+    for (int w = 0; w < 8; ++w) v += part[w][lane];
+    db_g[e] = __float2bfloat16_rn(v);
+  }
 }
 
 // ---- router GEMMs on CUDA cores ---------------------------------------------------------------
@@ -230,31 +250,38 @@ __global__ void __launch_bounds__(256)
 // C[m, n] = sum_k A(m, k) B[k, n] with A fp32 addressed by strides (am, ak)
 // and B bf16 row-major [K, ldb]; C fp32 or bf16 row-major [M, ldc].
 constexpr int kRg = 64, kRk = 16;
+constexpr int kRouterMaxSplits = 32;
 
+// blockIdx.z splits K into chunks of kc; split z writes its partial sums to
+// C + z * M * ldc (fp32), summed afterwards by splitk_reduce_kernel.
 template <typename TOut>
 __global__ void __launch_bounds__(256)
     router_grad_gemm_kernel(const float* __restrict__ A, int64_t am, int64_t ak,
                             const __nv_bfloat16* __restrict__ B, int64_t ldb, int64_t M,
-                            int64_t Nn, int64_t K, TOut* __restrict__ C, int64_t ldc) {
+                            int64_t Nn, int64_t K, int64_t kc, TOut* __restrict__ C,
+                            int64_t ldc) {
   __shared__ float As[kRk][kRg + 4];
   __shared__ float Bs[kRk][kRg + 4];
   pdl_launch_dependents();
   pdl_wait_previous();
   const int64_t m0 = int64_t(blockIdx.y) * kRg, n0 = int64_t(blockIdx.x) * kRg;
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  const int64_t kb = int64_t(blockIdx.z) * kc;
+  const int64_t ke = kb + kc < K ? kb + kc : K;
+  C += int64_t(blockIdx.z) * M * ldc;
   float acc[4][4] = {};
-  for (int64_t k0 = 0; k0 < K; k0 += kRk) {
+  for (int64_t k0 = kb; k0 < ke; k0 += kRk) {
     // A tile 64 x 16: along m when A is m-contiguous, else along k
     for (int i = tid; i < kRg * kRk; i += 256) {
       int mm, kk;
       if (am == 1) { mm = i % kRg; kk = i / kRg; } else { kk = i % kRk; mm = i / kRk; }
       const int64_t gm = m0 + mm, gk = k0 + kk;
-      As[kk][mm] = (gm < M && gk < K) ? A[gm * am + gk * ak] : 0.f;
+      As[kk][mm] = (gm < M && gk < ke) ? A[gm * am + gk * ak] : 0.f;
     }
     for (int i = tid; i < kRg * kRk; i += 256) {
       const int nn = i % kRg, kk = i / kRg;
       const int64_t gn = n0 + nn, gk = k0 + kk;
-      Bs[kk][nn] = (gn < Nn && gk < K) ? __bfloat162float(B[gk * ldb + gn]) : 0.f;
+      Bs[kk][nn] = (gn < Nn && gk < ke) ? __bfloat162float(B[gk * ldb + gn]) : 0.f;
     }
     __syncthreads();
 #pragma unroll
@@ -283,14 +310,30 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// out[i] = sum over the S splits of part[z * n + i], in split order.
+__global__ void __launch_bounds__(256)
+    splitk_reduce_kernel(const float* __restrict__ part, int S, int64_t n,
+                         __nv_bfloat16* __restrict__ out) {
+  pdl_launch_dependents();
+  pdl_wait_previous();
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    float v = 0.f;
+    for (int z = 0; z < S; ++z) v += part[int64_t(z) * n + i];
+    out[i] = __float2bfloat16_rn(v);
+  }
+}
+
 // ---- dx -----------------------------------------------------------------------------------------
 
 constexpr int kDxWarps = 8;
 
-// dx[t] = sum over t's kept rows of dXp (slot order) + the shared row + dxr[t]
+// dx[t] = dxr[t] (the router's part, fp32 or bf16) + sum over t's kept rows
+// of dXp (slot order) + the shared row
+template <typename TR>
 __global__ void __launch_bounds__(kDxWarps * 32)
     bwd_dx_kernel(const __nv_bfloat16* __restrict__ dXp, const int32_t* __restrict__ token_row,
-                  const int32_t* __restrict__ offsets, const float* __restrict__ dxr, int T,
+                  const int32_t* __restrict__ offsets, const TR* __restrict__ dxr, int T,
                   int k, int N, int has_shared, int64_t d, __nv_bfloat16* __restrict__ dx) {
   pdl_launch_dependents();
   pdl_wait_previous();
@@ -300,10 +343,21 @@ __global__ void __launch_bounds__(kDxWarps * 32)
   const int64_t nv = d / 8;
   for (int64_t c = lane; c < nv; c += 32) {
     float acc[8];
-    const float4* xr = reinterpret_cast<const float4*>(dxr + t * d) + 2 * c;
-    const float4 r0 = xr[0], r1 = xr[1];
-    acc[0] = r0.x; acc[1] = r0.y; acc[2] = r0.z; acc[3] = r0.w;
-    acc[4] = r1.x; acc[5] = r1.y; acc[6] = r1.z; acc[7] = r1.w;
+    if constexpr (sizeof(TR) == 4) {
+      const float4* xr = reinterpret_cast<const float4*>(dxr + t * d) + 2 * c;
+      const float4 r0 = xr[0], r1 = xr[1];
+      acc[0] = r0.x; acc[1] = r0.y; acc[2] = r0.z; acc[3] = r0.w;
+      acc[4] = r1.x; acc[5] = r1.y; acc[6] = r1.z; acc[7] = r1.w;
+    } else {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(dxr + t * d) + c);
+      const __nv_bfloat162* v2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(v2[i]);
+        acc[2 * i] = f.x;
+        acc[2 * i + 1] = f.y;
+      }
+    }
     for (int j = 0; j <= k; ++j) {
       int64_t r;
       if (j < k) r = token_row[t * k + j];
@@ -333,7 +387,17 @@ cudaError_t launch_router_grad_gemm(const float* A, int64_t am, int64_t ak,
   if (M == 0 || Nn == 0) return cudaSuccess;
   dim3 grid(unsigned((Nn + kRg - 1) / kRg), unsigned((M + kRg - 1) / kRg));
   return launch_pdl(router_grad_gemm_kernel<TOut>, grid, dim3(256), 0, s, A, am, ak, B, ldb, M,
-                    Nn, K, C, ldc);
+                    Nn, K, K, C, ldc);
+}
+
+// Splits of K for dW_g = dz^T x on CUDA cores: enough blocks for two waves.
+int router_splits(const moe_config& c) {
+  const int64_t tiles = ((c.d_model + kRg - 1) / kRg) * ((c.n_experts + kRg - 1) / kRg);
+  int64_t S = (2 * 148 + tiles - 1) / tiles;
+  const int64_t by_k = (c.T + 255) / 256;
+  if (S > by_k) S = by_k;
+  if (S > kRouterMaxSplits) S = kRouterMaxSplits;
+  return int(S < 1 ? 1 : S);
 }
 
 // n bf16 zeros: 16-byte words, then the tail element by element.
@@ -369,14 +433,32 @@ cudaError_t zero_param_grads(const moe_config& c, const moe_grads* g, cudaStream
 
 }  // namespace
 
-int backward_launch_count(const moe_config& c) {
-  if (c.T == 0) return c.d_ff_shared > 0 ? 10 : 6;    // zero parameter gradients
-  // gate, padding, A1, dA, dXp, dW2, dW1, db2, db1, dx_router, dW_g, db_g, dx
-  return 13;
+bool router_bwd_on_tensor_cores(const moe_config& c) { return c.n_experts % 64 == 0; }
+
+size_t router_bwd_partial_bytes(const moe_config& c) {
+  return router_bwd_on_tensor_cores(c)
+             ? 0
+             : size_t(router_splits(c)) * size_t(c.n_experts * c.d_model) * sizeof(float);
 }
 
-cudaError_t launch_backward(const moe_config& c, const BackwardArgs& a, cudaStream_t s) {
-  if (c.T == 0) return zero_param_grads(c, a.g, s);
+int backward_launch_count(const moe_config& c) {
+  if (c.T == 0) return c.d_ff_shared > 0 ? 10 : 6;    // zero parameter gradients
+  // gate, padding, A1, dA, dXp, dW2, dW1, db2, db1, dx_router, dW_g (+ split-K
+  // reduce on CUDA cores), db_g, dx
+  return router_bwd_on_tensor_cores(c) ? 13 : 14;
+}
+
+cudaError_t launch_backward(const moe_config& c, const BackwardArgs& a, void* const* events,
+                            cudaStream_t s) {
+  void* const none[8] = {};
+  void* const* ev = events ? events : none;
+  cudaError_t er = record_event(ev[0], s);
+  if (er != cudaSuccess) return er;
+  if (c.T == 0) {
+    er = zero_param_grads(c, a.g, s);
+    for (int i = 1; i < 8 && er == cudaSuccess; ++i) er = record_event(ev[i], s);
+    return er;
+  }
   const int N = int(c.n_experts), k = int(c.top_k), T = int(c.T);
   const int64_t d = c.d_model, f = c.d_ff;
   const int hs = c.d_ff_shared > 0 ? 1 : 0;
@@ -396,7 +478,9 @@ cudaError_t launch_backward(const moe_config& c, const BackwardArgs& a, cudaStre
         dim3(kGateWarps * 32), smem, s, static_cast<const __nv_bfloat16*>(a.dy),
         static_cast<const __nv_bfloat16*>(a.Yp), a.token_row, a.topk_idx, a.topk_w, a.logits,
         a.mean_prob, a.offsets, T, d, N, k, c.renormalize ? 1 : 0, hs, a.aux_weight,
-        static_cast<__nv_bfloat16*>(a.dO), a.dz, a.dw);
+        static_cast<__nv_bfloat16*>(a.dO), a.dz, a.dw,
+        router_bwd_on_tensor_cores(c) ? static_cast<__nv_bfloat16*>(a.dz_bf) : nullptr,
+        router_bwd_on_tensor_cores(c) ? a.rgrp : nullptr);
     if (e != cudaSuccess) return e;
   }
   // padding rows of dO, H and Xp -> 0 (the wgrads run K over whole 64-row blocks)
@@ -406,10 +490,12 @@ cudaError_t launch_backward(const moe_config& c, const BackwardArgs& a, cudaStre
     pb.buf[1] = a.H; pb.width[1] = f;
     pb.buf[2] = a.Xp; pb.width[2] = d;
     pb.n = 3;
-    const cudaError_t e = launch_pdl(zero_pad_rows_kernel, dim3(unsigned(groups)), dim3(256), 0,
-                                     s, a.offsets, a.kept, N, hs ? T : 0, pb);
+    const cudaError_t e = launch_pdl(zero_pad_rows_kernel, dim3(unsigned(groups), 16),
+                                     dim3(256), 0, s, a.offsets, a.kept, N, hs ? T : 0, pb);
     if (e != cudaSuccess) return e;
   }
+  er = record_event(ev[1], s);
+  if (er != cudaSuccess) return er;
   GroupedFfnArgs ga{};
   ga.offsets = a.offsets; ga.kept = a.kept; ga.w = w; ga.rows_max = a.rows_max;
   ga.status = a.status; ga.wait_limit_ns = a.wait_limit_ns; ga.num_sms = a.num_sms;
@@ -419,16 +505,21 @@ cudaError_t launch_backward(const moe_config& c, const BackwardArgs& a, cudaStre
   cudaError_t e;
   // A1 = Xp W1^T + b1 (the pre-activation, recomputed)
   e = launch_grouped_linear_bf16(c, ga, a.Xp, w->W1, w->W1s, w->b1, w->b1s, a.A1, d, f, s);
+  if (e == cudaSuccess) e = record_event(ev[2], s);
   if (e != cudaSuccess) return e;
   // dA = (dO . W2) act'(A1);  dXp = dA . W1
   e = launch_bwd_dgrad(c, bg, a.dO, w->W2, w->W2s, d, f, c.act, a.A1, a.dA, s);
+  if (e == cudaSuccess) e = record_event(ev[3], s);
   if (e != cudaSuccess) return e;
   e = launch_bwd_dgrad(c, bg, a.dA, w->W1, w->W1s, f, d, -1, nullptr, a.dXp, s);
+  if (e == cudaSuccess) e = record_event(ev[4], s);
   if (e != cudaSuccess) return e;
   // dW2 = dO^T H [d, f];  dW1 = dA^T Xp [f, d]
   e = launch_bwd_wgrad(c, bg, a.dO, d, a.H, f, a.g->dW2, a.g->dW2s, s);
+  if (e == cudaSuccess) e = record_event(ev[5], s);
   if (e != cudaSuccess) return e;
   e = launch_bwd_wgrad(c, bg, a.dA, f, a.Xp, d, a.g->dW1, a.g->dW1s, s);
+  if (e == cudaSuccess) e = record_event(ev[6], s);
   if (e != cudaSuccess) return e;
   // db2, db1
   e = launch_pdl(group_colsum_kernel, dim3(unsigned(groups), unsigned((d + 255) / 256)),
@@ -441,23 +532,57 @@ cudaError_t launch_backward(const moe_config& c, const BackwardArgs& a, cudaStre
                  a.kept, N, hs ? T : 0, static_cast<__nv_bfloat16*>(a.g->db1),
                  static_cast<__nv_bfloat16*>(a.g->db1s));
   if (e != cudaSuccess) return e;
-  // router: dxr = dz W_g [T, d] fp32; dW_g = dz^T x [N, d]; db_g = sum_t dz
-  e = launch_router_grad_gemm<float>(a.dz, N, 1, static_cast<const __nv_bfloat16*>(w->W_g), d,
-                                     T, d, N, a.dxr, d, s);
-  if (e != cudaSuccess) return e;
-  e = launch_router_grad_gemm<__nv_bfloat16>(a.dz, 1, N, static_cast<const __nv_bfloat16*>(a.x),
-                                             d, N, d, T,
-                                             static_cast<__nv_bfloat16*>(a.g->dW_g), d, s);
-  if (e != cudaSuccess) return e;
-  e = launch_pdl(router_bias_grad_kernel, dim3(unsigned((N + 255) / 256)), dim3(256), 0, s,
+  // router: dx_router = dz W_g [T, d]; dW_g = dz^T x [N, d]; db_g = sum_t dz
+  const bool tc_router = router_bwd_on_tensor_cores(c);
+  if (tc_router) {
+    // the dgrad / wgrad kernels on one group of T rows, dz rounded to bf16
+    moe_config rc = c;
+    rc.n_experts = 1;
+    rc.d_ff_shared = 0;
+    BwdGemmArgs rg = bg;
+    rg.offsets = a.rgrp;
+    rg.kept = a.rgrp + 3;
+    rg.rows_max = T;
+    e = launch_bwd_dgrad(rc, rg, a.dz_bf, w->W_g, nullptr, N, d, -1, nullptr, a.dxr_bf, s);
+    if (e != cudaSuccess) return e;
+    e = launch_bwd_wgrad(rc, rg, a.dz_bf, N, a.x, d, a.g->dW_g, nullptr, s);
+    if (e != cudaSuccess) return e;
+  } else {
+    e = launch_router_grad_gemm<float>(a.dz, N, 1, static_cast<const __nv_bfloat16*>(w->W_g),
+                                       d, T, d, N, a.dxr, d, s);
+    if (e != cudaSuccess) return e;
+    const int S = router_splits(c);
+    const int64_t kc = ((T + S - 1) / S + kRk - 1) / kRk * kRk;
+    dim3 grid(unsigned((d + kRg - 1) / kRg), unsigned((N + kRg - 1) / kRg), unsigned(S));
+    e = launch_pdl(router_grad_gemm_kernel<float>, grid, dim3(256), 0, s,
+                   static_cast<const float*>(a.dz), int64_t(1), int64_t(N),
+                   static_cast<const __nv_bfloat16*>(a.x), d, int64_t(N), d, int64_t(T), kc,
+                   a.part, d);
+    if (e != cudaSuccess) return e;
+    const int64_t n = int64_t(N) * d;
+    const int64_t blocks = (n + 255) / 256;
+    e = launch_pdl(splitk_reduce_kernel, dim3(unsigned(blocks < 1184 ? blocks : 1184)),
+                   dim3(256), 0, s, static_cast<const float*>(a.part), S, n,
+                   static_cast<__nv_bfloat16*>(a.g->dW_g));
+    if (e != cudaSuccess) return e;
+  }
+  e = launch_pdl(router_bias_grad_kernel, dim3(unsigned((N + 31) / 32)), dim3(256), 0, s,
                  static_cast<const float*>(a.dz), T, N,
                  static_cast<__nv_bfloat16*>(a.g->db_g));
   if (e != cudaSuccess) return e;
   // dx
-  return launch_pdl(bwd_dx_kernel, dim3(unsigned((T + kDxWarps - 1) / kDxWarps)),
-                    dim3(kDxWarps * 32), 0, s, static_cast<const __nv_bfloat16*>(a.dXp),
-                    a.token_row, a.offsets, static_cast<const float*>(a.dxr), T, k, N, hs, d,
-                    static_cast<__nv_bfloat16*>(a.g->dx));
+  if (tc_router)
+    e = launch_pdl(bwd_dx_kernel<__nv_bfloat16>, dim3(unsigned((T + kDxWarps - 1) / kDxWarps)),
+                   dim3(kDxWarps * 32), 0, s, static_cast<const __nv_bfloat16*>(a.dXp),
+                   a.token_row, a.offsets, static_cast<const __nv_bfloat16*>(a.dxr_bf), T, k, N,
+                   hs, d, static_cast<__nv_bfloat16*>(a.g->dx));
+  else
+    e = launch_pdl(bwd_dx_kernel<float>, dim3(unsigned((T + kDxWarps - 1) / kDxWarps)),
+                   dim3(kDxWarps * 32), 0, s, static_cast<const __nv_bfloat16*>(a.dXp),
+                   a.token_row, a.offsets, static_cast<const float*>(a.dxr), T, k, N, hs, d,
+                   static_cast<__nv_bfloat16*>(a.g->dx));
+  if (e != cudaSuccess) return e;
+  return record_event(ev[7], s);
 }
 
 }  // namespace moe

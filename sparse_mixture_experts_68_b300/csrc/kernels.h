@@ -206,14 +206,23 @@ struct BackwardArgs {
   void* dXp;                // [rows_max, d]
   float* dz;                // [T, N]
   float* dw;                // [T, k]
-  float* dxr;               // [T, d]
+  float* dxr;               // [T, d] fp32 (router part of dx on CUDA cores)
+  void* dz_bf;              // [T, N] bf16 (router GEMMs on tensor cores)
+  void* dxr_bf;             // [round_up(T, 128), d] bf16 (router part of dx on tensor cores)
+  int32_t* rgrp;            // 4 ints: the router GEMMs' one-group offsets and row count
+  float* part;              // split-K partial sums of dW_g on CUDA cores
   int64_t rows_max;
   int32_t* status;
   uint64_t wait_limit_ns;
   int num_sms;
 };
-cudaError_t launch_backward(const moe_config& c, const BackwardArgs& a, cudaStream_t s);
+// events: NULL or 8 cudaEvent_t recorded at the step boundaries (see moe_backward_profiled)
+cudaError_t launch_backward(const moe_config& c, const BackwardArgs& a, void* const* events,
+                            cudaStream_t s);
 int backward_launch_count(const moe_config& c);
+// router gradients on the tensor cores (N % 64 == 0), else CUDA cores with split K
+bool router_bwd_on_tensor_cores(const moe_config& c);
+size_t router_bwd_partial_bytes(const moe_config& c);
 
 // the first Linear without its activation: out = A W^T + b per group (bf16)
 cudaError_t launch_grouped_linear_bf16(const moe_config& c, const GroupedFfnArgs& g,
