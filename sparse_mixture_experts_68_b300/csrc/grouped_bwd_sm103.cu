@@ -39,7 +39,13 @@ constexpr int kMaxGroups = 1025;
 enum { MODE_DGRAD = 0, MODE_WGRAD = 1 };
 enum { BEPI_STORE = 0, BEPI_DGELU = 1, BEPI_DRELU = 2 };
 
-template <int BN, int STAGES>
+// Output staging (WGRAD): each epilogue warp's 32 rows x 32 columns of bf16,
+// rows padded to 80 bytes so that both the row-wise writes and the
+// transposed reads of shared memory stay (nearly) free of bank conflicts.
+constexpr int kStagePitch = 80;
+constexpr int kStageWarpBytes = 32 * kStagePitch;
+
+template <int BN, int STAGES, int STAGE_BYTES = 0>
 struct BwdLayout {
   static constexpr int kABytes = BM * BK * 2;
   static constexpr int kBBytes = BN * BK * 2;
@@ -53,7 +59,8 @@ struct BwdLayout {
   static constexpr int kTileStart = (kAbort + 4 + 15) / 16 * 16;     // [kMaxGroups + 1]
   static constexpr int kGroupOff = kTileStart + (kMaxGroups + 1) * 4;  // [kMaxGroups]
   static constexpr int kGroupLive = kGroupOff + kMaxGroups * 4;        // [kMaxGroups]
-  static constexpr int kBytes = kGroupLive + kMaxGroups * 4;
+  static constexpr int kStage = (kGroupLive + kMaxGroups * 4 + 127) / 128 * 128;
+  static constexpr int kBytes = kStage + STAGE_BYTES;
   static constexpr int kAlloc = kBytes + 1024;
   static_assert(kAlloc <= 227 * 1024, "shared memory budget");
 };
@@ -132,7 +139,10 @@ __global__ void __launch_bounds__(18 * 32, 1)
                        const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmBs, const BwdParams p) {
   constexpr int kEpiWarps = 16;
-  using L = BwdLayout<BN, STAGES>;
+  // the wgrads write whole weight-sized outputs: their stores go through
+  // shared memory so that each warp store covers 8 rows x 64 contiguous bytes
+  constexpr bool kStaged = MODE == MODE_WGRAD;
+  using L = BwdLayout<BN, STAGES, kStaged ? kEpiWarps * kStageWarpBytes : 0>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -333,6 +343,37 @@ __global__ void __launch_bounds__(18 * 32, 1)
       for (int c = part * kCols; c < (part + 1) * kCols; c += CW) {
         uint32_t r[CW];
         tmem_ld_cols<CW>(tmem_base + (uint32_t(q * 32) << 16) + acc * BN + c, r);
+        if (kStaged) {
+          // this lane's row into shared memory, then 8 / 16 rows per warp store
+          uint8_t* stg = smem + L::kStage + (warp - 2) * kStageWarpBytes;
+#pragma unroll
+          for (int v = 0; v < CW / 8; ++v) {
+            uint4 o;
+            __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              o2[i] = zero ? __floats2bfloat162_rn(0.f, 0.f)
+                           : __floats2bfloat162_rn(__uint_as_float(r[8 * v + 2 * i]),
+                                                   __uint_as_float(r[8 * v + 2 * i + 1]));
+            *reinterpret_cast<uint4*>(stg + lane * kStagePitch + v * 16) = o;
+          }
+          __syncwarp();
+          constexpr int kChunks = CW / 8;          // 16-byte chunks per row
+          constexpr int kRowsPerPass = 32 / kChunks;
+          const int64_t col = int64_t(tc.n) * BN + c + (lane % kChunks) * 8;
+          __nv_bfloat16* base = dst_row - int64_t(lane) * p.Nd;   // row 0 of this warp
+          const int row0 = tc.m * BM + q * 32;
+#pragma unroll
+          for (int pass = 0; pass < kChunks; ++pass) {
+            const int rr = pass * kRowsPerPass + lane / kChunks;
+            const uint4 v = *reinterpret_cast<const uint4*>(stg + rr * kStagePitch +
+                                                             (lane % kChunks) * 16);
+            if (row0 + rr < p.Md)
+              *reinterpret_cast<uint4*>(base + int64_t(rr) * p.Nd + col) = v;
+          }
+          __syncwarp();
+          continue;
+        }
         if (store) {
           const int64_t col = int64_t(tc.n) * BN + c;
           uint4* dst = reinterpret_cast<uint4*>(dst_row + col);
@@ -406,8 +447,10 @@ bool bwd_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, u
 template <int BN, int MODE, int EPI>
 cudaError_t launch_bwd(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& Bs,
                        const BwdParams& p, int64_t max_tiles, int num_sms, cudaStream_t s) {
-  constexpr int STAGES = 4;
-  constexpr int smem = BwdLayout<BN, STAGES>::kAlloc;
+  // the wgrads trade a ring stage for their store staging
+  constexpr int STAGES = MODE == MODE_WGRAD ? 3 : 4;
+  constexpr int smem =
+      BwdLayout<BN, STAGES, MODE == MODE_WGRAD ? 16 * kStageWarpBytes : 0>::kAlloc;
   auto kern = tc_bwd_gemm_kernel<BN, STAGES, MODE, EPI>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
