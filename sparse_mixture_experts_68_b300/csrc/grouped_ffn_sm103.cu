@@ -46,15 +46,19 @@ enum { EPI_BIAS = 0, EPI_BIAS_GELU = 1, EPI_BIAS_RELU = 2, EPI_BIAS_F32 = 3 };
 
 // A kernel variant: output tile width BN, depth of the shared-memory ring,
 // number of epilogue warps (a multiple of 4: one set per TMEM lane quarter).
-template <int BN_, int STAGES_, int EPI_WARPS_>
+// STAGED: the epilogue's bf16 stores go through shared memory (16-column
+// pieces, warp_staged_store).
+template <int BN_, int STAGES_, int EPI_WARPS_, bool STAGED_ = true>
 struct TileCfg {
   static constexpr int BN = BN_;
   static constexpr int STAGES = STAGES_;
   static constexpr int EPI_WARPS = EPI_WARPS_;
   static constexpr int THREADS = (2 + EPI_WARPS) * 32;
+  static constexpr bool STAGED = STAGED_;
+  static constexpr int STAGE_BYTES = STAGED_ ? EPI_WARPS_ * staged_warp_bytes<16>() : 0;
 };
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int STAGE_BYTES = 0>
 struct Layout {
   static constexpr int kABytes = BM * BK * 2;
   static constexpr int kBBytes = BN * BK * 2;
@@ -67,7 +71,8 @@ struct Layout {
   static constexpr int kAbort = kTmemSlot + 4;
   static constexpr int kTileStart = (kAbort + 4 + 15) / 16 * 16;   // int32 [kMaxGroups + 1]
   static constexpr int kGroupOff = kTileStart + (kMaxGroups + 1) * 4;  // int32 [kMaxGroups]
-  static constexpr int kBytes = kGroupOff + kMaxGroups * 4;
+  static constexpr int kStage = (kGroupOff + kMaxGroups * 4 + 127) / 128 * 128;
+  static constexpr int kBytes = kStage + STAGE_BYTES;
   static constexpr int kAlloc = kBytes + 1024;              // room to align the base to 1 KB
   static_assert(kAlloc <= 227 * 1024, "shared memory budget");
 };
@@ -132,6 +137,29 @@ __device__ __forceinline__ void epilogue_store(const uint32_t (&r)[CW],
   }
 }
 
+// The bf16 epilogues as 16-byte words: + bias, activation, bf16 of CW columns.
+template <int EPI, int CW>
+__device__ __forceinline__ void epilogue_words(const uint32_t* r,
+                                               const __nv_bfloat16* __restrict__ bias,
+                                               uint4 (&w)[CW / 8]) {
+  const uint4* bsrc = reinterpret_cast<const uint4*>(bias);
+#pragma unroll
+  for (int v = 0; v < CW / 8; ++v) {
+    const uint4 bv = __ldg(bsrc + v);
+    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&bv);
+    __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(&w[v]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 bf = __bfloat1622float2(b2[i]);
+      float x0 = __uint_as_float(r[8 * v + 2 * i]) + bf.x;
+      float x1 = __uint_as_float(r[8 * v + 2 * i + 1]) + bf.y;
+      if (EPI == EPI_BIAS_GELU) { x0 = gelu_erf(x0); x1 = gelu_erf(x1); }
+      if (EPI == EPI_BIAS_RELU) { x0 = fmaxf(x0, 0.f); x1 = fmaxf(x1, 0.f); }
+      o2[i] = __floats2bfloat162_rn(x0, x1);
+    }
+  }
+}
+
 // Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major.
 template <int BN>
 __host__ __device__ constexpr uint32_t idesc_bf16_f32() {
@@ -183,7 +211,7 @@ __global__ void __launch_bounds__(CFG::THREADS, MINB)
   constexpr int BN = CFG::BN;
   constexpr int kStages = CFG::STAGES;
   constexpr int kEpiWarps = CFG::EPI_WARPS;
-  using L = Layout<BN, kStages>;
+  using L = Layout<BN, kStages, CFG::STAGE_BYTES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -351,12 +379,24 @@ __global__ void __launch_bounds__(CFG::THREADS, MINB)
       const int64_t out_row = int64_t(grp_off[tc.g]) + row_in_group;
       const __nv_bfloat16* bias = routed ? p.bias + int64_t(tc.g) * p.Nd : p.bias_s;
       constexpr int kOutBytes = EPI == EPI_BIAS_F32 ? 4 : 2;
+      constexpr bool kStaged = CFG::STAGED && EPI != EPI_BIAS_F32;
 #pragma unroll 1
       for (int c = part * kCols; c < (part + 1) * kCols; c += CW) {
         uint32_t r[CW];
         tmem_ld_cols<CW>(tmem_base + (uint32_t(q * 32) << 16) + acc * BN + c, r);
-        if (valid) {
-          const int64_t col = int64_t(tc.n) * BN + c;
+        const int64_t col = int64_t(tc.n) * BN + c;
+        if constexpr (kStaged) {
+          uint8_t* stg = smem + L::kStage + (warp - 2) * staged_warp_bytes<16>();
+          const int row_base = tc.m * BM + q * 32;
+          __nv_bfloat16* out0 = static_cast<__nv_bfloat16*>(p.out) +
+                                (int64_t(grp_off[tc.g]) + row_base) * p.Nd + col;
+#pragma unroll
+          for (int h = 0; h < CW / 16; ++h) {
+            uint4 w[2];
+            epilogue_words<EPI, 16>(r + 16 * h, bias + col + 16 * h, w);
+            warp_staged_store<16>(w, stg, lane, out0 + 16 * h, p.Nd, live - row_base);
+          }
+        } else if (valid) {
           epilogue_store<EPI, CW>(r, bias + col,
                                   static_cast<uint8_t*>(p.out) +
                                       (out_row * p.Nd + col) * kOutBytes);
@@ -392,7 +432,7 @@ __global__ void __launch_bounds__(CFG::THREADS, MINB)
 // are multicast to both CTAs' "empty" and "accumulator full" barriers; both
 // CTAs' epilogue warps arrive on the even CTA's "accumulator empty" barrier.
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int STAGE_BYTES = 0>
 struct Layout2 {
   static constexpr int kABytes = 128 * BK * 2;          // this CTA's 128 rows of A
   static constexpr int kBBytes = (BN / 2) * BK * 2;     // this CTA's half of B
@@ -405,7 +445,8 @@ struct Layout2 {
   static constexpr int kAbort = kTmemSlot + 4;
   static constexpr int kTileStart = (kAbort + 4 + 15) / 16 * 16;
   static constexpr int kGroupOff = kTileStart + (kMaxGroups + 1) * 4;
-  static constexpr int kBytes = kGroupOff + kMaxGroups * 4;
+  static constexpr int kStage = (kGroupOff + kMaxGroups * 4 + 127) / 128 * 128;
+  static constexpr int kBytes = kStage + STAGE_BYTES;
   static constexpr int kAlloc = kBytes + 1024;
   static_assert(kAlloc <= 227 * 1024, "shared memory budget");
 };
@@ -505,7 +546,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CFG::THREADS, 1)
   constexpr int kStages = CFG::STAGES;
   constexpr int kEpiWarps = CFG::EPI_WARPS;
   constexpr int BM2 = 256;
-  using L = Layout2<BN, kStages>;
+  using L = Layout2<BN, kStages, CFG::STAGE_BYTES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -662,12 +703,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CFG::THREADS, 1)
       const int64_t out_row = int64_t(grp_off[tc.g]) + row_in_group;
       const __nv_bfloat16* bias = routed ? p.bias + int64_t(tc.g) * p.Nd : p.bias_s;
       constexpr int kOutBytes = EPI == EPI_BIAS_F32 ? 4 : 2;
+      constexpr bool kStaged = CFG::STAGED && EPI != EPI_BIAS_F32;
 #pragma unroll 1
       for (int c = part * kCols; c < (part + 1) * kCols; c += CW) {
         uint32_t r[CW];
         tmem_ld_cols<CW>(tmem_base + (uint32_t(q * 32) << 16) + acc * BN + c, r);
-        if (valid) {
-          const int64_t col = int64_t(tc.n) * BN + c;
+        const int64_t col = int64_t(tc.n) * BN + c;
+        if constexpr (kStaged) {
+          uint8_t* stg = smem + L::kStage + (warp - 2) * staged_warp_bytes<16>();
+          const int row_base = tc.m * BM2 + int(rank) * 128 + q * 32;
+          __nv_bfloat16* out0 = static_cast<__nv_bfloat16*>(p.out) +
+                                (int64_t(grp_off[tc.g]) + row_base) * p.Nd + col;
+#pragma unroll
+          for (int h = 0; h < CW / 16; ++h) {
+            uint4 w[2];
+            epilogue_words<EPI, 16>(r + 16 * h, bias + col + 16 * h, w);
+            warp_staged_store<16>(w, stg, lane, out0 + 16 * h, p.Nd, live - row_base);
+          }
+        } else if (valid) {
           epilogue_store<EPI, CW>(r, bias + col,
                                   static_cast<uint8_t*>(p.out) +
                                       (out_row * p.Nd + col) * kOutBytes);
@@ -941,7 +994,7 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, 
 template <class CFG, int EPI>
 cudaError_t launch_tc(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& Bs,
                       const TcParams& p, int grid, cudaStream_t s) {
-  constexpr int smem = Layout<CFG::BN, CFG::STAGES>::kAlloc;
+  constexpr int smem = Layout<CFG::BN, CFG::STAGES, CFG::STAGE_BYTES>::kAlloc;
   constexpr int minb = smem <= 110 * 1024 ? 2 : 1;    // two CTAs per SM when they fit
   auto kern = tc_grouped_gemm_kernel<CFG, EPI, minb>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -965,7 +1018,7 @@ enum TileChoice {
 using Cfg256 = TileCfg<256, 4, 16>;        // one CTA per SM, 192 KB ring
 using Cfg128 = TileCfg<128, 4, 16>;
 using Cfg64 = TileCfg<64, 6, 16>;
-using Cfg128x2 = TileCfg<128, 3, 8>;       // two CTAs per SM, 96 KB ring each
+using Cfg128x2 = TileCfg<128, 3, 8, false>;  // two CTAs per SM, 96 KB ring each
 using Cfg256Pair = TileCfg<256, 6, 16>;    // CTA pair, 256 x 256 tiles, 6 x 32 KB ring per CTA
 
 int tile_bn(int choice) {
@@ -982,7 +1035,7 @@ int tile_ctas_per_sm(int choice) { return choice == TILE_128_2CTA ? 2 : 1; }
 template <class CFG, int EPI>
 cudaError_t launch_pair(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& Bs,
                         const TcParams& p, int64_t tiles, int num_sms, cudaStream_t s) {
-  constexpr int smem = Layout2<CFG::BN, CFG::STAGES>::kAlloc;
+  constexpr int smem = Layout2<CFG::BN, CFG::STAGES, CFG::STAGE_BYTES>::kAlloc;
   auto kern = tc2_grouped_gemm_kernel<CFG, EPI>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;

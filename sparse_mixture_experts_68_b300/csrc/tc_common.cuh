@@ -80,6 +80,38 @@ __device__ __forceinline__ void tmem_ld_16cols(uint32_t taddr, uint32_t (&r)[16]
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Output staging of one epilogue warp: 32 rows (one per lane) x SW bf16
+// columns.  Each lane writes its row piece into `stg` (rows padded to SW * 2
+// + 16 bytes, which keeps the accesses nearly free of bank conflicts), then
+// every warp store covers 32 / (SW / 8) whole rows of SW * 2 contiguous bytes
+// (full 32-byte sectors) instead of 32 rows of 16 bytes.  Rows >= rows_valid
+// are not stored.  All 32 lanes must call it.
+template <int SW>
+__device__ __forceinline__ void warp_staged_store(const uint4 (&w)[SW / 8], uint8_t* stg,
+                                                  int lane, __nv_bfloat16* row0_col,
+                                                  int64_t ld, int rows_valid) {
+  constexpr int kPitch = SW * 2 + 16;
+  constexpr int kChunks = SW / 8;
+  constexpr int kRowsPerPass = 32 / kChunks;
+#pragma unroll
+  for (int v = 0; v < kChunks; ++v)
+    *reinterpret_cast<uint4*>(stg + lane * kPitch + v * 16) = w[v];
+  __syncwarp();
+#pragma unroll
+  for (int pass = 0; pass < kChunks; ++pass) {
+    const int rr = pass * kRowsPerPass + lane / kChunks;
+    const int ch = lane % kChunks;
+    const uint4 v = *reinterpret_cast<const uint4*>(stg + rr * kPitch + ch * 16);
+    if (rr < rows_valid) *reinterpret_cast<uint4*>(row0_col + int64_t(rr) * ld + ch * 8) = v;
+  }
+  __syncwarp();
+}
+
+template <int SW>
+__host__ __device__ constexpr int staged_warp_bytes() {
+  return 32 * (SW * 2 + 16);
+}
+
 template <int CW>
 __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[CW]) {
   if constexpr (CW == 32) tmem_ld_32cols(taddr, r);
