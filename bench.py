@@ -68,7 +68,8 @@ def peaks():
 # DRAM traffic of the dominant kernel, from the committed ncu summary
 
 KERNEL_SOURCES = ("sparse_mixture_experts_68_b300/csrc/grouped_ffn_sm103.cu",
-                  "sparse_mixture_experts_68_b300/csrc/common.cuh")
+                  "sparse_mixture_experts_68_b300/csrc/common.cuh",
+                  "sparse_mixture_experts_68_b300/csrc/tc_common.cuh")
 
 
 def profiled_traffic(workload):
