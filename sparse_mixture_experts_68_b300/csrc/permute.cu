@@ -170,8 +170,8 @@ __global__ void __launch_bounds__(kSortWarps * 32)
   const int A = T * k;
   int32_t* cnt = sm;                              // [kSortWarps][N], then base ranks
   int32_t* off = cnt + kSortWarps * N;            // [N] group offsets
-  int32_t* warp_tot = off + N;                    // [32]
-  int16_t* ids = reinterpret_cast<int16_t*>(warp_tot + 32);   // [A]
+  int32_t* warp_tot = off + N;                    // [32], then kept [N], counts [N]
+  int16_t* ids = reinterpret_cast<int16_t*>(warp_tot + 32 + 2 * N);   // [A]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < kSortWarps * N; i += blockDim.x) cnt[i] = 0;
   {
@@ -213,21 +213,29 @@ __global__ void __launch_bounds__(kSortWarps * 32)
     __syncwarp();
   }
   __syncthreads();
-  // per expert: base rank of each warp, totals, capacity, padded size
-  int32_t padded = 0;
-  for (int e = threadIdx.x; e < N; e += blockDim.x) {
-    int32_t run = 0;
-    for (int w = 0; w < kSortWarps; ++w) {
-      const int32_t c = cnt[w * N + e];
-      cnt[w * N + e] = run;
-      run += c;
+  // per expert: base rank of each warp (a warp-wide scan over the 32 warps'
+  // counts, lane = warp index), totals, capacity; warp w takes experts w, w+32, ...
+  for (int e = warp; e < N; e += kSortWarps) {
+    const int32_t c = cnt[lane * N + e];
+    int32_t inc = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t v = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += v;
     }
-    const int32_t kp = (capacity > 0 && int64_t(run) > capacity) ? int32_t(capacity) : run;
-    counts[e] = run;
-    kept[e] = kp;
-    off[e] = kp;                                   // kept for now; offsets below
-    padded = int32_t(round_up(kp, kGroupAlign));   // N <= blockDim: one expert per thread
+    cnt[lane * N + e] = inc - c;
+    const int32_t run = __shfl_sync(0xffffffffu, inc, 31);
+    if (lane == 0) {
+      const int32_t kp = (capacity > 0 && int64_t(run) > capacity) ? int32_t(capacity) : run;
+      counts[e] = run;
+      kept[e] = kp;
+      off[e] = kp;                                 // kept for now; offsets below
+      warp_tot[32 + N + e] = run;                  // counts, for the statistics
+    }
   }
+  __syncthreads();
+  // N <= blockDim: thread e holds expert e's padded size
+  const int32_t padded = threadIdx.x < N ? int32_t(round_up(off[threadIdx.x], kGroupAlign)) : 0;
   // exclusive scan of padded sizes over experts (thread e holds expert e)
   int32_t incl = padded;
 #pragma unroll
@@ -249,13 +257,19 @@ __global__ void __launch_bounds__(kSortWarps * 32)
   __syncthreads();
   const int32_t excl = incl - padded + (warp > 0 ? warp_tot[warp - 1] : 0);
   const int e_me = threadIdx.x;
+  int32_t* kept_s = warp_tot + 32;                 // [N] kept, next to the ids' alignment pad
   if (e_me < N) {
-    const int32_t kp = off[e_me];
+    kept_s[e_me] = off[e_me];
     offsets[e_me] = excl;
-    for (int32_t r = excl + kp; r < excl + padded; ++r) row_token[r] = -1;
   }
   __syncthreads();
   if (e_me < N) off[e_me] = excl;
+  __syncthreads();
+  // padding rows (-1): warp w takes experts w, w+32, ..., its lanes the rows
+  for (int e = warp; e < N; e += kSortWarps) {
+    const int32_t r0 = off[e] + kept_s[e], r1 = off[e] + int32_t(round_up(kept_s[e], kGroupAlign));
+    for (int32_t r = r0 + lane; r < r1; r += 32) row_token[r] = -1;
+  }
   if (e_me == N - 1) {
     offsets[N] = excl + padded;
     offsets[N + 1] = excl + padded + (has_shared ? int32_t(round_up(T, kGroupAlign)) : 0);
@@ -285,14 +299,15 @@ __global__ void __launch_bounds__(kSortWarps * 32)
   if (stats.prob_partials) {
     // the load statistics as well, once counts and kept are in memory
     __syncthreads();
-    block_load_stats(stats.prob_partials, stats.nblk, N, T, counts, kept, stats.mean_prob,
-                     stats.balance, stats.dropped, stats.cv_squared);
+    // counts and kept from shared memory (generic pointers), not read back from global
+    block_load_stats(stats.prob_partials, stats.nblk, N, T, kept_s + N, kept_s,
+                     stats.mean_prob, stats.balance, stats.dropped, stats.cv_squared);
   }
 }
 
 size_t sort_smem_bytes(const moe_config& c) {
   const int64_t A = c.T * c.top_k;
-  return size_t(kSortWarps * c.n_experts + c.n_experts + 32) * 4 + size_t(A) * 2 + 16;
+  return size_t(kSortWarps * c.n_experts + 3 * c.n_experts + 32) * 4 + size_t(A) * 2 + 16;
 }
 
 // Above ~16K assignments the multi-block histogram path is faster.

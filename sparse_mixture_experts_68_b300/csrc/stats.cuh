@@ -40,6 +40,19 @@ __device__ __forceinline__ void stats_kahan_add(float v, float& s, float& comp) 
   s = t;
 }
 
+// var(c) / mean(c)^2 = N (N Q - S^2) / ((N - 1) S^2) from S = sum c, Q = sum c^2:
+// N Q - S^2 exactly in 128-bit integers, one rounding at the end.
+__device__ __forceinline__ float cv_squared_of(int N, long long S, long long Q) {
+  if (N <= 1 || S <= 0) return 0.f;
+  const unsigned __int128 nq = (unsigned __int128)(unsigned long long)N * (unsigned long long)Q;
+  const unsigned __int128 s2 = (unsigned __int128)(unsigned long long)S * (unsigned long long)S;
+  const unsigned __int128 num = nq - s2;                   // >= 0 (Cauchy-Schwarz)
+  const double numd = double((unsigned long long)(num >> 64)) * 18446744073709551616.0 +
+                      double((unsigned long long)num);
+  const double sd = double(S);
+  return float(double(N) * numd / (double(N - 1) * sd * sd));
+}
+
 // Runs on all kStatsThreads threads of a block (blockDim.x == kStatsThreads).
 __device__ __forceinline__ void block_load_stats(const float* __restrict__ prob_partials,
                                                  int nblk, int N, int Ttok,
@@ -57,6 +70,79 @@ __device__ __forceinline__ void block_load_stats(const float* __restrict__ prob_
   const int nchunks = (N + 31) / 32;
   const float invT = Ttok > 0 ? 1.0f / float(Ttok) : 0.f;
   const float tN = float(Ttok) / float(N);        // the per-expert sum of a uniform router
+  if (nchunks == 1) {
+    // N <= 32: warp g sums row group g (every 32nd... rows g*R .. g*R + R-1)
+    // for all experts (lane = expert); warp e then combines expert e's 32
+    // groups and warp 0 the experts, both as shuffle trees of error-free
+    // additions (a fixed order, so the result is reproducible).
+    {
+      const int rows = (nblk + kStatsWarps - 1) / kStatsWarps;
+      const int b0 = warp * rows, b1 = min(nblk, b0 + rows);
+      float s = 0.f, comp = 0.f;
+      if (lane < N) {
+        int b = b0;
+        for (; b + 8 <= b1; b += 8) {
+          float v[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) v[u] = prob_partials[int64_t(b + u) * N + lane];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) stats_kahan_add(v[u], s, comp);
+        }
+        for (; b < b1; ++b) stats_kahan_add(prob_partials[int64_t(b) * N + lane], s, comp);
+      }
+      part[warp][lane] = make_float2(s, -comp);
+    }
+    __syncthreads();
+    if (warp < N) {
+      const int e = warp;
+      const float2 pv = part[lane][e];            // lane = row group
+      float hi = pv.x, lo = pv.y;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ohi = __shfl_xor_sync(0xffffffffu, hi, o);
+        const float olo = __shfl_xor_sync(0xffffffffu, lo, o);
+        float ns, ne;
+        stats_two_sum(hi, ohi, ns, ne);
+        hi = ns;
+        lo = lo + olo + ne;
+      }
+      if (lane == 0) {
+        mean_prob[e] = (hi + lo) * invT;
+        float dhi, dlo;
+        stats_two_sum(hi, -tN, dhi, dlo);
+        const float dev = (dhi + (dlo + lo)) * invT;
+        sq[e] = make_float2(dev * dev, 0.f);
+        const int ce = counts[e];
+        dr[e] = ce - kept[e];
+        cs[e] = ce;
+        cq[e] = (long long)ce * ce;
+      }
+    }
+    __syncthreads();
+    if (warp == 0) {
+      float v = lane < N ? sq[lane].x : 0.f, vc = 0.f;
+      int w = lane < N ? dr[lane] : 0;
+      long long S = lane < N ? cs[lane] : 0, Q = lane < N ? cq[lane] : 0;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+        const float oc = __shfl_xor_sync(0xffffffffu, vc, o);
+        float ns, ne;
+        stats_two_sum(v, ov, ns, ne);
+        v = ns;
+        vc = vc + oc + ne;
+        w += __shfl_xor_sync(0xffffffffu, w, o);
+        S += __shfl_xor_sync(0xffffffffu, S, o);
+        Q += __shfl_xor_sync(0xffffffffu, Q, o);
+      }
+      if (lane == 0) {
+        *balance = (N > 1 && Ttok > 0) ? (v + vc) / float(N - 1) : 0.f;
+        *dropped = w;
+        if (cv_squared) *cv_squared = cv_squared_of(N, S, Q);
+      }
+    }
+    return;
+  }
   float sq_s = 0.f, sq_c = 0.f;
   int my_dr = 0;
   long long my_cs = 0, my_cq = 0;
@@ -137,21 +223,7 @@ __device__ __forceinline__ void block_load_stats(const float* __restrict__ prob_
     }
     *balance = (N > 1 && Ttok > 0) ? (v - vc) / float(N - 1) : 0.f;
     *dropped = w;
-    if (cv_squared) {
-      float r = 0.f;
-      if (N > 1 && S > 0) {
-        const unsigned __int128 nq = (unsigned __int128)(unsigned long long)N *
-                                     (unsigned long long)Q;
-        const unsigned __int128 s2 = (unsigned __int128)(unsigned long long)S *
-                                     (unsigned long long)S;
-        const unsigned __int128 num = nq - s2;            // >= 0 (Cauchy-Schwarz)
-        const double numd = double((unsigned long long)(num >> 64)) * 18446744073709551616.0 +
-                            double((unsigned long long)num);
-        const double sd = double(S);
-        r = float(double(N) * numd / (double(N - 1) * sd * sd));
-      }
-      *cv_squared = r;
-    }
+    if (cv_squared) *cv_squared = cv_squared_of(N, S, Q);
   }
 }
 

@@ -155,3 +155,35 @@ def test_expert_choice_sizes_and_validation(lib):
     o = B.MoeEcOutputs(*([fake] * 7 + [None]))
     assert lib.moe_ec_forward(C.byref(cfg), fake, C.byref(w), C.byref(o), fake, 1024, None) \
         == B.MOE_ERR_WORKSPACE
+
+
+def test_backward_sizes_and_validation(lib):
+    cfg = B.make_config(WORKLOADS["c1_page1_bf16"])
+    assert B.backward_workspace_size(cfg) > B.rows_max(cfg) * (2 * 768 + 2 * 3072) * 2
+    assert B.backward_launch_count(cfg) == 14          # N = 8: router gradients on CUDA cores
+    c4 = B.make_config(WORKLOADS["c4_deepseek_v3"])
+    assert B.backward_launch_count(c4) == 13           # N % 64 == 0: on the tensor cores
+    f32 = B.make_config(WORKLOADS["c0_pr1_fp32"])
+    assert B.backward_workspace_size(f32) == 0          # bf16 layers only
+    assert B.backward_launch_count(f32) == -1
+    t0 = B.make_config(WORKLOADS["c1_page1_bf16"], T=0)
+    assert B.backward_launch_count(t0) == 6             # zero parameter gradients
+    w = B.MoeWeights()
+    o = B.MoeOutputs()
+    g = B.MoeGrads()
+    st = lib.moe_backward(C.byref(f32), None, C.byref(w), C.byref(o), None, 0, None, 0.01,
+                          C.byref(g), None, 0, None)
+    assert st == B.MOE_ERR_UNSUPPORTED
+    st = lib.moe_backward(C.byref(cfg), None, C.byref(w), C.byref(o), None, 0, None, 0.01,
+                          C.byref(g), None, 0, None)
+    assert st == B.MOE_ERR_INVALID_ARG
+    fake = 0x10000
+    w = B.MoeWeights(*([fake] * 6 + [None] * 4))
+    o = B.MoeOutputs(*([fake] * 8 + [None, None]))
+    g = B.MoeGrads(*([fake] * 7 + [None] * 6))
+    st = lib.moe_backward(C.byref(cfg), fake, C.byref(w), C.byref(o), fake, 1 << 40, fake,
+                          0.01, C.byref(g), fake, 1024, None)
+    assert st == B.MOE_ERR_WORKSPACE
+    st = lib.moe_backward(C.byref(cfg), fake, C.byref(w), C.byref(o), fake, 1 << 40, fake,
+                          float("nan"), C.byref(g), fake, 1 << 40, None)
+    assert st == B.MOE_ERR_INVALID_ARG
