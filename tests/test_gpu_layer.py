@@ -66,9 +66,10 @@ SMALL = [
              act=ACT_RELU, dtype=DT_F32, seed=22),
     Workload("f32_simt_router", T=70, d_model=1024, d_ff=64, n_experts=64, top_k=2,
              act=ACT_GELU_ERF, dtype=DT_F32, seed=23),
-    # groups of >= 256 rows: the CTA-pair 256 x 256 tiles, with a shared expert
-    Workload("bf16_pair_shared", T=700, d_model=128, d_ff=256, n_experts=2, top_k=2,
-             act=ACT_GELU_ERF, dtype=DT_BF16, d_ff_shared=256, seed=27),
+    # groups of >= 256 rows and K >= 2048: the CTA-pair 256 x 256 tiles for both
+    # Linears, with a shared expert and ragged groups
+    Workload("bf16_pair_shared", T=700, d_model=2048, d_ff=2048, n_experts=2, top_k=2,
+             act=ACT_GELU_ERF, dtype=DT_BF16, d_ff_shared=2048, seed=27),
     # few tokens per expert: weights as the MMA's 128-row operand (decode)
     Workload("bf16_decode_nb16", T=9, d_model=256, d_ff=384, n_experts=8, top_k=2,
              act=ACT_RELU, dtype=DT_BF16, seed=28),
