@@ -80,13 +80,6 @@ struct BwdParams {
   uint64_t wait_limit_ns;
 };
 
-// MN-major operand, 128-byte swizzle: MN chunks of 64 elements `lbo` bytes
-// apart, 8-row K groups 1024 bytes apart.
-__device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t saddr, uint32_t lbo) {
-  return uint64_t((saddr & 0x3FFFFu) >> 4) | (uint64_t(lbo >> 4) << 16) |
-         (uint64_t(1024 >> 4) << 32) | (uint64_t(1) << 46) | (uint64_t(2) << 61);
-}
-
 // kind::f16, D fp32, A and B bf16; bit 15: A MN-major, bit 16: B MN-major.
 template <int BN, int MODE>
 __host__ __device__ constexpr uint32_t idesc_bwd() {
@@ -476,6 +469,8 @@ int bwd_bn(int64_t Nd) { return Nd % 256 == 0 ? 256 : (Nd % 128 == 0 ? 128 : 64)
 cudaError_t launch_bwd_dgrad(const moe_config& c, const BwdGemmArgs& g, const void* dOut,
                              const void* W, const void* Ws, int64_t K, int64_t Nd, int act,
                              const void* pre, void* out, cudaStream_t s) {
+  if (bwd_dgrad_on_pair(c, K, Nd))
+    return launch_bwd_dgrad_pair(c, g, dOut, W, Ws, K, Nd, act, pre, out, s);
   CUtensorMap mA, mB, mBs;
   const int bn = bwd_bn(Nd);
   if (!bwd_map(&mA, dOut, uint64_t(K), uint64_t(g.rows_max), 0, BM)) return cudaErrorInvalidValue;

@@ -42,7 +42,11 @@ constexpr int kMaxGroups = 1025;        // 1024 routed + 1 shared
 
 // Epilogues: + bias then bf16 (second Linear), + bias, GELU / ReLU then bf16
 // (first Linear), + bias then fp32 (router scores).
-enum { EPI_BIAS = 0, EPI_BIAS_GELU = 1, EPI_BIAS_RELU = 2, EPI_BIAS_F32 = 3 };
+enum { EPI_BIAS = 0, EPI_BIAS_GELU = 1, EPI_BIAS_RELU = 2, EPI_BIAS_F32 = 3,
+       // backward dgrad on the CTA pair (weights as MN-major B): no bias; the
+       // result times the activation's derivative at TcParams::pre, or as is
+       EPI_DGRAD_GELU = 4, EPI_DGRAD_RELU = 5, EPI_DGRAD = 6 };
+constexpr bool epi_is_dgrad(int e) { return e >= EPI_DGRAD_GELU; }
 
 // A kernel variant: output tile width BN, depth of the shared-memory ring,
 // number of epilogue warps (a multiple of 4: one set per TMEM lane quarter).
@@ -81,6 +85,7 @@ struct TcParams {
   const int32_t* offsets;          // [n_groups + 1] first row of each group; nullptr:
                                    // one group of dense_rows rows starting at row 0
   const int32_t* kept;             // [n_routed] live rows of each routed group
+  const __nv_bfloat16* pre;        // dgrad epilogues: the pre-activation [rows, Nd]
   const __nv_bfloat16* bias;       // [n_routed, Nd]
   const __nv_bfloat16* bias_s;     // [Nd] shared expert
   void* out;                       // [rows, Nd], bf16 (fp32 for EPI_BIAS_F32)
@@ -157,6 +162,38 @@ __device__ __forceinline__ void epilogue_words(const uint32_t* r,
       if (EPI == EPI_BIAS_RELU) { x0 = fmaxf(x0, 0.f); x1 = fmaxf(x1, 0.f); }
       o2[i] = __floats2bfloat162_rn(x0, x1);
     }
+  }
+}
+
+// The dgrad epilogues as 16-byte words: bf16(acc * act'(pre)) (or bf16(acc)),
+// zeros for a padding row.
+template <int EPI, int CW>
+__device__ __forceinline__ void dgrad_words(const uint32_t* r, const __nv_bfloat16* pre,
+                                            bool zero, uint4 (&w)[CW / 8]) {
+#pragma unroll
+  for (int v = 0; v < CW / 8; ++v) {
+    if (zero) {
+      w[v] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    float gr[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) gr[i] = 1.f;
+    if (EPI != EPI_DGRAD) {
+      const uint4 pv = __ldg(reinterpret_cast<const uint4*>(pre) + v);
+      const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&pv);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 a = __bfloat1622float2(p2[i]);
+        gr[2 * i] = EPI == EPI_DGRAD_GELU ? gelu_erf_grad(a.x) : (a.x > 0.f ? 1.f : 0.f);
+        gr[2 * i + 1] = EPI == EPI_DGRAD_GELU ? gelu_erf_grad(a.y) : (a.y > 0.f ? 1.f : 0.f);
+      }
+    }
+    __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(&w[v]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      o2[i] = __floats2bfloat162_rn(__uint_as_float(r[8 * v + 2 * i]) * gr[2 * i],
+                                    __uint_as_float(r[8 * v + 2 * i + 1]) * gr[2 * i + 1]);
   }
 }
 
@@ -636,11 +673,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CFG::THREADS, 1)
           const uint32_t fb = peer_addr(smem_u32(&full[stage]), 0);
           mbar_arrive_expect_tx_cluster(fb, L::kStageBytes);
           tma2_load_2d(&tmA, smem_u32(smem + L::kA + stage * L::kABytes), fb, kb * BK, row0);
-          if (tc.g < p.n_routed)
+          if constexpr (epi_is_dgrad(EPI)) {
+            // the weight as stored, [K, Nd]: this CTA's BN / 2 columns as
+            // 64-column boxes of 64 K-rows (MN-major)
+            const uint32_t b_dst = smem_u32(smem + L::kB + stage * L::kBBytes);
+#pragma unroll
+            for (int c = 0; c < BN / 128; ++c) {
+              if (tc.g < p.n_routed)
+                tma2_load_3d(&tmB, b_dst + c * 8192, fb, col0 + 64 * c, kb * BK, tc.g);
+              else
+                tma2_load_2d(&tmBs, b_dst + c * 8192, fb, col0 + 64 * c, kb * BK);
+            }
+          } else if (tc.g < p.n_routed) {
             tma2_load_3d(&tmB, smem_u32(smem + L::kB + stage * L::kBBytes), fb, kb * BK, col0,
                          tc.g);
-          else
+          } else {
             tma2_load_2d(&tmBs, smem_u32(smem + L::kB + stage * L::kBBytes), fb, kb * BK, col0);
+          }
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
       }
@@ -648,7 +697,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CFG::THREADS, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer (CTA 0 of the pair) ----------------
     if (lane == 0 && rank == 0) {
-      constexpr uint32_t idesc = idesc2_bf16_f32<BN>();
+      // dgrad: B MN-major ("transpose B", bit 16)
+      constexpr uint32_t idesc = idesc2_bf16_f32<BN>() | (epi_is_dgrad(EPI) ? (1u << 16) : 0u);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (int tile = pair; ok && tile < total_tiles; tile += npairs) {
@@ -659,11 +709,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CFG::THREADS, 1)
           if (!wait_or_abort(&full[stage], phase, p, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const uint64_t ad = sdesc_sw128(smem_u32(smem + L::kA + stage * L::kABytes));
-          const uint64_t bd = sdesc_sw128(smem_u32(smem + L::kB + stage * L::kBBytes));
+          const uint32_t b_s = smem_u32(smem + L::kB + stage * L::kBBytes);
+          const uint64_t bd = sdesc_sw128(b_s);
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            tc2_mma(d_tmem, ad + uint64_t(2 * kk), bd + uint64_t(2 * kk), idesc,
-                    (kb | kk) != 0 ? 1u : 0u);
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            // MN-major B (dgrad): 64-column chunks 8 KB apart, +2 K groups per step
+            const uint64_t bk = epi_is_dgrad(EPI) ? sdesc_mn_sw128(b_s + kk * 2048, 8192)
+                                                  : bd + uint64_t(2 * kk);
+            tc2_mma(d_tmem, ad + uint64_t(2 * kk), bk, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
           tc2_commit_both(smem_u32(&empty[stage]));
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
@@ -709,7 +763,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CFG::THREADS, 1)
         uint32_t r[CW];
         tmem_ld_cols<CW>(tmem_base + (uint32_t(q * 32) << 16) + acc * BN + c, r);
         const int64_t col = int64_t(tc.n) * BN + c;
-        if constexpr (kStaged) {
+        if constexpr (epi_is_dgrad(EPI)) {
+          // live rows get the result, the group's padding rows (up to its
+          // 128-row boundary, which a 256-row tile may pass) zeros
+          uint8_t* stg = smem + L::kStage + (warp - 2) * staged_warp_bytes<16>();
+          const int row_base = tc.m * BM2 + int(rank) * 128 + q * 32;
+          const int padded = (live + 127) / 128 * 128;
+          __nv_bfloat16* out0 = static_cast<__nv_bfloat16*>(p.out) +
+                                (int64_t(grp_off[tc.g]) + row_base) * p.Nd + col;
+          const __nv_bfloat16* pre_row = p.pre + out_row * p.Nd + col;
+#pragma unroll
+          for (int h = 0; h < CW / 16; ++h) {
+            uint4 w[2];
+            dgrad_words<EPI, 16>(r + 16 * h, pre_row + 16 * h, !valid, w);
+            warp_staged_store<16>(w, stg, lane, out0 + 16 * h, p.Nd, padded - row_base);
+          }
+        } else if constexpr (kStaged) {
           uint8_t* stg = smem + L::kStage + (warp - 2) * staged_warp_bytes<16>();
           const int row_base = tc.m * BM2 + int(rank) * 128 + q * 32;
           __nv_bfloat16* out0 = static_cast<__nv_bfloat16*>(p.out) +
@@ -1207,6 +1276,47 @@ cudaError_t launch_grouped_linear_bf16(const moe_config& c, const GroupedFfnArgs
                                        int64_t K, int64_t Nd, cudaStream_t s) {
   if (g.rows_max == 0) return cudaSuccess;
   return grouped_linear(c, g, A, W, Ws, bias, bias_s, out, K, Nd, EPI_BIAS, s);
+}
+
+bool bwd_dgrad_on_pair(const moe_config& c, int64_t K, int64_t Nd) {
+  const int64_t groups = c.n_experts + (c.d_ff_shared > 0 ? 1 : 0);
+  const int64_t rows = c.T * c.top_k + (c.d_ff_shared > 0 ? c.T : 0);
+  return pick_tile(Nd, rows / groups, K) == TILE_256_PAIR;
+}
+
+cudaError_t launch_bwd_dgrad_pair(const moe_config& c, const BwdGemmArgs& g, const void* dOut,
+                                  const void* W, const void* Ws, int64_t K, int64_t Nd,
+                                  int act, const void* pre, void* out, cudaStream_t s) {
+  const int64_t N = c.n_experts;
+  CUtensorMap mA, mB, mBs;
+  // A = dOut [rows, K] K-major; B = the weight as stored [N, K, Nd], MN-major boxes
+  if (!make_map(&mA, dOut, uint64_t(K), uint64_t(g.rows_max), 0, BM))
+    return cudaErrorInvalidValue;
+  if (!make_map(&mB, W, uint64_t(Nd), uint64_t(K), uint64_t(N), BK))
+    return cudaErrorInvalidValue;
+  if (c.d_ff_shared > 0) {
+    if (!make_map(&mBs, Ws, uint64_t(Nd), uint64_t(K), 0, BK)) return cudaErrorInvalidValue;
+  } else {
+    mBs = mB;
+  }
+  TcParams p{};
+  p.offsets = g.offsets;
+  p.kept = g.kept;
+  p.pre = static_cast<const __nv_bfloat16*>(pre);
+  p.out = out;
+  p.Nd = Nd;
+  p.n_routed = int32_t(N);
+  p.shared_rows = c.d_ff_shared > 0 ? int32_t(c.T) : 0;
+  p.num_kb = int32_t(K / BK);
+  p.status = g.status;
+  p.wait_limit_ns = g.wait_limit_ns;
+  const int64_t groups = N + (c.d_ff_shared > 0 ? 1 : 0);
+  const int64_t max_tiles = (ceil_div(g.rows_max, 256) + groups) * (Nd / 256);
+  if (act < 0)
+    return launch_pair<Cfg256Pair, EPI_DGRAD>(mA, mB, mBs, p, max_tiles, g.num_sms, s);
+  if (act == MOE_ACT_RELU)
+    return launch_pair<Cfg256Pair, EPI_DGRAD_RELU>(mA, mB, mBs, p, max_tiles, g.num_sms, s);
+  return launch_pair<Cfg256Pair, EPI_DGRAD_GELU>(mA, mB, mBs, p, max_tiles, g.num_sms, s);
 }
 
 cudaError_t launch_grouped_ffn_bf16(const moe_config& c, const GroupedFfnArgs& g,

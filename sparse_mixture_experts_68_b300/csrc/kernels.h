@@ -178,6 +178,12 @@ struct BwdGemmArgs {
 cudaError_t launch_bwd_dgrad(const moe_config& c, const BwdGemmArgs& g, const void* dOut,
                              const void* W, const void* Ws, int64_t K, int64_t Nd, int act,
                              const void* pre, void* out, cudaStream_t s);
+// the same dgrad on CTA-pair 256 x 256 tiles (grouped_ffn_sm103.cu), used when
+// bwd_dgrad_on_pair: groups of >= 256 rows, Nd % 256 == 0, K >= 2048
+bool bwd_dgrad_on_pair(const moe_config& c, int64_t K, int64_t Nd);
+cudaError_t launch_bwd_dgrad_pair(const moe_config& c, const BwdGemmArgs& g, const void* dOut,
+                                  const void* W, const void* Ws, int64_t K, int64_t Nd,
+                                  int act, const void* pre, void* out, cudaStream_t s);
 // out[e] = L[group e]^T . R[group e] ([Md, Nd] per group; shared into out_s)
 cudaError_t launch_bwd_wgrad(const moe_config& c, const BwdGemmArgs& g, const void* Lm,
                              int64_t Md, const void* Rm, int64_t Nd, void* out, void* out_s,

@@ -126,6 +126,13 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
          (uint64_t(1024 >> 4) << 32) | (uint64_t(1) << 46) | (uint64_t(2) << 61);
 }
 
+// MN-major operand, 128-byte swizzle: MN chunks of 64 elements `lbo` bytes
+// apart, 8-row K groups 1024 bytes apart (descriptor version 1).
+__device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t saddr, uint32_t lbo) {
+  return uint64_t((saddr & 0x3FFFFu) >> 4) | (uint64_t(lbo >> 4) << 16) |
+         (uint64_t(1024 >> 4) << 32) | (uint64_t(1) << 46) | (uint64_t(2) << 61);
+}
+
 // ---- host side -----------------------------------------------------------------------
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {

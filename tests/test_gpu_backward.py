@@ -102,6 +102,10 @@ SMALL = [
     # N % 64 == 0 (tensor-core router), shared expert
     Workload("bwd_many_experts", T=400, d_model=128, d_ff=128, n_experts=64, top_k=6,
              act=ACT_GELU_ERF, dtype=DT_BF16, d_ff_shared=128, seed=84),
+    # groups of >= 256 rows and K = d = 2048: the dgrad dA = (dO W2) GELU'(A1) on
+    # CTA-pair tiles (MN-major weights), with a shared expert and ragged groups
+    Workload("bwd_pair_dgrad", T=600, d_model=2048, d_ff=512, n_experts=2, top_k=1,
+             act=ACT_GELU_ERF, dtype=DT_BF16, d_ff_shared=512, seed=86),
     # ~1000-row groups: several m-tiles per group in the dgrads, many K blocks in the wgrads
     Workload("bwd_big_groups", T=2000, d_model=256, d_ff=512, n_experts=2, top_k=1,
              act=ACT_GELU_ERF, dtype=DT_BF16, seed=85),
