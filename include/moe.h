@@ -284,9 +284,9 @@ moe_status moe_activation(int32_t act, const float* x, float* y, int64_t n, void
  * same call sequence: combine, expert FFNs (the first Linear's
  * pre-activation is recomputed), gates (softmax over the k selected scores,
  * or the raw probabilities), the balance statistic and the router.  The top-k
- * choice and the capacity drops pass no gradient.  bf16 layers only (an fp32
- * config returns MOE_ERR_UNSUPPORTED); top-k routing only.
- * Gradients are written in the layer dtype (bf16), accumulated in fp32. */
+ * choice and the capacity drops pass no gradient.  Top-k routing only.  bf16
+ * layers run their GEMMs on the tensor cores, fp32 layers on CUDA cores in
+ * fp32.  Gradients are written in the layer dtype, accumulated in fp32. */
 
 typedef struct moe_grads {
   void  *dx;                          /* [T, d_model]                      required */
@@ -297,10 +297,9 @@ typedef struct moe_grads {
   float *dw;                          /* [T, k] d total / d gate; NULL = skip       */
 } moe_grads;
 
-/* Bytes of device workspace moe_backward needs; 0 for an invalid or
- * unsupported config. */
+/* Bytes of device workspace moe_backward needs; 0 for an invalid config. */
 size_t moe_backward_workspace_size(const moe_config* cfg);
-/* Kernels one moe_backward launches; -1 for an invalid or unsupported config. */
+/* Kernels one moe_backward launches; -1 for an invalid config. */
 int32_t moe_backward_launch_count(const moe_config* cfg);
 
 /* The backward pass.  `fwd` and `fwd_workspace` are the outputs and the

@@ -115,10 +115,11 @@ BwdWorkspace bwd_layout(const moe_config& c, void* base) {
     return reinterpret_cast<void*>(p + at);
   };
   const int64_t rows = rows_max_of(c);
-  w.dO = take(size_t(rows * c.d_model) * 2);
-  w.A1 = take(size_t(rows * c.d_ff) * 2);
-  w.dA = take(size_t(rows * c.d_ff) * 2);
-  w.dXp = take(size_t(rows * c.d_model) * 2);
+  const int64_t es = elem_bytes(c);
+  w.dO = take(size_t(rows * c.d_model * es));
+  w.A1 = take(size_t(rows * c.d_ff * es));
+  w.dA = take(size_t(rows * c.d_ff * es));
+  w.dXp = take(size_t(rows * c.d_model * es));
   w.dz = static_cast<float*>(take(size_t(c.T * c.n_experts) * 4));
   w.dw = static_cast<float*>(take(size_t(c.T * c.top_k) * 4));
   w.dxr = static_cast<float*>(take(size_t(c.T * c.d_model) * 4));
@@ -130,12 +131,7 @@ BwdWorkspace bwd_layout(const moe_config& c, void* base) {
   return w;
 }
 
-moe_status check_bwd_config(const moe_config* cfg) {
-  const moe_status st = check_config(cfg);
-  if (st != MOE_OK) return st;
-  if (cfg->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
-  return MOE_OK;
-}
+moe_status check_bwd_config(const moe_config* cfg) { return check_config(cfg); }
 
 // ---- expert-choice routing ----
 

@@ -34,7 +34,7 @@ namespace {
 
 struct PadBufs {
   void* buf[3];
-  int64_t width[3];          // bf16 columns
+  int64_t vec16[3];          // 16-byte words per row
   int n;
 };
 
@@ -49,7 +49,7 @@ __global__ void __launch_bounds__(256)
   const int64_t r1 = offsets[g + 1];
   for (int64_t r = offsets[g] + live + blockIdx.y; r < r1; r += gridDim.y)
     for (int i = 0; i < b.n; ++i) {
-      const int64_t nv = b.width[i] / 8;
+      const int64_t nv = b.vec16[i];
       uint4* row = static_cast<uint4*>(b.buf[i]) + r * nv;
       for (int64_t j = threadIdx.x; j < nv; j += blockDim.x) row[j] = make_uint4(0, 0, 0, 0);
     }
@@ -72,13 +72,15 @@ __device__ __forceinline__ float warp_max(float v) {
 }
 
 // One warp per token.  Shared memory per warp: p [N], dp [N], dz [N], dw [k].
+// E: the layer's element type (dy, Yp, dO).
+template <typename E>
 __global__ void __launch_bounds__(kGateWarps * 32)
-    bwd_gate_kernel(const __nv_bfloat16* __restrict__ dy, const __nv_bfloat16* __restrict__ Yp,
+    bwd_gate_kernel(const E* __restrict__ dy, const E* __restrict__ Yp,
                     const int32_t* __restrict__ token_row, const int32_t* __restrict__ topk_idx,
                     const float* __restrict__ topk_w, const float* __restrict__ logits,
                     const float* __restrict__ mean_prob, const int32_t* __restrict__ offsets,
                     int T, int64_t d, int N, int k, int renorm, int has_shared, float aux,
-                    __nv_bfloat16* __restrict__ dO, float* __restrict__ dz_out,
+                    E* __restrict__ dO, float* __restrict__ dz_out,
                     float* __restrict__ dw_out, __nv_bfloat16* __restrict__ dz_bf,
                     int32_t* __restrict__ rgrp) {
   extern __shared__ float gsm[];
@@ -96,8 +98,9 @@ __global__ void __launch_bounds__(kGateWarps * 32)
   float* DP = P + N;
   float* DZ = DP + N;
   float* DW = DZ + N;
-  const int64_t nv = d / 8;
-  const uint4* dyr = reinterpret_cast<const uint4*>(dy + int64_t(t) * d);
+  constexpr int V = Vec16<E>::n;
+  const int64_t nv = d / V;
+  const E* dyr = dy + int64_t(t) * d;
 
   // dw_j = <dy, o_j> and dO rows
   for (int j = 0; j < k; ++j) {
@@ -105,21 +108,18 @@ __global__ void __launch_bounds__(kGateWarps * 32)
     float dot = 0.f;
     if (r >= 0) {
       const float wj = topk_w[int64_t(t) * k + j];
-      const uint4* orow = reinterpret_cast<const uint4*>(Yp + r * d);
-      uint4* drow = reinterpret_cast<uint4*>(dO + r * d);
+      const E* orow = Yp + r * d;
+      E* drow = dO + r * d;
       for (int64_t c = lane; c < nv; c += 32) {
-        const uint4 a = __ldg(dyr + c), o = __ldg(orow + c);
-        const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-        const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&o);
-        uint4 q;
-        __nv_bfloat162* q2 = reinterpret_cast<__nv_bfloat162*>(&q);
+        float av[V], ov[V], q[V];
+        Vec16<E>::load(dyr + c * V, av);
+        Vec16<E>::load(orow + c * V, ov);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 av = __bfloat1622float2(a2[i]), ov = __bfloat1622float2(o2[i]);
-          dot = fmaf(av.x, ov.x, fmaf(av.y, ov.y, dot));
-          q2[i] = __floats2bfloat162_rn(wj * av.x, wj * av.y);
+        for (int i = 0; i < V; ++i) {
+          dot = fmaf(av[i], ov[i], dot);
+          q[i] = wj * av[i];
         }
-        drow[c] = q;
+        Vec16<E>::store(drow + c * V, q);
       }
       dot = warp_sum(dot);
     }
@@ -127,8 +127,12 @@ __global__ void __launch_bounds__(kGateWarps * 32)
     if (dw_out && lane == 0) dw_out[int64_t(t) * k + j] = dot;
   }
   if (has_shared) {                           // the shared expert's gate is 1
-    uint4* drow = reinterpret_cast<uint4*>(dO + (int64_t(offsets[N]) + t) * d);
-    for (int64_t c = lane; c < nv; c += 32) drow[c] = __ldg(dyr + c);
+    E* drow = dO + (int64_t(offsets[N]) + t) * d;
+    for (int64_t c = lane; c < nv; c += 32) {
+      float av[V];
+      Vec16<E>::load(dyr + c * V, av);
+      Vec16<E>::store(drow + c * V, av);
+    }
   }
 
   // p = softmax(z) over all N
@@ -179,55 +183,54 @@ __global__ void __launch_bounds__(kGateWarps * 32)
 
 // ---- column sums of groups (bias gradients) -----------------------------------------------
 
-// Block (g, chunk): columns chunk*256 .. +255 of group g's live rows; eight
-// warps take every eighth row, lanes 8 columns each; warps combine in order.
+// Block (g, chunk): columns chunk*32V .. +32V-1 of group g's live rows (V
+// elements per 16-byte word); eight warps take every eighth row, lanes one word
+// each; warps combine in order.
+template <typename T>
 __global__ void __launch_bounds__(256)
-    group_colsum_kernel(const __nv_bfloat16* __restrict__ src, int64_t width,
+    group_colsum_kernel(const T* __restrict__ src, int64_t width,
                         const int32_t* __restrict__ offsets, const int32_t* __restrict__ kept,
-                        int n_routed, int shared_rows, __nv_bfloat16* __restrict__ out,
-                        __nv_bfloat16* __restrict__ out_s) {
-  __shared__ float part[8][256];
+                        int n_routed, int shared_rows, T* __restrict__ out, T* __restrict__ out_s) {
+  constexpr int V = Vec16<T>::n;
+  __shared__ float part[8][32 * V];
   pdl_launch_dependents();
   pdl_wait_previous();
   const int g = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t c0 = int64_t(blockIdx.y) * 256 + lane * 8;
+  const int64_t c0 = int64_t(blockIdx.y) * 32 * V + lane * V;
   const int64_t live = g < n_routed ? kept[g] : shared_rows;
   const int64_t r0 = offsets[g];
-  float acc[8];
+  float acc[V];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  for (int i = 0; i < V; ++i) acc[i] = 0.f;
   if (c0 < width) {
     for (int64_t r = warp; r < live; r += 8) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(src + (r0 + r) * width + c0));
-      const __nv_bfloat162* v2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+      float v[V];
+      Vec16<T>::load(src + (r0 + r) * width + c0, v);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = __bfloat1622float2(v2[i]);
-        acc[2 * i] += f.x;
-        acc[2 * i + 1] += f.y;
-      }
+      for (int i = 0; i < V; ++i) acc[i] += v[i];
     }
   }
 #pragma unroll
-  for (int i = 0; i < 8; ++i) part[warp][lane * 8 + i] = acc[i];
+  for (int i = 0; i < V; ++i) part[warp][lane * V + i] = acc[i];
   __syncthreads();
-  const int col = threadIdx.x;
-  const int64_t cc = int64_t(blockIdx.y) * 256 + col;
-  if (cc < width) {
-    float s = 0.f;
-    for (int w = 0; w < 8; ++w) s += part[w][col];
-    __nv_bfloat16* dst = g < n_routed ? out + int64_t(g) * width : out_s;
-    dst[cc] = __float2bfloat16_rn(s);
+  for (int col = threadIdx.x; col < 32 * V; col += blockDim.x) {
+    const int64_t cc = int64_t(blockIdx.y) * 32 * V + col;
+    if (cc < width) {
+      float s = 0.f;
+      for (int w = 0; w < 8; ++w) s += part[w][col];
+      T* dst = g < n_routed ? out + int64_t(g) * width : out_s;
+      dst[cc] = from_f32<T>(s);
+    }
   }
 }
 
 // db_g[e] = sum_t dz[t, e] (fp32 in, bf16 out): block b takes experts
 // 32 b .. 32 b + 31 (one per lane), its eight warps every eighth token, and
 // the warps combine in order.
+template <typename TO>
 __global__ void __launch_bounds__(256)
-    router_bias_grad_kernel(const float* __restrict__ dz, int T, int N,
-                            __nv_bfloat16* __restrict__ db_g) {
+    router_bias_grad_kernel(const float* __restrict__ dz, int T, int N, TO* __restrict__ db_g) {
   __shared__ float part[8][32];
   pdl_launch_dependents();
   pdl_wait_previous();
@@ -241,7 +244,7 @@ __global__ void __launch_bounds__(256)
   if (warp == 0 && e < N) {
     float v = 0.f;
     for (int w = 0; w < 8; ++w) v += part[w][lane];
-    db_g[e] = __float2bfloat16_rn(v);
+    db_g[e] = from_f32<TO>(v);
   }
 }
 
@@ -254,10 +257,10 @@ constexpr int kRouterMaxSplits = 32;
 
 // blockIdx.z splits K into chunks of kc; split z writes its partial sums to
 // C + z * M * ldc (fp32), summed afterwards by splitk_reduce_kernel.
-template <typename TOut>
+template <typename TB, typename TOut>
 __global__ void __launch_bounds__(256)
     router_grad_gemm_kernel(const float* __restrict__ A, int64_t am, int64_t ak,
-                            const __nv_bfloat16* __restrict__ B, int64_t ldb, int64_t M,
+                            const TB* __restrict__ B, int64_t ldb, int64_t M,
                             int64_t Nn, int64_t K, int64_t kc, TOut* __restrict__ C,
                             int64_t ldc) {
   __shared__ float As[kRk][kRg + 4];
@@ -281,7 +284,7 @@ __global__ void __launch_bounds__(256)
     for (int i = tid; i < kRg * kRk; i += 256) {
       const int nn = i % kRg, kk = i / kRg;
       const int64_t gn = n0 + nn, gk = k0 + kk;
-      Bs[kk][nn] = (gn < Nn && gk < ke) ? __bfloat162float(B[gk * ldb + gn]) : 0.f;
+      Bs[kk][nn] = (gn < Nn && gk < ke) ? to_f32(B[gk * ldb + gn]) : 0.f;
     }
     __syncthreads();
 #pragma unroll
@@ -311,16 +314,16 @@ __global__ void __launch_bounds__(256)
 }
 
 // out[i] = sum over the S splits of part[z * n + i], in split order.
+template <typename TO>
 __global__ void __launch_bounds__(256)
-    splitk_reduce_kernel(const float* __restrict__ part, int S, int64_t n,
-                         __nv_bfloat16* __restrict__ out) {
+    splitk_reduce_kernel(const float* __restrict__ part, int S, int64_t n, TO* __restrict__ out) {
   pdl_launch_dependents();
   pdl_wait_previous();
   for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
        i += int64_t(gridDim.x) * blockDim.x) {
     float v = 0.f;
     for (int z = 0; z < S; ++z) v += part[int64_t(z) * n + i];
-    out[i] = __float2bfloat16_rn(v);
+    out[i] = from_f32<TO>(v);
   }
 }
 
@@ -329,65 +332,45 @@ __global__ void __launch_bounds__(256)
 constexpr int kDxWarps = 8;
 
 // dx[t] = dxr[t] (the router's part, fp32 or bf16) + sum over t's kept rows
-// of dXp (slot order) + the shared row
-template <typename TR>
+// of dXp (slot order) + the shared row; T: the layer's element type.
+template <typename TR, typename T>
 __global__ void __launch_bounds__(kDxWarps * 32)
-    bwd_dx_kernel(const __nv_bfloat16* __restrict__ dXp, const int32_t* __restrict__ token_row,
-                  const int32_t* __restrict__ offsets, const TR* __restrict__ dxr, int T,
-                  int k, int N, int has_shared, int64_t d, __nv_bfloat16* __restrict__ dx) {
+    bwd_dx_kernel(const T* __restrict__ dXp, const int32_t* __restrict__ token_row,
+                  const int32_t* __restrict__ offsets, const TR* __restrict__ dxr, int Ttok,
+                  int k, int N, int has_shared, int64_t d, T* __restrict__ dx) {
+  constexpr int V = Vec16<T>::n;
   pdl_launch_dependents();
   pdl_wait_previous();
   const int lane = threadIdx.x & 31;
   const int64_t t = int64_t(blockIdx.x) * kDxWarps + (threadIdx.x >> 5);
-  if (t >= T) return;
-  const int64_t nv = d / 8;
+  if (t >= Ttok) return;
+  const int64_t nv = d / V;
   for (int64_t c = lane; c < nv; c += 32) {
-    float acc[8];
-    if constexpr (sizeof(TR) == 4) {
-      const float4* xr = reinterpret_cast<const float4*>(dxr + t * d) + 2 * c;
-      const float4 r0 = xr[0], r1 = xr[1];
-      acc[0] = r0.x; acc[1] = r0.y; acc[2] = r0.z; acc[3] = r0.w;
-      acc[4] = r1.x; acc[5] = r1.y; acc[6] = r1.z; acc[7] = r1.w;
-    } else {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(dxr + t * d) + c);
-      const __nv_bfloat162* v2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+    float acc[V];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = __bfloat1622float2(v2[i]);
-        acc[2 * i] = f.x;
-        acc[2 * i + 1] = f.y;
-      }
-    }
+    for (int i = 0; i < V; ++i) acc[i] = to_f32(dxr[t * d + c * V + i]);
     for (int j = 0; j <= k; ++j) {
       int64_t r;
       if (j < k) r = token_row[t * k + j];
       else r = has_shared ? int64_t(offsets[N]) + t : -1;
       if (r < 0) continue;
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(dXp + r * d) + c);
-      const __nv_bfloat162* v2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+      float v[V];
+      Vec16<T>::load(dXp + r * d + c * V, v);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = __bfloat1622float2(v2[i]);
-        acc[2 * i] += f.x;
-        acc[2 * i + 1] += f.y;
-      }
+      for (int i = 0; i < V; ++i) acc[i] += v[i];
     }
-    uint4 o;
-    __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(&o);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) o2[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
-    reinterpret_cast<uint4*>(dx + t * d)[c] = o;
+    Vec16<T>::store(dx + t * d + c * V, acc);
   }
 }
 
-template <typename TOut>
-cudaError_t launch_router_grad_gemm(const float* A, int64_t am, int64_t ak,
-                                    const __nv_bfloat16* B, int64_t ldb, int64_t M, int64_t Nn,
-                                    int64_t K, TOut* C, int64_t ldc, cudaStream_t s) {
+template <typename TB, typename TOut>
+cudaError_t launch_router_grad_gemm(const float* A, int64_t am, int64_t ak, const TB* B,
+                                    int64_t ldb, int64_t M, int64_t Nn, int64_t K, TOut* C,
+                                    int64_t ldc, cudaStream_t s) {
   if (M == 0 || Nn == 0) return cudaSuccess;
   dim3 grid(unsigned((Nn + kRg - 1) / kRg), unsigned((M + kRg - 1) / kRg));
-  return launch_pdl(router_grad_gemm_kernel<TOut>, grid, dim3(256), 0, s, A, am, ak, B, ldb, M,
-                    Nn, K, K, C, ldc);
+  return launch_pdl(router_grad_gemm_kernel<TB, TOut>, grid, dim3(256), 0, s, A, am, ak, B,
+                    ldb, M, Nn, K, K, C, ldc);
 }
 
 // Splits of K for dW_g = dz^T x on CUDA cores: enough blocks for two waves.
@@ -400,17 +383,18 @@ int router_splits(const moe_config& c) {
   return int(S < 1 ? 1 : S);
 }
 
-// n bf16 zeros: 16-byte words, then the tail element by element.
-__global__ void __launch_bounds__(256) fill_zero_kernel(__nv_bfloat16* __restrict__ p,
-                                                        int64_t n) {
+// n zeros of T: 16-byte words, then the tail element by element.
+template <typename T>
+__global__ void __launch_bounds__(256) fill_zero_kernel(T* __restrict__ p, int64_t n) {
+  constexpr int V = Vec16<T>::n;
   pdl_launch_dependents();
   pdl_wait_previous();
-  const int64_t n16 = n / 8;
+  const int64_t n16 = n / V;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
   const int64_t i0 = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   for (int64_t i = i0; i < n16; i += stride)
     reinterpret_cast<uint4*>(p)[i] = make_uint4(0, 0, 0, 0);
-  for (int64_t i = n16 * 8 + i0; i < n; i += stride) p[i] = __float2bfloat16_rn(0.f);
+  for (int64_t i = n16 * V + i0; i < n; i += stride) p[i] = from_f32<T>(0.f);
 }
 
 // No tokens: every parameter gradient is zero.
@@ -422,10 +406,14 @@ cudaError_t zero_param_grads(const moe_config& c, const moe_grads* g, cudaStream
                       {g->dW2s, d * f},  {g->db2s, d}};
   const int nb = c.d_ff_shared > 0 ? 10 : 6;
   for (int i = 0; i < nb; ++i) {
-    const int64_t want = (bufs[i].n / 8 + 255) / 256 + 1;
+    const int64_t want = (bufs[i].n / 4 + 255) / 256 + 1;
+    const dim3 grid(unsigned(want < 1184 ? want : 1184));
     const cudaError_t e =
-        launch_pdl(fill_zero_kernel, dim3(unsigned(want < 1184 ? want : 1184)), dim3(256), 0, s,
-                   static_cast<__nv_bfloat16*>(bufs[i].p), bufs[i].n);
+        c.dtype == MOE_F32
+            ? launch_pdl(fill_zero_kernel<float>, grid, dim3(256), 0, s,
+                         static_cast<float*>(bufs[i].p), bufs[i].n)
+            : launch_pdl(fill_zero_kernel<__nv_bfloat16>, grid, dim3(256), 0, s,
+                         static_cast<__nv_bfloat16*>(bufs[i].p), bufs[i].n);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -433,7 +421,9 @@ cudaError_t zero_param_grads(const moe_config& c, const moe_grads* g, cudaStream
 
 }  // namespace
 
-bool router_bwd_on_tensor_cores(const moe_config& c) { return c.n_experts % 64 == 0; }
+bool router_bwd_on_tensor_cores(const moe_config& c) {
+  return c.dtype == MOE_BF16 && c.n_experts % 64 == 0;
+}
 
 size_t router_bwd_partial_bytes(const moe_config& c) {
   return router_bwd_on_tensor_cores(c)
@@ -443,13 +433,19 @@ size_t router_bwd_partial_bytes(const moe_config& c) {
 
 int backward_launch_count(const moe_config& c) {
   if (c.T == 0) return c.d_ff_shared > 0 ? 10 : 6;    // zero parameter gradients
-  // gate, padding, A1, dA, dXp, dW2, dW1, db2, db1, dx_router, dW_g (+ split-K
-  // reduce on CUDA cores), db_g, dx
-  return router_bwd_on_tensor_cores(c) ? 13 : 14;
+  // gate, padding (bf16 only), A1, dA, dXp, dW2, dW1, db2, db1, dx_router,
+  // dW_g (+ split-K reduce on CUDA cores), db_g, dx
+  return (router_bwd_on_tensor_cores(c) ? 13 : 14) - (c.dtype == MOE_F32 ? 1 : 0);
 }
 
-cudaError_t launch_backward(const moe_config& c, const BackwardArgs& a, void* const* events,
-                            cudaStream_t s) {
+namespace {
+
+// The backward for layers of element type T (bf16: tensor-core GEMMs; fp32:
+// CUDA-core GEMMs), with the events of moe_backward_profiled.
+template <typename E>
+cudaError_t backward_t(const moe_config& c, const BackwardArgs& a, void* const* events,
+                       cudaStream_t s) {
+  constexpr bool kBf16 = sizeof(E) == 2;
   void* const none[8] = {};
   void* const* ev = events ? events : none;
   cudaError_t er = record_event(ev[0], s);
@@ -470,25 +466,25 @@ cudaError_t launch_backward(const moe_config& c, const BackwardArgs& a, void* co
     const size_t smem = size_t(kGateWarps) * (3 * N + k) * sizeof(float);
     if (smem > 48 * 1024) {
       const cudaError_t e = cudaFuncSetAttribute(
-          bwd_gate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+          bwd_gate_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
       if (e != cudaSuccess) return e;
     }
+    const bool tcr = router_bwd_on_tensor_cores(c);
     const cudaError_t e = launch_pdl(
-        bwd_gate_kernel, dim3(unsigned((T + kGateWarps - 1) / kGateWarps)),
-        dim3(kGateWarps * 32), smem, s, static_cast<const __nv_bfloat16*>(a.dy),
-        static_cast<const __nv_bfloat16*>(a.Yp), a.token_row, a.topk_idx, a.topk_w, a.logits,
+        bwd_gate_kernel<E>, dim3(unsigned((T + kGateWarps - 1) / kGateWarps)),
+        dim3(kGateWarps * 32), smem, s, static_cast<const E*>(a.dy),
+        static_cast<const E*>(a.Yp), a.token_row, a.topk_idx, a.topk_w, a.logits,
         a.mean_prob, a.offsets, T, d, N, k, c.renormalize ? 1 : 0, hs, a.aux_weight,
-        static_cast<__nv_bfloat16*>(a.dO), a.dz, a.dw,
-        router_bwd_on_tensor_cores(c) ? static_cast<__nv_bfloat16*>(a.dz_bf) : nullptr,
-        router_bwd_on_tensor_cores(c) ? a.rgrp : nullptr);
+        static_cast<E*>(a.dO), a.dz, a.dw, tcr ? static_cast<__nv_bfloat16*>(a.dz_bf) : nullptr,
+        tcr ? a.rgrp : nullptr);
     if (e != cudaSuccess) return e;
   }
-  // padding rows of dO, H and Xp -> 0 (the wgrads run K over whole 64-row blocks)
-  {
+  if (kBf16) {
+    // padding rows of dO, H and Xp -> 0 (the wgrads run K over whole 64-row blocks)
     PadBufs pb{};
-    pb.buf[0] = a.dO; pb.width[0] = d;
-    pb.buf[1] = a.H; pb.width[1] = f;
-    pb.buf[2] = a.Xp; pb.width[2] = d;
+    pb.buf[0] = a.dO; pb.vec16[0] = d / 8;
+    pb.buf[1] = a.H; pb.vec16[1] = f / 8;
+    pb.buf[2] = a.Xp; pb.vec16[2] = d / 8;
     pb.n = 3;
     const cudaError_t e = launch_pdl(zero_pad_rows_kernel, dim3(unsigned(groups), 16),
                                      dim3(256), 0, s, a.offsets, a.kept, N, hs ? T : 0, pb);
@@ -504,33 +500,37 @@ cudaError_t launch_backward(const moe_config& c, const BackwardArgs& a, void* co
   bg.wait_limit_ns = a.wait_limit_ns; bg.num_sms = a.num_sms;
   cudaError_t e;
   // A1 = Xp W1^T + b1 (the pre-activation, recomputed)
-  e = launch_grouped_linear_bf16(c, ga, a.Xp, w->W1, w->W1s, w->b1, w->b1s, a.A1, d, f, s);
+  e = kBf16 ? launch_grouped_linear_bf16(c, ga, a.Xp, w->W1, w->W1s, w->b1, w->b1s, a.A1, d, f, s)
+            : launch_grouped_linear_f32(c, bg, a.Xp, w->W1, w->W1s, w->b1, w->b1s, a.A1, d, f, s);
   if (e == cudaSuccess) e = record_event(ev[2], s);
   if (e != cudaSuccess) return e;
   // dA = (dO . W2) act'(A1);  dXp = dA . W1
-  e = launch_bwd_dgrad(c, bg, a.dO, w->W2, w->W2s, d, f, c.act, a.A1, a.dA, s);
+  auto dgrad = kBf16 ? launch_bwd_dgrad : launch_bwd_dgrad_f32;
+  e = dgrad(c, bg, a.dO, w->W2, w->W2s, d, f, c.act, a.A1, a.dA, s);
   if (e == cudaSuccess) e = record_event(ev[3], s);
   if (e != cudaSuccess) return e;
-  e = launch_bwd_dgrad(c, bg, a.dA, w->W1, w->W1s, f, d, -1, nullptr, a.dXp, s);
+  e = dgrad(c, bg, a.dA, w->W1, w->W1s, f, d, -1, nullptr, a.dXp, s);
   if (e == cudaSuccess) e = record_event(ev[4], s);
   if (e != cudaSuccess) return e;
   // dW2 = dO^T H [d, f];  dW1 = dA^T Xp [f, d]
-  e = launch_bwd_wgrad(c, bg, a.dO, d, a.H, f, a.g->dW2, a.g->dW2s, s);
+  auto wgrad = kBf16 ? launch_bwd_wgrad : launch_bwd_wgrad_f32;
+  e = wgrad(c, bg, a.dO, d, a.H, f, a.g->dW2, a.g->dW2s, s);
   if (e == cudaSuccess) e = record_event(ev[5], s);
   if (e != cudaSuccess) return e;
-  e = launch_bwd_wgrad(c, bg, a.dA, f, a.Xp, d, a.g->dW1, a.g->dW1s, s);
+  e = wgrad(c, bg, a.dA, f, a.Xp, d, a.g->dW1, a.g->dW1s, s);
   if (e == cudaSuccess) e = record_event(ev[6], s);
   if (e != cudaSuccess) return e;
   // db2, db1
-  e = launch_pdl(group_colsum_kernel, dim3(unsigned(groups), unsigned((d + 255) / 256)),
-                 dim3(256), 0, s, static_cast<const __nv_bfloat16*>(a.dO), d, a.offsets,
-                 a.kept, N, hs ? T : 0, static_cast<__nv_bfloat16*>(a.g->db2),
-                 static_cast<__nv_bfloat16*>(a.g->db2s));
+  constexpr int kColsPerBlock = 32 * Vec16<E>::n;
+  e = launch_pdl(group_colsum_kernel<E>,
+                 dim3(unsigned(groups), unsigned((d + kColsPerBlock - 1) / kColsPerBlock)),
+                 dim3(256), 0, s, static_cast<const E*>(a.dO), d, a.offsets, a.kept, N,
+                 hs ? T : 0, static_cast<E*>(a.g->db2), static_cast<E*>(a.g->db2s));
   if (e != cudaSuccess) return e;
-  e = launch_pdl(group_colsum_kernel, dim3(unsigned(groups), unsigned((f + 255) / 256)),
-                 dim3(256), 0, s, static_cast<const __nv_bfloat16*>(a.dA), f, a.offsets,
-                 a.kept, N, hs ? T : 0, static_cast<__nv_bfloat16*>(a.g->db1),
-                 static_cast<__nv_bfloat16*>(a.g->db1s));
+  e = launch_pdl(group_colsum_kernel<E>,
+                 dim3(unsigned(groups), unsigned((f + kColsPerBlock - 1) / kColsPerBlock)),
+                 dim3(256), 0, s, static_cast<const E*>(a.dA), f, a.offsets, a.kept, N,
+                 hs ? T : 0, static_cast<E*>(a.g->db1), static_cast<E*>(a.g->db1s));
   if (e != cudaSuccess) return e;
   // router: dx_router = dz W_g [T, d]; dW_g = dz^T x [N, d]; db_g = sum_t dz
   const bool tc_router = router_bwd_on_tensor_cores(c);
@@ -548,41 +548,48 @@ cudaError_t launch_backward(const moe_config& c, const BackwardArgs& a, void* co
     e = launch_bwd_wgrad(rc, rg, a.dz_bf, N, a.x, d, a.g->dW_g, nullptr, s);
     if (e != cudaSuccess) return e;
   } else {
-    e = launch_router_grad_gemm<float>(a.dz, N, 1, static_cast<const __nv_bfloat16*>(w->W_g),
-                                       d, T, d, N, a.dxr, d, s);
+    e = launch_router_grad_gemm<E, float>(a.dz, N, 1, static_cast<const E*>(w->W_g), d, T, d,
+                                          N, a.dxr, d, s);
     if (e != cudaSuccess) return e;
     const int S = router_splits(c);
     const int64_t kc = ((T + S - 1) / S + kRk - 1) / kRk * kRk;
     dim3 grid(unsigned((d + kRg - 1) / kRg), unsigned((N + kRg - 1) / kRg), unsigned(S));
-    e = launch_pdl(router_grad_gemm_kernel<float>, grid, dim3(256), 0, s,
+    e = launch_pdl(router_grad_gemm_kernel<E, float>, grid, dim3(256), 0, s,
                    static_cast<const float*>(a.dz), int64_t(1), int64_t(N),
-                   static_cast<const __nv_bfloat16*>(a.x), d, int64_t(N), d, int64_t(T), kc,
-                   a.part, d);
+                   static_cast<const E*>(a.x), d, int64_t(N), d, int64_t(T), kc, a.part, d);
     if (e != cudaSuccess) return e;
     const int64_t n = int64_t(N) * d;
     const int64_t blocks = (n + 255) / 256;
-    e = launch_pdl(splitk_reduce_kernel, dim3(unsigned(blocks < 1184 ? blocks : 1184)),
+    e = launch_pdl(splitk_reduce_kernel<E>, dim3(unsigned(blocks < 1184 ? blocks : 1184)),
                    dim3(256), 0, s, static_cast<const float*>(a.part), S, n,
-                   static_cast<__nv_bfloat16*>(a.g->dW_g));
+                   static_cast<E*>(a.g->dW_g));
     if (e != cudaSuccess) return e;
   }
-  e = launch_pdl(router_bias_grad_kernel, dim3(unsigned((N + 31) / 32)), dim3(256), 0, s,
-                 static_cast<const float*>(a.dz), T, N,
-                 static_cast<__nv_bfloat16*>(a.g->db_g));
+  e = launch_pdl(router_bias_grad_kernel<E>, dim3(unsigned((N + 31) / 32)), dim3(256), 0, s,
+                 static_cast<const float*>(a.dz), T, N, static_cast<E*>(a.g->db_g));
   if (e != cudaSuccess) return e;
   // dx
   if (tc_router)
-    e = launch_pdl(bwd_dx_kernel<__nv_bfloat16>, dim3(unsigned((T + kDxWarps - 1) / kDxWarps)),
-                   dim3(kDxWarps * 32), 0, s, static_cast<const __nv_bfloat16*>(a.dXp),
-                   a.token_row, a.offsets, static_cast<const __nv_bfloat16*>(a.dxr_bf), T, k, N,
-                   hs, d, static_cast<__nv_bfloat16*>(a.g->dx));
+    e = launch_pdl(bwd_dx_kernel<__nv_bfloat16, E>,
+                   dim3(unsigned((T + kDxWarps - 1) / kDxWarps)), dim3(kDxWarps * 32), 0, s,
+                   static_cast<const E*>(a.dXp), a.token_row, a.offsets,
+                   static_cast<const __nv_bfloat16*>(a.dxr_bf), T, k, N, hs, d,
+                   static_cast<E*>(a.g->dx));
   else
-    e = launch_pdl(bwd_dx_kernel<float>, dim3(unsigned((T + kDxWarps - 1) / kDxWarps)),
-                   dim3(kDxWarps * 32), 0, s, static_cast<const __nv_bfloat16*>(a.dXp),
-                   a.token_row, a.offsets, static_cast<const float*>(a.dxr), T, k, N, hs, d,
-                   static_cast<__nv_bfloat16*>(a.g->dx));
+    e = launch_pdl(bwd_dx_kernel<float, E>, dim3(unsigned((T + kDxWarps - 1) / kDxWarps)),
+                   dim3(kDxWarps * 32), 0, s, static_cast<const E*>(a.dXp), a.token_row,
+                   a.offsets, static_cast<const float*>(a.dxr), T, k, N, hs, d,
+                   static_cast<E*>(a.g->dx));
   if (e != cudaSuccess) return e;
   return record_event(ev[7], s);
+}
+
+}  // namespace
+
+cudaError_t launch_backward(const moe_config& c, const BackwardArgs& a, void* const* events,
+                            cudaStream_t s) {
+  return c.dtype == MOE_F32 ? backward_t<float>(c, a, events, s)
+                            : backward_t<__nv_bfloat16>(c, a, events, s);
 }
 
 }  // namespace moe

@@ -33,4 +33,60 @@ cudaError_t launch_grouped_ffn_f32(const moe_config& c, const GroupedFfnArgs& g,
   return launch_pdl(simt_gemm_kernel<float, float>, grid2, dim3(kSimtThreads), 0, s, a);
 }
 
+// ---- backward on CUDA cores (fp32 layers) ----------------------------------------------
+
+// out = A W^T + b per group, no activation (the recomputed pre-activation)
+cudaError_t launch_grouped_linear_f32(const moe_config& c, const BwdGemmArgs& g, const void* A,
+                                      const void* W, const void* Ws, const void* bias,
+                                      const void* bias_s, void* out, int64_t K, int64_t Nd,
+                                      cudaStream_t s) {
+  if (g.rows_max == 0) return cudaSuccess;
+  SimtGemmArgs a{};
+  a.offsets = g.offsets;
+  a.kept = g.kept;
+  a.n_routed = int32_t(c.n_experts);
+  a.shared_rows = c.d_ff_shared > 0 ? int32_t(c.T) : 0;
+  a.act = -1;
+  a.A = A; a.B = W; a.Bs = Ws; a.bias = bias; a.bias_s = bias_s;
+  a.C = out; a.K = K; a.Nc = Nd;
+  dim3 grid(unsigned(ceil_div(Nd, kSimtBN)), unsigned(ceil_div(g.rows_max, kSimtBM)));
+  return launch_pdl(simt_gemm_kernel<float, float>, grid, dim3(kSimtThreads), 0, s, a);
+}
+
+// out = dOut W[e] per group (the weight as stored, [K, Nd]), times act'(pre)
+// when act >= 0
+cudaError_t launch_bwd_dgrad_f32(const moe_config& c, const BwdGemmArgs& g, const void* dOut,
+                                 const void* W, const void* Ws, int64_t K, int64_t Nd, int act,
+                                 const void* pre, void* out, cudaStream_t s) {
+  if (g.rows_max == 0) return cudaSuccess;
+  SimtGemmArgs a{};
+  a.offsets = g.offsets;
+  a.kept = g.kept;
+  a.n_routed = int32_t(c.n_experts);
+  a.shared_rows = c.d_ff_shared > 0 ? int32_t(c.T) : 0;
+  a.act = -1;
+  a.b_kn = 1;
+  a.dact = act;
+  a.pre = act >= 0 ? pre : nullptr;
+  a.A = dOut; a.B = W; a.Bs = Ws;
+  a.C = out; a.K = K; a.Nc = Nd;
+  dim3 grid(unsigned(ceil_div(Nd, kSimtBN)), unsigned(ceil_div(g.rows_max, kSimtBM)));
+  return launch_pdl(simt_gemm_kernel<float, float>, grid, dim3(kSimtThreads), 0, s, a);
+}
+
+// out[e] = L[group e]^T R[group e] per group ([Md, Nd]; the shared one in out_s)
+cudaError_t launch_bwd_wgrad_f32(const moe_config& c, const BwdGemmArgs& g, const void* Lm,
+                                 int64_t Md, const void* Rm, int64_t Nd, void* out, void* out_s,
+                                 cudaStream_t s) {
+  SimtWgradArgs a{};
+  a.L = Lm; a.R = Rm; a.C = out; a.Cs = out_s; a.Md = Md; a.Nd = Nd;
+  a.offsets = g.offsets;
+  a.kept = g.kept;
+  a.n_routed = int32_t(c.n_experts);
+  a.shared_rows = c.d_ff_shared > 0 ? int32_t(c.T) : 0;
+  const unsigned groups = unsigned(c.n_experts + (c.d_ff_shared > 0 ? 1 : 0));
+  dim3 grid(unsigned(ceil_div(Nd, kSimtBN)), unsigned(ceil_div(Md, kSimtBM)), groups);
+  return launch_pdl(simt_wgrad_kernel<float>, grid, dim3(kSimtThreads), 0, s, a);
+}
+
 }  // namespace moe

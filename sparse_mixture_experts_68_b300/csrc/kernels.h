@@ -230,6 +230,18 @@ int backward_launch_count(const moe_config& c);
 bool router_bwd_on_tensor_cores(const moe_config& c);
 size_t router_bwd_partial_bytes(const moe_config& c);
 
+// fp32 layers: the same three backward GEMMs on CUDA cores (grouped_ffn_f32.cu)
+cudaError_t launch_grouped_linear_f32(const moe_config& c, const BwdGemmArgs& g, const void* A,
+                                      const void* W, const void* Ws, const void* bias,
+                                      const void* bias_s, void* out, int64_t K, int64_t Nd,
+                                      cudaStream_t s);
+cudaError_t launch_bwd_dgrad_f32(const moe_config& c, const BwdGemmArgs& g, const void* dOut,
+                                 const void* W, const void* Ws, int64_t K, int64_t Nd, int act,
+                                 const void* pre, void* out, cudaStream_t s);
+cudaError_t launch_bwd_wgrad_f32(const moe_config& c, const BwdGemmArgs& g, const void* Lm,
+                                 int64_t Md, const void* Rm, int64_t Nd, void* out, void* out_s,
+                                 cudaStream_t s);
+
 // the first Linear without its activation: out = A W^T + b per group (bf16)
 cudaError_t launch_grouped_linear_bf16(const moe_config& c, const GroupedFfnArgs& g,
                                        const void* A, const void* W, const void* Ws,

@@ -25,6 +25,11 @@ struct SimtGemmArgs {
   int32_t n_routed;
   int32_t shared_rows;      // live rows of the shared group (0: none)
   int32_t act;              // -1: none, else MOE_ACT_*
+  // backward: B stored [K, Nc] (the weight as is) instead of [Nc, K], and
+  // the result multiplied by act'(pre[row, col]) when pre is set (no bias)
+  int32_t b_kn;
+  int32_t dact;             // MOE_ACT_* of act' (read only when pre is set)
+  const void* pre;          // [rows, Nc] or nullptr
 };
 
 constexpr int kSimtBM = 64, kSimtBN = 64, kSimtBK = 16, kSimtThreads = 256;
@@ -82,10 +87,21 @@ __global__ void __launch_bounds__(kSimtThreads) simt_gemm_kernel(SimtGemmArgs a)
       const bool ok = r < row_end && kk < a.K;   // K % 4 == 0: 4 values all in or all out
 #pragma unroll
       for (int q = 0; q < 4; ++q) As[lk + q][lr] = ok ? to_f32(A[r * a.K + kk + q]) : 0.f;
-      const int64_t c = col0 + lr;
-      const bool okb = c < a.Nc && kk < a.K;
+      if (a.b_kn) {
+        // B[k, n]: 64 consecutive columns of 4 K-rows per pass of 256 threads
+        const int nn = tid & 63, kq = tid >> 6;
+        const int64_t c = col0 + nn;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) Bs[lk + q][lr] = okb ? to_f32(B[c * a.K + kk + q]) : 0.f;
+        for (int q = 0; q < 4; ++q) {
+          const int64_t kr = k0 + 4 * kq + q;
+          Bs[4 * kq + q][nn] = (c < a.Nc && kr < a.K) ? to_f32(B[kr * a.Nc + c]) : 0.f;
+        }
+      } else {
+        const int64_t c = col0 + lr;
+        const bool okb = c < a.Nc && kk < a.K;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) Bs[lk + q][lr] = okb ? to_f32(B[c * a.K + kk + q]) : 0.f;
+      }
     }
     __syncthreads();
 #pragma unroll
@@ -115,7 +131,78 @@ __global__ void __launch_bounds__(kSimtThreads) simt_gemm_kernel(SimtGemmArgs a)
       float v = acc[i][j];
       if (bias) v += to_f32(bias[c]);
       if (a.act >= 0) v = apply_act(v, a.act);
+      if (a.pre) {
+        const float pa = to_f32(static_cast<const TIn*>(a.pre)[r * a.Nc + c]);
+        v *= a.dact == MOE_ACT_RELU ? (pa > 0.f ? 1.f : 0.f) : gelu_erf_grad(pa);
+      }
       C[r * a.Nc + c] = from_f32<TOut>(v);
+    }
+  }
+}
+
+// Grouped weight gradient on CUDA cores: for group g (blockIdx.z),
+// C_g[m, n] = sum over the group's live rows r of L[r, m] R[r, n]
+// (L [rows, Md], R [rows, Nd], both row-major; C_g [Md, Nd] at C + g Md Nd,
+// the shared group's at Cs).  The K loop covers exactly the live rows.
+struct SimtWgradArgs {
+  const void* L;
+  const void* R;
+  void* C;
+  void* Cs;
+  int64_t Md, Nd;
+  const int32_t* offsets;
+  const int32_t* kept;
+  int32_t n_routed;
+  int32_t shared_rows;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kSimtThreads) simt_wgrad_kernel(SimtWgradArgs a) {
+  __shared__ float Ls[kSimtBK][kSimtBM + 4];
+  __shared__ float Rs[kSimtBK][kSimtBN + 4];
+  pdl_launch_dependents();
+  pdl_wait_previous();
+  const int g = blockIdx.z;
+  const int64_t m0 = int64_t(blockIdx.y) * kSimtBM, n0 = int64_t(blockIdx.x) * kSimtBN;
+  const int64_t r0 = a.offsets[g];
+  const int64_t live = g < a.n_routed ? a.kept[g] : a.shared_rows;
+  const T* L = static_cast<const T*>(a.L);
+  const T* R = static_cast<const T*>(a.R);
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  const int cc = tid & 63, kq = tid >> 6;       // loaders: 64 columns x 4 rows per pass
+  float acc[4][4] = {};
+  for (int64_t k0 = 0; k0 < live; k0 += kSimtBK) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int64_t r = k0 + 4 * kq + q;
+      const bool okr = r < live;
+      Ls[4 * kq + q][cc] = (okr && m0 + cc < a.Md) ? to_f32(L[(r0 + r) * a.Md + m0 + cc]) : 0.f;
+      Rs[4 * kq + q][cc] = (okr && n0 + cc < a.Nd) ? to_f32(R[(r0 + r) * a.Nd + n0 + cc]) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < kSimtBK; ++kk) {
+      float av[4], bv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) av[i] = Ls[kk][ty + 16 * i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) bv[j] = Rs[kk][tx + 16 * j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+  T* C = g < a.n_routed ? static_cast<T*>(a.C) + int64_t(g) * a.Md * a.Nd : static_cast<T*>(a.Cs);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int64_t m = m0 + ty + 16 * i;
+    if (m >= a.Md) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int64_t n = n0 + tx + 16 * j;
+      if (n < a.Nd) C[m * a.Nd + n] = from_f32<T>(acc[i][j]);
     }
   }
 }
