@@ -107,6 +107,11 @@ typedef struct moe_outputs {
   float   *balance;    /* [1] std_unbiased(mean_prob)^2                 required */
   float   *logits;     /* [T, N] router scores z; NULL = keep in workspace      */
   float   *cv_squared; /* [1] var_unbiased(counts) / mean(counts)^2; NULL = skip */
+  void    *pre_act;    /* [moe_rows_max(cfg), d_ff], cfg->dtype: the first Linear's
+                          pre-activation in the grouped row layout, kept for
+                          moe_backward (which then skips recomputing it);
+                          NULL = not kept.  Device memory (moe_forward_host
+                          ignores it). */
 } moe_outputs;
 
 /* ---- sizes --------------------------------------------------------------- */
@@ -299,7 +304,8 @@ typedef struct moe_grads {
 
 /* Bytes of device workspace moe_backward needs; 0 for an invalid config. */
 size_t moe_backward_workspace_size(const moe_config* cfg);
-/* Kernels one moe_backward launches; -1 for an invalid config. */
+/* Kernels one moe_backward launches without a kept pre-activation (one fewer
+ * when the forward kept it in moe_outputs.pre_act); -1 for an invalid config. */
 int32_t moe_backward_launch_count(const moe_config* cfg);
 
 /* The backward pass.  `fwd` and `fwd_workspace` are the outputs and the

@@ -61,7 +61,7 @@ class MoeOutputs(C.Structure):
     _fields_ = [("y", C.c_void_p), ("topk_idx", C.c_void_p), ("topk_w", C.c_void_p),
                 ("counts", C.c_void_p), ("kept", C.c_void_p), ("dropped", C.c_void_p),
                 ("mean_prob", C.c_void_p), ("balance", C.c_void_p), ("logits", C.c_void_p),
-                ("cv_squared", C.c_void_p)]
+                ("cv_squared", C.c_void_p), ("pre_act", C.c_void_p)]
 
 
 class MoeGrads(C.Structure):
@@ -281,15 +281,17 @@ class Outputs:
     balance: torch.Tensor
     logits: torch.Tensor | None = None
     cv_squared: torch.Tensor | None = None
+    pre_act: torch.Tensor | None = None      # kept for moe_backward (grouped rows)
 
     def struct(self) -> MoeOutputs:
         return MoeOutputs(_ptr(self.y), _ptr(self.topk_idx), _ptr(self.topk_w),
                           _ptr(self.counts), _ptr(self.kept), _ptr(self.dropped),
                           _ptr(self.mean_prob), _ptr(self.balance), _ptr(self.logits),
-                          _ptr(self.cv_squared))
+                          _ptr(self.cv_squared), _ptr(self.pre_act))
 
 
-def alloc_outputs(cfg: MoeConfig, device, with_logits=False, pin_memory=False) -> Outputs:
+def alloc_outputs(cfg: MoeConfig, device, with_logits=False, pin_memory=False,
+                  with_pre_act=False) -> Outputs:
     T, k, N, d = cfg.T, cfg.top_k, cfg.n_experts, cfg.d_model
     dt = torch.float32 if cfg.dtype == MOE_F32 else torch.bfloat16
     kw = dict(device=device, pin_memory=pin_memory) if pin_memory else dict(device=device)
@@ -303,7 +305,8 @@ def alloc_outputs(cfg: MoeConfig, device, with_logits=False, pin_memory=False) -
         mean_prob=torch.empty((N,), dtype=torch.float32, **kw),
         balance=torch.empty((1,), dtype=torch.float32, **kw),
         logits=torch.empty((T, N), dtype=torch.float32, **kw) if with_logits else None,
-        cv_squared=torch.empty((1,), dtype=torch.float32, **kw))
+        cv_squared=torch.empty((1,), dtype=torch.float32, **kw),
+        pre_act=torch.empty((rows_max(cfg), cfg.d_ff), dtype=dt, **kw) if with_pre_act else None)
 
 
 def forward(cfg: MoeConfig, x, weights: MoeWeights, out: Outputs, workspace, stream=None):
@@ -421,9 +424,12 @@ class MoeLayer:
         if need > self.workspace.numel():
             self.workspace = torch.empty(need, dtype=torch.uint8, device=self.device)
 
-    def forward(self, x, out: Outputs | None = None, with_logits=False, stream=None) -> Outputs:
+    def forward(self, x, out: Outputs | None = None, with_logits=False, with_pre_act=False,
+                stream=None) -> Outputs:
+        """with_pre_act keeps the first Linear's pre-activation for ``backward``."""
         if out is None:
-            out = alloc_outputs(self.cfg, self.device, with_logits=with_logits)
+            out = alloc_outputs(self.cfg, self.device, with_logits=with_logits,
+                                with_pre_act=with_pre_act)
         forward(self.cfg, x, self.weights, out, self.workspace, stream)
         return out
 

@@ -436,6 +436,7 @@ static moe_status forward_impl(const moe_config* cfg, const void* x, const moe_w
     if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
   if (!out->dropped || !out->mean_prob || !out->balance) return MOE_ERR_INVALID_ARG;
   if (out->logits && !aligned16(out->logits)) return MOE_ERR_INVALID_ARG;
+  if (out->pre_act && !aligned16(out->pre_act)) return MOE_ERR_INVALID_ARG;
   Workspace ws = layout(c, workspace);
   if (workspace_bytes < ws.bytes) return MOE_ERR_WORKSPACE;
   DeviceInfo di;
@@ -465,6 +466,7 @@ static moe_status forward_impl(const moe_config* cfg, const void* x, const moe_w
     a.Yp = ws.Yp; a.rows_max = rows_max_of(c); a.status = di.status;
     a.wait_limit_ns = g_wait_limit_ns.load(); a.num_sms = di.num_sms;
     a.mid_event = ev[3];
+    a.pre_out = out->pre_act;
     e = c.dtype == MOE_F32 ? launch_grouped_ffn_f32(c, a, s) : launch_grouped_ffn_bf16(c, a, s);
   }
   if (e == cudaSuccess) e = record_event(ev[4], s);
@@ -546,6 +548,7 @@ moe_status moe_forward_host(const moe_config* cfg, const void* x_host, const moe
   od.balance = static_cast<float*>(take(4));
   od.logits = oh->logits ? static_cast<float*>(take(lb)) : nullptr;
   od.cv_squared = oh->cv_squared ? static_cast<float*>(take(4)) : nullptr;
+  od.pre_act = nullptr;                              // device-only: not kept here
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (xb && cudaMemcpyAsync(xd, x_host, xb, cudaMemcpyHostToDevice, s) != cudaSuccess)
     return MOE_ERR_CUDA;
@@ -620,7 +623,11 @@ static moe_status backward_impl(const moe_config* cfg, const void* x, const moe_
   a.token_row = fws.token_row; a.topk_idx = fwd->topk_idx; a.topk_w = fwd->topk_w;
   a.logits = fwd->logits ? fwd->logits : fws.logits; a.mean_prob = fwd->mean_prob;
   a.aux_weight = aux_weight;
-  a.dO = ws.dO; a.A1 = ws.A1; a.dA = ws.dA; a.dXp = ws.dXp;
+  a.dO = ws.dO; a.dA = ws.dA; a.dXp = ws.dXp;
+  // the forward's kept pre-activation, else recomputed into the workspace
+  if (fwd->pre_act && !aligned16(fwd->pre_act)) return MOE_ERR_INVALID_ARG;
+  a.A1 = fwd->pre_act ? fwd->pre_act : ws.A1;
+  a.recompute_A1 = fwd->pre_act == nullptr;
   a.dz = grads->dz ? grads->dz : ws.dz;
   a.dw = grads->dw ? grads->dw : ws.dw;
   a.dxr = ws.dxr;

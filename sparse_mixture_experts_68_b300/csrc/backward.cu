@@ -499,8 +499,11 @@ cudaError_t backward_t(const moe_config& c, const BackwardArgs& a, void* const* 
   bg.offsets = a.offsets; bg.kept = a.kept; bg.rows_max = a.rows_max; bg.status = a.status;
   bg.wait_limit_ns = a.wait_limit_ns; bg.num_sms = a.num_sms;
   cudaError_t e;
-  // A1 = Xp W1^T + b1 (the pre-activation, recomputed)
-  e = kBf16 ? launch_grouped_linear_bf16(c, ga, a.Xp, w->W1, w->W1s, w->b1, w->b1s, a.A1, d, f, s)
+  // A1 = Xp W1^T + b1 (the pre-activation), unless the forward kept it
+  e = cudaSuccess;
+  if (a.recompute_A1)
+    e = kBf16
+            ? launch_grouped_linear_bf16(c, ga, a.Xp, w->W1, w->W1s, w->b1, w->b1s, a.A1, d, f, s)
             : launch_grouped_linear_f32(c, bg, a.Xp, w->W1, w->W1s, w->b1, w->b1s, a.A1, d, f, s);
   if (e == cudaSuccess) e = record_event(ev[2], s);
   if (e != cudaSuccess) return e;

@@ -23,6 +23,13 @@ cudaError_t launch_grouped_ffn_f32(const moe_config& c, const GroupedFfnArgs& g,
   a.C = g.H; a.K = c.d_model; a.Nc = c.d_ff;
   dim3 grid1(unsigned(ceil_div(c.d_ff, kSimtBN)), unsigned(ceil_div(g.rows_max, kSimtBM)));
   cudaError_t e = launch_pdl(simt_gemm_kernel<float, float>, grid1, dim3(kSimtThreads), 0, s, a);
+  if (e == cudaSuccess && g.pre_out) {
+    // the pre-activation for a later backward: the same Linear without it
+    SimtGemmArgs pa = a;
+    pa.act = -1;
+    pa.C = g.pre_out;
+    e = launch_pdl(simt_gemm_kernel<float, float>, grid1, dim3(kSimtThreads), 0, s, pa);
+  }
   if (e == cudaSuccess) e = record_event(g.mid_event, s);
   if (e != cudaSuccess) return e;
   // second Linear: [rows, d_ff] x [d, d_ff]^T

@@ -86,6 +86,9 @@ struct TcParams {
                                    // one group of dense_rows rows starting at row 0
   const int32_t* kept;             // [n_routed] live rows of each routed group
   const __nv_bfloat16* pre;        // dgrad epilogues: the pre-activation [rows, Nd]
+  // first Linear with an activation, staged tiles: also store the
+  // pre-activation (bias added, before the activation) here, [rows, Nd]
+  void* out_pre;
   const __nv_bfloat16* bias;       // [n_routed, Nd]
   const __nv_bfloat16* bias_s;     // [Nd] shared expert
   void* out;                       // [rows, Nd], bf16 (fp32 for EPI_BIAS_F32)
@@ -432,6 +435,13 @@ __global__ void __launch_bounds__(CFG::THREADS, MINB)
             uint4 w[2];
             epilogue_words<EPI, 16>(r + 16 * h, bias + col + 16 * h, w);
             warp_staged_store<16>(w, stg, lane, out0 + 16 * h, p.Nd, live - row_base);
+            if (EPI != EPI_BIAS && p.out_pre) {
+              epilogue_words<EPI_BIAS, 16>(r + 16 * h, bias + col + 16 * h, w);
+              warp_staged_store<16>(w, stg, lane,
+                                    static_cast<__nv_bfloat16*>(p.out_pre) +
+                                        (out0 - static_cast<__nv_bfloat16*>(p.out)) + 16 * h,
+                                    p.Nd, live - row_base);
+            }
           }
         } else if (valid) {
           epilogue_store<EPI, CW>(r, bias + col,
@@ -788,6 +798,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CFG::THREADS, 1)
             uint4 w[2];
             epilogue_words<EPI, 16>(r + 16 * h, bias + col + 16 * h, w);
             warp_staged_store<16>(w, stg, lane, out0 + 16 * h, p.Nd, live - row_base);
+            if (EPI != EPI_BIAS && p.out_pre) {
+              epilogue_words<EPI_BIAS, 16>(r + 16 * h, bias + col + 16 * h, w);
+              warp_staged_store<16>(w, stg, lane,
+                                    static_cast<__nv_bfloat16*>(p.out_pre) +
+                                        (out0 - static_cast<__nv_bfloat16*>(p.out)) + 16 * h,
+                                    p.Nd, live - row_base);
+            }
           }
         } else if (valid) {
           epilogue_store<EPI, CW>(r, bias + col,
@@ -1198,10 +1215,12 @@ int swap_rows(int64_t Nd, int64_t rows_per_group, int epi) {
 }
 
 // One grouped Linear: out[group g] = epi(A[group g] . W[g]^T + bias[g]).
+// out_pre: with an activation epilogue, also store the pre-activation there
+// (only on the staged tile families; see linear_saves_pre).
 cudaError_t grouped_linear(const moe_config& c, const GroupedFfnArgs& g, const void* A,
                            const void* W, const void* Ws, const void* bias,
                            const void* bias_s, void* out, int64_t K, int64_t Nd, int epi,
-                           cudaStream_t s) {
+                           cudaStream_t s, void* out_pre = nullptr) {
   const int64_t groups = c.n_experts + (c.d_ff_shared > 0 ? 1 : 0);
   const int64_t routed = g.routed_rows > 0 ? g.routed_rows : c.T * c.top_k;
   const int64_t rows = routed + (c.d_ff_shared > 0 ? c.T : 0);
@@ -1262,6 +1281,7 @@ cudaError_t grouped_linear(const moe_config& c, const GroupedFfnArgs& g, const v
   p.num_kb = int32_t(K / BK);
   p.status = g.status;
   p.wait_limit_ns = g.wait_limit_ns;
+  p.out_pre = out_pre;
   // upper bound on the tiles (every group may add one partial m-tile)
   const int64_t max_tiles =
       (ceil_div(g.rows_max, tile_rows(choice)) + groups) * (Nd / bn);
@@ -1319,12 +1339,29 @@ cudaError_t launch_bwd_dgrad_pair(const moe_config& c, const BwdGemmArgs& g, con
   return launch_pair<Cfg256Pair, EPI_DGRAD_GELU>(mA, mB, mBs, p, max_tiles, g.num_sms, s);
 }
 
+// Whether the first Linear's epilogue can also store its pre-activation: the
+// staged single-CTA and CTA-pair tiles can, the decode (swap) tiles and the
+// two-CTAs-per-SM tiles cannot.
+bool linear_saves_pre(const moe_config& c) {
+  const int epi1 = c.act == MOE_ACT_RELU ? EPI_BIAS_RELU : EPI_BIAS_GELU;
+  const int64_t groups = c.n_experts + (c.d_ff_shared > 0 ? 1 : 0);
+  const int64_t rows = c.T * c.top_k + (c.d_ff_shared > 0 ? c.T : 0);
+  return swap_rows(c.d_ff, rows / groups, epi1) == 0 &&
+         pick_tile(c.d_ff, rows / groups, c.d_model) != TILE_128_2CTA;
+}
+
 cudaError_t launch_grouped_ffn_bf16(const moe_config& c, const GroupedFfnArgs& g,
                                     cudaStream_t s) {
   if (g.rows_max == 0) return cudaSuccess;
   const int epi1 = c.act == MOE_ACT_RELU ? EPI_BIAS_RELU : EPI_BIAS_GELU;
+  // the pre-activation for a later backward: from the epilogue, or else by a
+  // second pass of the first Linear without its activation
+  const bool in_epi = g.pre_out && linear_saves_pre(c);
   cudaError_t e = grouped_linear(c, g, g.Xp, g.w->W1, g.w->W1s, g.w->b1, g.w->b1s, g.H,
-                                 c.d_model, c.d_ff, epi1, s);
+                                 c.d_model, c.d_ff, epi1, s, in_epi ? g.pre_out : nullptr);
+  if (e == cudaSuccess && g.pre_out && !in_epi)
+    e = grouped_linear(c, g, g.Xp, g.w->W1, g.w->W1s, g.w->b1, g.w->b1s, g.pre_out, c.d_model,
+                       c.d_ff, EPI_BIAS, s);
   if (e == cudaSuccess) e = record_event(g.mid_event, s);
   if (e != cudaSuccess) return e;
   return grouped_linear(c, g, g.H, g.w->W2, g.w->W2s, g.w->b2, g.w->b2s, g.Yp, c.d_ff,

@@ -132,7 +132,12 @@ struct GroupedFfnArgs {
   int num_sms;
   void* mid_event;          // cudaEvent_t recorded between the two Linears, or nullptr
   int64_t routed_rows;      // live routed rows for the tile heuristics; 0: T * top_k
+  void* pre_out;            // [rows_max, d_ff]: also keep the first Linear's
+                            // pre-activation (for the backward), or nullptr
 };
+// whether the bf16 first Linear stores its pre-activation from its epilogue
+// (else a second pass does)
+bool linear_saves_pre(const moe_config& c);
 
 // Records a caller's event on s (as an external node while s is capturing).
 cudaError_t record_event(void* event, cudaStream_t s);
@@ -207,7 +212,8 @@ struct BackwardArgs {
   float aux_weight;
   // backward scratch
   void* dO;                 // [rows_max, d]
-  void* A1;                 // [rows_max, d_ff]
+  void* A1;                 // [rows_max, d_ff] the first Linear's pre-activation
+  bool recompute_A1;        // false: A1 holds the forward's kept pre-activation
   void* dA;                 // [rows_max, d_ff]
   void* dXp;                // [rows_max, d]
   float* dz;                // [T, N]

@@ -223,3 +223,30 @@ def test_training_step_graph_replay_matches_eager():
     for n in ("dx", "dW_g", "db_g", "dW1", "db1", "dW2", "db2", "dW1s", "db1s", "dW2s", "db2s",
               "dz", "dw"):
         assert torch.equal(getattr(g2, n), getattr(g_eager, n)), n
+
+
+KEEP_PRE = [
+    SMALL[0],                                    # 128 x 256 tiles: from the epilogue
+    SMALL[1],                                    # 64-wide tiles, shared expert
+    Workload("bwd_keep_decode", T=40, d_model=256, d_ff=384, n_experts=8, top_k=1,
+             act=ACT_GELU_ERF, dtype=DT_BF16, seed=89),   # decode tiles: a second pass
+    Workload("bwd_keep_f32", T=120, d_model=64, d_ff=96, n_experts=4, top_k=2,
+             act=ACT_RELU, dtype=DT_F32, seed=90),        # CUDA cores: a second pass
+]
+
+
+@pytest.mark.parametrize("wl", KEEP_PRE, ids=[w.name for w in KEEP_PRE])
+def test_kept_pre_activation_gives_the_same_gradients(wl):
+    """A forward that keeps the first Linear's pre-activation gives the same
+    outputs, and the backward that uses it (no recompute) the same gradients,
+    bit for bit, as the forward / backward without it."""
+    t, layer, out, dy, g_plain = run_backward(wl, 0.01)
+    out_k = layer.forward(t["x"], with_logits=True, with_pre_act=True)
+    g_kept = layer.backward(t["x"], out_k, dy, aux_weight=0.01, with_scores=True)
+    torch.cuda.synchronize()
+    assert torch.equal(out_k.y, out.y)
+    for n in ("dx", "dW_g", "db_g", "dW1", "db1", "dW2", "db2", "dz", "dw"):
+        assert torch.equal(getattr(g_kept, n), getattr(g_plain, n)), n
+    if wl.d_ff_shared:
+        for n in ("dW1s", "db1s", "dW2s", "db2s"):
+            assert torch.equal(getattr(g_kept, n), getattr(g_plain, n)), n
