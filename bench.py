@@ -64,6 +64,12 @@ def peaks():
             "source": "fallback"}
 
 
+# fp32 layers run their GEMMs on the CUDA cores (FFMA): 148 SMs x 128 fp32 lanes x
+# 2 flop per FFMA x the 2032 MHz maximum SM clock
+F32_ALU_TFLOPS = 148 * 128 * 2 * 2032e6 / 1e12
+F32_ALU_SOURCE = "derived: 148 SMs x 128 fp32 lanes x 2 flop (FFMA) x 2032 MHz"
+
+
 # ---------------------------------------------------------------------------------------
 # DRAM traffic of the dominant kernel, from the committed ncu summary
 
@@ -456,7 +462,11 @@ def run_ours(args, wl, rank, world, local_rank):
     ffn_ms = mean_stage["ffn_linear1"] + mean_stage["ffn_linear2"]
     launches = 2
     ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
-    if (2 * f1) / (b1 + b2) >= ridge:  # the two Linears are tensor-bound
+    if wl.dtype != 1:                   # fp32: FFMA on the CUDA cores
+        achieved = 2 * f1 / launches / (ffn_ms / launches * 1e-3) / 1e12
+        roof = {"bound": "alu", "achieved": achieved, "peak": F32_ALU_TFLOPS,
+                "unit": "TFLOP/s"}
+    elif (2 * f1) / (b1 + b2) >= ridge:  # the two Linears are tensor-bound
         achieved = 2 * f1 / launches / (ffn_ms / launches * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
                 "unit": "TFLOP/s"}
@@ -466,8 +476,12 @@ def run_ours(args, wl, rank, world, local_rank):
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"], roof["traffic_source"] = profiled_traffic(wl.name)
     roof["algorithmic_bytes_per_launch"] = (b1 + b2) / launches
-    roof["kernel"] = "tc_grouped_gemm_kernel (two launches per step: Linear 1, Linear 2)"
-    roof["peak_source"] = pk["source"] + " (burst)"
+    if wl.dtype != 1:
+        roof["kernel"] = "simt_gemm_kernel (two launches per step: Linear 1, Linear 2)"
+        roof["peak_source"] = F32_ALU_SOURCE
+    else:
+        roof["kernel"] = "tc_grouped_gemm_kernel (two launches per step: Linear 1, Linear 2)"
+        roof["peak_source"] = pk["source"] + " (burst)"
     roof["per_launch"] = {
         "linear1": {"ms": mean_stage["ffn_linear1"], "flop": f1, "bytes": b1,
                     "tflops": f1 / (mean_stage["ffn_linear1"] * 1e-3) / 1e12,
@@ -599,7 +613,7 @@ def run_train(args, wl, rank, world, local_rank):
         bwd_stage.append([bev[j].elapsed_time(bev[j + 1]) for j in range(7)])
     assert B.get_device_status() == B.MOE_OK
     fnames = STAGES
-    bnames = ("gate_and_padding", "recompute_A1", "dgrad_dA", "dgrad_dXp", "wgrad_dW2",
+    bnames = ("gate", "recompute_A1", "dgrad_dA", "dgrad_dXp", "wgrad_dW2",
               "wgrad_dW1", "bias_router_dx")        # recompute_A1: ~0, the forward kept A1
     fmean = {n: statistics.mean(s[i] for s in fwd_stage) for i, n in enumerate(fnames)}
     bmean = {n: statistics.mean(s[i] for s in bwd_stage) for i, n in enumerate(bnames)}
@@ -622,7 +636,10 @@ def run_train(args, wl, rank, world, local_rank):
     launches = len(gemm_names)
     gemm_bytes = launches * (wbytes + act)
     ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
-    if gemm_flop * launches / gemm_bytes >= ridge:
+    if wl.dtype != 1:                   # fp32: FFMA on the CUDA cores
+        ach = gemm_flop * launches / (gemm_ms * 1e-3) / 1e12
+        roof = {"bound": "alu", "achieved": ach, "peak": F32_ALU_TFLOPS, "unit": "TFLOP/s"}
+    elif gemm_flop * launches / gemm_bytes >= ridge:
         ach = gemm_flop * launches / (gemm_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"], "unit": "TFLOP/s"}
     else:
@@ -631,10 +648,16 @@ def run_train(args, wl, rank, world, local_rank):
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = None
     roof["traffic_source"] = "no ncu summary for the training step"
-    roof["kernel"] = ("tcgen05 grouped GEMMs: tc_grouped_gemm_kernel / tc2_grouped_gemm_kernel "
-                      "(forward Linear 1 keeping its pre-activation, Linear 2; dgrads on CTA "
-                      "pairs) and tc_bwd_gemm_kernel (dgrads, wgrads)")
-    roof["peak_source"] = pk["source"] + " (burst)"
+    if wl.dtype != 1:
+        roof["kernel"] = ("CUDA-core GEMMs: simt_gemm_kernel (forward Linears, dgrads) and "
+                          "simt_wgrad_kernel (wgrads)")
+        roof["peak_source"] = F32_ALU_SOURCE
+    else:
+        roof["kernel"] = ("tcgen05 grouped GEMMs: tc_grouped_gemm_kernel / "
+                          "tc2_grouped_gemm_kernel (forward Linear 1 keeping its "
+                          "pre-activation, Linear 2; dgrads on CTA pairs) and "
+                          "tc_bwd_gemm_kernel (dgrads, wgrads)")
+        roof["peak_source"] = pk["source"] + " (burst)"
     roof["per_launch"] = {n: {"ms": ms, "tflops": gemm_flop / (ms * 1e-3) / 1e12}
                           for n, ms in gemm_names}
     train_flop = 6.0 * gemm_flop + 3 * 2.0 * T * wl.d_model * wl.n_experts
@@ -642,7 +665,7 @@ def run_train(args, wl, rank, world, local_rank):
         "metric": TRAIN_METRIC, "value": job_tokens_per_s(T, K, world, total_ms),
         "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": "bf16" if wl.dtype == 1 else "f32", "data": "synthetic",
         "config": {"workload": wl.name, "description": wl.description, "T": T,
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "aux_weight": AUX_WEIGHT,

@@ -311,8 +311,9 @@ int32_t moe_backward_launch_count(const moe_config* cfg);
 /* The backward pass.  `fwd` and `fwd_workspace` are the outputs and the
  * workspace of the moe_forward call on the same cfg, x and weights (the
  * backward reads the saved grouping, the expert rows Xp, H and Yp, the
- * scores, gates and mean_prob from them, and zeroes the padding rows of Xp
- * and H in fwd_workspace).  dy [T, d_model] in the layer dtype.  `workspace`
+ * scores, gates and mean_prob from them; it writes nothing there; padding
+ * rows of the grouped buffers are never read as data).  dy [T, d_model] in
+ * the layer dtype.  `workspace`
  * (device, >= moe_backward_workspace_size(cfg) bytes, 256-byte aligned) holds
  * the backward's intermediates. */
 moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights* w,
@@ -324,7 +325,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
  * the step boundaries (kernels not overlapping their neighbours):
  *   events[0] start                     events[4] after dXp = dA W1
  *   events[1] after the gate step       events[5] after dW2 = dO^T H
- *             and the padding zeroing   events[6] after dW1 = dA^T Xp
+ *                                       events[6] after dW1 = dA^T Xp
  *   events[2] after the recomputed A1   events[7] after the bias sums, the
  *   events[3] after dA = (dO W2) act'(A1)         router gradients and dx
  * A NULL entry is skipped. */

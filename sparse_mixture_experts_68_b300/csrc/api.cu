@@ -102,6 +102,7 @@ struct BwdWorkspace {
   void* dxr_bf;
   int32_t* rgrp;
   float* part;
+  float* bpart;
   size_t bytes;
 };
 
@@ -127,6 +128,7 @@ BwdWorkspace bwd_layout(const moe_config& c, void* base) {
   w.dxr_bf = take(size_t(round_up(c.T, kGroupAlign) * c.d_model) * 2);
   w.rgrp = static_cast<int32_t*>(take(16));
   w.part = static_cast<float*>(take(router_bwd_partial_bytes(c)));
+  w.bpart = static_cast<float*>(take(bias_partial_bytes(c, rows)));
   w.bytes = off;
   return w;
 }
@@ -635,6 +637,7 @@ static moe_status backward_impl(const moe_config* cfg, const void* x, const moe_
   a.dxr_bf = ws.dxr_bf;
   a.rgrp = ws.rgrp;
   a.part = ws.part;
+  a.bpart = ws.bpart;
   a.rows_max = rows_max_of(c);
   a.status = di.status; a.wait_limit_ns = g_wait_limit_ns.load(); a.num_sms = di.num_sms;
   return cuda_status(launch_backward(c, a, events, static_cast<cudaStream_t>(stream)));

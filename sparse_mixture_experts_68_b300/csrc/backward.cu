@@ -30,31 +30,6 @@
 namespace moe {
 namespace {
 
-// ---- zero the padding rows of grouped buffers ------------------------------------------
-
-struct PadBufs {
-  void* buf[3];
-  int64_t vec16[3];          // 16-byte words per row
-  int n;
-};
-
-// Blocks (g, y): rows offsets[g] + live_g + y, + gridDim.y, ... below offsets[g + 1].
-__global__ void __launch_bounds__(256)
-    zero_pad_rows_kernel(const int32_t* __restrict__ offsets, const int32_t* __restrict__ kept,
-                         int n_routed, int shared_rows, PadBufs b) {
-  pdl_launch_dependents();
-  pdl_wait_previous();
-  const int g = blockIdx.x;
-  const int64_t live = g < n_routed ? kept[g] : shared_rows;
-  const int64_t r1 = offsets[g + 1];
-  for (int64_t r = offsets[g] + live + blockIdx.y; r < r1; r += gridDim.y)
-    for (int i = 0; i < b.n; ++i) {
-      const int64_t nv = b.vec16[i];
-      uint4* row = static_cast<uint4*>(b.buf[i]) + r * nv;
-      for (int64_t j = threadIdx.x; j < nv; j += blockDim.x) row[j] = make_uint4(0, 0, 0, 0);
-    }
-}
-
 // ---- gate step ------------------------------------------------------------------------
 
 constexpr int kGateWarps = 8;
@@ -82,11 +57,33 @@ __global__ void __launch_bounds__(kGateWarps * 32)
                     int T, int64_t d, int N, int k, int renorm, int has_shared, float aux,
                     E* __restrict__ dO, float* __restrict__ dz_out,
                     float* __restrict__ dw_out, __nv_bfloat16* __restrict__ dz_bf,
-                    int32_t* __restrict__ rgrp) {
+                    int32_t* __restrict__ rgrp, const int32_t* __restrict__ kept,
+                    E* __restrict__ H, E* __restrict__ Xp, int64_t f, int pad_groups) {
   extern __shared__ float gsm[];
   pdl_launch_dependents();
   pdl_wait_previous();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tok_blocks = (T + kGateWarps - 1) / kGateWarps;
+  if (int(blockIdx.x) >= tok_blocks) {
+    // blocks past the tokens: group g's padding rows [live, round_up(live, 16))
+    // of dO, H and Xp -> 0, the rows the tensor-core wgrads' last K step reads
+    const int g = int(blockIdx.x) - tok_blocks;
+    if (g >= pad_groups) return;
+    const int64_t live = g < N ? kept[g] : T;
+    const int64_t r0 = int64_t(offsets[g]) + live, r1 = int64_t(offsets[g]) + (live + 15) / 16 * 16;
+    const int64_t nd = d * int64_t(sizeof(E)) / 16, nf = f * int64_t(sizeof(E)) / 16;
+    for (int64_t r = r0; r < r1; ++r) {
+      uint4* a = reinterpret_cast<uint4*>(dO + r * d);
+      uint4* b = reinterpret_cast<uint4*>(Xp + r * d);
+      uint4* c = reinterpret_cast<uint4*>(H + r * f);
+      for (int64_t j = threadIdx.x; j < nd; j += blockDim.x) {
+        a[j] = make_uint4(0, 0, 0, 0);
+        b[j] = make_uint4(0, 0, 0, 0);
+      }
+      for (int64_t j = threadIdx.x; j < nf; j += blockDim.x) c[j] = make_uint4(0, 0, 0, 0);
+    }
+    return;
+  }
   if (rgrp && blockIdx.x == 0 && threadIdx.x == 0) {
     // the router's tensor-core GEMMs see one group of T rows
     const int32_t tp = (T + 127) / 128 * 128;
@@ -182,29 +179,67 @@ __global__ void __launch_bounds__(kGateWarps * 32)
 }
 
 // ---- column sums of groups (bias gradients) -----------------------------------------------
+//
+// db2[g] = sum of dO's live rows of group g, db1[g] the same over dA.  Groups
+// start on 128-row boundaries, so each 128-row chunk of the grouped row space
+// lies in one group.  Pass 1: block (c, y) sums chunk c's live rows over one
+// column block (32 lanes x one 16-byte word) of dO (y < the dO column
+// blocks) or of dA; its eight warps take every eighth row and combine in order;
+// fp32 partials part[c][col], col over dO's d then dA's f columns.  Pass 2:
+// each output sums its group's chunks in order.  Rows past a group's live rows
+// (padding, never read) do not enter.
+constexpr int kChunkRows = MOE_GROUP_ALIGN;
 
-// Block (g, chunk): columns chunk*32V .. +32V-1 of group g's live rows (V
-// elements per 16-byte word); eight warps take every eighth row, lanes one word
-// each; warps combine in order.
 template <typename T>
 __global__ void __launch_bounds__(256)
-    group_colsum_kernel(const T* __restrict__ src, int64_t width,
-                        const int32_t* __restrict__ offsets, const int32_t* __restrict__ kept,
-                        int n_routed, int shared_rows, T* __restrict__ out, T* __restrict__ out_s) {
+    colsum_partial_kernel(const T* __restrict__ m2, int64_t w2, const T* __restrict__ m1,
+                          int64_t w1, const int32_t* __restrict__ offsets,
+                          const int32_t* __restrict__ kept, int n_routed, int shared_rows,
+                          int n_groups, float* __restrict__ part) {
   constexpr int V = Vec16<T>::n;
-  __shared__ float part[8][32 * V];
+  __shared__ float red[8][32 * V];
+  __shared__ int s_live;
   pdl_launch_dependents();
   pdl_wait_previous();
-  const int g = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t c0 = int64_t(blockIdx.y) * 32 * V + lane * V;
-  const int64_t live = g < n_routed ? kept[g] : shared_rows;
-  const int64_t r0 = offsets[g];
+  const int64_t r0 = int64_t(blockIdx.x) * kChunkRows;
+  if (threadIdx.x == 0) {
+    int nl = 0;
+    if (r0 < offsets[n_groups]) {
+      int lo = 0, hi = n_groups - 1;            // the last group starting at or before r0
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (offsets[mid] <= r0) lo = mid; else hi = mid - 1;
+      }
+      const int64_t live = lo < n_routed ? kept[lo] : shared_rows;
+      const int64_t n = int64_t(offsets[lo]) + live - r0;
+      nl = int(n < 0 ? 0 : (n > kChunkRows ? kChunkRows : n));
+    }
+    s_live = nl;
+  }
+  __syncthreads();
+  const int nlive = s_live;
+  const int64_t cb2 = (w2 + 32 * V - 1) / (32 * V);
+  const bool second = blockIdx.y >= cb2;
+  const T* src = second ? m1 : m2;
+  const int64_t width = second ? w1 : w2;
+  const int64_t cblk = second ? blockIdx.y - cb2 : blockIdx.y;
+  const int64_t c0 = cblk * 32 * V + lane * V;
   float acc[V];
 #pragma unroll
   for (int i = 0; i < V; ++i) acc[i] = 0.f;
   if (c0 < width) {
-    for (int64_t r = warp; r < live; r += 8) {
+    int r = warp;
+    for (; r + 24 < nlive; r += 32) {            // four rows in flight per lane
+      float v[4][V];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) Vec16<T>::load(src + (r0 + r + 8 * u) * width + c0, v[u]);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc[i] += v[u][i];
+    }
+    for (; r < nlive; r += 8) {
       float v[V];
       Vec16<T>::load(src + (r0 + r) * width + c0, v);
 #pragma unroll
@@ -212,38 +247,76 @@ __global__ void __launch_bounds__(256)
     }
   }
 #pragma unroll
-  for (int i = 0; i < V; ++i) part[warp][lane * V + i] = acc[i];
+  for (int i = 0; i < V; ++i) red[warp][lane * V + i] = acc[i];
   __syncthreads();
+  float* dst = part + int64_t(blockIdx.x) * (w2 + w1) + (second ? w2 : 0);
   for (int col = threadIdx.x; col < 32 * V; col += blockDim.x) {
-    const int64_t cc = int64_t(blockIdx.y) * 32 * V + col;
+    const int64_t cc = cblk * 32 * V + col;
     if (cc < width) {
-      float s = 0.f;
-      for (int w = 0; w < 8; ++w) s += part[w][col];
-      T* dst = g < n_routed ? out + int64_t(g) * width : out_s;
-      dst[cc] = from_f32<T>(s);
+      float sum = 0.f;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) sum += red[w][col];
+      dst[cc] = sum;
     }
   }
 }
 
-// db_g[e] = sum_t dz[t, e] (fp32 in, bf16 out): block b takes experts
-// 32 b .. 32 b + 31 (one per lane), its eight warps every eighth token, and
-// the warps combine in order.
-template <typename TO>
+template <typename T>
 __global__ void __launch_bounds__(256)
+    colsum_reduce_kernel(const float* __restrict__ part, int64_t w2, int64_t w1,
+                         const int32_t* __restrict__ offsets, int n_routed, int n_groups,
+                         T* __restrict__ db2, T* __restrict__ db2s, T* __restrict__ db1,
+                         T* __restrict__ db1s) {
+  pdl_launch_dependents();
+  pdl_wait_previous();
+  const int64_t W = w2 + w1;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n_groups * W;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    const int g = int(i / W);
+    const int64_t col = i - int64_t(g) * W;
+    const int c0 = offsets[g] / kChunkRows, c1 = offsets[g + 1] / kChunkRows;
+    float v[4] = {0.f, 0.f, 0.f, 0.f};          // chunks c0 + 4j + u, combined in order
+    int c = c0;
+    for (; c + 3 < c1; c += 4) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] += part[int64_t(c + u) * W + col];
+    }
+    for (; c < c1; ++c) v[0] += part[int64_t(c) * W + col];
+    const float sum = (v[0] + v[1]) + (v[2] + v[3]);
+    if (col < w2) (g < n_routed ? db2 + int64_t(g) * w2 : db2s)[col] = from_f32<T>(sum);
+    else (g < n_routed ? db1 + int64_t(g) * w1 : db1s)[col - w2] = from_f32<T>(sum);
+  }
+}
+
+// db_g[e] = sum_t dz[t, e] (fp32 in): block b takes experts 32 b .. 32 b + 31
+// (one per lane), its 32 warps every 32nd token with four tokens in flight,
+// and the warps combine in order.
+constexpr int kBiasWarps = 32;
+
+template <typename TO>
+__global__ void __launch_bounds__(kBiasWarps * 32)
     router_bias_grad_kernel(const float* __restrict__ dz, int T, int N, TO* __restrict__ db_g) {
-  __shared__ float part[8][32];
+  __shared__ float part[kBiasWarps][32];
   pdl_launch_dependents();
   pdl_wait_previous();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x * 32 + lane;
   float s = 0.f;
-  if (e < N)
-    for (int t = warp; t < T; t += 8) s += dz[int64_t(t) * N + e];
+  if (e < N) {
+    int t = warp;
+    for (; t + 3 * kBiasWarps < T; t += 4 * kBiasWarps) {
+      float v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = dz[int64_t(t + u * kBiasWarps) * N + e];
+      s += (v[0] + v[1]) + (v[2] + v[3]);
+    }
+    for (; t < T; t += kBiasWarps) s += dz[int64_t(t) * N + e];
+  }
   part[warp][lane] = s;
   __syncthreads();
   if (warp == 0 && e < N) {
     float v = 0.f;
-    for (int w = 0; w < 8; ++w) v += part[w][lane];
+    for (int w = 0; w < kBiasWarps; ++w) v += part[w][lane];
     db_g[e] = from_f32<TO>(v);
   }
 }
@@ -327,39 +400,197 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// ---- router gradients for few experts (N <= 32) on CUDA cores -----------------------------------
+//
+// dW_g[e, i] = sum_t dz[t, e] x[t, i] and db_g[e] = sum_t dz[t, e].  Block
+// (cb, z): tokens [z*tc, (z+1)*tc), columns cb*256*CPT ...; each thread keeps
+// NMAX x CPT accumulators for its CPT columns (NMAX * CPT <= 64, experts
+// n..NMAX-1 read zeros); the chunk's dz rows are staged in shared memory.
+// Partial sums per chunk, summed afterwards in chunk order
+// (splitk_reduce2_kernel): [S][n*d] for dW_g, then [S][n] for db_g.
+constexpr int kRouterSmallMaxN = 32;
+constexpr int kRouterSmallRows = 64;            // dz rows staged per pass
+
+template <typename T, int NMAX, int CPT>
+__global__ void __launch_bounds__(256)
+    router_grad_small_kernel(const float* __restrict__ dz, const T* __restrict__ x, int Ttok,
+                             int n, int64_t d, int tc, float* __restrict__ part) {
+  __shared__ float dzs[kRouterSmallRows][NMAX];
+  pdl_launch_dependents();
+  for (int i = threadIdx.x; i < kRouterSmallRows * NMAX; i += 256) (&dzs[0][0])[i] = 0.f;
+  pdl_wait_previous();
+  const int z = blockIdx.y, S = gridDim.y;
+  const int t0 = z * tc, t1 = min(Ttok, t0 + tc);
+  const int64_t col0 = (int64_t(blockIdx.x) * 256 + threadIdx.x) * CPT;
+  float acc[NMAX][CPT];
+#pragma unroll
+  for (int e = 0; e < NMAX; ++e)
+#pragma unroll
+    for (int j = 0; j < CPT; ++j) acc[e][j] = 0.f;
+  float bacc = 0.f;                               // db_g: thread e < n of block x = 0
+  for (int tb = t0; tb < t1; tb += kRouterSmallRows) {
+    const int nr = min(kRouterSmallRows, t1 - tb);
+    __syncthreads();
+    for (int i = threadIdx.x; i < nr * n; i += 256) dzs[i / n][i % n] = dz[int64_t(tb) * n + i];
+    __syncthreads();
+    if (blockIdx.x == 0 && threadIdx.x < n)
+      for (int rr = 0; rr < nr; ++rr) bacc += dzs[rr][threadIdx.x];
+    if (col0 < d) {
+      // four rows of x in flight (past nr: the last row again, weighted 0)
+      for (int rr = 0; rr < nr; rr += 4) {
+        float xv[4][CPT];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int row = tb + min(rr + u, nr - 1);
+          const T* xr = x + int64_t(row) * d + col0;
+          if constexpr (CPT % Vec16<T>::n == 0) {
+#pragma unroll
+            for (int j = 0; j < CPT; j += Vec16<T>::n) Vec16<T>::load(xr + j, xv[u] + j);
+          } else {
+#pragma unroll
+            for (int j = 0; j < CPT; ++j) xv[u][j] = to_f32(xr[j]);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const bool in = rr + u < nr;
+#pragma unroll
+          for (int e = 0; e < NMAX; ++e) {
+            const float g = in ? dzs[rr + u][e] : 0.f;
+#pragma unroll
+            for (int j = 0; j < CPT; ++j) acc[e][j] = fmaf(g, xv[u][j], acc[e][j]);
+          }
+        }
+      }
+    }
+  }
+  if (col0 < d) {
+#pragma unroll
+    for (int e = 0; e < NMAX; ++e)
+      if (e < n)
+#pragma unroll
+        for (int j = 0; j < CPT; ++j)
+          part[int64_t(z) * n * d + int64_t(e) * d + col0 + j] = acc[e][j];
+  }
+  if (blockIdx.x == 0 && threadIdx.x < n)
+    part[int64_t(S) * n * d + int64_t(z) * n + threadIdx.x] = bacc;
+}
+
+// out1[i] = sum_z part[z * n1 + i] (i < n1), out2[i] = sum_z part[S * n1 + z * n2 + i]
+template <typename TO>
+__global__ void __launch_bounds__(256)
+    splitk_reduce2_kernel(const float* __restrict__ part, int S, int64_t n1,
+                          TO* __restrict__ out1, int64_t n2, TO* __restrict__ out2) {
+  pdl_launch_dependents();
+  pdl_wait_previous();
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n1 + n2;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    // four running sums (chunks z mod 4), combined in a fixed order
+    const float* src = i < n1 ? part + i : part + int64_t(S) * n1 + (i - n1);
+    const int64_t stride = i < n1 ? n1 : n2;
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    int z = 0;
+    for (; z + 3 < S; z += 4) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] += src[int64_t(z + u) * stride];
+    }
+    for (; z < S; ++z) v[0] += src[int64_t(z) * stride];
+    const float sum = (v[0] + v[1]) + (v[2] + v[3]);
+    if (i < n1) out1[i] = from_f32<TO>(sum);
+    else out2[i - n1] = from_f32<TO>(sum);
+  }
+}
+
 // ---- dx -----------------------------------------------------------------------------------------
 
 constexpr int kDxWarps = 8;
 
-// dx[t] = dxr[t] (the router's part, fp32 or bf16) + sum over t's kept rows
-// of dXp (slot order) + the shared row; T: the layer's element type.
+// dx[t] = dxr[t] (the router's part, fp32 or bf16; or, with dxr == nullptr,
+// dz[t] W_g computed here) + sum over t's kept rows of dXp (slot order) + the
+// shared row; T: the layer's element type.  Warp (token, column chunk): each
+// lane takes kDxVec 16-byte words of the chunk, 32 words apart, so that every
+// row read keeps kDxVec loads in flight.
+constexpr int kDxVec = 4;
+
 template <typename TR, typename T>
 __global__ void __launch_bounds__(kDxWarps * 32)
     bwd_dx_kernel(const T* __restrict__ dXp, const int32_t* __restrict__ token_row,
                   const int32_t* __restrict__ offsets, const TR* __restrict__ dxr, int Ttok,
-                  int k, int N, int has_shared, int64_t d, T* __restrict__ dx) {
+                  int k, int N, int has_shared, int64_t d, T* __restrict__ dx,
+                  const float* __restrict__ dz, const T* __restrict__ W_g) {
   constexpr int V = Vec16<T>::n;
+  __shared__ float dzs[kDxWarps][32];
   pdl_launch_dependents();
   pdl_wait_previous();
-  const int lane = threadIdx.x & 31;
-  const int64_t t = int64_t(blockIdx.x) * kDxWarps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t t = int64_t(blockIdx.x) * kDxWarps + warp;
   if (t >= Ttok) return;
+  if (!dxr) {                                   // few experts (N <= 32): dz[t] per warp
+    dzs[warp][lane] = lane < N ? dz[t * N + lane] : 0.f;
+    __syncwarp();
+  }
   const int64_t nv = d / V;
-  for (int64_t c = lane; c < nv; c += 32) {
-    float acc[V];
+  const int64_t cbase = int64_t(blockIdx.y) * 32 * kDxVec + lane;
+  float acc[kDxVec][V];
 #pragma unroll
-    for (int i = 0; i < V; ++i) acc[i] = to_f32(dxr[t * d + c * V + i]);
-    for (int j = 0; j <= k; ++j) {
-      int64_t r;
-      if (j < k) r = token_row[t * k + j];
-      else r = has_shared ? int64_t(offsets[N]) + t : -1;
-      if (r < 0) continue;
-      float v[V];
-      Vec16<T>::load(dXp + r * d + c * V, v);
+  for (int u = 0; u < kDxVec; ++u)
 #pragma unroll
-      for (int i = 0; i < V; ++i) acc[i] += v[i];
+    for (int i = 0; i < V; ++i) acc[u][i] = 0.f;
+  for (int j = 0; j <= k; ++j) {
+    int64_t r;
+    if (j < k) r = token_row[t * k + j];
+    else r = has_shared ? int64_t(offsets[N]) + t : -1;
+    if (r < 0) continue;
+    float v[kDxVec][V];
+#pragma unroll
+    for (int u = 0; u < kDxVec; ++u) {
+      const int64_t c = cbase + 32 * u;
+      if (c < nv) Vec16<T>::load(dXp + r * d + c * V, v[u]);
     }
-    Vec16<T>::store(dx + t * d + c * V, acc);
+#pragma unroll
+    for (int u = 0; u < kDxVec; ++u)
+      if (cbase + 32 * u < nv)
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc[u][i] += v[u][i];
+  }
+  if (dxr) {
+#pragma unroll
+    for (int u = 0; u < kDxVec; ++u) {
+      const int64_t c = cbase + 32 * u;
+      if (c < nv)
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc[u][i] += to_f32(dxr[t * d + c * V + i]);
+    }
+  } else {
+    // the router's part dz[t] W_g (W_g of few experts stays in cache)
+    float rt[kDxVec][V];
+#pragma unroll
+    for (int u = 0; u < kDxVec; ++u)
+#pragma unroll
+      for (int i = 0; i < V; ++i) rt[u][i] = 0.f;
+    for (int e = 0; e < N; ++e) {
+      const float g = dzs[warp][e];
+      float wv[kDxVec][V];
+#pragma unroll
+      for (int u = 0; u < kDxVec; ++u) {
+        const int64_t c = cbase + 32 * u;
+        if (c < nv) Vec16<T>::load(W_g + int64_t(e) * d + c * V, wv[u]);
+      }
+#pragma unroll
+      for (int u = 0; u < kDxVec; ++u)
+        if (cbase + 32 * u < nv)
+#pragma unroll
+          for (int i = 0; i < V; ++i) rt[u][i] = fmaf(g, wv[u][i], rt[u][i]);
+    }
+#pragma unroll
+    for (int u = 0; u < kDxVec; ++u)
+#pragma unroll
+      for (int i = 0; i < V; ++i) acc[u][i] += rt[u][i];
+  }
+#pragma unroll
+  for (int u = 0; u < kDxVec; ++u) {
+    const int64_t c = cbase + 32 * u;
+    if (c < nv) Vec16<T>::store(dx + t * d + c * V, acc[u]);
   }
 }
 
@@ -371,6 +602,45 @@ cudaError_t launch_router_grad_gemm(const float* A, int64_t am, int64_t ak, cons
   dim3 grid(unsigned((Nn + kRg - 1) / kRg), unsigned((M + kRg - 1) / kRg));
   return launch_pdl(router_grad_gemm_kernel<TB, TOut>, grid, dim3(256), 0, s, A, am, ak, B,
                     ldb, M, Nn, K, K, C, ldc);
+}
+
+// Chunks of T for router_grad_small_kernel: about two waves of blocks.
+int router_small_chunks(const moe_config& c) {
+  const int N = int(c.n_experts);
+  const int cpt = N <= 8 ? 8 : (N <= 16 ? 4 : 2);
+  const int64_t cblocks = (c.d_model + 256 * cpt - 1) / (256 * cpt);
+  int64_t S = (2 * 148 + cblocks - 1) / cblocks;
+  const int64_t by_t = (c.T + 31) / 32;           // at least 32 tokens a chunk
+  if (S > by_t) S = by_t;
+  return int(S < 1 ? 1 : S);
+}
+
+template <typename E>
+cudaError_t launch_router_small(const moe_config& c, const float* dz, const E* x, float* part,
+                                E* dW_g, E* db_g, cudaStream_t s) {
+  const int N = int(c.n_experts), T = int(c.T);
+  const int64_t d = c.d_model;
+  const int S = router_small_chunks(c);
+  const int tc = (T + S - 1) / S;
+  cudaError_t e;
+#define MOE_ROUTER_SMALL(NN, CPT)                                                          \
+  {                                                                                        \
+    const dim3 grid(unsigned((d + 256 * CPT - 1) / (256 * CPT)), unsigned(S));            \
+    e = launch_pdl(router_grad_small_kernel<E, NN, CPT>, grid, dim3(256), 0, s, dz, x, T, N, \
+                   d, tc, part);                                                           \
+  }
+  if (N <= 1) MOE_ROUTER_SMALL(1, 8)
+  else if (N <= 2) MOE_ROUTER_SMALL(2, 8)
+  else if (N <= 4) MOE_ROUTER_SMALL(4, 8)
+  else if (N <= 8) MOE_ROUTER_SMALL(8, 8)
+  else if (N <= 16) MOE_ROUTER_SMALL(16, 4)
+  else MOE_ROUTER_SMALL(32, 2)
+#undef MOE_ROUTER_SMALL
+  if (e != cudaSuccess) return e;
+  const int64_t n1 = int64_t(N) * d, n2 = N;
+  const int64_t blocks = (n1 + n2 + 255) / 256;
+  return launch_pdl(splitk_reduce2_kernel<E>, dim3(unsigned(blocks < 1184 ? blocks : 1184)),
+                    dim3(256), 0, s, static_cast<const float*>(part), S, n1, dW_g, n2, db_g);
 }
 
 // Splits of K for dW_g = dz^T x on CUDA cores: enough blocks for two waves.
@@ -425,17 +695,28 @@ bool router_bwd_on_tensor_cores(const moe_config& c) {
   return c.dtype == MOE_BF16 && c.n_experts % 64 == 0;
 }
 
+size_t bias_partial_bytes(const moe_config& c, int64_t rows_max) {
+  return size_t((rows_max + kChunkRows - 1) / kChunkRows) * size_t(c.d_model + c.d_ff) *
+         sizeof(float);
+}
+
 size_t router_bwd_partial_bytes(const moe_config& c) {
-  return router_bwd_on_tensor_cores(c)
-             ? 0
-             : size_t(router_splits(c)) * size_t(c.n_experts * c.d_model) * sizeof(float);
+  if (router_bwd_on_tensor_cores(c)) return 0;
+  if (c.n_experts <= kRouterSmallMaxN)
+    return size_t(router_small_chunks(c)) * size_t(c.n_experts * (c.d_model + 1)) *
+           sizeof(float);
+  return size_t(router_splits(c)) * size_t(c.n_experts * c.d_model) * sizeof(float);
 }
 
 int backward_launch_count(const moe_config& c) {
   if (c.T == 0) return c.d_ff_shared > 0 ? 10 : 6;    // zero parameter gradients
-  // gate, padding (bf16 only), A1, dA, dXp, dW2, dW1, db2, db1, dx_router,
-  // dW_g (+ split-K reduce on CUDA cores), db_g, dx
-  return (router_bwd_on_tensor_cores(c) ? 13 : 14) - (c.dtype == MOE_F32 ? 1 : 0);
+  // gate, A1, dA, dXp, dW2, dW1, the bias column sums (partials, reduction),
+  // then the router: tensor cores dx_router + dW_g + db_g; few experts (<= 32)
+  // dW_g with db_g + their reduction (dx_router inside dx); otherwise
+  // dx_router, split-K dW_g + reduction, db_g; then dx
+  const int router = router_bwd_on_tensor_cores(c) ? 3
+                     : c.n_experts <= kRouterSmallMaxN ? 2 : 4;
+  return 8 + router + 1;
 }
 
 namespace {
@@ -470,24 +751,16 @@ cudaError_t backward_t(const moe_config& c, const BackwardArgs& a, void* const* 
       if (e != cudaSuccess) return e;
     }
     const bool tcr = router_bwd_on_tensor_cores(c);
+    // bf16: one more block per group zeroes the padding rows its wgrads read
+    const int pad_groups = kBf16 ? groups : 0;
     const cudaError_t e = launch_pdl(
-        bwd_gate_kernel<E>, dim3(unsigned((T + kGateWarps - 1) / kGateWarps)),
+        bwd_gate_kernel<E>, dim3(unsigned((T + kGateWarps - 1) / kGateWarps + pad_groups)),
         dim3(kGateWarps * 32), smem, s, static_cast<const E*>(a.dy),
         static_cast<const E*>(a.Yp), a.token_row, a.topk_idx, a.topk_w, a.logits,
         a.mean_prob, a.offsets, T, d, N, k, c.renormalize ? 1 : 0, hs, a.aux_weight,
         static_cast<E*>(a.dO), a.dz, a.dw, tcr ? static_cast<__nv_bfloat16*>(a.dz_bf) : nullptr,
-        tcr ? a.rgrp : nullptr);
-    if (e != cudaSuccess) return e;
-  }
-  if (kBf16) {
-    // padding rows of dO, H and Xp -> 0 (the wgrads run K over whole 64-row blocks)
-    PadBufs pb{};
-    pb.buf[0] = a.dO; pb.vec16[0] = d / 8;
-    pb.buf[1] = a.H; pb.vec16[1] = f / 8;
-    pb.buf[2] = a.Xp; pb.vec16[2] = d / 8;
-    pb.n = 3;
-    const cudaError_t e = launch_pdl(zero_pad_rows_kernel, dim3(unsigned(groups), 16),
-                                     dim3(256), 0, s, a.offsets, a.kept, N, hs ? T : 0, pb);
+        tcr ? a.rgrp : nullptr, a.kept, static_cast<E*>(a.H), static_cast<E*>(a.Xp), f,
+        pad_groups);
     if (e != cudaSuccess) return e;
   }
   er = record_event(ev[1], s);
@@ -523,20 +796,27 @@ cudaError_t backward_t(const moe_config& c, const BackwardArgs& a, void* const* 
   e = wgrad(c, bg, a.dA, f, a.Xp, d, a.g->dW1, a.g->dW1s, s);
   if (e == cudaSuccess) e = record_event(ev[6], s);
   if (e != cudaSuccess) return e;
-  // db2, db1
-  constexpr int kColsPerBlock = 32 * Vec16<E>::n;
-  e = launch_pdl(group_colsum_kernel<E>,
-                 dim3(unsigned(groups), unsigned((d + kColsPerBlock - 1) / kColsPerBlock)),
-                 dim3(256), 0, s, static_cast<const E*>(a.dO), d, a.offsets, a.kept, N,
-                 hs ? T : 0, static_cast<E*>(a.g->db2), static_cast<E*>(a.g->db2s));
-  if (e != cudaSuccess) return e;
-  e = launch_pdl(group_colsum_kernel<E>,
-                 dim3(unsigned(groups), unsigned((f + kColsPerBlock - 1) / kColsPerBlock)),
-                 dim3(256), 0, s, static_cast<const E*>(a.dA), f, a.offsets, a.kept, N,
-                 hs ? T : 0, static_cast<E*>(a.g->db1), static_cast<E*>(a.g->db1s));
-  if (e != cudaSuccess) return e;
+  // db2, db1: chunk partials, then each group's chunks in order
+  {
+    constexpr int kColsPerBlock = 32 * Vec16<E>::n;
+    const int64_t cb = (d + kColsPerBlock - 1) / kColsPerBlock +
+                       (f + kColsPerBlock - 1) / kColsPerBlock;
+    const int64_t chunks = (a.rows_max + kChunkRows - 1) / kChunkRows;
+    e = launch_pdl(colsum_partial_kernel<E>, dim3(unsigned(chunks), unsigned(cb)), dim3(256), 0,
+                   s, static_cast<const E*>(a.dO), d, static_cast<const E*>(a.dA), f,
+                   a.offsets, a.kept, N, hs ? T : 0, groups, a.bpart);
+    if (e != cudaSuccess) return e;
+    const int64_t outs = int64_t(groups) * (d + f);
+    const int64_t blocks = (outs + 255) / 256;
+    e = launch_pdl(colsum_reduce_kernel<E>, dim3(unsigned(blocks < 4096 ? blocks : 4096)),
+                   dim3(256), 0, s, static_cast<const float*>(a.bpart), d, f, a.offsets, N,
+                   groups, static_cast<E*>(a.g->db2), static_cast<E*>(a.g->db2s),
+                   static_cast<E*>(a.g->db1), static_cast<E*>(a.g->db1s));
+    if (e != cudaSuccess) return e;
+  }
   // router: dx_router = dz W_g [T, d]; dW_g = dz^T x [N, d]; db_g = sum_t dz
   const bool tc_router = router_bwd_on_tensor_cores(c);
+  const bool small_router = !tc_router && N <= kRouterSmallMaxN;
   if (tc_router) {
     // the dgrad / wgrad kernels on one group of T rows, dz rounded to bf16
     moe_config rc = c;
@@ -549,6 +829,10 @@ cudaError_t backward_t(const moe_config& c, const BackwardArgs& a, void* const* 
     e = launch_bwd_dgrad(rc, rg, a.dz_bf, w->W_g, nullptr, N, d, -1, nullptr, a.dxr_bf, s);
     if (e != cudaSuccess) return e;
     e = launch_bwd_wgrad(rc, rg, a.dz_bf, N, a.x, d, a.g->dW_g, nullptr, s);
+    if (e != cudaSuccess) return e;
+  } else if (small_router) {
+    e = launch_router_small<E>(c, a.dz, static_cast<const E*>(a.x), a.part,
+                               static_cast<E*>(a.g->dW_g), static_cast<E*>(a.g->db_g), s);
     if (e != cudaSuccess) return e;
   } else {
     e = launch_router_grad_gemm<E, float>(a.dz, N, 1, static_cast<const E*>(w->W_g), d, T, d,
@@ -568,21 +852,27 @@ cudaError_t backward_t(const moe_config& c, const BackwardArgs& a, void* const* 
                    static_cast<E*>(a.g->dW_g));
     if (e != cudaSuccess) return e;
   }
-  e = launch_pdl(router_bias_grad_kernel<E>, dim3(unsigned((N + 31) / 32)), dim3(256), 0, s,
-                 static_cast<const float*>(a.dz), T, N, static_cast<E*>(a.g->db_g));
-  if (e != cudaSuccess) return e;
+  if (!small_router) {
+    e = launch_pdl(router_bias_grad_kernel<E>, dim3(unsigned((N + 31) / 32)),
+                   dim3(kBiasWarps * 32), 0, s, static_cast<const float*>(a.dz), T, N,
+                   static_cast<E*>(a.g->db_g));
+    if (e != cudaSuccess) return e;
+  }
   // dx
+  const dim3 dx_grid(unsigned((T + kDxWarps - 1) / kDxWarps),
+                     unsigned((d / Vec16<E>::n + 32 * kDxVec - 1) / (32 * kDxVec)));
   if (tc_router)
-    e = launch_pdl(bwd_dx_kernel<__nv_bfloat16, E>,
-                   dim3(unsigned((T + kDxWarps - 1) / kDxWarps)), dim3(kDxWarps * 32), 0, s,
+    e = launch_pdl(bwd_dx_kernel<__nv_bfloat16, E>, dx_grid, dim3(kDxWarps * 32), 0, s,
                    static_cast<const E*>(a.dXp), a.token_row, a.offsets,
                    static_cast<const __nv_bfloat16*>(a.dxr_bf), T, k, N, hs, d,
-                   static_cast<E*>(a.g->dx));
+                   static_cast<E*>(a.g->dx), static_cast<const float*>(nullptr),
+                   static_cast<const E*>(nullptr));
   else
-    e = launch_pdl(bwd_dx_kernel<float, E>, dim3(unsigned((T + kDxWarps - 1) / kDxWarps)),
-                   dim3(kDxWarps * 32), 0, s, static_cast<const E*>(a.dXp), a.token_row,
-                   a.offsets, static_cast<const float*>(a.dxr), T, k, N, hs, d,
-                   static_cast<E*>(a.g->dx));
+    e = launch_pdl(bwd_dx_kernel<float, E>, dx_grid, dim3(kDxWarps * 32), 0, s,
+                   static_cast<const E*>(a.dXp), a.token_row,
+                   a.offsets, small_router ? nullptr : static_cast<const float*>(a.dxr), T, k,
+                   N, hs, d, static_cast<E*>(a.g->dx), static_cast<const float*>(a.dz),
+                   static_cast<const E*>(w->W_g));
   if (e != cudaSuccess) return e;
   return record_event(ev[7], s);
 }

@@ -39,11 +39,15 @@ constexpr int kMaxGroups = 1025;
 enum { MODE_DGRAD = 0, MODE_WGRAD = 1 };
 enum { BEPI_STORE = 0, BEPI_DGELU = 1, BEPI_DRELU = 2 };
 
-// Output staging (WGRAD): each epilogue warp's 32 rows x 32 columns of bf16,
-// rows padded to 80 bytes so that both the row-wise writes and the
-// transposed reads of shared memory stay (nearly) free of bank conflicts.
-constexpr int kStagePitch = 80;
-constexpr int kStageWarpBytes = 32 * kStagePitch;
+// Output staging (WGRAD): each epilogue warp's 32 rows x BN/4 columns of
+// bf16, laid out as the tensor store's box with the swizzle matching its row
+// width (BN/4 * 2 = 128, 64 or 32 bytes): the 16-byte chunk c of row r sits
+// at chunk c ^ (r / (128 / width)) mod (width / 16), so that a warp writing
+// one chunk of 32 rows (lane = row) hits every bank once per quarter warp.
+template <int BN>
+__host__ __device__ constexpr int stage_warp_bytes() {
+  return 32 * (BN / 4) * 2;
+}
 
 template <int BN, int STAGES, int STAGE_BYTES = 0>
 struct BwdLayout {
@@ -59,7 +63,7 @@ struct BwdLayout {
   static constexpr int kTileStart = (kAbort + 4 + 15) / 16 * 16;     // [kMaxGroups + 1]
   static constexpr int kGroupOff = kTileStart + (kMaxGroups + 1) * 4;  // [kMaxGroups]
   static constexpr int kGroupLive = kGroupOff + kMaxGroups * 4;        // [kMaxGroups]
-  static constexpr int kStage = (kGroupLive + kMaxGroups * 4 + 127) / 128 * 128;
+  static constexpr int kStage = (kGroupLive + kMaxGroups * 4 + 1023) / 1024 * 1024;
   static constexpr int kBytes = kStage + STAGE_BYTES;
   static constexpr int kAlloc = kBytes + 1024;
   static_assert(kAlloc <= 227 * 1024, "shared memory budget");
@@ -130,12 +134,16 @@ template <int BN, int STAGES, int MODE, int EPI>
 __global__ void __launch_bounds__(18 * 32, 1)
     tc_bwd_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB,
-                       const __grid_constant__ CUtensorMap tmBs, const BwdParams p) {
+                       const __grid_constant__ CUtensorMap tmBs,
+                       const __grid_constant__ CUtensorMap tmO,
+                       const __grid_constant__ CUtensorMap tmOs, const BwdParams p) {
   constexpr int kEpiWarps = 16;
-  // the wgrads write whole weight-sized outputs: their stores go through
-  // shared memory so that each warp store covers 8 rows x 64 contiguous bytes
+  // the wgrads write whole weight-sized outputs: each epilogue warp puts its
+  // 32 x BN/4 piece of a tile into shared memory and one lane hands it to a
+  // tensor store (tmO: [n_routed, Md, Nd], tmOs: the shared expert's [Md, Nd])
   constexpr bool kStaged = MODE == MODE_WGRAD;
-  using L = BwdLayout<BN, STAGES, kStaged ? kEpiWarps * kStageWarpBytes : 0>;
+  constexpr int kWarpStage = stage_warp_bytes<BN>();
+  using L = BwdLayout<BN, STAGES, kStaged ? kEpiWarps * kWarpStage : 0>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -260,13 +268,19 @@ __global__ void __launch_bounds__(18 * 32, 1)
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
+    // WGRAD: a group's last K block issues only the 16-row K steps that hold
+    // live rows; the rows past the live ones inside the last of those steps
+    // are the group's padding rows, which the caller zeroes (up to the next
+    // multiple of 16).  A K block never reaches into the next group: groups
+    // start on 128-row boundaries.
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bwd<BN, MODE>();
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
         const BwdTile tc = bwd_decode(tile, tile_start, n_groups, ntiles);
-        const int nkb = tile_kb<MODE>(p, grp_live[tc.g]);
+        const int live = grp_live[tc.g];
+        const int nkb = tile_kb<MODE>(p, live);
         if (!bwd_wait(&tempty[acc], acc_phase ^ 1u, p, abort_flag)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
@@ -275,13 +289,17 @@ __global__ void __launch_bounds__(18 * 32, 1)
           tc_fence_after();
           const uint32_t a_s = smem_u32(smem + L::kA + stage * L::kABytes);
           const uint32_t b_s = smem_u32(smem + L::kB + stage * L::kBBytes);
+          const int rem = live - kb * BK;
+          const int ksteps = MODE == MODE_WGRAD && rem < BK ? (rem + 15) / 16 : BK / 16;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            // K-major A: +32 bytes per K step; MN-major operands: +2 K groups
-            const uint64_t ad = MODE == MODE_DGRAD ? sdesc_sw128(a_s) + uint64_t(2 * kk)
-                                                   : sdesc_mn_sw128(a_s + kk * 2048, 8192);
-            const uint64_t bd = sdesc_mn_sw128(b_s + kk * 2048, 8192);
-            tc_mma(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            if (kk < ksteps) {
+              // K-major A: +32 bytes per K step; MN-major operands: +2 K groups
+              const uint64_t ad = MODE == MODE_DGRAD ? sdesc_sw128(a_s) + uint64_t(2 * kk)
+                                                     : sdesc_mn_sw128(a_s + kk * 2048, 8192);
+              const uint64_t bd = sdesc_mn_sw128(b_s + kk * 2048, 8192);
+              tc_mma(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            }
           }
           tc_commit(smem_u32(&empty[stage]));
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -332,13 +350,24 @@ __global__ void __launch_bounds__(18 * 32, 1)
         store = row < p.Md;
         zero = !has_acc;
       }
-#pragma unroll 1
-      for (int c = part * kCols; c < (part + 1) * kCols; c += CW) {
-        uint32_t r[CW];
-        tmem_ld_cols<CW>(tmem_base + (uint32_t(q * 32) << 16) + acc * BN + c, r);
-        if (kStaged) {
-          // this lane's row into shared memory, then 8 / 16 rows per warp store
-          uint8_t* stg = smem + L::kStage + (warp - 2) * kStageWarpBytes;
+      if constexpr (kStaged) {
+        // wait until this warp's previous tensor store has read its staging
+        uint8_t* stg = smem + L::kStage + (warp - 2) * kWarpStage;
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+        constexpr int kRowBytes = kCols * 2;           // 128, 64 or 32
+        constexpr int kChunks = kRowBytes / 16;
+        const int swz = (lane / (128 / kRowBytes)) % kChunks;
+#pragma unroll
+        for (int c = 0; c < kCols; c += CW) {
+          uint32_t r[CW];
+          tmem_ld_cols<CW>(tmem_base + (uint32_t(q * 32) << 16) + acc * BN + part * kCols + c,
+                           r);
+          if (c + CW == kCols) {                       // the accumulator is free again
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);
+          }
 #pragma unroll
           for (int v = 0; v < CW / 8; ++v) {
             uint4 o;
@@ -348,68 +377,70 @@ __global__ void __launch_bounds__(18 * 32, 1)
               o2[i] = zero ? __floats2bfloat162_rn(0.f, 0.f)
                            : __floats2bfloat162_rn(__uint_as_float(r[8 * v + 2 * i]),
                                                    __uint_as_float(r[8 * v + 2 * i + 1]));
-            *reinterpret_cast<uint4*>(stg + lane * kStagePitch + v * 16) = o;
+            const int ch = (c / 8 + v) ^ swz;
+            *reinterpret_cast<uint4*>(stg + lane * kRowBytes + ch * 16) = o;
           }
-          __syncwarp();
-          constexpr int kChunks = CW / 8;          // 16-byte chunks per row
-          constexpr int kRowsPerPass = 32 / kChunks;
-          const int64_t col = int64_t(tc.n) * BN + c + (lane % kChunks) * 8;
-          __nv_bfloat16* base = dst_row - int64_t(lane) * p.Nd;   // row 0 of this warp
-          const int row0 = tc.m * BM + q * 32;
-#pragma unroll
-          for (int pass = 0; pass < kChunks; ++pass) {
-            const int rr = pass * kRowsPerPass + lane / kChunks;
-            const uint4 v = *reinterpret_cast<const uint4*>(stg + rr * kStagePitch +
-                                                             (lane % kChunks) * 16);
-            if (row0 + rr < p.Md)
-              *reinterpret_cast<uint4*>(base + int64_t(rr) * p.Nd + col) = v;
-          }
-          __syncwarp();
-          continue;
         }
-        if (store) {
-          const int64_t col = int64_t(tc.n) * BN + c;
-          uint4* dst = reinterpret_cast<uint4*>(dst_row + col);
+        fence_proxy_async_smem();
+        __syncwarp();
+        const int row0 = tc.m * BM + q * 32;
+        if (lane == 0 && row0 < p.Md) {
+          const int x = tc.n * BN + part * kCols;
+          if (tc.g < p.n_routed) tma_store_3d(&tmO, smem_u32(stg), x, row0, tc.g);
+          else tma_store_2d(&tmOs, smem_u32(stg), x, row0);
+          bulk_commit();
+        }
+      } else {
+#pragma unroll 1
+        for (int c = part * kCols; c < (part + 1) * kCols; c += CW) {
+          uint32_t r[CW];
+          tmem_ld_cols<CW>(tmem_base + (uint32_t(q * 32) << 16) + acc * BN + c, r);
+          if (store) {
+            const int64_t col = int64_t(tc.n) * BN + c;
+            uint4* dst = reinterpret_cast<uint4*>(dst_row + col);
 #pragma unroll
-          for (int v = 0; v < CW / 8; ++v) {
-            uint4 o;
-            __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(&o);
-            if (zero) {
-              o = make_uint4(0, 0, 0, 0);
-            } else {
-              float gr[8];
-              if (EPI != BEPI_STORE) {
-                const uint4 pv = __ldg(reinterpret_cast<const uint4*>(pre_row + col) + v);
-                const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&pv);
+            for (int v = 0; v < CW / 8; ++v) {
+              uint4 o;
+              __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(&o);
+              if (zero) {
+                o = make_uint4(0, 0, 0, 0);
+              } else {
+                float gr[8];
+                if (EPI != BEPI_STORE) {
+                  const uint4 pv = __ldg(reinterpret_cast<const uint4*>(pre_row + col) + v);
+                  const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&pv);
+#pragma unroll
+                  for (int i = 0; i < 4; ++i) {
+                    const float2 a = __bfloat1622float2(p2[i]);
+                    gr[2 * i] = EPI == BEPI_DGELU ? gelu_erf_grad(a.x) : (a.x > 0.f ? 1.f : 0.f);
+                    gr[2 * i + 1] =
+                        EPI == BEPI_DGELU ? gelu_erf_grad(a.y) : (a.y > 0.f ? 1.f : 0.f);
+                  }
+                }
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                  const float2 a = __bfloat1622float2(p2[i]);
-                  gr[2 * i] = EPI == BEPI_DGELU ? gelu_erf_grad(a.x) : (a.x > 0.f ? 1.f : 0.f);
-                  gr[2 * i + 1] =
-                      EPI == BEPI_DGELU ? gelu_erf_grad(a.y) : (a.y > 0.f ? 1.f : 0.f);
+                  float x0 = __uint_as_float(r[8 * v + 2 * i]);
+                  float x1 = __uint_as_float(r[8 * v + 2 * i + 1]);
+                  if (EPI != BEPI_STORE) {
+                    x0 *= gr[2 * i];
+                    x1 *= gr[2 * i + 1];
+                  }
+                  o2[i] = __floats2bfloat162_rn(x0, x1);
                 }
               }
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                float x0 = __uint_as_float(r[8 * v + 2 * i]);
-                float x1 = __uint_as_float(r[8 * v + 2 * i + 1]);
-                if (EPI != BEPI_STORE) {
-                  x0 *= gr[2 * i];
-                  x1 *= gr[2 * i + 1];
-                }
-                o2[i] = __floats2bfloat162_rn(x0, x1);
-              }
+              dst[v] = o;
             }
-            dst[v] = o;
           }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
+    // the tensor stores complete before the block's shared memory goes away
+    if (kStaged && lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -421,43 +452,49 @@ __global__ void __launch_bounds__(18 * 32, 1)
   }
 }
 
-// bf16 tensor [outer, inner] (or [z, outer, inner]) read in boxes of
-// [box_outer, 64] (128-byte swizzle).
+// bf16 tensor [outer, inner] (or [z, outer, inner]) in boxes of
+// [box_outer, box_inner] (box_inner = 64, 32 or 16: a 128-, 64- or 32-byte
+// swizzle, the row width).
 bool bwd_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t z,
-             uint32_t box_outer) {
+             uint32_t box_outer, uint32_t box_inner = BK) {
   auto fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[3] = {inner, outer, z};
   const cuuint64_t strides[2] = {inner * 2, inner * outer * 2};
-  const cuuint32_t box[3] = {uint32_t(BK), box_outer, 1};
+  const cuuint32_t box[3] = {box_inner, box_outer, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   const cuuint32_t rank = z > 0 ? 3 : 2;
+  const CUtensorMapSwizzle sw = box_inner == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : box_inner == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                  : CU_TENSOR_MAP_SWIZZLE_32B;
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides,
-            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int BN, int MODE, int EPI>
 cudaError_t launch_bwd(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& Bs,
-                       const BwdParams& p, int64_t max_tiles, int num_sms, cudaStream_t s) {
+                       const CUtensorMap& O, const CUtensorMap& Os, const BwdParams& p,
+                       int64_t max_tiles, int num_sms, cudaStream_t s) {
   // the wgrads trade a ring stage for their store staging
   constexpr int STAGES = MODE == MODE_WGRAD ? 3 : 4;
   constexpr int smem =
-      BwdLayout<BN, STAGES, MODE == MODE_WGRAD ? 16 * kStageWarpBytes : 0>::kAlloc;
+      BwdLayout<BN, STAGES, MODE == MODE_WGRAD ? 16 * stage_warp_bytes<BN>() : 0>::kAlloc;
   auto kern = tc_bwd_gemm_kernel<BN, STAGES, MODE, EPI>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int grid = int(max_tiles < num_sms ? (max_tiles > 0 ? max_tiles : 1) : num_sms);
-  return launch_pdl(kern, dim3(grid), dim3(18 * 32), smem, s, A, B, Bs, p);
+  return launch_pdl(kern, dim3(grid), dim3(18 * 32), smem, s, A, B, Bs, O, Os, p);
 }
 
+// O, Os: the wgrads' output maps (DGRAD ignores them)
 template <int MODE, int EPI>
 cudaError_t launch_bwd_bn(int bn, const CUtensorMap& A, const CUtensorMap& B,
-                          const CUtensorMap& Bs, const BwdParams& p, int64_t max_tiles,
-                          int num_sms, cudaStream_t s) {
-  if (bn == 256) return launch_bwd<256, MODE, EPI>(A, B, Bs, p, max_tiles, num_sms, s);
-  if (bn == 128) return launch_bwd<128, MODE, EPI>(A, B, Bs, p, max_tiles, num_sms, s);
-  return launch_bwd<64, MODE, EPI>(A, B, Bs, p, max_tiles, num_sms, s);
+                          const CUtensorMap& Bs, const CUtensorMap& O, const CUtensorMap& Os,
+                          const BwdParams& p, int64_t max_tiles, int num_sms, cudaStream_t s) {
+  if (bn == 256) return launch_bwd<256, MODE, EPI>(A, B, Bs, O, Os, p, max_tiles, num_sms, s);
+  if (bn == 128) return launch_bwd<128, MODE, EPI>(A, B, Bs, O, Os, p, max_tiles, num_sms, s);
+  return launch_bwd<64, MODE, EPI>(A, B, Bs, O, Os, p, max_tiles, num_sms, s);
 }
 
 int bwd_bn(int64_t Nd) { return Nd % 256 == 0 ? 256 : (Nd % 128 == 0 ? 128 : 64); }
@@ -495,10 +532,13 @@ cudaError_t launch_bwd_dgrad(const moe_config& c, const BwdGemmArgs& g, const vo
   const int64_t groups = c.n_experts + (c.d_ff_shared > 0 ? 1 : 0);
   const int64_t max_tiles = ((g.rows_max + BM - 1) / BM + groups) * (Nd / bn);
   if (act < 0)
-    return launch_bwd_bn<MODE_DGRAD, BEPI_STORE>(bn, mA, mB, mBs, p, max_tiles, g.num_sms, s);
+    return launch_bwd_bn<MODE_DGRAD, BEPI_STORE>(bn, mA, mB, mBs, mA, mA, p, max_tiles,
+                                                 g.num_sms, s);
   if (act == MOE_ACT_RELU)
-    return launch_bwd_bn<MODE_DGRAD, BEPI_DRELU>(bn, mA, mB, mBs, p, max_tiles, g.num_sms, s);
-  return launch_bwd_bn<MODE_DGRAD, BEPI_DGELU>(bn, mA, mB, mBs, p, max_tiles, g.num_sms, s);
+    return launch_bwd_bn<MODE_DGRAD, BEPI_DRELU>(bn, mA, mB, mBs, mA, mA, p, max_tiles,
+                                                 g.num_sms, s);
+  return launch_bwd_bn<MODE_DGRAD, BEPI_DGELU>(bn, mA, mB, mBs, mA, mA, p, max_tiles,
+                                               g.num_sms, s);
 }
 
 // out[e] = L[group e]^T . R[group e]: L [rows, Md], R [rows, Nd] -> [Md, Nd]
@@ -506,10 +546,20 @@ cudaError_t launch_bwd_dgrad(const moe_config& c, const BwdGemmArgs& g, const vo
 cudaError_t launch_bwd_wgrad(const moe_config& c, const BwdGemmArgs& g, const void* Lm,
                              int64_t Md, const void* Rm, int64_t Nd, void* out, void* out_s,
                              cudaStream_t s) {
-  CUtensorMap mA, mB;
+  CUtensorMap mA, mB, mO, mOs;
   const int bn = bwd_bn(Nd);
   if (!bwd_map(&mA, Lm, uint64_t(Md), uint64_t(g.rows_max), 0, BK)) return cudaErrorInvalidValue;
   if (!bwd_map(&mB, Rm, uint64_t(Nd), uint64_t(g.rows_max), 0, BK)) return cudaErrorInvalidValue;
+  // outputs: boxes of 32 rows x bn/4 columns, one per epilogue warp and tile
+  if (!bwd_map(&mO, out, uint64_t(Nd), uint64_t(Md), uint64_t(c.n_experts), 32,
+               uint32_t(bn / 4)))
+    return cudaErrorInvalidValue;
+  if (c.d_ff_shared > 0) {
+    if (!bwd_map(&mOs, out_s, uint64_t(Nd), uint64_t(Md), 0, 32, uint32_t(bn / 4)))
+      return cudaErrorInvalidValue;
+  } else {
+    mOs = mO;
+  }
   BwdParams p{};
   p.offsets = g.offsets;
   p.kept = g.kept;
@@ -523,7 +573,8 @@ cudaError_t launch_bwd_wgrad(const moe_config& c, const BwdGemmArgs& g, const vo
   p.wait_limit_ns = g.wait_limit_ns;
   const int64_t groups = c.n_experts + (c.d_ff_shared > 0 ? 1 : 0);
   const int64_t max_tiles = groups * ((Md + BM - 1) / BM) * (Nd / bn);
-  return launch_bwd_bn<MODE_WGRAD, BEPI_STORE>(bn, mA, mB, mB, p, max_tiles, g.num_sms, s);
+  return launch_bwd_bn<MODE_WGRAD, BEPI_STORE>(bn, mA, mB, mB, mO, mOs, p, max_tiles, g.num_sms,
+                                               s);
 }
 
 }  // namespace moe

@@ -200,8 +200,9 @@ struct BackwardArgs {
   const void* dy;           // [T, d]
   // saved by the forward
   const void* Yp;           // [rows_max, d]
-  void* H;                  // [rows_max, d_ff] (padding rows zeroed here)
-  void* Xp;                 // [rows_max, d] (padding rows zeroed here)
+  void* H;                  // [rows_max, d_ff] (bf16: padding rows up to each group's next
+                            // multiple of 16 zeroed here)
+  void* Xp;                 // [rows_max, d] (the same)
   const int32_t* offsets;
   const int32_t* kept;
   const int32_t* token_row;
@@ -223,6 +224,7 @@ struct BackwardArgs {
   void* dxr_bf;             // [round_up(T, 128), d] bf16 (router part of dx on tensor cores)
   int32_t* rgrp;            // 4 ints: the router GEMMs' one-group offsets and row count
   float* part;              // split-K partial sums of dW_g on CUDA cores
+  float* bpart;             // [ceil(rows_max / 128), d + d_ff] bias column-sum partials
   int64_t rows_max;
   int32_t* status;
   uint64_t wait_limit_ns;
@@ -235,6 +237,8 @@ int backward_launch_count(const moe_config& c);
 // router gradients on the tensor cores (N % 64 == 0), else CUDA cores with split K
 bool router_bwd_on_tensor_cores(const moe_config& c);
 size_t router_bwd_partial_bytes(const moe_config& c);
+// the bias column sums' per-chunk partials
+size_t bias_partial_bytes(const moe_config& c, int64_t rows_max);
 
 // fp32 layers: the same three backward GEMMs on CUDA cores (grouped_ffn_f32.cu)
 cudaError_t launch_grouped_linear_f32(const moe_config& c, const BwdGemmArgs& g, const void* A,

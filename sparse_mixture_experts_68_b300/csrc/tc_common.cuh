@@ -32,6 +32,44 @@ __device__ __forceinline__ void tma_load_3d(const CUtensorMap* map, uint32_t dst
       : "memory");
 }
 
+// Tensor stores from shared memory (bulk async-group completion): the box at
+// {x, y[, z]} of the map's tensor; elements outside its extents are skipped.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(x), "r"(y)
+               : "memory");
+}
+
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y,
+                                             int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// the committed stores no longer read their shared-memory source
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// the committed stores have completed
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// this thread's generic-proxy writes to shared memory become visible to the
+// async proxy (a following tensor store)
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -81,27 +119,38 @@ __device__ __forceinline__ void tmem_ld_16cols(uint32_t taddr, uint32_t (&r)[16]
 }
 
 // Output staging of one epilogue warp: 32 rows (one per lane) x SW bf16
-// columns.  Each lane writes its row piece into `stg` (rows padded to SW * 2
-// + 16 bytes, which keeps the accesses nearly free of bank conflicts), then
-// every warp store covers 32 / (SW / 8) whole rows of SW * 2 contiguous bytes
-// (full 32-byte sectors) instead of 32 rows of 16 bytes.  Rows >= rows_valid
-// are not stored.  All 32 lanes must call it.
+// columns.  Each lane writes its row piece into `stg`, then every warp store
+// covers 32 / (SW / 8) whole rows of SW * 2 contiguous bytes (full 32-byte
+// sectors) instead of 32 rows of 16 bytes.  Rows of SW * 2 bytes, unpadded;
+// the 16-byte chunk c of row r sits at chunk c ^ staged_swizzle(r), which
+// keeps both the lane-per-row writes and the row-wise reads free of bank
+// conflicts within each quarter warp.  Rows >= rows_valid are not stored.
+// All 32 lanes must call it.
+template <int SW>
+__device__ __forceinline__ int staged_swizzle(int r) {
+  constexpr int kChunks = SW / 8;                     // 16-byte chunks per row
+  if constexpr (kChunks >= 8) return r & 7;
+  else return (r / (8 / kChunks)) % kChunks;
+}
+
 template <int SW>
 __device__ __forceinline__ void warp_staged_store(const uint4 (&w)[SW / 8], uint8_t* stg,
                                                   int lane, __nv_bfloat16* row0_col,
                                                   int64_t ld, int rows_valid) {
-  constexpr int kPitch = SW * 2 + 16;
+  constexpr int kPitch = SW * 2;
   constexpr int kChunks = SW / 8;
   constexpr int kRowsPerPass = 32 / kChunks;
+  const int sw = staged_swizzle<SW>(lane);
 #pragma unroll
   for (int v = 0; v < kChunks; ++v)
-    *reinterpret_cast<uint4*>(stg + lane * kPitch + v * 16) = w[v];
+    *reinterpret_cast<uint4*>(stg + lane * kPitch + (v ^ sw) * 16) = w[v];
   __syncwarp();
 #pragma unroll
   for (int pass = 0; pass < kChunks; ++pass) {
     const int rr = pass * kRowsPerPass + lane / kChunks;
     const int ch = lane % kChunks;
-    const uint4 v = *reinterpret_cast<const uint4*>(stg + rr * kPitch + ch * 16);
+    const uint4 v =
+        *reinterpret_cast<const uint4*>(stg + rr * kPitch + (ch ^ staged_swizzle<SW>(rr)) * 16);
     if (rr < rows_valid) *reinterpret_cast<uint4*>(row0_col + int64_t(rr) * ld + ch * 8) = v;
   }
   __syncwarp();
@@ -109,7 +158,7 @@ __device__ __forceinline__ void warp_staged_store(const uint4 (&w)[SW / 8], uint
 
 template <int SW>
 __host__ __device__ constexpr int staged_warp_bytes() {
-  return 32 * (SW * 2 + 16);
+  return 32 * SW * 2;
 }
 
 template <int CW>

@@ -117,6 +117,17 @@ SMALL = [
     # ~1000-row groups: several m-tiles per group in the dgrads, many K blocks in the wgrads
     Workload("bwd_big_groups", T=2000, d_model=256, d_ff=512, n_experts=2, top_k=1,
              act=ACT_GELU_ERF, dtype=DT_BF16, seed=85),
+    # 32 < N, N % 64 != 0: router gradients by the split-K CUDA-core GEMMs
+    Workload("bwd_router_splitk", T=700, d_model=128, d_ff=128, n_experts=40, top_k=4,
+             act=ACT_GELU_ERF, dtype=DT_BF16, seed=89),
+    # N = 32 (the widest few-expert router kernel), fp32, d = 2056 spans two column blocks
+    Workload("bwd_f32_router32", T=150, d_model=2056, d_ff=64, n_experts=32, top_k=2,
+             act=ACT_RELU, dtype=DT_F32, seed=90),
+    # N = 1 and N = 12: the narrowest and a non-power-of-two few-expert router
+    Workload("bwd_single_expert", T=100, d_model=64, d_ff=64, n_experts=1, top_k=1,
+             act=ACT_GELU_ERF, dtype=DT_BF16, seed=91),
+    Workload("bwd_twelve_experts", T=333, d_model=1088, d_ff=128, n_experts=12, top_k=3,
+             act=ACT_GELU_ERF, dtype=DT_BF16, seed=92),
 ]
 
 
@@ -150,8 +161,9 @@ def test_backward_deterministic_and_launch_count():
     for n in ("dx", "dW_g", "db_g", "dW1", "db1", "dW2", "db2", "dW1s", "db1s", "dW2s", "db2s",
               "dz", "dw"):
         assert torch.equal(getattr(g1, n), getattr(g2, n)), n
-    # N = 8: router gradients on CUDA cores, with a split-K reduction
-    assert B.backward_launch_count(layer.cfg) == 14
+    # N = 8: few-expert router gradients (dW_g with db_g, their reduction; the
+    # router's part of dx inside the dx kernel)
+    assert B.backward_launch_count(layer.cfg) == 11
 
 
 def test_backward_no_tokens():
