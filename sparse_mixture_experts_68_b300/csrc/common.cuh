@@ -60,30 +60,59 @@ template <> struct Vec16<__nv_bfloat16> {
 
 // ---- activations -------------------------------------------------------------
 
+// The hardware's approximate reciprocal and base-2 exponential (relative
+// errors of a few fp32 ulps), one special-function instruction each.
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ float ex2_approx(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
 // erf by Abramowitz & Stegun, "Handbook of Mathematical Functions", formula
 // 7.1.26: erf(z) = 1 - t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-z^2),
 // t = 1 / (1 + p z) for z >= 0, odd in z; absolute error <= 1.5e-7, below
 // fp32 resolution near 1 and far below the bf16 the hidden layer is stored in.
+constexpr float kAsP = 0.3275911f;
+constexpr float kAsA1 = 0.254829592f, kAsA2 = -0.284496736f, kAsA3 = 1.421413741f,
+                kAsA4 = -1.453152027f, kAsA5 = 1.061405429f;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRsqrt2 = 0.70710678118654752440f;
+
 __device__ __forceinline__ float erf_as7126(float z) {
   const float a = fabsf(z);
-  const float t = __frcp_rn(fmaf(0.3275911f, a, 1.0f));
-  float poly = fmaf(t, 1.061405429f, -1.453152027f);
-  poly = fmaf(t, poly, 1.421413741f);
-  poly = fmaf(t, poly, -0.284496736f);
-  poly = fmaf(t, poly, 0.254829592f);
-  const float r = 1.0f - t * poly * __expf(-a * a);
+  const float t = rcp_approx(fmaf(kAsP, a, 1.0f));
+  float poly = fmaf(t, kAsA5, kAsA4);
+  poly = fmaf(t, poly, kAsA3);
+  poly = fmaf(t, poly, kAsA2);
+  poly = fmaf(t, poly, kAsA1);
+  const float r = 1.0f - t * poly * ex2_approx(-a * a * kLog2e);
   return copysignf(r, z);
 }
 
-// GELU with the exact (erf) form: 0.5 v (1 + erf(v / sqrt(2))).
+// GELU with the exact (erf) form: 0.5 v (1 + erf(v / sqrt(2))).  With the
+// erf above and q = t P(t) exp(-v^2 / 2) / 2 (z = |v| / sqrt(2)), this is
+// v - v q for v >= 0 and v q for v < 0: the halving is folded into the
+// coefficients and the sign into the last select.
 __device__ __forceinline__ float gelu_erf(float v) {
-  return 0.5f * v * (1.0f + erf_as7126(v * 0.70710678118654752440f));
+  const float t = rcp_approx(fmaf(kAsP * kRsqrt2, fabsf(v), 1.0f));
+  float q = fmaf(t, 0.5f * kAsA5, 0.5f * kAsA4);
+  q = fmaf(t, q, 0.5f * kAsA3);
+  q = fmaf(t, q, 0.5f * kAsA2);
+  q = fmaf(t, q, 0.5f * kAsA1);
+  const float e = ex2_approx(v * v * (-0.5f * kLog2e));
+  const float r = v * (t * q * e);
+  return v < 0.0f ? r : v - r;
 }
 // d GELU / d v = Phi(v) + v phi(v): the normal CDF (from the erf above) plus
 // v times the normal density exp(-v^2 / 2) / sqrt(2 pi).
 __device__ __forceinline__ float gelu_erf_grad(float v) {
-  return 0.5f * (1.0f + erf_as7126(v * 0.70710678118654752440f)) +
-         v * 0.39894228040143267794f * __expf(-0.5f * v * v);
+  return 0.5f * (1.0f + erf_as7126(v * kRsqrt2)) +
+         v * 0.39894228040143267794f * ex2_approx(v * v * (-0.5f * kLog2e));
 }
 __device__ __forceinline__ float apply_act(float v, int act) {
   return act == MOE_ACT_RELU ? fmaxf(v, 0.0f) : gelu_erf(v);

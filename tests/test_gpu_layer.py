@@ -83,6 +83,12 @@ SMALL = [
     # T*k too large for the one-block counting sort: histogram/scan/rank blocks
     Workload("bf16_multiblock_permute", T=40000, d_model=64, d_ff=64, n_experts=12,
              top_k=3, act=ACT_RELU, dtype=DT_BF16, capacity_factor=1.05, seed=24),
+    # 256-wide tiles in both Linears: with a shared expert and GELU; with ReLU,
+    # capacity drops and ragged groups
+    Workload("bf16_bn256_shared", T=1000, d_model=256, d_ff=512, n_experts=8, top_k=2,
+             act=ACT_GELU_ERF, dtype=DT_BF16, d_ff_shared=512, seed=25),
+    Workload("bf16_bn256_relu_cap", T=777, d_model=512, d_ff=256, n_experts=6, top_k=2,
+             act=ACT_RELU, dtype=DT_BF16, capacity_factor=0.9, seed=26),
 ]
 
 
