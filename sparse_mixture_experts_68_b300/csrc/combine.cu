@@ -6,10 +6,9 @@
 // one warp per token, fp32 accumulation in slot order, 16-byte vectors.
 // Dropped slots (token_row < 0) add nothing; the shared expert's row adds
 // with weight 1 (roadtointelligence.com "Total versus active parameters").
-// With many slots per token (k > 8: wide top-k, or one slot per expert under
-// expert-choice routing) the warp first reads its token's slots 32 at a time
-// and keeps the live ones, in slot order, in shared memory, so the column
-// passes walk only those.
+// The warp first reads its token's slots 32 at a time and keeps the live
+// ones (and the shared row), in slot order, in shared memory, so that the
+// column passes walk only those, two rows' loads in flight at a time.
 //
 // Load statistics: see stats.cuh.
 #include "kernels.h"
@@ -20,36 +19,37 @@ namespace moe {
 namespace {
 
 constexpr int kCombineWarps = 8;
-constexpr int kCompactAbove = 8;                   // slots per token above which to compact
 
-template <typename T, bool COMPACT>
+template <typename T>
 __global__ void __launch_bounds__(kCombineWarps * 32)
     combine_kernel(const T* __restrict__ Yp, const int32_t* __restrict__ token_row,
                    const float* __restrict__ topk_w, const int32_t* __restrict__ offsets,
                    int Ttok, int k, int N, int has_shared, int64_t d, T* __restrict__ y) {
   constexpr int V = Vec16<T>::n;
   constexpr int CB = 4;                            // 16-byte columns per lane per pass
-  extern __shared__ int2 live[];                   // COMPACT: [kCombineWarps][k] (row, gate)
+  extern __shared__ int2 live[];                   // [kCombineWarps][k + 1] (row, gate)
   pdl_launch_dependents();
   pdl_wait_previous();
   const int lane = threadIdx.x & 31;
   const int64_t t = int64_t(blockIdx.x) * kCombineWarps + (threadIdx.x >> 5);
   if (t >= Ttok) return;
-  const int64_t shared_row = has_shared ? int64_t(offsets[N]) + t : -1;
-  int n_live = k;
-  int2* mine = live + (threadIdx.x >> 5) * k;
-  if (COMPACT) {
-    n_live = 0;
-    for (int j0 = 0; j0 < k; j0 += 32) {
-      const int j = j0 + lane;
-      const int r = j < k ? token_row[t * k + j] : -1;
-      const float g = j < k ? topk_w[t * k + j] : 0.f;
-      const uint32_t m = __ballot_sync(0xffffffffu, r >= 0);
-      if (r >= 0) mine[n_live + __popc(m & ((1u << lane) - 1u))] = make_int2(r, __float_as_int(g));
-      n_live += __popc(m);
-    }
-    __syncwarp();
+  // the token's kept rows in slot order, then the shared expert's (gate 1):
+  // all slots read at once, so that the row loads below depend on one round trip
+  int2* mine = live + (threadIdx.x >> 5) * (k + 1);
+  int n_live = 0;
+  for (int j0 = 0; j0 < k; j0 += 32) {
+    const int j = j0 + lane;
+    const int r = j < k ? token_row[t * k + j] : -1;
+    const float g = j < k ? topk_w[t * k + j] : 0.f;
+    const uint32_t m = __ballot_sync(0xffffffffu, r >= 0);
+    if (r >= 0) mine[n_live + __popc(m & ((1u << lane) - 1u))] = make_int2(r, __float_as_int(g));
+    n_live += __popc(m);
   }
+  if (has_shared) {
+    if (lane == 0) mine[n_live] = make_int2(offsets[N] + int(t), __float_as_int(1.f));
+    ++n_live;
+  }
+  __syncwarp();
   const int64_t nv = d / V;
   for (int64_t c0 = lane; c0 < nv; c0 += 32 * CB) {
     float acc[CB][V];
@@ -57,36 +57,36 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
     for (int b = 0; b < CB; ++b)
 #pragma unroll
       for (int i = 0; i < V; ++i) acc[b][i] = 0.f;
-    for (int j = 0; j <= n_live; ++j) {
-      int64_t r;
-      float g;
-      if (j < n_live) {
-        if (COMPACT) {
-          const int2 rg = mine[j];
-          r = rg.x;
-          g = __int_as_float(rg.y);
-        } else {
-          r = token_row[t * k + j];
-          g = topk_w[t * k + j];
-        }
-      } else {
-        r = shared_row;                            // the shared expert, weight 1
-        g = 1.f;
-      }
-      if (r < 0) continue;
-      const uint4* row = reinterpret_cast<const uint4*>(Yp + r * d);
-      uint4 q[CB];
+    // two rows' loads in flight, accumulated in slot order
+    for (int j = 0; j < n_live; j += 2) {
+      const bool two = j + 1 < n_live;
+      const int2 rg0 = mine[j];
+      const int2 rg1 = two ? mine[j + 1] : rg0;
+      const uint4* row0 = reinterpret_cast<const uint4*>(Yp + int64_t(rg0.x) * d);
+      const uint4* row1 = reinterpret_cast<const uint4*>(Yp + int64_t(rg1.x) * d);
+      uint4 q0[CB], q1[CB];
 #pragma unroll
       for (int b = 0; b < CB; ++b) {
         const int64_t c = c0 + 32 * b;
-        q[b] = c < nv ? __ldg(row + c) : make_uint4(0, 0, 0, 0);
+        q0[b] = c < nv ? __ldg(row0 + c) : make_uint4(0, 0, 0, 0);
+        q1[b] = (two && c < nv) ? __ldg(row1 + c) : make_uint4(0, 0, 0, 0);
       }
+      const float g0 = __int_as_float(rg0.y), g1 = __int_as_float(rg1.y);
 #pragma unroll
       for (int b = 0; b < CB; ++b) {
         float v[V];
-        Vec16<T>::load(reinterpret_cast<const T*>(&q[b]), v);
+        Vec16<T>::load(reinterpret_cast<const T*>(&q0[b]), v);
 #pragma unroll
-        for (int i = 0; i < V; ++i) acc[b][i] = fmaf(g, v[i], acc[b][i]);
+        for (int i = 0; i < V; ++i) acc[b][i] = fmaf(g0, v[i], acc[b][i]);
+      }
+      if (two) {
+#pragma unroll
+        for (int b = 0; b < CB; ++b) {
+          float v[V];
+          Vec16<T>::load(reinterpret_cast<const T*>(&q1[b]), v);
+#pragma unroll
+          for (int i = 0; i < V; ++i) acc[b][i] = fmaf(g1, v[i], acc[b][i]);
+        }
       }
     }
 #pragma unroll
@@ -116,8 +116,7 @@ cudaError_t launch_combine(const moe_config& c, const void* Yp, const int32_t* t
   if (c.T == 0) return cudaSuccess;
   const unsigned blocks = unsigned(ceil_div(c.T, kCombineWarps));
   const int hs = c.d_ff_shared > 0 ? 1 : 0;
-  const bool compact = c.top_k > kCompactAbove;
-  const size_t smem = compact ? size_t(kCombineWarps) * size_t(c.top_k) * sizeof(int2) : 0;
+  const size_t smem = size_t(kCombineWarps) * size_t(c.top_k + 1) * sizeof(int2);
   auto go = [&](auto kern, auto* Yt, auto* yt) -> cudaError_t {
     if (smem > 48 * 1024) {
       const cudaError_t e =
@@ -131,13 +130,11 @@ cudaError_t launch_combine(const moe_config& c, const void* Yp, const int32_t* t
   if (c.dtype == MOE_F32) {
     const float* Yt = static_cast<const float*>(Yp);
     float* yt = static_cast<float*>(y);
-    return compact ? go(combine_kernel<float, true>, Yt, yt)
-                   : go(combine_kernel<float, false>, Yt, yt);
+    return go(combine_kernel<float>, Yt, yt);
   }
   const __nv_bfloat16* Yt = static_cast<const __nv_bfloat16*>(Yp);
   __nv_bfloat16* yt = static_cast<__nv_bfloat16*>(y);
-  return compact ? go(combine_kernel<__nv_bfloat16, true>, Yt, yt)
-                 : go(combine_kernel<__nv_bfloat16, false>, Yt, yt);
+  return go(combine_kernel<__nv_bfloat16>, Yt, yt);
 }
 
 cudaError_t launch_load_stats(const moe_config& c, const float* prob_partials,

@@ -41,7 +41,10 @@ __device__ __forceinline__ void stats_kahan_add(float v, float& s, float& comp) 
 }
 
 // var(c) / mean(c)^2 = N (N Q - S^2) / ((N - 1) S^2) from S = sum c, Q = sum c^2:
-// N Q - S^2 exactly in 128-bit integers, one rounding at the end.
+// N Q - S^2 exactly in 128-bit integers; numerator a and denominator b in
+// fp64 products, and the quotient without an fp64 division: q0 = a / b in
+// fp32, then one correction q0 + (a - q0 b) / b with the residual exact in
+// an fp64 fma and its quotient needing only fp32 accuracy; then one rounding.
 __device__ __forceinline__ float cv_squared_of(int N, long long S, long long Q) {
   if (N <= 1 || S <= 0) return 0.f;
   const unsigned __int128 nq = (unsigned __int128)(unsigned long long)N * (unsigned long long)Q;
@@ -50,7 +53,11 @@ __device__ __forceinline__ float cv_squared_of(int N, long long S, long long Q) 
   const double numd = double((unsigned long long)(num >> 64)) * 18446744073709551616.0 +
                       double((unsigned long long)num);
   const double sd = double(S);
-  return float(double(N) * numd / (double(N - 1) * sd * sd));
+  const double a = double(N) * numd, b = double(N - 1) * sd * sd;
+  const float bf = float(b);
+  const float q0 = float(a) / bf;
+  const double r = fma(-double(q0), b, a);
+  return float(double(q0) + r * double(1.0f / bf));
 }
 
 // Runs on all kStatsThreads threads of a block (blockDim.x == kStatsThreads).
