@@ -21,14 +21,13 @@ cudaError_t launch_grouped_ffn_f32(const moe_config& c, const GroupedFfnArgs& g,
   // first Linear: [rows, d] x [d_ff, d]^T
   a.A = g.Xp; a.B = g.w->W1; a.Bs = g.w->W1s; a.bias = g.w->b1; a.bias_s = g.w->b1s;
   a.C = g.H; a.K = c.d_model; a.Nc = c.d_ff;
-  dim3 grid1(unsigned(ceil_div(c.d_ff, kSimtBN)), unsigned(ceil_div(g.rows_max, kSimtBM)));
-  cudaError_t e = launch_pdl(simt_gemm_kernel<float, float>, grid1, dim3(kSimtThreads), 0, s, a);
+  cudaError_t e = launch_simt_gemm<float, float>(a, g.rows_max, g.num_sms, s);
   if (e == cudaSuccess && g.pre_out) {
     // the pre-activation for a later backward: the same Linear without it
     SimtGemmArgs pa = a;
     pa.act = -1;
     pa.C = g.pre_out;
-    e = launch_pdl(simt_gemm_kernel<float, float>, grid1, dim3(kSimtThreads), 0, s, pa);
+    e = launch_simt_gemm<float, float>(pa, g.rows_max, g.num_sms, s);
   }
   if (e == cudaSuccess) e = record_event(g.mid_event, s);
   if (e != cudaSuccess) return e;
@@ -36,8 +35,7 @@ cudaError_t launch_grouped_ffn_f32(const moe_config& c, const GroupedFfnArgs& g,
   a.act = -1;
   a.A = g.H; a.B = g.w->W2; a.Bs = g.w->W2s; a.bias = g.w->b2; a.bias_s = g.w->b2s;
   a.C = g.Yp; a.K = c.d_ff; a.Nc = c.d_model;
-  dim3 grid2(unsigned(ceil_div(c.d_model, kSimtBN)), unsigned(ceil_div(g.rows_max, kSimtBM)));
-  return launch_pdl(simt_gemm_kernel<float, float>, grid2, dim3(kSimtThreads), 0, s, a);
+  return launch_simt_gemm<float, float>(a, g.rows_max, g.num_sms, s);
 }
 
 // ---- backward on CUDA cores (fp32 layers) ----------------------------------------------
@@ -56,8 +54,7 @@ cudaError_t launch_grouped_linear_f32(const moe_config& c, const BwdGemmArgs& g,
   a.act = -1;
   a.A = A; a.B = W; a.Bs = Ws; a.bias = bias; a.bias_s = bias_s;
   a.C = out; a.K = K; a.Nc = Nd;
-  dim3 grid(unsigned(ceil_div(Nd, kSimtBN)), unsigned(ceil_div(g.rows_max, kSimtBM)));
-  return launch_pdl(simt_gemm_kernel<float, float>, grid, dim3(kSimtThreads), 0, s, a);
+  return launch_simt_gemm<float, float>(a, g.rows_max, g.num_sms, s);
 }
 
 // out = dOut W[e] per group (the weight as stored, [K, Nd]), times act'(pre)
@@ -77,8 +74,7 @@ cudaError_t launch_bwd_dgrad_f32(const moe_config& c, const BwdGemmArgs& g, cons
   a.pre = act >= 0 ? pre : nullptr;
   a.A = dOut; a.B = W; a.Bs = Ws;
   a.C = out; a.K = K; a.Nc = Nd;
-  dim3 grid(unsigned(ceil_div(Nd, kSimtBN)), unsigned(ceil_div(g.rows_max, kSimtBM)));
-  return launch_pdl(simt_gemm_kernel<float, float>, grid, dim3(kSimtThreads), 0, s, a);
+  return launch_simt_gemm<float, float>(a, g.rows_max, g.num_sms, s);
 }
 
 // out[e] = L[group e]^T R[group e] per group ([Md, Nd]; the shared one in out_s)

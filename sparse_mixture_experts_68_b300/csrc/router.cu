@@ -17,10 +17,8 @@ cudaError_t launch_router_logits(const moe_config& c, const void* x, const void*
   a.A = x; a.B = W_g; a.bias = b_g; a.C = logits;
   a.rows = c.T; a.K = c.d_model; a.Nc = c.n_experts;
   a.act = -1;
-  dim3 grid(unsigned(ceil_div(c.n_experts, kSimtBN)), unsigned(ceil_div(c.T, kSimtBM)));
-  if (c.dtype == MOE_F32)
-    return launch_pdl(simt_gemm_kernel<float, float>, grid, dim3(kSimtThreads), 0, s, a);
-  return launch_pdl(simt_gemm_kernel<__nv_bfloat16, float>, grid, dim3(kSimtThreads), 0, s, a);
+  if (c.dtype == MOE_F32) return launch_simt_gemm<float, float>(a, c.T, 0, s);
+  return launch_simt_gemm<__nv_bfloat16, float>(a, c.T, 0, s);
 }
 
 // One warp per token.  Lane l holds the scores of experts l, l+32, ...,

@@ -8,6 +8,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "kernels.h"
 
 namespace moe {
 
@@ -34,15 +35,56 @@ struct SimtGemmArgs {
 
 constexpr int kSimtBM = 64, kSimtBN = 64, kSimtBK = 16, kSimtThreads = 256;
 
-template <typename TIn, typename TOut>
-__global__ void __launch_bounds__(kSimtThreads) simt_gemm_kernel(SimtGemmArgs a) {
-  __shared__ float As[kSimtBK][kSimtBM + 4];
-  __shared__ float Bs[kSimtBK][kSimtBN + 4];
+// L consecutive elements (L = 2 or 4, aligned to L) as fp32.
+template <typename TIn, int L>
+__device__ __forceinline__ void simt_load(const TIn* p, float (&v)[L]) {
+  if constexpr (sizeof(TIn) == 4) {
+    if constexpr (L == 4) {
+      const float4 q = *reinterpret_cast<const float4*>(p);
+      v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+    } else {
+      const float2 q = *reinterpret_cast<const float2*>(p);
+      v[0] = q.x; v[1] = q.y;
+    }
+  } else {
+    if constexpr (L == 4) {
+      const uint2 q = *reinterpret_cast<const uint2*>(p);
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&q.x));
+      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&q.y));
+      v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+    } else {
+      const uint32_t q = *reinterpret_cast<const uint32_t*>(p);
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&q));
+      v[0] = a.x; v[1] = a.y;
+    }
+  }
+}
+
+// Register-tiled CUDA-core GEMM: a BM x BN tile per block of 256 threads as
+// 16 x 16 threads of TM x TN outputs (TM = BM / 16, TN = BN / 16, each 4 or
+// 8), K in steps of 8 through two shared-memory buffers (the next step's
+// global loads are in flight while the current one is multiplied; one
+// barrier per step).  A (and B in the [Nc, K] layout) is stored transposed,
+// [k][row] with rows padded by 4 floats, so that the loader's writes are free
+// of bank conflicts.  A thread's rows (columns) are groups of 4 consecutive
+// ones, BM / 2 (BN / 2) apart when it holds 8: its 16-byte reads then cover
+// 16 consecutive words across the warp, free of bank conflicts.  Rows past
+// the group's live rows read as zeros and are not stored; K % 8 == 0.
+template <typename TIn, typename TOut, int BM, int BN>
+__global__ void __launch_bounds__(kSimtThreads, 2) simt_gemm_kernel(SimtGemmArgs a) {
+  constexpr int BK = 8;
+  constexpr int TM = BM / 16, TN = BN / 16;
+  constexpr int LA = BM / 32, LB = BN / 32;       // elements per thread per k-step
+  // row (column) of a thread's i-th output: 4-wide groups, BM / 2 apart
+  auto trow = [](int ty, int i) { return (i >> 2) * (BM / 2) + ty * 4 + (i & 3); };
+  auto tcol = [](int tx, int j) { return (j >> 2) * (BN / 2) + tx * 4 + (j & 3); };
+  __shared__ __align__(16) float As[2][BK][BM + 4];
+  __shared__ __align__(16) float Bs[2][BK][BN + 4];
   pdl_launch_dependents();
   pdl_wait_previous();
 
-  const int64_t row0 = int64_t(blockIdx.y) * kSimtBM;
-  const int64_t col0 = int64_t(blockIdx.x) * kSimtBN;
+  const int64_t row0 = int64_t(blockIdx.y) * BM;
+  const int64_t col0 = int64_t(blockIdx.x) * BN;
   const TIn* B = static_cast<const TIn*>(a.B);
   const TIn* bias = static_cast<const TIn*>(a.bias);
   int64_t row_end;                     // one past the last live row of this tile's group
@@ -72,61 +114,96 @@ __global__ void __launch_bounds__(kSimtThreads) simt_gemm_kernel(SimtGemmArgs a)
   const TIn* A = static_cast<const TIn*>(a.A);
   const int tid = threadIdx.x;
   const int tx = tid & 15, ty = tid >> 4;
-  const int lr = tid >> 2;             // loader: row within the tile
-  const int lk = (tid & 3) * 4;        // loader: first of 4 k values
+  // loaders: A row a_r, k offset a_k; B as [Nc, K] the same with LB; B as
+  // [K, Nc]: k-row kn_k, columns kn_c .. kn_c + LB - 1
+  const int a_r = tid / (BK / LA), a_k = (tid % (BK / LA)) * LA;
+  const int b_r = tid / (BK / LB), b_k = (tid % (BK / LB)) * LB;
+  const int kn_k = tid / (BN / LB), kn_c = (tid % (BN / LB)) * LB;
+  const bool a_ok = row0 + a_r < row_end;
+  const bool b_ok = a.b_kn ? true : col0 + b_r < a.Nc;
+  float ra[LA], rb[LB];
 
-  float acc[4][4];
+  auto fetch = [&](int64_t k0) {
+    if (a_ok) {
+      simt_load<TIn, LA>(A + (row0 + a_r) * a.K + k0 + a_k, ra);
+    } else {
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-
-  for (int64_t k0 = 0; k0 < a.K; k0 += kSimtBK) {
-    {
-      const int64_t r = row0 + lr, kk = k0 + lk;
-      const bool ok = r < row_end && kk < a.K;   // K % 4 == 0: 4 values all in or all out
-#pragma unroll
-      for (int q = 0; q < 4; ++q) As[lk + q][lr] = ok ? to_f32(A[r * a.K + kk + q]) : 0.f;
-      if (a.b_kn) {
-        // B[k, n]: 64 consecutive columns of 4 K-rows per pass of 256 threads
-        const int nn = tid & 63, kq = tid >> 6;
-        const int64_t c = col0 + nn;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int64_t kr = k0 + 4 * kq + q;
-          Bs[4 * kq + q][nn] = (c < a.Nc && kr < a.K) ? to_f32(B[kr * a.Nc + c]) : 0.f;
-        }
+      for (int q = 0; q < LA; ++q) ra[q] = 0.f;
+    }
+    if (a.b_kn) {
+      const int64_t c = col0 + kn_c;
+      const TIn* src = B + (k0 + kn_k) * a.Nc + c;
+      if (c + LB <= a.Nc && (a.Nc % LB) == 0) {
+        simt_load<TIn, LB>(src, rb);
       } else {
-        const int64_t c = col0 + lr;
-        const bool okb = c < a.Nc && kk < a.K;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) Bs[lk + q][lr] = okb ? to_f32(B[c * a.K + kk + q]) : 0.f;
+        for (int q = 0; q < LB; ++q) rb[q] = c + q < a.Nc ? to_f32(src[q]) : 0.f;
       }
+    } else if (b_ok) {
+      simt_load<TIn, LB>(B + (col0 + b_r) * a.K + k0 + b_k, rb);
+    } else {
+#pragma unroll
+      for (int q = 0; q < LB; ++q) rb[q] = 0.f;
     }
-    __syncthreads();
+  };
+  auto stash = [&](int buf) {
 #pragma unroll
-    for (int kk = 0; kk < kSimtBK; ++kk) {
-      float av[4], bv[4];
+    for (int q = 0; q < LA; ++q) As[buf][a_k + q][a_r] = ra[q];
+    if (a.b_kn) {
+      if constexpr (LB == 4)
+        *reinterpret_cast<float4*>(&Bs[buf][kn_k][kn_c]) = make_float4(rb[0], rb[1], rb[2], rb[3]);
+      else
+        *reinterpret_cast<float2*>(&Bs[buf][kn_k][kn_c]) = make_float2(rb[0], rb[1]);
+    } else {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) av[i] = As[kk][ty + 16 * i];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) bv[j] = Bs[kk][tx + 16 * j];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+      for (int q = 0; q < LB; ++q) Bs[buf][b_k + q][b_r] = rb[q];
     }
+  };
+
+  float acc[TM][TN];
+#pragma unroll
+  for (int i = 0; i < TM; ++i)
+#pragma unroll
+    for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
+
+  fetch(0);
+  stash(0);
+  __syncthreads();
+  int buf = 0;
+  for (int64_t k0 = 0; k0 < a.K; k0 += BK) {
+    const bool more = k0 + BK < a.K;
+    if (more) fetch(k0 + BK);
+#pragma unroll
+    for (int kk = 0; kk < BK; ++kk) {
+      float av[TM], bv[TN];
+#pragma unroll
+      for (int i = 0; i < TM; i += 4) {
+        const float4 q = *reinterpret_cast<const float4*>(&As[buf][kk][trow(ty, i)]);
+        av[i] = q.x; av[i + 1] = q.y; av[i + 2] = q.z; av[i + 3] = q.w;
+      }
+#pragma unroll
+      for (int j = 0; j < TN; j += 4) {
+        const float4 q = *reinterpret_cast<const float4*>(&Bs[buf][kk][tcol(tx, j)]);
+        bv[j] = q.x; bv[j + 1] = q.y; bv[j + 2] = q.z; bv[j + 3] = q.w;
+      }
+#pragma unroll
+      for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    if (more) stash(buf ^ 1);
     __syncthreads();
+    buf ^= 1;
   }
 
   TOut* C = static_cast<TOut*>(a.C);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int64_t r = row0 + ty + 16 * i;
+  for (int i = 0; i < TM; ++i) {
+    const int64_t r = row0 + trow(ty, i);
     if (r >= row_end) continue;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int64_t c = col0 + tx + 16 * j;
+    for (int j = 0; j < TN; ++j) {
+      const int64_t c = col0 + tcol(tx, j);
       if (c >= a.Nc) continue;
       float v = acc[i][j];
       if (bias) v += to_f32(bias[c]);
@@ -135,9 +212,42 @@ __global__ void __launch_bounds__(kSimtThreads) simt_gemm_kernel(SimtGemmArgs a)
         const float pa = to_f32(static_cast<const TIn*>(a.pre)[r * a.Nc + c]);
         v *= a.dact == MOE_ACT_RELU ? (pa > 0.f ? 1.f : 0.f) : gelu_erf_grad(pa);
       }
-      C[r * a.Nc + c] = from_f32<TOut>(v);
+      acc[i][j] = v;
+    }
+#pragma unroll
+    for (int j = 0; j < TN; j += 4) {
+      const int64_t cb = col0 + tcol(tx, j);           // 4 consecutive columns
+      if constexpr (sizeof(TOut) == 4) {
+        if (cb + 4 <= a.Nc && (a.Nc % 4) == 0) {
+          *reinterpret_cast<float4*>(C + r * a.Nc + cb) =
+              make_float4(acc[i][j], acc[i][j + 1], acc[i][j + 2], acc[i][j + 3]);
+          continue;
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (cb + q < a.Nc) C[r * a.Nc + cb + q] = from_f32<TOut>(acc[i][j + q]);
     }
   }
+}
+
+// Launches simt_gemm_kernel over `rows` rows (grouped: the grouped row count)
+// with the widest tile that still gives about two blocks per SM.
+template <typename TIn, typename TOut>
+cudaError_t launch_simt_gemm(const SimtGemmArgs& a, int64_t rows, int num_sms, cudaStream_t s) {
+  auto blocks = [&](int bm, int bn) { return ceil_div(a.Nc, bn) * ceil_div(rows, bm); };
+  const int64_t want = 2 * int64_t(num_sms > 0 ? num_sms : 148);
+  if (blocks(128, 128) >= want)
+    return launch_pdl(simt_gemm_kernel<TIn, TOut, 128, 128>,
+                      dim3(unsigned(ceil_div(a.Nc, 128)), unsigned(ceil_div(rows, 128))),
+                      dim3(kSimtThreads), 0, s, a);
+  if (blocks(128, 64) >= want)
+    return launch_pdl(simt_gemm_kernel<TIn, TOut, 128, 64>,
+                      dim3(unsigned(ceil_div(a.Nc, 64)), unsigned(ceil_div(rows, 128))),
+                      dim3(kSimtThreads), 0, s, a);
+  return launch_pdl(simt_gemm_kernel<TIn, TOut, 64, 64>,
+                    dim3(unsigned(ceil_div(a.Nc, 64)), unsigned(ceil_div(rows, 64))),
+                    dim3(kSimtThreads), 0, s, a);
 }
 
 // Grouped weight gradient on CUDA cores: for group g (blockIdx.z),
