@@ -89,6 +89,10 @@ SMALL = [
              act=ACT_GELU_ERF, dtype=DT_BF16, d_ff_shared=512, seed=25),
     Workload("bf16_bn256_relu_cap", T=777, d_model=512, d_ff=256, n_experts=6, top_k=2,
              act=ACT_RELU, dtype=DT_BF16, capacity_factor=0.9, seed=26),
+    # fp32 CUDA-core GEMMs on each tile size: the first Linear (d_ff = 1024 columns
+    # over ~4500 grouped rows) on 128 x 64 tiles, the second on 64 x 64
+    Workload("f32_tile128x64", T=2000, d_model=64, d_ff=1024, n_experts=4, top_k=2,
+             act=ACT_GELU_ERF, dtype=DT_F32, seed=27),
 ]
 
 
