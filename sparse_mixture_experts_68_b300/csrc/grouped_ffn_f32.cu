@@ -21,14 +21,10 @@ cudaError_t launch_grouped_ffn_f32(const moe_config& c, const GroupedFfnArgs& g,
   // first Linear: [rows, d] x [d_ff, d]^T
   a.A = g.Xp; a.B = g.w->W1; a.Bs = g.w->W1s; a.bias = g.w->b1; a.bias_s = g.w->b1s;
   a.C = g.H; a.K = c.d_model; a.Nc = c.d_ff;
+  // the pre-activation for a later backward, from the same epilogue
+  a.C_pre = g.pre_out;
   cudaError_t e = launch_simt_gemm<float, float>(a, g.rows_max, g.num_sms, s);
-  if (e == cudaSuccess && g.pre_out) {
-    // the pre-activation for a later backward: the same Linear without it
-    SimtGemmArgs pa = a;
-    pa.act = -1;
-    pa.C = g.pre_out;
-    e = launch_simt_gemm<float, float>(pa, g.rows_max, g.num_sms, s);
-  }
+  a.C_pre = nullptr;
   if (e == cudaSuccess) e = record_event(g.mid_event, s);
   if (e != cudaSuccess) return e;
   // second Linear: [rows, d_ff] x [d, d_ff]^T
@@ -88,8 +84,15 @@ cudaError_t launch_bwd_wgrad_f32(const moe_config& c, const BwdGemmArgs& g, cons
   a.n_routed = int32_t(c.n_experts);
   a.shared_rows = c.d_ff_shared > 0 ? int32_t(c.T) : 0;
   const unsigned groups = unsigned(c.n_experts + (c.d_ff_shared > 0 ? 1 : 0));
-  dim3 grid(unsigned(ceil_div(Nd, kSimtBN)), unsigned(ceil_div(Md, kSimtBM)), groups);
-  return launch_pdl(simt_wgrad_kernel<float>, grid, dim3(kSimtThreads), 0, s, a);
+  // 128 x 128 tiles when they still give about two blocks per SM, else 64 x 64
+  const int64_t want = 2 * int64_t(g.num_sms > 0 ? g.num_sms : 148);
+  if (ceil_div(Nd, 128) * ceil_div(Md, 128) * groups >= want)
+    return launch_pdl(simt_wgrad_kernel<float, 128, 128>,
+                      dim3(unsigned(ceil_div(Nd, 128)), unsigned(ceil_div(Md, 128)), groups),
+                      dim3(kSimtThreads), 0, s, a);
+  return launch_pdl(simt_wgrad_kernel<float, 64, 64>,
+                    dim3(unsigned(ceil_div(Nd, 64)), unsigned(ceil_div(Md, 64)), groups),
+                    dim3(kSimtThreads), 0, s, a);
 }
 
 }  // namespace moe

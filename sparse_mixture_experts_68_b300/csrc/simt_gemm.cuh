@@ -31,9 +31,10 @@ struct SimtGemmArgs {
   int32_t b_kn;
   int32_t dact;             // MOE_ACT_* of act' (read only when pre is set)
   const void* pre;          // [rows, Nc] or nullptr
+  void* C_pre;              // with act >= 0: also store the pre-activation here (or nullptr)
 };
 
-constexpr int kSimtBM = 64, kSimtBN = 64, kSimtBK = 16, kSimtThreads = 256;
+constexpr int kSimtThreads = 256;
 
 // L consecutive elements (L = 2 or 4, aligned to L) as fp32.
 template <typename TIn, int L>
@@ -60,6 +61,58 @@ __device__ __forceinline__ void simt_load(const TIn* p, float (&v)[L]) {
   }
 }
 
+// Row (column) of a thread's i-th output in a BM (BN) tile: 4-wide groups,
+// BM / 2 (BN / 2) apart when a thread holds 8.
+template <int BM>
+__device__ __forceinline__ int simt_trow(int ty, int i) {
+  return (i >> 2) * (BM / 2) + ty * 4 + (i & 3);
+}
+
+// The shared K loop of the register-tiled kernels: `fetch(k0)` loads the
+// k-step at k0 into registers, `stash(buf)` writes them to buffer buf; the
+// next step's loads are in flight while the current step is multiplied.
+template <int BM, int BN, class Fetch, class Stash>
+__device__ __forceinline__ void simt_mainloop(float (&As)[2][8][BM + 4],
+                                              float (&Bs)[2][8][BN + 4], int64_t K,
+                                              Fetch&& fetch, Stash&& stash,
+                                              float (&acc)[BM / 16][BN / 16], int tx, int ty) {
+  constexpr int BK = 8, TM = BM / 16, TN = BN / 16;
+#pragma unroll
+  for (int i = 0; i < TM; ++i)
+#pragma unroll
+    for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
+  if (K <= 0) return;
+  fetch(0);
+  stash(0);
+  __syncthreads();
+  int buf = 0;
+  for (int64_t k0 = 0; k0 < K; k0 += BK) {
+    const bool more = k0 + BK < K;
+    if (more) fetch(k0 + BK);
+#pragma unroll
+    for (int kk = 0; kk < BK; ++kk) {
+      float av[TM], bv[TN];
+#pragma unroll
+      for (int i = 0; i < TM; i += 4) {
+        const float4 q = *reinterpret_cast<const float4*>(&As[buf][kk][simt_trow<BM>(ty, i)]);
+        av[i] = q.x; av[i + 1] = q.y; av[i + 2] = q.z; av[i + 3] = q.w;
+      }
+#pragma unroll
+      for (int j = 0; j < TN; j += 4) {
+        const float4 q = *reinterpret_cast<const float4*>(&Bs[buf][kk][simt_trow<BN>(tx, j)]);
+        bv[j] = q.x; bv[j + 1] = q.y; bv[j + 2] = q.z; bv[j + 3] = q.w;
+      }
+#pragma unroll
+      for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    if (more) stash(buf ^ 1);
+    __syncthreads();
+    buf ^= 1;
+  }
+}
+
 // Register-tiled CUDA-core GEMM: a BM x BN tile per block of 256 threads as
 // 16 x 16 threads of TM x TN outputs (TM = BM / 16, TN = BN / 16, each 4 or
 // 8), K in steps of 8 through two shared-memory buffers (the next step's
@@ -75,9 +128,6 @@ __global__ void __launch_bounds__(kSimtThreads, 2) simt_gemm_kernel(SimtGemmArgs
   constexpr int BK = 8;
   constexpr int TM = BM / 16, TN = BN / 16;
   constexpr int LA = BM / 32, LB = BN / 32;       // elements per thread per k-step
-  // row (column) of a thread's i-th output: 4-wide groups, BM / 2 apart
-  auto trow = [](int ty, int i) { return (i >> 2) * (BM / 2) + ty * 4 + (i & 3); };
-  auto tcol = [](int tx, int j) { return (j >> 2) * (BN / 2) + tx * 4 + (j & 3); };
   __shared__ __align__(16) float As[2][BK][BM + 4];
   __shared__ __align__(16) float Bs[2][BK][BN + 4];
   pdl_launch_dependents();
@@ -161,52 +211,20 @@ __global__ void __launch_bounds__(kSimtThreads, 2) simt_gemm_kernel(SimtGemmArgs
   };
 
   float acc[TM][TN];
-#pragma unroll
-  for (int i = 0; i < TM; ++i)
-#pragma unroll
-    for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
-
-  fetch(0);
-  stash(0);
-  __syncthreads();
-  int buf = 0;
-  for (int64_t k0 = 0; k0 < a.K; k0 += BK) {
-    const bool more = k0 + BK < a.K;
-    if (more) fetch(k0 + BK);
-#pragma unroll
-    for (int kk = 0; kk < BK; ++kk) {
-      float av[TM], bv[TN];
-#pragma unroll
-      for (int i = 0; i < TM; i += 4) {
-        const float4 q = *reinterpret_cast<const float4*>(&As[buf][kk][trow(ty, i)]);
-        av[i] = q.x; av[i + 1] = q.y; av[i + 2] = q.z; av[i + 3] = q.w;
-      }
-#pragma unroll
-      for (int j = 0; j < TN; j += 4) {
-        const float4 q = *reinterpret_cast<const float4*>(&Bs[buf][kk][tcol(tx, j)]);
-        bv[j] = q.x; bv[j + 1] = q.y; bv[j + 2] = q.z; bv[j + 3] = q.w;
-      }
-#pragma unroll
-      for (int i = 0; i < TM; ++i)
-#pragma unroll
-        for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
-    }
-    if (more) stash(buf ^ 1);
-    __syncthreads();
-    buf ^= 1;
-  }
+  simt_mainloop<BM, BN>(As, Bs, a.K, fetch, stash, acc, tx, ty);
 
   TOut* C = static_cast<TOut*>(a.C);
 #pragma unroll
   for (int i = 0; i < TM; ++i) {
-    const int64_t r = row0 + trow(ty, i);
+    const int64_t r = row0 + simt_trow<BM>(ty, i);
     if (r >= row_end) continue;
 #pragma unroll
     for (int j = 0; j < TN; ++j) {
-      const int64_t c = col0 + tcol(tx, j);
+      const int64_t c = col0 + simt_trow<BN>(tx, j);
       if (c >= a.Nc) continue;
       float v = acc[i][j];
       if (bias) v += to_f32(bias[c]);
+      if (a.C_pre) static_cast<TOut*>(a.C_pre)[r * a.Nc + c] = from_f32<TOut>(v);
       if (a.act >= 0) v = apply_act(v, a.act);
       if (a.pre) {
         const float pa = to_f32(static_cast<const TIn*>(a.pre)[r * a.Nc + c]);
@@ -216,7 +234,7 @@ __global__ void __launch_bounds__(kSimtThreads, 2) simt_gemm_kernel(SimtGemmArgs
     }
 #pragma unroll
     for (int j = 0; j < TN; j += 4) {
-      const int64_t cb = col0 + tcol(tx, j);           // 4 consecutive columns
+      const int64_t cb = col0 + simt_trow<BN>(tx, j);   // 4 consecutive columns
       if constexpr (sizeof(TOut) == 4) {
         if (cb + 4 <= a.Nc && (a.Nc % 4) == 0) {
           *reinterpret_cast<float4*>(C + r * a.Nc + cb) =
@@ -266,53 +284,77 @@ struct SimtWgradArgs {
   int32_t shared_rows;
 };
 
-template <typename T>
-__global__ void __launch_bounds__(kSimtThreads) simt_wgrad_kernel(SimtWgradArgs a) {
-  __shared__ float Ls[kSimtBK][kSimtBM + 4];
-  __shared__ float Rs[kSimtBK][kSimtBN + 4];
+// The weight gradient on the register-tiled loop: block (n-tile, m-tile,
+// group g) computes its BM x BN tile of C_g = L_g^T R_g, K = the group's live
+// rows in steps of 8 (rows past them read as zeros).  Both operands are
+// [rows, M] row-major, so each k-step loads 16-byte runs along M and N and
+// stores them as they are.  A group with no rows writes zeros.  Md % 4 == 0,
+// Nd % 4 == 0.
+template <typename T, int BM, int BN>
+__global__ void __launch_bounds__(kSimtThreads, 2) simt_wgrad_kernel(SimtWgradArgs a) {
+  constexpr int TM = BM / 16, TN = BN / 16;
+  constexpr int LA = BM / 32, LB = BN / 32;
+  __shared__ __align__(16) float As[2][8][BM + 4];
+  __shared__ __align__(16) float Bs[2][8][BN + 4];
   pdl_launch_dependents();
   pdl_wait_previous();
   const int g = blockIdx.z;
-  const int64_t m0 = int64_t(blockIdx.y) * kSimtBM, n0 = int64_t(blockIdx.x) * kSimtBN;
+  const int64_t m0 = int64_t(blockIdx.y) * BM, n0 = int64_t(blockIdx.x) * BN;
   const int64_t r0 = a.offsets[g];
   const int64_t live = g < a.n_routed ? a.kept[g] : a.shared_rows;
   const T* L = static_cast<const T*>(a.L);
   const T* R = static_cast<const T*>(a.R);
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-  const int cc = tid & 63, kq = tid >> 6;       // loaders: 64 columns x 4 rows per pass
-  float acc[4][4] = {};
-  for (int64_t k0 = 0; k0 < live; k0 += kSimtBK) {
+  const int ka = tid / (BM / LA), ma = (tid % (BM / LA)) * LA;   // k-row, first m
+  const int kb = tid / (BN / LB), nb = (tid % (BN / LB)) * LB;   // k-row, first n
+  const bool a_ok = m0 + ma + LA <= a.Md, b_ok = n0 + nb + LB <= a.Nd;
+  float ra[LA], rb[LB];
+  auto fetch = [&](int64_t k0) {
+    const bool ka_in = k0 + ka < live, kb_in = k0 + kb < live;
+    if (ka_in && a_ok) {
+      simt_load<T, LA>(L + (r0 + k0 + ka) * a.Md + m0 + ma, ra);
+    } else {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int64_t r = k0 + 4 * kq + q;
-      const bool okr = r < live;
-      Ls[4 * kq + q][cc] = (okr && m0 + cc < a.Md) ? to_f32(L[(r0 + r) * a.Md + m0 + cc]) : 0.f;
-      Rs[4 * kq + q][cc] = (okr && n0 + cc < a.Nd) ? to_f32(R[(r0 + r) * a.Nd + n0 + cc]) : 0.f;
+      for (int q = 0; q < LA; ++q) ra[q] = 0.f;
     }
-    __syncthreads();
+    if (kb_in && b_ok) {
+      simt_load<T, LB>(R + (r0 + k0 + kb) * a.Nd + n0 + nb, rb);
+    } else {
 #pragma unroll
-    for (int kk = 0; kk < kSimtBK; ++kk) {
-      float av[4], bv[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) av[i] = Ls[kk][ty + 16 * i];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) bv[j] = Rs[kk][tx + 16 * j];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+      for (int q = 0; q < LB; ++q) rb[q] = 0.f;
     }
-    __syncthreads();
-  }
+  };
+  auto stash = [&](int buf) {
+    if constexpr (LA == 4)
+      *reinterpret_cast<float4*>(&As[buf][ka][ma]) = make_float4(ra[0], ra[1], ra[2], ra[3]);
+    else
+      *reinterpret_cast<float2*>(&As[buf][ka][ma]) = make_float2(ra[0], ra[1]);
+    if constexpr (LB == 4)
+      *reinterpret_cast<float4*>(&Bs[buf][kb][nb]) = make_float4(rb[0], rb[1], rb[2], rb[3]);
+    else
+      *reinterpret_cast<float2*>(&Bs[buf][kb][nb]) = make_float2(rb[0], rb[1]);
+  };
+  float acc[TM][TN];
+  simt_mainloop<BM, BN>(As, Bs, live, fetch, stash, acc, tx, ty);
+
   T* C = g < a.n_routed ? static_cast<T*>(a.C) + int64_t(g) * a.Md * a.Nd : static_cast<T*>(a.Cs);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int64_t m = m0 + ty + 16 * i;
+  for (int i = 0; i < TM; ++i) {
+    const int64_t m = m0 + simt_trow<BM>(ty, i);
     if (m >= a.Md) continue;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int64_t n = n0 + tx + 16 * j;
-      if (n < a.Nd) C[m * a.Nd + n] = from_f32<T>(acc[i][j]);
+    for (int j = 0; j < TN; j += 4) {
+      const int64_t n = n0 + simt_trow<BN>(tx, j);    // 4 consecutive columns
+      if constexpr (sizeof(T) == 4) {
+        if (n + 4 <= a.Nd) {
+          *reinterpret_cast<float4*>(C + m * a.Nd + n) =
+              make_float4(acc[i][j], acc[i][j + 1], acc[i][j + 2], acc[i][j + 3]);
+          continue;
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (n + q < a.Nd) C[m * a.Nd + n + q] = from_f32<T>(acc[i][j + q]);
     }
   }
 }

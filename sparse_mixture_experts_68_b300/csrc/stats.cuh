@@ -87,15 +87,15 @@ __device__ __forceinline__ void block_load_stats(const float* __restrict__ prob_
       const int b0 = warp * rows, b1 = min(nblk, b0 + rows);
       float s = 0.f, comp = 0.f;
       if (lane < N) {
-        int b = b0;
-        for (; b + 8 <= b1; b += 8) {
+        for (int b = b0; b < b1; b += 8) {        // eight loads in flight, added in order
           float v[8];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) v[u] = prob_partials[int64_t(b + u) * N + lane];
+          for (int u = 0; u < 8; ++u)
+            v[u] = b + u < b1 ? prob_partials[int64_t(b + u) * N + lane] : 0.f;
 #pragma unroll
-          for (int u = 0; u < 8; ++u) stats_kahan_add(v[u], s, comp);
+          for (int u = 0; u < 8; ++u)
+            if (b + u < b1) stats_kahan_add(v[u], s, comp);
         }
-        for (; b < b1; ++b) stats_kahan_add(prob_partials[int64_t(b) * N + lane], s, comp);
       }
       part[warp][lane] = make_float2(s, -comp);
     }
@@ -163,15 +163,15 @@ __device__ __forceinline__ void block_load_stats(const float* __restrict__ prob_
     if (live) {
       const int rows = (nblk + RG - 1) / RG;
       const int b0 = rg * rows, b1 = min(nblk, b0 + rows);
-      int b = b0;
-      for (; b + 8 <= b1; b += 8) {
+      for (int b = b0; b < b1; b += 8) {          // eight loads in flight, added in order
         float v[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) v[u] = prob_partials[int64_t(b + u) * N + e];
+        for (int u = 0; u < 8; ++u)
+          v[u] = b + u < b1 ? prob_partials[int64_t(b + u) * N + e] : 0.f;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) stats_kahan_add(v[u], s, comp);
+        for (int u = 0; u < 8; ++u)
+          if (b + u < b1) stats_kahan_add(v[u], s, comp);
       }
-      for (; b < b1; ++b) stats_kahan_add(prob_partials[int64_t(b) * N + e], s, comp);
     }
     part[warp][lane] = make_float2(s, -comp);
     __syncthreads();

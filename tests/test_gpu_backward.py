@@ -243,7 +243,7 @@ KEEP_PRE = [
     Workload("bwd_keep_decode", T=40, d_model=256, d_ff=384, n_experts=8, top_k=1,
              act=ACT_GELU_ERF, dtype=DT_BF16, seed=89),   # decode tiles: a second pass
     Workload("bwd_keep_f32", T=120, d_model=64, d_ff=96, n_experts=4, top_k=2,
-             act=ACT_RELU, dtype=DT_F32, seed=90),        # CUDA cores: a second pass
+             act=ACT_RELU, dtype=DT_F32, seed=90),        # CUDA cores: from the epilogue
     # 256-wide tiles, shared expert: the pre-activation from the first Linear's epilogue
     Workload("bwd_keep_bn256", T=600, d_model=256, d_ff=512, n_experts=4, top_k=2,
              act=ACT_GELU_ERF, dtype=DT_BF16, d_ff_shared=512, seed=93),
