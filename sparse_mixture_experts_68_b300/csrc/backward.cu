@@ -10,12 +10,15 @@
 //                  scores, or the raw probabilities), plus the balance term
 //                  d p[t, e] = alpha 2 (m_e - 1/N) / ((N - 1) T), through the
 //                  softmax over all N -> dz [T, N]
-//   expert FFNs    A1 recomputed (first Linear without its activation), then
+//   expert FFNs    A1 (the forward's kept pre-activation, or recomputed by
+//                  the first Linear without its activation), then
 //                  dA = (dO W2) act'(A1), dXp = dA W1, dW2 = dO^T H,
-//                  dW1 = dA^T Xp on the tensor cores (grouped_bwd_sm103.cu);
-//                  db2, db1 = column sums of dO, dA over each group's rows
+//                  dW1 = dA^T Xp on the tensor cores (grouped_bwd_sm103.cu;
+//                  CUDA cores for fp32 layers); db2, db1 = column sums of
+//                  dO, dA over each group's rows
 //   router         dW_g = dz^T x, db_g = sum_t dz, dx_router = dz W_g
-//                  (CUDA-core GEMMs: K or M is the expert count)
+//                  (tensor cores when N % 64 == 0; else CUDA cores, with
+//                  dx_router folded into dx for N <= 32)
 //   dx             dx[t] = sum of dXp over t's kept rows (+ the shared row)
 //                  + dx_router[t]
 //
