@@ -265,3 +265,90 @@ def test_kept_pre_activation_gives_the_same_gradients(wl):
     if wl.d_ff_shared:
         for n in ("dW1s", "db1s", "dW2s", "db2s"):
             assert torch.equal(getattr(g_kept, n), getattr(g_plain, n)), n
+
+
+def sampled_token_grads(x, dy, W_g, idx, w, p, keep, experts, act, aux, tokens):
+    """Oracle dx, dz and dw of the given tokens only, by the chain rule of
+    moe_backward restricted to their rows: each kept slot's expert FFN
+    forward and backward on that one row, the gates' softmax backward, the
+    balance term (through all tokens' mean probabilities) and the router."""
+    W1, b1, W2, b2 = experts
+    T, N = p.shape
+    k = idx.shape[1]
+    m = p.mean(axis=0)
+    dm = aux * 2.0 * (m - 1.0 / N) / (N - 1)
+    dx = np.zeros((len(tokens), x.shape[1]))
+    dz = np.zeros((len(tokens), N))
+    dw = np.zeros((len(tokens), k))
+    for e in range(N):
+        slots = [(i, j) for i, t in enumerate(tokens) for j in range(k)
+                 if idx[t, j] == e and keep[t, j]]
+        if not slots:
+            continue
+        W1e, W2e = W1[e], W2[e]
+        for i, j in slots:
+            t = tokens[i]
+            a = x[t] @ W1e.T + b1[e]
+            h = O.round_to_bf16(O.activation(a, act))
+            o = h @ W2e.T + b2[e]
+            dw[i, j] = float(dy[t] @ o)
+            dh = (w[t, j] * dy[t]) @ W2e
+            dx[i] += (dh * O.activation_grad(a, act)) @ W1e
+    for i, t in enumerate(tokens):
+        dsel = w[t] * (dw[i] - np.sum(w[t] * dw[i]))
+        dz[i, idx[t]] = dsel
+        dz[i] += O.softmax_backward(p[t], dm / T)
+        dx[i] += dz[i] @ W_g
+    return dx, dz, dw
+
+
+def test_workload_c3_mixtral_prefill_sampled_grads():
+    """The Mixtral-sized layer (T = 4096, d = 4096, d_ff = 14336, 8 experts,
+    top-2, GELU) in the training configuration the bench times: the forward
+    keeps the pre-activation, the backward takes aux = 0.01.  Expert 0's
+    weight and bias gradients in full, and dx / dz / dw of sampled tokens,
+    against the oracle's chain rule on those rows (the full oracle backward
+    would take minutes of float64 GEMMs)."""
+    wl = WORKLOADS["c3_mixtral_prefill"]
+    aux = 0.01
+    t = synth.make_layer(wl, device="cuda")
+    layer = B.MoeLayer(wl, t)
+    out = layer.forward(t["x"], with_logits=True, with_pre_act=True)
+    dy = make_dy(wl, wl.seed)
+    g = layer.backward(t["x"], out, dy, aux_weight=aux, with_scores=True)
+    torch.cuda.synchronize()
+    assert B.get_device_status() == B.MOE_OK
+    cfg = layer.cfg
+    x, dy64 = to64(t["x"]), to64(dy)
+    idx = out.topk_idx.cpu().numpy().astype(np.int64)
+    z = O.router_logits(x, to64(t["W_g"]), to64(t["b_g"]))
+    p = O.softmax(z)
+    assert cfg.renormalize
+    w = O.gates_softmax_of_topk(z, idx)
+    grouping = O.group_by_expert(idx, cfg.n_experts, cfg.capacity)
+    experts = (Experts(t["W1"]), Experts(t["b1"]), Experts(t["W2"]), Experts(t["b2"]))
+
+    # expert 0: every weight and bias gradient
+    rows = grouping.groups[0]
+    ts = np.array([r for r, _ in rows])
+    js = np.array([j for _, j in rows])
+    dO = w[ts, js][:, None] * dy64[ts]
+    _, gW1, gb1, gW2, gb2 = O.expert_ffn_backward(
+        x[ts], experts[0][0], experts[1][0], experts[2][0], experts[3][0], cfg.act, dO,
+        round_hidden_bf16=True)
+    report = {"dW1[0]": rel_l2(to64(g.dW1[0]), gW1), "db1[0]": rel_l2(to64(g.db1[0]), gb1),
+              "dW2[0]": rel_l2(to64(g.dW2[0]), gW2), "db2[0]": rel_l2(to64(g.db2[0]), gb2)}
+
+    # sampled tokens: dx, dz, dw
+    rng = np.random.default_rng(11)
+    tokens = sorted(set(rng.choice(wl.T, size=12, replace=False).tolist()) | {0, wl.T - 1})
+    rdx, rdz, rdw = sampled_token_grads(x, dy64, to64(t["W_g"]), idx, w, p, grouping.keep,
+                                        experts, cfg.act, aux, tokens)
+    report["dx"] = rel_l2(to64(g.dx[tokens]), rdx)
+    report["dz"] = rel_l2(to64(g.dz[tokens]), rdz)
+    report["dw"] = rel_l2(to64(g.dw[tokens]), rdw)
+    print("grad parity c3_mixtral_prefill (sampled)", report)
+    bad = {n: v for n, v in report.items() if not v <= GRAD_TOL[DT_BF16]}
+    assert not bad, f"gradients off: {bad} (all: {report})"
+    del t, layer, out, g
+    torch.cuda.empty_cache()
