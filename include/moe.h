@@ -64,7 +64,7 @@ typedef int32_t moe_status;
 enum {
   MOE_OK = 0,
   MOE_ERR_INVALID_ARG = 1,   /* null / misaligned pointer, bad size */
-  MOE_ERR_UNSUPPORTED = 2,   /* valid layer this build does not run (shape rule) */
+  MOE_ERR_UNSUPPORTED = 2,   /* valid layer the library does not run (shape rule) */
   MOE_ERR_WORKSPACE = 3,     /* workspace or scratch smaller than required */
   MOE_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
   MOE_ERR_TIMEOUT = 5        /* a device-side barrier wait ran out of time */
