@@ -147,9 +147,13 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
 // rows to NE experts (8, 16, 32 or 64).  A butterfly reduce-scatter then
 // leaves each expert's score in DUP = 32/NE adjacent lanes (NE <= 32) or two
 // experts per lane (NE = 64); the softmax, the top-k and the gates follow as
-// above.  One pass over x, no score round trip.
-template <typename TIn, int NE>
-__global__ void __launch_bounds__(kRouterWarps * 32)
+// above.  One pass over x, no score round trip.  WF32 (bf16 layers with at
+// most 16 experts whose W_g takes <= 48 KB as fp32): W_g is staged converted to
+// fp32, laid out [NE][2][d / 8][4] so that a lane's two 16-byte reads of an
+// 8-element vector are each contiguous across the warp; the inner loop then
+// reads weights without converting them.
+template <typename TIn, int NE, bool WF32 = false>
+__global__ void __launch_bounds__(kRouterWarps * 32, WF32 ? 2 : 1)
     router_fused_kernel(const TIn* __restrict__ x, const TIn* __restrict__ W_g,
                         const TIn* __restrict__ b_g, int T, int d, int N, int k, int renorm,
                         float* __restrict__ logits, int32_t* __restrict__ topk_idx,
@@ -158,14 +162,28 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
   constexpr int V = Vec16<TIn>::n;
   constexpr int NPL = NE > 32 ? NE / 32 : 1;          // experts per lane after the reduce
   constexpr int DUP = NE < 32 ? 32 / NE : 1;          // lanes holding the same expert
-  constexpr int kBatch = NE <= 16 ? 16 : (NE == 32 ? 8 : 2);   // 16-byte x loads in flight
+  constexpr int kBatch = WF32 ? 8 : (NE <= 16 ? 16 : (NE == 32 ? 8 : 2));   // x loads in flight
   extern __shared__ uint4 wsm[];                      // W_g [NE][d] (zero rows), then sums
   pdl_launch_dependents();
   pdl_wait_previous();
   const int dv = d / V;
   const int nvec = N * dv, nvec_pad = NE * dv;
   const uint4* wsrc = reinterpret_cast<const uint4*>(W_g);
-  {
+  float4* wsf = reinterpret_cast<float4*>(wsm);       // WF32: [NE][2][dv] float4
+  if constexpr (WF32) {
+    for (int i = threadIdx.x; i < nvec_pad; i += blockDim.x) {
+      const int e = i / dv, c = i - e * dv;
+      float v[8];
+      if (i < nvec) {
+        Vec16<TIn>::load(reinterpret_cast<const TIn*>(wsrc + i), v);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = 0.f;
+      }
+      wsf[(2 * e) * dv + c] = make_float4(v[0], v[1], v[2], v[3]);
+      wsf[(2 * e + 1) * dv + c] = make_float4(v[4], v[5], v[6], v[7]);
+    }
+  } else {
     int i = threadIdx.x;
     for (; i + 3 * int(blockDim.x) < nvec; i += 4 * blockDim.x) {
       const uint4 a0 = __ldg(wsrc + i), a1 = __ldg(wsrc + i + blockDim.x),
@@ -177,7 +195,8 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
     for (int j = nvec + int(threadIdx.x); j < nvec_pad; j += blockDim.x)
       wsm[j] = make_uint4(0, 0, 0, 0);
   }
-  float* red = reinterpret_cast<float*>(wsm + nvec_pad);   // [kRouterWarps][NE]
+  float* red = WF32 ? reinterpret_cast<float*>(wsf + 2 * nvec_pad)
+                    : reinterpret_cast<float*>(wsm + nvec_pad);   // [kRouterWarps][NE]
   __syncthreads();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -212,7 +231,13 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
 #pragma unroll
         for (int e = 0; e < NE; ++e) {
           float wv[V];
-          Vec16<TIn>::load(reinterpret_cast<const TIn*>(wsm + e * dv + c), wv);
+          if constexpr (WF32) {
+            const float4 lo = wsf[(2 * e) * dv + c], hi = wsf[(2 * e + 1) * dv + c];
+            wv[0] = lo.x; wv[1] = lo.y; wv[2] = lo.z; wv[3] = lo.w;
+            wv[4] = hi.x; wv[5] = hi.y; wv[6] = hi.z; wv[7] = hi.w;
+          } else {
+            Vec16<TIn>::load(reinterpret_cast<const TIn*>(wsm + e * dv + c), wv);
+          }
 #pragma unroll
           for (int i = 0; i < V; ++i) acc[e] = fmaf(xv[i], wv[i], acc[e]);
         }
@@ -331,8 +356,17 @@ int fused_ne(int64_t n) { return n <= 8 ? 8 : n <= 16 ? 16 : n <= 32 ? 32 : 64; 
 
 constexpr size_t kFusedRouterSmemLimit = 200 * 1024;
 
+// bf16 layers stage W_g as fp32 when that takes at most 48 KB (several blocks
+// per SM still fit)
+constexpr size_t kFusedRouterF32Limit = 48 * 1024;
+
+bool fused_router_wf32(const moe_config& c) {
+  return c.dtype == MOE_BF16 && fused_ne(c.n_experts) <= 16 &&
+         size_t(fused_ne(c.n_experts) * c.d_model) * 4 <= kFusedRouterF32Limit;
+}
+
 size_t fused_router_smem(const moe_config& c) {
-  const size_t es = c.dtype == MOE_F32 ? 4 : 2;
+  const size_t es = (c.dtype == MOE_F32 || fused_router_wf32(c)) ? 4 : 2;
   const int ne = fused_ne(c.n_experts);
   return size_t(ne * c.d_model) * es + size_t(kRouterWarps) * ne * sizeof(float);
 }
@@ -351,9 +385,9 @@ cudaError_t launch_router_fused(const moe_config& c, int k, const void* x, const
   const size_t smem = fused_router_smem(c);
   const int T = int(c.T), d = int(c.d_model), N = int(c.n_experts);
   const int rn = c.renormalize ? 1 : 0;
-#define MOE_FUSED_CASE(TIN, NPAD)                                                          \
+#define MOE_FUSED_CASE(TIN, NPAD, WF)                                                      \
   {                                                                                        \
-    auto kern = router_fused_kernel<TIN, NPAD>;                                            \
+    auto kern = router_fused_kernel<TIN, NPAD, WF>;                                        \
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,  \
                                          int(smem));                                       \
     if (e != cudaSuccess) return e;                                                        \
@@ -363,15 +397,19 @@ cudaError_t launch_router_fused(const moe_config& c, int k, const void* x, const
                       topk_w, prob_partials, probT, picks);                                \
   }
   if (c.dtype == MOE_F32) {
-    if (N <= 8) MOE_FUSED_CASE(float, 8)
-    if (N <= 16) MOE_FUSED_CASE(float, 16)
-    if (N <= 32) MOE_FUSED_CASE(float, 32)
-    MOE_FUSED_CASE(float, 64)
+    if (N <= 8) MOE_FUSED_CASE(float, 8, false)
+    if (N <= 16) MOE_FUSED_CASE(float, 16, false)
+    if (N <= 32) MOE_FUSED_CASE(float, 32, false)
+    MOE_FUSED_CASE(float, 64, false)
   }
-  if (N <= 8) MOE_FUSED_CASE(__nv_bfloat16, 8)
-  if (N <= 16) MOE_FUSED_CASE(__nv_bfloat16, 16)
-  if (N <= 32) MOE_FUSED_CASE(__nv_bfloat16, 32)
-  MOE_FUSED_CASE(__nv_bfloat16, 64)
+  if (fused_router_wf32(c)) {
+    if (N <= 8) MOE_FUSED_CASE(__nv_bfloat16, 8, true)
+    MOE_FUSED_CASE(__nv_bfloat16, 16, true)
+  }
+  if (N <= 8) MOE_FUSED_CASE(__nv_bfloat16, 8, false)
+  if (N <= 16) MOE_FUSED_CASE(__nv_bfloat16, 16, false)
+  if (N <= 32) MOE_FUSED_CASE(__nv_bfloat16, 32, false)
+  MOE_FUSED_CASE(__nv_bfloat16, 64, false)
 #undef MOE_FUSED_CASE
 }
 
