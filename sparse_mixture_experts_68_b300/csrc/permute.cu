@@ -153,9 +153,11 @@ __global__ void __launch_bounds__(32)
 // assignments (T*k) and per-warp expert counts fit in shared memory: the
 // expert ids are staged as 16-bit values; warp w owns the contiguous range
 // [w*L, (w+1)*L) of assignments.  Pass 1 counts per (warp, expert) with
-// __match_any_sync; a per-expert scan over warps gives each warp's base rank;
-// a scan over experts gives the padded group offsets; pass 2 re-walks the
-// ranges and writes ranks.  Same results as hist + scan + rank.
+// __match_any_sync and keeps each assignment's rank within its warp's range
+// (16-bit, in shared memory); a per-expert scan over warps gives each warp's
+// base rank; a scan over experts gives the padded group offsets; pass 2 adds
+// the two ranks and writes rows, with no further warp-wide matching.  Same
+// results as hist + scan + rank.
 constexpr int kSortWarps = 32;
 
 __global__ void __launch_bounds__(kSortWarps * 32)
@@ -172,6 +174,7 @@ __global__ void __launch_bounds__(kSortWarps * 32)
   int32_t* off = cnt + kSortWarps * N;            // [N] group offsets
   int32_t* warp_tot = off + N;                    // [32], then kept [N], counts [N]
   int16_t* ids = reinterpret_cast<int16_t*>(warp_tot + 32 + 2 * N);   // [A]
+  int16_t* lrank = ids + A;                       // [A] rank within the warp's range
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < kSortWarps * N; i += blockDim.x) cnt[i] = 0;
   {
@@ -203,13 +206,18 @@ __global__ void __launch_bounds__(kSortWarps * 32)
   const int a_begin = warp * L, a_end = min(A, a_begin + L);
   const uint32_t lt_mask = (1u << lane) - 1u;
   int32_t* my = cnt + warp * N;
-  // pass 1: per-warp counts
+  // pass 1: per-warp counts, and each assignment's rank among its expert's
+  // assignments in the warp's range (the running count before this group of
+  // 32 plus the equal lanes below it)
   for (int base = a_begin; base < a_end; base += 32) {
     const int a = base + lane;
     const int e = a < a_end ? ids[a] : -1;
     const int key = e >= 0 ? e : (0x40000000 | lane);
     const uint32_t same = __match_any_sync(0xffffffffu, key);
+    const int32_t before = e >= 0 ? my[e] : 0;
+    __syncwarp();
     if (e >= 0 && (same & lt_mask) == 0) my[e] += __popc(same);
+    if (a < a_end) lrank[a] = int16_t(before + __popc(same & lt_mask));
     __syncwarp();
   }
   __syncthreads();
@@ -275,26 +283,19 @@ __global__ void __launch_bounds__(kSortWarps * 32)
     offsets[N + 1] = excl + padded + (has_shared ? int32_t(round_up(T, kGroupAlign)) : 0);
   }
   __syncthreads();
-  // pass 2: ranks in token-major order
-  for (int base = a_begin; base < a_end; base += 32) {
-    const int a = base + lane;
-    const int e = a < a_end ? ids[a] : -1;
-    const int key = e >= 0 ? e : (0x40000000 | lane);
-    const uint32_t same = __match_any_sync(0xffffffffu, key);
-    int32_t rank = 0;
-    if (e >= 0) rank = my[e] + __popc(same & lt_mask);
-    __syncwarp();
-    if (e >= 0 && (same & lt_mask) == 0) my[e] += __popc(same);
-    __syncwarp();
-    if (a < a_end) {
-      const bool keep = e >= 0 && (capacity <= 0 || rank < capacity);
-      int32_t row = -1;
-      if (keep) {
+  // pass 2: rank = the warp's base rank for the expert (my[e] after the scan)
+  // + the rank within the warp's range from pass 1
+  for (int a = a_begin + lane; a < a_end; a += 32) {
+    const int e = ids[a];
+    int32_t row = -1;
+    if (e >= 0) {
+      const int32_t rank = my[e] + lrank[a];
+      if (capacity <= 0 || rank < capacity) {
         row = off[e] + rank;
         row_token[row] = a / k;
       }
-      token_row[a] = row;
     }
+    token_row[a] = row;
   }
   if (stats.prob_partials) {
     // the load statistics as well, once counts and kept are in memory
@@ -307,7 +308,7 @@ __global__ void __launch_bounds__(kSortWarps * 32)
 
 size_t sort_smem_bytes(const moe_config& c) {
   const int64_t A = c.T * c.top_k;
-  return size_t(kSortWarps * c.n_experts + 3 * c.n_experts + 32) * 4 + size_t(A) * 2 + 16;
+  return size_t(kSortWarps * c.n_experts + 3 * c.n_experts + 32) * 4 + size_t(A) * 4 + 16;
 }
 
 // Above ~16K assignments the multi-block histogram path is faster.
