@@ -14,8 +14,14 @@ step, outside the events.  Multi-GPU (torchrun): every rank runs its own
 replica of the layer on its own GPU (data parallel, no exchange); the time is
 the max over ranks and the value counts every rank's tokens.
 
---impl reference times the CPU oracle (float64 numpy) on the host cores, on a
-bounded sample of the same workload per step.
+The headline line times the Mixtral-sized prefill layer (T=4096, d=4096,
+d_ff=14336, 8 experts, top-2).  The same run adds ``per_workload``: full
+sub-lines (value, ms_per_step, roofline, e2e, cpu_baseline, clocks) for the
+Mixtral-sized decode (T=16), the DeepSeek-V3-sized layer, the page-1 layer and
+the Switch layer with renormalised and with raw-probability gates.
+
+--impl reference times the CPU oracle (plain single-threaded C++, float64) on
+one host core, on a bounded sample of the same workload per step.
 """
 
 from __future__ import annotations
@@ -31,7 +37,11 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-DEFAULT_WORKLOAD = "c1_page1_bf16"
+DEFAULT_WORKLOAD = "c3_mixtral_prefill"
+SUB_WORKLOADS = ("c3_mixtral_decode", "c4_deepseek_v3", "c1_page1_bf16", "c2_switch_top1",
+                 "c2_switch_top1_raw")
+# the B300's nominal HBM3e bandwidth, beside the measured copy rate
+NOMINAL_HBM_GBS = 8000.0
 METRIC = "MoE-layer tokens/s on 1 B300; % of bf16 tensor peak / % of HBM BW"
 TRAIN_METRIC = ("MoE-layer training tokens/s (forward + backward of task + 0.01 balance) "
                 "on 1 B300")
@@ -45,6 +55,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--sub-workloads", default=",".join(SUB_WORKLOADS),
+                    help="comma list of workloads timed as per_workload sub-lines; 'none'")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -176,93 +188,81 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------------------
-# the CPU oracle as a timed baseline
+# the CPU oracle as a timed baseline (plain single-threaded C++, one host core)
 
-def oracle_step(tensors, wl, tokens):
-    """The oracle on the first `tokens` tokens of the batch, as a layer of that
-    many tokens (float64 numpy)."""
-    import numpy as np
+def host_copy(tensors):
+    """Host copies of a layer's tensors in their storage dtype; the oracle
+    upcasts each value to float64 as it reads it."""
+    return {n: v.detach().to("cpu") for n, v in tensors.items()}
+
+
+def oracle_step(host, wl, S, train=False):
+    """One oracle pass over the first S tokens of the batch, run as a layer of
+    S tokens (its capacity recomputed for S tokens); with train=True, the
+    forward and the backward of task + 0.01 balance."""
     import torch
 
     from oracle import moe_oracle as O
-
-    f64 = lambda v: v.detach().to("cpu", torch.float64).numpy()  # noqa: E731
-    x = f64(tensors["x"][:tokens])
-    W = {n: f64(tensors[n]) for n in ("W_g", "b_g", "W1", "b1", "W2", "b2")}
-    shared = None
-    if wl.d_ff_shared:
-        shared = tuple(f64(tensors[n]) for n in ("W1s", "b1s", "W2s", "b2s"))
-    cap = O.expert_capacity(wl.capacity_factor, tokens, wl.n_experts) \
+    x = host["x"][:S]
+    shared = tuple(host[n] for n in ("W1s", "b1s", "W2s", "b2s")) if wl.d_ff_shared else None
+    cap = O.expert_capacity(wl.capacity_factor, S, wl.n_experts) \
         if wl.capacity_factor > 0 else 0
+    W = [host[n] for n in ("W_g", "b_g", "W1", "b1", "W2", "b2")]
+    bf16 = wl.dtype == 1
+    dy = torch.randn(x.shape, generator=torch.Generator().manual_seed(7)).to(x.dtype) \
+        if train else None
 
     def run():
         if wl.expert_choice:
-            return O.expert_choice_forward(x, W["W_g"], W["b_g"], W["W1"], W["b1"], W["W2"],
-                                           W["b2"], capacity=cap, act=wl.act, shared=shared,
-                                           round_hidden_bf16=(wl.dtype == 1))
-        return O.moe_forward(x, W["W_g"], W["b_g"], W["W1"], W["b1"], W["W2"], W["b2"],
-                             k=wl.top_k, act=wl.act, capacity=cap,
+            return O.expert_choice_forward(x, *W, capacity=cap, act=wl.act, shared=shared,
+                                           round_hidden_bf16=bf16)
+        if train:
+            return O.moe_backward(x, *W, dy, k=wl.top_k, act=wl.act, capacity=cap,
+                                  renormalize=bool(wl.renormalize), shared=shared,
+                                  aux_weight=AUX_WEIGHT, round_hidden_bf16=bf16)
+        return O.moe_forward(x, *W, k=wl.top_k, act=wl.act, capacity=cap,
                              renormalize=bool(wl.renormalize), shared=shared,
-                             round_hidden_bf16=(wl.dtype == 1))
-    del np
+                             round_hidden_bf16=bf16)
     return run
 
 
-def oracle_train_step(tensors, wl, tokens):
-    """Forward and backward of the oracle on the first `tokens` tokens."""
-    import numpy as np
-    import torch
+def oracle_sample_size(host, wl, budget_s, train=False):
+    """Tokens per oracle pass so that one pass takes about budget_s: the time
+    of a 2-token pass, scaled."""
+    t0 = time.perf_counter()
+    oracle_step(host, wl, min(2, wl.T), train)()
+    per_token = (time.perf_counter() - t0) / min(2, wl.T)
+    return int(max(1, min(wl.T, budget_s / max(per_token, 1e-9))))
 
+
+def cpu_baseline(wl, host, budget_s, train=False):
+    """The oracle, as it stands, on one host core over a bounded sample."""
     from oracle import moe_oracle as O
-
-    f64 = lambda v: v.detach().to("cpu", torch.float64).numpy()  # noqa: E731
-    x = f64(tensors["x"][:tokens])
-    W = {n: f64(tensors[n]) for n in ("W_g", "b_g", "W1", "b1", "W2", "b2")}
-    shared = None
-    if wl.d_ff_shared:
-        shared = tuple(f64(tensors[n]) for n in ("W1s", "b1s", "W2s", "b2s"))
-    cap = O.expert_capacity(wl.capacity_factor, tokens, wl.n_experts) \
-        if wl.capacity_factor > 0 else 0
-    dy = np.random.default_rng(0).normal(0, 1, x.shape)
-
-    def run():
-        O.moe_forward(x, W["W_g"], W["b_g"], W["W1"], W["b1"], W["W2"], W["b2"], k=wl.top_k,
-                      act=wl.act, capacity=cap, renormalize=bool(wl.renormalize),
-                      shared=shared, round_hidden_bf16=True)
-        return O.moe_backward(x, W["W_g"], W["b_g"], W["W1"], W["b1"], W["W2"], W["b2"], dy,
-                              k=wl.top_k, act=wl.act, capacity=cap,
-                              renormalize=bool(wl.renormalize), shared=shared,
-                              aux_weight=AUX_WEIGHT, round_hidden_bf16=True)
-    return run
-
-
-def oracle_threads():
-    try:
-        from threadpoolctl import threadpool_info
-        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
-        return max(n) if n else 1
-    except Exception:
-        return os.cpu_count() or 1
-
-
-def cpu_sample_tokens(wl):
-    # a sample that keeps one oracle pass to a few seconds of host work
-    from sparse_mixture_experts_68_b300.workloads import routed_rows
-    per_token_flop = (4.0 * wl.d_model * wl.d_ff * routed_rows(wl) / max(wl.T, 1)
-                      + 4.0 * wl.d_model * wl.d_ff_shared)
-    return int(max(16, min(wl.T, 2.0e10 / per_token_flop)))
+    S = oracle_sample_size(host, wl, budget_s / 2, train)
+    step = oracle_step(host, wl, S, train)
+    t0 = time.perf_counter()
+    n = 0
+    while n < 2 or (time.perf_counter() - t0 < budget_s / 2 and n < 3):
+        step()
+        n += 1
+    dt = time.perf_counter() - t0
+    return {"value": S * n / dt, "unit": "tokens/s", "cores": O.threads(), "kind": "oracle",
+            "sample": f"{n} pass(es) over the first {S} of {wl.T} tokens, each run as a "
+                      f"layer of {S} tokens ({O.describe()}"
+                      + (", forward and backward)" if train else ")")}
 
 
 def run_reference(args, wl, rank, world):
-    import torch
-
+    from oracle import moe_oracle as O
     from sparse_mixture_experts_68_b300 import synth
     if rank != 0:
         return None
-    tensors = synth.make_layer(wl, device="cpu")
     train = args.mode == "train"
-    S = max(16, cpu_sample_tokens(wl) // 4) if train else cpu_sample_tokens(wl)
-    step = oracle_train_step(tensors, wl, S) if train else oracle_step(tensors, wl, S)
+    host = host_copy(synth.make_layer(wl, device="cpu"))
+    # each step a bounded sample, so that the K + W steps end in a few minutes
+    S = oracle_sample_size(host, wl, min(3.0, 120.0 / max(1, args.steps + args.warmup)),
+                           train)
+    step = oracle_step(host, wl, S, train)
     for _ in range(args.warmup):
         step()
     t0 = time.perf_counter()
@@ -270,22 +270,31 @@ def run_reference(args, wl, rank, world):
         step()
     dt = time.perf_counter() - t0
     value = S * args.steps / dt
-    cores = oracle_threads()
-    del torch
     return {
         "metric": TRAIN_METRIC if train else METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "impl": "reference",
-        "config": {"workload": wl.name, "description": wl.description, "T": wl.T,
-                   "sample_tokens_per_step": S},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": f"first {S} of {wl.T} tokens per step, as a layer of {S} "
-                                   "tokens (float64 numpy oracle)"},
+        "config": run_config(wl, world, train),
+        "sample_tokens_per_step": S,
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": O.threads(),
+                         "kind": "oracle",
+                         "sample": f"first {S} of {wl.T} tokens per step, each run as a layer "
+                                   f"of {S} tokens ({O.describe()})"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
+
+
+def run_config(wl, world, train=False):
+    """The `config` object of a line: the same for both arms."""
+    cfg = {"workload": wl.name, "description": wl.description, "T": wl.T,
+           "parallelism": f"replicas{world}" if world > 1 else "single",
+           "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write)"}
+    if train:
+        cfg["aux_weight"] = AUX_WEIGHT
+    return cfg
 
 
 # ---------------------------------------------------------------------------------------
@@ -360,7 +369,7 @@ def job_tokens_per_s(tokens_per_step: int, steps: int, world: int, job_ms: float
     return tokens_per_step * steps * world / (job_ms * 1e-3)
 
 
-def run_ours(args, wl, rank, world, local_rank):
+def run_ours(args, wl, rank, world, local_rank, cpu_budget_s=None):
     import torch
     import torch.distributed as dist
 
@@ -476,12 +485,11 @@ def run_ours(args, wl, rank, world, local_rank):
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"], roof["traffic_source"] = profiled_traffic(wl.name)
     roof["algorithmic_bytes_per_launch"] = (b1 + b2) / launches
-    if wl.dtype != 1:
-        roof["kernel"] = "simt_gemm_kernel (two launches per step: Linear 1, Linear 2)"
-        roof["peak_source"] = F32_ALU_SOURCE
-    else:
-        roof["kernel"] = "tc_grouped_gemm_kernel (two launches per step: Linear 1, Linear 2)"
-        roof["peak_source"] = pk["source"] + " (burst)"
+    names = [B.ffn_kernel_name(layer.cfg, i) for i in (1, 2)]
+    roof["kernel"] = f"Linear 1: {names[0]}; Linear 2: {names[1]}"
+    roof["peak_source"] = F32_ALU_SOURCE if wl.dtype != 1 else pk["source"] + " (burst)"
+    if roof["bound"] == "hbm":
+        roof["frac_of_nominal_8tbs"] = roof["achieved"] / NOMINAL_HBM_GBS
     roof["per_launch"] = {
         "linear1": {"ms": mean_stage["ffn_linear1"], "flop": f1, "bytes": b1,
                     "tflops": f1 / (mean_stage["ffn_linear1"] * 1e-3) / 1e12,
@@ -490,25 +498,31 @@ def run_ours(args, wl, rank, world, local_rank):
                     "tflops": f1 / (mean_stage["ffn_linear2"] * 1e-3) / 1e12,
                     "gbs": b2 / (mean_stage["ffn_linear2"] * 1e-3) / 1e9}}
 
-    # whole-layer roofline time against the same peaks
+    # whole-layer roofline time against the same peaks: both weight matrices of
+    # every expert with a kept row, the router weight, x read and y written
     layer_flop = flops(wl, kept_rows)
-    layer_bytes = wbytes + wl.n_experts * wl.d_model * es + 2 * T * wl.d_model * es
+    layer_bytes = (2 * wbytes + wl.n_experts * wl.d_model * es + 2 * T * wl.d_model * es)
     floor_ms = max(layer_flop / (pk["bf16_tflops"] * 1e12),
                    layer_bytes / (pk["hbm_gbs"] * 1e9)) * 1e3
+    step_s = total_ms / K * 1e-3
+    lfig = {"flop": layer_flop, "bytes": layer_bytes,
+            "tflops": layer_flop / step_s / 1e12, "gbs": layer_bytes / step_s / 1e9}
+    lfig["frac_of_tensor_peak"] = lfig["tflops"] / pk["bf16_tflops"]
+    lfig["frac_of_hbm_measured"] = lfig["gbs"] / pk["hbm_gbs"]
+    lfig["frac_of_nominal_8tbs"] = lfig["gbs"] / NOMINAL_HBM_GBS
 
     res = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if wl.dtype == 1 else "f32", "data": "synthetic",
-        "config": {"workload": wl.name, "description": wl.description, "T": T,
-                   "parallelism": f"replicas{world}" if world > 1 else "single",
-                   "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write)",
-                   "launch": f"{calls.entry} captured once as a CUDA graph, replayed; "
-                             f"per-kernel times from direct {calls.entry}_profiled calls"},
+        "config": run_config(wl, world),
+        "launch": f"{calls.entry} captured once as a CUDA graph, replayed; per-kernel "
+                  f"times from direct {calls.entry}_profiled calls",
         "tflops": layer_flop / (total_ms / K * 1e-3) / 1e12,
         "layer_roofline_floor_ms": floor_ms,
         "layer_roofline_frac": floor_ms / (total_ms / K),
+        "layer": lfig,
         "stage_ms": mean_stage,
         "profiled_ms_per_step": statistics.mean(prof_step_ms),
         "roofline": roof,
@@ -518,11 +532,15 @@ def run_ours(args, wl, rank, world, local_rank):
 
     if not args.no_e2e:
         res["e2e"] = measure_e2e_ec(args, calls, wl, dev) if calls.ec else \
-            measure_e2e(args, layer, wl, dev)
+            measure_e2e(args, calls.layer, wl, dev)
+    if rank == 0 and cpu_budget_s:
+        host = host_copy(tensors)
+        del tensors, calls, x
+        res["cpu_baseline"] = cpu_baseline(wl, host, cpu_budget_s)
     return res
 
 
-def run_train(args, wl, rank, world, local_rank):
+def run_train(args, wl, rank, world, local_rank, cpu_budget_s=None):
     """One step = moe_forward + moe_backward of total = task + 0.01 balance with
     a fixed synthetic dy, captured once as a CUDA graph and replayed."""
     import torch
@@ -666,12 +684,9 @@ def run_train(args, wl, rank, world, local_rank):
         "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if wl.dtype == 1 else "f32", "data": "synthetic",
-        "config": {"workload": wl.name, "description": wl.description, "T": T,
-                   "parallelism": f"replicas{world}" if world > 1 else "single",
-                   "aux_weight": AUX_WEIGHT,
-                   "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write)",
-                   "launch": "moe_forward + moe_backward captured once as a CUDA graph, "
-                             "replayed; per-kernel times from direct *_profiled calls"},
+        "config": run_config(wl, world, train=True),
+        "launch": "moe_forward + moe_backward captured once as a CUDA graph, replayed; "
+                  "per-kernel times from direct *_profiled calls",
         "tflops": train_flop / (total_ms / K * 1e-3) / 1e12,
         "forward_stage_ms": fmean, "backward_stage_ms": bmean,
         "roofline": roof,
@@ -708,6 +723,10 @@ def run_train(args, wl, rank, world, local_rank):
                       "d2h_bytes_per_step": T * wl.d_model * es,
                       "api": "moe_forward + moe_backward between pinned host copies of x, dy "
                              "and dx on one stream (synchronous)"}
+    if rank == 0 and cpu_budget_s:
+        host = host_copy(tensors)
+        del tensors, layer, out, grads, bws
+        res["cpu_baseline"] = cpu_baseline(wl, host, cpu_budget_s, train=True)
     return res
 
 
@@ -773,29 +792,6 @@ def measure_e2e_ec(args, calls, wl, dev):
             "api": "moe_ec_forward between pinned host copies on its stream (synchronous)"}
 
 
-def cpu_baseline(wl, train=False):
-    import torch
-
-    from sparse_mixture_experts_68_b300 import synth
-    tensors = synth.make_layer(wl, device="cpu")
-    S = max(16, cpu_sample_tokens(wl) // 4) if train else cpu_sample_tokens(wl)
-    step = oracle_train_step(tensors, wl, S) if train else oracle_step(tensors, wl, S)
-    t0 = time.perf_counter()
-    n = 0
-    while True:
-        step()
-        n += 1
-        if time.perf_counter() - t0 > 10.0 or n >= 3:
-            break
-    dt = time.perf_counter() - t0
-    del torch
-    return {"value": S * n / dt, "unit": "tokens/s", "cores": oracle_threads(),
-            "kind": "oracle",
-            "sample": f"{n} pass(es) over the first {S} of {wl.T} tokens, as a layer of "
-                      f"{S} tokens (float64 numpy oracle"
-                      + (", forward and backward)" if train else ")")}
-
-
 def main():
     args = parse()
     from sparse_mixture_experts_68_b300.workloads import WORKLOADS
@@ -813,13 +809,20 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
+    import torch
+    cpu = not args.no_cpu_baseline
     if args.mode == "train":
-        res = run_train(args, wl, rank, world, local_rank)
+        res = run_train(args, wl, rank, world, local_rank, cpu_budget_s=24.0 if cpu else None)
     else:
-        res = run_ours(args, wl, rank, world, local_rank)
+        res = run_ours(args, wl, rank, world, local_rank, cpu_budget_s=24.0 if cpu else None)
+        subs = [n for n in args.sub_workloads.split(",") if n and n != "none" and n != wl.name]
+        if subs:
+            res["per_workload"] = {}
+        for name in subs:
+            torch.cuda.empty_cache()
+            res["per_workload"][name] = run_ours(args, WORKLOADS[name], rank, world, local_rank,
+                                                 cpu_budget_s=6.0 if cpu else None)
     if rank == 0:
-        if not args.no_cpu_baseline:
-            res["cpu_baseline"] = cpu_baseline(wl, train=args.mode == "train")
         print(json.dumps(res), flush=True)
     if world > 1:
         import torch.distributed as dist

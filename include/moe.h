@@ -134,6 +134,13 @@ size_t moe_workspace_size(const moe_config* cfg);
  * kernels are chosen by shape); -1 for an invalid config. */
 int32_t moe_forward_launch_count(const moe_config* cfg);
 
+/* Name of the kernel, with its tile shape, that moe_forward launches for
+ * grouped Linear `linear` (1: Xp -> H, 2: H -> Yp) of this layer; the choice
+ * depends on the shape only.  A static string owned by the library; NULL for
+ * an invalid config or `linear` outside {1, 2}.  A host-side query for
+ * profiling reports: the pages have no counterpart. */
+const char* moe_ffn_kernel_name(const moe_config* cfg, int32_t linear);
+
 /* ---- the steps of the layer ------------------------------------------------ */
 
 /* Router scores, softmax over all N experts, top-k and gates
@@ -187,8 +194,11 @@ moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk
  * overlap on the GPU (different streams, no ordering) race on it, so order
  * them on one stream or with events.  Nothing in it needs clearing between
  * calls: every entry is written before it is read.  The first call on each
- * device looks up the array's device address (cudaGetSymbolAddress); make that
- * first call before any stream capture.  No memory is allocated by this call. */
+ * device looks up the array's device address (cudaGetSymbolAddress) and
+ * caches it; the lookup is repeated when the device's context has changed
+ * (for example after cudaDeviceReset).  Make the first call on a device, and
+ * the first after such a change, before any stream capture.  No memory is
+ * allocated by this call. */
 #define MOE_PERMUTE_STATIC_SCRATCH_INTS (1 << 18)
 moe_status moe_permute_noalloc(const moe_config* cfg, const void* x,
                                const int32_t* topk_idx, int32_t* counts, int32_t* kept,

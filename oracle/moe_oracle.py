@@ -1,194 +1,493 @@
-"""CPU oracle for the sparse Mixture-of-Experts FFN forward pass.
+"""CPU oracle for the sparse Mixture-of-Experts FFN layer.
 
 TEST INFRASTRUCTURE ONLY.  Nothing in the library path imports this module:
 only the tests, the smoke check in ``__graft_entry__`` and the CPU-baseline leg
 of ``bench.py`` may call it.  It shares no code with the CUDA path.
 
-Everything here is the plain definition of what the layer computes, in
-float64 numpy, with no blocking, fusion or reordering beyond the definition:
+The arithmetic is in ``moe_oracle.cpp``: plain single-threaded C++ in float64,
+each function the plain definition of one step of the layer, citing the page
+passage it follows (router scores, softmax, top-k, gates, grouping with a
+capacity, expert FFNs, combine, balance statistic and cv^2, expert-choice
+routing, and the backward pass of task + alpha * balance).  This module only
+marshals arrays to it through ctypes and arranges the results in the shapes the
+tests use.  Inputs may be numpy arrays or CPU torch tensors in float32,
+bfloat16 or float64: the C++ side reads each element in its own format and
+upcasts it exactly.
 
-* router scores ``z = x . W_g^T + b_g`` -- botmartz.com "Mixture of Experts (MoE)
-  and Mixtral: Scaling Without Dense Computation", section "Expert Routing"
-  (the router is an ``nn.Linear(d_model, num_experts)``); roadtointelligence.com
-  "Mixture of Experts (MoE)", the router formula G(x) = Softmax(TopK(x . W_g)).
-* softmax over all N experts, then the top-k, then renormalisation of the kept
-  k probabilities -- botmartz.com "Expert Routing"; matteuscruz.github.io
-  "What is a Mixture of Experts?", section "Architecture: router + experts".
-* the same gates written as a softmax over only the kept top-k logits --
-  roadtointelligence.com, router formula and the "Tiny example".
-* gates without renormalisation (the raw softmax probability of each kept
-  expert) -- codingnowai.in "Mixture of Experts", section "Code".
-* expert FFN Linear -> GELU -> Linear (botmartz.com "Expert Routing") or
-  Linear -> ReLU -> Linear (codingnowai.in "Code"), each with bias.
-* output y = sum over kept experts of gate * expert(x) -- roadtointelligence.com
-  output equation; matteuscruz.github.io "Architecture: router + experts".
-* expert capacity = capacity factor x batch / num_experts, tokens over capacity
-  dropped (layer output 0, the token passes on through the residual) --
-  matteuscruz.github.io "Load balancing: the core training challenge";
-  roadtointelligence.com "Keeping the experts busy".
-* one shared expert applied to every token with weight 1 --
-  roadtointelligence.com "Total versus active parameters" (DeepSeek-V3).
-* balance statistic std(mean_t router_probs)^2 with torch's default
-  (unbiased) std -- botmartz.com "Load Balancing: The Hidden Challenge".
-* expert-choice routing: each expert takes the tokens it scores highest
-  instead of each token taking its top-k experts, so every expert gets the same
-  load -- matteuscruz.github.io "Load balancing: the core training challenge"
-  (Zhou et al., 2022, as the page describes it).  Readings: the score is the
-  router probability p[t, e]; an expert takes C tokens (C = the capacity,
-  clamped to T; C <= 0 means all T); ties go to the lower token index; a picked
-  token's gate is p[t, e]; a token no expert picked outputs 0.
-* the backward pass of the layer for the training loss
-  total = task + alpha * balance (botmartz.com "Load Balancing: The Hidden
-  Challenge": total_loss = task_loss + 0.01 * balance_loss; roadtointelligence.com
-  "Keeping the experts busy": coefficient 0.01).  The task loss enters as its
-  gradient dy = d task / d y; every other derivative is the chain rule through
-  the forward above, written out step by step (no automatic differentiation).
-  The top-k choice and the capacity drops are piecewise constant: they pass
-  no gradient.
-* squared coefficient of variation of the expert counts, the quantity the
-  auxiliary loss penalises -- matteuscruz.github.io "Load balancing: the core
-  training challenge"; named cv_squared(expert_counts) in invest-in.ai
-  "MoE - Mixture of Experts", "Common Usage Examples".  The pages give no
-  formula; read as var/mean^2 with the unbiased variance over the N counts.
-
-Readings taken where the pages are silent (each also listed in the design
-notes): top-k ties go to the lower expert index; slot 0 holds the largest
-score; capacity priority is token-major (token, then slot); the capacity is
-ceil(capacity_factor * T / N); a dropped (token, slot) contributes exactly 0;
-the shared expert uses the routed experts' FFN form and activation.
+``workers`` (where offered) splits independent token rows over that many
+threads, each running the single-threaded oracle on its own rows; the results
+are those of one call.
 """
 
 from __future__ import annotations
 
-import math
+import ctypes as C
+import os
+from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass, field
 
 import numpy as np
 
-try:                                    # library erf; math.erf elementwise otherwise
-    from scipy.special import erf as _erf
-except ImportError:                     # pragma: no cover
-    _erf = np.vectorize(math.erf, otypes=[np.float64])
-
 ACT_GELU_ERF = 0
 ACT_RELU = 1
+_F32, _BF16, _F64 = 0, 1, 2
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def threads() -> int:
+    """Host threads one oracle call uses."""
+    return 1
+
+
+def describe() -> str:
+    return "plain single-threaded C++ oracle, float64"
 
 
 # ---------------------------------------------------------------------------
-# number formats
+# the shared library
+
+class _Tensor(C.Structure):
+    _fields_ = [("data", C.c_void_p), ("dtype", C.c_int32), ("reserved", C.c_int32)]
+
+
+_TENSORS = ("x", "W_g", "b_g", "W1", "b1", "W2", "b2", "W1s", "b1s", "W2s", "b2s")
+
+
+class _Layer(C.Structure):
+    _fields_ = ([(n, C.c_int64) for n in ("T", "d", "f", "N", "k", "f_shared")] +
+                [("act", C.c_int32), ("round_hidden_bf16", C.c_int32)] +
+                [(n, _Tensor) for n in _TENSORS])
+
+
+_lib = None
+
+
+def lib() -> C.CDLL:
+    global _lib
+    if _lib is None:
+        from . import build
+        L = C.CDLL(build.build())
+        P, I64, I32, D = C.c_void_p, C.c_int64, C.c_int32, C.c_double
+        LP = C.POINTER(_Layer)
+        sig = {
+            "orc_round_bf16_array": (None, [P, P, I64]),
+            "orc_activation": (I32, [I32, P, P, I64]),
+            "orc_activation_grad": (I32, [I32, P, P, I64]),
+            "orc_router_logits": (I32, [LP, I64, I64, P]),
+            "orc_softmax_rows": (I32, [I64, I64, P, P]),
+            "orc_topk": (I32, [I64, I64, I64, P, P]),
+            "orc_topk_gap": (I32, [I64, I64, I64, P, P]),
+            "orc_gates_softmax_of_topk": (I32, [I64, I64, I64, P, P, P]),
+            "orc_gates_renormalised_probs": (I32, [I64, I64, I64, P, P, P]),
+            "orc_gates_raw_probs": (I32, [I64, I64, I64, P, P, P]),
+            "orc_capacity": (I64, [D, I64, I64]),
+            "orc_group": (I64, [I64, I64, I64, I64, P, P, P, P, P, P, P]),
+            "orc_balance": (I32, [I64, I64, P, P, P]),
+            "orc_cv_squared": (D, [I64, P]),
+            "orc_route": (I32, [LP, I64, I32, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P,
+                                P]),
+            "orc_expert_rows": (I32, [LP, I64, P, I64, P, P, P]),
+            "orc_combine_rows": (I32, [LP, P, P, P, P, I64, P]),
+            "orc_bruteforce": (I32, [LP, I64, I32, P]),
+            "orc_ec_tokens": (I64, [I64, I64]),
+            "orc_ec_select": (I32, [I64, I64, I64, P, P]),
+            "orc_ec_gap": (I32, [I64, I64, I64, P, P]),
+            "orc_ec_picks": (I64, [I64, I64, I64, P, P]),
+            "orc_ec_combine_rows": (I32, [LP, I64, P, P, P, I64, P]),
+            "orc_backward": (I32, [LP, I64, I32, P, _Tensor, D] + [P] * 13),
+            "orc_expert_weight_grads": (I32, [LP, I64, P, P, I64, _Tensor, P, I64, P, P, P,
+                                              P]),
+            "orc_token_grads": (I32, [LP, I32, P, P, P, P, _Tensor, D, P, I64, P, P, P]),
+            "orc_router_weight_grads": (I32, [LP, P, P, P]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _ok(rc, what):
+    if rc != 0:
+        raise ValueError(f"oracle {what}: invalid argument")
+
+
 # ---------------------------------------------------------------------------
+# marshalling
+
+def _host(a):
+    """(C-contiguous host array, format code) of a in its own number format:
+    float32, bfloat16 (its raw 16-bit patterns) or float64; anything else as
+    float64."""
+    try:
+        import torch
+    except ImportError:                                     # pragma: no cover
+        torch = None
+    if torch is not None and isinstance(a, torch.Tensor):
+        t = a.detach()
+        if t.device.type != "cpu":
+            t = t.cpu()
+        t = t.contiguous()
+        if t.dtype == torch.bfloat16:
+            return t.view(torch.int16).numpy().view(np.uint16), _BF16
+        if t.dtype == torch.float32:
+            return t.numpy(), _F32
+        return t.to(torch.float64).numpy(), _F64
+    if isinstance(a, (list, tuple)):          # per-expert pieces: stacked as float64
+        a = np.stack([_values(v) for v in a])
+    a = np.asarray(a)
+    if a.dtype == np.float32:
+        return np.ascontiguousarray(a), _F32
+    return np.ascontiguousarray(a, dtype=np.float64), _F64
+
+
+def _values(a):
+    """The values of a as a float64 array (bfloat16 is the upper half of a float32)."""
+    arr, code = _host(a)
+    if code == _BF16:
+        return (arr.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return arr.astype(np.float64)
+
+
+def _f64(a):
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _i64(a):
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int64))
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data
+
+
+def _shape(a):
+    return tuple(a.shape) if a is not None else None
+
+
+def _chunks(n, parts):
+    parts = max(1, min(parts, n))
+    bounds = np.linspace(0, n, parts + 1).astype(np.int64)
+    return [(int(bounds[i]), int(bounds[i + 1])) for i in range(parts) if bounds[i] < bounds[i + 1]]
+
+
+def _parallel(fn, n, workers):
+    """fn(lo, hi) over row ranges covering [0, n), on up to `workers` threads
+    (ctypes drops the GIL for the duration of each oracle call)."""
+    ranges = _chunks(n, workers)
+    if len(ranges) <= 1:
+        for lo, hi in ranges:
+            fn(lo, hi)
+        return
+    with ThreadPoolExecutor(max_workers=len(ranges)) as ex:
+        for fut in [ex.submit(fn, lo, hi) for lo, hi in ranges]:
+            fut.result()
+
+
+class Layer:
+    """One layer's tensors marshalled once for the C++ oracle.
+
+    x [T, d]; W_g [N, d]; b_g [N]; W1 [N, f, d]; b1 [N, f]; W2 [N, d, f];
+    b2 [N, d]; shared = (W1s [fs, d], b1s, W2s [d, fs], b2s) or None.  Any of the
+    router or expert tensors may be None for calls that do not read them."""
+
+    def __init__(self, x, W_g=None, b_g=None, W1=None, b1=None, W2=None, b2=None, *, k=1,
+                 act=ACT_GELU_ERF, shared=None, round_hidden_bf16=False):
+        self._keep = []
+        ts = {}
+        for name, a in zip(_TENSORS, (x, W_g, b_g, W1, b1, W2, b2) +
+                           (tuple(shared) if shared is not None else (None,) * 4)):
+            if a is None:
+                ts[name] = _Tensor(None, _F64, 0)
+                continue
+            arr, code = _host(a)
+            self._keep.append(arr)
+            ts[name] = _Tensor(arr.ctypes.data, code, 0)
+        T, d = _shape(x)
+        if b_g is not None:
+            N = _shape(b_g)[0]
+        elif W1 is not None:
+            N = len(W1) if isinstance(W1, (list, tuple)) else _shape(W1)[0]
+        else:
+            N = 1
+        f = 1
+        if W1 is not None:
+            f = _host(W1[0])[0].shape[0] if isinstance(W1, (list, tuple)) else _shape(W1)[-2]
+        fs = _shape(shared[0])[0] if shared is not None else 0
+        self.T, self.d, self.f, self.N, self.k, self.fs = int(T), int(d), int(f), int(N), \
+            int(k), int(fs)
+        self.act = int(act)
+        self.c = _Layer(self.T, self.d, self.f, self.N, self.k, self.fs, self.act,
+                        int(bool(round_hidden_bf16)), *[ts[n] for n in _TENSORS])
+
+    def ref(self):
+        return C.byref(self.c)
+
+    # ---- router and routing
+    def logits(self, workers=1):
+        z = np.empty((self.T, self.N))
+
+        def run(lo, hi):
+            _ok(lib().orc_router_logits(self.ref(), lo, hi, _p(z[lo:hi])), "router")
+        _parallel(run, self.T, workers)
+        return z
+
+    def route(self, capacity=0, renormalize=True, idx_override=None, workers=1, z=None):
+        """Returns a Routing of all T tokens (z: the scores, when already computed)."""
+        T, N, k = self.T, self.N, self.k
+        z = self.logits(workers) if z is None else _f64(z)
+        r = Routing(z=np.empty((T, N)), p=np.empty((T, N)), idx=np.empty((T, k), np.int64),
+                    w=np.empty((T, k)), counts=np.empty(N, np.int64),
+                    kept=np.empty(N, np.int64), rank=np.empty((T, k), np.int64),
+                    keep=np.empty((T, k), np.uint8), order=np.empty(T * k, np.int64),
+                    group_start=np.empty(N + 1, np.int64), mean_prob=np.empty(N))
+        dropped = C.c_int64()
+        bal = C.c_double()
+        cv = C.c_double()
+        ov = _i64(idx_override) if idx_override is not None else None
+        _ok(lib().orc_route(self.ref(), int(capacity), int(bool(renormalize)), _p(ov), _p(z),
+                            _p(r.z), _p(r.p), _p(r.idx), _p(r.w), _p(r.counts), _p(r.kept),
+                            _p(r.rank), _p(r.keep), _p(r.order), _p(r.group_start),
+                            C.byref(dropped), _p(r.mean_prob), C.byref(bal), C.byref(cv)),
+            "route")
+        r.dropped, r.balance, r.cv_squared = int(dropped.value), float(bal.value), \
+            float(cv.value)
+        return r
+
+    # ---- experts and the layer
+    def expert_rows(self, e, tokens, want=("o",)):
+        """(pre, h, o) of expert e (e == N: shared) on x[tokens]; only the
+        requested ones are computed, the others are None."""
+        tok = _i64(tokens)
+        fe = self.fs if e == self.N else self.f
+        pre = np.empty((len(tok), fe)) if "pre" in want else None
+        h = np.empty((len(tok), fe)) if "h" in want else None
+        o = np.empty((len(tok), self.d)) if "o" in want else None
+        _ok(lib().orc_expert_rows(self.ref(), int(e), _p(tok), len(tok), _p(pre), _p(h), _p(o)),
+            "expert_rows")
+        return pre, h, o
+
+    def combine_rows(self, routing, tokens, workers=1):
+        tok = _i64(tokens)
+        y = np.empty((len(tok), self.d))
+
+        def run(lo, hi):
+            _ok(lib().orc_combine_rows(self.ref(), _p(routing.idx), _p(routing.w),
+                                       _p(routing.keep), _p(tok[lo:hi]), hi - lo, _p(y[lo:hi])),
+                "combine_rows")
+        _parallel(run, len(tok), workers)
+        return y
+
+    def ec_combine_rows(self, C_, sel, p, tokens, workers=1):
+        tok = _i64(tokens)
+        sel = _i64(sel)
+        p = _f64(p)
+        y = np.empty((len(tok), self.d))
+
+        def run(lo, hi):
+            _ok(lib().orc_ec_combine_rows(self.ref(), int(C_), _p(sel), _p(p), _p(tok[lo:hi]),
+                                          hi - lo, _p(y[lo:hi])), "ec_combine_rows")
+        _parallel(run, len(tok), workers)
+        return y
+
+    # ---- backward pieces
+    def token_grads(self, routing, dy, aux_weight, tokens, renormalize=True, workers=1):
+        """(dw [n, k], dz [n, N], dx [n, d]) of the listed tokens."""
+        tok = _i64(tokens)
+        dyh, code = _host(dy)
+        dyt = _Tensor(dyh.ctypes.data, code, 0)
+        n = len(tok)
+        dw, dz, dx = np.empty((n, self.k)), np.empty((n, self.N)), np.empty((n, self.d))
+
+        def run(lo, hi):
+            _ok(lib().orc_token_grads(self.ref(), int(bool(renormalize)), _p(routing.p),
+                                      _p(routing.idx), _p(routing.w), _p(routing.keep), dyt,
+                                      float(aux_weight), _p(tok[lo:hi]), hi - lo,
+                                      _p(dw[lo:hi]), _p(dz[lo:hi]), _p(dx[lo:hi])),
+                "token_grads")
+        _parallel(run, n, workers)
+        return dw, dz, dx
+
+    def router_weight_grads(self, dz):
+        """(dW_g [N, d], db_g [N]) from the score gradients dz [T, N]."""
+        dz = _f64(dz)
+        dW_g, db_g = np.empty((self.N, self.d)), np.empty(self.N)
+        _ok(lib().orc_router_weight_grads(self.ref(), _p(dz), _p(dW_g), _p(db_g)),
+            "router_weight_grads")
+        return dW_g, db_g
+
+    def backward(self, routing, dy, aux_weight, renormalize=True, workers=1):
+        """The whole backward pass from its pieces: every token's dw, dz and dx
+        (token rows split over `workers` threads), every expert's weight
+        gradients (experts spread over the threads), the router's.  Equal to
+        moe_backward up to the order of floating-point sums."""
+        T, N, k = self.T, self.N, self.k
+        dw, dz, dx = self.token_grads(routing, dy, aux_weight, np.arange(T), renormalize,
+                                      workers)
+        grp = routing.grouping()
+        jobs = list(range(N + (1 if self.fs else 0)))
+
+        def one(e):
+            if e == N:
+                return self.expert_weight_grads(e, np.arange(T), np.ones(T), dy)
+            rows = grp.groups[e]
+            ts = np.array([t for t, _ in rows], dtype=np.int64)
+            gs = np.array([routing.w[t, j] for t, j in rows])
+            return self.expert_weight_grads(e, ts, gs, dy)
+
+        with ThreadPoolExecutor(max_workers=max(1, workers)) as ex:
+            res = list(ex.map(one, jobs))
+        dW_g, db_g = self.router_weight_grads(dz)
+        g = LayerGrads(dx, dW_g, db_g, np.stack([r[0] for r in res[:N]]),
+                       np.stack([r[1] for r in res[:N]]), np.stack([r[2] for r in res[:N]]),
+                       np.stack([r[3] for r in res[:N]]), dz, dw, None)
+        if self.fs:
+            g.shared = res[N]
+        return g
+
+    def expert_weight_grads(self, e, tokens, gates, dy, units=None):
+        """(dW1 rows [u, d], db1 [u], dW2 columns [d, u], db2 [d]) of expert e
+        (e == N: shared) over rows tokens with gates; units=None: all."""
+        tok = _i64(tokens)
+        g = _f64(gates)
+        dyh, code = _host(dy)
+        fe = self.fs if e == self.N else self.f
+        un = _i64(units) if units is not None else None
+        u = fe if un is None else len(un)
+        dW1, db1, dW2, db2 = np.empty((u, self.d)), np.empty(u), np.empty((self.d, u)), \
+            np.empty(self.d)
+        _ok(lib().orc_expert_weight_grads(self.ref(), int(e), _p(tok), _p(g), len(tok),
+                                          _Tensor(dyh.ctypes.data, code, 0), _p(un), u,
+                                          _p(dW1), _p(db1), _p(dW2), _p(db2)),
+            "expert_weight_grads")
+        return dW1, db1, dW2, db2
+
+
+@dataclass
+class Routing:
+    z: np.ndarray
+    p: np.ndarray
+    idx: np.ndarray
+    w: np.ndarray
+    counts: np.ndarray
+    kept: np.ndarray
+    rank: np.ndarray
+    keep: np.ndarray
+    order: np.ndarray
+    group_start: np.ndarray
+    mean_prob: np.ndarray
+    dropped: int = 0
+    balance: float = 0.0
+    cv_squared: float = 0.0
+
+    def grouping(self) -> "Grouping":
+        k = self.idx.shape[1]
+        gs = self.group_start
+        groups = [[(int(a) // k, int(a) % k) for a in self.order[gs[e]:gs[e + 1]]]
+                  for e in range(len(self.counts))]
+        return Grouping(groups, self.counts.copy(), self.kept.copy(), self.rank.copy(),
+                        self.keep.astype(bool), self.dropped)
+
+
+# ---------------------------------------------------------------------------
+# number formats and elementwise definitions
 
 def round_to_bf16(v):
-    """Round float64 values to the nearest bfloat16 value (ties to even).
+    """Nearest bfloat16 value (8 significant bits, ties to even)."""
+    v = _f64(v)
+    out = np.empty_like(v)
+    lib().orc_round_bf16_array(_p(v), _p(out), v.size)
+    return out
 
-    bfloat16 keeps 8 significant bits and float32's exponent range, so for the
-    normal numbers this layer produces, rounding to 8 significant bits with
-    round-half-to-even is the whole definition.  Zeros, infinities and NaNs
-    pass through unchanged.
-    """
-    v = np.asarray(v, dtype=np.float64)
-    mant, expo = np.frexp(v)                      # v = mant * 2**expo, |mant| in [0.5, 1)
-    q = np.round(mant * 256.0)                    # numpy rounds half to even
-    out = np.ldexp(q / 256.0, expo)
-    return np.where(np.isfinite(v), out, v)
+
+def activation(h, act):
+    h = _f64(h)
+    out = np.empty_like(h)
+    _ok(lib().orc_activation(int(act), _p(h), _p(out), h.size), "activation")
+    return out
+
+
+def activation_grad(a, act):
+    a = _f64(a)
+    out = np.empty_like(a)
+    _ok(lib().orc_activation_grad(int(act), _p(a), _p(out), a.size), "activation_grad")
+    return out
 
 
 # ---------------------------------------------------------------------------
 # router: scores, softmax, top-k, gates
-# ---------------------------------------------------------------------------
 
 def router_logits(x, W_g, b_g):
-    """z[t, e] = sum_i x[t, i] * W_g[e, i] + b_g[e]   (nn.Linear(d_model, N))."""
-    x = np.asarray(x, dtype=np.float64)
-    W_g = np.asarray(W_g, dtype=np.float64)
-    b_g = np.asarray(b_g, dtype=np.float64)
-    return x @ W_g.T + b_g
+    """z[t, e] = sum_i x[t, i] W_g[e, i] + b_g[e]  (nn.Linear(d_model, N))."""
+    return Layer(x, W_g, b_g).logits()
 
 
 def softmax(z):
-    """Softmax over the last axis (over all N experts), max-subtracted."""
-    z = np.asarray(z, dtype=np.float64)
-    m = np.max(z, axis=-1, keepdims=True)
-    e = np.exp(z - m)
-    return e / np.sum(e, axis=-1, keepdims=True)
+    """Softmax over the last axis, max-subtracted."""
+    z = _f64(z)
+    flat = z.reshape(-1, z.shape[-1])
+    p = np.empty_like(flat)
+    _ok(lib().orc_softmax_rows(flat.shape[0], flat.shape[1], _p(flat), _p(p)), "softmax")
+    return p.reshape(z.shape)
 
 
 def topk_indices(z, k):
-    """Indices of the k largest scores per row, largest first.
+    """Indices of the k largest scores per row, largest first; equal scores
+    in ascending index order."""
+    z = _f64(z)
+    idx = np.empty((z.shape[0], k), np.int64)
+    _ok(lib().orc_topk(z.shape[0], z.shape[1], int(k), _p(z), _p(idx)), "topk")
+    return idx
 
-    Equal scores are ordered by the lower expert index (a stable sort of -z).
-    Selecting on the logits is the same as selecting on the softmax
-    probabilities, since the softmax is strictly increasing in each logit.
-    """
-    z = np.asarray(z, dtype=np.float64)
-    order = np.argsort(-z, axis=-1, kind="stable")
-    return order[..., :k]
+
+def topk_gap(z, k):
+    z = _f64(z)
+    g = np.empty(z.shape[0])
+    _ok(lib().orc_topk_gap(z.shape[0], z.shape[1], int(k), _p(z), _p(g)), "topk_gap")
+    return g
+
+
+def _gates(fn, a, idx, what):
+    a = _f64(a)
+    idx = _i64(idx)
+    w = np.empty(idx.shape)
+    _ok(fn(a.shape[0], a.shape[1], idx.shape[1], _p(a), _p(idx), _p(w)), what)
+    return w
 
 
 def gates_softmax_of_topk(z, idx):
-    """Gates as Softmax(TopK(z)): the scores outside the top-k are set to
-    minus infinity and a softmax is taken, so only the kept k are non-zero
-    (roadtointelligence.com router formula and "Tiny example")."""
-    z = np.asarray(z, dtype=np.float64)
-    masked = np.full_like(z, -np.inf)
-    np.put_along_axis(masked, idx, np.take_along_axis(z, idx, axis=-1), axis=-1)
-    g = softmax(masked)
-    return np.take_along_axis(g, idx, axis=-1)
+    """Softmax(TopK(z)) at the kept experts."""
+    return _gates(lib().orc_gates_softmax_of_topk, z, idx, "gates_softmax_of_topk")
 
 
 def gates_renormalised_probs(p, idx):
-    """Gates as top-k probabilities divided by their sum
-    (botmartz.com "Expert Routing"; matteuscruz.github.io "Architecture")."""
-    kept = np.take_along_axis(np.asarray(p, dtype=np.float64), idx, axis=-1)
-    return kept / np.sum(kept, axis=-1, keepdims=True)
+    return _gates(lib().orc_gates_renormalised_probs, p, idx, "gates_renormalised_probs")
 
 
 def gates_raw_probs(p, idx):
-    """Gates as the raw softmax probability of each kept expert, no
-    renormalisation (codingnowai.in "Mixture of Experts", section "Code")."""
-    return np.take_along_axis(np.asarray(p, dtype=np.float64), idx, axis=-1)
+    return _gates(lib().orc_gates_raw_probs, p, idx, "gates_raw_probs")
 
 
 def route(x, W_g, b_g, k, renormalize=True):
     """Router + softmax + top-k (+ renormalise).  Returns (z, p, idx, w)."""
-    z = router_logits(x, W_g, b_g)
-    p = softmax(z)
-    idx = topk_indices(z, k)
-    w = gates_softmax_of_topk(z, idx) if renormalize else gates_raw_probs(p, idx)
-    return z, p, idx, w
-
-
-def topk_gap(z, k):
-    """Score gap between the k-th and (k+1)-th largest score of each token
-    (infinite when k == N).  Tokens with a gap below a threshold are near-ties
-    whose top-k set may legitimately differ under another summation order."""
-    z = np.asarray(z, dtype=np.float64)
-    N = z.shape[-1]
-    if k >= N:
-        return np.full(z.shape[:-1], np.inf)
-    s = -np.sort(-z, axis=-1)
-    return s[..., k - 1] - s[..., k]
+    r = Layer(x, W_g, b_g, k=k).route(renormalize=renormalize)
+    return r.z, r.p, r.idx, r.w
 
 
 # ---------------------------------------------------------------------------
-# capacity and the per-expert grouping of (token, slot) assignments
-# ---------------------------------------------------------------------------
+# capacity, grouping, statistics
 
 def expert_capacity(capacity_factor, T, N):
-    """capacity factor x batch size / number of experts, rounded up."""
-    return int(math.ceil(capacity_factor * T / N))
+    """ceil(capacity factor x batch / number of experts)."""
+    return int(lib().orc_capacity(float(capacity_factor), int(T), int(N)))
 
 
 @dataclass
 class Grouping:
-    """Assignments grouped by expert.
-
-    groups[e]  : list of (t, j) kept for expert e, in token-major order
-    counts[e]  : assignments routed to e before capacity
-    kept[e]    : assignments kept (min(counts[e], capacity))
-    rank[t, j] : position of (t, j) among the assignments to its expert
-    keep[t, j] : True when the assignment is within capacity
-    """
+    """groups[e]: kept (t, j) of expert e in token-major order; counts / kept
+    per expert; rank[t, j]; keep[t, j]; dropped total."""
     groups: list
     counts: np.ndarray
     kept: np.ndarray
@@ -198,380 +497,193 @@ class Grouping:
 
 
 def group_by_expert(idx, N, capacity=0):
-    """Walk the assignments (t, j) in ascending token, then ascending slot;
-    an assignment's rank is how many earlier assignments chose the same
-    expert; it is kept when capacity <= 0 (unlimited) or rank < capacity."""
-    idx = np.asarray(idx)
+    idx = _i64(idx)
     T, k = idx.shape
-    counts = np.zeros(N, dtype=np.int64)
-    rank = np.zeros((T, k), dtype=np.int64)
-    keep = np.zeros((T, k), dtype=bool)
-    groups = [[] for _ in range(N)]
-    for t in range(T):
-        for j in range(k):
-            e = int(idx[t, j])
-            r = int(counts[e])
-            counts[e] += 1
-            rank[t, j] = r
-            if capacity <= 0 or r < capacity:
-                keep[t, j] = True
-                groups[e].append((t, j))
-    kept = np.array([len(g) for g in groups], dtype=np.int64)
-    return Grouping(groups, counts, kept, rank, keep, int(counts.sum() - kept.sum()))
+    r = Routing(z=None, p=None, idx=idx, w=None, counts=np.empty(N, np.int64),
+                kept=np.empty(N, np.int64), rank=np.empty((T, k), np.int64),
+                keep=np.empty((T, k), np.uint8), order=np.empty(T * k, np.int64),
+                group_start=np.empty(N + 1, np.int64), mean_prob=None)
+    dropped = lib().orc_group(T, k, int(N), int(capacity), _p(idx), _p(r.counts), _p(r.kept),
+                              _p(r.rank), _p(r.keep), _p(r.order), _p(r.group_start))
+    if dropped < 0:
+        raise ValueError("oracle group: invalid argument")
+    r.dropped = int(dropped)
+    return r.grouping()
+
+
+def balance_statistic(p):
+    """(mean_prob, std_unbiased(mean_prob)^2)."""
+    p = _f64(p)
+    T, N = p.shape
+    m = np.empty(N)
+    b = C.c_double()
+    _ok(lib().orc_balance(T, N, _p(p), _p(m), C.byref(b)), "balance")
+    return m, float(b.value)
+
+
+def cv_squared(counts):
+    c = _i64(counts)
+    return float(lib().orc_cv_squared(c.shape[0], _p(c)))
 
 
 # ---------------------------------------------------------------------------
 # experts and the layer
-# ---------------------------------------------------------------------------
-
-def activation(h, act):
-    h = np.asarray(h, dtype=np.float64)
-    if act == ACT_GELU_ERF:
-        # nn.GELU() default: 0.5 * h * (1 + erf(h / sqrt(2)))
-        return 0.5 * h * (1.0 + _erf(h / math.sqrt(2.0)))
-    if act == ACT_RELU:
-        return np.maximum(h, 0.0)
-    raise ValueError(f"unknown activation {act}")
-
 
 def expert_ffn(xr, W1, b1, W2, b2, act, round_hidden_bf16=False):
-    """Linear(d, d_ff) -> activation -> Linear(d_ff, d) on the rows xr.
-
-    With round_hidden_bf16 the hidden activation is rounded to bfloat16
-    before the second Linear, the storage format of the hidden layer in the
-    bf16 layer; everything else stays float64.
-    """
-    xr = np.asarray(xr, dtype=np.float64)
-    h = xr @ np.asarray(W1, dtype=np.float64).T + np.asarray(b1, dtype=np.float64)
-    h = activation(h, act)
-    if round_hidden_bf16:
-        h = round_to_bf16(h)
-    return h @ np.asarray(W2, dtype=np.float64).T + np.asarray(b2, dtype=np.float64)
+    """Linear -> activation -> Linear of one expert (W1 [f, d], W2 [d, f]) on the rows xr."""
+    L = Layer(xr, None, None, [W1], [b1], [W2], [b2], act=act,
+              round_hidden_bf16=round_hidden_bf16)
+    return L.expert_rows(0, np.arange(L.T))[2]
 
 
 @dataclass
 class LayerOutput:
-    y: np.ndarray            # [len(tokens), d] float64 layer output
-    tokens: np.ndarray       # token ids the rows of y belong to
-    z: np.ndarray            # [T, N] router scores
-    p: np.ndarray            # [T, N] router probabilities
-    idx: np.ndarray          # [T, k] selected experts, largest first
-    w: np.ndarray            # [T, k] gates
+    y: np.ndarray            # [len(tokens), d]
+    tokens: np.ndarray
+    z: np.ndarray            # [T, N]
+    p: np.ndarray            # [T, N]
+    idx: np.ndarray          # [T, k]
+    w: np.ndarray            # [T, k]
     grouping: Grouping
     mean_prob: np.ndarray    # [N]
     balance: float
-    cv_squared: float = 0.0  # of the routed counts
+    cv_squared: float = 0.0
 
 
-def balance_statistic(p):
-    """std(mean over tokens of the router probabilities)^2, torch.std's default
-    unbiased estimator (botmartz.com "Load Balancing: The Hidden Challenge").
-    Returns (mean_prob, balance); balance is 0 for a single expert."""
-    m = np.mean(np.asarray(p, dtype=np.float64), axis=0)
-    if m.shape[0] < 2:
-        return m, 0.0
-    return m, float(np.std(m, ddof=1) ** 2)
+def moe_forward(x, W_g, b_g, W1, b1, W2, b2, *, k, act, capacity=0, renormalize=True,
+                shared=None, round_hidden_bf16=False, tokens=None, idx_override=None,
+                workers=1):
+    """The whole layer; y for the tokens listed in ``tokens`` (default all).
+    Routing, grouping and statistics always cover all T tokens.
+    ``idx_override`` replaces the top-k choice (near-tie tokens)."""
+    L = Layer(x, W_g, b_g, W1, b1, W2, b2, k=k, act=act, shared=shared,
+              round_hidden_bf16=round_hidden_bf16)
+    r = L.route(capacity, renormalize, idx_override, workers)
+    tok = np.arange(L.T) if tokens is None else _i64(tokens)
+    y = L.combine_rows(r, tok, workers)
+    return LayerOutput(y, tok, r.z, r.p, r.idx, r.w, r.grouping(), r.mean_prob, r.balance,
+                       r.cv_squared)
 
 
-def cv_squared(counts):
-    """Squared coefficient of variation of the per-expert counts: the unbiased
-    variance over the N experts divided by the squared mean (matteuscruz.github.io
-    "Load balancing: the core training challenge" names the coefficient of
-    variation of the expert load; invest-in.ai "MoE - Mixture of Experts",
-    "Common Usage Examples", names cv_squared(expert_counts); the variance
-    estimator is torch's default, as in the balance statistic).  0 for a single
-    expert or when nothing was routed."""
-    c = np.asarray(counts, dtype=np.float64)
-    if c.shape[0] < 2:
-        return 0.0
-    m = float(np.mean(c))
-    if m == 0.0:
-        return 0.0
-    return float(np.var(c, ddof=1) / (m * m))
-
-
-def moe_forward(x, W_g, b_g, W1, b1, W2, b2, *, k, act, capacity=0,
-                renormalize=True, shared=None, round_hidden_bf16=False,
-                tokens=None, idx_override=None):
-    """The whole layer for the tokens listed in ``tokens`` (default: all).
-
-    Routing, grouping and the statistics always cover all T tokens, because a
-    token's capacity rank depends on every earlier token.  ``W1`` etc. may be
-    any indexable of per-expert arrays (W1[e] is [d_ff, d]); experts are read
-    one at a time.  ``shared`` is None or (W1s, b1s, W2s, b2s).
-    ``idx_override`` replaces the top-k choice (used only for tokens whose
-    k-th score gap is a near-tie); the gates are then taken for those experts.
-    """
-    x = np.asarray(x, dtype=np.float64)
-    T = x.shape[0]
-    N = np.asarray(b_g).shape[0]
-    z = router_logits(x, W_g, b_g)
-    p = softmax(z)
-    idx = topk_indices(z, k) if idx_override is None else np.asarray(idx_override, dtype=np.int64)
-    w = gates_softmax_of_topk(z, idx) if renormalize else gates_raw_probs(p, idx)
-    grouping = group_by_expert(idx, N, capacity)
-    mean_prob, balance = balance_statistic(p)
-
-    tokens = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
-    pos = {int(t): i for i, t in enumerate(tokens)}
-    y = np.zeros((len(tokens), x.shape[1]), dtype=np.float64)
-    for e in range(N):
-        rows = [(t, j) for (t, j) in grouping.groups[e] if t in pos]
-        if not rows:
-            continue
-        ts = np.array([t for t, _ in rows])
-        js = np.array([j for _, j in rows])
-        o = expert_ffn(x[ts], W1[e], b1[e], W2[e], b2[e], act, round_hidden_bf16)
-        for r, (t, j) in enumerate(zip(ts, js)):
-            y[pos[int(t)]] += w[t, j] * o[r]
-    if shared is not None:
-        W1s, b1s, W2s, b2s = shared
-        y += expert_ffn(x[tokens], W1s, b1s, W2s, b2s, act, round_hidden_bf16)
-    return LayerOutput(y, tokens, z, p, idx, w, grouping, mean_prob, balance,
-                       cv_squared(grouping.counts))
-
-
-def moe_bruteforce(x, W_g, b_g, W1, b1, W2, b2, *, k, act, capacity=0,
-                   renormalize=True, shared=None):
-    """Every expert on every token, then mask and weight: the per-slot,
-    per-expert loop of botmartz.com "Expert Routing" and codingnowai.in "Code"
-    (output[mask] += weight[mask] * expert(x)[mask]), with the capacity mask
-    applied on top.  For tiny inputs only."""
-    x = np.asarray(x, dtype=np.float64)
-    T, d = x.shape
-    N = np.asarray(b_g).shape[0]
-    z = router_logits(x, W_g, b_g)
-    p = softmax(z)
-    idx = topk_indices(z, k)
-    if renormalize:
-        w = gates_renormalised_probs(p, idx)
-    else:
-        w = gates_raw_probs(p, idx)
-    keep = group_by_expert(idx, N, capacity).keep
-    all_out = np.stack([expert_ffn(x, W1[e], b1[e], W2[e], b2[e], act) for e in range(N)])
-    y = np.zeros((T, d))
-    for j in range(k):
-        for e in range(N):
-            mask = (idx[:, j] == e) & keep[:, j]
-            y[mask] += w[mask, j][:, None] * all_out[e][mask]
-    if shared is not None:
-        y += expert_ffn(x, *shared, act)
+def moe_bruteforce(x, W_g, b_g, W1, b1, W2, b2, *, k, act, capacity=0, renormalize=True,
+                   shared=None):
+    """Every expert on every token, then masks and weights (tiny inputs only)."""
+    L = Layer(x, W_g, b_g, W1, b1, W2, b2, k=k, act=act, shared=shared)
+    y = np.empty((L.T, L.d))
+    _ok(lib().orc_bruteforce(L.ref(), int(capacity), int(bool(renormalize)), _p(y)),
+        "bruteforce")
     return y
 
 
 # ---------------------------------------------------------------------------
 # expert-choice routing
-# ---------------------------------------------------------------------------
 
 def expert_choice_tokens(T, capacity):
-    """Tokens each expert takes: the capacity, clamped to T; <= 0 means T."""
-    return T if capacity <= 0 else min(int(capacity), T)
+    return int(lib().orc_ec_tokens(int(T), int(capacity)))
 
 
-def expert_choice_select(p, C):
-    """For every expert e, the C tokens with the largest p[t, e], the lower
-    token index first among equal scores (matteuscruz.github.io "Load balancing:
-    the core training challenge": each expert selects its top tokens).  Returns
-    a list of N int arrays, each in ascending token order."""
-    p = np.asarray(p, dtype=np.float64)
+def expert_choice_select(p, C_):
+    p = _f64(p)
     T, N = p.shape
-    sel = []
-    for e in range(N):
-        order = np.lexsort((np.arange(T), -p[:, e]))   # by score descending, then token
-        sel.append(np.sort(order[:C]).astype(np.int64))
-    return sel
+    sel = np.empty((N, C_), np.int64)
+    _ok(lib().orc_ec_select(T, N, int(C_), _p(p), _p(sel)), "ec_select")
+    return [sel[e].copy() for e in range(N)]
 
 
-def expert_choice_gap(p, C):
-    """Per expert, the score gap between its C-th and (C+1)-th largest token
-    (inf when C = T or C = 0)."""
-    p = np.asarray(p, dtype=np.float64)
+def expert_choice_gap(p, C_):
+    p = _f64(p)
     T, N = p.shape
-    gaps = np.full(N, np.inf)
-    if 0 < C < T:
-        srt = -np.sort(-p, axis=0)
-        gaps = srt[C - 1] - srt[C]
-    return gaps
+    g = np.empty(N)
+    _ok(lib().orc_ec_gap(T, N, int(C_), _p(p), _p(g)), "ec_gap")
+    return g
+
+
+def expert_choice_picks(T, sel):
+    """(picks [T]: experts that picked each token, number of tokens no expert picked)."""
+    sel = _i64(sel)
+    N, C_ = sel.shape if sel.ndim == 2 else (0, 0)
+    picks = np.empty(T, np.int64)
+    unpicked = int(lib().orc_ec_picks(int(T), max(N, 1) if N else 1, C_ if N else 0,
+                                      _p(sel), _p(picks)))
+    if unpicked < 0:
+        raise ValueError("oracle ec_picks: invalid argument")
+    return picks, unpicked
 
 
 @dataclass
 class ExpertChoiceOutput:
-    y: np.ndarray            # [len(tokens), d]
+    y: np.ndarray
     tokens: np.ndarray
-    z: np.ndarray            # [T, N]
-    p: np.ndarray            # [T, N]
+    z: np.ndarray
+    p: np.ndarray
     sel: list                # N arrays of picked tokens, ascending
     gate: list               # N arrays: p[sel[e], e]
-    token_picks: np.ndarray  # [T] experts that picked each token
-    unpicked: int            # tokens no expert picked
+    token_picks: np.ndarray  # [T]
+    unpicked: int
     mean_prob: np.ndarray
     balance: float
 
 
 def expert_choice_forward(x, W_g, b_g, W1, b1, W2, b2, *, capacity, act, shared=None,
-                          round_hidden_bf16=False, tokens=None, sel_override=None):
-    """The layer with expert-choice routing: router scores and softmax as in
-    top-k routing, then every expert e runs its FFN on its C picked tokens and
-    y[t] = sum over the experts that picked t of p[t, e] * expert_e(x[t])
-    (+ the shared expert with weight 1).  ``sel_override`` replaces the
-    selection (used only for experts whose C-th score gap is a near-tie)."""
-    x = np.asarray(x, dtype=np.float64)
-    T = x.shape[0]
-    N = np.asarray(b_g).shape[0]
-    z = router_logits(x, W_g, b_g)
+                          round_hidden_bf16=False, tokens=None, sel_override=None, workers=1):
+    """Expert-choice layer; ``sel_override`` replaces the selection (near-tie experts)."""
+    L = Layer(x, W_g, b_g, W1, b1, W2, b2, k=1, act=act, shared=shared,
+              round_hidden_bf16=round_hidden_bf16)
+    z = L.logits(workers)
     p = softmax(z)
-    C = expert_choice_tokens(T, capacity)
-    sel = expert_choice_select(p, C) if sel_override is None else \
-        [np.asarray(s_, dtype=np.int64) for s_ in sel_override]
-    gate = [p[s_, e] for e, s_ in enumerate(sel)]
-    picks = np.zeros(T, dtype=np.int64)
-    for s_ in sel:
-        picks[s_] += 1
-    mean_prob, balance = balance_statistic(p)
-    tokens = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
-    pos = {int(t): i for i, t in enumerate(tokens)}
-    y = np.zeros((len(tokens), x.shape[1]), dtype=np.float64)
-    for e in range(N):
-        ts = np.array([t for t in sel[e] if int(t) in pos], dtype=np.int64)
-        if ts.size == 0:
-            continue
-        o = expert_ffn(x[ts], W1[e], b1[e], W2[e], b2[e], act, round_hidden_bf16)
-        for r, t in enumerate(ts):
-            y[pos[int(t)]] += p[t, e] * o[r]
-    if shared is not None:
-        W1s, b1s, W2s, b2s = shared
-        y += expert_ffn(x[tokens], W1s, b1s, W2s, b2s, act, round_hidden_bf16)
-    return ExpertChoiceOutput(y, tokens, z, p, sel, gate, picks, int((picks == 0).sum()),
-                              mean_prob, balance)
+    T, N = p.shape
+    C_ = expert_choice_tokens(T, capacity)
+    if sel_override is None:
+        sel = np.empty((N, C_), np.int64)
+        _ok(lib().orc_ec_select(T, N, C_, _p(p), _p(sel)), "ec_select")
+    else:
+        sel = _i64(np.stack([np.asarray(s, np.int64) for s in sel_override])
+                   if N else np.empty((0, C_), np.int64)).reshape(N, C_)
+    picks = np.empty(T, np.int64)
+    unpicked = int(lib().orc_ec_picks(T, N, C_, _p(sel), _p(picks)))
+    if unpicked < 0:
+        raise ValueError("oracle ec_picks: invalid argument")
+    m, bal = balance_statistic(p)
+    tok = np.arange(T) if tokens is None else _i64(tokens)
+    y = L.ec_combine_rows(C_, sel, p, tok, workers)
+    return ExpertChoiceOutput(y, tok, z, p, [sel[e].copy() for e in range(N)],
+                              [p[sel[e], e] for e in range(N)], picks, unpicked, m, bal)
 
 
 # ---------------------------------------------------------------------------
 # backward pass
-# ---------------------------------------------------------------------------
-
-def activation_grad(a, act):
-    """d act / d a.  GELU(a) = a Phi(a), so GELU'(a) = Phi(a) + a phi(a) with
-    Phi the normal CDF 0.5 (1 + erf(a / sqrt 2)) and phi its density."""
-    a = np.asarray(a, dtype=np.float64)
-    if act == ACT_GELU_ERF:
-        cdf = 0.5 * (1.0 + _erf(a / math.sqrt(2.0)))
-        pdf = np.exp(-0.5 * a * a) / math.sqrt(2.0 * math.pi)
-        return cdf + a * pdf
-    if act == ACT_RELU:
-        return (a > 0.0).astype(np.float64)
-    raise ValueError(f"unknown activation {act}")
-
-
-def softmax_backward(p, dp):
-    """Gradient through p = softmax(z) along the last axis: p (dp - <p, dp>)."""
-    p = np.asarray(p, dtype=np.float64)
-    dp = np.asarray(dp, dtype=np.float64)
-    return p * (dp - np.sum(p * dp, axis=-1, keepdims=True))
-
 
 @dataclass
 class LayerGrads:
-    dx: np.ndarray           # [T, d]
-    dW_g: np.ndarray         # [N, d]
-    db_g: np.ndarray         # [N]
-    dW1: np.ndarray          # [N, d_ff, d]
-    db1: np.ndarray          # [N, d_ff]
-    dW2: np.ndarray          # [N, d, d_ff]
-    db2: np.ndarray          # [N, d]
-    dz: np.ndarray           # [T, N] gradient of the router scores
-    dw: np.ndarray           # [T, k] gradient of the gates
-    shared: tuple | None     # (dW1s, db1s, dW2s, db2s) or None
-
-
-def expert_ffn_backward(xr, W1, b1, W2, b2, act, dO, round_hidden_bf16=False):
-    """One expert's FFN backward on its rows xr given dO = d loss / d output:
-    returns (dxr, dW1, db1, dW2, db2).  The hidden activation h that multiplies
-    dO in dW2 is the one the forward fed to the second Linear (bf16-rounded
-    with round_hidden_bf16)."""
-    xr = np.asarray(xr, dtype=np.float64)
-    W1 = np.asarray(W1, dtype=np.float64)
-    W2 = np.asarray(W2, dtype=np.float64)
-    a = xr @ W1.T + np.asarray(b1, dtype=np.float64)      # pre-activation
-    h = activation(a, act)
-    if round_hidden_bf16:
-        h = round_to_bf16(h)
-    dW2 = dO.T @ h                                        # [d, d_ff]
-    db2 = dO.sum(axis=0)
-    dh = dO @ W2                                          # [rows, d_ff]
-    da = dh * activation_grad(a, act)
-    dW1 = da.T @ xr                                       # [d_ff, d]
-    db1 = da.sum(axis=0)
-    dxr = da @ W1                                         # [rows, d]
-    return dxr, dW1, db1, dW2, db2
+    dx: np.ndarray
+    dW_g: np.ndarray
+    db_g: np.ndarray
+    dW1: np.ndarray
+    db1: np.ndarray
+    dW2: np.ndarray
+    db2: np.ndarray
+    dz: np.ndarray
+    dw: np.ndarray
+    shared: tuple | None
 
 
 def moe_backward(x, W_g, b_g, W1, b1, W2, b2, dy, *, k, act, capacity=0, renormalize=True,
                  shared=None, aux_weight=0.0, round_hidden_bf16=False, idx_override=None):
-    """Gradients of total = <dy, y> + aux_weight * balance with respect to x
-    and every parameter (botmartz.com "Load Balancing": total_loss = task_loss
-    + 0.01 * balance_loss, with dy standing for d task_loss / d y).
-
-    Steps, each the chain rule through the matching forward step:
-      1. combine y[t] = sum_kept w[t,j] o[t,j] (+ shared): d o[t,j] = w[t,j] dy[t],
-         d w[t,j] = <dy[t], o[t,j]> for kept (t, j), 0 for dropped ones;
-      2. each expert's FFN on its kept rows (expert_ffn_backward);
-      3. gates: renormalised, w = softmax over the k selected scores, so
-         dz[selected] = w (dw - <w, dw>); raw, w = p[selected], so
-         dp[selected] = dw and dz = p (dp - <p, dp>);
-      4. balance = sum_e (m_e - 1/N)^2 / (N - 1), m_e = mean_t p[t,e]:
-         d m_e = 2 (m_e - 1/N) / (N - 1), d p[t,e] = d m_e / T, through the softmax;
-      5. router scores z = x W_g^T + b_g: dW_g = dz^T x, db_g = sum_t dz, dx += dz W_g.
-    """
-    x = np.asarray(x, dtype=np.float64)
-    dy = np.asarray(dy, dtype=np.float64)
-    W_g = np.asarray(W_g, dtype=np.float64)
-    T, d = x.shape
-    N = W_g.shape[0]
-    z = router_logits(x, W_g, b_g)
-    p = softmax(z)
-    idx = topk_indices(z, k) if idx_override is None else np.asarray(idx_override, dtype=np.int64)
-    w = gates_softmax_of_topk(z, idx) if renormalize else gates_raw_probs(p, idx)
-    grouping = group_by_expert(idx, N, capacity)
-
-    dx = np.zeros_like(x)
-    dw = np.zeros((T, k))
-    dW1, db1, dW2, db2 = [], [], [], []
-    for e in range(N):
-        rows = grouping.groups[e]
-        W1e, W2e = np.asarray(W1[e], dtype=np.float64), np.asarray(W2[e], dtype=np.float64)
-        if not rows:
-            dW1.append(np.zeros_like(W1e)); db1.append(np.zeros(W1e.shape[0]))
-            dW2.append(np.zeros_like(W2e)); db2.append(np.zeros(W2e.shape[0]))
-            continue
-        ts = np.array([t for t, _ in rows])
-        js = np.array([j for _, j in rows])
-        o = expert_ffn(x[ts], W1e, b1[e], W2e, b2[e], act, round_hidden_bf16)
-        dw[ts, js] = np.sum(dy[ts] * o, axis=1)                       # step 1
-        dO = w[ts, js][:, None] * dy[ts]
-        dxr, gW1, gb1, gW2, gb2 = expert_ffn_backward(x[ts], W1e, b1[e], W2e, b2[e], act, dO,
-                                                      round_hidden_bf16)   # step 2
-        np.add.at(dx, ts, dxr)
-        dW1.append(gW1); db1.append(gb1); dW2.append(gW2); db2.append(gb2)
-    shared_grads = None
-    if shared is not None:
-        dxs, gW1, gb1, gW2, gb2 = expert_ffn_backward(x, *shared, act, dy, round_hidden_bf16)
-        dx += dxs
-        shared_grads = (gW1, gb1, gW2, gb2)
-
-    dz = np.zeros((T, N))                                             # step 3
-    if renormalize:
-        dz_sel = w * (dw - np.sum(w * dw, axis=1, keepdims=True))
-        np.put_along_axis(dz, idx, dz_sel, axis=1)
-    else:
-        dp = np.zeros((T, N))
-        np.put_along_axis(dp, idx, dw, axis=1)
-        dz += softmax_backward(p, dp)
-    if aux_weight != 0.0 and N > 1 and T > 0:                         # step 4
-        m = p.mean(axis=0)
-        dm = aux_weight * 2.0 * (m - 1.0 / N) / (N - 1)
-        dz += softmax_backward(p, np.broadcast_to(dm / T, p.shape))
-    dW_g = dz.T @ x                                                   # step 5
-    db_g = dz.sum(axis=0)
-    dx += dz @ W_g
-    return LayerGrads(dx, dW_g, db_g, np.stack(dW1), np.stack(db1), np.stack(dW2),
-                      np.stack(db2), dz, dw, shared_grads)
+    """Gradients of total = <dy, y> + aux_weight * balance w.r.t. x and every parameter."""
+    L = Layer(x, W_g, b_g, W1, b1, W2, b2, k=k, act=act, shared=shared,
+              round_hidden_bf16=round_hidden_bf16)
+    T, d, f, N, fs = L.T, L.d, L.f, L.N, L.fs
+    dyh, code = _host(dy)
+    g = LayerGrads(np.empty((T, d)), np.empty((N, d)), np.empty(N), np.empty((N, f, d)),
+                   np.empty((N, f)), np.empty((N, d, f)), np.empty((N, d)), np.empty((T, N)),
+                   np.empty((T, k)), None)
+    sh = (np.empty((fs, d)), np.empty(fs), np.empty((d, fs)), np.empty(d)) if fs else \
+        (None,) * 4
+    ov = _i64(idx_override) if idx_override is not None else None
+    _ok(lib().orc_backward(L.ref(), int(capacity), int(bool(renormalize)), _p(ov),
+                           _Tensor(dyh.ctypes.data, code, 0), float(aux_weight), _p(g.dx),
+                           _p(g.dW_g), _p(g.db_g), _p(g.dW1), _p(g.db1), _p(g.dW2), _p(g.db2),
+                           *[_p(a) for a in sh], _p(g.dz), _p(g.dw)), "backward")
+    if fs:
+        g.shared = sh
+    return g

@@ -34,7 +34,7 @@ EXPORTS = [
     "moe_ec_tokens_per_expert", "moe_ec_rows_max", "moe_ec_workspace_size",
     "moe_ec_forward_launch_count", "moe_ec_router", "moe_ec_select", "moe_ec_forward",
     "moe_ec_forward_profiled", "moe_backward", "moe_backward_workspace_size",
-    "moe_backward_launch_count", "moe_backward_profiled",
+    "moe_backward_launch_count", "moe_backward_profiled", "moe_ffn_kernel_name",
 ]
 PERMUTE_STATIC_SCRATCH_INTS = 1 << 18
 
@@ -96,6 +96,7 @@ def lib() -> C.CDLL:
         "moe_permute_scratch_size": (C.c_size_t, [CP]),
         "moe_workspace_size": (C.c_size_t, [CP]),
         "moe_forward_launch_count": (C.c_int32, [CP]),
+        "moe_ffn_kernel_name": (C.c_char_p, [CP, C.c_int32]),
         "moe_host_workspace_size": (C.c_size_t, [CP]),
         "moe_router_topk": (C.c_int32, [CP, P, P, P, P, P, P, P, P]),
         "moe_permute": (C.c_int32, [CP, P, P, P, P, P, P, P, P, P, C.c_size_t, P]),
@@ -191,6 +192,12 @@ def workspace_size(cfg: MoeConfig) -> int:
 
 def forward_launch_count(cfg: MoeConfig) -> int:
     return int(lib().moe_forward_launch_count(C.byref(cfg)))
+
+
+def ffn_kernel_name(cfg: MoeConfig, linear: int) -> str | None:
+    """Kernel and tile that moe_forward launches for grouped Linear 1 or 2."""
+    r = lib().moe_ffn_kernel_name(C.byref(cfg), int(linear))
+    return None if r is None else r.decode()
 
 
 def host_workspace_size(cfg: MoeConfig) -> int:

@@ -1,5 +1,7 @@
 // C ABI of libmoe (declared in include/moe.h): host-side validation,
 // workspace layout, and the sequence of launches of one layer.
+#include <cuda.h>
+
 #include <atomic>
 #include <cmath>
 #include <mutex>
@@ -213,10 +215,42 @@ EcWorkspace ec_layout(const moe_config& c, void* base) {
   return w;
 }
 
-// Device status word address and SM count, per device.
+}  // namespace
+
+// Unique id of the calling thread's current CUDA context, 0 when none is
+// current or the driver cannot say.  Per-device caches of device addresses and
+// kernel attributes belong to one context; after cudaDeviceReset the device's
+// next context has a new id, so a cache keyed on it is refilled.
+uint64_t context_id() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(p);
+  });
+  CUcontext c = nullptr;
+  if (!get_current || !get_id || get_current(&c) != CUDA_SUCCESS || c == nullptr) return 0;
+  unsigned long long id = 0;
+  return get_id(c, &id) == CUDA_SUCCESS ? uint64_t(id) : 0;
+}
+
+namespace {
+
+// Device status word address and SM count, per device (and context).
 struct DeviceInfo {
   int32_t* status = nullptr;
   int num_sms = 0;
+  uint64_t ctx = 0;
 };
 
 bool device_info(DeviceInfo* out) {
@@ -225,7 +259,8 @@ bool device_info(DeviceInfo* out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
   std::lock_guard<std::mutex> lock(mu);
-  if (!cache[dev].status) {
+  const uint64_t ctx = context_id();
+  if (!cache[dev].status || (ctx != 0 && ctx != cache[dev].ctx)) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_device_status) != cudaSuccess) return false;
     int sms = 0;
@@ -233,6 +268,7 @@ bool device_info(DeviceInfo* out) {
       return false;
     cache[dev].status = static_cast<int32_t*>(ptr);
     cache[dev].num_sms = sms;
+    cache[dev].ctx = context_id();       // current now: the lookup made it so
   }
   *out = cache[dev];
   return true;
@@ -505,6 +541,11 @@ int32_t moe_forward_launch_count(const moe_config* cfg) {
   const int ffn = rows_max_of(c) > 0 ? 2 : 0;
   return router_launch_count(c) + permute_launch_count(c) + ffn + (c.T > 0 ? 1 : 0) +
          (permute_fuses_stats(c) ? 0 : 1);
+}
+
+const char* moe_ffn_kernel_name(const moe_config* cfg, int32_t linear) {
+  if (check_config(cfg) != MOE_OK || (linear != 1 && linear != 2)) return nullptr;
+  return grouped_linear_kernel_name(*cfg, linear, 0);
 }
 
 size_t moe_host_workspace_size(const moe_config* cfg) {

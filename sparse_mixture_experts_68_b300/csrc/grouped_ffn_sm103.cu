@@ -1368,6 +1368,29 @@ cudaError_t launch_grouped_ffn_bf16(const moe_config& c, const GroupedFfnArgs& g
                         c.d_model, EPI_BIAS, s);
 }
 
+// Name of the kernel (and tile) one grouped Linear of moe_forward launches,
+// chosen by the same rules as grouped_linear (linear 1: Xp -> H, 2: H -> Yp).
+const char* grouped_linear_kernel_name(const moe_config& c, int linear, int64_t routed_rows) {
+  if (c.dtype == MOE_F32) return "simt_gemm_kernel (fp32 CUDA cores)";
+  const int64_t K = linear == 1 ? c.d_model : c.d_ff;
+  const int64_t Nd = linear == 1 ? c.d_ff : c.d_model;
+  const int epi = linear == 2 ? EPI_BIAS
+                              : (c.act == MOE_ACT_RELU ? EPI_BIAS_RELU : EPI_BIAS_GELU);
+  const int64_t groups = c.n_experts + (c.d_ff_shared > 0 ? 1 : 0);
+  const int64_t routed = routed_rows > 0 ? routed_rows : c.T * c.top_k;
+  const int64_t rows = routed + (c.d_ff_shared > 0 ? c.T : 0);
+  const int nb = swap_rows(Nd, rows / groups, epi);
+  if (nb == 16) return "tc_swap_gemm_kernel (128 weight rows x 16 tokens)";
+  if (nb == 32) return "tc_swap_gemm_kernel (128 weight rows x 32 tokens)";
+  switch (pick_tile(Nd, rows / groups, K)) {
+    case TILE_256_PAIR: return "tc2_grouped_gemm_kernel (256 x 256 on a CTA pair)";
+    case TILE_256: return "tc_grouped_gemm_kernel (128 x 256)";
+    case TILE_128: return "tc_grouped_gemm_kernel (128 x 128)";
+    case TILE_64: return "tc_grouped_gemm_kernel (128 x 64)";
+    default: return "tc_grouped_gemm_kernel (128 x 128, two CTAs per SM)";
+  }
+}
+
 // Router scores z = x . W_g^T + b_g (fp32) as one dense group on the tensor
 // cores: bf16 products are exact in fp32, so only the summation order differs
 // from a CUDA-core dot product.  N % 64 == 0; 64-wide tiles give ceil(T/128)

@@ -138,6 +138,10 @@ struct GroupedFfnArgs {
 // whether the bf16 first Linear stores its pre-activation from its epilogue
 // (else a second pass does)
 bool linear_saves_pre(const moe_config& c);
+// Unique id of the calling thread's current CUDA context (0: none current).
+uint64_t context_id();
+// Kernel (and tile) of grouped Linear 1 or 2 for this layer; routed_rows 0: T * top_k.
+const char* grouped_linear_kernel_name(const moe_config& c, int linear, int64_t routed_rows);
 
 // Records a caller's event on s (as an external node while s is capturing).
 cudaError_t record_event(void* event, cudaStream_t s);

@@ -311,10 +311,30 @@ size_t sort_smem_bytes(const moe_config& c) {
   return size_t(kSortWarps * c.n_experts + 3 * c.n_experts + 32) * 4 + size_t(A) * 4 + 16;
 }
 
+constexpr int kSortSmemMax = 190 * 1024;
+
 // Above ~16K assignments the multi-block histogram path is faster.
 bool single_block_sort_fits(const moe_config& c) {
   return c.n_experts <= kSortWarps * 32 && c.T * c.top_k <= 16384 &&
-         sort_smem_bytes(c) <= 190 * 1024;
+         sort_smem_bytes(c) <= size_t(kSortSmemMax);
+}
+
+// Lets permute_sort_kernel take up to kSortSmemMax of dynamic shared memory:
+// set once per device and context rather than on every launch.
+cudaError_t allow_sort_smem() {
+  static std::mutex mu;
+  static uint64_t done_ctx[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  const uint64_t ctx = context_id();
+  if (ctx != 0 && done_ctx[dev] == ctx) return cudaSuccess;
+  e = cudaFuncSetAttribute(permute_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSortSmemMax);
+  if (e == cudaSuccess) done_ctx[dev] = context_id();
+  return e;
 }
 
 template <typename T>
@@ -404,8 +424,7 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* to
   cudaError_t e;
   if (single_block_sort_fits(c)) {
     const size_t smem = sort_smem_bytes(c);
-    e = cudaFuncSetAttribute(permute_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(smem));
+    e = allow_sort_smem();
     if (e != cudaSuccess) return e;
     const StatsArgs none{};
     e = launch_pdl(permute_sort_kernel, dim3(1), dim3(kSortWarps * 32), smem, s, topk_idx, T, k,
@@ -449,19 +468,24 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_static_scratch_mu;
 void* g_static_scratch_addr[kMaxDevices] = {};
+uint64_t g_static_scratch_ctx[kMaxDevices] = {};
 
-// Device address of the array for the current device (looked up on first use).
+// Device address of the array for the current device, looked up on the
+// device's first use and again whenever the device's context has changed
+// (for example after cudaDeviceReset), since the address belongs to one context.
 cudaError_t static_scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_static_scratch_mu);
-  if (g_static_scratch_addr[dev] == nullptr) {
+  const uint64_t ctx = context_id();
+  if (g_static_scratch_addr[dev] == nullptr || (ctx != 0 && ctx != g_static_scratch_ctx[dev])) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_permute_static_scratch);
     if (e != cudaSuccess) return e;
     g_static_scratch_addr[dev] = p;
+    g_static_scratch_ctx[dev] = context_id();
   }
   *out = g_static_scratch_addr[dev];
   return cudaSuccess;

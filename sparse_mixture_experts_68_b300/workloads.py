@@ -75,6 +75,15 @@ WORKLOADS = {
         seed=2,
         description="T=8192, d=1024, d_ff=4096, N=64, top-1, ReLU, capacity "
                     "ceil(1.25 T/N)=160, Zipf-skewed router bias, bf16"),
+    # the same layer with the raw softmax probability as the gate, no
+    # renormalisation (codingnowai.in "Mixture of Experts", section "Code")
+    "c2_switch_top1_raw": Workload(
+        "c2_switch_top1_raw", T=8192, d_model=1024, d_ff=4096, n_experts=64, top_k=1,
+        act=ACT_RELU, dtype=DT_BF16, capacity_factor=1.25, zipf_router_bias=True,
+        renormalize=0, seed=2,
+        description="T=8192, d=1024, d_ff=4096, N=64, top-1, ReLU, capacity "
+                    "ceil(1.25 T/N)=160, Zipf-skewed router bias, raw-probability "
+                    "gates (no renormalisation), bf16"),
     "c3_mixtral_prefill": Workload(
         "c3_mixtral_prefill", T=4096, d_model=4096, d_ff=14336, n_experts=8,
         top_k=2, act=ACT_GELU_ERF, dtype=DT_BF16, seed=3,

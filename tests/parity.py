@@ -12,10 +12,15 @@ oracle's own wherever it is not a near-tie).
 
 from __future__ import annotations
 
+import os
+
 import numpy as np
 import torch
 
 from oracle import moe_oracle as O
+
+# threads that each run the single-threaded oracle on their own token rows
+WORKERS = max(1, min(48, os.cpu_count() or 1))
 
 TIE_EPS = 1e-4
 TOL = {0: 1e-4, 1: 2e-2}          # by dtype code: fp32, bf16
@@ -29,15 +34,17 @@ def to64(t: torch.Tensor) -> np.ndarray:
     return t.detach().to("cpu", torch.float64).numpy()
 
 
-class Experts:
-    """Per-expert float64 copies of a stacked device weight, fetched on use
-    (nothing is kept, so a layer with 15 GB of weights fits in host memory)."""
+def host_tensors(tensors: dict) -> dict:
+    """Host copies of a layer's tensors in their storage dtype (the oracle reads
+    bf16 values as they are stored)."""
+    return {n: v.detach().cpu() for n, v in tensors.items()}
 
-    def __init__(self, t: torch.Tensor):
-        self.t = t
 
-    def __getitem__(self, e):
-        return to64(self.t[e])
+def oracle_layer(cfg, th: dict, k=None) -> O.Layer:
+    shared = tuple(th[n] for n in ("W1s", "b1s", "W2s", "b2s")) if cfg.d_ff_shared else None
+    return O.Layer(th["x"], th["W_g"], th["b_g"], th["W1"], th["b1"], th["W2"], th["b2"],
+                   k=cfg.top_k if k is None else k, act=cfg.act, shared=shared,
+                   round_hidden_bf16=(cfg.dtype == 1))
 
 
 def near_tie_sets(z: np.ndarray, k: int):
@@ -94,55 +101,54 @@ def check_routing(wl_dtype, cfg, tensors, out, z_ref, report, z_gpu=None):
     return idx_gpu
 
 
-def check_layer(wl, cfg, tensors, out, tokens=None, capacity=None, check_logits=True):
-    """Full comparison of one moe_forward against the oracle.  Returns a report."""
+def check_layer(wl, cfg, tensors, out, tokens=None, capacity=None, check_logits=True,
+                th=None, L=None):
+    """Full comparison of one moe_forward against the oracle.  Returns
+    (report, oracle LayerOutput for `tokens`)."""
     report = {}
-    x = to64(tensors["x"])
-    W_g, b_g = to64(tensors["W_g"]), to64(tensors["b_g"])
-    z_ref = O.router_logits(x, W_g, b_g)
+    th = host_tensors(tensors) if th is None else th
+    L = oracle_layer(cfg, th) if L is None else L
+    z_ref = L.logits(WORKERS)
     zg = None
     if check_logits and out.logits is not None:
         # fp32 sums of d products: the statistical rounding error is about
         # sqrt(d) * 2^-24 * |partial sums|, ~1e-6 of the largest score here;
         # the bar leaves a 10x margin.
         zg = out.logits.cpu().numpy().astype(np.float64)
-        err = np.abs(zg - z_ref).max() / max(np.abs(z_ref).max(), 1e-30)
+        err = np.abs(zg - z_ref).max() / max(np.abs(z_ref).max(), 1e-30) if zg.size else 0.0
         report["logit_max_rel"] = float(err)
         assert err < 1e-5, f"router scores differ: {err}"
     idx_gpu = check_routing(cfg.dtype, cfg, tensors, out, z_ref, report, z_gpu=zg)
 
     cap = cfg.capacity if capacity is None else capacity
-    shared = None
-    if cfg.d_ff_shared:
-        shared = tuple(to64(tensors[n]) for n in ("W1s", "b1s", "W2s", "b2s"))
-    ref = O.moe_forward(x, W_g, b_g, Experts(tensors["W1"]), Experts(tensors["b1"]),
-                        Experts(tensors["W2"]), Experts(tensors["b2"]), k=cfg.top_k,
-                        act=cfg.act, capacity=cap, renormalize=bool(cfg.renormalize),
-                        shared=shared, round_hidden_bf16=(cfg.dtype == 1), tokens=tokens,
-                        idx_override=idx_gpu)
-    g = ref.grouping
+    r = L.route(cap, bool(cfg.renormalize), idx_gpu, workers=WORKERS, z=z_ref)
+    g = r.grouping()
     # counts and drops: exact
     np.testing.assert_array_equal(out.counts.cpu().numpy(), g.counts)
     np.testing.assert_array_equal(out.kept.cpu().numpy(), g.kept)
     assert int(out.dropped.cpu().item()) == g.dropped
     # statistics
-    np.testing.assert_allclose(out.mean_prob.cpu().numpy(), ref.mean_prob,
+    np.testing.assert_allclose(out.mean_prob.cpu().numpy(), r.mean_prob,
                                rtol=MEAN_PROB_RTOL, atol=1e-8)
     bal = float(out.balance.cpu().item())
-    assert abs(bal - ref.balance) <= BALANCE_RTOL * abs(ref.balance) + 1e-9, \
-        f"balance {bal} vs {ref.balance}"
+    assert abs(bal - r.balance) <= BALANCE_RTOL * abs(r.balance) + 1e-9, \
+        f"balance {bal} vs {r.balance}"
     if out.cv_squared is not None:
         # exact integer sums, then one fp64 quotient rounded to fp32
         cv = float(out.cv_squared.cpu().item())
-        assert abs(cv - ref.cv_squared) <= CV_RTOL * abs(ref.cv_squared), \
-            f"cv_squared {cv} vs {ref.cv_squared}"
+        assert abs(cv - r.cv_squared) <= CV_RTOL * abs(r.cv_squared), \
+            f"cv_squared {cv} vs {r.cv_squared}"
     # output rows
+    rows = np.arange(cfg.T) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    y_ref = L.combine_rows(r, rows, WORKERS)
+    ref = O.LayerOutput(y_ref, rows, r.z, r.p, r.idx, r.w, g, r.mean_prob, r.balance,
+                        r.cv_squared)
     y_gpu = out.y.float().cpu().numpy().astype(np.float64)
-    rows = ref.tokens
-    e = row_errors(y_gpu[rows], ref.y)
+    e = row_errors(y_gpu[rows], y_ref)
+    report["rows_compared"] = int(len(rows))
     report["max_row_rel_l2"] = float(e.max()) if e.size else 0.0
-    report["tensor_rel_l2"] = float(np.linalg.norm(y_gpu[rows] - ref.y) /
-                                    max(np.linalg.norm(ref.y), 1e-30)) if e.size else 0.0
+    report["tensor_rel_l2"] = float(np.linalg.norm(y_gpu[rows] - y_ref) /
+                                    max(np.linalg.norm(y_ref), 1e-30)) if e.size else 0.0
     tol = TOL[cfg.dtype]
     assert report["max_row_rel_l2"] <= tol, \
         f"max row rel L2 {report['max_row_rel_l2']} > {tol} (token {rows[int(np.argmax(e))]})"
@@ -153,6 +159,72 @@ def check_layer(wl, cfg, tensors, out, tokens=None, capacity=None, check_logits=
             assert np.all(y_gpu[t] == 0.0), f"dropped token {t} is not zero"
         report["fully_dropped_checked"] = int(dropped_all[rows].sum())
     return report, ref
+
+
+def tile_cover(live: int, rng, tile=128):
+    """Positions in a group of `live` rows that visit every `tile`-row m-tile:
+    each tile's first and last live row and one at random in between."""
+    pos = set()
+    for s0 in range(0, live, tile):
+        s1 = min(live, s0 + tile) - 1
+        pos |= {s0, s1, int(rng.integers(s0, s1 + 1))}
+    return sorted(pos)
+
+
+def tile_cover_tokens(grouping, T, seed, shared=False):
+    """Tokens whose grouped rows visit every 128-row m-tile of every expert
+    group (and of the shared group: every token is a row of it)."""
+    rng = np.random.default_rng(seed)
+    toks = set()
+    for e, grp in enumerate(grouping.groups):
+        for i in tile_cover(len(grp), rng):
+            toks.add(grp[i][0])
+    if shared:
+        toks |= set(tile_cover(T, rng))
+    return np.array(sorted(toks), dtype=np.int64)
+
+
+def check_grouped_rows(cfg, L, grouping, offsets, H, Yp, seed, all_shared=False):
+    """Grouped hidden rows H and expert outputs Yp against the oracle's expert
+    FFN on the same token, at positions that visit every 128-row m-tile of
+    every group (the first and last live row of each tile and one more), and
+    every row of the shared group when all_shared.  Per-row relative L2 within
+    the layer's bar.  Returns a report."""
+    rng = np.random.default_rng(seed)
+    off = offsets.cpu().numpy().astype(np.int64)
+    N, T = cfg.n_experts, cfg.T
+    jobs = []                                   # (group, positions, tokens)
+    for e in range(N):
+        grp = grouping.groups[e]
+        pos = tile_cover(len(grp), rng)
+        if pos:
+            jobs.append((e, np.array(pos), np.array([grp[i][0] for i in pos], np.int64)))
+    if cfg.d_ff_shared and T:
+        pos = np.arange(T) if all_shared else np.array(tile_cover(T, rng))
+        # the shared group holds token t at row offsets[N] + t
+        for lo in range(0, len(pos), 256):
+            jobs.append((N, pos[lo:lo + 256], pos[lo:lo + 256].astype(np.int64)))
+    from concurrent.futures import ThreadPoolExecutor
+
+    def run(job):
+        e, pos, toks = job
+        _, h, o = L.expert_rows(e, toks, want=("h", "o"))
+        rows = off[e] + pos
+        hg = H[torch.from_numpy(rows)].float().cpu().numpy().astype(np.float64)
+        og = Yp[torch.from_numpy(rows)].float().cpu().numpy().astype(np.float64)
+        return e, row_errors(hg, h), row_errors(og, o)
+
+    with ThreadPoolExecutor(max_workers=WORKERS) as ex:
+        res = list(ex.map(run, jobs))
+    tol = TOL[cfg.dtype]
+    worst_h = max((float(eh.max()) for _, eh, _ in res), default=0.0)
+    worst_o = max((float(eo.max()) for _, _, eo in res), default=0.0)
+    n_rows = sum(len(eo) for _, _, eo in res)
+    for e, eh, eo in res:
+        assert eh.max() <= tol, f"group {e}: hidden row error {eh.max()}"
+        assert eo.max() <= tol, f"group {e}: expert output row error {eo.max()}"
+    return {"grouped_rows_compared": n_rows, "max_hidden_row_rel_l2": worst_h,
+            "max_expert_row_rel_l2": worst_o}
 
 
 def check_grouping(cfg, tensors_x, offsets, row_token, token_row, Xp, ref_grouping, T):
@@ -190,7 +262,7 @@ def check_grouping(cfg, tensors_x, offsets, row_token, token_row, Xp, ref_groupi
 EC_GATE_RTOL = 1e-5
 
 
-def check_ec_layer(wl, cfg, tensors, out, tokens=None):
+def check_ec_layer(wl, cfg, tensors, out, tokens=None, th=None, L=None):
     """Full comparison of one moe_ec_forward against the oracle.
 
     The selection is exact for every expert whose oracle gap between its C-th
@@ -200,9 +272,9 @@ def check_ec_layer(wl, cfg, tensors, out, tokens=None):
     token clearly above the cut and none clearly below.  The oracle then runs
     on the GPU's selection."""
     report = {}
-    x = to64(tensors["x"])
-    W_g, b_g = to64(tensors["W_g"]), to64(tensors["b_g"])
-    z_ref = O.router_logits(x, W_g, b_g)
+    th = host_tensors(tensors) if th is None else th
+    L = oracle_layer(cfg, th, k=1) if L is None else L
+    z_ref = L.logits(WORKERS)
     p_ref = O.softmax(z_ref)
     T, N = z_ref.shape
     C = O.expert_choice_tokens(T, cfg.capacity)
@@ -237,24 +309,24 @@ def check_ec_layer(wl, cfg, tensors, out, tokens=None):
             np.testing.assert_allclose(gate_gpu[e], p_ref[g, e], rtol=2.0 * dz + EC_GATE_RTOL,
                                        atol=1e-7, err_msg=f"expert {e} gates")
     report["near_tie_experts"] = int(near.sum())
-    shared = None
-    if cfg.d_ff_shared:
-        shared = tuple(to64(tensors[n]) for n in ("W1s", "b1s", "W2s", "b2s"))
-    ref = O.expert_choice_forward(x, W_g, b_g, Experts(tensors["W1"]), Experts(tensors["b1"]),
-                                  Experts(tensors["W2"]), Experts(tensors["b2"]),
-                                  capacity=cfg.capacity, act=cfg.act, shared=shared,
-                                  round_hidden_bf16=(cfg.dtype == 1), tokens=tokens,
-                                  sel_override=sel_use)
-    np.testing.assert_array_equal(out.token_picks.cpu().numpy(), ref.token_picks)
-    assert int(out.unpicked.cpu().item()) == ref.unpicked
-    np.testing.assert_allclose(out.mean_prob.cpu().numpy(), ref.mean_prob,
+    sel = np.stack(sel_use) if N else np.empty((0, C), np.int64)
+    picks, unpicked = O.expert_choice_picks(T, sel)
+    np.testing.assert_array_equal(out.token_picks.cpu().numpy(), picks)
+    assert int(out.unpicked.cpu().item()) == unpicked
+    mean_prob, balance = O.balance_statistic(p_ref)
+    np.testing.assert_allclose(out.mean_prob.cpu().numpy(), mean_prob,
                                rtol=MEAN_PROB_RTOL, atol=1e-8)
     bal = float(out.balance.cpu().item())
-    assert abs(bal - ref.balance) <= BALANCE_RTOL * abs(ref.balance) + 1e-9, \
-        f"balance {bal} vs {ref.balance}"
+    assert abs(bal - balance) <= BALANCE_RTOL * abs(balance) + 1e-9, \
+        f"balance {bal} vs {balance}"
+    rows = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    y_ref = L.ec_combine_rows(C, sel, p_ref, rows, WORKERS)
+    ref = O.ExpertChoiceOutput(y_ref, rows, z_ref, p_ref, sel_use,
+                               [p_ref[s_, e] for e, s_ in enumerate(sel_use)], picks,
+                               unpicked, mean_prob, balance)
     y_gpu = out.y.float().cpu().numpy().astype(np.float64)
-    rows = ref.tokens
-    e = row_errors(y_gpu[rows], ref.y)
+    e = row_errors(y_gpu[rows], y_ref)
+    report["rows_compared"] = int(len(rows))
     report["max_row_rel_l2"] = float(e.max()) if e.size else 0.0
     tol = TOL[cfg.dtype]
     assert report["max_row_rel_l2"] <= tol, \

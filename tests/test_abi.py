@@ -187,3 +187,18 @@ def test_backward_sizes_and_validation(lib):
     st = lib.moe_backward(C.byref(cfg), fake, C.byref(w), C.byref(o), fake, 1 << 40, fake,
                           float("nan"), C.byref(g), fake, 1 << 40, None)
     assert st == B.MOE_ERR_INVALID_ARG
+
+
+def test_ffn_kernel_names_follow_the_layer_shape():
+    """moe_ffn_kernel_name (host only) names the tile family each grouped
+    Linear launches for the benchmark's layers."""
+    from sparse_mixture_experts_68_b300.workloads import WORKLOADS
+    name = lambda w, i: B.ffn_kernel_name(B.make_config(WORKLOADS[w]), i)   # noqa: E731
+    assert "tc2_grouped_gemm_kernel" in name("c3_mixtral_prefill", 1)
+    assert "tc2_grouped_gemm_kernel" in name("c3_mixtral_prefill", 2)
+    assert "tc_swap_gemm_kernel" in name("c3_mixtral_decode", 1)
+    assert "tc_swap_gemm_kernel" in name("c3_mixtral_decode", 2)
+    assert name("c1_page1_bf16", 1).startswith("tc_grouped_gemm_kernel")
+    assert "simt_gemm_kernel" in name("c0_pr1_fp32", 1)
+    cfg = B.make_config(WORKLOADS["c1_page1_bf16"])
+    assert B.lib().moe_ffn_kernel_name(C.byref(cfg), 3) is None

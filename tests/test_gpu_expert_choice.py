@@ -1,7 +1,8 @@
 """Expert-choice routing on the GPU (through the C ABI) against the CPU oracle:
 the selection step alone, bit for bit on fp32 scores with many exact ties;
-whole layers on small shapes in full; the two expert-choice workloads on
-sampled tokens; edge cases."""
+whole layers on small shapes in full; the two expert-choice workloads at full
+size with the output compared on tokens that visit every 128-row m-tile of
+every expert's group; edge cases."""
 
 import numpy as np
 import pytest
@@ -195,19 +196,33 @@ def test_profiled_matches_forward_and_is_deterministic():
     assert B.ec_forward_launch_count(layer.cfg) == 7
 
 
-def test_workload_c3_mixtral_prefill_ec_sampled():
+def tile_tokens(sel, T, seed):
+    """One picked token at a random row of every 128-row m-tile of every
+    expert's group (the GPU's selection; check_ec_layer checks it against the
+    oracle's), plus the first and last token."""
+    rng = np.random.default_rng(seed)
+    toks = {0, T - 1}
+    for s_ in sel:
+        for s0 in range(0, len(s_), 128):
+            toks.add(int(s_[int(rng.integers(s0, min(len(s_), s0 + 128)))]))
+    return np.array(sorted(toks), dtype=np.int64)
+
+
+def test_workload_c3_mixtral_prefill_ec_every_tile():
     wl = WORKLOADS["c3_mixtral_prefill_ec"]
     t, layer, out = run_ec(wl)
     assert B.ec_tokens_per_expert(layer.cfg) == 1024
-    report, ref = check_ec_layer(wl, layer.cfg, t, out, tokens=sample(wl.T, 24, 6))
+    sel = out.ec_token.cpu().numpy().reshape(wl.n_experts, 1024)
+    report, ref = check_ec_layer(wl, layer.cfg, t, out, tokens=tile_tokens(sel, wl.T, 6))
     print("parity", wl.name, report, "unpicked", ref.unpicked)
 
 
-def test_workload_c4_deepseek_v3_ec_sampled():
+def test_workload_c4_deepseek_v3_ec_every_tile():
     wl = WORKLOADS["c4_deepseek_v3_ec"]
     t, layer, out = run_ec(wl)
     assert B.ec_tokens_per_expert(layer.cfg) == 128
-    report, ref = check_ec_layer(wl, layer.cfg, t, out, tokens=sample(wl.T, 10, 7))
+    sel = out.ec_token.cpu().numpy().reshape(wl.n_experts, 128)
+    report, ref = check_ec_layer(wl, layer.cfg, t, out, tokens=tile_tokens(sel, wl.T, 7))
     print("parity", wl.name, report, "unpicked", ref.unpicked)
     del t, layer, out
     torch.cuda.empty_cache()

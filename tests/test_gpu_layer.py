@@ -1,9 +1,13 @@
 """Parity of the CUDA path (through the C ABI) with the CPU oracle.
 
-Small shapes run in full and span several tiles with ragged tails; the five
-layer workloads run at their full sizes, with every token routed and grouped
-and the output rows compared on all tokens (small layers) or on a seeded
-sample of tokens (large layers)."""
+Small shapes run in full and span several tiles with ragged tails.  The
+layer workloads run at their full sizes with every token routed and grouped;
+the output rows are compared on all tokens (the page-1, PR1 and Switch
+layers), and on the two largest layers (Mixtral- and DeepSeek-V3-sized) the
+grouped hidden rows and expert outputs are compared at rows that visit every
+128-row m-tile of every expert group (first, last and one random live row per
+tile) and every row of the shared group, with the layer output on a sample of
+tokens that visits every m-tile."""
 
 import numpy as np
 import pytest
@@ -15,7 +19,8 @@ from sparse_mixture_experts_68_b300 import synth
 from sparse_mixture_experts_68_b300.workloads import (ACT_GELU_ERF, ACT_RELU, DT_BF16, DT_F32,
                                                       WORKLOADS, Workload)
 
-from parity import check_grouping, check_layer, to64
+from parity import (check_grouped_rows, check_grouping, check_layer, host_tensors, oracle_layer,
+                    tile_cover)
 
 pytestmark = pytest.mark.gpu
 
@@ -103,62 +108,63 @@ def test_small_layers_full_parity(wl):
     assert report["max_row_rel_l2"] <= (1e-4 if wl.dtype == DT_F32 else 2e-2)
 
 
+def run_staged(cfg, t, dev="cuda"):
+    """The layer's steps called one by one through the ABI: router + top-k,
+    permute, grouped FFN (hidden rows H and expert outputs Yp kept), combine,
+    statistics.  Returns every buffer."""
+    T, k, N = cfg.T, cfg.top_k, cfg.n_experts
+    rows = B.rows_max(cfg)
+    dt = torch.float32 if cfg.dtype == B.MOE_F32 else torch.bfloat16
+    f32, i32 = torch.float32, torch.int32
+    b = dict(logits=torch.empty((T, N), dtype=f32, device=dev),
+             idx=torch.empty((T, k), dtype=i32, device=dev),
+             w=torch.empty((T, k), dtype=f32, device=dev),
+             pp=torch.empty((B.router_blocks(cfg), N), dtype=f32, device=dev),
+             counts=torch.empty(N, dtype=i32, device=dev),
+             kept=torch.empty(N, dtype=i32, device=dev),
+             offsets=torch.empty(N + 2, dtype=i32, device=dev),
+             row_token=torch.empty(rows, dtype=i32, device=dev),
+             token_row=torch.empty((T, k), dtype=i32, device=dev),
+             Xp=torch.empty((rows, cfg.d_model), dtype=dt, device=dev),
+             scratch=torch.empty(B.permute_scratch_size(cfg), dtype=torch.uint8, device=dev),
+             H=torch.empty((rows, cfg.d_ff), dtype=dt, device=dev),
+             Yp=torch.empty((rows, cfg.d_model), dtype=dt, device=dev),
+             y=torch.empty((T, cfg.d_model), dtype=dt, device=dev),
+             mean_prob=torch.empty(N, dtype=f32, device=dev),
+             balance=torch.empty(1, dtype=f32, device=dev),
+             dropped=torch.empty(1, dtype=i32, device=dev),
+             cv2=torch.empty(1, dtype=f32, device=dev))
+    B.router_topk(cfg, t["x"], t["W_g"], t["b_g"], b["logits"], b["idx"], b["w"], b["pp"])
+    B.permute(cfg, t["x"], b["idx"], b["counts"], b["kept"], b["offsets"], b["row_token"],
+              b["token_row"], b["Xp"], b["scratch"])
+    B.grouped_ffn(cfg, b["Xp"], b["offsets"], b["kept"], B.make_weights(t), b["H"], b["Yp"])
+    B.combine(cfg, b["Yp"], b["token_row"], b["w"], b["offsets"], b["y"])
+    B.load_stats(cfg, b["pp"], b["counts"], b["kept"], b["mean_prob"], b["balance"],
+                 b["dropped"], b["cv2"])
+    torch.cuda.synchronize()
+    b["out"] = B.Outputs(b["y"], b["idx"], b["w"], b["counts"], b["kept"], b["dropped"],
+                         b["mean_prob"], b["balance"], b["logits"], b["cv2"])
+    return b
+
+
 def test_stages_through_the_abi():
     """Each step called on its own: router, permute (layout checked), grouped
-    FFN (hidden rows checked), combine, stats."""
+    FFN (hidden rows and expert outputs of every group checked), combine, stats."""
     wl = Workload("stages", T=700, d_model=128, d_ff=256, n_experts=6, top_k=2,
                   act=ACT_GELU_ERF, dtype=DT_BF16, capacity_factor=1.1, d_ff_shared=256,
                   seed=21)
     t = synth.make_layer(wl, device="cuda")
     cfg = B.make_config(wl)
-    dev = "cuda"
-    T, k, N = wl.T, wl.top_k, wl.n_experts
-    rows = B.rows_max(cfg)
-    logits = torch.empty((T, N), dtype=torch.float32, device=dev)
-    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
-    w = torch.empty((T, k), dtype=torch.float32, device=dev)
-    pp = torch.empty((B.router_blocks(cfg), N), dtype=torch.float32, device=dev)
-    B.router_topk(cfg, t["x"], t["W_g"], t["b_g"], logits, idx, w, pp)
-    counts = torch.empty(N, dtype=torch.int32, device=dev)
-    kept = torch.empty(N, dtype=torch.int32, device=dev)
-    offsets = torch.empty(N + 2, dtype=torch.int32, device=dev)
-    row_token = torch.empty(rows, dtype=torch.int32, device=dev)
-    token_row = torch.empty((T, k), dtype=torch.int32, device=dev)
-    Xp = torch.empty((rows, wl.d_model), dtype=torch.bfloat16, device=dev)
-    scratch = torch.empty(B.permute_scratch_size(cfg), dtype=torch.uint8, device=dev)
-    B.permute(cfg, t["x"], idx, counts, kept, offsets, row_token, token_row, Xp, scratch)
-    H = torch.empty((rows, wl.d_ff), dtype=torch.bfloat16, device=dev)
-    Yp = torch.empty((rows, wl.d_model), dtype=torch.bfloat16, device=dev)
-    weights = B.make_weights(t)
-    B.grouped_ffn(cfg, Xp, offsets, kept, weights, H, Yp)
-    y = torch.empty((T, wl.d_model), dtype=torch.bfloat16, device=dev)
-    B.combine(cfg, Yp, token_row, w, offsets, y)
-    mean_prob = torch.empty(N, dtype=torch.float32, device=dev)
-    balance = torch.empty(1, dtype=torch.float32, device=dev)
-    dropped = torch.empty(1, dtype=torch.int32, device=dev)
-    cv2 = torch.empty(1, dtype=torch.float32, device=dev)
-    B.load_stats(cfg, pp, counts, kept, mean_prob, balance, dropped, cv2)
-    torch.cuda.synchronize()
-
-    out = B.Outputs(y, idx, w, counts, kept, dropped, mean_prob, balance, logits, cv2)
-    report, ref = check_layer(wl, cfg, t, out)
+    st = run_staged(cfg, t)
+    th = host_tensors(t)
+    L = oracle_layer(cfg, th)
+    report, ref = check_layer(wl, cfg, t, st["out"], th=th, L=L)
     assert ref.grouping.dropped > 0                   # the capacity bites
-    check_grouping(cfg, t["x"], offsets, row_token, token_row, Xp, ref.grouping, T)
-    # hidden rows of every group against the oracle's first Linear + GELU
-    off = offsets.cpu().numpy()
-    x64 = to64(t["x"])
-    for e in range(N + 1):
-        n_live = int(kept[e].item()) if e < N else T
-        if n_live == 0:
-            continue
-        r0 = int(off[e])
-        toks = row_token[r0: r0 + n_live].cpu().numpy() if e < N else np.arange(T)
-        W1 = to64(t["W1"][e] if e < N else t["W1s"])
-        b1 = to64(t["b1"][e] if e < N else t["b1s"])
-        h_ref = O.activation(x64[toks] @ W1.T + b1, wl.act)
-        h_gpu = H[r0: r0 + n_live].double().cpu().numpy()
-        err = np.linalg.norm(h_gpu - h_ref) / np.linalg.norm(h_ref)
-        assert err < 5e-3, (e, err)
+    check_grouping(cfg, t["x"], st["offsets"], st["row_token"], st["token_row"], st["Xp"],
+                   ref.grouping, wl.T)
+    rep = check_grouped_rows(cfg, L, ref.grouping, st["offsets"], st["H"], st["Yp"], seed=21,
+                             all_shared=True)
+    assert rep["grouped_rows_compared"] >= wl.T
 
 
 def test_edge_cases_tokens_0_and_1():
@@ -258,9 +264,8 @@ def test_workload_c2_switch_top1_capacity():
     t, layer, out = run_layer(wl)
     kept = out.kept.cpu().numpy()
     grp = O.group_by_expert(out.topk_idx.cpu().numpy(), wl.n_experts, 160)
-    dropped_tokens = np.nonzero(~grp.keep[:, 0])[0]
-    toks = sample_tokens(wl.T, 384, 2, must=dropped_tokens[:64].tolist())
-    report, ref = check_layer(wl, layer.cfg, t, out, tokens=toks)
+    assert (~grp.keep[:, 0]).sum() > 0
+    report, ref = check_layer(wl, layer.cfg, t, out)
     print("parity", wl.name, report, "dropped", ref.grouping.dropped)
     assert ref.grouping.dropped > 0 and kept.max() == 160
     assert report["fully_dropped_checked"] > 0
@@ -281,20 +286,64 @@ def test_workload_c3_mixtral_decode_full():
     print("parity", wl.name, report)
 
 
-def test_workload_c3_mixtral_prefill_sampled():
-    wl = WORKLOADS["c3_mixtral_prefill"]
-    t, layer, out = run_layer(wl)
-    report, _ = check_layer(wl, layer.cfg, t, out, tokens=sample_tokens(wl.T, 24, 4))
-    print("parity", wl.name, report)
+def tile_tokens(grouping, T, seed, shared=False, extra=0):
+    """One token at a random live row of every 128-row m-tile of every group
+    (and of the shared group), plus `extra` seeded tokens."""
+    rng = np.random.default_rng(seed)
+    toks = set()
+    for grp in grouping.groups:
+        for s0 in range(0, len(grp), 128):
+            toks.add(grp[int(rng.integers(s0, min(len(grp), s0 + 128)))][0])
+    if shared:
+        toks |= {int(rng.integers(s0, min(T, s0 + 128))) for s0 in range(0, T, 128)}
+    if extra:
+        toks |= set(rng.choice(T, size=min(extra, T), replace=False).tolist())
+    return np.array(sorted(toks | {0, T - 1}), dtype=np.int64)
 
 
-def test_workload_c4_deepseek_v3_sampled():
-    wl = WORKLOADS["c4_deepseek_v3"]
-    t, layer, out = run_layer(wl)
-    report, _ = check_layer(wl, layer.cfg, t, out, tokens=sample_tokens(wl.T, 10, 5))
+def check_large_layer(wl, seed, y_extra=0, y_tile_tokens=True):
+    """A large layer at full size: the staged calls (keeping H and Yp) and
+    moe_forward give the same results; the grouped rows are compared at every
+    m-tile of every group and every shared row; y on tokens that visit every
+    m-tile (plus a seeded sample)."""
+    t = synth.make_layer(wl, device="cuda")
+    cfg = B.make_config(wl)
+    st = run_staged(cfg, t)
+    layer = B.MoeLayer(wl, t)
+    out = layer.forward(t["x"], with_logits=True)
+    torch.cuda.synchronize()
+    # the same kernels on the same inputs: the same bits
+    for name in ("y", "topk_idx", "topk_w", "counts", "kept", "logits"):
+        assert torch.equal(getattr(out, name), getattr(st["out"], name)), name
+    th = host_tensors(t)
+    L = oracle_layer(cfg, th)
+    grp = O.group_by_expert(out.topk_idx.cpu().numpy(), cfg.n_experts, cfg.capacity)
+    if y_tile_tokens:
+        toks = tile_tokens(grp, wl.T, seed, shared=bool(cfg.d_ff_shared), extra=y_extra)
+    else:
+        toks = sample_tokens(wl.T, y_extra, seed)
+    report, ref = check_layer(wl, cfg, t, out, tokens=toks, th=th, L=L)
+    check_grouping(cfg, t["x"], st["offsets"], st["row_token"], st["token_row"], st["Xp"],
+                   ref.grouping, wl.T)
+    report.update(check_grouped_rows(cfg, L, ref.grouping, st["offsets"], st["H"], st["Yp"],
+                                     seed, all_shared=True))
     print("parity", wl.name, report)
-    del t, layer, out
+    del t, layer, out, st
     torch.cuda.empty_cache()
+    return report
+
+
+def test_workload_c3_mixtral_prefill_every_tile():
+    report = check_large_layer(WORKLOADS["c3_mixtral_prefill"], 4)
+    # 8 groups of ~1024 rows: ~8 m-tiles each, three rows per tile
+    assert report["grouped_rows_compared"] >= 8 * 8 * 2
+
+
+def test_workload_c4_deepseek_v3_every_tile():
+    wl = WORKLOADS["c4_deepseek_v3"]
+    report = check_large_layer(wl, 5, y_extra=64, y_tile_tokens=False)
+    # 256 groups of ~128 rows (one or two m-tiles each) and all 4096 shared rows
+    assert report["grouped_rows_compared"] >= 256 * 2 + wl.T
 
 
 def test_forward_profiled_and_graph_replay_match_forward():

@@ -4,13 +4,17 @@ allocation while it runs the layer, or a latency-bound loop that cannot
 afford the device-wide synchronisation of a cudaMalloc).  Its scratch is a
 fixed array inside the library, so the caller passes only inputs and outputs.
 
-Checked against moe_permute (caller-provided scratch) on two calls in a row
-with different layers, so stale contents of the shared array from the first
-call cannot leak into the second.  Integer and row-copy results: bit-exact.
-This file is collected last on purpose."""
+Checked against moe_permute (caller-provided scratch) and against the CPU
+oracle's grouping of the same top-k choice, on two calls in a row with
+different layers, so stale contents of the shared array from the first call
+cannot leak into the second.  Integer and row-copy results: bit-exact.  This
+file is collected last on purpose."""
 
+import numpy as np
 import pytest
 import torch
+
+from oracle import moe_oracle as O
 
 from sparse_mixture_experts_68_b300 import binding as B
 from sparse_mixture_experts_68_b300 import synth
@@ -55,6 +59,24 @@ def _same(ref, got, cfg):
     assert torch.equal(ref["Xp"][:end][live], got["Xp"][:end][live])
 
 
+def _matches_oracle(got, idx, cfg):
+    """counts, kept, group order and each assignment's row: the oracle's
+    grouping of the same top-k choice."""
+    g = O.group_by_expert(idx.cpu().numpy(), cfg.n_experts, cfg.capacity)
+    np.testing.assert_array_equal(got["counts"].cpu().numpy(), g.counts)
+    np.testing.assert_array_equal(got["kept"].cpu().numpy(), g.kept)
+    off = got["offsets"].cpu().numpy().astype(np.int64)
+    rt = got["row_token"].cpu().numpy()
+    tr = got["token_row"].cpu().numpy().reshape(cfg.T, cfg.top_k)
+    for e in range(cfg.n_experts):
+        assert off[e + 1] - off[e] == -(-int(g.kept[e]) // 128) * 128
+        toks = np.array([t for t, _ in g.groups[e]], dtype=np.int64)
+        np.testing.assert_array_equal(rt[off[e]: off[e] + len(toks)], toks)
+        for r, (t, j) in enumerate(g.groups[e]):
+            assert tr[t, j] == off[e] + r
+    assert np.all(tr[~g.keep] == -1)
+
+
 # The first layer is large enough that the permute step runs as several
 # blocks and uses the scratch array; the second is small enough for the
 # one-block sort.  Both calls go through moe_permute_noalloc.
@@ -84,6 +106,7 @@ def test_noalloc_permute_matches_permute_on_two_calls_in_a_row():
         torch.cuda.synchronize()
         _same(ref, got, cfg)
         assert int(ref["counts"].sum().item()) == wl.T * wl.top_k
+        _matches_oracle(got, idx, cfg)
     assert B.get_device_status() == B.MOE_OK
 
 
