@@ -384,6 +384,10 @@ def run_ours(args, wl, rank, world, local_rank, cpu_budget_s=None):
     layer = calls.layer
     x = tensors["x"]
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    # The inputs and buffers come from torch's current stream, the layer runs on
+    # its own stream: let every producer finish (torch may hand out memory that
+    # a still-running kernel of the current stream is writing) before the first call.
+    torch.cuda.synchronize(dev)
 
     # the layer as a CUDA graph of moe_forward (kernels overlap their
     # neighbours through programmatic dependent launch); per-kernel times come
@@ -563,6 +567,7 @@ def run_train(args, wl, rank, world, local_rank, cpu_budget_s=None):
     dy = torch.randn((wl.T, wl.d_model), generator=g).to(torch.bfloat16).to(dev)
     x = tensors["x"]
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    torch.cuda.synchronize(dev)          # see run_ours: the layer runs on its own stream
     stream = torch.cuda.Stream(dev)
     fev = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
     bev = [torch.cuda.Event(enable_timing=True) for _ in range(8)]

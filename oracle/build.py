@@ -20,6 +20,11 @@ LIB = os.path.join(HERE, "libmoe_oracle.so")
 
 
 def build(force: bool = False) -> str:
+    """Path of the oracle library, compiled if missing or older than its
+    sources.  MOE_ORACLE_LIB names a prebuilt one instead (for example an
+    AddressSanitizer build)."""
+    if os.environ.get("MOE_ORACLE_LIB"):
+        return os.environ["MOE_ORACLE_LIB"]
     newest = max(os.path.getmtime(SRC), os.path.getmtime(HDR))
     if not force and os.path.exists(LIB) and os.path.getmtime(LIB) > newest:
         return LIB

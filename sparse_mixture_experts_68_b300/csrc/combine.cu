@@ -37,9 +37,11 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
   // all slots read at once, so that the row loads below depend on one round trip
   int2* mine = live + (threadIdx.x >> 5) * (k + 1);
   int n_live = 0;
+  const int routed_end = offsets[N];             // rows past it are not routed rows
   for (int j0 = 0; j0 < k; j0 += 32) {
     const int j = j0 + lane;
-    const int r = j < k ? token_row[t * k + j] : -1;
+    int r = j < k ? token_row[t * k + j] : -1;
+    if (r >= routed_end) r = -1;
     const float g = j < k ? topk_w[t * k + j] : 0.f;
     const uint32_t m = __ballot_sync(0xffffffffu, r >= 0);
     if (r >= 0) mine[n_live + __popc(m & ((1u << lane) - 1u))] = make_int2(r, __float_as_int(g));

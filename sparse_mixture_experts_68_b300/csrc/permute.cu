@@ -357,7 +357,7 @@ __global__ void __launch_bounds__(256)
       t = r - routed_end;
       if (t >= Ttok) t = -1;
     }
-    if (t < 0) continue;                          // padding row
+    if (t < 0 || t >= Ttok) continue;             // padding row (or no such token)
     const uint4* src = reinterpret_cast<const uint4*>(x + t * d);
     uint4* dst = reinterpret_cast<uint4*>(Xp + r * d);
     const int64_t nv = d / V;

@@ -8,8 +8,9 @@ every intermediate in fp32: a few 1e-7 of rounding per value), applied
     dW2[e] and db2[e] (and the shared expert's), maximised over experts;
   * per token row: the relative L2 error of dx[t] and dz[t], maximised over
     tokens, with each row's norm floored at a thousandth of the median row
-    norm (a row whose every slot was dropped carries only the tiny balance
-    term);
+    norm for dx (a row whose every slot was dropped carries only the tiny
+    balance term) and at the median row norm for dz (a difference of gate
+    gradients that can cancel; see DZ_FLOOR);
   * dW_g, db_g and dw as whole tensors.
 The GPU stores five bf16 intermediates on the way (dO = w dy, the recomputed
 pre-activation, dA, dXp and the expert outputs behind dw), each rounded to 8
@@ -43,6 +44,11 @@ from parity import WORKERS, check_layer, check_routing, host_tensors, oracle_lay
 pytestmark = pytest.mark.gpu
 
 GRAD_TOL = {DT_BF16: 2e-2, DT_F32: 1e-4}
+# A token's score gradient is a difference of its gate gradients (for k = 2,
+# dz = w0 w1 (dw0 - dw1) on the two kept experts), which can cancel to almost
+# nothing while its rounding error stays at the gate gradients' scale: each
+# row's error is therefore measured against at least the median row norm.
+DZ_FLOOR = 1.0
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -67,14 +73,14 @@ def rel_l2(a, b):
     return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
 
 
-def row_max_rel(a, b):
-    """Max over rows of ||a_r - b_r|| / max(||b_r||, 1e-3 median_r ||b_r||)."""
+def row_max_rel(a, b, floor_frac=1e-3):
+    """Max over rows of ||a_r - b_r|| / max(||b_r||, floor_frac median_r ||b_r||)."""
     a = np.asarray(a, dtype=np.float64)
     b = np.asarray(b, dtype=np.float64)
     if a.shape[0] == 0:
         return 0.0
     nb = np.linalg.norm(b, axis=1)
-    floor = max(1e-3 * float(np.median(nb)), 1e-30)
+    floor = max(floor_frac * float(np.median(nb)), 1e-30)
     return float(np.max(np.linalg.norm(a - b, axis=1) / np.maximum(nb, floor)))
 
 
@@ -100,7 +106,7 @@ def check_backward(wl, layer, t, out, dy, aux, grads):
                 workers=WORKERS)
     ref = L.backward(r, dy.cpu(), aux, renormalize=bool(cfg.renormalize), workers=WORKERS)
     report = {"dx_row": row_max_rel(to64(grads.dx), ref.dx),
-              "dz_row": row_max_rel(to64(grads.dz), ref.dz),
+              "dz_row": row_max_rel(to64(grads.dz), ref.dz, DZ_FLOOR),
               "dw": rel_l2(to64(grads.dw), ref.dw),
               "dW_g": rel_l2(to64(grads.dW_g), ref.dW_g),
               "db_g": rel_l2(to64(grads.db_g), ref.db_g)}
@@ -338,7 +344,7 @@ def check_large_backward(wl, aux, tokens_per_group, seed):
     rdw, rdz, rdx = L.token_grads(r, dyh, aux, toks, bool(cfg.renormalize), WORKERS)
     report = {"tokens": len(toks),
               "dx_row": row_max_rel(to64(g.dx[torch.from_numpy(toks).cuda()]), rdx),
-              "dz_row": row_max_rel(to64(g.dz[torch.from_numpy(toks).cuda()]), rdz),
+              "dz_row": row_max_rel(to64(g.dz[torch.from_numpy(toks).cuda()]), rdz, DZ_FLOOR),
               "dw": rel_l2(to64(g.dw[torch.from_numpy(toks).cuda()]), rdw)}
 
     # every expert (and the shared one): sampled hidden units
