@@ -62,6 +62,9 @@ struct Workspace {
   void* Xp;
   void* H;
   void* Yp;
+  float* sk_partials;     // stream-K decode tiles (nullptr when the layer has none)
+  int32_t* sk_counters;
+  int64_t sk_counter_ints;
   size_t bytes;
 };
 
@@ -86,6 +89,12 @@ Workspace layout(const moe_config& c, void* base) {
   w.Xp = take(size_t(rows * c.d_model * es));
   w.H = take(size_t(rows * c.d_ff * es));
   w.Yp = take(size_t(rows * c.d_model * es));
+  const size_t skp = c.dtype == MOE_F32 ? 0 : swap_sk_partial_bytes(c);
+  if (skp > 0) {
+    w.sk_counter_ints = swap_sk_counter_ints(c, 1) + swap_sk_counter_ints(c, 2);
+    w.sk_partials = static_cast<float*>(take(skp));
+    w.sk_counters = static_cast<int32_t*>(take(size_t(w.sk_counter_ints) * 4));
+  }
   w.bytes = off;
   return w;
 }
@@ -404,7 +413,7 @@ moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk
   if (scratch_bytes < permute_scratch_bytes(*cfg)) return MOE_ERR_WORKSPACE;
   return cuda_status(launch_permute(*cfg, x, topk_idx, counts, kept, offsets, row_token,
                                     token_row, Xp, scratch, rows_max_of(*cfg),
-                                    static_cast<cudaStream_t>(stream), nullptr));
+                                    static_cast<cudaStream_t>(stream), nullptr, nullptr, 0));
 }
 
 moe_status moe_grouped_ffn(const moe_config* cfg, const void* Xp, const int32_t* offsets,
@@ -496,7 +505,7 @@ static moe_status forward_impl(const moe_config* cfg, const void* x, const moe_w
   if (e == cudaSuccess)
     e = launch_permute(c, x, out->topk_idx, out->counts, out->kept, ws.offsets, ws.row_token,
                        ws.token_row, ws.Xp, ws.scratch, rows_max_of(c), s,
-                       fused_stats ? &stats : nullptr);
+                       fused_stats ? &stats : nullptr, ws.sk_counters, ws.sk_counter_ints);
   if (e == cudaSuccess) e = record_event(ev[2], s);
   if (e == cudaSuccess) {
     GroupedFfnArgs a{};
@@ -505,6 +514,8 @@ static moe_status forward_impl(const moe_config* cfg, const void* x, const moe_w
     a.wait_limit_ns = g_wait_limit_ns.load(); a.num_sms = di.num_sms;
     a.mid_event = ev[3];
     a.pre_out = out->pre_act;
+    a.sk_partials = ws.sk_partials;
+    a.sk_counters = ws.sk_counters;
     e = c.dtype == MOE_F32 ? launch_grouped_ffn_f32(c, a, s) : launch_grouped_ffn_bf16(c, a, s);
   }
   if (e == cudaSuccess) e = record_event(ev[4], s);

@@ -99,6 +99,10 @@ struct TcParams {
   int32_t num_kb;                  // K / BK
   int32_t* status;
   uint64_t wait_limit_ns;
+  // decode tiles, stream-K (both nullptr: whole tiles): [kSkMaxCtas][2][NB][128]
+  // fp32 partial accumulators and one counter per tile, 0 at launch
+  float* sk_partials;
+  int32_t* sk_counters;
 };
 
 // Epilogue of CW accumulator columns of one row: + bias, activation, store.
@@ -852,13 +856,63 @@ struct LayoutS {
   static constexpr int kNumBars = 2 * STAGES + 5;
   static constexpr int kTmemSlot = kBar + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
-  static constexpr int kTileStart = (kAbort + 4 + 15) / 16 * 16;
+  static constexpr int kSkLast = kAbort + 4;             // stream-K: this CTA finishes the tile
+  static constexpr int kSkStop = kSkLast + 4;            // stream-K: an epilogue warp gave up
+  static constexpr int kTileStart = (kSkStop + 4 + 15) / 16 * 16;
   static constexpr int kGroupOff = kTileStart + (kMaxGroups + 1) * 4;
   static constexpr int kBytes = kGroupOff + kMaxGroups * 4;
   static constexpr int kAlloc = kBytes + 1024;
   static_assert(kXBytes % 1024 == 0, "token tiles must keep the 1 KB swizzle alignment");
   static_assert(kAlloc <= 227 * 1024, "shared memory budget");
 };
+
+// Stream-K over the decode tiles.  A layer's decode tiles are few and long
+// (for a Mixtral-sized decode, 256 tiles of 224 k-blocks in the second Linear),
+// so whole tiles per CTA leave the last wave of 148 CTAs partly idle.  Instead
+// every CTA takes an equal share of all tiles' k-blocks -- units
+// [b * upc, (b + 1) * upc) of total_tiles * num_kb -- so each streams the same
+// number of weight bytes.  A tile cut by share boundaries is summed by the last
+// of its CTAs to finish: each writes its fp32 partial accumulator (slot 0 when
+// the piece starts its share, else slot 1), counts itself on the tile's
+// counter, and the one that completes the count adds the pieces in k order
+// (deterministic) and runs the epilogue.
+constexpr int kSkMaxCtas = 256;
+
+struct SegIter {
+  int64_t u = 0, u1 = 0;
+  int t, stride, total, nkb;
+  bool sk;
+  __device__ SegIter(bool sk_, int b, int G, int total_, int nkb_, int64_t upc)
+      : t(b), stride(G), total(total_), nkb(nkb_), sk(sk_) {
+    if (sk) {
+      u = int64_t(b) * upc;
+      const int64_t U = int64_t(total_) * nkb_;
+      u1 = u + upc < U ? u + upc : U;
+    }
+  }
+  // the next (tile, [kb0, kb1)) of this CTA
+  __device__ bool next(int& tile, int& kb0, int& kb1) {
+    if (sk) {
+      if (u >= u1) return false;
+      tile = int(u / nkb);
+      kb0 = int(u - int64_t(tile) * nkb);
+      const int64_t rest = u1 - u;
+      kb1 = rest < int64_t(nkb - kb0) ? kb0 + int(rest) : nkb;
+      u += kb1 - kb0;
+      return true;
+    }
+    if (t >= total) return false;
+    tile = t;
+    kb0 = 0;
+    kb1 = nkb;
+    t += stride;
+    return true;
+  }
+};
+
+__device__ __forceinline__ void epi_bar_sync() {    // the four epilogue warps
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
 
 template <int NB>
 __host__ __device__ constexpr uint32_t idesc_swap_bf16_f32() {
@@ -905,6 +959,7 @@ __global__ void __launch_bounds__(6 * 32, 1)
     }
     mbar_init(done, 1);
     *abort_flag = 0;
+    *reinterpret_cast<volatile int*>(smem + L::kSkStop) = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
@@ -945,6 +1000,9 @@ __global__ void __launch_bounds__(6 * 32, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int total_tiles = tile_start[n_groups];
+  const bool sk = p.sk_counters != nullptr;
+  const int64_t units = int64_t(total_tiles) * p.num_kb;
+  const int64_t upc = sk ? (units + gridDim.x - 1) / gridDim.x : 0;   // units per CTA
 
   if (warp == 0) {
     if (lane == 0) {
@@ -953,11 +1011,13 @@ __global__ void __launch_bounds__(6 * 32, 1)
 #pragma unroll
       for (int s = 0; s < kStages; ++s) last_parity[s] = -1;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+      SegIter it(sk, blockIdx.x, gridDim.x, total_tiles, p.num_kb, upc);
+      int tile, kb0, kb1;
+      while (ok && it.next(tile, kb0, kb1)) {
         const TileCoord tc = decode_tile(tile, tile_start, n_groups, ntiles);
         const int r0 = grp_off[tc.g] + tc.m * NB;
         const int f0 = tc.n * kFeat;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_or_abort(&empty[stage], phase ^ 1u, p, abort_flag)) { ok = false; break; }
           const uint32_t fb = smem_u32(&full[stage]);
           mbar_arrive_expect_tx(&full[stage], L::kStageBytes);
@@ -987,11 +1047,13 @@ __global__ void __launch_bounds__(6 * 32, 1)
       constexpr uint32_t idesc = idesc_swap_bf16_f32<NB>();
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+      SegIter it(sk, blockIdx.x, gridDim.x, total_tiles, p.num_kb, upc);
+      int tile, kb0, kb1;
+      while (ok && it.next(tile, kb0, kb1)) {
         if (!wait_or_abort(&tempty[acc], acc_phase ^ 1u, p, abort_flag)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * NB;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_or_abort(&full[stage], phase, p, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const uint64_t wd = sdesc_sw128(smem_u32(smem + L::kW + stage * L::kWBytes));
@@ -999,7 +1061,7 @@ __global__ void __launch_bounds__(6 * 32, 1)
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
             tc_mma(d_tmem, wd + uint64_t(2 * kk), xd + uint64_t(2 * kk), idesc,
-                   (kb | kk) != 0 ? 1u : 0u);
+                   (kb != kb0 || kk != 0) ? 1u : 0u);
           tc_commit(smem_u32(&empty[stage]));
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
@@ -1016,17 +1078,31 @@ __global__ void __launch_bounds__(6 * 32, 1)
   } else {
     // epilogue: warps 2-5, one TMEM lane quarter each; thread = one feature
     const int q = warp & 3;
+    const int fl = q * 32 + lane;                  // feature within the tile
+    volatile int* sk_last = reinterpret_cast<volatile int*>(smem + L::kSkLast);
+    volatile int* sk_stop = reinterpret_cast<volatile int*>(smem + L::kSkStop);
+    const int64_t my_u0 = int64_t(blockIdx.x) * upc;
     uint32_t acc = 0, acc_phase = 0;
-    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+    SegIter it(sk, blockIdx.x, gridDim.x, total_tiles, p.num_kb, upc);
+    int tile, kb0, kb1;
+    while (it.next(tile, kb0, kb1)) {
       const TileCoord tc = decode_tile(tile, tile_start, n_groups, ntiles);
       bool ok = true;
       if (lane == 0) ok = wait_or_abort(&tfull[acc], acc_phase, p, abort_flag);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (sk) {
+        // stream-K synchronises the four epilogue warps below: they stop
+        // together, whichever of them gave up waiting
+        if (!ok && lane == 0) *sk_stop = 1;
+        epi_bar_sync();
+        ok = *sk_stop == 0;
+        epi_bar_sync();                      // every warp has read the flag
+      }
       if (!ok) break;
       tc_fence_after();
       const bool routed = tc.g < p.n_routed;
       const int live = routed ? p.kept[tc.g] : p.shared_rows;
-      const int feat = tc.n * kFeat + q * 32 + lane;
+      const int feat = tc.n * kFeat + fl;
       const __nv_bfloat16* bias = routed ? p.bias + int64_t(tc.g) * p.Nd : p.bias_s;
       const float b = __bfloat162float(bias[feat]);
       uint32_t r[NB];
@@ -1034,19 +1110,53 @@ __global__ void __launch_bounds__(6 * 32, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);     // accumulator is in registers now
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+      float v[NB];
+#pragma unroll
+      for (int i = 0; i < NB; ++i) v[i] = __uint_as_float(r[i]);
+      if (kb0 != 0 || kb1 != p.num_kb) {
+        // a piece of a tile: publish it; the last of the tile's CTAs sums them
+        const int64_t t0 = int64_t(tile) * p.num_kb;
+        const int c_first = int(t0 / upc), c_last = int((t0 + p.num_kb - 1) / upc);
+        const int slot = t0 + kb0 == my_u0 ? 0 : 1;
+        float* mine = p.sk_partials + (int64_t(blockIdx.x) * 2 + slot) * (NB * kFeat);
+#pragma unroll
+        for (int i = 0; i < NB; ++i) __stcg(mine + i * kFeat + fl, v[i]);
+        __threadfence();
+        epi_bar_sync();
+        if (warp == 2 && lane == 0) {
+          const int done_before = atomicAdd(p.sk_counters + tile, 1);
+          const int last = done_before == c_last - c_first;
+          if (last) p.sk_counters[tile] = 0;           // ready for the next call
+          *sk_last = last;
+        }
+        epi_bar_sync();
+        const bool last = *sk_last != 0;
+        epi_bar_sync();                                // the flag is read before reuse
+        if (!last) continue;
+        __threadfence();
+#pragma unroll
+        for (int i = 0; i < NB; ++i) v[i] = 0.f;
+        for (int c = c_first; c <= c_last; ++c) {      // the pieces in k order
+          const int64_t cu0 = int64_t(c) * upc;
+          const float* part = p.sk_partials +
+                              (int64_t(c) * 2 + (t0 > cu0 ? 1 : 0)) * (NB * kFeat);
+#pragma unroll
+          for (int i = 0; i < NB; ++i) v[i] += __ldcg(part + i * kFeat + fl);
+        }
+      }
       __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
 #pragma unroll
       for (int i = 0; i < NB; ++i) {
         const int row_in_group = tc.m * NB + i;
         if (row_in_group < live) {
-          float v = __uint_as_float(r[i]) + b;
-          if (EPI == EPI_BIAS_GELU) v = gelu_erf(v);
-          if (EPI == EPI_BIAS_RELU) v = fmaxf(v, 0.f);
-          out[(int64_t(grp_off[tc.g]) + row_in_group) * p.Nd + feat] = __float2bfloat16_rn(v);
+          float o = v[i] + b;
+          if (EPI == EPI_BIAS_GELU) o = gelu_erf(o);
+          if (EPI == EPI_BIAS_RELU) o = fmaxf(o, 0.f);
+          out[(int64_t(grp_off[tc.g]) + row_in_group) * p.Nd + feat] = __float2bfloat16_rn(o);
         }
       }
-      acc ^= 1u;
-      if (acc == 0) acc_phase ^= 1u;
     }
   }
 
@@ -1217,10 +1327,13 @@ int swap_rows(int64_t Nd, int64_t rows_per_group, int epi) {
 // One grouped Linear: out[group g] = epi(A[group g] . W[g]^T + bias[g]).
 // out_pre: with an activation epilogue, also store the pre-activation there
 // (only on the staged tile families; see linear_saves_pre).
+// sk_counters: the decode tiles run stream-K with these counters (all 0) and
+// g.sk_partials; nullptr: whole tiles per CTA.
 cudaError_t grouped_linear(const moe_config& c, const GroupedFfnArgs& g, const void* A,
                            const void* W, const void* Ws, const void* bias,
                            const void* bias_s, void* out, int64_t K, int64_t Nd, int epi,
-                           cudaStream_t s, void* out_pre = nullptr) {
+                           cudaStream_t s, void* out_pre = nullptr,
+                           int32_t* sk_counters = nullptr) {
   const int64_t groups = c.n_experts + (c.d_ff_shared > 0 ? 1 : 0);
   const int64_t routed = g.routed_rows > 0 ? g.routed_rows : c.T * c.top_k;
   const int64_t rows = routed + (c.d_ff_shared > 0 ? c.T : 0);
@@ -1250,7 +1363,13 @@ cudaError_t grouped_linear(const moe_config& c, const GroupedFfnArgs& g, const v
     p.status = g.status;
     p.wait_limit_ns = g.wait_limit_ns;
     const int64_t max_tiles = (ceil_div(rows, nb) + groups) * (Nd / 128);
-    const int grid = int(max_tiles < g.num_sms ? max_tiles : g.num_sms);
+    int grid = int(max_tiles < g.num_sms ? max_tiles : g.num_sms);
+    if (sk_counters && g.sk_partials) {
+      // stream-K: every CTA takes an equal share of the k-blocks
+      p.sk_partials = g.sk_partials;
+      p.sk_counters = sk_counters;
+      grid = g.num_sms < kSkMaxCtas ? g.num_sms : kSkMaxCtas;
+    }
     return nb == 16 ? launch_swap<16>(epi, mW, mWs, mX, p, grid, s)
                     : launch_swap<32>(epi, mW, mWs, mX, p, grid, s);
   }
@@ -1350,6 +1469,23 @@ bool linear_saves_pre(const moe_config& c) {
          pick_tile(c.d_ff, rows / groups, c.d_model) != TILE_128_2CTA;
 }
 
+int64_t swap_sk_counter_ints(const moe_config& c, int linear) {
+  if (c.dtype == MOE_F32) return 0;
+  const int64_t Nd = linear == 1 ? c.d_ff : c.d_model;
+  const int epi = linear == 2 ? EPI_BIAS
+                              : (c.act == MOE_ACT_RELU ? EPI_BIAS_RELU : EPI_BIAS_GELU);
+  const int64_t groups = c.n_experts + (c.d_ff_shared > 0 ? 1 : 0);
+  const int64_t rows = c.T * c.top_k + (c.d_ff_shared > 0 ? c.T : 0);
+  const int nb = swap_rows(Nd, rows / groups, epi);
+  if (nb == 0) return 0;
+  return (ceil_div(rows, nb) + groups) * (Nd / 128);     // the tile bound of grouped_linear
+}
+
+size_t swap_sk_partial_bytes(const moe_config& c) {
+  if (swap_sk_counter_ints(c, 1) == 0 && swap_sk_counter_ints(c, 2) == 0) return 0;
+  return size_t(kSkMaxCtas) * 2 * 32 * 128 * sizeof(float);   // NB <= 32
+}
+
 cudaError_t launch_grouped_ffn_bf16(const moe_config& c, const GroupedFfnArgs& g,
                                     cudaStream_t s) {
   if (g.rows_max == 0) return cudaSuccess;
@@ -1357,15 +1493,23 @@ cudaError_t launch_grouped_ffn_bf16(const moe_config& c, const GroupedFfnArgs& g
   // the pre-activation for a later backward: from the epilogue, or else by a
   // second pass of the first Linear without its activation
   const bool in_epi = g.pre_out && linear_saves_pre(c);
+  int32_t* sk1 = nullptr;
+  int32_t* sk2 = nullptr;
+  if (g.sk_counters && g.sk_partials) {
+    const int64_t n1 = swap_sk_counter_ints(c, 1);
+    if (n1 > 0) sk1 = g.sk_counters;
+    if (swap_sk_counter_ints(c, 2) > 0) sk2 = g.sk_counters + n1;
+  }
   cudaError_t e = grouped_linear(c, g, g.Xp, g.w->W1, g.w->W1s, g.w->b1, g.w->b1s, g.H,
-                                 c.d_model, c.d_ff, epi1, s, in_epi ? g.pre_out : nullptr);
+                                 c.d_model, c.d_ff, epi1, s, in_epi ? g.pre_out : nullptr,
+                                 sk1);
   if (e == cudaSuccess && g.pre_out && !in_epi)
     e = grouped_linear(c, g, g.Xp, g.w->W1, g.w->W1s, g.w->b1, g.w->b1s, g.pre_out, c.d_model,
                        c.d_ff, EPI_BIAS, s);
   if (e == cudaSuccess) e = record_event(g.mid_event, s);
   if (e != cudaSuccess) return e;
   return grouped_linear(c, g, g.H, g.w->W2, g.w->W2s, g.w->b2, g.w->b2s, g.Yp, c.d_ff,
-                        c.d_model, EPI_BIAS, s);
+                        c.d_model, EPI_BIAS, s, nullptr, sk2);
 }
 
 // Name of the kernel (and tile) one grouped Linear of moe_forward launches,

@@ -82,10 +82,13 @@ struct StatsArgs {
 size_t permute_scratch_bytes(const moe_config& c);
 // true when launch_permute can also produce the load statistics
 bool permute_fuses_stats(const moe_config& c);
+// zero / n_zero: int32 counters the row copy sets to 0 for the kernels after it
+// (nullptr / 0: none)
 cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* topk_idx,
                            int32_t* counts, int32_t* kept, int32_t* offsets,
                            int32_t* row_token, int32_t* token_row, void* Xp, void* scratch,
-                           int64_t rows_max, cudaStream_t s, const StatsArgs* stats);
+                           int64_t rows_max, cudaStream_t s, const StatsArgs* stats,
+                           int32_t* zero, int64_t n_zero);
 
 // ---- expert-choice routing (router.cu, expert_choice.cu) -------------------------
 
@@ -134,7 +137,17 @@ struct GroupedFfnArgs {
   int64_t routed_rows;      // live routed rows for the tile heuristics; 0: T * top_k
   void* pre_out;            // [rows_max, d_ff]: also keep the first Linear's
                             // pre-activation (for the backward), or nullptr
+  // stream-K scratch of the decode tiles (both nullptr: whole tiles per CTA):
+  // per-CTA fp32 partial accumulators, and per-tile counters that start at 0
+  // (swap_sk_counter_ints(c, 1) for Linear 1, then those of Linear 2)
+  float* sk_partials;
+  int32_t* sk_counters;
 };
+// Stream-K bookkeeping of moe_forward's decode tiles: counters of grouped
+// Linear 1 or 2 (0 when that Linear does not run the decode tiles), and the
+// partial-accumulator bytes (0 when neither does).
+int64_t swap_sk_counter_ints(const moe_config& c, int linear);
+size_t swap_sk_partial_bytes(const moe_config& c);
 // whether the bf16 first Linear stores its pre-activation from its epilogue
 // (else a second pass does)
 bool linear_saves_pre(const moe_config& c);

@@ -341,9 +341,14 @@ template <typename T>
 __global__ void __launch_bounds__(256)
     permute_copy_kernel(const T* __restrict__ x, int64_t d, int Ttok, int N,
                         const int32_t* __restrict__ offsets,
-                        const int32_t* __restrict__ row_token, T* __restrict__ Xp) {
+                        const int32_t* __restrict__ row_token, T* __restrict__ Xp,
+                        int32_t* __restrict__ zero, int64_t n_zero) {
   pdl_launch_dependents();
   pdl_wait_previous();
+  // counters the next kernels count up from zero (the grouped FFN's split tiles)
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n_zero;
+       i += int64_t(gridDim.x) * blockDim.x)
+    zero[i] = 0;
   const int lane = threadIdx.x & 31;
   const int64_t routed_end = offsets[N], total = offsets[N + 1];
   const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
@@ -383,18 +388,20 @@ size_t permute_scratch_bytes(const moe_config& c) {
 namespace {
 
 cudaError_t launch_copy(const moe_config& c, const void* x, const int32_t* offsets,
-                        const int32_t* row_token, void* Xp, int64_t rows_max, cudaStream_t s) {
+                        const int32_t* row_token, void* Xp, int64_t rows_max, cudaStream_t s,
+                        int32_t* zero = nullptr, int64_t n_zero = 0) {
   if (rows_max <= 0) return cudaSuccess;
   const int N = int(c.n_experts), T = int(c.T);
   const int64_t want = ceil_div(rows_max, 8);
   const unsigned blocks = unsigned(want < 148 * 8 ? want : 148 * 8);
+  if (!zero) n_zero = 0;
   if (c.dtype == MOE_F32)
     return launch_pdl(permute_copy_kernel<float>, dim3(blocks), dim3(256), 0, s,
                       static_cast<const float*>(x), c.d_model, T, N, offsets, row_token,
-                      static_cast<float*>(Xp));
+                      static_cast<float*>(Xp), zero, n_zero);
   return launch_pdl(permute_copy_kernel<__nv_bfloat16>, dim3(blocks), dim3(256), 0, s,
                     static_cast<const __nv_bfloat16*>(x), c.d_model, T, N, offsets,
-                    row_token, static_cast<__nv_bfloat16*>(Xp));
+                    row_token, static_cast<__nv_bfloat16*>(Xp), zero, n_zero);
 }
 
 }  // namespace
@@ -416,7 +423,8 @@ bool permute_fuses_stats(const moe_config& c) { return single_block_sort_fits(c)
 cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* topk_idx,
                            int32_t* counts, int32_t* kept, int32_t* offsets,
                            int32_t* row_token, int32_t* token_row, void* Xp, void* scratch,
-                           int64_t rows_max, cudaStream_t s, const StatsArgs* stats) {
+                           int64_t rows_max, cudaStream_t s, const StatsArgs* stats,
+                           int32_t* zero, int64_t n_zero) {
   const int N = int(c.n_experts), k = int(c.top_k), T = int(c.T);
   const int nblk = int(permute_blocks(c));
   PermuteScratch p = carve(c, scratch);
@@ -431,7 +439,7 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* to
                    N, c.capacity, c.d_ff_shared > 0 ? 1 : 0, counts, kept, offsets, row_token,
                    token_row, stats ? *stats : none);
     if (e != cudaSuccess) return e;
-    return launch_copy(c, x, offsets, row_token, Xp, rows_max, s);
+    return launch_copy(c, x, offsets, row_token, Xp, rows_max, s, zero, n_zero);
   }
   if (nblk > 0) {
     e = launch_pdl(permute_hist_kernel, dim3(nblk), dim3(256), smemN, s, topk_idx, T, k, N,
@@ -447,7 +455,7 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* to
                    c.capacity, p.block_base, offsets, row_token, token_row);
     if (e != cudaSuccess) return e;
   }
-  return launch_copy(c, x, offsets, row_token, Xp, rows_max, s);
+  return launch_copy(c, x, offsets, row_token, Xp, rows_max, s, zero, n_zero);
 }
 
 }  // namespace moe
@@ -510,6 +518,6 @@ extern "C" moe_status moe_permute_noalloc(const moe_config* cfg, const void* x,
   if (static_scratch_address(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
   const cudaError_t e = launch_permute(*cfg, x, topk_idx, counts, kept, offsets, row_token,
                                        token_row, Xp, scratch, rows_max_for(*cfg),
-                                       static_cast<cudaStream_t>(stream), nullptr);
+                                       static_cast<cudaStream_t>(stream), nullptr, nullptr, 0);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

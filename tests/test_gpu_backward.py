@@ -118,6 +118,15 @@ def check_backward(wl, layer, t, out, dy, aux, grads):
         for name, rr in zip(("dW1s", "db1s", "dW2s", "db2s"), ref.shared):
             report[name] = rel_l2(to64(getattr(grads, name)), rr)
     bad = {n: v for n, v in report.items() if not v <= GRAD_TOL[wl.dtype]}
+    if "dz_row" in bad:
+        gz, rz = to64(grads.dz), ref.dz
+        nb = np.linalg.norm(rz, axis=1)
+        err = np.linalg.norm(gz - rz, axis=1) / np.maximum(nb, DZ_FLOOR * np.median(nb))
+        for t in np.argsort(-err)[:4]:
+            print("dz row", int(t), "err", err[t], "idx", r.idx[t], "keep", r.keep[t], "w", r.w[t],
+                  "dw gpu", to64(grads.dw)[t], "dw ref", ref.dw[t], "dz gpu", gz[t][r.idx[t]],
+                  "dz ref", rz[t][r.idx[t]], "|dz| gpu", np.linalg.norm(gz[t]), "ref", nb[t],
+                  "median", np.median(nb))
     assert not bad, f"gradients off: {bad} (all: {report})"
     # dropped slots pass no gradient to their gate; an expert with no rows
     # gets exact zeros
