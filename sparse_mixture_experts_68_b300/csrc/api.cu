@@ -89,9 +89,9 @@ Workspace layout(const moe_config& c, void* base) {
   w.Xp = take(size_t(rows * c.d_model * es));
   w.H = take(size_t(rows * c.d_ff * es));
   w.Yp = take(size_t(rows * c.d_model * es));
-  const size_t skp = c.dtype == MOE_F32 ? 0 : swap_sk_partial_bytes(c);
+  const size_t skp = sk_partial_bytes(c);
   if (skp > 0) {
-    w.sk_counter_ints = swap_sk_counter_ints(c, 1) + swap_sk_counter_ints(c, 2);
+    w.sk_counter_ints = sk_counter_ints(c, 1) + sk_counter_ints(c, 2);
     w.sk_partials = static_cast<float*>(take(skp));
     w.sk_counters = static_cast<int32_t*>(take(size_t(w.sk_counter_ints) * 4));
   }

@@ -73,7 +73,9 @@ struct Layout {
   static constexpr int kNumBars = 2 * STAGES + 5;
   static constexpr int kTmemSlot = kBar + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
-  static constexpr int kTileStart = (kAbort + 4 + 15) / 16 * 16;   // int32 [kMaxGroups + 1]
+  static constexpr int kSkLast = kAbort + 4;                // stream-K: finish this tile
+  static constexpr int kSkStop = kSkLast + 4;               // stream-K: an epilogue warp gave up
+  static constexpr int kTileStart = (kSkStop + 4 + 15) / 16 * 16;   // int32 [kMaxGroups + 1]
   static constexpr int kGroupOff = kTileStart + (kMaxGroups + 1) * 4;  // int32 [kMaxGroups]
   static constexpr int kStage = (kGroupOff + kMaxGroups * 4 + 127) / 128 * 128;
   static constexpr int kBytes = kStage + STAGE_BYTES;
@@ -103,6 +105,9 @@ struct TcParams {
   // fp32 partial accumulators and one counter per tile, 0 at launch
   float* sk_partials;
   int32_t* sk_counters;
+  // decode tiles: weight k-blocks each CTA prefetches into L2 before the
+  // previous kernels (the routing) have finished; 0: none
+  int32_t prefetch_kb;
 };
 
 // Epilogue of CW accumulator columns of one row: + bias, activation, store.
@@ -247,6 +252,56 @@ __device__ __forceinline__ TileCoord decode_tile(int tile, const int32_t* tile_s
   return TileCoord{lo, local % mt, local / mt};
 }
 
+// Stream-K.  When a layer has few output tiles for the SM count (the
+// Mixtral-sized decode: 256 tiles of 224 k-blocks in its second Linear; the
+// page-1 layer: 96 to 400 tiles of 12 to 48 k-blocks), whole tiles per CTA
+// leave the last wave of 148 CTAs partly idle.  Instead
+// every CTA takes an equal share of all tiles' k-blocks -- units
+// [b * upc, (b + 1) * upc) of total_tiles * num_kb -- so each streams the same
+// number of weight bytes.  A tile cut by share boundaries is summed by the last
+// of its CTAs to finish: each writes its fp32 partial accumulator (slot 0 when
+// the piece starts its share, else slot 1), counts itself on the tile's
+// counter, and the one that completes the count adds the pieces in k order
+// (deterministic) and runs the epilogue.
+constexpr int kSkMaxCtas = 256;
+
+struct SegIter {
+  int64_t u = 0, u1 = 0;
+  int t, stride, total, nkb;
+  bool sk;
+  __device__ SegIter(bool sk_, int b, int G, int total_, int nkb_, int64_t upc)
+      : t(b), stride(G), total(total_), nkb(nkb_), sk(sk_) {
+    if (sk) {
+      u = int64_t(b) * upc;
+      const int64_t U = int64_t(total_) * nkb_;
+      u1 = u + upc < U ? u + upc : U;
+    }
+  }
+  // the next (tile, [kb0, kb1)) of this CTA
+  __device__ bool next(int& tile, int& kb0, int& kb1) {
+    if (sk) {
+      if (u >= u1) return false;
+      tile = int(u / nkb);
+      kb0 = int(u - int64_t(tile) * nkb);
+      const int64_t rest = u1 - u;
+      kb1 = rest < int64_t(nkb - kb0) ? kb0 + int(rest) : nkb;
+      u += kb1 - kb0;
+      return true;
+    }
+    if (t >= total) return false;
+    tile = t;
+    kb0 = 0;
+    kb1 = nkb;
+    t += stride;
+    return true;
+  }
+};
+
+// Barrier of the epilogue warps only (named barrier 1).
+__device__ __forceinline__ void epi_bar_sync(int threads = 128) {
+  asm volatile("bar.sync 1, %0;" ::"r"(threads) : "memory");
+}
+
 template <class CFG, int EPI, int MINB>
 __global__ void __launch_bounds__(CFG::THREADS, MINB)
     tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -285,6 +340,7 @@ __global__ void __launch_bounds__(CFG::THREADS, MINB)
     }
     mbar_init(done, 1);
     *abort_flag = 0;
+    *reinterpret_cast<volatile int*>(smem + L::kSkStop) = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
@@ -330,6 +386,9 @@ __global__ void __launch_bounds__(CFG::THREADS, MINB)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int total_tiles = tile_start[n_groups];
+  const bool sk = p.sk_counters != nullptr;
+  const int64_t units = int64_t(total_tiles) * p.num_kb;
+  const int64_t upc = sk ? (units + gridDim.x - 1) / gridDim.x : 0;   // units per CTA
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -339,10 +398,12 @@ __global__ void __launch_bounds__(CFG::THREADS, MINB)
 #pragma unroll
       for (int s = 0; s < kStages; ++s) last_parity[s] = -1;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+      SegIter it(sk, blockIdx.x, gridDim.x, total_tiles, p.num_kb, upc);
+      int tile, kb0, kb1;
+      while (ok && it.next(tile, kb0, kb1)) {
         const TileCoord tc = decode_tile(tile, tile_start, n_groups, ntiles);
         const int row0 = grp_off[tc.g] + tc.m * BM;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_or_abort(&empty[stage], phase ^ 1u, p, abort_flag)) { ok = false; break; }
           const uint32_t fb = smem_u32(&full[stage]);
           mbar_arrive_expect_tx(&full[stage], L::kStageBytes);
@@ -375,11 +436,13 @@ __global__ void __launch_bounds__(CFG::THREADS, MINB)
       constexpr uint32_t idesc = idesc_bf16_f32<BN>();
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+      SegIter it(sk, blockIdx.x, gridDim.x, total_tiles, p.num_kb, upc);
+      int tile, kb0, kb1;
+      while (ok && it.next(tile, kb0, kb1)) {
         if (!wait_or_abort(&tempty[acc], acc_phase ^ 1u, p, abort_flag)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_or_abort(&full[stage], phase, p, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const uint64_t ad = sdesc_sw128(smem_u32(smem + L::kA + stage * L::kABytes));
@@ -387,7 +450,7 @@ __global__ void __launch_bounds__(CFG::THREADS, MINB)
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)   // +32 bytes along K per step
             tc_mma(d_tmem, ad + uint64_t(2 * kk), bd + uint64_t(2 * kk), idesc,
-                   (kb | kk) != 0 ? 1u : 0u);
+                   (kb != kb0 || kk != 0) ? 1u : 0u);
           tc_commit(smem_u32(&empty[stage]));
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
@@ -408,12 +471,26 @@ __global__ void __launch_bounds__(CFG::THREADS, MINB)
     const int part = (warp - 2) >> 2;            // which share of the tile's columns
     constexpr int kCols = BN / (kEpiWarps / 4);
     constexpr int CW = kCols < 32 ? kCols : 32;  // columns per tcgen05.ld
+    constexpr int kEpiThreads = kEpiWarps * 32;
+    volatile int* sk_last = reinterpret_cast<volatile int*>(smem + L::kSkLast);
+    volatile int* sk_stop = reinterpret_cast<volatile int*>(smem + L::kSkStop);
+    const int64_t my_u0 = int64_t(blockIdx.x) * upc;
     uint32_t acc = 0, acc_phase = 0;
-    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+    SegIter it(sk, blockIdx.x, gridDim.x, total_tiles, p.num_kb, upc);
+    int tile, kb0, kb1;
+    while (it.next(tile, kb0, kb1)) {
       const TileCoord tc = decode_tile(tile, tile_start, n_groups, ntiles);
       bool ok = true;
       if (lane == 0) ok = wait_or_abort(&tfull[acc], acc_phase, p, abort_flag);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (sk) {
+        // the epilogue warps synchronise below: they stop together, whichever
+        // of them gave up waiting
+        if (!ok && lane == 0) *sk_stop = 1;
+        epi_bar_sync(kEpiThreads);
+        ok = *sk_stop == 0;
+        epi_bar_sync(kEpiThreads);               // every warp has read the flag
+      }
       if (!ok) break;
       tc_fence_after();
       const bool routed = tc.g < p.n_routed;
@@ -424,10 +501,8 @@ __global__ void __launch_bounds__(CFG::THREADS, MINB)
       const __nv_bfloat16* bias = routed ? p.bias + int64_t(tc.g) * p.Nd : p.bias_s;
       constexpr int kOutBytes = EPI == EPI_BIAS_F32 ? 4 : 2;
       constexpr bool kStaged = CFG::STAGED && EPI != EPI_BIAS_F32;
-#pragma unroll 1
-      for (int c = part * kCols; c < (part + 1) * kCols; c += CW) {
-        uint32_t r[CW];
-        tmem_ld_cols<CW>(tmem_base + (uint32_t(q * 32) << 16) + acc * BN + c, r);
+      // + bias, activation and store of the CW accumulator columns at c
+      auto store_chunk = [&](int c, const uint32_t (&r)[CW]) {
         const int64_t col = int64_t(tc.n) * BN + c;
         if constexpr (kStaged) {
           uint8_t* stg = smem + L::kStage + (warp - 2) * staged_warp_bytes<16>();
@@ -452,10 +527,75 @@ __global__ void __launch_bounds__(CFG::THREADS, MINB)
                                   static_cast<uint8_t*>(p.out) +
                                       (out_row * p.Nd + col) * kOutBytes);
         }
+      };
+      if (kb0 == 0 && kb1 == p.num_kb) {          // a whole tile
+#pragma unroll 1
+        for (int c = part * kCols; c < (part + 1) * kCols; c += CW) {
+          uint32_t r[CW];
+          tmem_ld_cols<CW>(tmem_base + (uint32_t(q * 32) << 16) + acc * BN + c, r);
+          store_chunk(c, r);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+      } else {
+        // a piece of a tile: publish it; the last of the tile's CTAs sums the
+        // pieces in k order and runs the epilogue
+        const int64_t t0 = int64_t(tile) * p.num_kb;
+        const int c_first = int(t0 / upc), c_last = int((t0 + p.num_kb - 1) / upc);
+        const int slot = t0 + kb0 == my_u0 ? 0 : 1;
+        const int row = q * 32 + lane;
+        float* mine = p.sk_partials + (int64_t(blockIdx.x) * 2 + slot) * (BM * BN) +
+                      int64_t(row) * BN;
+#pragma unroll 1
+        for (int c = part * kCols; c < (part + 1) * kCols; c += CW) {
+          uint32_t r[CW];
+          tmem_ld_cols<CW>(tmem_base + (uint32_t(q * 32) << 16) + acc * BN + c, r);
+#pragma unroll
+          for (int i = 0; i < CW; i += 4)
+            __stcg(reinterpret_cast<float4*>(mine + c + i),
+                   make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]),
+                               __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3])));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+        __threadfence();
+        epi_bar_sync(kEpiThreads);
+        if (warp == 2 && lane == 0) {
+          const int done_before = atomicAdd(p.sk_counters + tile, 1);
+          const int last = done_before == c_last - c_first;
+          if (last) p.sk_counters[tile] = 0;      // ready for the next call
+          *sk_last = last;
+        }
+        epi_bar_sync(kEpiThreads);
+        const bool last = *sk_last != 0;
+        epi_bar_sync(kEpiThreads);                // the flag is read before reuse
+        if (last) {
+          __threadfence();
+#pragma unroll 1
+          for (int c = part * kCols; c < (part + 1) * kCols; c += CW) {
+            float sum[CW];
+#pragma unroll
+            for (int i = 0; i < CW; ++i) sum[i] = 0.f;
+            for (int cc = c_first; cc <= c_last; ++cc) {   // the pieces in k order
+              const int64_t cu0 = int64_t(cc) * upc;
+              const float* piece = p.sk_partials +
+                                   (int64_t(cc) * 2 + (t0 > cu0 ? 1 : 0)) * (BM * BN) +
+                                   int64_t(row) * BN + c;
+#pragma unroll
+              for (int i = 0; i < CW; i += 4) {
+                const float4 v = __ldcg(reinterpret_cast<const float4*>(piece + i));
+                sum[i] += v.x; sum[i + 1] += v.y; sum[i + 2] += v.z; sum[i + 3] += v.w;
+              }
+            }
+            uint32_t r[CW];
+#pragma unroll
+            for (int i = 0; i < CW; ++i) r[i] = __float_as_uint(sum[i]);
+            store_chunk(c, r);
+          }
+        }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
@@ -866,54 +1006,6 @@ struct LayoutS {
   static_assert(kAlloc <= 227 * 1024, "shared memory budget");
 };
 
-// Stream-K over the decode tiles.  A layer's decode tiles are few and long
-// (for a Mixtral-sized decode, 256 tiles of 224 k-blocks in the second Linear),
-// so whole tiles per CTA leave the last wave of 148 CTAs partly idle.  Instead
-// every CTA takes an equal share of all tiles' k-blocks -- units
-// [b * upc, (b + 1) * upc) of total_tiles * num_kb -- so each streams the same
-// number of weight bytes.  A tile cut by share boundaries is summed by the last
-// of its CTAs to finish: each writes its fp32 partial accumulator (slot 0 when
-// the piece starts its share, else slot 1), counts itself on the tile's
-// counter, and the one that completes the count adds the pieces in k order
-// (deterministic) and runs the epilogue.
-constexpr int kSkMaxCtas = 256;
-
-struct SegIter {
-  int64_t u = 0, u1 = 0;
-  int t, stride, total, nkb;
-  bool sk;
-  __device__ SegIter(bool sk_, int b, int G, int total_, int nkb_, int64_t upc)
-      : t(b), stride(G), total(total_), nkb(nkb_), sk(sk_) {
-    if (sk) {
-      u = int64_t(b) * upc;
-      const int64_t U = int64_t(total_) * nkb_;
-      u1 = u + upc < U ? u + upc : U;
-    }
-  }
-  // the next (tile, [kb0, kb1)) of this CTA
-  __device__ bool next(int& tile, int& kb0, int& kb1) {
-    if (sk) {
-      if (u >= u1) return false;
-      tile = int(u / nkb);
-      kb0 = int(u - int64_t(tile) * nkb);
-      const int64_t rest = u1 - u;
-      kb1 = rest < int64_t(nkb - kb0) ? kb0 + int(rest) : nkb;
-      u += kb1 - kb0;
-      return true;
-    }
-    if (t >= total) return false;
-    tile = t;
-    kb0 = 0;
-    kb1 = nkb;
-    t += stride;
-    return true;
-  }
-};
-
-__device__ __forceinline__ void epi_bar_sync() {    // the four epilogue warps
-  asm volatile("bar.sync 1, 128;" ::: "memory");
-}
-
 template <int NB>
 __host__ __device__ constexpr uint32_t idesc_swap_bf16_f32() {
   return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(NB >> 3) << 17) |
@@ -972,6 +1064,22 @@ __global__ void __launch_bounds__(6 * 32, 1)
   // touched only after the previous kernel has completed
   __syncthreads();
   pdl_launch_dependents();
+  if (p.prefetch_kb > 0 && warp == 0 && lane == 0) {
+    // While the routing still runs, HBM is idle: warm L2 with the weight
+    // boxes this CTA will stream first if every routed group holds 1..NB
+    // tokens (one tile row per group, the usual decode case).  A wrong guess
+    // only spends otherwise idle bandwidth.
+    const int guess_tiles = p.n_routed * ntiles;
+    const int64_t gu = int64_t(guess_tiles) * p.num_kb;
+    const bool gsk = p.sk_counters != nullptr;
+    SegIter it(gsk, blockIdx.x, gridDim.x, guess_tiles, p.num_kb,
+               gsk ? (gu + gridDim.x - 1) / gridDim.x : 0);
+    int left = p.prefetch_kb, tile, kb0, kb1;
+    while (left > 0 && it.next(tile, kb0, kb1)) {
+      const int g = tile / ntiles, f0 = (tile - g * ntiles) * kFeat;
+      for (int kb = kb0; kb < kb1 && left > 0; ++kb, --left) tma_prefetch_3d(&tmW, kb * BK, f0, g);
+    }
+  }
   pdl_wait_previous();
   if (warp == 2) {
     int32_t carry = 0;
@@ -1324,6 +1432,51 @@ int swap_rows(int64_t Nd, int64_t rows_per_group, int epi) {
   return 0;
 }
 
+// How one grouped Linear runs: the decode tiles (nb token columns) or a tile
+// family, with or without stream-K, and a bound on its tiles (the size of its
+// stream-K counters).  Stream-K needs moe_forward's workspace (`forward`);
+// there, a Linear with fewer CTA-pair tiles than SMs takes single-CTA tiles
+// and stream-K instead of leaving SMs idle.
+struct LinearPlan {
+  int nb = 0;              // decode tiles: token columns; 0: regular tiles
+  int choice = TILE_256;   // regular tiles: TileChoice
+  bool sk = false;
+  int64_t max_tiles = 0;
+};
+
+constexpr int kPlanSms = 148;   // B300 SMs: the family is chosen before any device query
+
+LinearPlan plan_linear(const moe_config& c, int64_t K, int64_t Nd, int epi, int64_t routed_rows,
+                       bool forward) {
+  LinearPlan pl;
+  const int64_t groups = c.n_experts + (c.d_ff_shared > 0 ? 1 : 0);
+  const int64_t routed = routed_rows > 0 ? routed_rows : c.T * c.top_k;
+  const int64_t rows = routed + (c.d_ff_shared > 0 ? c.T : 0);
+  pl.nb = swap_rows(Nd, rows / groups, epi);
+  if (pl.nb > 0) {
+    pl.sk = forward;
+    pl.max_tiles = (ceil_div(rows, pl.nb) + groups) * (Nd / 128);
+    return pl;
+  }
+  pl.choice = pick_tile(Nd, rows / groups, K);
+  if (forward && pl.choice == TILE_256_PAIR &&
+      (ceil_div(rows, 256) + groups) * (Nd / 256) < kPlanSms)
+    pl.choice = TILE_256;
+  pl.sk = forward && epi != EPI_BIAS_F32 &&
+          (pl.choice == TILE_256 || pl.choice == TILE_128 || pl.choice == TILE_64);
+  pl.max_tiles = (ceil_div(rows_max_for(c), tile_rows(pl.choice)) + groups) *
+                 (Nd / tile_bn(pl.choice));
+  return pl;
+}
+
+LinearPlan plan_forward_linear(const moe_config& c, int linear) {
+  const int64_t K = linear == 1 ? c.d_model : c.d_ff;
+  const int64_t Nd = linear == 1 ? c.d_ff : c.d_model;
+  const int epi = linear == 2 ? EPI_BIAS
+                              : (c.act == MOE_ACT_RELU ? EPI_BIAS_RELU : EPI_BIAS_GELU);
+  return plan_linear(c, K, Nd, epi, 0, true);
+}
+
 // One grouped Linear: out[group g] = epi(A[group g] . W[g]^T + bias[g]).
 // out_pre: with an activation epilogue, also store the pre-activation there
 // (only on the staged tile families; see linear_saves_pre).
@@ -1333,11 +1486,11 @@ cudaError_t grouped_linear(const moe_config& c, const GroupedFfnArgs& g, const v
                            const void* W, const void* Ws, const void* bias,
                            const void* bias_s, void* out, int64_t K, int64_t Nd, int epi,
                            cudaStream_t s, void* out_pre = nullptr,
-                           int32_t* sk_counters = nullptr) {
+                           int32_t* sk_counters = nullptr, int prefetch_kb = 0) {
   const int64_t groups = c.n_experts + (c.d_ff_shared > 0 ? 1 : 0);
-  const int64_t routed = g.routed_rows > 0 ? g.routed_rows : c.T * c.top_k;
-  const int64_t rows = routed + (c.d_ff_shared > 0 ? c.T : 0);
-  const int nb = swap_rows(Nd, rows / groups, epi);
+  const bool forward = sk_counters != nullptr && g.sk_partials != nullptr;
+  const LinearPlan pl = plan_linear(c, K, Nd, epi, g.routed_rows, forward);
+  const int nb = pl.nb;
   if (nb > 0) {
     // decode: weights as the MMA's 128-row operand, tokens as its NB columns
     CUtensorMap mW, mWs, mX;
@@ -1362,18 +1515,19 @@ cudaError_t grouped_linear(const moe_config& c, const GroupedFfnArgs& g, const v
     p.num_kb = int32_t(K / BK);
     p.status = g.status;
     p.wait_limit_ns = g.wait_limit_ns;
-    const int64_t max_tiles = (ceil_div(rows, nb) + groups) * (Nd / 128);
+    const int64_t max_tiles = pl.max_tiles;
     int grid = int(max_tiles < g.num_sms ? max_tiles : g.num_sms);
-    if (sk_counters && g.sk_partials) {
+    if (pl.sk) {
       // stream-K: every CTA takes an equal share of the k-blocks
       p.sk_partials = g.sk_partials;
       p.sk_counters = sk_counters;
       grid = g.num_sms < kSkMaxCtas ? g.num_sms : kSkMaxCtas;
     }
+    p.prefetch_kb = prefetch_kb;
     return nb == 16 ? launch_swap<16>(epi, mW, mWs, mX, p, grid, s)
                     : launch_swap<32>(epi, mW, mWs, mX, p, grid, s);
   }
-  const int choice = pick_tile(Nd, rows / groups, K);
+  const int choice = pl.choice;
   const int bn = tile_bn(choice);
   // the CTA pair loads half of each B tile per CTA
   const uint32_t b_box = uint32_t(choice == TILE_256_PAIR ? bn / 2 : bn);
@@ -1404,6 +1558,12 @@ cudaError_t grouped_linear(const moe_config& c, const GroupedFfnArgs& g, const v
   // upper bound on the tiles (every group may add one partial m-tile)
   const int64_t max_tiles =
       (ceil_div(g.rows_max, tile_rows(choice)) + groups) * (Nd / bn);
+  if (pl.sk) {
+    // stream-K: one CTA per SM, each an equal share of the k-blocks
+    p.sk_partials = g.sk_partials;
+    p.sk_counters = sk_counters;
+    return launch_choice(choice, epi, mA, mB, mBs, p, kSkMaxCtas, g.num_sms, s);
+  }
   return launch_choice(choice, epi, mA, mB, mBs, p, max_tiles, g.num_sms, s);
 }
 
@@ -1469,21 +1629,23 @@ bool linear_saves_pre(const moe_config& c) {
          pick_tile(c.d_ff, rows / groups, c.d_model) != TILE_128_2CTA;
 }
 
-int64_t swap_sk_counter_ints(const moe_config& c, int linear) {
+int64_t sk_counter_ints(const moe_config& c, int linear) {
   if (c.dtype == MOE_F32) return 0;
-  const int64_t Nd = linear == 1 ? c.d_ff : c.d_model;
-  const int epi = linear == 2 ? EPI_BIAS
-                              : (c.act == MOE_ACT_RELU ? EPI_BIAS_RELU : EPI_BIAS_GELU);
-  const int64_t groups = c.n_experts + (c.d_ff_shared > 0 ? 1 : 0);
-  const int64_t rows = c.T * c.top_k + (c.d_ff_shared > 0 ? c.T : 0);
-  const int nb = swap_rows(Nd, rows / groups, epi);
-  if (nb == 0) return 0;
-  return (ceil_div(rows, nb) + groups) * (Nd / 128);     // the tile bound of grouped_linear
+  const LinearPlan pl = plan_forward_linear(c, linear);
+  return pl.sk ? pl.max_tiles : 0;
 }
 
-size_t swap_sk_partial_bytes(const moe_config& c) {
-  if (swap_sk_counter_ints(c, 1) == 0 && swap_sk_counter_ints(c, 2) == 0) return 0;
-  return size_t(kSkMaxCtas) * 2 * 32 * 128 * sizeof(float);   // NB <= 32
+size_t sk_partial_bytes(const moe_config& c) {
+  if (c.dtype == MOE_F32) return 0;
+  size_t slot = 0;                       // fp32 partial accumulator of one tile
+  for (int linear = 1; linear <= 2; ++linear) {
+    const LinearPlan pl = plan_forward_linear(c, linear);
+    if (!pl.sk) continue;
+    const size_t b = pl.nb > 0 ? size_t(pl.nb) * 128 * sizeof(float)
+                               : size_t(BM) * size_t(tile_bn(pl.choice)) * sizeof(float);
+    if (b > slot) slot = b;
+  }
+  return size_t(kSkMaxCtas) * 2 * slot;
 }
 
 cudaError_t launch_grouped_ffn_bf16(const moe_config& c, const GroupedFfnArgs& g,
@@ -1496,13 +1658,16 @@ cudaError_t launch_grouped_ffn_bf16(const moe_config& c, const GroupedFfnArgs& g
   int32_t* sk1 = nullptr;
   int32_t* sk2 = nullptr;
   if (g.sk_counters && g.sk_partials) {
-    const int64_t n1 = swap_sk_counter_ints(c, 1);
+    const int64_t n1 = sk_counter_ints(c, 1);
     if (n1 > 0) sk1 = g.sk_counters;
-    if (swap_sk_counter_ints(c, 2) > 0) sk2 = g.sk_counters + n1;
+    if (sk_counter_ints(c, 2) > 0) sk2 = g.sk_counters + n1;
   }
+  // the first Linear of moe_forward's decode tiles warms L2 while the routing runs
+  constexpr int kDecodePrefetchKb = 32;          // x 16 KB per CTA
+  const bool decode1 = sk1 && plan_forward_linear(c, 1).nb > 0;
   cudaError_t e = grouped_linear(c, g, g.Xp, g.w->W1, g.w->W1s, g.w->b1, g.w->b1s, g.H,
                                  c.d_model, c.d_ff, epi1, s, in_epi ? g.pre_out : nullptr,
-                                 sk1);
+                                 sk1, decode1 ? kDecodePrefetchKb : 0);
   if (e == cudaSuccess && g.pre_out && !in_epi)
     e = grouped_linear(c, g, g.Xp, g.w->W1, g.w->W1s, g.w->b1, g.w->b1s, g.pre_out, c.d_model,
                        c.d_ff, EPI_BIAS, s);
@@ -1520,17 +1685,14 @@ const char* grouped_linear_kernel_name(const moe_config& c, int linear, int64_t 
   const int64_t Nd = linear == 1 ? c.d_ff : c.d_model;
   const int epi = linear == 2 ? EPI_BIAS
                               : (c.act == MOE_ACT_RELU ? EPI_BIAS_RELU : EPI_BIAS_GELU);
-  const int64_t groups = c.n_experts + (c.d_ff_shared > 0 ? 1 : 0);
-  const int64_t routed = routed_rows > 0 ? routed_rows : c.T * c.top_k;
-  const int64_t rows = routed + (c.d_ff_shared > 0 ? c.T : 0);
-  const int nb = swap_rows(Nd, rows / groups, epi);
-  if (nb == 16) return "tc_swap_gemm_kernel (128 weight rows x 16 tokens)";
-  if (nb == 32) return "tc_swap_gemm_kernel (128 weight rows x 32 tokens)";
-  switch (pick_tile(Nd, rows / groups, K)) {
+  const LinearPlan pl = plan_linear(c, K, Nd, epi, routed_rows, true);
+  if (pl.nb == 16) return "tc_swap_gemm_kernel (128 weight rows x 16 tokens, stream-K)";
+  if (pl.nb == 32) return "tc_swap_gemm_kernel (128 weight rows x 32 tokens, stream-K)";
+  switch (pl.choice) {
     case TILE_256_PAIR: return "tc2_grouped_gemm_kernel (256 x 256 on a CTA pair)";
-    case TILE_256: return "tc_grouped_gemm_kernel (128 x 256)";
-    case TILE_128: return "tc_grouped_gemm_kernel (128 x 128)";
-    case TILE_64: return "tc_grouped_gemm_kernel (128 x 64)";
+    case TILE_256: return "tc_grouped_gemm_kernel (128 x 256, stream-K)";
+    case TILE_128: return "tc_grouped_gemm_kernel (128 x 128, stream-K)";
+    case TILE_64: return "tc_grouped_gemm_kernel (128 x 64, stream-K)";
     default: return "tc_grouped_gemm_kernel (128 x 128, two CTAs per SM)";
   }
 }

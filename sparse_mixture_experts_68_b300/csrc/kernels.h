@@ -137,17 +137,17 @@ struct GroupedFfnArgs {
   int64_t routed_rows;      // live routed rows for the tile heuristics; 0: T * top_k
   void* pre_out;            // [rows_max, d_ff]: also keep the first Linear's
                             // pre-activation (for the backward), or nullptr
-  // stream-K scratch of the decode tiles (both nullptr: whole tiles per CTA):
-  // per-CTA fp32 partial accumulators, and per-tile counters that start at 0
-  // (swap_sk_counter_ints(c, 1) for Linear 1, then those of Linear 2)
+  // stream-K scratch (both nullptr: whole tiles per CTA): per-CTA fp32
+  // partial accumulators, and per-tile counters that start at 0
+  // (sk_counter_ints(c, 1) for Linear 1, then those of Linear 2)
   float* sk_partials;
   int32_t* sk_counters;
 };
-// Stream-K bookkeeping of moe_forward's decode tiles: counters of grouped
-// Linear 1 or 2 (0 when that Linear does not run the decode tiles), and the
-// partial-accumulator bytes (0 when neither does).
-int64_t swap_sk_counter_ints(const moe_config& c, int linear);
-size_t swap_sk_partial_bytes(const moe_config& c);
+// Stream-K bookkeeping of moe_forward's grouped Linears: counters of Linear
+// 1 or 2 (0 when that Linear runs whole tiles), and the partial-accumulator
+// bytes (0 when neither runs stream-K).
+int64_t sk_counter_ints(const moe_config& c, int linear);
+size_t sk_partial_bytes(const moe_config& c);
 // whether the bf16 first Linear stores its pre-activation from its epilogue
 // (else a second pass does)
 bool linear_saves_pre(const moe_config& c);
