@@ -1,6 +1,7 @@
 // C ABI of libmoe (declared in include/moe.h): host-side validation,
 // workspace layout, and the sequence of launches of one layer.
 #include <cuda.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <atomic>
 #include <cmath>
@@ -16,6 +17,15 @@ __device__ int32_t g_device_status = MOE_OK;
 namespace {
 
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+
+// One NVTX range (a profiler's timeline label) for the scope of a call or a
+// step; nothing happens unless a profiler is attached.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -493,21 +503,27 @@ static moe_status forward_impl(const moe_config* cfg, const void* x, const moe_w
   void* const none[7] = {};
   void* const* ev = events ? events : none;
 
+  const NvtxRange call_range("moe_forward");
   cudaError_t e = record_event(ev[0], s);
-  if (e == cudaSuccess)
+  if (e == cudaSuccess) {
+    const NvtxRange r("router_topk");
     e = launch_router(c, x, w->W_g, w->b_g, logits, out->topk_idx, out->topk_w,
                       ws.prob_partials, di.num_sms, di.status, g_wait_limit_ns.load(), s);
+  }
   if (e == cudaSuccess) e = record_event(ev[1], s);
   // small layers: the one-block permutation also computes the load statistics
   const bool fused_stats = permute_fuses_stats(c);
   const StatsArgs stats{ws.prob_partials, int(router_blocks_of(c)), out->mean_prob,
                         out->balance, out->dropped, out->cv_squared};
-  if (e == cudaSuccess)
+  if (e == cudaSuccess) {
+    const NvtxRange r("permute");
     e = launch_permute(c, x, out->topk_idx, out->counts, out->kept, ws.offsets, ws.row_token,
                        ws.token_row, ws.Xp, ws.scratch, rows_max_of(c), s,
                        fused_stats ? &stats : nullptr, ws.sk_counters, ws.sk_counter_ints);
+  }
   if (e == cudaSuccess) e = record_event(ev[2], s);
   if (e == cudaSuccess) {
+    const NvtxRange r("grouped_ffn");
     GroupedFfnArgs a{};
     a.Xp = ws.Xp; a.offsets = ws.offsets; a.kept = out->kept; a.w = w; a.H = ws.H;
     a.Yp = ws.Yp; a.rows_max = rows_max_of(c); a.status = di.status;
@@ -519,12 +535,16 @@ static moe_status forward_impl(const moe_config* cfg, const void* x, const moe_w
     e = c.dtype == MOE_F32 ? launch_grouped_ffn_f32(c, a, s) : launch_grouped_ffn_bf16(c, a, s);
   }
   if (e == cudaSuccess) e = record_event(ev[4], s);
-  if (e == cudaSuccess)
+  if (e == cudaSuccess) {
+    const NvtxRange r("combine");
     e = launch_combine(c, ws.Yp, ws.token_row, out->topk_w, ws.offsets, out->y, s);
+  }
   if (e == cudaSuccess) e = record_event(ev[5], s);
-  if (e == cudaSuccess && !fused_stats)
+  if (e == cudaSuccess && !fused_stats) {
+    const NvtxRange r("load_stats");
     e = launch_load_stats(c, ws.prob_partials, out->counts, out->kept, out->mean_prob,
                           out->balance, out->dropped, out->cv_squared, s);
+  }
   if (e == cudaSuccess) e = record_event(ev[6], s);
   return cuda_status(e);
 }
@@ -642,6 +662,7 @@ static moe_status backward_impl(const moe_config* cfg, const void* x, const moe_
                                 size_t fwd_workspace_bytes, const void* dy, float aux_weight,
                                 const moe_grads* grads, void* workspace, size_t workspace_bytes,
                                 void* const* events, void* stream) {
+  const NvtxRange call_range("moe_backward");
   moe_status st = check_bwd_config(cfg);
   if (st != MOE_OK) return st;
   const moe_config& c = *cfg;
@@ -783,6 +804,7 @@ moe_status moe_ec_select(const moe_config* cfg, const float* probT, int32_t* ec_
 static moe_status ec_forward_impl(const moe_config* cfg, const void* x, const moe_weights* w,
                                   const moe_ec_outputs* out, void* workspace,
                                   size_t workspace_bytes, void* const* events, void* stream) {
+  const NvtxRange call_range("moe_ec_forward");
   moe_status st = check_ec_config(cfg);
   if (st != MOE_OK) return st;
   const moe_config& c = *cfg;

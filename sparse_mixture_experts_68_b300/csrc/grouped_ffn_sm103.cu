@@ -73,9 +73,7 @@ struct Layout {
   static constexpr int kNumBars = 2 * STAGES + 5;
   static constexpr int kTmemSlot = kBar + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
-  static constexpr int kSkLast = kAbort + 4;                // stream-K: finish this tile
-  static constexpr int kSkStop = kSkLast + 4;               // stream-K: an epilogue warp gave up
-  static constexpr int kTileStart = (kSkStop + 4 + 15) / 16 * 16;   // int32 [kMaxGroups + 1]
+  static constexpr int kTileStart = (kAbort + 4 + 15) / 16 * 16;   // int32 [kMaxGroups + 1]
   static constexpr int kGroupOff = kTileStart + (kMaxGroups + 1) * 4;  // int32 [kMaxGroups]
   static constexpr int kStage = (kGroupOff + kMaxGroups * 4 + 127) / 128 * 128;
   static constexpr int kBytes = kStage + STAGE_BYTES;
@@ -252,10 +250,9 @@ __device__ __forceinline__ TileCoord decode_tile(int tile, const int32_t* tile_s
   return TileCoord{lo, local % mt, local / mt};
 }
 
-// Stream-K.  When a layer has few output tiles for the SM count (the
-// Mixtral-sized decode: 256 tiles of 224 k-blocks in its second Linear; the
-// page-1 layer: 96 to 400 tiles of 12 to 48 k-blocks), whole tiles per CTA
-// leave the last wave of 148 CTAs partly idle.  Instead
+// Stream-K over the decode tiles.  A layer's decode tiles are few and long
+// (for a Mixtral-sized decode, 256 tiles of 224 k-blocks in the second Linear),
+// so whole tiles per CTA leave the last wave of 148 CTAs partly idle.  Instead
 // every CTA takes an equal share of all tiles' k-blocks -- units
 // [b * upc, (b + 1) * upc) of total_tiles * num_kb -- so each streams the same
 // number of weight bytes.  A tile cut by share boundaries is summed by the last
@@ -340,7 +337,6 @@ __global__ void __launch_bounds__(CFG::THREADS, MINB)
     }
     mbar_init(done, 1);
     *abort_flag = 0;
-    *reinterpret_cast<volatile int*>(smem + L::kSkStop) = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
@@ -386,9 +382,6 @@ __global__ void __launch_bounds__(CFG::THREADS, MINB)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int total_tiles = tile_start[n_groups];
-  const bool sk = p.sk_counters != nullptr;
-  const int64_t units = int64_t(total_tiles) * p.num_kb;
-  const int64_t upc = sk ? (units + gridDim.x - 1) / gridDim.x : 0;   // units per CTA
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -398,12 +391,10 @@ __global__ void __launch_bounds__(CFG::THREADS, MINB)
 #pragma unroll
       for (int s = 0; s < kStages; ++s) last_parity[s] = -1;
       bool ok = true;
-      SegIter it(sk, blockIdx.x, gridDim.x, total_tiles, p.num_kb, upc);
-      int tile, kb0, kb1;
-      while (ok && it.next(tile, kb0, kb1)) {
+      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
         const TileCoord tc = decode_tile(tile, tile_start, n_groups, ntiles);
         const int row0 = grp_off[tc.g] + tc.m * BM;
-        for (int kb = kb0; kb < kb1; ++kb) {
+        for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!wait_or_abort(&empty[stage], phase ^ 1u, p, abort_flag)) { ok = false; break; }
           const uint32_t fb = smem_u32(&full[stage]);
           mbar_arrive_expect_tx(&full[stage], L::kStageBytes);
@@ -436,13 +427,11 @@ __global__ void __launch_bounds__(CFG::THREADS, MINB)
       constexpr uint32_t idesc = idesc_bf16_f32<BN>();
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
-      SegIter it(sk, blockIdx.x, gridDim.x, total_tiles, p.num_kb, upc);
-      int tile, kb0, kb1;
-      while (ok && it.next(tile, kb0, kb1)) {
+      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
         if (!wait_or_abort(&tempty[acc], acc_phase ^ 1u, p, abort_flag)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = kb0; kb < kb1; ++kb) {
+        for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!wait_or_abort(&full[stage], phase, p, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const uint64_t ad = sdesc_sw128(smem_u32(smem + L::kA + stage * L::kABytes));
@@ -450,7 +439,7 @@ __global__ void __launch_bounds__(CFG::THREADS, MINB)
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)   // +32 bytes along K per step
             tc_mma(d_tmem, ad + uint64_t(2 * kk), bd + uint64_t(2 * kk), idesc,
-                   (kb != kb0 || kk != 0) ? 1u : 0u);
+                   (kb | kk) != 0 ? 1u : 0u);
           tc_commit(smem_u32(&empty[stage]));
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
@@ -471,26 +460,12 @@ __global__ void __launch_bounds__(CFG::THREADS, MINB)
     const int part = (warp - 2) >> 2;            // which share of the tile's columns
     constexpr int kCols = BN / (kEpiWarps / 4);
     constexpr int CW = kCols < 32 ? kCols : 32;  // columns per tcgen05.ld
-    constexpr int kEpiThreads = kEpiWarps * 32;
-    volatile int* sk_last = reinterpret_cast<volatile int*>(smem + L::kSkLast);
-    volatile int* sk_stop = reinterpret_cast<volatile int*>(smem + L::kSkStop);
-    const int64_t my_u0 = int64_t(blockIdx.x) * upc;
     uint32_t acc = 0, acc_phase = 0;
-    SegIter it(sk, blockIdx.x, gridDim.x, total_tiles, p.num_kb, upc);
-    int tile, kb0, kb1;
-    while (it.next(tile, kb0, kb1)) {
+    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
       const TileCoord tc = decode_tile(tile, tile_start, n_groups, ntiles);
       bool ok = true;
       if (lane == 0) ok = wait_or_abort(&tfull[acc], acc_phase, p, abort_flag);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (sk) {
-        // the epilogue warps synchronise below: they stop together, whichever
-        // of them gave up waiting
-        if (!ok && lane == 0) *sk_stop = 1;
-        epi_bar_sync(kEpiThreads);
-        ok = *sk_stop == 0;
-        epi_bar_sync(kEpiThreads);               // every warp has read the flag
-      }
       if (!ok) break;
       tc_fence_after();
       const bool routed = tc.g < p.n_routed;
@@ -501,8 +476,10 @@ __global__ void __launch_bounds__(CFG::THREADS, MINB)
       const __nv_bfloat16* bias = routed ? p.bias + int64_t(tc.g) * p.Nd : p.bias_s;
       constexpr int kOutBytes = EPI == EPI_BIAS_F32 ? 4 : 2;
       constexpr bool kStaged = CFG::STAGED && EPI != EPI_BIAS_F32;
-      // + bias, activation and store of the CW accumulator columns at c
-      auto store_chunk = [&](int c, const uint32_t (&r)[CW]) {
+#pragma unroll 1
+      for (int c = part * kCols; c < (part + 1) * kCols; c += CW) {
+        uint32_t r[CW];
+        tmem_ld_cols<CW>(tmem_base + (uint32_t(q * 32) << 16) + acc * BN + c, r);
         const int64_t col = int64_t(tc.n) * BN + c;
         if constexpr (kStaged) {
           uint8_t* stg = smem + L::kStage + (warp - 2) * staged_warp_bytes<16>();
@@ -527,75 +504,10 @@ __global__ void __launch_bounds__(CFG::THREADS, MINB)
                                   static_cast<uint8_t*>(p.out) +
                                       (out_row * p.Nd + col) * kOutBytes);
         }
-      };
-      if (kb0 == 0 && kb1 == p.num_kb) {          // a whole tile
-#pragma unroll 1
-        for (int c = part * kCols; c < (part + 1) * kCols; c += CW) {
-          uint32_t r[CW];
-          tmem_ld_cols<CW>(tmem_base + (uint32_t(q * 32) << 16) + acc * BN + c, r);
-          store_chunk(c, r);
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[acc]);
-      } else {
-        // a piece of a tile: publish it; the last of the tile's CTAs sums the
-        // pieces in k order and runs the epilogue
-        const int64_t t0 = int64_t(tile) * p.num_kb;
-        const int c_first = int(t0 / upc), c_last = int((t0 + p.num_kb - 1) / upc);
-        const int slot = t0 + kb0 == my_u0 ? 0 : 1;
-        const int row = q * 32 + lane;
-        float* mine = p.sk_partials + (int64_t(blockIdx.x) * 2 + slot) * (BM * BN) +
-                      int64_t(row) * BN;
-#pragma unroll 1
-        for (int c = part * kCols; c < (part + 1) * kCols; c += CW) {
-          uint32_t r[CW];
-          tmem_ld_cols<CW>(tmem_base + (uint32_t(q * 32) << 16) + acc * BN + c, r);
-#pragma unroll
-          for (int i = 0; i < CW; i += 4)
-            __stcg(reinterpret_cast<float4*>(mine + c + i),
-                   make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]),
-                               __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3])));
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[acc]);
-        __threadfence();
-        epi_bar_sync(kEpiThreads);
-        if (warp == 2 && lane == 0) {
-          const int done_before = atomicAdd(p.sk_counters + tile, 1);
-          const int last = done_before == c_last - c_first;
-          if (last) p.sk_counters[tile] = 0;      // ready for the next call
-          *sk_last = last;
-        }
-        epi_bar_sync(kEpiThreads);
-        const bool last = *sk_last != 0;
-        epi_bar_sync(kEpiThreads);                // the flag is read before reuse
-        if (last) {
-          __threadfence();
-#pragma unroll 1
-          for (int c = part * kCols; c < (part + 1) * kCols; c += CW) {
-            float sum[CW];
-#pragma unroll
-            for (int i = 0; i < CW; ++i) sum[i] = 0.f;
-            for (int cc = c_first; cc <= c_last; ++cc) {   // the pieces in k order
-              const int64_t cu0 = int64_t(cc) * upc;
-              const float* piece = p.sk_partials +
-                                   (int64_t(cc) * 2 + (t0 > cu0 ? 1 : 0)) * (BM * BN) +
-                                   int64_t(row) * BN + c;
-#pragma unroll
-              for (int i = 0; i < CW; i += 4) {
-                const float4 v = __ldcg(reinterpret_cast<const float4*>(piece + i));
-                sum[i] += v.x; sum[i + 1] += v.y; sum[i + 2] += v.z; sum[i + 3] += v.w;
-              }
-            }
-            uint32_t r[CW];
-#pragma unroll
-            for (int i = 0; i < CW; ++i) r[i] = __float_as_uint(sum[i]);
-            store_chunk(c, r);
-          }
-        }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
@@ -1432,19 +1344,15 @@ int swap_rows(int64_t Nd, int64_t rows_per_group, int epi) {
   return 0;
 }
 
-// How one grouped Linear runs: the decode tiles (nb token columns) or a tile
-// family, with or without stream-K, and a bound on its tiles (the size of its
-// stream-K counters).  Stream-K needs moe_forward's workspace (`forward`);
-// there, a Linear with fewer CTA-pair tiles than SMs takes single-CTA tiles
-// and stream-K instead of leaving SMs idle.
+// How one grouped Linear runs: the decode tiles (nb token columns, stream-K
+// when moe_forward's workspace holds its scratch: `forward`) or a tile family,
+// and a bound on its tiles (the size of its stream-K counters).
 struct LinearPlan {
   int nb = 0;              // decode tiles: token columns; 0: regular tiles
   int choice = TILE_256;   // regular tiles: TileChoice
   bool sk = false;
   int64_t max_tiles = 0;
 };
-
-constexpr int kPlanSms = 148;   // B300 SMs: the family is chosen before any device query
 
 LinearPlan plan_linear(const moe_config& c, int64_t K, int64_t Nd, int epi, int64_t routed_rows,
                        bool forward) {
@@ -1459,11 +1367,6 @@ LinearPlan plan_linear(const moe_config& c, int64_t K, int64_t Nd, int epi, int6
     return pl;
   }
   pl.choice = pick_tile(Nd, rows / groups, K);
-  if (forward && pl.choice == TILE_256_PAIR &&
-      (ceil_div(rows, 256) + groups) * (Nd / 256) < kPlanSms)
-    pl.choice = TILE_256;
-  pl.sk = forward && epi != EPI_BIAS_F32 &&
-          (pl.choice == TILE_256 || pl.choice == TILE_128 || pl.choice == TILE_64);
   pl.max_tiles = (ceil_div(rows_max_for(c), tile_rows(pl.choice)) + groups) *
                  (Nd / tile_bn(pl.choice));
   return pl;
@@ -1558,12 +1461,6 @@ cudaError_t grouped_linear(const moe_config& c, const GroupedFfnArgs& g, const v
   // upper bound on the tiles (every group may add one partial m-tile)
   const int64_t max_tiles =
       (ceil_div(g.rows_max, tile_rows(choice)) + groups) * (Nd / bn);
-  if (pl.sk) {
-    // stream-K: one CTA per SM, each an equal share of the k-blocks
-    p.sk_partials = g.sk_partials;
-    p.sk_counters = sk_counters;
-    return launch_choice(choice, epi, mA, mB, mBs, p, kSkMaxCtas, g.num_sms, s);
-  }
   return launch_choice(choice, epi, mA, mB, mBs, p, max_tiles, g.num_sms, s);
 }
 
@@ -1641,8 +1538,7 @@ size_t sk_partial_bytes(const moe_config& c) {
   for (int linear = 1; linear <= 2; ++linear) {
     const LinearPlan pl = plan_forward_linear(c, linear);
     if (!pl.sk) continue;
-    const size_t b = pl.nb > 0 ? size_t(pl.nb) * 128 * sizeof(float)
-                               : size_t(BM) * size_t(tile_bn(pl.choice)) * sizeof(float);
+    const size_t b = size_t(pl.nb) * 128 * sizeof(float);   // decode tiles only
     if (b > slot) slot = b;
   }
   return size_t(kSkMaxCtas) * 2 * slot;
@@ -1690,9 +1586,9 @@ const char* grouped_linear_kernel_name(const moe_config& c, int linear, int64_t 
   if (pl.nb == 32) return "tc_swap_gemm_kernel (128 weight rows x 32 tokens, stream-K)";
   switch (pl.choice) {
     case TILE_256_PAIR: return "tc2_grouped_gemm_kernel (256 x 256 on a CTA pair)";
-    case TILE_256: return "tc_grouped_gemm_kernel (128 x 256, stream-K)";
-    case TILE_128: return "tc_grouped_gemm_kernel (128 x 128, stream-K)";
-    case TILE_64: return "tc_grouped_gemm_kernel (128 x 64, stream-K)";
+    case TILE_256: return "tc_grouped_gemm_kernel (128 x 256)";
+    case TILE_128: return "tc_grouped_gemm_kernel (128 x 128)";
+    case TILE_64: return "tc_grouped_gemm_kernel (128 x 64)";
     default: return "tc_grouped_gemm_kernel (128 x 128, two CTAs per SM)";
   }
 }

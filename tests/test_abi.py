@@ -199,8 +199,7 @@ def test_ffn_kernel_names_follow_the_layer_shape():
     assert "tc_swap_gemm_kernel" in name("c3_mixtral_decode", 1)
     assert "tc_swap_gemm_kernel" in name("c3_mixtral_decode", 2)
     assert name("c1_page1_bf16", 1).startswith("tc_grouped_gemm_kernel")
-    # fewer CTA-pair tiles than SMs: single-CTA tiles with stream-K instead
-    assert name("c1_page1_bf16", 2) == "tc_grouped_gemm_kernel (128 x 256, stream-K)"
+    assert "tc2_grouped_gemm_kernel" in name("c1_page1_bf16", 2)
     assert "simt_gemm_kernel" in name("c0_pr1_fp32", 1)
     cfg = B.make_config(WORKLOADS["c1_page1_bf16"])
     assert B.lib().moe_ffn_kernel_name(C.byref(cfg), 3) is None

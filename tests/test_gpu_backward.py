@@ -10,8 +10,8 @@ every intermediate in fp32: a few 1e-7 of rounding per value), applied
     tokens, with each row's norm floored at a thousandth of the median row
     norm for dx (a row whose every slot was dropped carries only the tiny
     balance term), and for dz against the larger of its norm and its gate
-    gradients' scale sum_j w_j |dw_j| (a difference of gate gradients that can
-    cancel; see dz_row_max_rel);
+    gradients' scale ||dy[t]|| sum_j w_j ||o[t, j]|| (a difference of gate
+    gradients that can cancel; see dz_row_max_rel);
   * dW_g, db_g and dw as whole tensors.
 The GPU stores five bf16 intermediates on the way (dO = w dy, the recomputed
 pre-activation, dA, dXp and the expert outputs behind dw), each rounded to 8
@@ -47,18 +47,46 @@ pytestmark = pytest.mark.gpu
 GRAD_TOL = {DT_BF16: 2e-2, DT_F32: 1e-4}
 
 
-def dz_row_max_rel(gz, rz, w, rdw):
-    """Max over tokens of ||dz_gpu[t] - dz_ref[t]|| / max(||dz_ref[t]||, S_t),
-    S_t = sum_j w[t, j] |dw_ref[t, j]|.  A token's renormalised score gradient
-    is a difference of its gate gradients -- for k = 2, w0 w1 (dw0 - dw1) on
-    its two experts -- which can cancel to almost nothing, while the rounding
-    error it inherits from dw (inner products with bf16 expert outputs) stays
-    at the scale of the gate gradients themselves, S_t."""
+def gate_grad_scale(L, r, dy, tokens):
+    """S_t = ||dy[t]|| sum_j w[t, j] ||o[t, j]|| over the token's kept slots,
+    o[t, j] the oracle's expert output.  By Cauchy-Schwarz it bounds
+    sum_j w[t, j] |dw[t, j]|, the scale of the gate gradients whose rounding
+    reaches the score gradient dz[t]."""
+    from concurrent.futures import ThreadPoolExecutor
+    tokens = np.asarray(tokens, dtype=np.int64)
+    k = r.idx.shape[1]
+    slots = {}
+    for i, t in enumerate(tokens):
+        for j in range(k):
+            if r.keep[t, j]:
+                slots.setdefault(int(r.idx[t, j]), []).append((i, j))
+
+    def one(item):
+        e, lst = item
+        _, _, o = L.expert_rows(e, tokens[[i for i, _ in lst]], want=("o",))
+        return lst, np.linalg.norm(o, axis=1)
+
+    S = np.zeros(len(tokens))
+    with ThreadPoolExecutor(max_workers=WORKERS) as ex:
+        for lst, on in ex.map(one, slots.items()):
+            for (i, j), n in zip(lst, on):
+                S[i] += r.w[tokens[i], j] * n
+    dyn = np.linalg.norm(np.asarray(dy, dtype=np.float64)[tokens], axis=1)
+    return S * dyn
+
+
+def dz_row_max_rel(gz, rz, scale):
+    """Max over tokens of ||dz_gpu[t] - dz_ref[t]|| / max(||dz_ref[t]||, scale[t]).
+    A token's renormalised score gradient is a difference of its gate
+    gradients -- for k = 2, w0 w1 (dw0 - dw1) on its two experts -- which can
+    cancel to almost nothing, while the rounding it inherits from dw (inner
+    products of dy with bf16 expert outputs) stays at the gate gradients'
+    scale: scale = gate_grad_scale."""
     gz, rz = np.asarray(gz, np.float64), np.asarray(rz, np.float64)
     if gz.shape[0] == 0:
         return 0.0
-    scale = np.maximum(np.linalg.norm(rz, axis=1), np.sum(np.abs(w * rdw), axis=1))
-    return float(np.max(np.linalg.norm(gz - rz, axis=1) / np.maximum(scale, 1e-30)))
+    den = np.maximum(np.maximum(np.linalg.norm(rz, axis=1), scale), 1e-30)
+    return float(np.max(np.linalg.norm(gz - rz, axis=1) / den))
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -116,7 +144,8 @@ def check_backward(wl, layer, t, out, dy, aux, grads):
                 workers=WORKERS)
     ref = L.backward(r, dy.cpu(), aux, renormalize=bool(cfg.renormalize), workers=WORKERS)
     report = {"dx_row": row_max_rel(to64(grads.dx), ref.dx),
-              "dz_row": dz_row_max_rel(to64(grads.dz), ref.dz, r.w, ref.dw),
+              "dz_row": dz_row_max_rel(to64(grads.dz), ref.dz,
+                                       gate_grad_scale(L, r, to64(dy), np.arange(cfg.T))),
               "dw": rel_l2(to64(grads.dw), ref.dw),
               "dW_g": rel_l2(to64(grads.dW_g), ref.dW_g),
               "db_g": rel_l2(to64(grads.db_g), ref.db_g)}
@@ -355,7 +384,7 @@ def check_large_backward(wl, aux, tokens_per_group, seed):
     report = {"tokens": len(toks),
               "dx_row": row_max_rel(to64(g.dx[torch.from_numpy(toks).cuda()]), rdx),
               "dz_row": dz_row_max_rel(to64(g.dz[torch.from_numpy(toks).cuda()]), rdz,
-                                       r.w[toks], rdw),
+                                       gate_grad_scale(L, r, to64(dy), toks)),
               "dw": rel_l2(to64(g.dw[torch.from_numpy(toks).cuda()]), rdw)}
 
     # every expert (and the shared one): sampled hidden units
