@@ -103,9 +103,6 @@ struct TcParams {
   // fp32 partial accumulators and one counter per tile, 0 at launch
   float* sk_partials;
   int32_t* sk_counters;
-  // decode tiles: weight k-blocks each CTA prefetches into L2 before the
-  // previous kernels (the routing) have finished; 0: none
-  int32_t prefetch_kb;
 };
 
 // Epilogue of CW accumulator columns of one row: + bias, activation, store.
@@ -976,22 +973,6 @@ __global__ void __launch_bounds__(6 * 32, 1)
   // touched only after the previous kernel has completed
   __syncthreads();
   pdl_launch_dependents();
-  if (p.prefetch_kb > 0 && warp == 0 && lane == 0) {
-    // While the routing still runs, HBM is idle: warm L2 with the weight
-    // boxes this CTA will stream first if every routed group holds 1..NB
-    // tokens (one tile row per group, the usual decode case).  A wrong guess
-    // only spends otherwise idle bandwidth.
-    const int guess_tiles = p.n_routed * ntiles;
-    const int64_t gu = int64_t(guess_tiles) * p.num_kb;
-    const bool gsk = p.sk_counters != nullptr;
-    SegIter it(gsk, blockIdx.x, gridDim.x, guess_tiles, p.num_kb,
-               gsk ? (gu + gridDim.x - 1) / gridDim.x : 0);
-    int left = p.prefetch_kb, tile, kb0, kb1;
-    while (left > 0 && it.next(tile, kb0, kb1)) {
-      const int g = tile / ntiles, f0 = (tile - g * ntiles) * kFeat;
-      for (int kb = kb0; kb < kb1 && left > 0; ++kb, --left) tma_prefetch_3d(&tmW, kb * BK, f0, g);
-    }
-  }
   pdl_wait_previous();
   if (warp == 2) {
     int32_t carry = 0;
@@ -1186,6 +1167,34 @@ __global__ void __launch_bounds__(6 * 32, 1)
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
                  "r"(kTmemCols));
+  }
+}
+
+// ---- decode: warm L2 with the first Linear's weights while the routing runs ----------
+//
+// Launched first in moe_forward when the first Linear runs the decode tiles.
+// Block b issues L2 prefetches (TMA, no shared memory) of the first
+// kDecodePrefetchKb weight boxes that CTA b of the stream-K first Linear will
+// stream if every routed expert holds 1..NB tokens (the usual decode case:
+// one tile row per expert), then exits.  HBM is otherwise idle during the
+// router, the sort and the row copy; a wrong guess only spends that idle
+// bandwidth.
+
+constexpr int kDecodePrefetchKb = 40;           // 40 x 16 KB per CTA: ~95 MB over 148 CTAs
+
+__global__ void __launch_bounds__(32)
+    decode_prefetch_kernel(const __grid_constant__ CUtensorMap tmW, int n_routed, int ntiles,
+                           int num_kb) {
+  pdl_launch_dependents();
+  if (threadIdx.x != 0) return;
+  const int guess_tiles = n_routed * ntiles;
+  const int64_t units = int64_t(guess_tiles) * num_kb;
+  SegIter it(true, blockIdx.x, gridDim.x, guess_tiles, num_kb,
+             (units + gridDim.x - 1) / gridDim.x);
+  int left = kDecodePrefetchKb, tile, kb0, kb1;
+  while (left > 0 && it.next(tile, kb0, kb1)) {
+    const int g = tile / ntiles, f0 = (tile - g * ntiles) * 128;
+    for (int kb = kb0; kb < kb1 && left > 0; ++kb, --left) tma_prefetch_3d(&tmW, kb * BK, f0, g);
   }
 }
 
@@ -1389,7 +1398,7 @@ cudaError_t grouped_linear(const moe_config& c, const GroupedFfnArgs& g, const v
                            const void* W, const void* Ws, const void* bias,
                            const void* bias_s, void* out, int64_t K, int64_t Nd, int epi,
                            cudaStream_t s, void* out_pre = nullptr,
-                           int32_t* sk_counters = nullptr, int prefetch_kb = 0) {
+                           int32_t* sk_counters = nullptr) {
   const int64_t groups = c.n_experts + (c.d_ff_shared > 0 ? 1 : 0);
   const bool forward = sk_counters != nullptr && g.sk_partials != nullptr;
   const LinearPlan pl = plan_linear(c, K, Nd, epi, g.routed_rows, forward);
@@ -1426,7 +1435,6 @@ cudaError_t grouped_linear(const moe_config& c, const GroupedFfnArgs& g, const v
       p.sk_counters = sk_counters;
       grid = g.num_sms < kSkMaxCtas ? g.num_sms : kSkMaxCtas;
     }
-    p.prefetch_kb = prefetch_kb;
     return nb == 16 ? launch_swap<16>(epi, mW, mWs, mX, p, grid, s)
                     : launch_swap<32>(epi, mW, mWs, mX, p, grid, s);
   }
@@ -1472,6 +1480,22 @@ cudaError_t launch_grouped_linear_bf16(const moe_config& c, const GroupedFfnArgs
                                        int64_t K, int64_t Nd, cudaStream_t s) {
   if (g.rows_max == 0) return cudaSuccess;
   return grouped_linear(c, g, A, W, Ws, bias, bias_s, out, K, Nd, EPI_BIAS, s);
+}
+
+cudaError_t launch_decode_prefetch(const moe_config& c, const moe_weights* w, int num_sms,
+                                   cudaStream_t s) {
+  const LinearPlan pl = plan_forward_linear(c, 1);
+  if (c.dtype == MOE_F32 || pl.nb == 0 || c.T == 0) return cudaSuccess;
+  CUtensorMap mW;
+  if (!make_map(&mW, w->W1, uint64_t(c.d_model), uint64_t(c.d_ff), uint64_t(c.n_experts), 128))
+    return cudaErrorInvalidValue;
+  const int grid = num_sms < kSkMaxCtas ? num_sms : kSkMaxCtas;   // the first Linear's grid
+  return launch_pdl(decode_prefetch_kernel, dim3(grid), dim3(32), 0, s, mW,
+                    int(c.n_experts), int(c.d_ff / 128), int(c.d_model / BK));
+}
+
+int decode_prefetch_launches(const moe_config& c) {
+  return c.dtype != MOE_F32 && c.T > 0 && plan_forward_linear(c, 1).nb > 0 ? 1 : 0;
 }
 
 bool bwd_dgrad_on_pair(const moe_config& c, int64_t K, int64_t Nd) {
@@ -1558,12 +1582,9 @@ cudaError_t launch_grouped_ffn_bf16(const moe_config& c, const GroupedFfnArgs& g
     if (n1 > 0) sk1 = g.sk_counters;
     if (sk_counter_ints(c, 2) > 0) sk2 = g.sk_counters + n1;
   }
-  // the first Linear of moe_forward's decode tiles warms L2 while the routing runs
-  constexpr int kDecodePrefetchKb = 32;          // x 16 KB per CTA
-  const bool decode1 = sk1 && plan_forward_linear(c, 1).nb > 0;
   cudaError_t e = grouped_linear(c, g, g.Xp, g.w->W1, g.w->W1s, g.w->b1, g.w->b1s, g.H,
                                  c.d_model, c.d_ff, epi1, s, in_epi ? g.pre_out : nullptr,
-                                 sk1, decode1 ? kDecodePrefetchKb : 0);
+                                 sk1);
   if (e == cudaSuccess && g.pre_out && !in_epi)
     e = grouped_linear(c, g, g.Xp, g.w->W1, g.w->W1s, g.w->b1, g.w->b1s, g.pre_out, c.d_model,
                        c.d_ff, EPI_BIAS, s);
