@@ -449,6 +449,35 @@ moe_status moe_selftest_bounded_wait(uint64_t limit_ns, void* stream);
 const char* moe_status_string(moe_status s);
 int32_t moe_version(void);
 
+/* ---- build variants and device checks ----------------------------------------
+ *
+ * The library can be built with -DMOE_CHECKS (libmoe_checks.so): every kernel
+ * then checks the indices it gathers or scatters through (expert ids, token
+ * rows, group extents) before the access, and a failed check is counted in a
+ * device record -- the kernel carries on with its accesses bounded, nothing
+ * traps.  The forward workspace also gets a 256-byte guard gap after each of
+ * its regions, so a test can fill the workspace with a pattern and see that no
+ * kernel wrote outside its region.  Test and debugging aids: the pages have no
+ * counterpart.
+ *
+ * moe_build_flags: MOE_BUILD_CHECKS when this is the checks build, else 0.
+ * moe_workspace_guards: the guard gaps of moe_forward's workspace for this
+ *   layer (offsets in bytes from its start, each 256 bytes long), up to
+ *   max_guards of them written to offsets; returns their number (0 in the
+ *   ordinary build) or -1 for an invalid config.
+ * moe_checks_read: the number of failed checks since the last clear, with the
+ *   site (MOE_CHECK_* below) and source line of the first; clear != 0 resets
+ *   the records.  Synchronous with the device; always 0 in the ordinary build. */
+#define MOE_BUILD_CHECKS 1
+enum {
+  MOE_CHECK_ROUTER_TOPK = 1, MOE_CHECK_SORT_EXPERT = 2, MOE_CHECK_COPY_TOKEN = 3,
+  MOE_CHECK_ROWS_TOTAL = 4, MOE_CHECK_COMBINE_ROW = 5, MOE_CHECK_GEMM_ROWS = 6,
+  MOE_CHECK_EC_PICK = 7
+};
+int32_t moe_build_flags(void);
+int32_t moe_workspace_guards(const moe_config* cfg, int64_t* offsets, int32_t max_guards);
+moe_status moe_checks_read(int32_t* fails, int32_t* site, int32_t* line, int32_t clear);
+
 #ifdef __cplusplus
 }
 #endif

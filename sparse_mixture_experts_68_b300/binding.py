@@ -16,7 +16,10 @@ import torch
 from .workloads import DT_F32, Workload
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libmoe.so")
+# MOE_LIBRARY=checks loads the build with device index checks and workspace
+# guards (libmoe_checks.so, same ABI); the default is libmoe.so.
+LIB_PATH = os.path.join(_HERE, "libmoe_checks.so" if os.environ.get("MOE_LIBRARY") == "checks"
+                        else "libmoe.so")
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, \
     MOE_ERR_TIMEOUT = range(6)
@@ -35,7 +38,10 @@ EXPORTS = [
     "moe_ec_forward_launch_count", "moe_ec_router", "moe_ec_select", "moe_ec_forward",
     "moe_ec_forward_profiled", "moe_backward", "moe_backward_workspace_size",
     "moe_backward_launch_count", "moe_backward_profiled", "moe_ffn_kernel_name",
+    "moe_build_flags", "moe_workspace_guards", "moe_checks_read",
 ]
+MOE_BUILD_CHECKS = 1
+GUARD_BYTES = 256
 PERMUTE_STATIC_SCRATCH_INTS = 1 << 18
 
 
@@ -77,6 +83,7 @@ class MoeEcOutputs(C.Structure):
 
 
 _lib = None
+_LAYERS = []        # checks build: layers whose workspace guards tests inspect
 
 
 def lib() -> C.CDLL:
@@ -97,6 +104,9 @@ def lib() -> C.CDLL:
         "moe_workspace_size": (C.c_size_t, [CP]),
         "moe_forward_launch_count": (C.c_int32, [CP]),
         "moe_ffn_kernel_name": (C.c_char_p, [CP, C.c_int32]),
+        "moe_build_flags": (C.c_int32, []),
+        "moe_workspace_guards": (C.c_int32, [CP, P, C.c_int32]),
+        "moe_checks_read": (C.c_int32, [P, P, P, C.c_int32]),
         "moe_host_workspace_size": (C.c_size_t, [CP]),
         "moe_router_topk": (C.c_int32, [CP, P, P, P, P, P, P, P, P]),
         "moe_permute": (C.c_int32, [CP, P, P, P, P, P, P, P, P, P, C.c_size_t, P]),
@@ -147,6 +157,14 @@ def lib() -> C.CDLL:
     return L
 
 
+def take_checked_layers() -> list:
+    """Checks build: the MoeLayers made since the last call (their guards can
+    be inspected), forgetting them."""
+    out = list(_LAYERS)
+    _LAYERS.clear()
+    return out
+
+
 def status_string(s: int) -> str:
     return lib().moe_status_string(s).decode()
 
@@ -192,6 +210,28 @@ def workspace_size(cfg: MoeConfig) -> int:
 
 def forward_launch_count(cfg: MoeConfig) -> int:
     return int(lib().moe_forward_launch_count(C.byref(cfg)))
+
+
+def is_checks_build() -> bool:
+    return (int(lib().moe_build_flags()) & MOE_BUILD_CHECKS) != 0
+
+
+def workspace_guards(cfg: MoeConfig) -> list:
+    """Byte offsets of the guard gaps in moe_forward's workspace (checks build)."""
+    n = int(lib().moe_workspace_guards(C.byref(cfg), None, 0))
+    if n <= 0:
+        return []
+    buf = (C.c_int64 * n)()
+    lib().moe_workspace_guards(C.byref(cfg), buf, n)
+    return list(buf)
+
+
+def checks_read(clear: bool = True):
+    """(failed checks since the last clear, site of the first, its source line)."""
+    f, s_, l_ = C.c_int32(), C.c_int32(), C.c_int32()
+    _check(lib().moe_checks_read(C.byref(f), C.byref(s_), C.byref(l_), int(clear)),
+           "moe_checks_read")
+    return int(f.value), int(s_.value), int(l_.value)
 
 
 def ffn_kernel_name(cfg: MoeConfig, linear: int) -> str | None:
@@ -424,12 +464,30 @@ class MoeLayer:
         self.weights = make_weights(tensors)
         self.workspace = torch.empty(max(workspace_size(self.cfg), 256), dtype=torch.uint8,
                                      device=self.device)
+        self._fill_guards()
+
+    GUARD_PATTERN = 0xA5
+
+    def _fill_guards(self):
+        """Checks build: the guard gaps hold a fixed pattern (see guards_intact)."""
+        if self.device.type == "cuda" and is_checks_build():
+            self.workspace.fill_(self.GUARD_PATTERN)
+            _LAYERS.append(self)
+
+    def guards_intact(self) -> bool:
+        """Whether every guard gap of the workspace still holds the pattern."""
+        for off in workspace_guards(self.cfg):
+            gap = self.workspace[off: off + GUARD_BYTES]
+            if not bool(torch.all(gap == self.GUARD_PATTERN)):
+                return False
+        return True
 
     def set_tokens(self, T: int):
         self.cfg = make_config(self.wl, T=T, capacity=self.cfg.capacity)
         need = workspace_size(self.cfg)
         if need > self.workspace.numel():
             self.workspace = torch.empty(need, dtype=torch.uint8, device=self.device)
+        self._fill_guards()
 
     def forward(self, x, out: Outputs | None = None, with_logits=False, with_pre_act=False,
                 stream=None) -> Outputs:

@@ -76,7 +76,17 @@ struct Workspace {
   int32_t* sk_counters;
   int64_t sk_counter_ints;
   size_t bytes;
+  // checks build: a 256-byte guard after every region (offsets from the base)
+  static constexpr int kMaxGuards = 16;
+  int64_t guard[kMaxGuards];
+  int32_t n_guards;
 };
+
+#ifdef MOE_CHECKS
+constexpr size_t kGuardBytes = 256;
+#else
+constexpr size_t kGuardBytes = 0;
+#endif
 
 Workspace layout(const moe_config& c, void* base) {
   Workspace w{};
@@ -85,6 +95,10 @@ Workspace layout(const moe_config& c, void* base) {
   auto take = [&](size_t n) {
     const size_t at = off;
     off += (n + 255) / 256 * 256;
+    if (kGuardBytes > 0 && w.n_guards < Workspace::kMaxGuards) {
+      w.guard[w.n_guards++] = int64_t(off);
+      off += kGuardBytes;
+    }
     return reinterpret_cast<void*>(p + at);
   };
   const int64_t rows = rows_max_of(c);
@@ -882,6 +896,42 @@ moe_status moe_ec_forward_profiled(const moe_config* cfg, const void* x, const m
       ec_forward_impl(cfg, x, w, out, workspace, workspace_bytes, events, stream);
   pdl_enabled() = true;
   return st;
+}
+
+int32_t moe_build_flags(void) {
+#ifdef MOE_CHECKS
+  return MOE_BUILD_CHECKS;
+#else
+  return 0;
+#endif
+}
+
+int32_t moe_workspace_guards(const moe_config* cfg, int64_t* offsets, int32_t max_guards) {
+  if (check_config(cfg) != MOE_OK) return -1;
+  const Workspace w = layout(*cfg, nullptr);
+  for (int32_t i = 0; i < w.n_guards && i < max_guards && offsets; ++i) offsets[i] = w.guard[i];
+  return w.n_guards;
+}
+
+moe_status moe_checks_read(int32_t* fails, int32_t* site, int32_t* line, int32_t clear) {
+  if (!fails || !site || !line) return MOE_ERR_INVALID_ARG;
+  cudaError_t (*readers[])(CheckRecord*, bool) = {
+      checks_read_router, checks_read_permute, checks_read_combine,
+      checks_read_expert_choice, checks_read_backward, checks_read_grouped_bwd,
+      checks_read_grouped_ffn_f32, checks_read_grouped_ffn};
+  *fails = 0;
+  *site = 0;
+  *line = 0;
+  for (auto rd : readers) {
+    CheckRecord r{};
+    if (rd(&r, clear != 0) != cudaSuccess) return MOE_ERR_CUDA;
+    if (r.fails > 0 && *fails == 0) {
+      *site = r.site;
+      *line = r.line;
+    }
+    *fails += r.fails;
+  }
+  return MOE_OK;
 }
 
 moe_status moe_get_device_status(void* stream) {

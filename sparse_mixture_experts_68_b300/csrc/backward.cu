@@ -888,4 +888,6 @@ cudaError_t launch_backward(const moe_config& c, const BackwardArgs& a, void* co
                             : backward_t<__nv_bfloat16>(c, a, events, s);
 }
 
+MOE_CHECKS_UNIT(backward)
+
 }  // namespace moe

@@ -41,6 +41,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
   for (int j0 = 0; j0 < k; j0 += 32) {
     const int j = j0 + lane;
     int r = j < k ? token_row[t * k + j] : -1;
+    MOE_CHECK(r < routed_end, CK_COMBINE_ROW);
     if (r >= routed_end) r = -1;
     const float g = j < k ? topk_w[t * k + j] : 0.f;
     const uint32_t m = __ballot_sync(0xffffffffu, r >= 0);
@@ -53,7 +54,10 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
   }
   __syncwarp();
   const int64_t nv = d / V;
-  for (int64_t c0 = lane; c0 < nv; c0 += 32 * CB) {
+  // few tokens (decode): the columns are split over gridDim.y blocks per token group
+  const int64_t per = (nv + gridDim.y - 1) / gridDim.y;
+  const int64_t c_end = min(nv, per * (blockIdx.y + 1));
+  for (int64_t c0 = per * blockIdx.y + lane; c0 < c_end; c0 += 32 * CB) {
     float acc[CB][V];
 #pragma unroll
     for (int b = 0; b < CB; ++b)
@@ -70,8 +74,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
 #pragma unroll
       for (int b = 0; b < CB; ++b) {
         const int64_t c = c0 + 32 * b;
-        q0[b] = c < nv ? __ldg(row0 + c) : make_uint4(0, 0, 0, 0);
-        q1[b] = (two && c < nv) ? __ldg(row1 + c) : make_uint4(0, 0, 0, 0);
+        q0[b] = c < c_end ? __ldg(row0 + c) : make_uint4(0, 0, 0, 0);
+        q1[b] = (two && c < c_end) ? __ldg(row1 + c) : make_uint4(0, 0, 0, 0);
       }
       const float g0 = __int_as_float(rg0.y), g1 = __int_as_float(rg1.y);
 #pragma unroll
@@ -94,7 +98,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
 #pragma unroll
     for (int b = 0; b < CB; ++b) {
       const int64_t c = c0 + 32 * b;
-      if (c < nv) Vec16<T>::store(y + t * d + c * V, acc[b]);
+      if (c < c_end) Vec16<T>::store(y + t * d + c * V, acc[b]);
     }
   }
 }
@@ -117,6 +121,13 @@ cudaError_t launch_combine(const moe_config& c, const void* Yp, const int32_t* t
                            cudaStream_t s) {
   if (c.T == 0) return cudaSuccess;
   const unsigned blocks = unsigned(ceil_div(c.T, kCombineWarps));
+  // few tokens: split each token's columns into chunks of at least one
+  // warp pass (32 lanes x 4 x 16 bytes), until there are about eight warps per SM
+  const int64_t vec = c.dtype == MOE_F32 ? 4 : 8;
+  const int64_t passes = ceil_div(c.d_model / vec, 32 * 4);
+  int64_t split = ceil_div(148 * 8, int64_t(blocks) * kCombineWarps);
+  if (split > passes) split = passes;
+  if (split < 1) split = 1;
   const int hs = c.d_ff_shared > 0 ? 1 : 0;
   const size_t smem = size_t(kCombineWarps) * size_t(c.top_k + 1) * sizeof(int2);
   auto go = [&](auto kern, auto* Yt, auto* yt) -> cudaError_t {
@@ -125,7 +136,8 @@ cudaError_t launch_combine(const moe_config& c, const void* Yp, const int32_t* t
           cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
       if (e != cudaSuccess) return e;
     }
-    return launch_pdl(kern, dim3(blocks), dim3(kCombineWarps * 32), smem, s, Yt, token_row,
+    return launch_pdl(kern, dim3(blocks, unsigned(split)), dim3(kCombineWarps * 32), smem, s,
+                      Yt, token_row,
                       topk_w, offsets, int(c.T), int(c.top_k), int(c.n_experts), hs,
                       c.d_model, yt);
   };
@@ -148,5 +160,7 @@ cudaError_t launch_load_stats(const moe_config& c, const float* prob_partials,
                     int(c.n_experts), int(c.T), counts, kept, mean_prob, balance, dropped,
                     cv_squared);
 }
+
+MOE_CHECKS_UNIT(combine)
 
 }  // namespace moe

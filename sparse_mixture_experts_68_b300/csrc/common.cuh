@@ -188,4 +188,66 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+// ---- optional device-side checks (a build with -DMOE_CHECKS) ----------------
+//
+// MOE_CHECK(cond, site) guards an index before the access it controls.  In a
+// checks build a failed check counts itself in its translation unit's record
+// and the first one also records the site, the source line and the block;
+// nothing traps, and the kernel carries on (the accesses stay bounded as in
+// the ordinary build).  moe_checks_read gathers and clears every unit's
+// record.  In the ordinary build the checks compile to nothing.
+struct CheckRecord {
+  int32_t fails, site, line, block;
+};
+
+enum CheckSite {
+  CK_ROUTER_TOPK = 1,    // a selected expert outside [0, N)
+  CK_SORT_EXPERT = 2,    // an expert id outside [0, N) reached the permutation
+  CK_COPY_TOKEN = 3,     // a grouped row names a token outside [-1, T)
+  CK_ROWS_TOTAL = 4,     // the grouped layout ends past rows_max
+  CK_COMBINE_ROW = 5,    // a kept slot's row lies outside the routed groups
+  CK_GEMM_ROWS = 6,      // a grouped Linear's group reaches past rows_max
+  CK_EC_PICK = 7,        // an expert-choice pick outside [0, T)
+};
+
+#ifdef MOE_CHECKS
+static __device__ CheckRecord g_tu_checks = {0, 0, 0, 0};
+
+static __device__ __noinline__ void check_fail(int site, int line) {
+  if (atomicAdd(&g_tu_checks.fails, 1) == 0) {
+    g_tu_checks.site = site;
+    g_tu_checks.line = line;
+    g_tu_checks.block = int32_t(blockIdx.x);
+  }
+}
+#define MOE_CHECK(cond, site)                                   \
+  do {                                                          \
+    if (!(cond)) ::moe::check_fail(int(site), __LINE__);        \
+  } while (0)
+
+// Host side: this unit's record (then cleared when `clear`).
+inline cudaError_t read_tu_checks(CheckRecord* out, bool clear) {
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_tu_checks, sizeof(CheckRecord));
+  if (e == cudaSuccess && clear) {
+    const CheckRecord zero = {0, 0, 0, 0};
+    e = cudaMemcpyToSymbol(g_tu_checks, &zero, sizeof(CheckRecord));
+  }
+  return e;
+}
+#else
+#define MOE_CHECK(cond, site) \
+  do {                        \
+  } while (0)
+inline cudaError_t read_tu_checks(CheckRecord* out, bool) {
+  *out = CheckRecord{0, 0, 0, 0};
+  return cudaSuccess;
+}
+#endif
+
+// Defines checks_read_<unit>(), the reader of one translation unit's record.
+#define MOE_CHECKS_UNIT(unit)                                              \
+  cudaError_t checks_read_##unit(::moe::CheckRecord* out, bool clear) {    \
+    return ::moe::read_tu_checks(out, clear);                              \
+  }
+
 }  // namespace moe

@@ -180,6 +180,7 @@ __global__ void __launch_bounds__(kSelThreads)
       const int64_t slot = int64_t(t) * N + e;
       if (take[j] && pos < C) {                  // exactly C are taken; the bound is a guard
         const float pv = __uint_as_float(kv[j]);
+        MOE_CHECK(t >= 0 && t < T, CK_EC_PICK);
         ec_token[int64_t(e) * C + pos] = t;
         ec_gate[int64_t(e) * C + pos] = pv;
         row_token[base + pos] = t;
@@ -243,5 +244,7 @@ cudaError_t launch_ec_stats(const moe_config& c, const float* prob_partials,
                     int(c.n_experts), int(c.T), counts, picks, mean_prob, balance, scratch,
                     unpicked);
 }
+
+MOE_CHECKS_UNIT(expert_choice)
 
 }  // namespace moe

@@ -577,4 +577,6 @@ cudaError_t launch_bwd_wgrad(const moe_config& c, const BwdGemmArgs& g, const vo
                                                s);
 }
 
+MOE_CHECKS_UNIT(grouped_bwd)
+
 }  // namespace moe

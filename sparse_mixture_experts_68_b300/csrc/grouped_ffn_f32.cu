@@ -95,4 +95,6 @@ cudaError_t launch_bwd_wgrad_f32(const moe_config& c, const BwdGemmArgs& g, cons
                     dim3(kSimtThreads), 0, s, a);
 }
 
+MOE_CHECKS_UNIT(grouped_ffn_f32)
+
 }  // namespace moe

@@ -99,6 +99,7 @@ struct TcParams {
   int32_t num_kb;                  // K / BK
   int32_t* status;
   uint64_t wait_limit_ns;
+  int64_t rows_total;              // rows of the grouped buffers (device checks; 0: unknown)
   // decode tiles, stream-K (both nullptr: whole tiles): [kSkMaxCtas][2][NB][128]
   // fp32 partial accumulators and one counter per tile, 0 at launch
   float* sk_partials;
@@ -467,6 +468,9 @@ __global__ void __launch_bounds__(CFG::THREADS, MINB)
       tc_fence_after();
       const bool routed = tc.g < p.n_routed;
       const int live = p.offsets ? (routed ? p.kept[tc.g] : p.shared_rows) : p.dense_rows;
+      if (warp == 2 && lane == 0)
+        MOE_CHECK(p.rows_total == 0 || int64_t(grp_off[tc.g]) + live <= p.rows_total,
+                  CK_GEMM_ROWS);
       const int row_in_group = tc.m * BM + q * 32 + lane;
       const bool valid = row_in_group < live;
       const int64_t out_row = int64_t(grp_off[tc.g]) + row_in_group;
@@ -815,6 +819,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CFG::THREADS, 1)
       tc_fence_after();
       const bool routed = tc.g < p.n_routed;
       const int live = p.offsets ? (routed ? p.kept[tc.g] : p.shared_rows) : p.dense_rows;
+      if (warp == 2 && lane == 0)
+        MOE_CHECK(p.rows_total == 0 || int64_t(grp_off[tc.g]) + live <= p.rows_total,
+                  CK_GEMM_ROWS);
       const int row_in_group = tc.m * BM2 + int(rank) * 128 + q * 32 + lane;
       const bool valid = row_in_group < live;
       const int64_t out_row = int64_t(grp_off[tc.g]) + row_in_group;
@@ -1103,6 +1110,9 @@ __global__ void __launch_bounds__(6 * 32, 1)
       tc_fence_after();
       const bool routed = tc.g < p.n_routed;
       const int live = routed ? p.kept[tc.g] : p.shared_rows;
+      if (warp == 2 && lane == 0)
+        MOE_CHECK(p.rows_total == 0 || int64_t(grp_off[tc.g]) + live <= p.rows_total,
+                  CK_GEMM_ROWS);
       const int feat = tc.n * kFeat + fl;
       const __nv_bfloat16* bias = routed ? p.bias + int64_t(tc.g) * p.Nd : p.bias_s;
       const float b = __bfloat162float(bias[feat]);
@@ -1427,6 +1437,7 @@ cudaError_t grouped_linear(const moe_config& c, const GroupedFfnArgs& g, const v
     p.num_kb = int32_t(K / BK);
     p.status = g.status;
     p.wait_limit_ns = g.wait_limit_ns;
+    p.rows_total = g.rows_max;
     const int64_t max_tiles = pl.max_tiles;
     int grid = int(max_tiles < g.num_sms ? max_tiles : g.num_sms);
     if (pl.sk) {
@@ -1466,6 +1477,7 @@ cudaError_t grouped_linear(const moe_config& c, const GroupedFfnArgs& g, const v
   p.status = g.status;
   p.wait_limit_ns = g.wait_limit_ns;
   p.out_pre = out_pre;
+  p.rows_total = g.rows_max;
   // upper bound on the tiles (every group may add one partial m-tile)
   const int64_t max_tiles =
       (ceil_div(g.rows_max, tile_rows(choice)) + groups) * (Nd / bn);
@@ -1644,5 +1656,7 @@ cudaError_t launch_router_logits_tc(const moe_config& c, const void* x, const vo
   const int grid = int(tiles < num_sms ? tiles : num_sms);
   return launch_tc<Cfg64, EPI_BIAS_F32>(mA, mB, mB, p, grid, s);
 }
+
+MOE_CHECKS_UNIT(grouped_ffn)
 
 }  // namespace moe

@@ -158,6 +158,16 @@ size_t sk_partial_bytes(const moe_config& c);
 bool linear_saves_pre(const moe_config& c);
 // Unique id of the calling thread's current CUDA context (0: none current).
 uint64_t context_id();
+// Device-check records of each translation unit (zeros in the ordinary build).
+struct CheckRecord;
+cudaError_t checks_read_router(CheckRecord* out, bool clear);
+cudaError_t checks_read_permute(CheckRecord* out, bool clear);
+cudaError_t checks_read_combine(CheckRecord* out, bool clear);
+cudaError_t checks_read_expert_choice(CheckRecord* out, bool clear);
+cudaError_t checks_read_backward(CheckRecord* out, bool clear);
+cudaError_t checks_read_grouped_bwd(CheckRecord* out, bool clear);
+cudaError_t checks_read_grouped_ffn_f32(CheckRecord* out, bool clear);
+cudaError_t checks_read_grouped_ffn(CheckRecord* out, bool clear);
 // Kernel (and tile) of grouped Linear 1 or 2 for this layer; routed_rows 0: T * top_k.
 const char* grouped_linear_kernel_name(const moe_config& c, int linear, int64_t routed_rows);
 

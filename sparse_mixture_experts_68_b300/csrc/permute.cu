@@ -51,6 +51,7 @@ __global__ void __launch_bounds__(256)
   const int64_t a1 = min(int64_t(T) * k, a0 + int64_t(kPermuteTokensPerBlock) * k);
   for (int64_t a = a0 + threadIdx.x; a < a1; a += blockDim.x) {
     const int e = topk_idx[a];
+    MOE_CHECK(e >= 0 && e < N, CK_SORT_EXPERT);
     if (e >= 0 && e < N) atomicAdd(&cnt[e], 1);  // out-of-range experts are not counted
   }
   __syncthreads();
@@ -130,6 +131,7 @@ __global__ void __launch_bounds__(32)
     const int64_t a = base + lane;
     const int e = a < a1 ? topk_idx[a] : -1;
     const bool valid = e >= 0 && e < N;          // out-of-range experts: dropped
+    MOE_CHECK(a >= a1 || valid, CK_SORT_EXPERT);
     const int key = valid ? e : (0x40000000 | lane);     // invalid lanes match nobody
     const uint32_t same = __match_any_sync(0xffffffffu, key);
     int32_t rank = 0;
@@ -179,7 +181,10 @@ __global__ void __launch_bounds__(kSortWarps * 32)
   for (int i = threadIdx.x; i < kSortWarps * N; i += blockDim.x) cnt[i] = 0;
   {
     // stage the expert ids: 16-byte loads, four in flight per thread
-    auto clamp = [N](int e) { return int16_t((e >= 0 && e < N) ? e : -1); };  // out of range: dropped
+    auto clamp = [N](int e) {                    // out of range: dropped
+      MOE_CHECK(e >= 0 && e < N, CK_SORT_EXPERT);
+      return int16_t((e >= 0 && e < N) ? e : -1);
+    };
     const int A4 = A / 4;
     const int4* src = reinterpret_cast<const int4*>(topk_idx);
     int i = threadIdx.x;
@@ -342,7 +347,7 @@ __global__ void __launch_bounds__(256)
     permute_copy_kernel(const T* __restrict__ x, int64_t d, int Ttok, int N,
                         const int32_t* __restrict__ offsets,
                         const int32_t* __restrict__ row_token, T* __restrict__ Xp,
-                        int32_t* __restrict__ zero, int64_t n_zero) {
+                        int32_t* __restrict__ zero, int64_t n_zero, int64_t rows_max) {
   pdl_launch_dependents();
   pdl_wait_previous();
   // counters the next kernels count up from zero (the grouped FFN's split tiles)
@@ -351,6 +356,7 @@ __global__ void __launch_bounds__(256)
     zero[i] = 0;
   const int lane = threadIdx.x & 31;
   const int64_t routed_end = offsets[N], total = offsets[N + 1];
+  if (blockIdx.x == 0 && threadIdx.x == 0) MOE_CHECK(total <= rows_max, CK_ROWS_TOTAL);
   const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
   constexpr int V = Vec16<T>::n;
   for (int64_t r = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); r < total;
@@ -362,6 +368,7 @@ __global__ void __launch_bounds__(256)
       t = r - routed_end;
       if (t >= Ttok) t = -1;
     }
+    MOE_CHECK(t >= -1 && t < Ttok, CK_COPY_TOKEN);
     if (t < 0 || t >= Ttok) continue;             // padding row (or no such token)
     const uint4* src = reinterpret_cast<const uint4*>(x + t * d);
     uint4* dst = reinterpret_cast<uint4*>(Xp + r * d);
@@ -398,10 +405,10 @@ cudaError_t launch_copy(const moe_config& c, const void* x, const int32_t* offse
   if (c.dtype == MOE_F32)
     return launch_pdl(permute_copy_kernel<float>, dim3(blocks), dim3(256), 0, s,
                       static_cast<const float*>(x), c.d_model, T, N, offsets, row_token,
-                      static_cast<float*>(Xp), zero, n_zero);
+                      static_cast<float*>(Xp), zero, n_zero, rows_max);
   return launch_pdl(permute_copy_kernel<__nv_bfloat16>, dim3(blocks), dim3(256), 0, s,
                     static_cast<const __nv_bfloat16*>(x), c.d_model, T, N, offsets,
-                    row_token, static_cast<__nv_bfloat16*>(Xp), zero, n_zero);
+                    row_token, static_cast<__nv_bfloat16*>(Xp), zero, n_zero, rows_max);
 }
 
 }  // namespace
@@ -521,3 +528,7 @@ extern "C" moe_status moe_permute_noalloc(const moe_config* cfg, const void* x,
                                        static_cast<cudaStream_t>(stream), nullptr, nullptr, 0);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
+
+namespace moe {
+MOE_CHECKS_UNIT(permute)
+}  // namespace moe

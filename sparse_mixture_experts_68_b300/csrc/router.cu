@@ -5,6 +5,7 @@
 // section "Code", for gates without renormalisation).
 #include <float.h>
 
+#include "common.cuh"
 #include "kernels.h"
 #include "simt_gemm.cuh"
 
@@ -106,6 +107,7 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
       if ((be & 31) == lane) taken |= 1u << (be >> 5);
       const float g = expf(bv - m);              // m is the largest score: slot 0's
       kept_sum += g;
+      if (lane == 0) MOE_CHECK(be >= 0 && be < N, CK_ROUTER_TOPK);
       if (lane == (j & 31)) { my_e = be; my_g = g; }   // slot j is held by lane j % 32
       if (k > 32 && ((j & 31) == 31 || j == k - 1)) {  // k > 32: flush 32 slots at a time
         const int j0 = j & ~31;
@@ -319,6 +321,7 @@ __global__ void __launch_bounds__(kRouterWarps * 32, WF32 ? 2 : 1)
       if (be >= e0 && be < e0 + NPL) taken |= 1u << (be - e0);
       const float g = expf(bv - m);
       kept_sum += g;
+      if (lane == 0) MOE_CHECK(be >= 0 && be < N, CK_ROUTER_TOPK);
       if (lane == (j & 31)) { my_e = be; my_g = g; }   // slot j is held by lane j % 32
       if (k > 32 && ((j & 31) == 31 || j == k - 1)) {  // k > 32: flush 32 slots at a time
         const int j0 = j & ~31;
@@ -495,5 +498,7 @@ cudaError_t launch_router_probs(const moe_config& c, const void* x, const void* 
   return launch_router_softmax_topk(c, 0, logits, nullptr, nullptr, prob_partials, probT,
                                     picks, s);
 }
+
+MOE_CHECKS_UNIT(router)
 
 }  // namespace moe

@@ -203,3 +203,30 @@ def test_ffn_kernel_names_follow_the_layer_shape():
     assert "simt_gemm_kernel" in name("c0_pr1_fp32", 1)
     cfg = B.make_config(WORKLOADS["c1_page1_bf16"])
     assert B.lib().moe_ffn_kernel_name(C.byref(cfg), 3) is None
+
+
+def test_checks_build_flags_and_workspace_guards():
+    """The ordinary build reports no checks and no guard gaps; the checks
+    build (when built) reports both, with the gaps inside the workspace."""
+    from sparse_mixture_experts_68_b300.workloads import WORKLOADS
+    lib = B.lib()
+    assert lib.moe_build_flags() == 0 or os.environ.get("MOE_LIBRARY") == "checks"
+    path = os.path.join(os.path.dirname(B.LIB_PATH), "libmoe_checks.so")
+    if not os.path.exists(path):
+        pytest.skip("libmoe_checks.so not built")
+    chk = C.CDLL(path)
+    chk.moe_build_flags.restype = C.c_int32
+    chk.moe_workspace_guards.restype = C.c_int32
+    chk.moe_workspace_guards.argtypes = [C.POINTER(B.MoeConfig), C.c_void_p, C.c_int32]
+    chk.moe_workspace_size.restype = C.c_size_t
+    chk.moe_workspace_size.argtypes = [C.POINTER(B.MoeConfig)]
+    assert chk.moe_build_flags() == B.MOE_BUILD_CHECKS
+    cfg = B.make_config(WORKLOADS["c1_page1_bf16"])
+    n = chk.moe_workspace_guards(C.byref(cfg), None, 0)
+    assert n >= 8
+    buf = (C.c_int64 * n)()
+    chk.moe_workspace_guards(C.byref(cfg), buf, n)
+    size = chk.moe_workspace_size(C.byref(cfg))
+    offs = list(buf)
+    assert offs == sorted(offs) and offs[-1] + B.GUARD_BYTES <= size
+    assert lib.moe_workspace_guards(C.byref(cfg), None, 0) == 0
