@@ -90,25 +90,23 @@ KERNEL_SOURCES = ("sparse_mixture_experts_68_b300/csrc/grouped_ffn_sm103.cu",
                   "sparse_mixture_experts_68_b300/csrc/tc_common.cuh")
 
 
-def profiled_traffic(workload):
-    """(bytes per launch, summary path) from profiles/*_<workload>.md when the
-    kernel sources still hash to the summary's source_sha256, else (None, why)."""
+def kernel_sources_sha256():
     import hashlib
-    for kind in ("grouped_gemm", "swap_gemm"):
-        path = os.path.join(ROOT, "profiles", f"{kind}_{workload}.md")
-        if not os.path.exists(path):
-            continue
-        fields = {}
-        for line in open(path):
-            if ":" in line and line.split(":")[0] in ("traffic_bytes_per_launch", "source_sha256"):
-                k, v = line.split(":", 1)
-                fields[k.strip()] = v.strip()
-        sha = hashlib.sha256(b"".join(open(os.path.join(ROOT, f), "rb").read()
-                                      for f in KERNEL_SOURCES)).hexdigest()
-        if fields.get("source_sha256") != sha:
-            return None, f"profiles/{kind}_{workload}.md predates the current kernel sources"
-        return float(fields["traffic_bytes_per_launch"]), f"profiles/{kind}_{workload}.md"
-    return None, "no ncu summary for this workload"
+    return hashlib.sha256(b"".join(open(os.path.join(ROOT, f), "rb").read()
+                                   for f in KERNEL_SOURCES)).hexdigest()
+
+
+def profiled_traffic(workload):
+    """(DRAM bytes per launch of the grouped FFN, source) from the machine-readable
+    ncu summary profiles/ffn_<workload>.json, when the kernel sources still hash
+    to its source_sha256; else (None, why)."""
+    path = os.path.join(ROOT, "profiles", f"ffn_{workload}.json")
+    if not os.path.exists(path):
+        return None, "no ncu summary for this workload"
+    rec = json.load(open(path))
+    if rec.get("source_sha256") != kernel_sources_sha256():
+        return None, f"profiles/ffn_{workload}.json predates the current kernel sources"
+    return float(rec["traffic_bytes_per_launch"]), f"profiles/ffn_{workload}.json"
 
 
 # ---------------------------------------------------------------------------------------
