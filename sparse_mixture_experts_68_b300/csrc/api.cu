@@ -519,11 +519,6 @@ static moe_status forward_impl(const moe_config* cfg, const void* x, const moe_w
 
   const NvtxRange call_range("moe_forward");
   cudaError_t e = record_event(ev[0], s);
-  if (e == cudaSuccess && c.dtype != MOE_F32) {
-    // decode layers: HBM is idle during the routing, so warm L2 with the
-    // first Linear's weights (prefetch only; the router starts at once)
-    e = launch_decode_prefetch(c, w, di.num_sms, s);
-  }
   if (e == cudaSuccess) {
     const NvtxRange r("router_topk");
     e = launch_router(c, x, w->W_g, w->b_g, logits, out->topk_idx, out->topk_w,
@@ -589,8 +584,8 @@ int32_t moe_forward_launch_count(const moe_config* cfg) {
   if (check_config(cfg) != MOE_OK) return -1;
   const moe_config& c = *cfg;
   const int ffn = rows_max_of(c) > 0 ? 2 : 0;
-  return decode_prefetch_launches(c) + router_launch_count(c) + permute_launch_count(c) + ffn +
-         (c.T > 0 ? 1 : 0) + (permute_fuses_stats(c) ? 0 : 1);
+  return router_launch_count(c) + permute_launch_count(c) + ffn + (c.T > 0 ? 1 : 0) +
+         (permute_fuses_stats(c) ? 0 : 1);
 }
 
 const char* moe_ffn_kernel_name(const moe_config* cfg, int32_t linear) {

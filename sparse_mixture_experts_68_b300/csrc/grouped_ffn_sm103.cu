@@ -1180,34 +1180,6 @@ __global__ void __launch_bounds__(6 * 32, 1)
   }
 }
 
-// ---- decode: warm L2 with the first Linear's weights while the routing runs ----------
-//
-// Launched first in moe_forward when the first Linear runs the decode tiles.
-// Block b issues L2 prefetches (TMA, no shared memory) of the first
-// kDecodePrefetchKb weight boxes that CTA b of the stream-K first Linear will
-// stream if every routed expert holds 1..NB tokens (the usual decode case:
-// one tile row per expert), then exits.  HBM is otherwise idle during the
-// router, the sort and the row copy; a wrong guess only spends that idle
-// bandwidth.
-
-constexpr int kDecodePrefetchKb = 40;           // 40 x 16 KB per CTA: ~95 MB over 148 CTAs
-
-__global__ void __launch_bounds__(32)
-    decode_prefetch_kernel(const __grid_constant__ CUtensorMap tmW, int n_routed, int ntiles,
-                           int num_kb) {
-  pdl_launch_dependents();
-  if (threadIdx.x != 0) return;
-  const int guess_tiles = n_routed * ntiles;
-  const int64_t units = int64_t(guess_tiles) * num_kb;
-  SegIter it(true, blockIdx.x, gridDim.x, guess_tiles, num_kb,
-             (units + gridDim.x - 1) / gridDim.x);
-  int left = kDecodePrefetchKb, tile, kb0, kb1;
-  while (left > 0 && it.next(tile, kb0, kb1)) {
-    const int g = tile / ntiles, f0 = (tile - g * ntiles) * 128;
-    for (int kb = kb0; kb < kb1 && left > 0; ++kb, --left) tma_prefetch_3d(&tmW, kb * BK, f0, g);
-  }
-}
-
 // ---- host side -----------------------------------------------------------------------
 
 // bf16 tensor [outer, inner] (or [z, outer, inner]) read in boxes of
@@ -1492,22 +1464,6 @@ cudaError_t launch_grouped_linear_bf16(const moe_config& c, const GroupedFfnArgs
                                        int64_t K, int64_t Nd, cudaStream_t s) {
   if (g.rows_max == 0) return cudaSuccess;
   return grouped_linear(c, g, A, W, Ws, bias, bias_s, out, K, Nd, EPI_BIAS, s);
-}
-
-cudaError_t launch_decode_prefetch(const moe_config& c, const moe_weights* w, int num_sms,
-                                   cudaStream_t s) {
-  const LinearPlan pl = plan_forward_linear(c, 1);
-  if (c.dtype == MOE_F32 || pl.nb == 0 || c.T == 0) return cudaSuccess;
-  CUtensorMap mW;
-  if (!make_map(&mW, w->W1, uint64_t(c.d_model), uint64_t(c.d_ff), uint64_t(c.n_experts), 128))
-    return cudaErrorInvalidValue;
-  const int grid = num_sms < kSkMaxCtas ? num_sms : kSkMaxCtas;   // the first Linear's grid
-  return launch_pdl(decode_prefetch_kernel, dim3(grid), dim3(32), 0, s, mW,
-                    int(c.n_experts), int(c.d_ff / 128), int(c.d_model / BK));
-}
-
-int decode_prefetch_launches(const moe_config& c) {
-  return c.dtype != MOE_F32 && c.T > 0 && plan_forward_linear(c, 1).nb > 0 ? 1 : 0;
 }
 
 bool bwd_dgrad_on_pair(const moe_config& c, int64_t K, int64_t Nd) {

@@ -147,11 +147,7 @@ struct GroupedFfnArgs {
 // 1 or 2 (0 when that Linear runs whole tiles), and the partial-accumulator
 // bytes (0 when neither runs stream-K).
 int64_t sk_counter_ints(const moe_config& c, int linear);
-// moe_forward's decode layers: L2 prefetch of the first Linear's weights,
-// launched before the router (no-op and 0 launches otherwise)
-cudaError_t launch_decode_prefetch(const moe_config& c, const moe_weights* w, int num_sms,
-                                   cudaStream_t s);
-int decode_prefetch_launches(const moe_config& c);
+
 size_t sk_partial_bytes(const moe_config& c);
 // whether the bf16 first Linear stores its pre-activation from its epilogue
 // (else a second pass does)
