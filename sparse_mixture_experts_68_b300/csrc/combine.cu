@@ -21,7 +21,7 @@ namespace {
 constexpr int kCombineWarps = 8;
 
 template <typename T>
-__global__ void __launch_bounds__(kCombineWarps * 32)
+__global__ void __launch_bounds__(kCombineWarps * 32, 4)   // 4 blocks per SM: latency-bound gathers
     combine_kernel(const T* __restrict__ Yp, const int32_t* __restrict__ token_row,
                    const float* __restrict__ topk_w, const int32_t* __restrict__ offsets,
                    int Ttok, int k, int N, int has_shared, int64_t d, T* __restrict__ y) {
