@@ -98,6 +98,16 @@ WORKLOADS = {
         router_scale=3.0, seed=4,
         description="T=4096, d=7168, 256 routed experts d_ff=2048 + 1 shared, "
                     "top-8, GELU, router weights x3, bf16"),
+    # the DeepSeek-V3-sized layer at a quarter of its experts and tokens (same
+    # d, d_ff, top-8 and ~128-row groups; 3.7 GB of weights): a case small
+    # enough for an ncu capture of many passes, its DRAM traffic scaled by the
+    # experts to the full layer
+    "c4_deepseek_v3_quarter": Workload(
+        "c4_deepseek_v3_quarter", T=1024, d_model=7168, d_ff=2048, n_experts=64,
+        top_k=8, act=ACT_GELU_ERF, dtype=DT_BF16, d_ff_shared=2048, router_scale=3.0,
+        seed=4,
+        description="T=1024, d=7168, 64 routed experts d_ff=2048 + 1 shared, top-8, "
+                    "GELU, router weights x3, bf16"),
     # expert-choice routing (matteuscruz.github.io "Load balancing": every
     # expert picks its top tokens) at the same expert work as top-k routing:
     # C = ceil(k * T / N) tokens per expert
