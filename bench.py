@@ -9,10 +9,12 @@ tokens, through the library's C ABI.  Prints one JSON line (rank 0).
 
 Timing: W untimed warm-up steps, then K timed steps between a barrier and a
 device synchronise on both sides; each step is bracketed by CUDA events on the
-launching stream, with L2 flushed (a 512 MiB buffer written) before every
-step, outside the events.  Multi-GPU (torchrun): every rank runs its own
-replica of the layer on its own GPU (data parallel, no exchange); the time is
-the max over ranks and the value counts every rank's tokens.
+launching stream, with L2 flushed before every step, outside the events: a
+512 MiB buffer is written, then a separate 384 MiB buffer is read, so that the
+flush's own dirty lines are written back before the step starts.  Multi-GPU
+(torchrun): every rank runs its own replica of the layer on its own GPU (data
+parallel, no exchange); the time is the max over ranks and the value counts
+every rank's tokens.
 
 The headline line times the Mixtral-sized prefill layer (T=4096, d=4096,
 d_ff=14336, 8 experts, top-2).  The same run adds ``per_workload``: full
@@ -47,6 +49,26 @@ TRAIN_METRIC = ("MoE-layer training tokens/s (forward + backward of task + 0.01 
                 "on 1 B300")
 AUX_WEIGHT = 0.01
 L2_FLUSH_BYTES = 512 << 20
+L2_FLUSH_READ_BYTES = 384 << 20
+
+
+class L2Flush:
+    """Evicts the layer's data from L2 between steps, outside the timed events:
+    a write of L2_FLUSH_BYTES, then a read of L2_FLUSH_READ_BYTES from another
+    buffer.  The write alone would leave L2 full of the flush's dirty lines,
+    whose write-back to HBM would then fall inside the next timed step."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+        self.r = torch.ones(L2_FLUSH_READ_BYTES // 4, dtype=torch.int32, device=dev)
+        self.acc = torch.empty((), dtype=torch.int64, device=dev)
+
+    def __call__(self, i, stream):
+        import torch
+        with torch.cuda.stream(stream):
+            self.w.fill_(i)
+            torch.sum(self.r, dtype=torch.int64, out=self.acc)
 
 
 def parse():
@@ -289,7 +311,8 @@ def run_config(wl, world, train=False):
     """The `config` object of a line: the same for both arms."""
     cfg = {"workload": wl.name, "description": wl.description, "T": wl.T,
            "parallelism": f"replicas{world}" if world > 1 else "single",
-           "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write)"}
+           "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB written, then "
+                 f"{L2_FLUSH_READ_BYTES >> 20} MiB of another buffer read)"}
     if train:
         cfg["aux_weight"] = AUX_WEIGHT
     return cfg
@@ -381,7 +404,7 @@ def run_ours(args, wl, rank, world, local_rank, cpu_budget_s=None):
     calls = LayerCalls(wl, tensors, dev)
     layer = calls.layer
     x = tensors["x"]
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    flush = L2Flush(dev)
     # The inputs and buffers come from torch's current stream, the layer runs on
     # its own stream: let every producer finish (torch may hand out memory that
     # a still-running kernel of the current stream is writing) before the first call.
@@ -405,8 +428,7 @@ def run_ours(args, wl, rank, world, local_rank, cpu_budget_s=None):
     torch.cuda.synchronize(dev)
 
     def flush_l2(i):
-        with torch.cuda.stream(stream):
-            flush.fill_(i)                  # L2 flush, outside the timed events
+        flush(i, stream)                    # L2 flush, outside the timed events
 
     for i in range(max(args.warmup, 3)):
         flush_l2(i)
@@ -564,7 +586,7 @@ def run_train(args, wl, rank, world, local_rank, cpu_budget_s=None):
     g = torch.Generator(device="cpu").manual_seed(7)
     dy = torch.randn((wl.T, wl.d_model), generator=g).to(torch.bfloat16).to(dev)
     x = tensors["x"]
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    flush = L2Flush(dev)
     torch.cuda.synchronize(dev)          # see run_ours: the layer runs on its own stream
     stream = torch.cuda.Stream(dev)
     fev = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
@@ -593,8 +615,7 @@ def run_train(args, wl, rank, world, local_rank, cpu_budget_s=None):
     torch.cuda.synchronize(dev)
 
     def flush_l2(i):
-        with torch.cuda.stream(stream):
-            flush.fill_(i)
+        flush(i, stream)
 
     for i in range(max(args.warmup, 3)):
         flush_l2(i)
