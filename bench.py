@@ -68,7 +68,7 @@ class L2Flush:
         import torch
         with torch.cuda.stream(stream):
             self.w.fill_(i)
-            torch.sum(self.r, dtype=torch.int64, out=self.acc)
+            torch.sum(self.r, dim=0, dtype=torch.int64, out=self.acc)
 
 
 def parse():
