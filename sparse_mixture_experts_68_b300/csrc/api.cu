@@ -72,6 +72,7 @@ struct Workspace {
   void* Xp;
   void* H;
   void* Yp;
+  float* front_part;      // small-batch front end: router score slices (or nullptr)
   float* sk_partials;     // stream-K decode tiles (nullptr when the layer has none)
   int32_t* sk_counters;
   int64_t sk_counter_ints;
@@ -113,6 +114,8 @@ Workspace layout(const moe_config& c, void* base) {
   w.Xp = take(size_t(rows * c.d_model * es));
   w.H = take(size_t(rows * c.d_ff * es));
   w.Yp = take(size_t(rows * c.d_model * es));
+  const int64_t fp = small_front_partial_floats(c);
+  if (fp > 0) w.front_part = static_cast<float*>(take(size_t(fp) * 4));
   const size_t skp = sk_partial_bytes(c);
   if (skp > 0) {
     w.sk_counter_ints = sk_counter_ints(c, 1) + sk_counter_ints(c, 2);
@@ -518,22 +521,35 @@ static moe_status forward_impl(const moe_config* cfg, const void* x, const moe_w
   void* const* ev = events ? events : none;
 
   const NvtxRange call_range("moe_forward");
+  // a few tokens and experts: router, sort and statistics in the two
+  // front-end kernels, then the row copy
+  const bool front = ws.front_part != nullptr;
   cudaError_t e = record_event(ev[0], s);
   if (e == cudaSuccess) {
     const NvtxRange r("router_topk");
-    e = launch_router(c, x, w->W_g, w->b_g, logits, out->topk_idx, out->topk_w,
-                      ws.prob_partials, di.num_sms, di.status, g_wait_limit_ns.load(), s);
+    if (front)
+      e = launch_small_front(c, x, w->W_g, w->b_g, ws.front_part, logits, out->topk_idx,
+                             out->topk_w, out->counts, out->kept, ws.offsets, ws.row_token,
+                             ws.token_row, out->mean_prob, out->balance, out->dropped,
+                             out->cv_squared, s);
+    else
+      e = launch_router(c, x, w->W_g, w->b_g, logits, out->topk_idx, out->topk_w,
+                        ws.prob_partials, di.num_sms, di.status, g_wait_limit_ns.load(), s);
   }
   if (e == cudaSuccess) e = record_event(ev[1], s);
   // small layers: the one-block permutation also computes the load statistics
-  const bool fused_stats = permute_fuses_stats(c);
+  const bool fused_stats = front || permute_fuses_stats(c);
   const StatsArgs stats{ws.prob_partials, int(router_blocks_of(c)), out->mean_prob,
                         out->balance, out->dropped, out->cv_squared};
   if (e == cudaSuccess) {
     const NvtxRange r("permute");
-    e = launch_permute(c, x, out->topk_idx, out->counts, out->kept, ws.offsets, ws.row_token,
-                       ws.token_row, ws.Xp, ws.scratch, rows_max_of(c), s,
-                       fused_stats ? &stats : nullptr, ws.sk_counters, ws.sk_counter_ints);
+    if (front)
+      e = launch_row_copy(c, x, ws.offsets, ws.row_token, ws.Xp, rows_max_of(c), s,
+                          ws.sk_counters, ws.sk_counter_ints);
+    else
+      e = launch_permute(c, x, out->topk_idx, out->counts, out->kept, ws.offsets,
+                         ws.row_token, ws.token_row, ws.Xp, ws.scratch, rows_max_of(c), s,
+                         fused_stats ? &stats : nullptr, ws.sk_counters, ws.sk_counter_ints);
   }
   if (e == cudaSuccess) e = record_event(ev[2], s);
   if (e == cudaSuccess) {
@@ -584,6 +600,7 @@ int32_t moe_forward_launch_count(const moe_config* cfg) {
   if (check_config(cfg) != MOE_OK) return -1;
   const moe_config& c = *cfg;
   const int ffn = rows_max_of(c) > 0 ? 2 : 0;
+  if (small_front_fits(c)) return 2 + (rows_max_of(c) > 0 ? 1 : 0) + ffn + 1;
   return router_launch_count(c) + permute_launch_count(c) + ffn + (c.T > 0 ? 1 : 0) +
          (permute_fuses_stats(c) ? 0 : 1);
 }
@@ -913,7 +930,7 @@ moe_status moe_checks_read(int32_t* fails, int32_t* site, int32_t* line, int32_t
   cudaError_t (*readers[])(CheckRecord*, bool) = {
       checks_read_router, checks_read_permute, checks_read_combine,
       checks_read_expert_choice, checks_read_backward, checks_read_grouped_bwd,
-      checks_read_grouped_ffn_f32, checks_read_grouped_ffn};
+      checks_read_grouped_ffn_f32, checks_read_grouped_ffn, checks_read_front_small};
   *fails = 0;
   *site = 0;
   *line = 0;

@@ -100,10 +100,12 @@ struct TcParams {
   int32_t* status;
   uint64_t wait_limit_ns;
   int64_t rows_total;              // rows of the grouped buffers (device checks; 0: unknown)
-  // decode tiles, stream-K (both nullptr: whole tiles): [kSkMaxCtas][2][NB][128]
+  // token-column tiles, stream-K (both nullptr: whole tiles): [kSkMaxCtas][nb][128]
   // fp32 partial accumulators and one counter per tile, 0 at launch
   float* sk_partials;
   int32_t* sk_counters;
+  // token-column tiles: token columns per tile and depth of the ring
+  int32_t sw_nb, sw_stages;
 };
 
 // Epilogue of CW accumulator columns of one row: + bias, activation, store.
@@ -248,15 +250,23 @@ __device__ __forceinline__ TileCoord decode_tile(int tile, const int32_t* tile_s
   return TileCoord{lo, local % mt, local / mt};
 }
 
-// Stream-K over the decode tiles.  A layer's decode tiles are few and long
-// (for a Mixtral-sized decode, 256 tiles of 224 k-blocks in the second Linear),
-// so whole tiles per CTA leave the last wave of 148 CTAs partly idle.  Instead
-// every CTA takes an equal share of all tiles' k-blocks -- units
+__device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t* p) {
+  int32_t v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Stream-K over the token-column tiles.  A layer's token-column tiles are few
+// and long (for a Mixtral-sized decode, 256 tiles of 224 k-blocks in the second
+// Linear), so whole tiles per CTA leave the last wave of 148 CTAs partly idle.
+// Instead every CTA takes an equal share of all tiles' k-blocks -- units
 // [b * upc, (b + 1) * upc) of total_tiles * num_kb -- so each streams the same
-// number of weight bytes.  A tile cut by share boundaries is summed by the last
-// of its CTAs to finish: each writes its fp32 partial accumulator (slot 0 when
-// the piece starts its share, else slot 1), counts itself on the tile's
-// counter, and the one that completes the count adds the pieces in k order
+// number of weight bytes.  A tile cut by share boundaries is finished by the
+// CTA holding its first k-block: there the piece is the last of the CTA's
+// share, while every other piece of the tile begins its CTA's share and is
+// computed first.  Those CTAs write their fp32 partial accumulators to their
+// slot and count themselves on the tile's counter; the finishing CTA waits
+// for the count (bounded), adds the pieces to its own accumulator in k order
 // (deterministic) and runs the epilogue.
 constexpr int kSkMaxCtas = 256;
 
@@ -890,74 +900,102 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CFG::THREADS, 1)
   }
 }
 
-// ---- decode variant: the weights as the 128-row MMA operand ----------------------------
+// ---- token-column variant: the weights as the 128-row MMA operand ------------------------
 //
-// When an expert sees only a few tokens (decoding), a 128-row activation tile
-// would be almost all padding.  Here the roles swap: each MMA takes 128 rows
-// of the expert's weight matrix as its M=128 operand and the group's token
-// rows, padded to NB (16 or 32), as its N operand.  The accumulator holds
-// out^T for 128 output features x NB tokens; each epilogue thread owns one
-// feature and writes it for every live token.  Per k-block a CTA moves 16 KB
-// of weights and NB x 128 B of activations, so nearly every byte loaded is a
-// weight byte, and the ring is deep (STAGES x ~18 KB).
+// When an expert sees few tokens -- decoding, or a layer whose capacity caps
+// every group at a few hundred rows -- a 128-row activation tile is mostly
+// padding, and a weight tile is streamed once per 128-row m-tile of its group.
+// Here the roles swap: each MMA takes 128 rows of the expert's weight matrix
+// as its M=128 operand and up to nb of the group's token rows as its N operand
+// (nb = 16, or a multiple of 32 up to 256).  The accumulator holds out^T for
+// 128 output features x nb tokens; each epilogue thread owns one feature and
+// writes it for every live token, 32 (or 16) tokens at a time.  Per k-block a
+// CTA moves 16 KB of weights and nb x 128 B of activations; when nb covers the
+// largest group, every weight byte is read once.
 
-template <int NB, int STAGES>
-struct LayoutS {
-  static constexpr int kWBytes = 128 * BK * 2;
-  static constexpr int kXBytes = NB * BK * 2;
-  static constexpr int kStageBytes = kWBytes + kXBytes;
-  static constexpr int kW = 0;
-  static constexpr int kX = STAGES * kWBytes;
-  static constexpr int kBar = kX + STAGES * kXBytes;
-  static constexpr int kNumBars = 2 * STAGES + 5;
-  static constexpr int kTmemSlot = kBar + kNumBars * 8;
-  static constexpr int kAbort = kTmemSlot + 4;
-  static constexpr int kSkLast = kAbort + 4;             // stream-K: this CTA finishes the tile
-  static constexpr int kSkStop = kSkLast + 4;            // stream-K: an epilogue warp gave up
-  static constexpr int kTileStart = (kSkStop + 4 + 15) / 16 * 16;
-  static constexpr int kGroupOff = kTileStart + (kMaxGroups + 1) * 4;
-  static constexpr int kBytes = kGroupOff + kMaxGroups * 4;
-  static constexpr int kAlloc = kBytes + 1024;
-  static_assert(kXBytes % 1024 == 0, "token tiles must keep the 1 KB swizzle alignment");
-  static_assert(kAlloc <= 227 * 1024, "shared memory budget");
+// Shared-memory layout of the token-column kernel for nb token columns and a
+// ring of `stages` stages (1 KB-aligned base).
+struct LayoutSw {
+  int nb, stages;
+  __host__ __device__ constexpr int w_bytes() const { return 128 * BK * 2; }
+  __host__ __device__ constexpr int x_bytes() const { return nb * BK * 2; }
+  __host__ __device__ constexpr int stage_bytes() const { return w_bytes() + x_bytes(); }
+  __host__ __device__ constexpr int x_off() const { return stages * w_bytes(); }
+  __host__ __device__ constexpr int bar_off() const { return x_off() + stages * x_bytes(); }
+  __host__ __device__ constexpr int num_bars() const { return 2 * stages + 5; }
+  __host__ __device__ constexpr int tmem_slot() const { return bar_off() + num_bars() * 8; }
+  __host__ __device__ constexpr int abort_off() const { return tmem_slot() + 4; }
+  __host__ __device__ constexpr int sk_last() const { return abort_off() + 4; }  // finishes the tile
+  __host__ __device__ constexpr int sk_stop() const { return sk_last() + 4; }    // a warp gave up
+  __host__ __device__ constexpr int tile_start() const { return (sk_stop() + 4 + 15) / 16 * 16; }
+  __host__ __device__ constexpr int group_off() const { return tile_start() + (kMaxGroups + 1) * 4; }
+  __host__ __device__ constexpr int alloc() const { return group_off() + kMaxGroups * 4 + 1024; }
+  // TMEM columns: two accumulators of nb columns, a power of two >= 32
+  __host__ __device__ constexpr uint32_t tmem_cols() const {
+    return 2 * nb <= 32 ? 32u : 2 * nb <= 64 ? 64u : 2 * nb <= 128 ? 128u : 2 * nb <= 256 ? 256u : 512u;
+  }
 };
+constexpr int kSwapMaxStages = 10;
+constexpr int kSwapMaxNb = 256;
+constexpr int kSmemBudget = 227 * 1024;
 
-template <int NB>
-__host__ __device__ constexpr uint32_t idesc_swap_bf16_f32() {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(NB >> 3) << 17) |
+__host__ __device__ constexpr uint32_t idesc_swap_bf16_f32(int nb) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(nb >> 3) << 17) |
          (uint32_t(128 >> 4) << 24);
 }
 
-template <int NB, int STAGES, int EPI>
+// One chunk of CW token columns (tokens c0 .. c0 + CW - 1 of the tile) of a
+// feature: + bias, activation, bf16 store of the live rows.
+template <int EPI, int CW>
+__device__ __forceinline__ void swap_store_chunk(const float (&v)[CW], float b, int c0,
+                                                 int rows_left, __nv_bfloat16* out_col,
+                                                 int64_t ld) {
+#pragma unroll
+  for (int i = 0; i < CW; ++i) {
+    if (c0 + i < rows_left) {
+      float o = v[i] + b;
+      if (EPI == EPI_BIAS_GELU) o = gelu_erf(o);
+      if (EPI == EPI_BIAS_RELU) o = fmaxf(o, 0.f);
+      out_col[int64_t(c0 + i) * ld] = __float2bfloat16_rn(o);
+    }
+  }
+}
+
+// NBT: 16 for the 16-column decode tiles; 0 for p.sw_nb columns (a multiple
+// of 32), handled 32 at a time.
+template <int NBT, int EPI>
 __global__ void __launch_bounds__(6 * 32, 1)
     tc_swap_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
                         const __grid_constant__ CUtensorMap tmWs,
                         const __grid_constant__ CUtensorMap tmX, const TcParams p) {
-  constexpr int kStages = STAGES;
   constexpr int kEpiWarps = 4;
   constexpr int kFeat = 128;                   // output features per tile
-  using L = LayoutS<NB, STAGES>;
+  constexpr int CW = NBT == 16 ? 16 : 32;      // token columns per epilogue chunk
+  const int nb = NBT > 0 ? NBT : p.sw_nb;
+  const int stages = p.sw_stages;
+  const LayoutSw L{nb, stages};
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bar_off());
   uint64_t* full = bars;
-  uint64_t* empty = bars + kStages;
-  uint64_t* tfull = bars + 2 * kStages;
-  uint64_t* tempty = bars + 2 * kStages + 2;
-  uint64_t* done = bars + 2 * kStages + 4;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
-  int32_t* tile_start = reinterpret_cast<int32_t*>(smem + L::kTileStart);
-  int32_t* grp_off = reinterpret_cast<int32_t*>(smem + L::kGroupOff);
-  constexpr uint32_t kTmemCols = 2 * NB < 32 ? 32 : 2 * NB;
+  uint64_t* empty = bars + stages;
+  uint64_t* tfull = bars + 2 * stages;
+  uint64_t* tempty = bars + 2 * stages + 2;
+  uint64_t* done = bars + 2 * stages + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.tmem_slot());
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_off());
+  int32_t* tile_start = reinterpret_cast<int32_t*>(smem + L.tile_start());
+  int32_t* grp_off = reinterpret_cast<int32_t*>(smem + L.group_off());
+  const uint32_t tmem_cols = L.tmem_cols();
+  const int stage_bytes = L.stage_bytes();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_groups = p.n_routed + (p.shared_rows > 0 ? 1 : 0);
   const int ntiles = int(p.Nd / kFeat);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < stages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -967,13 +1005,13 @@ __global__ void __launch_bounds__(6 * 32, 1)
     }
     mbar_init(done, 1);
     *abort_flag = 0;
-    *reinterpret_cast<volatile int*>(smem + L::kSkStop) = 0;
+    *reinterpret_cast<volatile int*>(smem + L.sk_stop()) = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)),
-                 "r"(kTmemCols));
+                 "r"(tmem_cols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   // the next launch may start once this CTA holds its TMEM; global memory is
@@ -991,7 +1029,7 @@ __global__ void __launch_bounds__(6 * 32, 1)
         live = g < p.n_routed ? p.kept[g] : p.shared_rows;
         grp_off[g] = off;
       }
-      const int32_t tiles = int32_t((live + NB - 1) / NB) * ntiles;
+      const int32_t tiles = int32_t((live + nb - 1) / nb) * ntiles;
       int32_t incl = tiles;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -1015,44 +1053,45 @@ __global__ void __launch_bounds__(6 * 32, 1)
   if (warp == 0) {
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
-      int last_parity[kStages];
-#pragma unroll
-      for (int s = 0; s < kStages; ++s) last_parity[s] = -1;
+      int64_t issued = 0;
       bool ok = true;
       SegIter it(sk, blockIdx.x, gridDim.x, total_tiles, p.num_kb, upc);
       int tile, kb0, kb1;
       while (ok && it.next(tile, kb0, kb1)) {
         const TileCoord tc = decode_tile(tile, tile_start, n_groups, ntiles);
-        const int r0 = grp_off[tc.g] + tc.m * NB;
+        const int r0 = grp_off[tc.g] + tc.m * nb;
         const int f0 = tc.n * kFeat;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_or_abort(&empty[stage], phase ^ 1u, p, abort_flag)) { ok = false; break; }
           const uint32_t fb = smem_u32(&full[stage]);
-          mbar_arrive_expect_tx(&full[stage], L::kStageBytes);
+          mbar_arrive_expect_tx(&full[stage], uint32_t(stage_bytes));
           if (tc.g < p.n_routed)
-            tma_load_3d(&tmW, smem_u32(smem + L::kW + stage * L::kWBytes), fb, kb * BK, f0,
-                        tc.g);
+            tma_load_3d(&tmW, smem_u32(smem + stage * L.w_bytes()), fb, kb * BK, f0, tc.g);
           else
-            tma_load_2d(&tmWs, smem_u32(smem + L::kW + stage * L::kWBytes), fb, kb * BK, f0);
-          tma_load_2d(&tmX, smem_u32(smem + L::kX + stage * L::kXBytes), fb, kb * BK, r0);
-          last_parity[stage] = int(phase);
-          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+            tma_load_2d(&tmWs, smem_u32(smem + stage * L.w_bytes()), fb, kb * BK, f0);
+          tma_load_2d(&tmX, smem_u32(smem + L.x_off() + stage * L.x_bytes()), fb, kb * BK, r0);
+          ++issued;
+          if (++stage == uint32_t(stages)) { stage = 0; phase ^= 1u; }
         }
       }
       if (!ok) {
-        for (int s = 0; s < kStages; ++s)
-          if (last_parity[s] >= 0) {
-            const uint32_t a = smem_u32(&full[s]);
-            const uint64_t t0 = global_timer_ns();
-            while (!mbar_try_wait(a, uint32_t(last_parity[s])) &&
-                   global_timer_ns() - t0 < p.wait_limit_ns) {
-            }
+        // let the copies in flight land before the CTA exits: stage s was last
+        // filled by load number i (the largest i < issued with i % stages == s),
+        // whose completion is phase (i / stages) & 1 of full[s]
+        for (int s = 0; s < stages; ++s) {
+          if (issued <= s) continue;
+          const int64_t i = s + (issued - 1 - s) / stages * stages;
+          const uint32_t a = smem_u32(&full[s]);
+          const uint64_t t0 = global_timer_ns();
+          while (!mbar_try_wait(a, uint32_t((i / stages) & 1)) &&
+                 global_timer_ns() - t0 < p.wait_limit_ns) {
           }
+        }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_swap_bf16_f32<NB>();
+      const uint32_t idesc = idesc_swap_bf16_f32(nb);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       SegIter it(sk, blockIdx.x, gridDim.x, total_tiles, p.num_kb, upc);
@@ -1060,18 +1099,18 @@ __global__ void __launch_bounds__(6 * 32, 1)
       while (ok && it.next(tile, kb0, kb1)) {
         if (!wait_or_abort(&tempty[acc], acc_phase ^ 1u, p, abort_flag)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * NB;
+        const uint32_t d_tmem = tmem_base + acc * uint32_t(nb);
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_or_abort(&full[stage], phase, p, abort_flag)) { ok = false; break; }
           tc_fence_after();
-          const uint64_t wd = sdesc_sw128(smem_u32(smem + L::kW + stage * L::kWBytes));
-          const uint64_t xd = sdesc_sw128(smem_u32(smem + L::kX + stage * L::kXBytes));
+          const uint64_t wd = sdesc_sw128(smem_u32(smem + stage * L.w_bytes()));
+          const uint64_t xd = sdesc_sw128(smem_u32(smem + L.x_off() + stage * L.x_bytes()));
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
             tc_mma(d_tmem, wd + uint64_t(2 * kk), xd + uint64_t(2 * kk), idesc,
                    (kb != kb0 || kk != 0) ? 1u : 0u);
           tc_commit(smem_u32(&empty[stage]));
-          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+          if (++stage == uint32_t(stages)) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
         tc_commit(smem_u32(&tfull[acc]));
@@ -1084,12 +1123,18 @@ __global__ void __launch_bounds__(6 * 32, 1)
       }
     }
   } else {
-    // epilogue: warps 2-5, one TMEM lane quarter each; thread = one feature
+    // epilogue: warps 2-5, one TMEM lane quarter each; thread = one feature.
+    // Stream-K: a piece that does not hold its tile's first k-block is
+    // published to this CTA's partial slot (it always starts the CTA's share)
+    // and counted on the tile's counter.  The CTA that holds the first
+    // k-block -- the last piece of its share, so the other pieces, which
+    // began their CTAs' shares, are long done -- waits for that count, adds
+    // the other pieces to its own accumulator in k order and stores the tile.
     const int q = warp & 3;
     const int fl = q * 32 + lane;                  // feature within the tile
-    volatile int* sk_last = reinterpret_cast<volatile int*>(smem + L::kSkLast);
-    volatile int* sk_stop = reinterpret_cast<volatile int*>(smem + L::kSkStop);
-    const int64_t my_u0 = int64_t(blockIdx.x) * upc;
+    volatile int* sk_stop = reinterpret_cast<volatile int*>(smem + L.sk_stop());
+    const int chunks = nb / CW;
+    const int64_t slot_floats = int64_t(nb) * kFeat;
     uint32_t acc = 0, acc_phase = 0;
     SegIter it(sk, blockIdx.x, gridDim.x, total_tiles, p.num_kb, upc);
     int tile, kb0, kb1;
@@ -1098,16 +1143,36 @@ __global__ void __launch_bounds__(6 * 32, 1)
       bool ok = true;
       if (lane == 0) ok = wait_or_abort(&tfull[acc], acc_phase, p, abort_flag);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      const bool whole = kb0 == 0 && kb1 == p.num_kb;
+      const bool head = !whole && kb0 == 0;        // this CTA finishes the tile
+      const int64_t t0 = int64_t(tile) * p.num_kb;
+      const int c_first = sk ? int(t0 / upc) : 0;
+      const int c_last = sk ? int((t0 + p.num_kb - 1) / upc) : 0;
       if (sk) {
-        // stream-K synchronises the four epilogue warps below: they stop
-        // together, whichever of them gave up waiting
+        // the head waits until the tile's other pieces are published
+        if (ok && head && warp == 2 && lane == 0) {
+          const int want = c_last - c_first;
+          int32_t* cnt = p.sk_counters + tile;
+          const uint64_t w0 = global_timer_ns();
+          for (uint32_t it2 = 0; ld_acquire_gpu(cnt) < want; ++it2) {
+            if ((it2 & 63u) == 63u && (*abort_flag || global_timer_ns() - w0 > p.wait_limit_ns)) {
+              atomicCAS(p.status, MOE_OK, MOE_ERR_TIMEOUT);
+              *abort_flag = 1;
+              ok = false;
+              break;
+            }
+          }
+          if (ok) *reinterpret_cast<volatile int32_t*>(cnt) = 0;   // ready for the next call
+        }
+        // the four epilogue warps stop together, whichever of them gave up
         if (!ok && lane == 0) *sk_stop = 1;
         epi_bar_sync();
         ok = *sk_stop == 0;
-        epi_bar_sync();                      // every warp has read the flag
+        epi_bar_sync();                            // every warp has read the flag
       }
       if (!ok) break;
       tc_fence_after();
+      if (head) __threadfence();                   // the other pieces are visible
       const bool routed = tc.g < p.n_routed;
       const int live = routed ? p.kept[tc.g] : p.shared_rows;
       if (warp == 2 && lane == 0)
@@ -1116,67 +1181,66 @@ __global__ void __launch_bounds__(6 * 32, 1)
       const int feat = tc.n * kFeat + fl;
       const __nv_bfloat16* bias = routed ? p.bias + int64_t(tc.g) * p.Nd : p.bias_s;
       const float b = __bfloat162float(bias[feat]);
-      uint32_t r[NB];
-      tmem_ld_cols<NB>(tmem_base + (uint32_t(q * 32) << 16) + acc * NB, r);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);     // accumulator is in registers now
+      const int rows_left = live - tc.m * nb;      // live token rows of this tile
+      __nv_bfloat16* out_col = static_cast<__nv_bfloat16*>(p.out) +
+                               (int64_t(grp_off[tc.g]) + int64_t(tc.m) * nb) * p.Nd + feat;
+      const uint32_t tacc = tmem_base + (uint32_t(q * 32) << 16) + acc * uint32_t(nb);
+      const bool publish = !whole && !head;
+      float* mine = publish ? p.sk_partials + int64_t(blockIdx.x) * slot_floats : nullptr;
+      for (int c = 0; c < chunks; ++c) {
+        uint32_t r[CW];
+        tmem_ld_cols<CW>(tacc + uint32_t(c * CW), r);
+        if (c == chunks - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty[acc]);   // the accumulator is read
+        }
+        float v[CW];
+#pragma unroll
+        for (int i = 0; i < CW; ++i) v[i] = __uint_as_float(r[i]);
+        if (publish) {
+#pragma unroll
+          for (int i = 0; i < CW; ++i) __stcg(mine + (c * CW + i) * kFeat + fl, v[i]);
+          continue;
+        }
+        if (head) {
+          // the other pieces in k order, two at a time
+          int cta = c_first + 1;
+          for (; cta + 1 <= c_last; cta += 2) {
+            const float* pa = p.sk_partials + int64_t(cta) * slot_floats + (c * CW) * kFeat + fl;
+            const float* pb = pa + slot_floats;
+            float a[CW], a2[CW];
+#pragma unroll
+            for (int i = 0; i < CW; ++i) {
+              a[i] = __ldcg(pa + i * kFeat);
+              a2[i] = __ldcg(pb + i * kFeat);
+            }
+#pragma unroll
+            for (int i = 0; i < CW; ++i) v[i] = (v[i] + a[i]) + a2[i];
+          }
+          if (cta <= c_last) {
+            const float* pa = p.sk_partials + int64_t(cta) * slot_floats + (c * CW) * kFeat + fl;
+#pragma unroll
+            for (int i = 0; i < CW; ++i) v[i] += __ldcg(pa + i * kFeat);
+          }
+        }
+        swap_store_chunk<EPI, CW>(v, b, c * CW, rows_left, out_col, p.Nd);
+      }
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
-      float v[NB];
-#pragma unroll
-      for (int i = 0; i < NB; ++i) v[i] = __uint_as_float(r[i]);
-      if (kb0 != 0 || kb1 != p.num_kb) {
-        // a piece of a tile: publish it; the last of the tile's CTAs sums them
-        const int64_t t0 = int64_t(tile) * p.num_kb;
-        const int c_first = int(t0 / upc), c_last = int((t0 + p.num_kb - 1) / upc);
-        const int slot = t0 + kb0 == my_u0 ? 0 : 1;
-        float* mine = p.sk_partials + (int64_t(blockIdx.x) * 2 + slot) * (NB * kFeat);
-#pragma unroll
-        for (int i = 0; i < NB; ++i) __stcg(mine + i * kFeat + fl, v[i]);
-        __threadfence();
-        epi_bar_sync();
-        if (warp == 2 && lane == 0) {
-          const int done_before = atomicAdd(p.sk_counters + tile, 1);
-          const int last = done_before == c_last - c_first;
-          if (last) p.sk_counters[tile] = 0;           // ready for the next call
-          *sk_last = last;
-        }
-        epi_bar_sync();
-        const bool last = *sk_last != 0;
-        epi_bar_sync();                                // the flag is read before reuse
-        if (!last) continue;
-        __threadfence();
-#pragma unroll
-        for (int i = 0; i < NB; ++i) v[i] = 0.f;
-        for (int c = c_first; c <= c_last; ++c) {      // the pieces in k order
-          const int64_t cu0 = int64_t(c) * upc;
-          const float* part = p.sk_partials +
-                              (int64_t(c) * 2 + (t0 > cu0 ? 1 : 0)) * (NB * kFeat);
-#pragma unroll
-          for (int i = 0; i < NB; ++i) v[i] += __ldcg(part + i * kFeat + fl);
-        }
-      }
-      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
-#pragma unroll
-      for (int i = 0; i < NB; ++i) {
-        const int row_in_group = tc.m * NB + i;
-        if (row_in_group < live) {
-          float o = v[i] + b;
-          if (EPI == EPI_BIAS_GELU) o = gelu_erf(o);
-          if (EPI == EPI_BIAS_RELU) o = fmaxf(o, 0.f);
-          out[(int64_t(grp_off[tc.g]) + row_in_group) * p.Nd + feat] = __float2bfloat16_rn(o);
-        }
-      }
+      if (!publish) continue;
+      // count the piece once all four warps' stores are visible
+      __threadfence();
+      epi_bar_sync();
+      if (warp == 2 && lane == 0) atomicAdd(p.sk_counters + tile, 1);
     }
   }
-
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                 "r"(kTmemCols));
+                 "r"(tmem_cols));
   }
 }
 
@@ -1307,27 +1371,37 @@ int pick_tile(int64_t Nd, int64_t rows_per_group, int64_t K) {
   return TILE_64;
 }
 
-template <int NB, int EPI>
+// Deepest ring of the token-column kernel that fits the shared memory.
+int swap_stages(int nb) {
+  int st = kSwapMaxStages;
+  while (st > 2 && LayoutSw{nb, st}.alloc() > kSmemBudget) --st;
+  return st;
+}
+
+template <int NBT, int EPI>
 cudaError_t launch_swap_epi(const CUtensorMap& W, const CUtensorMap& Ws, const CUtensorMap& X,
                             const TcParams& p, int grid, cudaStream_t s) {
-  constexpr int kStagesSwap = 10;
-  constexpr int smem = LayoutS<NB, kStagesSwap>::kAlloc;
-  auto kern = tc_swap_gemm_kernel<NB, kStagesSwap, EPI>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const int smem = LayoutSw{p.sw_nb, p.sw_stages}.alloc();
+  auto kern = tc_swap_gemm_kernel<NBT, EPI>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(grid), dim3(6 * 32), smem, s, W, Ws, X, p);
 }
 
-template <int NB>
+template <int NBT>
 cudaError_t launch_swap(int epi, const CUtensorMap& W, const CUtensorMap& Ws,
                         const CUtensorMap& X, const TcParams& p, int grid, cudaStream_t s) {
-  if (epi == EPI_BIAS_GELU) return launch_swap_epi<NB, EPI_BIAS_GELU>(W, Ws, X, p, grid, s);
-  if (epi == EPI_BIAS_RELU) return launch_swap_epi<NB, EPI_BIAS_RELU>(W, Ws, X, p, grid, s);
-  return launch_swap_epi<NB, EPI_BIAS>(W, Ws, X, p, grid, s);
+  if (epi == EPI_BIAS_GELU) return launch_swap_epi<NBT, EPI_BIAS_GELU>(W, Ws, X, p, grid, s);
+  if (epi == EPI_BIAS_RELU) return launch_swap_epi<NBT, EPI_BIAS_RELU>(W, Ws, X, p, grid, s);
+  return launch_swap_epi<NBT, EPI_BIAS>(W, Ws, X, p, grid, s);
 }
 
-// Token rows per tile of the decode variant for an average group of
-// rows_per_group rows (0: use the regular tiles).
+// Token columns per tile of the token-column variant (0: the regular tiles):
+// 16 or 32 when an average group holds a few rows (decoding).  (Wider
+// token-column tiles -- a capacity-capped layer's groups as single column
+// tiles of up to 256 tokens -- measured slower than the regular tiles on the
+// Switch-sized layer, 45 vs 28 us for its first Linear, and are not used.)
 int swap_rows(int64_t Nd, int64_t rows_per_group, int epi) {
   if (epi == EPI_BIAS_F32 || Nd % 128 != 0) return 0;
   if (rows_per_group <= 8) return 16;
@@ -1339,7 +1413,7 @@ int swap_rows(int64_t Nd, int64_t rows_per_group, int epi) {
 // when moe_forward's workspace holds its scratch: `forward`) or a tile family,
 // and a bound on its tiles (the size of its stream-K counters).
 struct LinearPlan {
-  int nb = 0;              // decode tiles: token columns; 0: regular tiles
+  int nb = 0;              // token-column tiles: token columns; 0: regular tiles
   int choice = TILE_256;   // regular tiles: TileChoice
   bool sk = false;
   int64_t max_tiles = 0;
@@ -1418,8 +1492,10 @@ cudaError_t grouped_linear(const moe_config& c, const GroupedFfnArgs& g, const v
       p.sk_counters = sk_counters;
       grid = g.num_sms < kSkMaxCtas ? g.num_sms : kSkMaxCtas;
     }
+    p.sw_nb = nb;
+    p.sw_stages = swap_stages(nb);
     return nb == 16 ? launch_swap<16>(epi, mW, mWs, mX, p, grid, s)
-                    : launch_swap<32>(epi, mW, mWs, mX, p, grid, s);
+                    : launch_swap<0>(epi, mW, mWs, mX, p, grid, s);
   }
   const int choice = pl.choice;
   const int bn = tile_bn(choice);
@@ -1530,10 +1606,10 @@ size_t sk_partial_bytes(const moe_config& c) {
   for (int linear = 1; linear <= 2; ++linear) {
     const LinearPlan pl = plan_forward_linear(c, linear);
     if (!pl.sk) continue;
-    const size_t b = size_t(pl.nb) * 128 * sizeof(float);   // decode tiles only
+    const size_t b = size_t(pl.nb) * 128 * sizeof(float);   // token-column tiles only
     if (b > slot) slot = b;
   }
-  return size_t(kSkMaxCtas) * 2 * slot;
+  return size_t(kSkMaxCtas) * slot;
 }
 
 cudaError_t launch_grouped_ffn_bf16(const moe_config& c, const GroupedFfnArgs& g,

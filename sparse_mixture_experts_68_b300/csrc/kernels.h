@@ -94,9 +94,27 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* to
 
 // Xp[r] = x[row_token[r]] for the routed rows [0, offsets[N]) (-1: padding,
 // left as is), Xp[offsets[N] + t] = x[t] for the shared group (permute.cu)
+// zero / n_zero as in launch_permute.
 cudaError_t launch_row_copy(const moe_config& c, const void* x, const int32_t* offsets,
                             const int32_t* row_token, void* Xp, int64_t rows_max,
-                            cudaStream_t s);
+                            cudaStream_t s, int32_t* zero = nullptr, int64_t n_zero = 0);
+
+// ---- small-batch front end (front_small.cu) --------------------------------------
+
+// Whether moe_forward routes, sorts and computes the statistics of this layer
+// with the two front-end kernels (a few tokens and experts).
+bool small_front_fits(const moe_config& c);
+// fp32 slice sums of the router scores it keeps in the workspace (0: not used)
+int64_t small_front_partial_floats(const moe_config& c);
+// Router scores, softmax, top-k and gates, the counting sort (counts, kept,
+// offsets, row_token, token_row) and the load statistics; part: scratch of
+// small_front_partial_floats(c) floats.
+cudaError_t launch_small_front(const moe_config& c, const void* x, const void* W_g,
+                               const void* b_g, float* part, float* logits, int32_t* topk_idx,
+                               float* topk_w, int32_t* counts, int32_t* kept, int32_t* offsets,
+                               int32_t* row_token, int32_t* token_row, float* mean_prob,
+                               float* balance, int32_t* dropped, float* cv_squared,
+                               cudaStream_t s);
 
 // scores, expert-major probabilities probT [N, T] (and picks [T] zeroed), block
 // sums of p: the router without its top-k
@@ -164,6 +182,7 @@ cudaError_t checks_read_backward(CheckRecord* out, bool clear);
 cudaError_t checks_read_grouped_bwd(CheckRecord* out, bool clear);
 cudaError_t checks_read_grouped_ffn_f32(CheckRecord* out, bool clear);
 cudaError_t checks_read_grouped_ffn(CheckRecord* out, bool clear);
+cudaError_t checks_read_front_small(CheckRecord* out, bool clear);
 // Kernel (and tile) of grouped Linear 1 or 2 for this layer; routed_rows 0: T * top_k.
 const char* grouped_linear_kernel_name(const moe_config& c, int linear, int64_t routed_rows);
 

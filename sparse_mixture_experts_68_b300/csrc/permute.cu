@@ -415,8 +415,8 @@ cudaError_t launch_copy(const moe_config& c, const void* x, const int32_t* offse
 
 cudaError_t launch_row_copy(const moe_config& c, const void* x, const int32_t* offsets,
                             const int32_t* row_token, void* Xp, int64_t rows_max,
-                            cudaStream_t s) {
-  return launch_copy(c, x, offsets, row_token, Xp, rows_max, s);
+                            cudaStream_t s, int32_t* zero, int64_t n_zero) {
+  return launch_copy(c, x, offsets, row_token, Xp, rows_max, s, zero, n_zero);
 }
 
 int permute_launch_count(const moe_config& c) {

@@ -80,6 +80,23 @@ SMALL = [
              act=ACT_RELU, dtype=DT_BF16, seed=28),
     Workload("bf16_decode_nb32_cap", T=60, d_model=128, d_ff=256, n_experts=12, top_k=3,
              act=ACT_GELU_ERF, dtype=DT_BF16, capacity_factor=1.5, seed=29),
+    # capacity-capped groups: skewed routing leaves some experts empty and
+    # fills others to the cap; a capacity of 240 with two slots per token
+    Workload("bf16_cap_zipf", T=1000, d_model=256, d_ff=512, n_experts=16, top_k=1,
+             act=ACT_RELU, dtype=DT_BF16, capacity_factor=1.4, zipf_router_bias=True,
+             seed=38),
+    Workload("bf16_cap240_k2", T=1200, d_model=384, d_ff=256, n_experts=12, top_k=2,
+             act=ACT_GELU_ERF, dtype=DT_BF16, capacity_factor=2.4, seed=39),
+    # a few tokens: router, sort and statistics in the two front-end kernels
+    # (a ragged last slice of d; 64 experts x 32 tokens with capacity drops;
+    # 40 experts with a shared expert and raw gates)
+    Workload("f32_front_ragged_d", T=5, d_model=72, d_ff=64, n_experts=6, top_k=3,
+             act=ACT_GELU_ERF, dtype=DT_F32, seed=41),
+    Workload("bf16_front_n64_k8_cap", T=32, d_model=256, d_ff=256, n_experts=64, top_k=8,
+             act=ACT_RELU, dtype=DT_BF16, capacity_factor=4.0, seed=42),
+    Workload("bf16_front_n40_shared_raw", T=20, d_model=128, d_ff=128, n_experts=40,
+             top_k=2, act=ACT_GELU_ERF, dtype=DT_BF16, d_ff_shared=128, renormalize=0,
+             seed=43),
     # more than 32 slots per token: gates written in blocks of 32 lanes
     Workload("f32_k40_fused", T=50, d_model=64, d_ff=64, n_experts=64, top_k=40,
              act=ACT_RELU, dtype=DT_F32, seed=25),
@@ -93,6 +110,9 @@ SMALL = [
     Workload("bf16_bn256_shared", T=1000, d_model=256, d_ff=512, n_experts=8, top_k=2,
              act=ACT_GELU_ERF, dtype=DT_BF16, d_ff_shared=512, seed=25),
     Workload("bf16_bn256_relu_cap", T=777, d_model=512, d_ff=256, n_experts=6, top_k=2,
+             act=ACT_RELU, dtype=DT_BF16, capacity_factor=2.0, seed=26),
+    # the same layer with a capacity of 117 (half the assignments dropped)
+    Workload("bf16_cap117_relu", T=777, d_model=512, d_ff=256, n_experts=6, top_k=2,
              act=ACT_RELU, dtype=DT_BF16, capacity_factor=0.9, seed=26),
     # fp32 CUDA-core GEMMs on each tile size: the first Linear (d_ff = 1024 columns
     # over ~4500 grouped rows) on 128 x 64 tiles, the second on 64 x 64
@@ -402,16 +422,26 @@ def test_activation_matches_cuda_erf_gelu_and_relu():
     assert torch.equal(y, torch.relu(x))
 
 
-def test_decode_stream_k_deterministic_and_close_to_whole_tiles():
-    """moe_forward runs the decode tiles stream-K: every CTA streams an equal
-    share of the k-blocks, and a tile split between CTAs is summed by the
-    last of them, in k order.  Three calls give the same bits; the staged
+SK_LAYERS = [
+    (Workload("decode_sk", T=24, d_model=512, d_ff=1024, n_experts=8, top_k=2,
+              act=ACT_GELU_ERF, dtype=DT_BF16, seed=37), "x 16 tokens"),
+    (Workload("decode_sk_nb32_cap", T=40, d_model=512, d_ff=1024, n_experts=4, top_k=2,
+              act=ACT_RELU, dtype=DT_BF16, capacity_factor=0.9, seed=40), "x 32 tokens"),
+]
+
+
+@pytest.mark.parametrize("wl,tile", SK_LAYERS, ids=[w.name for w, _ in SK_LAYERS])
+def test_decode_stream_k_deterministic_and_close_to_whole_tiles(wl, tile):
+    """moe_forward runs the token-column tiles stream-K: every CTA streams an
+    equal share of the k-blocks, and a tile split between CTAs is summed by
+    the last of them, in k order.  Three calls give the same bits; the staged
     calls (moe_grouped_ffn, whole tiles per CTA) agree within bf16 rounding;
-    both match the oracle."""
-    wl = Workload("decode_sk", T=24, d_model=512, d_ff=1024, n_experts=8, top_k=2,
-                  act=ACT_GELU_ERF, dtype=DT_BF16, seed=37)
+    both match the oracle.  Cases: a decode layer (16 token columns) and one
+    with 32 token columns and capacity drops."""
     t, layer, out1 = run_layer(wl)
-    assert "stream-K" in B.ffn_kernel_name(layer.cfg, 1)
+    for linear in (1, 2):
+        name = B.ffn_kernel_name(layer.cfg, linear)
+        assert "stream-K" in name and tile in name, name
     again = [layer.forward(t["x"], with_logits=True) for _ in range(2)]
     torch.cuda.synchronize()
     for o in again:
