@@ -203,6 +203,12 @@ SMALL = [
              act=ACT_GELU_ERF, dtype=DT_BF16, seed=91),
     Workload("bwd_twelve_experts", T=333, d_model=1088, d_ff=128, n_experts=12, top_k=3,
              act=ACT_GELU_ERF, dtype=DT_BF16, seed=92),
+    # a few tokens: the forward routes with the small-batch front end and runs
+    # the token-column tiles; bf16, and fp32 with capacity drops and a shared expert
+    Workload("bwd_front_decode", T=24, d_model=256, d_ff=384, n_experts=8, top_k=2,
+             act=ACT_GELU_ERF, dtype=DT_BF16, seed=94),
+    Workload("bwd_front_f32_cap_shared", T=9, d_model=72, d_ff=64, n_experts=6, top_k=3,
+             act=ACT_RELU, dtype=DT_F32, capacity_factor=1.5, d_ff_shared=64, seed=95),
 ]
 
 
