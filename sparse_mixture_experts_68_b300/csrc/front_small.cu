@@ -71,6 +71,23 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// part[b0 .. b1)[q] added in slice order; the loads of eight slices are
+// unconditional (an index past b1 reads slice b1 - 1 and is not added), so
+// they are in flight together rather than one round trip each.
+__device__ __forceinline__ float sum_slices(const float* __restrict__ part, int P, int q,
+                                            int b0, int b1) {
+  float acc = 0.f;
+  for (int b = b0; b < b1; b += 8) {
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = __ldcg(part + int64_t(min(b + u, b1 - 1)) * P + q);
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (b + u < b1) acc += v[u];
+  }
+  return acc;
+}
+
 template <typename TIn>
 __global__ void __launch_bounds__(1024)
     front_route_kernel(const float* __restrict__ part, int G, const TIn* __restrict__ b_g,
@@ -99,17 +116,12 @@ __global__ void __launch_bounds__(1024)
     const int pr = tid % P, grp = tid / P;
     if (P <= 1024 && grp < S) {
       const int b0 = grp * Gs, b1 = min(G, b0 + Gs);
-      float acc = 0.f;
-      for (int b = b0; b < b1; ++b) acc += __ldcg(part + int64_t(b) * P + pr);
-      red[grp * P + pr] = acc;
+      red[grp * P + pr] = sum_slices(part, P, pr, b0, b1);
     } else if (P > 1024) {
       // P <= 2048: two pairs per thread, all slices
       for (int h = 0; h < 2; ++h) {
         const int q = tid + h * 1024;
-        float acc = 0.f;
-        if (q < P)
-          for (int b = 0; b < G; ++b) acc += __ldcg(part + int64_t(b) * P + q);
-        zsum[h] = acc;
+        zsum[h] = q < P ? sum_slices(part, P, q, 0, G) : 0.f;
       }
     }
   }

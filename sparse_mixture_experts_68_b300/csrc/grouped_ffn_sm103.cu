@@ -27,6 +27,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <float.h>
 #include <mutex>
 
 #include "kernels.h"
@@ -45,8 +46,12 @@ constexpr int kMaxGroups = 1025;        // 1024 routed + 1 shared
 enum { EPI_BIAS = 0, EPI_BIAS_GELU = 1, EPI_BIAS_RELU = 2, EPI_BIAS_F32 = 3,
        // backward dgrad on the CTA pair (weights as MN-major B): no bias; the
        // result times the activation's derivative at TcParams::pre, or as is
-       EPI_DGRAD_GELU = 4, EPI_DGRAD_RELU = 5, EPI_DGRAD = 6 };
-constexpr bool epi_is_dgrad(int e) { return e >= EPI_DGRAD_GELU; }
+       EPI_DGRAD_GELU = 4, EPI_DGRAD_RELU = 5, EPI_DGRAD = 6,
+       // router scores of 64 experts (one 64-wide tile per row): + bias, fp32
+       // scores out, then the softmax, top-k and gates of each row and the
+       // tile's column sums of p
+       EPI_ROUTER_TOPK = 7 };
+constexpr bool epi_is_dgrad(int e) { return e >= EPI_DGRAD_GELU && e <= EPI_DGRAD; }
 
 // A kernel variant: output tile width BN, depth of the shared-memory ring,
 // number of epilogue warps (a multiple of 4: one set per TMEM lane quarter).
@@ -106,6 +111,11 @@ struct TcParams {
   int32_t* sk_counters;
   // token-column tiles: token columns per tile and depth of the ring
   int32_t sw_nb, sw_stages;
+  // EPI_ROUTER_TOPK: [rows, k] experts and gates, [m-tiles, 64] column sums of p
+  int32_t* topk_idx;
+  float* topk_w;
+  float* prob_rows;
+  int32_t top_k, renorm;
 };
 
 // Epilogue of CW accumulator columns of one row: + bias, activation, store.
@@ -307,6 +317,98 @@ __device__ __forceinline__ void epi_bar_sync(int threads = 128) {
   asm volatile("bar.sync 1, %0;" ::"r"(threads) : "memory");
 }
 
+// EPI_ROUTER_TOPK, run by the four epilogue warps (128 threads, thread =
+// token row; CfgRouter, so that the 64 scores stay in registers): the row's 64 scores from TMEM + bias, written as fp32;
+// the softmax, k rounds of arg-max (the larger score first, then the lower
+// expert) and the gates, as in the router kernels; then the tile's column
+// sums of p -- a reduce-scatter across each warp's lanes (lane l ends with
+// experts 2l and 2l + 1), the four warps added in order through `red`
+// [4][64] -- written as row m of p.prob_rows.  Rows past the live ones add 0.
+__device__ __forceinline__ void router_topk_rows(const TcParams& p, uint32_t taddr,
+                                                 const __nv_bfloat16* __restrict__ bias,
+                                                 int row, bool valid, int m, int q, int lane,
+                                                 float* red) {
+  constexpr int NE = 64;
+  float z[NE];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t r[32];
+    tmem_ld_32cols(taddr + uint32_t(32 * h), r);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) z[32 * h + i] = __uint_as_float(r[i]) + __bfloat162float(bias[32 * h + i]);
+  }
+  if (valid) {
+    float4* zo = reinterpret_cast<float4*>(static_cast<float*>(p.out) + int64_t(row) * NE);
+#pragma unroll
+    for (int v = 0; v < NE / 4; ++v)
+      zo[v] = make_float4(z[4 * v], z[4 * v + 1], z[4 * v + 2], z[4 * v + 3]);
+  }
+  float mx = -FLT_MAX;
+#pragma unroll
+  for (int i = 0; i < NE; ++i) mx = fmaxf(mx, z[i]);
+  const int k = p.top_k;
+  uint64_t taken = 0;
+  int sel_e[8];
+  float g[8], kept_sum = 0.f;                   // gates exp(z - max), unnormalised
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    sel_e[j] = 0;
+    g[j] = 0.f;
+    if (j < k) {
+      float bv = -INFINITY;
+      int be = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < NE; ++i)
+        if (!((taken >> i) & 1ull) && (z[i] > bv || (z[i] == bv && i < be))) {
+          bv = z[i];
+          be = i;
+        }
+      if (be < NE) taken |= 1ull << be;
+      sel_e[j] = be;
+      g[j] = expf(bv - mx);
+      kept_sum += g[j];
+    }
+  }
+  float ssum = 0.f;
+#pragma unroll
+  for (int i = 0; i < NE; ++i) {
+    z[i] = expf(z[i] - mx);                     // z now holds exp(z - max)
+    ssum += z[i];
+  }
+  const float inv = 1.0f / ssum;
+  const float scale = p.renorm ? 1.0f / kept_sum : inv;
+  if (valid) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (j < k) {
+        MOE_CHECK(sel_e[j] >= 0 && sel_e[j] < NE, CK_ROUTER_TOPK);
+        p.topk_idx[int64_t(row) * k + j] = sel_e[j];
+        p.topk_w[int64_t(row) * k + j] = g[j] * scale;
+      }
+  }
+  // column sums of p over the tile's rows: reduce-scatter across the lanes
+#pragma unroll
+  for (int i = 0; i < NE; ++i) z[i] = valid ? z[i] * inv : 0.f;
+#pragma unroll
+  for (int step = 0; step < 5; ++step) {
+    const int o = 16 >> step;
+    const int S = NE >> step;                   // values still held per lane
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < S / 2; ++i) {
+      const float send = upper ? z[i] : z[i + S / 2];
+      const float keep = upper ? z[i + S / 2] : z[i];
+      z[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  red[q * NE + 2 * lane] = z[0];
+  red[q * NE + 2 * lane + 1] = z[1];
+  epi_bar_sync();
+  const int e = q * 32 + lane;
+  if (e < NE) p.prob_rows[int64_t(m) * NE + e] = ((red[e] + red[NE + e]) + red[2 * NE + e]) + red[3 * NE + e];
+  epi_bar_sync();                               // red is read before the next tile
+}
+
 template <class CFG, int EPI, int MINB>
 __global__ void __launch_bounds__(CFG::THREADS, MINB)
     tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -487,6 +589,11 @@ __global__ void __launch_bounds__(CFG::THREADS, MINB)
       const __nv_bfloat16* bias = routed ? p.bias + int64_t(tc.g) * p.Nd : p.bias_s;
       constexpr int kOutBytes = EPI == EPI_BIAS_F32 ? 4 : 2;
       constexpr bool kStaged = CFG::STAGED && EPI != EPI_BIAS_F32;
+      if constexpr (EPI == EPI_ROUTER_TOPK) {
+        if (part == 0) router_topk_rows(p, tmem_base + (uint32_t(q * 32) << 16) + acc * BN,
+                                        bias, row_in_group, valid, tc.m, q, lane,
+                                        reinterpret_cast<float*>(smem + L::kStage));
+      } else
 #pragma unroll 1
       for (int c = part * kCols; c < (part + 1) * kCols; c += CW) {
         uint32_t r[CW];
@@ -1291,6 +1398,7 @@ using Cfg128 = TileCfg<128, 4, 16>;
 using Cfg64 = TileCfg<64, 6, 16>;
 using Cfg128x2 = TileCfg<128, 3, 8, false>;  // two CTAs per SM, 96 KB ring each
 using Cfg256Pair = TileCfg<256, 6, 16>;    // CTA pair, 256 x 256 tiles, 6 x 32 KB ring per CTA
+using CfgRouter = TileCfg<64, 6, 4>;       // router with the top-k epilogue: a thread holds a row
 
 int tile_bn(int choice) {
   switch (choice) {
@@ -1687,6 +1795,39 @@ cudaError_t launch_router_logits_tc(const moe_config& c, const void* x, const vo
   const int64_t tiles = ceil_div(c.T, BM) * (c.n_experts / bn);
   const int grid = int(tiles < num_sms ? tiles : num_sms);
   return launch_tc<Cfg64, EPI_BIAS_F32>(mA, mB, mB, p, grid, s);
+}
+
+// The same GEMM for 64 experts with the softmax, top-k and gates in its
+// epilogue (router_topk_rows): one 64-wide tile holds a row's every score.
+// prob_rows [ceil(T/128), 64]: column sums of p per 128-row tile.
+cudaError_t launch_router_topk_tc(const moe_config& c, const void* x, const void* W_g,
+                                  const void* b_g, float* logits, int32_t* topk_idx,
+                                  float* topk_w, float* prob_rows, int num_sms,
+                                  int32_t* status, uint64_t wait_limit_ns, cudaStream_t s) {
+  if (c.T == 0) return cudaSuccess;
+  if (c.n_experts != 64 || c.top_k < 1 || c.top_k > 8) return cudaErrorInvalidValue;
+  constexpr int bn = 64;
+  CUtensorMap mA, mB;
+  if (!make_map(&mA, x, uint64_t(c.d_model), uint64_t(c.T), 0, BM)) return cudaErrorInvalidValue;
+  if (!make_map(&mB, W_g, uint64_t(c.d_model), uint64_t(c.n_experts), 1, bn))
+    return cudaErrorInvalidValue;
+  TcParams p{};
+  p.bias = static_cast<const __nv_bfloat16*>(b_g);
+  p.out = logits;
+  p.Nd = c.n_experts;
+  p.n_routed = 1;
+  p.dense_rows = int32_t(c.T);
+  p.num_kb = int32_t(c.d_model / BK);
+  p.status = status;
+  p.wait_limit_ns = wait_limit_ns;
+  p.topk_idx = topk_idx;
+  p.topk_w = topk_w;
+  p.prob_rows = prob_rows;
+  p.top_k = int32_t(c.top_k);
+  p.renorm = c.renormalize ? 1 : 0;
+  const int64_t tiles = ceil_div(c.T, BM);
+  const int grid = int(tiles < num_sms ? tiles : num_sms);
+  return launch_tc<CfgRouter, EPI_ROUTER_TOPK>(mA, mB, mB, p, grid, s);
 }
 
 MOE_CHECKS_UNIT(grouped_ffn)

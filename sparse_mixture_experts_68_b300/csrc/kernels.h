@@ -42,8 +42,16 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 constexpr int kRouterTokensPerBlock = 8;    // tokens per router pass (one per warp)
 constexpr int kRouterMaxBlocks = 296;       // router blocks (grid-stride over 8-token groups)
 
-// Rows of the router's probability partial sums: one per router block.
+// bf16 layers with 64 experts: the tensor-core router GEMM also takes the
+// softmax, top-k and gates in its epilogue (k <= 8).
+inline bool router_tc_topk(const moe_config& c) {
+  return c.dtype == MOE_BF16 && c.n_experts == 64 && c.top_k >= 1 && c.top_k <= 8;
+}
+
+// Rows of the router's probability partial sums: one per router block (one
+// per 128-token tile for the tensor-core router with the top-k epilogue).
 inline int64_t router_partial_rows(const moe_config& c) {
+  if (router_tc_topk(c)) return (c.T + 127) / 128;
   const int64_t groups = (c.T + kRouterTokensPerBlock - 1) / kRouterTokensPerBlock;
   return groups < kRouterMaxBlocks ? groups : kRouterMaxBlocks;
 }
@@ -205,6 +213,12 @@ cudaError_t launch_load_stats(const moe_config& c, const float* prob_partials,
                               cudaStream_t s);
 
 // ---- kernels launched per step, for the chosen dispatch ------------------------------
+// Router scores, softmax, top-k, gates and the per-tile sums of p for 64
+// experts in one tensor-core launch (router_tc_topk) (grouped_ffn_sm103.cu).
+cudaError_t launch_router_topk_tc(const moe_config& c, const void* x, const void* W_g,
+                                  const void* b_g, float* logits, int32_t* topk_idx,
+                                  float* topk_w, float* prob_rows, int num_sms,
+                                  int32_t* status, uint64_t wait_limit_ns, cudaStream_t s);
 int router_launch_count(const moe_config& c);
 int permute_launch_count(const moe_config& c);
 

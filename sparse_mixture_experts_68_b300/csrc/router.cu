@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(kRouterWarps * 32, WF32 ? 2 : 1)
 #pragma unroll
       for (int u = 0; u < kBatch; ++u) {
         const int c = c0 + 32 * u;
-        xq[u] = c < dv ? __ldg(xr + c) : make_uint4(0, 0, 0, 0);
+        xq[u] = __ldg(xr + (c < dv ? c : dv - 1));   // unconditional: all in flight at once
       }
 #pragma unroll
       for (int u = 0; u < kBatch; ++u) {
@@ -451,13 +451,16 @@ namespace moe {
 
 int router_launch_count(const moe_config& c) {
   if (c.T == 0) return 0;
+  if (router_tc_topk(c)) return 1;
   if (c.dtype == MOE_BF16 && c.n_experts % 64 == 0) return 2;
   return fused_router_fits(c) ? 1 : 2;
 }
 
 // Scores + softmax + top-k for one layer, choosing the kernels by shape:
-// bf16 with N a multiple of 64: the tensor-core GEMM (fp32 scores) then the
-// softmax/top-k kernel; otherwise, when N <= 64 and W_g fits in shared
+// bf16 with 64 experts (k <= 8): the tensor-core GEMM with the softmax, top-k
+// and gates in its epilogue; bf16 with N a multiple of 64: the tensor-core
+// GEMM (fp32 scores) then the softmax/top-k kernel; otherwise, when N <= 64
+// and W_g fits in shared
 // memory, the fused warp-per-token kernel; otherwise the CUDA-core GEMM then
 // the softmax/top-k kernel.
 cudaError_t launch_router(const moe_config& c, const void* x, const void* W_g,
@@ -467,6 +470,9 @@ cudaError_t launch_router(const moe_config& c, const void* x, const void* W_g,
   if (c.T == 0) return cudaSuccess;
   cudaError_t e;
   const int k = int(c.top_k);
+  if (router_tc_topk(c))
+    return launch_router_topk_tc(c, x, W_g, b_g, logits, topk_idx, topk_w, prob_partials,
+                                 num_sms, status, wait_limit_ns, s);
   if (c.dtype == MOE_BF16 && c.n_experts % 64 == 0)
     e = launch_router_logits_tc(c, x, W_g, b_g, logits, num_sms, status, wait_limit_ns, s);
   else if (fused_router_fits(c))

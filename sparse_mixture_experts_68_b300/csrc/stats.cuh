@@ -17,7 +17,11 @@ namespace moe {
 // comes from compensated arithmetic instead.  The partial-sum rows are split
 // into RG row groups and the experts into 32-wide chunks; warp w takes (row
 // group w % RG, chunk w / RG) with lane = expert, so every load is a
-// coalesced 128-byte row segment, eight of them in flight.  Each warp keeps a
+// coalesced 128-byte row segment, kStatsBatch of them in flight.  The loads
+// are unconditional (a row index past the warp's range is clamped to its last
+// row, and the sum skips it): with each load under the same condition as its
+// addition the compiler issued them one round trip at a time, which took 33 us
+// for 296 x 256 partial sums.  Each warp keeps a
 // Kahan sum per expert; the row groups are combined in order with
 // error-free additions (two-sum).  The deviation from the uniform load is
 // taken as (S - T/N) / T with S the compensated sum, so it keeps its
@@ -26,6 +30,7 @@ namespace moe {
 // var/mean^2 = N (N Q - S^2) / ((N - 1) S^2), N Q - S^2 in 128-bit integers.
 constexpr int kStatsThreads = 1024;
 constexpr int kStatsWarps = kStatsThreads / 32;
+constexpr int kStatsBatch = 16;                   // partial-sum rows loaded at once
 
 __device__ __forceinline__ void stats_two_sum(float a, float b, float& s, float& err) {
   s = a + b;
@@ -87,13 +92,13 @@ __device__ __forceinline__ void block_load_stats(const float* __restrict__ prob_
       const int b0 = warp * rows, b1 = min(nblk, b0 + rows);
       float s = 0.f, comp = 0.f;
       if (lane < N) {
-        for (int b = b0; b < b1; b += 8) {        // eight loads in flight, added in order
-          float v[8];
+        for (int b = b0; b < b1; b += kStatsBatch) {   // loads in flight, added in order
+          float v[kStatsBatch];
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
-            v[u] = b + u < b1 ? prob_partials[int64_t(b + u) * N + lane] : 0.f;
+          for (int u = 0; u < kStatsBatch; ++u)
+            v[u] = prob_partials[int64_t(min(b + u, b1 - 1)) * N + lane];   // unconditional
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
+          for (int u = 0; u < kStatsBatch; ++u)
             if (b + u < b1) stats_kahan_add(v[u], s, comp);
         }
       }
@@ -163,13 +168,13 @@ __device__ __forceinline__ void block_load_stats(const float* __restrict__ prob_
     if (live) {
       const int rows = (nblk + RG - 1) / RG;
       const int b0 = rg * rows, b1 = min(nblk, b0 + rows);
-      for (int b = b0; b < b1; b += 8) {          // eight loads in flight, added in order
-        float v[8];
+      for (int b = b0; b < b1; b += kStatsBatch) {     // loads in flight, added in order
+        float v[kStatsBatch];
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          v[u] = b + u < b1 ? prob_partials[int64_t(b + u) * N + e] : 0.f;
+        for (int u = 0; u < kStatsBatch; ++u)
+          v[u] = prob_partials[int64_t(min(b + u, b1 - 1)) * N + e];   // unconditional
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
+        for (int u = 0; u < kStatsBatch; ++u)
           if (b + u < b1) stats_kahan_add(v[u], s, comp);
       }
     }

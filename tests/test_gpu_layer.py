@@ -67,6 +67,14 @@ SMALL = [
     # with two experts per lane (32 < N <= 64), CUDA-core GEMM (large fp32 W_g)
     Workload("bf16_tc_router", T=333, d_model=128, d_ff=128, n_experts=128, top_k=3,
              act=ACT_GELU_ERF, dtype=DT_BF16, seed=20),
+    # 64 experts in bf16: the router GEMM with the softmax, top-k and gates in
+    # its epilogue (ragged last 128-row tile; raw gates; k = 8 with capacity
+    # drops and a shared expert)
+    Workload("bf16_router64_k4_raw", T=333, d_model=128, d_ff=128, n_experts=64, top_k=4,
+             act=ACT_GELU_ERF, dtype=DT_BF16, renormalize=0, seed=44),
+    Workload("bf16_router64_k8_cap_shared", T=700, d_model=256, d_ff=128, n_experts=64,
+             top_k=8, act=ACT_RELU, dtype=DT_BF16, capacity_factor=6.0, d_ff_shared=128,
+             seed=45),
     Workload("f32_fused_router_npl2", T=97, d_model=96, d_ff=64, n_experts=48, top_k=5,
              act=ACT_RELU, dtype=DT_F32, seed=22),
     Workload("f32_simt_router", T=70, d_model=1024, d_ff=64, n_experts=64, top_k=2,
