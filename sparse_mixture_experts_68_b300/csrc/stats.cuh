@@ -9,6 +9,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "loads.cuh"
 
 namespace moe {
 
@@ -19,9 +20,10 @@ namespace moe {
 // group w % RG, chunk w / RG) with lane = expert, so every load is a
 // coalesced 128-byte row segment, kStatsBatch of them in flight.  The loads
 // are unconditional (a row index past the warp's range is clamped to its last
-// row, and the sum skips it): with each load under the same condition as its
-// addition the compiler issued them one round trip at a time, which took 33 us
-// for 296 x 256 partial sums.  Each warp keeps a
+// row, and the sum skips it) and issued where they stand (ld_now): with each
+// load under the same condition as its addition the compiler issued them one
+// round trip at a time, which took 33 us for 296 x 256 partial sums.  Each
+// warp keeps a
 // Kahan sum per expert; the row groups are combined in order with
 // error-free additions (two-sum).  The deviation from the uniform load is
 // taken as (S - T/N) / T with S the compensated sum, so it keeps its
@@ -96,7 +98,7 @@ __device__ __forceinline__ void block_load_stats(const float* __restrict__ prob_
           float v[kStatsBatch];
 #pragma unroll
           for (int u = 0; u < kStatsBatch; ++u)
-            v[u] = prob_partials[int64_t(min(b + u, b1 - 1)) * N + lane];   // unconditional
+            v[u] = ld_now(prob_partials + int64_t(min(b + u, b1 - 1)) * N + lane);
 #pragma unroll
           for (int u = 0; u < kStatsBatch; ++u)
             if (b + u < b1) stats_kahan_add(v[u], s, comp);
@@ -172,7 +174,7 @@ __device__ __forceinline__ void block_load_stats(const float* __restrict__ prob_
         float v[kStatsBatch];
 #pragma unroll
         for (int u = 0; u < kStatsBatch; ++u)
-          v[u] = prob_partials[int64_t(min(b + u, b1 - 1)) * N + e];   // unconditional
+          v[u] = ld_now(prob_partials + int64_t(min(b + u, b1 - 1)) * N + e);
 #pragma unroll
         for (int u = 0; u < kStatsBatch; ++u)
           if (b + u < b1) stats_kahan_add(v[u], s, comp);
