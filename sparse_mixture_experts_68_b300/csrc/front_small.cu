@@ -22,7 +22,6 @@
 #include <float.h>
 
 #include "common.cuh"
-#include "loads.cuh"
 #include "kernels.h"
 #include "stats.cuh"
 
@@ -72,20 +71,19 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// part[b0 .. b1)[q] added in slice order; the loads of eight slices are
-// unconditional (an index past b1 reads slice b1 - 1 and is not added) and
-// issued where they stand (ld_now_cg), so they are in flight together rather
-// than one round trip each.
+// part[b0 .. b1)[q] added in slice order; the loads of eight slices and
+// their additions are unconditional (an index past b1 reads slice b1 - 1 and
+// a select adds 0 instead), so the loads are in flight together rather than
+// one round trip each.
 __device__ __forceinline__ float sum_slices(const float* __restrict__ part, int P, int q,
                                             int b0, int b1) {
   float acc = 0.f;
   for (int b = b0; b < b1; b += 8) {
     float v[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) v[u] = ld_now_cg(part + int64_t(min(b + u, b1 - 1)) * P + q);
+    for (int u = 0; u < 8; ++u) v[u] = __ldcg(part + int64_t(min(b + u, b1 - 1)) * P + q);
 #pragma unroll
-    for (int u = 0; u < 8; ++u)
-      if (b + u < b1) acc += v[u];
+    for (int u = 0; u < 8; ++u) acc += b + u < b1 ? v[u] : 0.f;   // + 0 changes nothing
   }
   return acc;
 }

@@ -6,7 +6,6 @@
 #include <float.h>
 
 #include "common.cuh"
-#include "loads.cuh"
 #include "kernels.h"
 #include "simt_gemm.cuh"
 
@@ -223,7 +222,7 @@ __global__ void __launch_bounds__(kRouterWarps * 32, WF32 ? 2 : 1)
 #pragma unroll
       for (int u = 0; u < kBatch; ++u) {
         const int c = c0 + 32 * u;
-        xq[u] = ld_now_nc_v4(xr + (c < dv ? c : dv - 1));   // all in flight at once
+        xq[u] = c < dv ? __ldg(xr + c) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
       for (int u = 0; u < kBatch; ++u) {

@@ -9,7 +9,6 @@
 #pragma once
 
 #include "common.cuh"
-#include "loads.cuh"
 
 namespace moe {
 
@@ -20,10 +19,10 @@ namespace moe {
 // group w % RG, chunk w / RG) with lane = expert, so every load is a
 // coalesced 128-byte row segment, kStatsBatch of them in flight.  The loads
 // are unconditional (a row index past the warp's range is clamped to its last
-// row, and the sum skips it) and issued where they stand (ld_now): with each
-// load under the same condition as its addition the compiler issued them one
-// round trip at a time, which took 33 us for 296 x 256 partial sums.  Each
-// warp keeps a
+// row, and the sum skips it): with each load under the same bounds test as its
+// addition the compiler issued them one round trip at a time, which took 33 us
+// for 296 x 256 partial sums.  The function is not inlined, so that every
+// caller gets the same schedule.  Each warp keeps a
 // Kahan sum per expert; the row groups are combined in order with
 // error-free additions (two-sum).  The deviation from the uniform load is
 // taken as (S - T/N) / T with S the compensated sum, so it keeps its
@@ -68,7 +67,7 @@ __device__ __forceinline__ float cv_squared_of(int N, long long S, long long Q) 
 }
 
 // Runs on all kStatsThreads threads of a block (blockDim.x == kStatsThreads).
-__device__ __forceinline__ void block_load_stats(const float* __restrict__ prob_partials,
+static __device__ __noinline__ void block_load_stats(const float* __restrict__ prob_partials,
                                                  int nblk, int N, int Ttok,
                                                  const int32_t* __restrict__ counts,
                                                  const int32_t* __restrict__ kept,
@@ -98,7 +97,7 @@ __device__ __forceinline__ void block_load_stats(const float* __restrict__ prob_
           float v[kStatsBatch];
 #pragma unroll
           for (int u = 0; u < kStatsBatch; ++u)
-            v[u] = ld_now(prob_partials + int64_t(min(b + u, b1 - 1)) * N + lane);
+            v[u] = prob_partials[int64_t(min(b + u, b1 - 1)) * N + lane];
 #pragma unroll
           for (int u = 0; u < kStatsBatch; ++u)
             if (b + u < b1) stats_kahan_add(v[u], s, comp);
@@ -174,7 +173,7 @@ __device__ __forceinline__ void block_load_stats(const float* __restrict__ prob_
         float v[kStatsBatch];
 #pragma unroll
         for (int u = 0; u < kStatsBatch; ++u)
-          v[u] = ld_now(prob_partials + int64_t(min(b + u, b1 - 1)) * N + e);
+          v[u] = prob_partials[int64_t(min(b + u, b1 - 1)) * N + e];
 #pragma unroll
         for (int u = 0; u < kStatsBatch; ++u)
           if (b + u < b1) stats_kahan_add(v[u], s, comp);
