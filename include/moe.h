@@ -273,10 +273,24 @@ moe_status moe_forward_profiled(const moe_config* cfg, const void* x, const moe_
  * every non-NULL pointer in `out` are host pointers (page-locked memory makes
  * the copies asynchronous); weights and workspace stay on the device.  The
  * call copies x in, runs the layer, copies the results out and synchronises
- * `stream` before returning.  The workspace must hold
- * moe_workspace_size(cfg) bytes plus room for x and every output
- * (moe_host_workspace_size). */
+ * before returning; when it returns, all of its work on `stream` is done.
+ * The workspace must hold moe_workspace_size(cfg) bytes plus room for x,
+ * every output and the chunk scratch below (moe_host_workspace_size).
+ *
+ * Layers of at least 1024 tokens without capacity, whose halves run the same
+ * grouped-FFN kernels as the whole batch and either keep >= 256 rows per
+ * expert or have <= 96 MB of expert weights, run as two token chunks so that
+ * the copies overlap the layer: chunk 1's tokens are copied in while chunk 0
+ * runs, and chunk 0's results copied out while chunk 1 runs (the copies on a
+ * second stream the library keeps per device; calls on one device take turns).
+ * Per token the results are those of moe_forward bit for bit; counts, kept
+ * and dropped are exact; mean_prob, balance and cv_squared come from both
+ * chunks' partial sums and may differ from moe_forward's in the last bits.
+ * This division of the work is an implementation choice: the pages have no
+ * counterpart.  moe_forward_host_chunks gives the number of chunks (1 or 2;
+ * -1 for an invalid config). */
 size_t moe_host_workspace_size(const moe_config* cfg);
+int32_t moe_forward_host_chunks(const moe_config* cfg);
 moe_status moe_forward_host(const moe_config* cfg, const void* x_host, const moe_weights* w,
                             const moe_outputs* out_host, void* workspace,
                             size_t workspace_bytes, void* stream);

@@ -30,7 +30,8 @@ MOE_ACT_GELU_ERF, MOE_ACT_RELU = 0, 1
 EXPORTS = [
     "moe_rows_max", "moe_router_blocks", "moe_permute_scratch_size", "moe_workspace_size",
     "moe_router_topk", "moe_permute", "moe_grouped_ffn", "moe_combine", "moe_load_stats",
-    "moe_forward", "moe_host_workspace_size", "moe_forward_host", "moe_get_device_status",
+    "moe_forward", "moe_host_workspace_size", "moe_forward_host", "moe_forward_host_chunks",
+    "moe_get_device_status",
     "moe_set_wait_limit_ns", "moe_get_wait_limit_ns", "moe_selftest_bounded_wait",
     "moe_status_string", "moe_version", "moe_permute_noalloc", "moe_forward_profiled",
     "moe_forward_launch_count", "moe_activation",
@@ -108,6 +109,7 @@ def lib() -> C.CDLL:
         "moe_workspace_guards": (C.c_int32, [CP, P, C.c_int32]),
         "moe_checks_read": (C.c_int32, [P, P, P, C.c_int32]),
         "moe_host_workspace_size": (C.c_size_t, [CP]),
+        "moe_forward_host_chunks": (C.c_int32, [CP]),
         "moe_router_topk": (C.c_int32, [CP, P, P, P, P, P, P, P, P]),
         "moe_permute": (C.c_int32, [CP, P, P, P, P, P, P, P, P, P, C.c_size_t, P]),
         "moe_permute_noalloc": (C.c_int32, [CP, P, P, P, P, P, P, P, P, P]),
@@ -242,6 +244,10 @@ def ffn_kernel_name(cfg: MoeConfig, linear: int) -> str | None:
 
 def host_workspace_size(cfg: MoeConfig) -> int:
     return int(lib().moe_host_workspace_size(C.byref(cfg)))
+
+
+def forward_host_chunks(cfg: MoeConfig) -> int:
+    return int(lib().moe_forward_host_chunks(C.byref(cfg)))
 
 
 def permute_scratch_size(cfg: MoeConfig) -> int:

@@ -5,6 +5,7 @@
 
 #include <atomic>
 #include <cmath>
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -490,9 +491,18 @@ moe_status moe_load_stats(const moe_config* cfg, const float* prob_partials,
                                        dropped, cv_squared, static_cast<cudaStream_t>(stream)));
 }
 
+// One token chunk of a batch (moe_forward_host): the router writes its
+// probability partial-sum rows to prob_rows, and the chunk computes no
+// statistics (counts and kept are still written; the batch's statistics come
+// after the last chunk).
+struct ChunkMode {
+  float* prob_rows;
+};
+
 static moe_status forward_impl(const moe_config* cfg, const void* x, const moe_weights* w,
                                const moe_outputs* out, void* workspace, size_t workspace_bytes,
-                               void* const* events, void* stream) {
+                               void* const* events, void* stream,
+                               const ChunkMode* chunk = nullptr) {
   moe_status st = check_config(cfg);
   if (st != MOE_OK) return st;
   const moe_config& c = *cfg;
@@ -523,7 +533,8 @@ static moe_status forward_impl(const moe_config* cfg, const void* x, const moe_w
   const NvtxRange call_range("moe_forward");
   // a few tokens and experts: router, sort and statistics in the two
   // front-end kernels, then the row copy
-  const bool front = ws.front_part != nullptr;
+  const bool front = ws.front_part != nullptr && chunk == nullptr;
+  float* prob_rows = chunk ? chunk->prob_rows : ws.prob_partials;
   cudaError_t e = record_event(ev[0], s);
   if (e == cudaSuccess) {
     const NvtxRange r("router_topk");
@@ -534,11 +545,11 @@ static moe_status forward_impl(const moe_config* cfg, const void* x, const moe_w
                              out->cv_squared, s);
     else
       e = launch_router(c, x, w->W_g, w->b_g, logits, out->topk_idx, out->topk_w,
-                        ws.prob_partials, di.num_sms, di.status, g_wait_limit_ns.load(), s);
+                        prob_rows, di.num_sms, di.status, g_wait_limit_ns.load(), s);
   }
   if (e == cudaSuccess) e = record_event(ev[1], s);
   // small layers: the one-block permutation also computes the load statistics
-  const bool fused_stats = front || permute_fuses_stats(c);
+  const bool fused_stats = chunk == nullptr && (front || permute_fuses_stats(c));
   const StatsArgs stats{ws.prob_partials, int(router_blocks_of(c)), out->mean_prob,
                         out->balance, out->dropped, out->cv_squared};
   if (e == cudaSuccess) {
@@ -570,7 +581,7 @@ static moe_status forward_impl(const moe_config* cfg, const void* x, const moe_w
     e = launch_combine(c, ws.Yp, ws.token_row, out->topk_w, ws.offsets, out->y, s);
   }
   if (e == cudaSuccess) e = record_event(ev[5], s);
-  if (e == cudaSuccess && !fused_stats) {
+  if (e == cudaSuccess && !fused_stats && chunk == nullptr) {
     const NvtxRange r("load_stats");
     e = launch_load_stats(c, ws.prob_partials, out->counts, out->kept, out->mean_prob,
                           out->balance, out->dropped, out->cv_squared, s);
@@ -610,6 +621,54 @@ const char* moe_ffn_kernel_name(const moe_config* cfg, int32_t linear) {
   return grouped_linear_kernel_name(*cfg, linear, 0);
 }
 
+// Chunk halves: tokens [0, T0) and [T0, T), T0 a multiple of 4 so that every
+// per-token array of the second chunk starts on a 16-byte boundary.
+static moe_config chunk_cfg(const moe_config& c, int i) {
+  moe_config h = c;
+  const int64_t t0 = (c.T / 2) & ~int64_t(3);
+  h.T = i == 0 ? t0 : c.T - t0;
+  return h;
+}
+
+// moe_forward_host overlaps its copies with the layer by running the batch as
+// two token chunks on the caller's stream, with the copies on a second stream:
+// chunk 1's tokens go in while chunk 0 runs, chunk 0's results come out while
+// chunk 1 runs.  Per token nothing changes -- routing, the grouped rows and the
+// combine are per token, and a half runs the same grouped-FFN kernels as the
+// whole batch -- so it is only done when that holds: no capacity (which would
+// depend on the whole batch), at least 1024 tokens, the same kernels, and
+// either FFN work above the ridge for a half (>= 256 rows per expert) or
+// weights small enough to be read twice (<= 96 MB).  The statistics of the
+// whole batch come from both chunks' partial sums after the second chunk.
+static int host_chunks(const moe_config& c) {
+  if (c.capacity > 0 || c.T < 1024 || c.dtype != MOE_BF16) return 1;
+  const moe_config h = chunk_cfg(c, 0);
+  if (small_front_fits(h)) return 1;
+  for (int linear = 1; linear <= 2; ++linear) {
+    const char* a = grouped_linear_kernel_name(c, linear, 0);
+    const char* b = grouped_linear_kernel_name(h, linear, 0);
+    if (a == nullptr || b == nullptr || std::strcmp(a, b) != 0) return 1;
+  }
+  if (linear_saves_pre(c) != linear_saves_pre(h)) return 1;
+  const double rows_per_group = double(h.T * h.top_k) / double(c.n_experts);
+  const double wbytes = 4.0 * double(c.n_experts + (c.d_ff_shared > 0 ? 1 : 0)) *
+                        double(c.d_model) * double(c.d_ff);   // both Linears, bf16
+  if (rows_per_group < 256.0 && wbytes > 96.0 * 1024 * 1024) return 1;
+  return 2;
+}
+
+// Bytes of the chunked path's scratch: both chunks' probability partial-sum
+// rows, their counts and kept counts, and per-chunk statistics outputs the
+// chunks do not fill.
+static size_t chunk_scratch_bytes(const moe_config& c) {
+  if (host_chunks(c) < 2) return 0;
+  auto r = [](size_t n) { return (n + 255) / 256 * 256; };
+  const size_t N = size_t(c.n_experts);
+  const size_t rows = size_t(router_partial_rows(chunk_cfg(c, 0)) +
+                             router_partial_rows(chunk_cfg(c, 1)));
+  return r(rows * N * 4) + 5 * r(N * 4) + 3 * r(4);
+}
+
 size_t moe_host_workspace_size(const moe_config* cfg) {
   if (check_config(cfg) != MOE_OK) return 0;
   const moe_config& c = *cfg;
@@ -617,7 +676,39 @@ size_t moe_host_workspace_size(const moe_config* cfg) {
   const size_t es = size_t(elem_bytes(c));
   return layout(c, nullptr).bytes + 2 * r(size_t(c.T * c.d_model) * es) +
          2 * r(size_t(c.T * c.top_k) * 4) + 3 * r(size_t(c.n_experts) * 4) + 3 * r(4) +
-         r(size_t(c.T * c.n_experts) * 4);   // dropped, balance, cv_squared; logits
+         r(size_t(c.T * c.n_experts) * 4) +   // dropped, balance, cv_squared; logits
+         chunk_scratch_bytes(c);
+}
+
+int32_t moe_forward_host_chunks(const moe_config* cfg) {
+  if (check_config(cfg) != MOE_OK) return -1;
+  return host_chunks(*cfg);
+}
+
+// The second stream and the events of the chunked path, one set per device and
+// context; a call holds its device's lock from the first copy to the final
+// synchronise, so concurrent callers do not share them.
+struct HostPipe {
+  uint64_t ctx = 0;
+  cudaStream_t copy = nullptr;
+  cudaEvent_t ev[6] = {};
+  std::mutex mu;
+};
+
+static HostPipe* host_pipe(int dev) {
+  static HostPipe pipes[64];
+  if (dev < 0 || dev >= 64) return nullptr;
+  return &pipes[dev];
+}
+
+static bool host_pipe_ready(HostPipe* hp) {
+  const uint64_t ctx = context_id();
+  if (hp->copy != nullptr && hp->ctx == ctx) return true;
+  if (cudaStreamCreateWithFlags(&hp->copy, cudaStreamNonBlocking) != cudaSuccess) return false;
+  for (cudaEvent_t& e : hp->ev)
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return false;
+  hp->ctx = ctx;
+  return true;
 }
 
 moe_status moe_forward_host(const moe_config* cfg, const void* x_host, const moe_weights* w,
@@ -655,25 +746,109 @@ moe_status moe_forward_host(const moe_config* cfg, const void* x_host, const moe
   od.cv_squared = oh->cv_squared ? static_cast<float*>(take(4)) : nullptr;
   od.pre_act = nullptr;                              // device-only: not kept here
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (xb && cudaMemcpyAsync(xd, x_host, xb, cudaMemcpyHostToDevice, s) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  st = moe_forward(cfg, xd, w, &od, workspace, base, stream);
-  if (st != MOE_OK) return st;
   struct Copy { void* dst; const void* src; size_t n; };
-  const Copy copies[] = {{oh->y, od.y, xb},
-                         {oh->topk_idx, od.topk_idx, kb},
-                         {oh->topk_w, od.topk_w, kb},
-                         {oh->counts, od.counts, nb},
-                         {oh->kept, od.kept, nb},
-                         {oh->mean_prob, od.mean_prob, nb},
-                         {oh->dropped, od.dropped, 4},
-                         {oh->balance, od.balance, 4},
-                         {oh->logits, od.logits, oh->logits ? lb : 0},
-                         {oh->cv_squared, od.cv_squared, oh->cv_squared ? size_t(4) : 0}};
-  for (const Copy& cp : copies)
-    if (cp.n && cudaMemcpyAsync(cp.dst, cp.src, cp.n, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+  const Copy small[] = {{oh->counts, od.counts, nb},
+                        {oh->kept, od.kept, nb},
+                        {oh->mean_prob, od.mean_prob, nb},
+                        {oh->dropped, od.dropped, 4},
+                        {oh->balance, od.balance, 4},
+                        {oh->cv_squared, od.cv_squared, oh->cv_squared ? size_t(4) : 0}};
+
+  if (host_chunks(c) < 2) {
+    if (xb && cudaMemcpyAsync(xd, x_host, xb, cudaMemcpyHostToDevice, s) != cudaSuccess)
       return MOE_ERR_CUDA;
-  return cuda_status(cudaStreamSynchronize(s));
+    st = moe_forward(cfg, xd, w, &od, workspace, base, stream);
+    if (st != MOE_OK) return st;
+    const Copy big[] = {{oh->y, od.y, xb},
+                        {oh->topk_idx, od.topk_idx, kb},
+                        {oh->topk_w, od.topk_w, kb},
+                        {oh->logits, od.logits, oh->logits ? lb : 0}};
+    for (const Copy& cp : big)
+      if (cp.n && cudaMemcpyAsync(cp.dst, cp.src, cp.n, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    for (const Copy& cp : small)
+      if (cp.n && cudaMemcpyAsync(cp.dst, cp.src, cp.n, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return cuda_status(cudaStreamSynchronize(s));
+  }
+
+  // two chunks: scratch for their partial sums, counts and unused statistics
+  const size_t N = size_t(c.n_experts);
+  const moe_config ch[2] = {chunk_cfg(c, 0), chunk_cfg(c, 1)};
+  const int64_t rows0 = router_partial_rows(ch[0]), rows1 = router_partial_rows(ch[1]);
+  float* prob_rows = static_cast<float*>(take(size_t(rows0 + rows1) * N * 4));
+  int32_t* counts_ch[2] = {static_cast<int32_t*>(take(N * 4)), static_cast<int32_t*>(take(N * 4))};
+  int32_t* kept_ch[2] = {static_cast<int32_t*>(take(N * 4)), static_cast<int32_t*>(take(N * 4))};
+  float* scratch_mean = static_cast<float*>(take(N * 4));
+  int32_t* scratch_dropped = static_cast<int32_t*>(take(4));
+  float* scratch_balance = static_cast<float*>(take(4));
+  float* scratch_cv = static_cast<float*>(take(4));
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  HostPipe* hp = host_pipe(dev);
+  if (!hp) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(hp->mu);
+  if (!host_pipe_ready(hp)) return MOE_ERR_CUDA;
+  cudaStream_t cs = hp->copy;
+  cudaEvent_t fork = hp->ev[0], in_done[2] = {hp->ev[1], hp->ev[2]},
+              out_ready[2] = {hp->ev[3], hp->ev[4]}, stats_done = hp->ev[5];
+  auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  // the copies start after the caller's earlier work on `stream`
+  if (!ok(cudaEventRecord(fork, s)) || !ok(cudaStreamWaitEvent(cs, fork, 0))) return MOE_ERR_CUDA;
+  const size_t row_bytes = size_t(c.d_model) * es;
+  int64_t t0 = 0;
+  for (int i = 0; i < 2; ++i) {
+    const size_t n = size_t(ch[i].T) * row_bytes;
+    if (!ok(cudaMemcpyAsync(static_cast<uint8_t*>(xd) + t0 * row_bytes,
+                            static_cast<const uint8_t*>(x_host) + t0 * row_bytes, n,
+                            cudaMemcpyHostToDevice, cs)) ||
+        !ok(cudaEventRecord(in_done[i], cs)))
+      return MOE_ERR_CUDA;
+    t0 += ch[i].T;
+  }
+  t0 = 0;
+  for (int i = 0; i < 2; ++i) {
+    const int64_t Ti = ch[i].T, k = c.top_k;
+    moe_outputs oc{};
+    oc.y = static_cast<uint8_t*>(od.y) + t0 * row_bytes;
+    oc.topk_idx = od.topk_idx + t0 * k;
+    oc.topk_w = od.topk_w + t0 * k;
+    oc.counts = counts_ch[i];
+    oc.kept = kept_ch[i];
+    oc.mean_prob = scratch_mean;
+    oc.dropped = scratch_dropped;
+    oc.balance = scratch_balance;
+    oc.cv_squared = scratch_cv;
+    oc.logits = od.logits ? od.logits + t0 * int64_t(N) : nullptr;
+    oc.pre_act = nullptr;
+    const ChunkMode mode{prob_rows + (i == 0 ? 0 : rows0) * int64_t(N)};
+    if (!ok(cudaStreamWaitEvent(s, in_done[i], 0))) return MOE_ERR_CUDA;
+    st = forward_impl(&ch[i], static_cast<uint8_t*>(xd) + t0 * row_bytes, w, &oc, workspace,
+                      base, nullptr, stream, &mode);
+    if (st != MOE_OK) return st;
+    if (!ok(cudaEventRecord(out_ready[i], s)) || !ok(cudaStreamWaitEvent(cs, out_ready[i], 0)))
+      return MOE_ERR_CUDA;
+    const Copy out[] = {{static_cast<uint8_t*>(oh->y) + t0 * row_bytes, oc.y, size_t(Ti) * row_bytes},
+                        {static_cast<int32_t*>(oh->topk_idx) + t0 * k, oc.topk_idx, size_t(Ti * k) * 4},
+                        {static_cast<float*>(oh->topk_w) + t0 * k, oc.topk_w, size_t(Ti * k) * 4},
+                        {oh->logits ? static_cast<float*>(oh->logits) + t0 * int64_t(N) : nullptr,
+                         oc.logits, oh->logits ? size_t(Ti) * N * 4 : 0}};
+    for (const Copy& cp : out)
+      if (cp.n && !ok(cudaMemcpyAsync(cp.dst, cp.src, cp.n, cudaMemcpyDeviceToHost, cs)))
+        return MOE_ERR_CUDA;
+    t0 += Ti;
+  }
+  if (!ok(launch_chunk_stats(c, prob_rows, int(rows0 + rows1), counts_ch[0], kept_ch[0],
+                             counts_ch[1], kept_ch[1], od.counts, od.kept, od.mean_prob,
+                             od.balance, od.dropped, od.cv_squared, s)) ||
+      !ok(cudaEventRecord(stats_done, s)) || !ok(cudaStreamWaitEvent(cs, stats_done, 0)))
+    return MOE_ERR_CUDA;
+  for (const Copy& cp : small)
+    if (cp.n && !ok(cudaMemcpyAsync(cp.dst, cp.src, cp.n, cudaMemcpyDeviceToHost, cs)))
+      return MOE_ERR_CUDA;
+  // every copy is on `cs`, after all of the layer's work on `stream`
+  return cuda_status(cudaStreamSynchronize(cs));
 }
 
 // ---- backward ----------------------------------------------------------------------

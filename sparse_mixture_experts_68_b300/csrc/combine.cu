@@ -114,7 +114,38 @@ __global__ void __launch_bounds__(kStatsThreads)
                    cv_squared);
 }
 
+// Statistics of a batch run as two consecutive token chunks (moe_forward_host):
+// the chunks' routed and kept counts added per expert, then the statistics
+// from both chunks' probability partial-sum rows.
+__global__ void __launch_bounds__(kStatsThreads)
+    chunk_stats_kernel(const float* __restrict__ prob_rows, int nblk, int N, int Ttok,
+                       const int32_t* __restrict__ counts0, const int32_t* __restrict__ kept0,
+                       const int32_t* __restrict__ counts1, const int32_t* __restrict__ kept1,
+                       int32_t* __restrict__ counts, int32_t* __restrict__ kept,
+                       float* __restrict__ mean_prob, float* __restrict__ balance,
+                       int32_t* __restrict__ dropped, float* __restrict__ cv_squared) {
+  pdl_launch_dependents();
+  pdl_wait_previous();
+  for (int e = threadIdx.x; e < N; e += blockDim.x) {
+    counts[e] = counts0[e] + counts1[e];
+    kept[e] = kept0[e] + kept1[e];
+  }
+  __syncthreads();
+  block_load_stats(prob_rows, nblk, N, Ttok, counts, kept, mean_prob, balance, dropped,
+                   cv_squared);
+}
+
 }  // namespace
+
+cudaError_t launch_chunk_stats(const moe_config& c, const float* prob_rows, int nblk,
+                               const int32_t* counts0, const int32_t* kept0,
+                               const int32_t* counts1, const int32_t* kept1, int32_t* counts,
+                               int32_t* kept, float* mean_prob, float* balance,
+                               int32_t* dropped, float* cv_squared, cudaStream_t s) {
+  return launch_pdl(chunk_stats_kernel, dim3(1), dim3(kStatsThreads), 0, s, prob_rows, nblk,
+                    int(c.n_experts), int(c.T), counts0, kept0, counts1, kept1, counts, kept,
+                    mean_prob, balance, dropped, cv_squared);
+}
 
 cudaError_t launch_combine(const moe_config& c, const void* Yp, const int32_t* token_row,
                            const float* topk_w, const int32_t* offsets, void* y,

@@ -211,6 +211,14 @@ cudaError_t launch_load_stats(const moe_config& c, const float* prob_partials,
                               const int32_t* counts, const int32_t* kept, float* mean_prob,
                               float* balance, int32_t* dropped, float* cv_squared,
                               cudaStream_t s);
+// Statistics of a batch run as two consecutive token chunks: counts and kept
+// summed from the chunks' arrays, then the statistics of the whole batch
+// (c.T tokens) from nblk partial-sum rows (both chunks' rows).
+cudaError_t launch_chunk_stats(const moe_config& c, const float* prob_rows, int nblk,
+                               const int32_t* counts0, const int32_t* kept0,
+                               const int32_t* counts1, const int32_t* kept1, int32_t* counts,
+                               int32_t* kept, float* mean_prob, float* balance,
+                               int32_t* dropped, float* cv_squared, cudaStream_t s);
 
 // ---- kernels launched per step, for the chosen dispatch ------------------------------
 // Router scores, softmax, top-k, gates and the per-tile sums of p for 64

@@ -55,11 +55,21 @@ def test_sizes(lib):
     c1 = B.make_config(WORKLOADS["c1_page1_bf16"])
     assert B.rows_max(c1) == 2048 * 2 + 8 * 127
     # the host path's extra room: x and y, topk_idx and topk_w, counts, kept and
-    # mean_prob, dropped, balance and cv_squared, logits; each 256-byte rounded
+    # mean_prob, dropped, balance and cv_squared, logits; each 256-byte rounded.
+    # This layer runs as two chunks of 1024 tokens, which adds both chunks'
+    # probability partial-sum rows (128 router blocks each), their counts and
+    # kept counts, and unused per-chunk statistics.
     r = lambda n: (n + 255) // 256 * 256
     T, d, k, N = 2048, 768, 2, 8
     extra = 2 * r(T * d * 2) + 2 * r(T * k * 4) + 3 * r(N * 4) + 3 * r(4) + r(T * N * 4)
+    assert B.forward_host_chunks(c1) == 2
+    extra += r(256 * N * 4) + 5 * r(N * 4) + 3 * r(4)
     assert B.host_workspace_size(c1) - B.workspace_size(c1) == extra
+    # capacity, few tokens, or a half with less FFN work than the ridge and
+    # weights that do not fit in L2: one pass
+    for name in ("c2_switch_top1", "c3_mixtral_decode", "c4_deepseek_v3", "c0_pr1_fp32"):
+        assert B.forward_host_chunks(B.make_config(WORKLOADS[name])) == 1, name
+    assert B.forward_host_chunks(B.make_config(WORKLOADS["c3_mixtral_prefill"])) == 2
 
 
 @pytest.mark.parametrize("field,value,status", [

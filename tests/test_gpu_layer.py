@@ -253,6 +253,35 @@ def test_forward_host_matches_device_path():
     assert torch.equal(oh.logits, out.logits.cpu())
 
 
+@pytest.mark.parametrize("wl", [
+    Workload("host_chunks", T=2048, d_model=256, d_ff=512, n_experts=8, top_k=2,
+             dtype=DT_BF16, seed=46),
+    # an odd token count (halves of 1024 and 1027 tokens) with a shared expert
+    Workload("host_chunks_shared", T=2051, d_model=128, d_ff=256, n_experts=4, top_k=2,
+             act=ACT_RELU, dtype=DT_BF16, d_ff_shared=256, seed=47),
+], ids=lambda w: w.name)
+def test_forward_host_in_two_chunks_matches_device_path(wl):
+    """moe_forward_host runs these layers as two token chunks, the copies
+    overlapping the layer on a second stream: per-token results and the counts
+    are those of moe_forward bit for bit, the statistics (summed over both
+    chunks' partial sums) equal up to fp32 rounding; two calls agree."""
+    t, layer, out = run_layer(wl)
+    cfg = layer.cfg
+    assert B.forward_host_chunks(cfg) == 2
+    ws = torch.empty(B.host_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    xh = t["x"].cpu().pin_memory()
+    for _ in range(2):
+        oh = B.alloc_outputs(cfg, "cpu", with_logits=True, pin_memory=True)
+        B.forward_host(cfg, xh, layer.weights, oh, ws)
+        for name in ("y", "topk_idx", "topk_w", "counts", "kept", "dropped", "logits"):
+            assert torch.equal(getattr(oh, name), getattr(out, name).cpu()), name
+        for name in ("mean_prob", "balance", "cv_squared"):
+            np.testing.assert_allclose(getattr(oh, name).numpy(),
+                                       getattr(out, name).cpu().numpy(), rtol=1e-5, atol=1e-7,
+                                       err_msg=name)
+    assert B.get_device_status() == B.MOE_OK
+
+
 def test_bounded_wait_reports_timeout_and_context_survives():
     B.selftest_bounded_wait(2_000_000)            # 2 ms; nothing ever arrives
     assert B.get_device_status() == B.MOE_ERR_TIMEOUT
