@@ -311,6 +311,140 @@ __global__ void __launch_bounds__(kSortWarps * 32)
   }
 }
 
+// Mid-size layers: the same counting sort in two launches over blocks of
+// kMidThreads assignments (one per thread), so that it runs on several SMs.
+//   mid_rank    : per block, each assignment's rank among its expert's
+//                 assignments in the block (__match_any_sync within each warp,
+//                 then a per-expert scan over the block's warps) and the
+//                 block's per-expert counts
+//   mid_scatter : every block sums the counts of all blocks (totals, capacity,
+//                 padded group offsets) and of the blocks before it (its base
+//                 ranks), then writes its assignments' rows; block 0 also
+//                 writes counts, kept, offsets and the padding rows.  With
+//                 statistics requested, one more block computes them from the
+//                 same totals, beside the scatter.
+// Ranks follow token-major assignment order, as in the other two paths.
+constexpr int kMidThreads = kStatsThreads;
+constexpr int kMidWarps = kMidThreads / 32;
+
+__global__ void __launch_bounds__(kMidThreads)
+    permute_mid_rank_kernel(const int32_t* __restrict__ topk_idx, int A, int N,
+                            int32_t* __restrict__ block_counts, int32_t* __restrict__ lrank) {
+  extern __shared__ int32_t wc[];                 // [kMidWarps][N] counts, then bases
+  pdl_launch_dependents();
+  pdl_wait_previous();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < kMidWarps * N; i += kMidThreads) wc[i] = 0;
+  __syncthreads();
+  const int a = blockIdx.x * kMidThreads + threadIdx.x;
+  const int e = a < A ? topk_idx[a] : -1;
+  const bool valid = e >= 0 && e < N;             // out-of-range experts: dropped
+  MOE_CHECK(a >= A || valid, CK_SORT_EXPERT);
+  const int key = valid ? e : (0x40000000 | lane);
+  const uint32_t same = __match_any_sync(0xffffffffu, key);
+  const int r = __popc(same & ((1u << lane) - 1u));
+  if (valid && r == 0) wc[warp * N + e] = __popc(same);   // one leader per expert and warp
+  __syncthreads();
+  for (int x = threadIdx.x; x < N; x += kMidThreads) {
+    int32_t run = 0;
+    for (int w = 0; w < kMidWarps; ++w) {
+      const int32_t c = wc[w * N + x];
+      wc[w * N + x] = run;
+      run += c;
+    }
+    block_counts[int64_t(blockIdx.x) * N + x] = run;
+  }
+  __syncthreads();
+  if (a < A) lrank[a] = valid ? wc[warp * N + e] + r : -1;
+}
+
+// N <= kMidThreads: thread e owns expert e.
+__global__ void __launch_bounds__(kMidThreads)
+    permute_mid_scatter_kernel(const int32_t* __restrict__ topk_idx,
+                               const int32_t* __restrict__ lrank,
+                               const int32_t* __restrict__ block_counts, int nblk, int T, int k,
+                               int N, int64_t capacity, int has_shared,
+                               int32_t* __restrict__ counts, int32_t* __restrict__ kept,
+                               int32_t* __restrict__ offsets, int32_t* __restrict__ row_token,
+                               int32_t* __restrict__ token_row, StatsArgs stats) {
+  extern __shared__ int32_t sm[];
+  int32_t* base = sm;                             // [N] this block's base rank per expert
+  int32_t* kp = base + N;                         // [N] kept
+  int32_t* off = kp + N;                          // [N] group offsets; the stats block: counts
+  __shared__ int32_t warp_tot[kMidWarps];
+  pdl_launch_dependents();
+  pdl_wait_previous();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e_me = threadIdx.x;
+  const bool stats_block = int(blockIdx.x) == nblk;
+  int32_t tot = 0, mine = 0, kv = 0;
+  if (e_me < N) {
+    for (int b = 0; b < nblk; ++b) {
+      const int32_t c = block_counts[int64_t(b) * N + e_me];
+      if (b == int(blockIdx.x)) mine = tot;
+      tot += c;
+    }
+    kv = (capacity > 0 && int64_t(tot) > capacity) ? int32_t(capacity) : tot;
+    base[e_me] = mine;
+    kp[e_me] = kv;
+  }
+  if (stats_block) {
+    if (e_me < N) off[e_me] = tot;
+    __syncthreads();
+    // counts and kept from shared memory (generic pointers)
+    block_load_stats(stats.prob_partials, stats.nblk, N, T, off, kp, stats.mean_prob,
+                     stats.balance, stats.dropped, stats.cv_squared);
+    return;
+  }
+  if (blockIdx.x == 0 && e_me < N) {
+    counts[e_me] = tot;
+    kept[e_me] = kv;
+  }
+  // exclusive scan of the padded sizes over experts
+  const int32_t padded = e_me < N ? int32_t(round_up(kv, kGroupAlign)) : 0;
+  int32_t incl = padded;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  int32_t before = 0;
+  for (int w = 0; w < warp; ++w) before += warp_tot[w];
+  const int32_t excl = before + incl - padded;
+  if (e_me < N) {
+    off[e_me] = excl;
+    if (blockIdx.x == 0) offsets[e_me] = excl;
+  }
+  if (blockIdx.x == 0 && e_me == N - 1) {
+    offsets[N] = excl + padded;
+    offsets[N + 1] = excl + padded + (has_shared ? int32_t(round_up(T, kGroupAlign)) : 0);
+  }
+  __syncthreads();
+  if (blockIdx.x == 0) {
+    // padding rows (-1): warp w takes experts w, w + kMidWarps, ..., its lanes the rows
+    for (int e = warp; e < N; e += kMidWarps) {
+      const int32_t r0 = off[e] + kp[e], r1 = off[e] + int32_t(round_up(kp[e], kGroupAlign));
+      for (int32_t r = r0 + lane; r < r1; r += 32) row_token[r] = -1;
+    }
+  }
+  const int a = blockIdx.x * kMidThreads + threadIdx.x;
+  if (a < T * k) {
+    const int32_t lr = lrank[a];
+    int32_t row = -1;
+    if (lr >= 0) {
+      const int e = topk_idx[a];
+      const int32_t rank = base[e] + lr;
+      if (capacity <= 0 || rank < capacity) {
+        row = off[e] + rank;
+        row_token[row] = a / k;
+      }
+    }
+    token_row[a] = row;
+  }
+}
+
 size_t sort_smem_bytes(const moe_config& c) {
   const int64_t A = c.T * c.top_k;
   return size_t(kSortWarps * c.n_experts + 3 * c.n_experts + 32) * 4 + size_t(A) * 4 + 16;
@@ -322,6 +456,19 @@ constexpr int kSortSmemMax = 190 * 1024;
 bool single_block_sort_fits(const moe_config& c) {
   return c.n_experts <= kSortWarps * 32 && c.T * c.top_k <= 16384 &&
          sort_smem_bytes(c) <= size_t(kSortSmemMax);
+}
+
+// From kMidMinAssign assignments up the two-launch path spreads the one-block
+// sort's work over many SMs (its statistics then run as their own launch).
+constexpr int64_t kMidMinAssign = 2048;
+
+inline int64_t mid_blocks(const moe_config& c) {
+  return ceil_div(c.T * c.top_k, kMidThreads);
+}
+
+bool mid_sort_used(const moe_config& c) {
+  return single_block_sort_fits(c) && c.n_experts <= kMidThreads &&
+         c.T * c.top_k >= kMidMinAssign;
 }
 
 // Lets permute_sort_kernel take up to kSortSmemMax of dynamic shared memory:
@@ -389,7 +536,13 @@ __global__ void __launch_bounds__(256)
 
 size_t permute_scratch_bytes(const moe_config& c) {
   const int64_t n = permute_blocks(c) * c.n_experts;
-  return size_t(2 * round_up(n, 64)) * sizeof(int32_t);
+  int64_t ints = 2 * round_up(n, 64);
+  if (mid_sort_used(c)) {
+    // [mid_blocks][N] counts, then [T * k] ranks
+    const int64_t m = round_up(mid_blocks(c) * c.n_experts, 64) + c.T * c.top_k;
+    if (m > ints) ints = m;
+  }
+  return size_t(ints) * sizeof(int32_t);
 }
 
 namespace {
@@ -421,6 +574,7 @@ cudaError_t launch_row_copy(const moe_config& c, const void* x, const int32_t* o
 
 int permute_launch_count(const moe_config& c) {
   const int copy = moe::rows_max_for(c) > 0 ? 1 : 0;
+  if (mid_sort_used(c)) return 2 + copy;
   if (single_block_sort_fits(c)) return 1 + copy;
   return (c.T > 0 ? 3 : 1) + copy;
 }
@@ -437,6 +591,25 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* to
   PermuteScratch p = carve(c, scratch);
   const size_t smemN = size_t(N) * sizeof(int32_t);
   cudaError_t e;
+  if (mid_sort_used(c)) {
+    const int A = T * k;
+    const int mb = int(mid_blocks(c));
+    int32_t* mcounts = static_cast<int32_t*>(scratch);
+    int32_t* lrank = mcounts + round_up(int64_t(mb) * N, 64);
+    e = launch_pdl(permute_mid_rank_kernel, dim3(mb), dim3(kMidThreads),
+                   size_t(kMidWarps) * N * sizeof(int32_t), s, topk_idx, A, N, mcounts, lrank);
+    if (e != cudaSuccess) return e;
+    const StatsArgs none{};
+    const bool with_stats = stats && stats->prob_partials;
+    e = launch_pdl(permute_mid_scatter_kernel, dim3(mb + (with_stats ? 1 : 0)),
+                   dim3(kMidThreads), size_t(3) * N * sizeof(int32_t), s,
+                   static_cast<const int32_t*>(topk_idx), static_cast<const int32_t*>(lrank),
+                   static_cast<const int32_t*>(mcounts), mb, T, k, N, c.capacity,
+                   c.d_ff_shared > 0 ? 1 : 0, counts, kept, offsets, row_token, token_row,
+                   with_stats ? *stats : none);
+    if (e != cudaSuccess) return e;
+    return launch_copy(c, x, offsets, row_token, Xp, rows_max, s, zero, n_zero);
+  }
   if (single_block_sort_fits(c)) {
     const size_t smem = sort_smem_bytes(c);
     e = allow_sort_smem();
