@@ -57,14 +57,16 @@ constexpr bool epi_is_dgrad(int e) { return e >= EPI_DGRAD_GELU && e <= EPI_DGRA
 // number of epilogue warps (a multiple of 4: one set per TMEM lane quarter).
 // STAGED: the epilogue's bf16 stores go through shared memory (16-column
 // pieces, warp_staged_store).
-template <int BN_, int STAGES_, int EPI_WARPS_, bool STAGED_ = true>
+// EXTRA: more shared memory for the epilogue (the router's reductions).
+template <int BN_, int STAGES_, int EPI_WARPS_, bool STAGED_ = true, int EXTRA_ = 0>
 struct TileCfg {
   static constexpr int BN = BN_;
   static constexpr int STAGES = STAGES_;
   static constexpr int EPI_WARPS = EPI_WARPS_;
   static constexpr int THREADS = (2 + EPI_WARPS) * 32;
   static constexpr bool STAGED = STAGED_;
-  static constexpr int STAGE_BYTES = STAGED_ ? EPI_WARPS_ * staged_warp_bytes<16>() : 0;
+  static constexpr int STAGE_BYTES =
+      (STAGED_ ? EPI_WARPS_ * staged_warp_bytes<16>() : 0) + EXTRA_;
 };
 
 template <int BN, int STAGES, int STAGE_BYTES = 0>
@@ -317,82 +319,134 @@ __device__ __forceinline__ void epi_bar_sync(int threads = 128) {
   asm volatile("bar.sync 1, %0;" ::"r"(threads) : "memory");
 }
 
-// EPI_ROUTER_TOPK, run by the four epilogue warps (128 threads, thread =
-// token row; CfgRouter, so that the 64 scores stay in registers): the row's 64 scores from TMEM + bias, written as fp32;
-// the softmax, k rounds of arg-max (the larger score first, then the lower
-// expert) and the gates, as in the router kernels; then the tile's column
-// sums of p -- a reduce-scatter across each warp's lanes (lane l ends with
-// experts 2l and 2l + 1), the four warps added in order through `red`
-// [4][64] -- written as row m of p.prob_rows.  Rows past the live ones add 0.
+// EPI_ROUTER_TOPK, run by the sixteen epilogue warps (CfgRouter): warp
+// (part, q) holds TMEM lane quarter q (32 token rows, thread = row) and score
+// columns [16 part, 16 part + 16), so that a row's 64 scores are spread over
+// four threads and each warp's code is short.  Per row: the scores + bias,
+// written as fp32; the maximum and the sum of exp(z - max) from the four
+// parts' partials (added in part order); the top k -- each part selects its
+// own k best (the larger score first, then the lower expert, as in the other
+// router kernels), and part 0 merges the four lists in the same order -- and
+// the gates; then the tile's column sums of p: a reduce-scatter across each
+// warp's lanes (lane l ends with column 16 part + l / 2), the four quarters
+// added in order, written as row m of p.prob_rows.  Rows past the live ones
+// add 0.  `red` holds RouterRed.
+constexpr int kRouterParts = 4;
+constexpr int kRouterMaxK = 8;
+struct RouterRed {
+  float mx[kRouterParts][128];
+  float sum[kRouterParts][128];
+  float cand_v[kRouterParts][kRouterMaxK][128];
+  uint8_t cand_e[kRouterParts][kRouterMaxK][128];
+  float col[4][64];
+};
+
 __device__ __forceinline__ void router_topk_rows(const TcParams& p, uint32_t taddr,
                                                  const __nv_bfloat16* __restrict__ bias,
-                                                 int row, bool valid, int m, int q, int lane,
-                                                 float* red) {
-  constexpr int NE = 64;
-  float z[NE];
+                                                 int row, bool valid, int m, int q, int part,
+                                                 int lane, RouterRed* red, int epi_threads) {
+  constexpr int NE = 64, NP = 16;
+  const int c0 = part * NP;
+  const int rl = q * 32 + lane;                  // row within the tile
+  float z[NP];
+  {
+    uint32_t r[NP];
+    tmem_ld_16cols(taddr + uint32_t(c0), r);
+    const uint4* bsrc = reinterpret_cast<const uint4*>(bias + c0);
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    uint32_t r[32];
-    tmem_ld_32cols(taddr + uint32_t(32 * h), r);
+    for (int v = 0; v < NP / 8; ++v) {
+      const uint4 bv = __ldg(bsrc + v);
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&bv);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) z[32 * h + i] = __uint_as_float(r[i]) + __bfloat162float(bias[32 * h + i]);
-  }
-  if (valid) {
-    float4* zo = reinterpret_cast<float4*>(static_cast<float*>(p.out) + int64_t(row) * NE);
-#pragma unroll
-    for (int v = 0; v < NE / 4; ++v)
-      zo[v] = make_float4(z[4 * v], z[4 * v + 1], z[4 * v + 2], z[4 * v + 3]);
-  }
-  float mx = -FLT_MAX;
-#pragma unroll
-  for (int i = 0; i < NE; ++i) mx = fmaxf(mx, z[i]);
-  const int k = p.top_k;
-  uint64_t taken = 0;
-  int sel_e[8];
-  float g[8], kept_sum = 0.f;                   // gates exp(z - max), unnormalised
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    sel_e[j] = 0;
-    g[j] = 0.f;
-    if (j < k) {
-      float bv = -INFINITY;
-      int be = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < NE; ++i)
-        if (!((taken >> i) & 1ull) && (z[i] > bv || (z[i] == bv && i < be))) {
-          bv = z[i];
-          be = i;
-        }
-      if (be < NE) taken |= 1ull << be;
-      sel_e[j] = be;
-      g[j] = expf(bv - mx);
-      kept_sum += g[j];
+      for (int i = 0; i < 4; ++i) {
+        const float2 bf = __bfloat1622float2(b2[i]);
+        z[8 * v + 2 * i] = __uint_as_float(r[8 * v + 2 * i]) + bf.x;
+        z[8 * v + 2 * i + 1] = __uint_as_float(r[8 * v + 2 * i + 1]) + bf.y;
+      }
     }
   }
-  float ssum = 0.f;
-#pragma unroll
-  for (int i = 0; i < NE; ++i) {
-    z[i] = expf(z[i] - mx);                     // z now holds exp(z - max)
-    ssum += z[i];
-  }
-  const float inv = 1.0f / ssum;
-  const float scale = p.renorm ? 1.0f / kept_sum : inv;
   if (valid) {
+    float4* zo = reinterpret_cast<float4*>(static_cast<float*>(p.out) + int64_t(row) * NE + c0);
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (j < k) {
-        MOE_CHECK(sel_e[j] >= 0 && sel_e[j] < NE, CK_ROUTER_TOPK);
-        p.topk_idx[int64_t(row) * k + j] = sel_e[j];
-        p.topk_w[int64_t(row) * k + j] = g[j] * scale;
+    for (int v = 0; v < NP / 4; ++v)
+      zo[v] = make_float4(z[4 * v], z[4 * v + 1], z[4 * v + 2], z[4 * v + 3]);
+  }
+  float mp = -FLT_MAX;
+#pragma unroll
+  for (int i = 0; i < NP; ++i) mp = fmaxf(mp, z[i]);
+  red->mx[part][rl] = mp;
+  // this part's k best, in selection order
+  const int k = p.top_k;
+  uint32_t taken = 0;
+#pragma unroll 1
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int be = 0xff;
+#pragma unroll
+    for (int i = 0; i < NP; ++i)
+      if (!((taken >> i) & 1u) && (z[i] > bv || (z[i] == bv && c0 + i < be))) {
+        bv = z[i];
+        be = c0 + i;
       }
+    if (be < NE) taken |= 1u << (be - c0);
+    red->cand_v[part][j][rl] = bv;
+    red->cand_e[part][j][rl] = uint8_t(be);
+  }
+  epi_bar_sync(epi_threads);
+  const float mx = fmaxf(fmaxf(red->mx[0][rl], red->mx[1][rl]),
+                         fmaxf(red->mx[2][rl], red->mx[3][rl]));
+  float sp = 0.f;
+#pragma unroll
+  for (int i = 0; i < NP; ++i) {
+    z[i] = expf(z[i] - mx);                      // z now holds exp(z - max)
+    sp += z[i];
+  }
+  red->sum[part][rl] = sp;
+  epi_bar_sync(epi_threads);
+  const float ssum = ((red->sum[0][rl] + red->sum[1][rl]) + red->sum[2][rl]) + red->sum[3][rl];
+  const float inv = 1.0f / ssum;
+  if (part == 0) {
+    // merge the four parts' lists: k rounds over the list heads
+    int h0 = 0, h1 = 0, h2 = 0, h3 = 0;
+    float kept_sum = 0.f;
+#pragma unroll 1
+    for (int j = 0; j < k; ++j) {
+      float bv = -INFINITY;
+      int be = 0x7fffffff, bp = -1;
+#pragma unroll
+      for (int pp = 0; pp < kRouterParts; ++pp) {
+        const int h = pp == 0 ? h0 : pp == 1 ? h1 : pp == 2 ? h2 : h3;
+        if (h >= k) continue;
+        const float v = red->cand_v[pp][h][rl];
+        const int e = red->cand_e[pp][h][rl];
+        if (v > bv || (v == bv && e < be)) {
+          bv = v;
+          be = e;
+          bp = pp;
+        }
+      }
+      h0 += bp == 0; h1 += bp == 1; h2 += bp == 2; h3 += bp == 3;
+      const float g = expf(bv - mx);
+      kept_sum += g;
+      if (valid) {
+        MOE_CHECK(be >= 0 && be < NE, CK_ROUTER_TOPK);
+        p.topk_idx[int64_t(row) * k + j] = be;
+        p.topk_w[int64_t(row) * k + j] = g;      // unnormalised for now
+      }
+    }
+    if (valid) {
+      const float scale = p.renorm ? 1.0f / kept_sum : inv;
+#pragma unroll 1
+      for (int j = 0; j < k; ++j) p.topk_w[int64_t(row) * k + j] *= scale;
+    }
   }
   // column sums of p over the tile's rows: reduce-scatter across the lanes
 #pragma unroll
-  for (int i = 0; i < NE; ++i) z[i] = valid ? z[i] * inv : 0.f;
+  for (int i = 0; i < NP; ++i) z[i] = valid ? z[i] * inv : 0.f;
 #pragma unroll
-  for (int step = 0; step < 5; ++step) {
+  for (int step = 0; step < 4; ++step) {
     const int o = 16 >> step;
-    const int S = NE >> step;                   // values still held per lane
+    const int S = NP >> step;                    // values still held per lane
     const bool upper = (lane & o) != 0;
 #pragma unroll
     for (int i = 0; i < S / 2; ++i) {
@@ -401,12 +455,16 @@ __device__ __forceinline__ void router_topk_rows(const TcParams& p, uint32_t tad
       z[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
     }
   }
-  red[q * NE + 2 * lane] = z[0];
-  red[q * NE + 2 * lane + 1] = z[1];
-  epi_bar_sync();
-  const int e = q * 32 + lane;
-  if (e < NE) p.prob_rows[int64_t(m) * NE + e] = ((red[e] + red[NE + e]) + red[2 * NE + e]) + red[3 * NE + e];
-  epi_bar_sync();                               // red is read before the next tile
+  z[0] += __shfl_xor_sync(0xffffffffu, z[0], 1);
+  if ((lane & 1) == 0) red->col[q][c0 + (lane >> 1)] = z[0];
+  epi_bar_sync(epi_threads);
+  if (part == 0) {
+    const int e = q * 32 + lane;
+    if (e < NE)
+      p.prob_rows[int64_t(m) * NE + e] =
+          ((red->col[0][e] + red->col[1][e]) + red->col[2][e]) + red->col[3][e];
+  }
+  epi_bar_sync(epi_threads);                     // red is read before the next tile
 }
 
 template <class CFG, int EPI, int MINB>
@@ -590,9 +648,10 @@ __global__ void __launch_bounds__(CFG::THREADS, MINB)
       constexpr int kOutBytes = EPI == EPI_BIAS_F32 ? 4 : 2;
       constexpr bool kStaged = CFG::STAGED && EPI != EPI_BIAS_F32;
       if constexpr (EPI == EPI_ROUTER_TOPK) {
-        if (part == 0) router_topk_rows(p, tmem_base + (uint32_t(q * 32) << 16) + acc * BN,
-                                        bias, row_in_group, valid, tc.m, q, lane,
-                                        reinterpret_cast<float*>(smem + L::kStage));
+        static_assert(kEpiWarps == 4 * kRouterParts && BN == 64, "router epilogue layout");
+        router_topk_rows(p, tmem_base + (uint32_t(q * 32) << 16) + acc * BN, bias,
+                         row_in_group, valid, tc.m, q, part, lane,
+                         reinterpret_cast<RouterRed*>(smem + L::kStage), kEpiWarps * 32);
       } else
 #pragma unroll 1
       for (int c = part * kCols; c < (part + 1) * kCols; c += CW) {
@@ -1043,7 +1102,6 @@ struct LayoutSw {
   }
 };
 constexpr int kSwapMaxStages = 10;
-constexpr int kSwapMaxNb = 256;
 constexpr int kSmemBudget = 227 * 1024;
 
 __host__ __device__ constexpr uint32_t idesc_swap_bf16_f32(int nb) {
@@ -1398,7 +1456,9 @@ using Cfg128 = TileCfg<128, 4, 16>;
 using Cfg64 = TileCfg<64, 6, 16>;
 using Cfg128x2 = TileCfg<128, 3, 8, false>;  // two CTAs per SM, 96 KB ring each
 using Cfg256Pair = TileCfg<256, 6, 16>;    // CTA pair, 256 x 256 tiles, 6 x 32 KB ring per CTA
-using CfgRouter = TileCfg<64, 6, 4>;       // router with the top-k epilogue: a thread holds a row
+// router with the top-k epilogue: four warps per TMEM lane quarter, a row's
+// 64 scores split over four threads (router_topk_rows)
+using CfgRouter = TileCfg<64, 6, 16, false, int(sizeof(RouterRed))>;
 
 int tile_bn(int choice) {
   switch (choice) {

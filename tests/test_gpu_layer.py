@@ -110,6 +110,12 @@ SMALL = [
              act=ACT_RELU, dtype=DT_F32, seed=25),
     Workload("bf16_k33_tc_router", T=70, d_model=64, d_ff=64, n_experts=128, top_k=33,
              act=ACT_GELU_ERF, dtype=DT_BF16, seed=26),
+    # 2048..16384 assignments: the two-launch sort (three blocks of 1024
+    # assignments, the last one ragged) with 300 experts, capacity drops and a
+    # shared expert; the statistics from the scatter launch's extra block
+    Workload("bf16_mid_sort_n300_cap_shared", T=333, d_model=128, d_ff=128, n_experts=300,
+             top_k=8, act=ACT_RELU, dtype=DT_BF16, capacity_factor=6.0, d_ff_shared=128,
+             seed=48),
     # T*k too large for the one-block counting sort: histogram/scan/rank blocks
     Workload("bf16_multiblock_permute", T=40000, d_model=64, d_ff=64, n_experts=12,
              top_k=3, act=ACT_RELU, dtype=DT_BF16, capacity_factor=1.05, seed=24),
