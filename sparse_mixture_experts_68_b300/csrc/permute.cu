@@ -458,17 +458,21 @@ bool single_block_sort_fits(const moe_config& c) {
          sort_smem_bytes(c) <= size_t(kSortSmemMax);
 }
 
-// From kMidMinAssign assignments up the two-launch path spreads the one-block
-// sort's work over many SMs (its statistics then run as their own launch).
+// The two-launch path, from kMidMinAssign assignments up to kMidMaxBlocks
+// blocks (every scatter block reads all blocks' counts): it spreads the sort
+// over several SMs.  Its per-warp counts take kMidWarps * N ints of shared
+// memory, at most the 48 KB a launch gets without opting in.
 constexpr int64_t kMidMinAssign = 2048;
+constexpr int64_t kMidMaxBlocks = 64;
+constexpr int64_t kMidMaxExperts = 48 * 1024 / (kMidWarps * 4);
 
 inline int64_t mid_blocks(const moe_config& c) {
   return ceil_div(c.T * c.top_k, kMidThreads);
 }
 
 bool mid_sort_used(const moe_config& c) {
-  return single_block_sort_fits(c) && c.n_experts <= kMidThreads &&
-         c.T * c.top_k >= kMidMinAssign;
+  return c.n_experts <= kMidMaxExperts && c.T * c.top_k >= kMidMinAssign &&
+         mid_blocks(c) <= kMidMaxBlocks;
 }
 
 // Lets permute_sort_kernel take up to kSortSmemMax of dynamic shared memory:
@@ -579,7 +583,9 @@ int permute_launch_count(const moe_config& c) {
   return (c.T > 0 ? 3 : 1) + copy;
 }
 
-bool permute_fuses_stats(const moe_config& c) { return single_block_sort_fits(c); }
+bool permute_fuses_stats(const moe_config& c) {
+  return mid_sort_used(c) || single_block_sort_fits(c);
+}
 
 cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* topk_idx,
                            int32_t* counts, int32_t* kept, int32_t* offsets,
