@@ -199,6 +199,41 @@ def test_backward_sizes_and_validation(lib):
     assert st == B.MOE_ERR_INVALID_ARG
 
 
+def test_permute_path_follows_the_assignment_count():
+    """The permutation path (host only: launch counts and scratch sizes) follows
+    T*k and N: the one-block sort below 2048 assignments (statistics fused), the
+    two-launch sort from 2048 up to 64 blocks of 1024 assignments with at most
+    384 experts (statistics fused; scratch [blocks][N] counts, then T*k ranks),
+    the histogram/scan/rank path beyond (statistics as their own launch;
+    scratch two [ceil(T/128)][N] arrays)."""
+    from sparse_mixture_experts_68_b300.workloads import ACT_RELU, DT_BF16, Workload
+    r64 = lambda n: (n + 63) // 64 * 64                                        # noqa: E731
+
+    def cfg(T, k, N):
+        return B.make_config(Workload("p", T=T, d_model=64, d_ff=64, n_experts=N, top_k=k,
+                                      act=ACT_RELU, dtype=DT_BF16, seed=1))
+
+    def hist_ints(T, N):
+        return 2 * r64((T + 127) // 128 * N)
+
+    # N = 8: router (1), sort launches, row copy, two Linears, combine
+    for T, k, sort_launches, stats in [(1023, 2, 1, 0), (1024, 2, 2, 0), (32768, 2, 2, 0),
+                                       (32769, 2, 3, 1)]:
+        c = cfg(T, k, 8)
+        assert B.forward_launch_count(c) == 1 + sort_launches + 1 + 3 + stats, (T, k)
+        ints = hist_ints(T, 8)
+        if sort_launches == 2:
+            mb = (T * k + 1023) // 1024
+            ints = max(ints, r64(mb * 8) + T * k)
+        assert B.permute_scratch_size(c) == 4 * ints, (T, k)
+    # 384 experts take the two-launch sort, 385 the one-block sort (16384
+    # assignments); past 16384 assignments with 385 experts, the histogram path.
+    # Router: scores on the tensor cores (N % 64 == 0) or CUDA cores, then top-k.
+    assert B.forward_launch_count(cfg(2048, 8, 384)) == 2 + 2 + 1 + 3
+    assert B.forward_launch_count(cfg(2048, 8, 385)) == 2 + 1 + 1 + 3
+    assert B.forward_launch_count(cfg(10000, 2, 385)) == 2 + 3 + 1 + 3 + 1
+
+
 def test_ffn_kernel_names_follow_the_layer_shape():
     """moe_ffn_kernel_name (host only) names the tile family each grouped
     Linear launches for the benchmark's layers."""

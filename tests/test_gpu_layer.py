@@ -116,6 +116,12 @@ SMALL = [
     Workload("bf16_mid_sort_n300_cap_shared", T=333, d_model=128, d_ff=128, n_experts=300,
              top_k=8, act=ACT_RELU, dtype=DT_BF16, capacity_factor=6.0, d_ff_shared=128,
              seed=48),
+    # the two-launch sort at its limits: 64 blocks of 1024 assignments; 384
+    # experts (the tensor-core router scores) with capacity drops
+    Workload("bf16_mid_sort_64_blocks", T=32768, d_model=64, d_ff=64, n_experts=8, top_k=2,
+             act=ACT_RELU, dtype=DT_BF16, seed=49),
+    Workload("bf16_mid_sort_n384_cap", T=2048, d_model=64, d_ff=64, n_experts=384, top_k=8,
+             act=ACT_GELU_ERF, dtype=DT_BF16, capacity_factor=1.5, seed=50),
     # T*k too large for the one-block counting sort: histogram/scan/rank blocks
     Workload("bf16_multiblock_permute", T=40000, d_model=64, d_ff=64, n_experts=12,
              top_k=3, act=ACT_RELU, dtype=DT_BF16, capacity_factor=1.05, seed=24),
