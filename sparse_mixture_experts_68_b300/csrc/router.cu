@@ -210,26 +210,45 @@ __global__ void __launch_bounds__(kRouterWarps * 32, WF32 ? 2 : 1)
   for (int i = 0; i < NPL; ++i) psum[i] = 0.f;
 
   const int groups = (T + kRouterTokensPerBlock - 1) / kRouterTokensPerBlock;
-  for (int grp = blockIdx.x; grp < groups; grp += gridDim.x) {
-    const int t = grp * kRouterTokensPerBlock + warp;
-    if (t >= T) break;
-    float acc[NE];
+  // a warp takes TPW of its grid-stride groups' tokens at once, so that each
+  // staged weight vector is read and converted once for TPW tokens; every
+  // token's sums run in the same order as with one token per pass
+  constexpr int TPW = (!WF32 && NE <= 16 && sizeof(TIn) == 2) ? 2 : 1;
+  constexpr int kB = kBatch / TPW;                    // x loads in flight per token
+  for (int grp = blockIdx.x; grp < groups; grp += TPW * gridDim.x) {
+    int tok[TPW];
+    bool live[TPW];
 #pragma unroll
-    for (int e = 0; e < NE; ++e) acc[e] = 0.f;
-    const uint4* xr = reinterpret_cast<const uint4*>(x + int64_t(t) * d);
-    for (int c0 = lane; c0 < dv; c0 += kBatch * 32) {
-      uint4 xq[kBatch];
+    for (int u = 0; u < TPW; ++u) {
+      const int g = grp + u * int(gridDim.x);
+      tok[u] = g * kRouterTokensPerBlock + warp;
+      live[u] = g < groups && tok[u] < T;
+    }
+    if (!live[0]) break;
+    float accs[TPW][NE];
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int c = c0 + 32 * u;
-        xq[u] = c < dv ? __ldg(xr + c) : make_uint4(0, 0, 0, 0);
+    for (int u = 0; u < TPW; ++u)
+#pragma unroll
+      for (int e = 0; e < NE; ++e) accs[u][e] = 0.f;
+    for (int c0 = lane; c0 < dv; c0 += kB * 32) {
+      uint4 xq[TPW][kB];
+#pragma unroll
+      for (int u = 0; u < TPW; ++u) {
+        const uint4* xr = reinterpret_cast<const uint4*>(x + int64_t(live[u] ? tok[u] : tok[0]) * d);
+#pragma unroll
+        for (int b = 0; b < kB; ++b) {
+          const int c = c0 + 32 * b;
+          xq[u][b] = (c < dv && live[u]) ? __ldg(xr + c) : make_uint4(0, 0, 0, 0);
+        }
       }
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int c = c0 + 32 * u;
+      for (int b = 0; b < kB; ++b) {
+        const int c = c0 + 32 * b;
         if (c >= dv) break;
-        float xv[V];
-        Vec16<TIn>::load(reinterpret_cast<const TIn*>(&xq[u]), xv);
+        float xv[TPW][V];
+#pragma unroll
+        for (int u = 0; u < TPW; ++u)
+          Vec16<TIn>::load(reinterpret_cast<const TIn*>(&xq[u][b]), xv[u]);
 #pragma unroll
         for (int e = 0; e < NE; ++e) {
           float wv[V];
@@ -241,104 +260,112 @@ __global__ void __launch_bounds__(kRouterWarps * 32, WF32 ? 2 : 1)
             Vec16<TIn>::load(reinterpret_cast<const TIn*>(wsm + e * dv + c), wv);
           }
 #pragma unroll
-          for (int i = 0; i < V; ++i) acc[e] = fmaf(xv[i], wv[i], acc[e]);
+          for (int u = 0; u < TPW; ++u)
+#pragma unroll
+            for (int i = 0; i < V; ++i) accs[u][e] = fmaf(xv[u][i], wv[i], accs[u][e]);
         }
       }
     }
-    // reduce-scatter while more than NPL values remain, then all-reduce
-    // across the DUP lanes that share an expert
-    constexpr int kRsSteps = NE > 32 ? 5 : (NE == 32 ? 5 : (NE == 16 ? 4 : 3));
 #pragma unroll
-    for (int step = 0; step < 5; ++step) {
-      const int o = 16 >> step;
-      if (step < kRsSteps) {
-        const int S = NE >> step;                     // values still held per lane
-        const bool upper = (lane & o) != 0;
+    for (int u = 0; u < TPW; ++u) {
+      if (!live[u]) break;
+      const int t = tok[u];
+      float (&acc)[NE] = accs[u];
+      // reduce-scatter while more than NPL values remain, then all-reduce
+      // across the DUP lanes that share an expert
+      constexpr int kRsSteps = NE > 32 ? 5 : (NE == 32 ? 5 : (NE == 16 ? 4 : 3));
 #pragma unroll
-        for (int i = 0; i < S / 2; ++i) {
-          const float send = upper ? acc[i] : acc[i + S / 2];
-          const float keep = upper ? acc[i + S / 2] : acc[i];
-          acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+      for (int step = 0; step < 5; ++step) {
+        const int o = 16 >> step;
+        if (step < kRsSteps) {
+          const int S = NE >> step;                     // values still held per lane
+          const bool upper = (lane & o) != 0;
+#pragma unroll
+          for (int i = 0; i < S / 2; ++i) {
+            const float send = upper ? acc[i] : acc[i + S / 2];
+            const float keep = upper ? acc[i + S / 2] : acc[i];
+            acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+          }
+        } else {
+          acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], o);
+        }
+      }
+      float z[NPL];
+      float m = -FLT_MAX;
+#pragma unroll
+      for (int i = 0; i < NPL; ++i) {
+        const int e = e0 + i;
+        z[i] = e < N ? acc[i] + to_f32(b_g[e]) : -INFINITY;
+        if (e < N && owner) logits[int64_t(t) * N + e] = z[i];
+        m = fmaxf(m, z[i]);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      float ex[NPL], ssum = 0.f;
+#pragma unroll
+      for (int i = 0; i < NPL; ++i) {
+        ex[i] = (e0 + i < N) ? expf(z[i] - m) : 0.f;
+        if (owner) ssum += ex[i];
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
+      const float inv = 1.0f / ssum;
+#pragma unroll
+      for (int i = 0; i < NPL; ++i) psum[i] += ex[i] * inv;
+      if (probT) {                                       // expert-major probabilities
+#pragma unroll
+        for (int i = 0; i < NPL; ++i) {
+          const int e = e0 + i;
+          if (e < N && owner) probT[int64_t(e) * T + t] = ex[i] * inv;
+        }
+        if (lane == 0) picks[t] = 0;
+      }
+
+      uint32_t taken = 0;                                // bit i: expert e0 + i selected
+      float kept_sum = 0.f;
+      int my_e = 0;
+      float my_g = 0.f;
+      int32_t* out_i = topk_idx + int64_t(t) * k;
+      float* out_w = topk_w + int64_t(t) * k;
+      for (int j = 0; j < k; ++j) {
+        float bv = -INFINITY;
+        int be = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < NPL; ++i) {
+          const int e = e0 + i;
+          if (e < N && !((taken >> i) & 1u) && (z[i] > bv || (z[i] == bv && e < be))) {
+            bv = z[i];
+            be = e;
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+          const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+          if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
+        }
+        if (be >= e0 && be < e0 + NPL) taken |= 1u << (be - e0);
+        const float g = expf(bv - m);
+        kept_sum += g;
+        if (lane == 0) MOE_CHECK(be >= 0 && be < N, CK_ROUTER_TOPK);
+        if (lane == (j & 31)) { my_e = be; my_g = g; }   // slot j is held by lane j % 32
+        if (k > 32 && ((j & 31) == 31 || j == k - 1)) {  // k > 32: flush 32 slots at a time
+          const int j0 = j & ~31;
+          if (lane <= j - j0) {
+            out_i[j0 + lane] = my_e;
+            out_w[j0 + lane] = my_g;                      // unnormalised for now
+          }
+        }
+      }
+      const float scale = renorm ? 1.0f / kept_sum : inv;
+      if (k <= 32) {
+        if (lane < k) {
+          out_i[lane] = my_e;
+          out_w[lane] = my_g * scale;
         }
       } else {
-        acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], o);
+        for (int j = lane; j < k; j += 32) out_w[j] *= scale;
       }
-    }
-    float z[NPL];
-    float m = -FLT_MAX;
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) {
-      const int e = e0 + i;
-      z[i] = e < N ? acc[i] + to_f32(b_g[e]) : -INFINITY;
-      if (e < N && owner) logits[int64_t(t) * N + e] = z[i];
-      m = fmaxf(m, z[i]);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    float ex[NPL], ssum = 0.f;
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) {
-      ex[i] = (e0 + i < N) ? expf(z[i] - m) : 0.f;
-      if (owner) ssum += ex[i];
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
-    const float inv = 1.0f / ssum;
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) psum[i] += ex[i] * inv;
-    if (probT) {                                       // expert-major probabilities
-#pragma unroll
-      for (int i = 0; i < NPL; ++i) {
-        const int e = e0 + i;
-        if (e < N && owner) probT[int64_t(e) * T + t] = ex[i] * inv;
-      }
-      if (lane == 0) picks[t] = 0;
-    }
-
-    uint32_t taken = 0;                                // bit i: expert e0 + i selected
-    float kept_sum = 0.f;
-    int my_e = 0;
-    float my_g = 0.f;
-    int32_t* out_i = topk_idx + int64_t(t) * k;
-    float* out_w = topk_w + int64_t(t) * k;
-    for (int j = 0; j < k; ++j) {
-      float bv = -INFINITY;
-      int be = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < NPL; ++i) {
-        const int e = e0 + i;
-        if (e < N && !((taken >> i) & 1u) && (z[i] > bv || (z[i] == bv && e < be))) {
-          bv = z[i];
-          be = e;
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
-      }
-      if (be >= e0 && be < e0 + NPL) taken |= 1u << (be - e0);
-      const float g = expf(bv - m);
-      kept_sum += g;
-      if (lane == 0) MOE_CHECK(be >= 0 && be < N, CK_ROUTER_TOPK);
-      if (lane == (j & 31)) { my_e = be; my_g = g; }   // slot j is held by lane j % 32
-      if (k > 32 && ((j & 31) == 31 || j == k - 1)) {  // k > 32: flush 32 slots at a time
-        const int j0 = j & ~31;
-        if (lane <= j - j0) {
-          out_i[j0 + lane] = my_e;
-          out_w[j0 + lane] = my_g;                      // unnormalised for now
-        }
-      }
-    }
-    const float scale = renorm ? 1.0f / kept_sum : inv;
-    if (k <= 32) {
-      if (lane < k) {
-        out_i[lane] = my_e;
-        out_w[lane] = my_g * scale;
-      }
-    } else {
-      for (int j = lane; j < k; j += 32) out_w[j] *= scale;
     }
   }
 
