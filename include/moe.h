@@ -124,7 +124,7 @@ int64_t moe_rows_max(const moe_config* cfg);
 /* Rows of the router's per-block probability partial sums ([rows, N] fp32). */
 int64_t moe_router_blocks(const moe_config* cfg);
 
-/* Bytes of scratch moe_permute needs (per-block histograms and bases). */
+/* Bytes of scratch moe_permute needs (per-block counts, bases or ranks). */
 size_t moe_permute_scratch_size(const moe_config* cfg);
 
 /* Bytes of workspace moe_forward needs; 0 for an invalid config. */
@@ -183,12 +183,13 @@ moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk
  * this is an interface convenience, not a step of the layer.
  *
  * Same arguments and results as moe_permute, minus the scratch: the
- * per-block histograms and bases live in a fixed array inside the library,
+ * per-block counts, bases or ranks live in a fixed array inside the library,
  * MOE_PERMUTE_STATIC_SCRATCH_INTS int32 (1 MiB) large, which every GPU that
  * loads the library holds until the process exits.  Layers whose scratch
  * need (moe_permute_scratch_size) exceeds it return MOE_ERR_WORKSPACE and
- * launch nothing; with 128 tokens per block that is ceil(T/128) * N > 131072
- * (for example T = 16384 with N = 1024 still fits).
+ * launch nothing.  Layers of 2048 to 65536 assignments (T * k) with at most
+ * 384 experts always fit; other layers need ceil(T/128) * N <= 131072 (for
+ * example T = 16384 with N = 1024 still fits).
  *
  * The array is shared by every call on a device: two calls whose kernels
  * overlap on the GPU (different streams, no ordering) race on it, so order

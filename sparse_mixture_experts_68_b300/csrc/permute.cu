@@ -539,14 +539,12 @@ __global__ void __launch_bounds__(256)
 }  // namespace
 
 size_t permute_scratch_bytes(const moe_config& c) {
+  // the two-launch sort: [mid_blocks][N] counts, then [T * k] ranks
+  if (mid_sort_used(c))
+    return size_t(round_up(mid_blocks(c) * c.n_experts, 64) + c.T * c.top_k) * sizeof(int32_t);
+  // the histogram path: per-block counts and bases
   const int64_t n = permute_blocks(c) * c.n_experts;
-  int64_t ints = 2 * round_up(n, 64);
-  if (mid_sort_used(c)) {
-    // [mid_blocks][N] counts, then [T * k] ranks
-    const int64_t m = round_up(mid_blocks(c) * c.n_experts, 64) + c.T * c.top_k;
-    if (m > ints) ints = m;
-  }
-  return size_t(ints) * sizeof(int32_t);
+  return size_t(2 * round_up(n, 64)) * sizeof(int32_t);
 }
 
 namespace {

@@ -224,8 +224,13 @@ def test_permute_path_follows_the_assignment_count():
         ints = hist_ints(T, 8)
         if sort_launches == 2:
             mb = (T * k + 1023) // 1024
-            ints = max(ints, r64(mb * 8) + T * k)
+            ints = r64(mb * 8) + T * k
         assert B.permute_scratch_size(c) == 4 * ints, (T, k)
+    # the two-launch sort's scratch fits the allocation-free entry's fixed array
+    # even where the histogram path's would not (65536 tokens, 384 experts)
+    big = cfg(65536, 1, 384)
+    assert B.permute_scratch_size(big) == 4 * (r64(64 * 384) + 65536)
+    assert hist_ints(65536, 384) > (1 << 18)
     # 384 experts take the two-launch sort, 385 the one-block sort (16384
     # assignments); past 16384 assignments with 385 experts, the histogram path.
     # Router: scores on the tensor cores (N % 64 == 0) or CUDA cores, then top-k.
