@@ -122,6 +122,9 @@ SMALL = [
              act=ACT_RELU, dtype=DT_BF16, seed=49),
     Workload("bf16_mid_sort_n384_cap", T=2048, d_model=64, d_ff=64, n_experts=384, top_k=8,
              act=ACT_GELU_ERF, dtype=DT_BF16, capacity_factor=1.5, seed=50),
+    # exactly 2048 assignments, one expert, half of them past the capacity
+    Workload("bf16_mid_sort_one_expert_cap", T=2048, d_model=64, d_ff=128, n_experts=1,
+             top_k=1, act=ACT_RELU, dtype=DT_BF16, capacity_factor=0.5, seed=51),
     # T*k too large for the one-block counting sort: histogram/scan/rank blocks
     Workload("bf16_multiblock_permute", T=40000, d_model=64, d_ff=64, n_experts=12,
              top_k=3, act=ACT_RELU, dtype=DT_BF16, capacity_factor=1.05, seed=24),
