@@ -153,9 +153,11 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
 // most 16 experts whose W_g takes <= 48 KB as fp32): W_g is staged converted to
 // fp32, laid out [NE][2][d / 8][4] so that a lane's two 16-byte reads of an
 // 8-element vector are each contiguous across the warp; the inner loop then
-// reads weights without converting them.
-template <typename TIn, int NE, bool WF32 = false>
-__global__ void __launch_bounds__(kRouterWarps * 32, WF32 ? 2 : 1)
+// reads weights without converting them.  WG (bf16, at most 8 experts, W_g at
+// most 16 KB): no staging; the inner loop reads W_g from global memory, where
+// it stays in L1, so the x loads start without waiting for a staged copy.
+template <typename TIn, int NE, bool WF32 = false, bool WG = false>
+__global__ void __launch_bounds__(kRouterWarps * 32, (WF32 || WG) ? 2 : 1)
     router_fused_kernel(const TIn* __restrict__ x, const TIn* __restrict__ W_g,
                         const TIn* __restrict__ b_g, int T, int d, int N, int k, int renorm,
                         float* __restrict__ logits, int32_t* __restrict__ topk_idx,
@@ -164,7 +166,7 @@ __global__ void __launch_bounds__(kRouterWarps * 32, WF32 ? 2 : 1)
   constexpr int V = Vec16<TIn>::n;
   constexpr int NPL = NE > 32 ? NE / 32 : 1;          // experts per lane after the reduce
   constexpr int DUP = NE < 32 ? 32 / NE : 1;          // lanes holding the same expert
-  constexpr int kBatch = WF32 ? 8 : (NE <= 16 ? 16 : (NE == 32 ? 8 : 2));   // x loads in flight
+  constexpr int kBatch = (WF32 || WG) ? 8 : (NE <= 16 ? 16 : (NE == 32 ? 8 : 2));   // x loads in flight
   extern __shared__ uint4 wsm[];                      // W_g [NE][d] (zero rows), then sums
   pdl_launch_dependents();
   pdl_wait_previous();
@@ -172,7 +174,9 @@ __global__ void __launch_bounds__(kRouterWarps * 32, WF32 ? 2 : 1)
   const int nvec = N * dv, nvec_pad = NE * dv;
   const uint4* wsrc = reinterpret_cast<const uint4*>(W_g);
   float4* wsf = reinterpret_cast<float4*>(wsm);       // WF32: [NE][2][dv] float4
-  if constexpr (WF32) {
+  if constexpr (WG) {
+    // W_g read straight from global memory (L1-resident) in the inner loop
+  } else if constexpr (WF32) {
     for (int i = threadIdx.x; i < nvec_pad; i += blockDim.x) {
       const int e = i / dv, c = i - e * dv;
       float v[8];
@@ -197,8 +201,9 @@ __global__ void __launch_bounds__(kRouterWarps * 32, WF32 ? 2 : 1)
     for (int j = nvec + int(threadIdx.x); j < nvec_pad; j += blockDim.x)
       wsm[j] = make_uint4(0, 0, 0, 0);
   }
-  float* red = WF32 ? reinterpret_cast<float*>(wsf + 2 * nvec_pad)
-                    : reinterpret_cast<float*>(wsm + nvec_pad);   // [kRouterWarps][NE]
+  float* red = WG     ? reinterpret_cast<float*>(wsm)
+               : WF32 ? reinterpret_cast<float*>(wsf + 2 * nvec_pad)
+                      : reinterpret_cast<float*>(wsm + nvec_pad);   // [kRouterWarps][NE]
   __syncthreads();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -213,7 +218,7 @@ __global__ void __launch_bounds__(kRouterWarps * 32, WF32 ? 2 : 1)
   // a warp takes TPW of its grid-stride groups' tokens at once, so that each
   // staged weight vector is read and converted once for TPW tokens; every
   // token's sums run in the same order as with one token per pass
-  constexpr int TPW = (!WF32 && NE <= 16 && sizeof(TIn) == 2) ? 2 : 1;
+  constexpr int TPW = (!WF32 && !WG && NE <= 16 && sizeof(TIn) == 2) ? 2 : 1;
   constexpr int kB = kBatch / TPW;                    // x loads in flight per token
   for (int grp = blockIdx.x; grp < groups; grp += TPW * gridDim.x) {
     int tok[TPW];
@@ -256,6 +261,9 @@ __global__ void __launch_bounds__(kRouterWarps * 32, WF32 ? 2 : 1)
             const float4 lo = wsf[(2 * e) * dv + c], hi = wsf[(2 * e + 1) * dv + c];
             wv[0] = lo.x; wv[1] = lo.y; wv[2] = lo.z; wv[3] = lo.w;
             wv[4] = hi.x; wv[5] = hi.y; wv[6] = hi.z; wv[7] = hi.w;
+          } else if constexpr (WG) {
+            const uint4 q = e < N ? __ldg(wsrc + e * dv + c) : make_uint4(0, 0, 0, 0);
+            Vec16<TIn>::load(reinterpret_cast<const TIn*>(&q), wv);
           } else {
             Vec16<TIn>::load(reinterpret_cast<const TIn*>(wsm + e * dv + c), wv);
           }
@@ -390,15 +398,26 @@ constexpr size_t kFusedRouterSmemLimit = 200 * 1024;
 // per SM still fit)
 constexpr size_t kFusedRouterF32Limit = 48 * 1024;
 
+// bf16 layers of at most 8 experts whose W_g takes at most 16 KB read it from
+// global memory in the inner loop (it stays in L1) instead of staging it first
+constexpr size_t kFusedRouterGlobalLimit = 16 * 1024;
+
+bool fused_router_wg(const moe_config& c) {
+  return c.dtype == MOE_BF16 && fused_ne(c.n_experts) <= 8 &&
+         size_t(c.n_experts * c.d_model) * 2 <= kFusedRouterGlobalLimit;
+}
+
 bool fused_router_wf32(const moe_config& c) {
-  return c.dtype == MOE_BF16 && fused_ne(c.n_experts) <= 16 &&
+  return c.dtype == MOE_BF16 && fused_ne(c.n_experts) <= 16 && !fused_router_wg(c) &&
          size_t(fused_ne(c.n_experts) * c.d_model) * 4 <= kFusedRouterF32Limit;
 }
 
 size_t fused_router_smem(const moe_config& c) {
-  const size_t es = (c.dtype == MOE_F32 || fused_router_wf32(c)) ? 4 : 2;
   const int ne = fused_ne(c.n_experts);
-  return size_t(ne * c.d_model) * es + size_t(kRouterWarps) * ne * sizeof(float);
+  const size_t red = size_t(kRouterWarps) * ne * sizeof(float);
+  if (fused_router_wg(c)) return red;
+  const size_t es = (c.dtype == MOE_F32 || fused_router_wf32(c)) ? 4 : 2;
+  return size_t(ne * c.d_model) * es + red;
 }
 
 bool fused_router_fits(const moe_config& c) {
@@ -415,9 +434,9 @@ cudaError_t launch_router_fused(const moe_config& c, int k, const void* x, const
   const size_t smem = fused_router_smem(c);
   const int T = int(c.T), d = int(c.d_model), N = int(c.n_experts);
   const int rn = c.renormalize ? 1 : 0;
-#define MOE_FUSED_CASE(TIN, NPAD, WF)                                                      \
+#define MOE_FUSED_CASE(TIN, NPAD, WF, ...)                                                 \
   {                                                                                        \
-    auto kern = router_fused_kernel<TIN, NPAD, WF>;                                        \
+    auto kern = router_fused_kernel<TIN, NPAD, WF, ##__VA_ARGS__>;                         \
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,  \
                                          int(smem));                                       \
     if (e != cudaSuccess) return e;                                                        \
@@ -432,6 +451,7 @@ cudaError_t launch_router_fused(const moe_config& c, int k, const void* x, const
     if (N <= 32) MOE_FUSED_CASE(float, 32, false)
     MOE_FUSED_CASE(float, 64, false)
   }
+  if (fused_router_wg(c)) MOE_FUSED_CASE(__nv_bfloat16, 8, false, true)
   if (fused_router_wf32(c)) {
     if (N <= 8) MOE_FUSED_CASE(__nv_bfloat16, 8, true)
     MOE_FUSED_CASE(__nv_bfloat16, 16, true)
